@@ -1,0 +1,131 @@
+"""CPU oracle for the first-order linear-recurrence scan (TEST INFRASTRUCTURE).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s cpu_baseline /
+reference leg may import this package.  The product path (the CUDA library and
+its Python binding) never imports, links or calls it.
+
+The arithmetic lives in ``linrec_oracle.c`` (plain sequential loops, see its
+header for the definition followed and the passages cited).  This module only
+compiles that file with gcc and marshals numpy arrays through ctypes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "linrec_oracle.c")
+_LIB = os.path.join(_HERE, "liblinrec_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+CFLAGS = ["-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared", "-pthread"]
+
+
+def build(force: bool = False) -> str:
+    """Compile linrec_oracle.c into liblinrec_oracle.so (skipped when up to date)."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", *CFLAGS, _SRC, "-o", tmp], check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def build_variant(src_text: str, out_path: str) -> str:
+    """Compile an edited copy of the oracle source (used by the planted-mistake tests)."""
+    src_path = out_path + ".c"
+    with open(src_path, "w") as f:
+        f.write(src_text)
+    subprocess.run(["gcc", *CFLAGS, src_path, "-o", out_path], check=True)
+    return out_path
+
+
+def source_text() -> str:
+    with open(_SRC) as f:
+        return f.read()
+
+
+def _bind(lib):
+    i64, i32 = ctypes.c_int64, ctypes.c_int
+    pf, pd = ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_double)
+    lib.linrec_oracle_f64.argtypes = [pf, pf, pd, i64, i64, i64, i32]
+    lib.linrec_oracle_f64.restype = i32
+    lib.linrec_oracle_f32seq.argtypes = [pf, pf, pf, i64, i64, i64, i32]
+    lib.linrec_oracle_f32seq.restype = i32
+    lib.linrec_oracle_f64_channel.argtypes = [pf, pf, pd, i64, i64, i64, i64, i64]
+    lib.linrec_oracle_f64_channel.restype = i32
+    lib.linrec_oracle_hardware_threads.argtypes = []
+    lib.linrec_oracle_hardware_threads.restype = i32
+    return lib
+
+
+def load(path: str | None = None):
+    """Load the oracle library (building it first if needed)."""
+    global _lib
+    if path is not None:
+        return _bind(ctypes.CDLL(path))
+    with _lock:
+        if _lib is None:
+            _lib = _bind(ctypes.CDLL(build()))
+        return _lib
+
+
+def _as_f32(x) -> np.ndarray:
+    if hasattr(x, "detach"):          # a CPU torch tensor
+        x = x.detach().cpu().numpy()
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    if x.ndim != 3:
+        raise ValueError("expected a (B, L, D) array")
+    return x
+
+
+def _ptr(x, ctype):
+    return x.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def f64(a, b, nthreads: int = 0, lib=None):
+    """h in float64 by the definition; returns (h, threads_used)."""
+    a, b = _as_f32(a), _as_f32(b)
+    if a.shape != b.shape:
+        raise ValueError("a and b differ in shape")
+    lib = lib or load()
+    h = np.empty(a.shape, dtype=np.float64)
+    n = lib.linrec_oracle_f64(_ptr(a, ctypes.c_float), _ptr(b, ctypes.c_float),
+                              _ptr(h, ctypes.c_double), *a.shape, nthreads)
+    if n < 0:
+        raise ValueError("oracle rejected its arguments")
+    return h, n
+
+
+def f32seq(a, b, nthreads: int = 0, lib=None):
+    """h in fp32 with one rounded multiply and one rounded add per step."""
+    a, b = _as_f32(a), _as_f32(b)
+    lib = lib or load()
+    h = np.empty(a.shape, dtype=np.float32)
+    n = lib.linrec_oracle_f32seq(_ptr(a, ctypes.c_float), _ptr(b, ctypes.c_float),
+                                 _ptr(h, ctypes.c_float), *a.shape, nthreads)
+    if n < 0:
+        raise ValueError("oracle rejected its arguments")
+    return h, n
+
+
+def f64_channel(a, b, i: int, d: int, lib=None) -> np.ndarray:
+    """One channel (i, d): h[i, :, d] in float64."""
+    a, b = _as_f32(a), _as_f32(b)
+    lib = lib or load()
+    h = np.empty(a.shape[1], dtype=np.float64)
+    rc = lib.linrec_oracle_f64_channel(_ptr(a, ctypes.c_float), _ptr(b, ctypes.c_float),
+                                       _ptr(h, ctypes.c_double), *a.shape, i, d)
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return h
+
+
+def hardware_threads() -> int:
+    return int(load().linrec_oracle_hardware_threads())

@@ -1,0 +1,170 @@
+/*
+ * linrec_oracle.c -- plain CPU oracle for the first-order linear-recurrence scan.
+ *
+ * TEST INFRASTRUCTURE.  Only tests/, __graft_entry__.smoke() and the
+ * cpu_baseline / reference leg of bench.py load this library.  The CUDA
+ * library under linear_recurrence_scan_fp32_gb300/csrc shares no code,
+ * header, helper or constant with it, and neither includes the other.
+ *
+ * What it computes.  The POPCORNBENCH trace "Kimi-K2.6 l1_p9" (problem
+ * statement; the same statement opens "FW-GLM-5-1 l1_p9") defines, for
+ * tensors a, b of shape (B, L, D), each channel (batch index i, channel d)
+ * independently:
+ *
+ *     h[i,0,d] = b[i,0,d]
+ *     h[i,t,d] = a[i,t,d] * h[i,t-1,d] + b[i,t,d]      for 0 < t < L
+ *
+ * with a, b, h row-major and D contiguous: element (i,t,d) sits at offset
+ * i*L*D + t*D + d.  A parallel scan reaches the same values (up to rounding
+ * order) by associativity of the affine-map composition, so the oracle is the
+ * definition itself: one sequential loop in t per channel.  a[i,0,d] is never
+ * read (h_0 is b_0 by definition).
+ *
+ * Functions:
+ *   linrec_oracle_f64     -- the definition in double precision (inputs
+ *                            widened exactly from fp32), double output.
+ *   linrec_oracle_f32seq  -- the same loop in fp32, one multiply and one add
+ *                            per step, each rounded (the pages' PyTorch loop
+ *                            `h = a[:, t] * h + b[:, t]` computes this).
+ *   linrec_oracle_f64_channel -- one channel's whole sequence, for sampled
+ *                            checks on workloads too large to hold in fp64.
+ *
+ * Threads only split the set of independent channels; every channel is still
+ * one sequential loop, so results do not depend on the thread count.
+ * Compiled with -O2 -ffp-contract=off (no fused multiply-add, no fast-math).
+ *
+ * Parity pins (all in tests/test_oracle_pins.py): closed forms for a=1
+ * (prefix sum), a=0 (copy), b=delta_0 (running product) and constant a, b
+ * (geometric series); exact rational brute force of the expanded sum on tiny
+ * inputs; the page's symbolic walk-through for t = 0, 1, 2; planted mistakes
+ * that each pin must catch.
+ */
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <unistd.h>
+
+typedef struct {
+    const float *a, *b;
+    void *h;
+    int64_t B, L, D;
+    int64_t n_units, d_per_unit, units_per_batch;
+    int tid, nthreads;
+    int f64;
+} job_t;
+
+/* One unit of work: batch index i, channels [d0, d1), all t. */
+static void run_unit_f64(const float *a, const float *b, double *h,
+                         int64_t L, int64_t D, int64_t i, int64_t d0, int64_t d1)
+{
+    const int64_t base = i * L * D;
+    for (int64_t d = d0; d < d1; ++d)
+        h[base + d] = (double)b[base + d];                 /* h_0 = b_0 */
+    for (int64_t t = 1; t < L; ++t) {
+        const int64_t row = base + t * D, prev = base + (t - 1) * D;
+        for (int64_t d = d0; d < d1; ++d)
+            h[row + d] = (double)a[row + d] * h[prev + d] + (double)b[row + d];
+    }
+}
+
+static void run_unit_f32(const float *a, const float *b, float *h,
+                         int64_t L, int64_t D, int64_t i, int64_t d0, int64_t d1)
+{
+    const int64_t base = i * L * D;
+    for (int64_t d = d0; d < d1; ++d)
+        h[base + d] = b[base + d];
+    for (int64_t t = 1; t < L; ++t) {
+        const int64_t row = base + t * D, prev = base + (t - 1) * D;
+        for (int64_t d = d0; d < d1; ++d) {
+            float prod = a[row + d] * h[prev + d];          /* rounded to fp32 */
+            h[row + d] = prod + b[row + d];                 /* rounded to fp32 */
+        }
+    }
+}
+
+static void *worker(void *arg)
+{
+    job_t *j = (job_t *)arg;
+    for (int64_t u = j->tid; u < j->n_units; u += j->nthreads) {
+        int64_t i = u / j->units_per_batch;
+        int64_t d0 = (u % j->units_per_batch) * j->d_per_unit;
+        int64_t d1 = d0 + j->d_per_unit;
+        if (d1 > j->D) d1 = j->D;
+        if (d0 >= d1) continue;
+        if (j->f64) run_unit_f64(j->a, j->b, (double *)j->h, j->L, j->D, i, d0, d1);
+        else        run_unit_f32(j->a, j->b, (float *)j->h, j->L, j->D, i, d0, d1);
+    }
+    return NULL;
+}
+
+int linrec_oracle_hardware_threads(void)
+{
+    long n = sysconf(_SC_NPROCESSORS_ONLN);
+    return n > 0 ? (int)n : 1;
+}
+
+/* Returns the number of threads used (>= 1), or -1 on bad arguments. */
+static int run(const float *a, const float *b, void *h, int64_t B, int64_t L, int64_t D,
+               int nthreads, int f64)
+{
+    if (B < 0 || L < 0 || D < 0) return -1;
+    if (B == 0 || L == 0 || D == 0) return 1;
+    if (!a || !b || !h) return -1;
+    if (nthreads <= 0) nthreads = linrec_oracle_hardware_threads();
+    if (nthreads > 256) nthreads = 256;
+
+    /* Split each batch's D channels into enough ranges to give every thread work. */
+    int64_t ranges = (nthreads + B - 1) / B;
+    if (ranges < 1) ranges = 1;
+    if (ranges > D) ranges = D;
+    int64_t d_per_unit = (D + ranges - 1) / ranges;
+    int64_t units_per_batch = (D + d_per_unit - 1) / d_per_unit;
+    int64_t n_units = B * units_per_batch;
+    if ((int64_t)nthreads > n_units) nthreads = (int)n_units;
+
+    job_t jobs[256];
+    pthread_t th[256];
+    for (int k = 0; k < nthreads; ++k) {
+        jobs[k] = (job_t){a, b, h, B, L, D, n_units, d_per_unit, units_per_batch, k, nthreads, f64};
+    }
+    int started = 0;
+    for (int k = 1; k < nthreads; ++k) {
+        if (pthread_create(&th[k], NULL, worker, &jobs[k]) != 0) break;
+        started = k;
+    }
+    /* Threads that failed to start: do their share here, in order. */
+    for (int k = started + 1; k < nthreads; ++k) worker(&jobs[k]);
+    worker(&jobs[0]);
+    for (int k = 1; k <= started; ++k) pthread_join(th[k], NULL);
+    return nthreads;
+}
+
+int linrec_oracle_f64(const float *a, const float *b, double *h,
+                      int64_t B, int64_t L, int64_t D, int nthreads)
+{
+    return run(a, b, h, B, L, D, nthreads, 1);
+}
+
+int linrec_oracle_f32seq(const float *a, const float *b, float *h,
+                         int64_t B, int64_t L, int64_t D, int nthreads)
+{
+    return run(a, b, h, B, L, D, nthreads, 0);
+}
+
+/* h_col[t] for t < L: the fp64 definition on channel (i, d) alone. */
+int linrec_oracle_f64_channel(const float *a, const float *b, double *h_col,
+                              int64_t B, int64_t L, int64_t D, int64_t i, int64_t d)
+{
+    if (B < 0 || L < 0 || D < 0 || i < 0 || i >= B || d < 0 || d >= D) return -1;
+    if (L == 0) return 0;
+    if (!a || !b || !h_col) return -1;
+    const int64_t base = i * L * D + d;
+    double h = (double)b[base];
+    h_col[0] = h;
+    for (int64_t t = 1; t < L; ++t) {
+        const int64_t k = base + t * D;
+        h = (double)a[k] * h + (double)b[k];
+        h_col[t] = h;
+    }
+    return 0;
+}

@@ -1,0 +1,285 @@
+"""Pins for the CPU oracle: what the pages and the mathematics fix, not the oracle itself.
+
+Each pin is a function of an oracle library handle, so that the planted-mistake
+test at the bottom can run every pin against edited copies of the oracle and
+check that each planted mistake is caught by at least one of them.
+
+Definition pinned (POPCORNBENCH trace "Kimi-K2.6 l1_p9", problem statement):
+h_0 = b_0, h_t = a_t*h_{t-1} + b_t, per channel of (B, L, D) tensors, D contiguous.
+"""
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+from linear_recurrence_scan_fp32_gb300 import inputs
+from tests._util import assert_close, excess
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _f32(x):
+    return np.ascontiguousarray(x, dtype=np.float32)
+
+
+# ---------------------------------------------------------------------------
+# pins (each returns None or raises AssertionError)
+# ---------------------------------------------------------------------------
+
+def pin_walkthrough(lib):
+    """The page's symbolic walk-through t = 0, 1, 2, on exact dyadic inputs."""
+    vals = {}
+    with open(os.path.join(HERE, "golden", "walkthrough_t012.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            key, rest = line.split(":", 1)
+            vals[key.strip()] = [float(v) for v in rest.split()]
+    B, L, D = (int(v) for v in vals["shape"])
+    a = _f32(np.array(vals["a"]).reshape(B, L, D))
+    b = _f32(np.array(vals["b"]).reshape(B, L, D))
+    want = np.array(vals["h"]).reshape(B, L, D)
+    h, _ = oracle.f64(a, b, lib=lib)
+    assert np.array_equal(h, want), f"walk-through: got {h.ravel()} want {want.ravel()}"
+
+
+def pin_prefix_sum(lib):
+    """a = 1: h_t is the inclusive prefix sum of b (textbook scan), exact on integers."""
+    rng = _rng(10)
+    b_int = _f32(rng.integers(-8, 9, size=(3, 257, 5)))
+    a = np.ones_like(b_int)
+    h, _ = oracle.f64(a, b_int, lib=lib)
+    assert np.array_equal(h, np.cumsum(b_int.astype(np.float64), axis=1)), "integer prefix sum"
+    b = _f32(rng.standard_normal((2, 300, 7)))
+    h, _ = oracle.f64(np.ones_like(b), b, lib=lib)
+    ref = np.cumsum(b.astype(np.float64), axis=1)
+    assert np.allclose(h, ref, rtol=0, atol=1e-12 * 300), "real prefix sum"
+
+
+def pin_copy(lib):
+    """a = 0: h = b exactly."""
+    b = _f32(_rng(11).standard_normal((2, 77, 9)))
+    h, _ = oracle.f64(np.zeros_like(b), b, lib=lib)
+    assert np.array_equal(h, b.astype(np.float64)), "a=0 must copy b"
+
+
+def pin_running_product(lib):
+    """b = (1, 0, 0, ...): h_t = a_1 * a_2 * ... * a_t (a_0 unused)."""
+    rng = _rng(12)
+    a = _f32(rng.uniform(-1.5, 1.5, size=(2, 64, 6)))
+    b = np.zeros_like(a)
+    b[:, 0, :] = 1.0
+    h, _ = oracle.f64(a, b, lib=lib)
+    want = np.ones((2, 64, 6))
+    want[:, 1:, :] = np.cumprod(a[:, 1:, :].astype(np.float64), axis=1)
+    assert np.allclose(h, want, rtol=1e-13, atol=0), "running product"
+
+
+def pin_geometric(lib):
+    """Constant a = c, b = beta: h_t = beta*(1 - c^(t+1))/(1 - c)."""
+    c, beta, L = 0.75, 1.25, 400
+    a = np.full((1, L, 3), c, dtype=np.float32)
+    b = np.full((1, L, 3), beta, dtype=np.float32)
+    h, _ = oracle.f64(a, b, lib=lib)
+    t = np.arange(L, dtype=np.float64)
+    want = beta * (1.0 - c ** (t + 1)) / (1.0 - c)
+    assert np.allclose(h[0, :, 1], want, rtol=1e-13, atol=0), "geometric series"
+    # c = -0.5 makes the signs alternate; a dropped or flipped term shows at once
+    c2 = -0.5
+    h, _ = oracle.f64(np.full((1, 50, 1), c2, np.float32), np.full((1, 50, 1), beta, np.float32), lib=lib)
+    t = np.arange(50, dtype=np.float64)
+    assert np.allclose(h[0, :, 0], beta * (1 - c2 ** (t + 1)) / (1 - c2), rtol=1e-13, atol=1e-15)
+
+
+def _expanded_exact(a, b):
+    """h_t = sum_{s<=t} (prod_{s<r<=t} a_r) b_s in exact rational arithmetic."""
+    B, L, D = a.shape
+    out = np.empty((B, L, D), dtype=object)
+    for i in range(B):
+        for d in range(D):
+            af = [Fraction(float(x)) for x in a[i, :, d]]
+            bf = [Fraction(float(x)) for x in b[i, :, d]]
+            for t in range(L):
+                acc = Fraction(0)
+                for s in range(t + 1):
+                    p = Fraction(1)
+                    for r in range(s + 1, t + 1):
+                        p *= af[r]
+                    acc += p * bf[s]
+                out[i, t, d] = acc
+    return out
+
+
+def pin_bruteforce(lib):
+    """Exact rational expansion of the recurrence on tiny random inputs (a_0 random too)."""
+    rng = _rng(13)
+    for L in (1, 2, 3, 5, 8):
+        a = _f32(rng.uniform(-2, 2, size=(2, L, 3)))
+        b = _f32(rng.standard_normal((2, L, 3)))
+        exact = _expanded_exact(a, b)
+        h, _ = oracle.f64(a, b, lib=lib)
+        # bound: a few fp64 roundings of each partial product and sum
+        for idx in np.ndindex(h.shape):
+            e = exact[idx]
+            err = abs(Fraction(float(h[idx])) - e)
+            assert err <= Fraction(1, 10 ** 12) * (1 + abs(e)), f"L={L} at {idx}: {float(h[idx])} vs {float(e)}"
+
+
+PINS = [pin_walkthrough, pin_prefix_sum, pin_copy, pin_running_product, pin_geometric, pin_bruteforce]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
+def test_pin(pin, oracle_lib):
+    pin(oracle_lib)
+
+
+# ---------------------------------------------------------------------------
+# properties of the oracle's own entry points
+# ---------------------------------------------------------------------------
+
+def test_a0_is_ignored(oracle_lib):
+    """h_0 = b_0: non-finite a_0 leaves every output finite and unchanged."""
+    a, b = inputs.generate(2, 40, 5, seed=21)
+    a, b = a.numpy().copy(), b.numpy()
+    h_ref, _ = oracle.f64(a, b)
+    a[:, 0, :] = np.nan
+    a[0, 0, 0] = np.inf
+    h, _ = oracle.f64(a, b)
+    assert np.array_equal(h, h_ref)
+    h32, _ = oracle.f32seq(a, b)
+    assert np.isfinite(h32).all()
+
+
+def test_thread_count_does_not_change_bits(oracle_lib):
+    a, b = inputs.generate(3, 500, 37, seed=22)
+    h1, n1 = oracle.f64(a, b, nthreads=1)
+    h7, n7 = oracle.f64(a, b, nthreads=7)
+    assert n1 == 1 and n7 >= 1
+    assert np.array_equal(h1, h7)
+    g1, _ = oracle.f32seq(a, b, nthreads=1)
+    g5, _ = oracle.f32seq(a, b, nthreads=5)
+    assert np.array_equal(g1, g5)
+
+
+def test_channel_entry_matches_full(oracle_lib):
+    a, b = inputs.generate(2, 300, 9, seed=23)
+    h, _ = oracle.f64(a, b)
+    for (i, d) in [(0, 0), (1, 8), (1, 3)]:
+        assert np.array_equal(oracle.f64_channel(a, b, i, d), h[i, :, d])
+
+
+def test_empty_and_degenerate_shapes(oracle_lib):
+    for shape in [(0, 5, 3), (2, 0, 3), (2, 5, 0)]:
+        a = np.zeros(shape, np.float32)
+        h, _ = oracle.f64(a, a)
+        assert h.shape == shape
+    a, b = inputs.generate(1, 1, 4, seed=24)   # L = 1: h = b
+    h, _ = oracle.f64(a, b)
+    assert np.array_equal(h, b.numpy().astype(np.float64))
+
+
+def test_f32_loop_meets_bound_on_every_workload(oracle_lib):
+    """The independent fp32 loop stays within 1e-4*(1+|h|) of fp64: the configs are well conditioned."""
+    for name in inputs.CONFIG_ORDER:
+        w = inputs.WORKLOADS[name]
+        # the two 134M-element configs are checked on their first batches only
+        B = w.B if w.numel <= 70_000_000 else max(1, w.B // 16)
+        a, b = inputs.generate(B, w.L, w.D, w.seed, w.a_dist, w.b_dist)
+        h64, _ = oracle.f64(a, b)
+        h32, _ = oracle.f32seq(a, b)
+        assert excess(h32, h64) <= 0, name
+        del a, b, h64, h32
+
+
+# ---------------------------------------------------------------------------
+# planted mistakes: every edit of the oracle must fail at least one pin
+# ---------------------------------------------------------------------------
+
+_F64_STEP = "h[row + d] = (double)a[row + d] * h[prev + d] + (double)b[row + d];"
+_F64_INIT = "h[base + d] = (double)b[base + d];                 /* h_0 = b_0 */"
+
+MUTANTS = {
+    "operands_transposed": (_F64_STEP, "h[row + d] = (double)b[row + d] * h[prev + d] + (double)a[row + d];"),
+    "a_index_off_by_one": (_F64_STEP, "h[row + d] = (double)a[prev + d] * h[prev + d] + (double)b[row + d];"),
+    "b_term_dropped": (_F64_STEP, "h[row + d] = (double)a[row + d] * h[prev + d];"),
+    "b_sign_flipped": (_F64_STEP, "h[row + d] = (double)a[row + d] * h[prev + d] - (double)b[row + d];"),
+    "carry_dropped": (_F64_STEP, "h[row + d] = (double)a[row + d] + (double)b[row + d];"),
+    "a0_applied": (_F64_INIT, "h[base + d] = (double)a[base + d] * (double)b[base + d];"),
+    "b_from_previous_step": (_F64_STEP, "h[row + d] = (double)a[row + d] * h[prev + d] + (double)b[prev + d];"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = oracle.source_text()
+    assert src.count(old) == 1, "the oracle source changed; update the planted edit"
+    lib = oracle.load(oracle.build_variant(src.replace(old, new), str(tmp_path / f"mut_{name}.so")))
+    caught = []
+    for pin in PINS:
+        try:
+            pin(lib)
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, f"no pin catches the planted mistake {name}"
+
+
+# ---------------------------------------------------------------------------
+# the composition order: a blocked scan is right with one order, wrong with the other
+# ---------------------------------------------------------------------------
+
+def _blocked_scan(a, b, block, combine):
+    """Chunked inclusive scan of (a_t, b_t) pairs with a carried prefix, in fp64 (test helper)."""
+    a = a.astype(np.float64).copy()
+    b = b.astype(np.float64)
+    a[:, 0, :] = 0.0   # h_{-1} = 0: the first map's slope never matters
+    B, L, D = a.shape
+    h = np.empty((B, L, D))
+    carry = (np.ones((B, D)), np.zeros((B, D)))   # identity (1, 0)
+    for t0 in range(0, L, block):
+        acc = (np.ones((B, D)), np.zeros((B, D)))
+        for t in range(t0, min(L, t0 + block)):
+            acc = combine(acc, (a[:, t], b[:, t]))
+            tot = combine(carry, acc)
+            h[:, t] = tot[1]
+        carry = combine(carry, acc)
+    return h
+
+
+def _combine_right(earlier, later):
+    # apply the earlier map first: (a2, b2) o (a1, b1) = (a2*a1, a2*b1 + b2)
+    # ("Kimi-K2.6 l1_p9", derivation of the associative operator)
+    a1, b1 = earlier
+    a2, b2 = later
+    return (a2 * a1, a2 * b1 + b2)
+
+
+def _combine_reversed(earlier, later):
+    # the later map applied first, the ordering mistake of the "FW-GLM-5-1 l1_p9" kernel
+    a1, b1 = earlier
+    a2, b2 = later
+    return (a1 * a2, a1 * b2 + b1)
+
+
+def _combine_stale_a(earlier, later):
+    # slope updated before it is used in the offset, the draft-kernel mistake of "Kimi-K2.6 l1_p9"
+    a1, b1 = earlier
+    a2, b2 = later
+    a_new = a2 * a1
+    return (a_new, a_new * b1 + b2)
+
+
+def test_composition_order(oracle_lib):
+    a, b = inputs.generate(2, 96, 8, seed=30)
+    h64, _ = oracle.f64(a, b)
+    a, b = a.numpy(), b.numpy()
+    assert excess(_blocked_scan(a, b, 16, _combine_right), h64, 1e-12, 1e-12) <= 0
+    assert excess(_blocked_scan(a, b, 16, _combine_reversed), h64) > 0
+    assert excess(_blocked_scan(a, b, 16, _combine_stale_a), h64) > 0
