@@ -1,0 +1,404 @@
+"""Throughput of the linear-recurrence scan on the pages' shape, one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+A step is one linrec_scan_f32 call over a (B=32, L=4096, D=256) fp32 batch
+(a ~ U[0,1), b ~ N(0,1), seed 1 + 1000*rank).  Inputs (268 MB) and output
+(134 MB) together exceed the 129 MB L2, so no flush is needed between steps.
+The metric is GB/s of algorithmic traffic, 12 bytes per element (read a and
+b, write h once).  Under torchrun each rank scans its own batch (weak scaling,
+no collective on the data path); rank 0 prints max-over-ranks timing.
+
+--impl reference times the CPU oracle (plain sequential loop, all host cores)
+on the same workload: the reference arm of this comparison.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "scan GB/s (a,b,h bytes) & % of GB300 HBM peak at B=32,L=4096,D=256 fp32"
+UNIT = "GB/s"
+WORKLOAD = "pages"
+FALLBACK_HBM_GBS = 6800.0
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+# ---------------------------------------------------------------------------
+# rank bookkeeping (host only; tested on CPU with gloo)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    """(rank, world_size, local_rank) from the torchrun environment, (0, 1, 0) without it."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def rank_seed(base_seed: int, rank: int) -> int:
+    """Each rank scans its own batch; rank 0's batch is the named workload itself."""
+    return base_seed + 1000 * rank
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_gbs(bytes_per_rank_step: int, world: int, steps: int, seconds: float) -> float:
+    """Whole-job throughput: the bytes every rank moved over the slowest rank's time."""
+    return bytes_per_rank_step * world * steps / seconds / 1e9
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    def __init__(self, index: int, period_ms: int = 100):
+        self.index, self.period_ms = index, period_ms
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+            self.fh = os.fdopen(fd, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                 f"-lms", str(self.period_ms)], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(float(r[1]) for r in rows),
+                "sm_max_mhz": max(float(r[2]) for r in rows),
+                "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit()) if rows else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# measured peaks and committed counters
+# ---------------------------------------------------------------------------
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_digest(names) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "linear_recurrence_scan_fp32_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel: str, workload: str):
+    """dram read+write bytes per launch from the committed ncu summary, if the kernel is unchanged."""
+    path = os.path.join(ROOT, "profiles", f"traffic_{kernel}_{workload}.txt")
+    try:
+        kv = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        src = kv["kernel_sources"].split(",")
+        if kernel_source_digest([s.strip() for s in src]) != kv["kernel_source_sha256_16"]:
+            return None
+        return int(kv["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------------
+# arms
+# ---------------------------------------------------------------------------
+
+def cpu_baseline(a, b, w, budget_s: float = 10.0):
+    """The oracle as it stands, all host cores, repeated over the full workload for ~budget_s."""
+    import oracle
+    oracle.build()
+    threads = oracle.hardware_threads()
+    reps, t_total = 0, 0.0
+    while t_total < budget_s and reps < 1000:
+        t0 = time.perf_counter()
+        _, used = oracle.f64(a, b, nthreads=threads)
+        t_total += time.perf_counter() - t0
+        reps += 1
+    return {"value": w.algorithmic_bytes * reps / t_total / 1e9, "unit": UNIT, "cores": used, "kind": "oracle",
+            "sample": f"full {w.name} workload {w.shape}, fp64 sequential oracle, {reps} repetitions, {t_total:.1f} s"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from linear_recurrence_scan_fp32_gb300 import inputs
+    import oracle
+    oracle.build()
+    w = inputs.WORKLOADS[WORKLOAD]
+    a, b = inputs.generate_workload(w)
+    a, b = a.numpy(), b.numpy()
+    threads = oracle.hardware_threads()
+    # size each step's sample so that warm-up + timed steps take about --ref-seconds
+    t0 = time.perf_counter()
+    oracle.f64(a, b, nthreads=threads)
+    t_full = time.perf_counter() - t0
+    per_step = args.ref_seconds / (args.steps + args.warmup)
+    nb = max(1, min(w.B, int(w.B * per_step / t_full)))
+    nl = w.L if nb > 1 else max(64, min(w.L, int(w.L * w.B * per_step / t_full)))
+    a_s = np.ascontiguousarray(a[:nb, :nl])
+    b_s = np.ascontiguousarray(b[:nb, :nl])
+    sample_bytes = 12 * a_s.size
+    for _ in range(args.warmup):
+        oracle.f64(a_s, b_s, nthreads=threads)
+    times = []
+    used = threads
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        _, used = oracle.f64(a_s, b_s, nthreads=threads)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = sample_bytes * args.steps / total / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "gpu_launches": 0,
+        "config": {"workload": w.about, "B": w.B, "L": w.L, "D": w.D, "seed": w.seed,
+                   "l2": "host run: no device cache involved"},
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": used, "kind": "oracle",
+                         "sample": f"per step: batches 0..{nb - 1}, steps 0..{nl - 1}, all {w.D} channels "
+                                   f"of the {w.name} workload {w.shape} ({a_s.size} elements)"},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import linear_recurrence_scan_fp32_gb300 as lr
+    from linear_recurrence_scan_fp32_gb300 import _build, inputs
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev) if "device_id" in dist.init_process_group.__code__.co_varnames \
+            else dist.init_process_group("nccl")
+    _build.build()
+    lr.lib()
+
+    w = inputs.WORKLOADS[WORKLOAD]
+    a_cpu, b_cpu = inputs.generate(w.B, w.L, w.D, rank_seed(w.seed, rank), w.a_dist, w.b_dist)
+    a = a_cpu.to(dev)
+    b = b_cpu.to(dev)
+    h = torch.empty_like(a)
+    stream = torch.cuda.current_stream(dev)
+    opt = {} if args.path == "auto" else {"path": args.path}
+    plan = lr.linrec_plan_f32(w.B, w.L, w.D, sm_count=torch.cuda.get_device_properties(dev).multi_processor_count,
+                              **opt)
+
+    def step():
+        if opt:
+            lr.linrec_scan_f32_ex(a, b, h, stream=stream, **opt)
+        else:
+            lr.linrec_scan_f32(a, b, h, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if lr.linrec_stream_status(stream) != lr.LINREC_OK:
+        raise SystemExit("device-side failure during warm-up")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        time.sleep(0.3)   # let the sampler start before the timed region
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        wall = time.perf_counter() - t0
+    elapsed_ms = starts[0].elapsed_time(ends[-1])
+    per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    status = lr.linrec_stream_status(stream)
+    if status != lr.LINREC_OK:
+        raise SystemExit(f"device-side failure: {lr.linrec_status_string(status)}")
+    seconds = max_over_ranks(elapsed_ms / 1e3, dev)
+    value = aggregate_gbs(w.algorithmic_bytes, world, args.steps, seconds)
+
+    # roofline of the scan kernel (one launch per step)
+    mean_launch_s = statistics.fmean(per_launch_ms) / 1e3
+    achieved = w.algorithmic_bytes / mean_launch_s / 1e9
+    peak, peak_kind = hbm_peak()
+    kernel = "chunked" if plan["path_name"] == "chunked" else "regcarry"
+    traffic = committed_traffic(kernel, WORKLOAD)
+
+    # in-run copy ceiling over the same byte count: 1.5*N floats read and written
+    n_copy = w.numel * 3 // 2
+    src = torch.empty(n_copy, device=dev).uniform_()
+    dst = torch.empty_like(src)
+    copy_gbs = {}
+    for name, fn in (("copy_kernel", lambda: lr.linrec_copy_f32(src, dst, stream=stream)),
+                     ("cudaMemcpy_d2d", lambda: dst.copy_(src))):
+        for _ in range(5):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 50
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        copy_gbs[name] = round(8 * n_copy * reps / (e0.elapsed_time(e1) / 1e3) / 1e9, 1)
+    del src, dst
+    ceiling = max(copy_gbs.values())
+
+    # end to end through the public API: pinned host inputs in, result out, every step
+    e2e = None
+    if not args.no_e2e:
+        a_h = a_cpu.pin_memory()
+        b_h = b_cpu.pin_memory()
+        h_h = torch.empty_like(a_cpu).pin_memory()
+        e_steps = max(3, min(args.steps, 20))
+
+        def e2e_step():
+            a.copy_(a_h, non_blocking=True)
+            b.copy_(b_h, non_blocking=True)
+            lr.linrec_scan_f32(a, b, h, stream=stream)
+            h_h.copy_(h, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_sec = max_over_ranks(e0.elapsed_time(e1) / 1e3, dev)
+        e2e = {"value": round(aggregate_gbs(w.algorithmic_bytes, world, e_steps, e_sec), 3), "unit": UNIT,
+               "h2d_bytes_per_step": 8 * w.numel, "d2h_bytes_per_step": 4 * w.numel, "steps": e_steps,
+               "path": "pinned host a,b -> device (cudaMemcpyAsync) -> linrec_scan_f32 -> pinned host h"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(a_cpu.numpy(), b_cpu.numpy(), w, budget_s=args.cpu_seconds)
+
+    if rank == 0:
+        clk = clocks.summary()
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(seconds * 1e3 / args.steps, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.about, "B": w.B, "L": w.L, "D": w.D, "seed": w.seed,
+                       "global_batch": w.B * world,
+                       "l2": "inputs larger than L2: 402 MB per step vs 129 MB L2, no flush",
+                       "path": plan["path_name"],
+                       "plan": {k: plan[k] for k in ("vec", "prefetch", "tile_t", "tile_d", "segments", "stages",
+                                                     "threads", "grid")}},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                         else "fallback 6.8 TB/s", "kernel": kernel,
+                         "algorithmic_bytes_per_launch": w.algorithmic_bytes},
+            "copy_ceiling_gbs": copy_gbs,
+            "frac_of_copy_ceiling": round(value / ceiling, 4),
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": args.steps,
+            "clocks": clk,
+            "wall_s": round(wall, 3),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10000)
+    p.add_argument("--warmup", type=int, default=100)
+    p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    p.add_argument("--path", choices=("auto", "regcarry", "chunked"), default="auto")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--ref-seconds", type=float, default=90.0,
+                   help="reference arm: CPU time budget for warm-up + timed steps")
+    args = p.parse_args(argv)
+    if args.warmup < 3:
+        p.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,144 @@
+/*
+ * linrec.h -- C ABI of liblinrec, a GB300 (sm_103a) first-order linear-recurrence scan.
+ *
+ * The operation (POPCORNBENCH trace "Kimi-K2.6 l1_p9", problem statement; the
+ * same statement opens "FW-GLM-5-1 l1_p9"): for fp32 tensors a, b, h of shape
+ * (B, L, D), row-major with D contiguous (element (i,t,d) at i*L*D + t*D + d),
+ * every channel (i, d) is an independent sequence
+ *
+ *     h[i,0,d] = b[i,0,d]
+ *     h[i,t,d] = a[i,t,d] * h[i,t-1,d] + b[i,t,d]        0 < t < L.
+ *
+ * a[i,0,d] is never used.  The kernels evaluate it as a scan of the affine maps
+ * x -> a_t*x + b_t under composition, later map on the left:
+ * (a2,b2) o (a1,b1) = (a2*a1, a2*b1 + b2) ("Kimi-K2.6 l1_p9", derivation of the
+ * associative operator), with only the running value h carried from one time
+ * chunk to the next (same page, the running_h carry).
+ *
+ * Conventions for every entry point below:
+ *  - Pointers a, b, h are device memory of the CURRENT CUDA device, owned by
+ *    the caller; the library never frees or retains them.  a and b are read,
+ *    h is written (B*L*D floats).  h must not overlap a or b (no in-place).
+ *    a and b may be the same buffer.
+ *  - Any alignment is accepted.  16-byte aligned a, b, h and D % 4 == 0 let
+ *    the fastest kernels run; other inputs take a scalar-load variant.
+ *  - stream is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Work is enqueued asynchronously on it: the returned status
+ *    covers argument checks and the launch; a kernel's own failure surfaces at
+ *    the caller's next synchronisation, or through linrec_stream_status().
+ *  - B*L*D == 0 returns LINREC_OK with no launch (pointers may then be NULL).
+ *  - Results are deterministic: a given build, device, shape and path returns
+ *    the same bits on every call.
+ *  - Thread-safe: calls from several host threads may run concurrently.  Calls
+ *    on one stream run in order; each stream gets its own look-back workspace,
+ *    so calls on different streams may overlap on the GPU.
+ */
+#ifndef LINREC_H_
+#define LINREC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    LINREC_OK = 0,
+    LINREC_ERR_INVALID_VALUE = 1,      /* negative size, NULL with a non-zero size, size overflow */
+    LINREC_ERR_ALIAS = 2,              /* h overlaps a or b */
+    LINREC_ERR_UNSUPPORTED_DEVICE = 3, /* the current device is not compute capability 10.3 */
+    LINREC_ERR_LAUNCH = 4,             /* a CUDA call failed while enqueueing the work */
+    LINREC_ERR_WORKSPACE = 5,          /* the look-back workspace could not be allocated */
+    LINREC_ERR_LOOKBACK_TIMEOUT = 6,   /* a kernel gave up waiting on a predecessor tile */
+    LINREC_ERR_TMA_TIMEOUT = 7         /* a kernel gave up waiting on a bulk copy */
+} linrec_status_t;
+
+typedef enum {
+    LINREC_PATH_AUTO = 0,      /* the dispatcher chooses */
+    LINREC_PATH_REGCARRY = 1,  /* one thread per 1/2/4 adjacent channels, loads prefetched in registers */
+    LINREC_PATH_CHUNKED = 2    /* TMA-staged (time x channel) tiles, shuffle scan, decoupled look-back */
+} linrec_path_t;
+
+/*
+ * linrec_scan_f32 -- h = scan(a, b) as defined above.  See the conventions.
+ * Returns LINREC_OK, or an error code without launching anything.
+ */
+linrec_status_t linrec_scan_f32(const float *a, const float *b, float *h,
+                                int64_t B, int64_t L, int64_t D, void *stream);
+
+/*
+ * Options for linrec_scan_f32_ex and linrec_plan_f32.  Zero-initialise, then
+ * set what you need; a zero field means "the dispatcher's choice".
+ */
+typedef struct {
+    int path;            /* linrec_path_t */
+    int vec;             /* regcarry: channels per thread, 1, 2 or 4 */
+    int prefetch;        /* regcarry: time steps loaded ahead, 4, 8 or 16 */
+    int tile_t;          /* chunked: time steps per tile */
+    int tile_d;          /* chunked: channels per tile */
+    int stages;          /* chunked: tiles in flight per CTA (shared-memory ring depth) */
+    int ctas_per_sm;     /* chunked: cap on resident CTAs per SM (0 = as many as fit) */
+    unsigned int *d_status; /* device word (may be NULL): the kernel ORs 1 << linrec_status_t
+                               into it on a device-side failure; otherwise the stream's own word
+                               is used (read it with linrec_stream_status) */
+    int64_t spin_limit;  /* chunked: polls of a predecessor before giving up (0 = default, ~1 s) */
+    int64_t test_silent_tile; /* chunked, tests only: 0 = off; k > 0 makes tile id k-1
+                                 publish nothing, so its successor's look-back times out */
+} linrec_options_t;
+
+/* linrec_scan_f32 with explicit options (forced path, tile shape, status word). */
+linrec_status_t linrec_scan_f32_ex(const float *a, const float *b, float *h,
+                                   int64_t B, int64_t L, int64_t D, void *stream,
+                                   const linrec_options_t *opt);
+
+/* What a call would launch: filled by linrec_plan_f32 without touching a GPU. */
+typedef struct {
+    int path;              /* LINREC_PATH_REGCARRY or LINREC_PATH_CHUNKED */
+    int vec, prefetch;     /* regcarry parameters */
+    int tile_t, tile_d, segments, stages; /* chunked parameters */
+    int threads;           /* threads per CTA */
+    int64_t grid;          /* CTAs launched */
+    int64_t n_tiles;       /* chunked: tiles of tile_t x tile_d */
+    int64_t chunks;        /* chunked: time chunks per channel slice */
+    size_t smem_bytes;     /* dynamic shared memory per CTA */
+    size_t workspace_bytes;/* chunked: look-back words for this call */
+} linrec_plan_t;
+
+/*
+ * linrec_plan_f32 -- run the dispatcher for a device with sm_count SMs.
+ * align_bytes: the largest of 16, 8, 4 that divides the addresses of a, b
+ * and h (4 for plain fp32 pointers).  ctas_per_sm: resident CTAs per SM that
+ * the chunked kernel gets on the device (0 = estimate from shared memory).
+ * Pure host logic; no CUDA call.  Returns LINREC_ERR_INVALID_VALUE for bad
+ * sizes or for options that name a path or variant these inputs cannot take.
+ */
+linrec_status_t linrec_plan_f32(int64_t B, int64_t L, int64_t D, int sm_count, int align_bytes,
+                                int ctas_per_sm, const linrec_options_t *opt, linrec_plan_t *plan);
+
+/*
+ * linrec_stream_status -- synchronise `stream`, then return and clear the
+ * device-side status of the library's work on it: LINREC_OK, or the first of
+ * LINREC_ERR_LOOKBACK_TIMEOUT / LINREC_ERR_TMA_TIMEOUT that a kernel recorded.
+ * A stream the library has not used reports LINREC_OK.
+ */
+linrec_status_t linrec_stream_status(void *stream);
+
+/*
+ * linrec_copy_f32 -- dst[i] = src[i], i < n, on the current device.  A plain
+ * 16-byte vector copy kernel used as the in-run copy-bandwidth ceiling next to
+ * the scan (no part of the scan itself).  Same pointer rules as the scan.
+ */
+linrec_status_t linrec_copy_f32(const float *src, float *dst, int64_t n, void *stream);
+
+/* Human-readable name of a status code (static storage). */
+const char *linrec_status_string(linrec_status_t status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int linrec_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LINREC_H_ */

@@ -1,1 +1,216 @@
-"""GB300-native first-order linear-recurrence scan (binding filled in below)."""
+"""GB300-native first-order linear-recurrence scan: Python binding of liblinrec.
+
+    h[i,0,d] = b[i,0,d];   h[i,t,d] = a[i,t,d] * h[i,t-1,d] + b[i,t,d]
+
+for fp32 (B, L, D) tensors with D contiguous (POPCORNBENCH "Kimi-K2.6 l1_p9",
+problem statement).  Every step runs in the CUDA kernels of ``liblinrec.so``
+(built in-tree for sm_103a by ``_build.build()``); this module only checks
+tensor properties and passes device pointers, sizes and the stream through the
+C ABI declared in ``include/linrec.h``.  There is no CPU fallback: a missing
+library raises ``LinrecError``.
+
+Functions keep the C names:
+    linrec_scan_f32(a, b, h=None, stream=None) -> h
+    linrec_scan_f32_ex(a, b, h=None, stream=None, **options) -> h
+    linrec_plan_f32(B, L, D, sm_count=152, align_bytes=16, resident_ctas=0, **options) -> dict
+    linrec_stream_status(stream=None) -> int
+    linrec_copy_f32(src, dst, stream=None)
+    linrec_status_string(code) -> str
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "liblinrec.so")
+
+LINREC_OK = 0
+LINREC_ERR_INVALID_VALUE = 1
+LINREC_ERR_ALIAS = 2
+LINREC_ERR_UNSUPPORTED_DEVICE = 3
+LINREC_ERR_LAUNCH = 4
+LINREC_ERR_WORKSPACE = 5
+LINREC_ERR_LOOKBACK_TIMEOUT = 6
+LINREC_ERR_TMA_TIMEOUT = 7
+
+PATHS = {"auto": 0, "regcarry": 1, "chunked": 2}
+PATH_NAMES = {v: k for k, v in PATHS.items()}
+
+
+class LinrecError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(msg)
+        self.code = code
+
+
+class Options(ctypes.Structure):
+    _fields_ = [
+        ("path", ctypes.c_int),
+        ("vec", ctypes.c_int),
+        ("prefetch", ctypes.c_int),
+        ("tile_t", ctypes.c_int),
+        ("tile_d", ctypes.c_int),
+        ("stages", ctypes.c_int),
+        ("ctas_per_sm", ctypes.c_int),
+        ("d_status", ctypes.c_void_p),
+        ("spin_limit", ctypes.c_int64),
+        ("test_silent_tile", ctypes.c_int64),
+    ]
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [
+        ("path", ctypes.c_int),
+        ("vec", ctypes.c_int),
+        ("prefetch", ctypes.c_int),
+        ("tile_t", ctypes.c_int),
+        ("tile_d", ctypes.c_int),
+        ("segments", ctypes.c_int),
+        ("stages", ctypes.c_int),
+        ("threads", ctypes.c_int),
+        ("grid", ctypes.c_int64),
+        ("n_tiles", ctypes.c_int64),
+        ("chunks", ctypes.c_int64),
+        ("smem_bytes", ctypes.c_size_t),
+        ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib():
+    """The loaded liblinrec.so (ctypes handle).  Raises LinrecError if it was not built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise LinrecError(-1, f"liblinrec.so is missing at {LIB_PATH}: build it with "
+                                  "__graft_entry__.build() (nvcc, sm_103a); there is no fallback")
+        L = ctypes.CDLL(LIB_PATH)
+        i64, vp, i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+        L.linrec_scan_f32.argtypes = [vp, vp, vp, i64, i64, i64, vp]
+        L.linrec_scan_f32.restype = i32
+        L.linrec_scan_f32_ex.argtypes = [vp, vp, vp, i64, i64, i64, vp, ctypes.POINTER(Options)]
+        L.linrec_scan_f32_ex.restype = i32
+        L.linrec_plan_f32.argtypes = [i64, i64, i64, i32, i32, i32, ctypes.POINTER(Options), ctypes.POINTER(Plan)]
+        L.linrec_plan_f32.restype = i32
+        L.linrec_stream_status.argtypes = [vp]
+        L.linrec_stream_status.restype = i32
+        L.linrec_copy_f32.argtypes = [vp, vp, i64, vp]
+        L.linrec_copy_f32.restype = i32
+        L.linrec_status_string.argtypes = [i32]
+        L.linrec_status_string.restype = ctypes.c_char_p
+        L.linrec_version.argtypes = []
+        L.linrec_version.restype = i32
+        _lib = L
+        return _lib
+
+
+def linrec_status_string(code: int) -> str:
+    return lib().linrec_status_string(int(code)).decode()
+
+
+def _check(code: int, what: str):
+    if code != LINREC_OK:
+        raise LinrecError(code, f"{what}: {linrec_status_string(code)}")
+
+
+def make_options(path="auto", vec=0, prefetch=0, tile_t=0, tile_d=0, stages=0, ctas_per_sm=0,
+                 d_status=None, spin_limit=0, test_silent_tile=0) -> Options:
+    o = Options()
+    o.path = PATHS[path] if isinstance(path, str) else int(path)
+    o.vec, o.prefetch, o.tile_t, o.tile_d, o.stages = int(vec), int(prefetch), int(tile_t), int(tile_d), int(stages)
+    o.ctas_per_sm = int(ctas_per_sm)
+    o.d_status = None if d_status is None else int(d_status.data_ptr() if hasattr(d_status, "data_ptr") else d_status)
+    o.spin_limit = int(spin_limit)
+    o.test_silent_tile = int(test_silent_tile)
+    return o
+
+
+def _stream_handle(stream):
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if hasattr(stream, "cuda_stream"):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _shape_of(a, b, h):
+    import torch
+    for name, t in (("a", a), ("b", b)) + ((("h", h),) if h is not None else ()):
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch.Tensor")
+        if t.dtype != torch.float32:
+            raise TypeError(f"{name} must be float32, got {t.dtype}")
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if t.dim() != 3:
+            raise ValueError(f"{name} must be 3-D (B, L, D)")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous (B, L, D), D innermost")
+    if a.shape != b.shape or (h is not None and h.shape != a.shape):
+        raise ValueError("a, b and h must have the same shape")
+    return tuple(a.shape)
+
+
+def linrec_scan_f32_ex(a, b, h=None, stream=None, **options):
+    """h = scan(a, b) with explicit options (path, vec, prefetch, tile_t, tile_d, stages, ...)."""
+    import torch
+    B, L, D = _shape_of(a, b, h)
+    if h is None:
+        h = torch.empty_like(a)
+    opt = make_options(**options)
+    code = lib().linrec_scan_f32_ex(a.data_ptr(), b.data_ptr(), h.data_ptr(), B, L, D,
+                                    _stream_handle(stream), ctypes.byref(opt))
+    _check(code, "linrec_scan_f32_ex")
+    return h
+
+
+def linrec_scan_f32(a, b, h=None, stream=None):
+    """h = scan(a, b): fp32 CUDA tensors of shape (B, L, D), contiguous; h is allocated if None."""
+    import torch
+    B, L, D = _shape_of(a, b, h)
+    if h is None:
+        h = torch.empty_like(a)
+    code = lib().linrec_scan_f32(a.data_ptr(), b.data_ptr(), h.data_ptr(), B, L, D, _stream_handle(stream))
+    _check(code, "linrec_scan_f32")
+    return h
+
+
+def linrec_plan_f32(B, L, D, sm_count=152, align_bytes=16, resident_ctas=0, **options) -> dict:
+    """The dispatcher's choice for a (B, L, D) problem, without a GPU.
+
+    resident_ctas: CTAs of the chunked kernel that fit on one SM (0 = estimate);
+    options as for linrec_scan_f32_ex."""
+    opt = make_options(**options)
+    plan = Plan()
+    code = lib().linrec_plan_f32(int(B), int(L), int(D), int(sm_count), int(align_bytes), int(resident_ctas),
+                                 ctypes.byref(opt), ctypes.byref(plan))
+    _check(code, "linrec_plan_f32")
+    out = {name: getattr(plan, name) for name, _ in Plan._fields_}
+    out["path_name"] = PATH_NAMES.get(out["path"], "none")
+    return out
+
+
+def linrec_stream_status(stream=None) -> int:
+    """Synchronise the stream; return and clear the device-side status of the library's work on it."""
+    return int(lib().linrec_stream_status(_stream_handle(stream)))
+
+
+def linrec_copy_f32(src, dst, stream=None):
+    """dst = src with the library's 16-byte copy kernel (copy-bandwidth ceiling)."""
+    if src.numel() != dst.numel():
+        raise ValueError("src and dst differ in size")
+    code = lib().linrec_copy_f32(src.data_ptr(), dst.data_ptr(), src.numel(), _stream_handle(stream))
+    _check(code, "linrec_copy_f32")
+    return dst
+
+
+def linrec_version() -> int:
+    return int(lib().linrec_version())

@@ -1,0 +1,70 @@
+// kernels.cuh -- interface between the host API (linrec_api.cu) and the
+// kernel translation units.  Internal to liblinrec; not installed.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace linrec {
+
+// Per-(device, stream) control block at the head of the look-back workspace.
+// Zeroed once when allocated; afterwards the last CTA of every chunked launch
+// resets the tile counter, the done counter and the abort word and advances
+// the epoch, so no memset is needed between calls.
+struct alignas(64) Control {
+    unsigned long long tile_counter;  // next tile id to hand out (dynamic, in order)
+    unsigned int done;                // CTAs of the current launch that have finished
+    unsigned int epoch;               // launches completed on this workspace
+    unsigned int status;              // OR of (1 << linrec_status_t) device-side failures
+    unsigned int abort;               // set when a bulk copy timed out: stop taking tiles
+    unsigned int pad[10];
+};
+static_assert(sizeof(Control) == 64, "control block layout");
+
+constexpr unsigned int kStatusLookbackTimeout = 1u << 6;  // 1 << LINREC_ERR_LOOKBACK_TIMEOUT
+constexpr unsigned int kStatusTmaTimeout = 1u << 7;       // 1 << LINREC_ERR_TMA_TIMEOUT
+
+// ---- register-carry path ---------------------------------------------------
+// One thread walks `vec` adjacent channels through all L steps, with the loads
+// of the next `prefetch` steps in flight in registers.
+bool regcarry_supported(int vec, int prefetch);
+cudaError_t launch_regcarry(int vec, int prefetch, int threads, const float *a, const float *b,
+                            float *h, int64_t B, int64_t L, int64_t D, cudaStream_t stream);
+
+// ---- chunked path ----------------------------------------------------------
+// A tile is (tile_t time steps) x (tile_d channels) of one batch index, staged in
+// shared memory by TMA.  `segments` threads share each channel's tile_t steps.
+struct ChunkedVariant {
+    int tile_d, tile_t, segments, stages;
+    int threads;         // tile_d * segments
+    size_t smem_bytes;   // dynamic shared memory per CTA
+};
+// The compiled variants (tile_d, tile_t, segments, stages combinations).
+const ChunkedVariant *chunked_variants(int *count);
+
+struct ChunkedLaunch {
+    const ChunkedVariant *variant;
+    CUtensorMap map_a, map_b;    // 3-D {D, L, B} fp32 maps, box {tile_d, tile_t, 1}
+    float *h;
+    int64_t L, D;
+    int64_t slices_per_batch;    // ceil(D / tile_d)
+    int64_t n_slices;            // B * slices_per_batch
+    int64_t chunks;              // ceil(L / tile_t)
+    int64_t n_tiles;             // n_slices * chunks
+    int64_t grid;
+    Control *ctrl;
+    unsigned long long *words;   // 3 * n_tiles * tile_d look-back words
+    unsigned int *status;        // where device-side failures are recorded
+    int64_t spin_limit;
+    int64_t silent_tile;         // tile id that publishes nothing (tests), or -1
+};
+// Number of CTAs of this variant that fit on one SM (occupancy API).
+cudaError_t chunked_ctas_per_sm(const ChunkedVariant *v, int *ctas);
+cudaError_t launch_chunked(const ChunkedLaunch &args, cudaStream_t stream);
+
+// ---- copy-ceiling kernel ---------------------------------------------------
+cudaError_t launch_copy(const float *src, float *dst, int64_t n, int sm_count, cudaStream_t stream);
+
+}  // namespace linrec

@@ -1,0 +1,381 @@
+// linrec_api.cu -- the C ABI of liblinrec (declared in include/linrec.h):
+// argument checks, the size-based dispatcher, the per-stream look-back
+// workspace, tensor-map encoding and the launches.  Host code only.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "kernels.cuh"
+#include "linrec.h"
+
+using namespace linrec;
+
+namespace {
+
+constexpr int kVersion = 100;               // 0.1.0
+constexpr int64_t kDefaultSpinLimit = 1 << 20;
+constexpr int kRegcarryThreads = 256;
+// Below this many channels (B*D) the register path cannot keep enough loads
+// in flight to cover HBM latency, and TMA-staged time chunks take over.
+constexpr int64_t kRegcarryMinChannels = 131072;
+constexpr size_t kWorkspaceHead = 256;      // Control block, padded
+
+struct DeviceInfo {
+    bool ready = false;
+    bool supported = false;
+    int sm_count = 0;
+    int ctas_per_sm[64] = {};               // per chunked variant, 0 = not queried yet
+};
+
+std::mutex g_mu;
+std::map<int, DeviceInfo> g_devices;
+
+struct Slot {
+    unsigned char *base = nullptr;
+    size_t bytes = 0;
+};
+std::map<std::pair<int, uintptr_t>, Slot> g_slots;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+bool overlaps(const void *x, const void *y, int64_t bytes) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(x), b0 = reinterpret_cast<uintptr_t>(y);
+    return a0 < b0 + (uintptr_t)bytes && b0 < a0 + (uintptr_t)bytes;
+}
+
+int align_of(const void *a, const void *b, const void *h) {
+    const uintptr_t u = reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(b) |
+                        reinterpret_cast<uintptr_t>(h);
+    if ((u & 15u) == 0) return 16;
+    if ((u & 7u) == 0) return 8;
+    return 4;
+}
+
+// Sizes: non-negative, and B*L*D*4 bytes representable.
+linrec_status_t check_sizes(int64_t B, int64_t L, int64_t D, int64_t *n_out) {
+    if (B < 0 || L < 0 || D < 0) return LINREC_ERR_INVALID_VALUE;
+    *n_out = 0;
+    if (B == 0 || L == 0 || D == 0) return LINREC_OK;
+    const int64_t lim = INT64_MAX / 16;
+    if (L > lim / D) return LINREC_ERR_INVALID_VALUE;
+    const int64_t ld = L * D;
+    if (B > lim / ld) return LINREC_ERR_INVALID_VALUE;
+    *n_out = B * ld;
+    return LINREC_OK;
+}
+
+const ChunkedVariant *find_variant(int tile_d, int tile_t, int stages, int *index) {
+    int n = 0;
+    const ChunkedVariant *v = chunked_variants(&n);
+    for (int i = 0; i < n; ++i) {
+        if (v[i].tile_d == tile_d && v[i].tile_t == tile_t && (stages == 0 || v[i].stages == stages)) {
+            if (index) *index = i;
+            return &v[i];
+        }
+    }
+    return nullptr;
+}
+
+// Default chunked tile for a channel count D: the widest slice that D fills.
+void default_tile(int64_t D, int *tile_d, int *tile_t) {
+    if (D >= 128) { *tile_d = 128; *tile_t = 64; }
+    else if (D >= 64) { *tile_d = 64; *tile_t = 128; }
+    else { *tile_d = 32; *tile_t = 128; }
+}
+
+linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int align_bytes, int ctas_per_sm,
+                          const linrec_options_t *opt, linrec_plan_t *plan, int *variant_index) {
+    linrec_options_t none = {};
+    if (!opt) opt = &none;
+    if (!plan || sm_count <= 0) return LINREC_ERR_INVALID_VALUE;
+    int64_t n = 0;
+    linrec_status_t st = check_sizes(B, L, D, &n);
+    if (st != LINREC_OK) return st;
+    *plan = linrec_plan_t{};
+    if (n == 0) return LINREC_OK;
+
+    const bool tma_ok = align_bytes >= 16 && D % 4 == 0 && D <= INT32_MAX && B <= INT32_MAX &&
+                        L <= (int64_t)INT32_MAX - 1024;
+    int path = opt->path;
+    if (path == LINREC_PATH_AUTO) {
+        path = (tma_ok && B * D < kRegcarryMinChannels) ? LINREC_PATH_CHUNKED : LINREC_PATH_REGCARRY;
+    }
+    plan->path = path;
+
+    if (path == LINREC_PATH_REGCARRY) {
+        int vec = opt->vec;
+        if (vec == 0) vec = (align_bytes >= 16 && D % 4 == 0) ? 4 : (align_bytes >= 8 && D % 2 == 0) ? 2 : 1;
+        if (D % vec != 0 || align_bytes < 4 * vec) return LINREC_ERR_INVALID_VALUE;
+        int prefetch = opt->prefetch ? opt->prefetch : (vec == 4 ? 8 : 16);
+        if (!regcarry_supported(vec, prefetch)) return LINREC_ERR_INVALID_VALUE;
+        plan->vec = vec;
+        plan->prefetch = prefetch;
+        plan->threads = kRegcarryThreads;
+        const int64_t groups = B * (D / vec);
+        plan->grid = (groups + kRegcarryThreads - 1) / kRegcarryThreads;
+        return LINREC_OK;
+    }
+    if (path != LINREC_PATH_CHUNKED || !tma_ok) return LINREC_ERR_INVALID_VALUE;
+
+    int tile_d = opt->tile_d, tile_t = opt->tile_t;
+    if (tile_d == 0 || tile_t == 0) {
+        int dd, dt;
+        default_tile(D, &dd, &dt);
+        if (tile_d == 0) tile_d = dd;
+        if (tile_t == 0) tile_t = dt;
+    }
+    const ChunkedVariant *v = find_variant(tile_d, tile_t, opt->stages, variant_index);
+    if (!v) return LINREC_ERR_INVALID_VALUE;
+    plan->tile_d = v->tile_d;
+    plan->tile_t = v->tile_t;
+    plan->segments = v->segments;
+    plan->stages = v->stages;
+    plan->threads = v->threads;
+    plan->smem_bytes = v->smem_bytes;
+    const int64_t spb = (D + v->tile_d - 1) / v->tile_d;
+    plan->chunks = (L + v->tile_t - 1) / v->tile_t;
+    plan->n_tiles = B * spb * plan->chunks;
+    int per_sm = ctas_per_sm;
+    if (per_sm <= 0) {
+        per_sm = (int)((227 * 1024) / (v->smem_bytes + 1024));
+        if (per_sm < 1) per_sm = 1;
+    }
+    if (opt->ctas_per_sm > 0 && opt->ctas_per_sm < per_sm) per_sm = opt->ctas_per_sm;
+    int64_t grid = (int64_t)sm_count * per_sm;
+    if (grid > plan->n_tiles) grid = plan->n_tiles;
+    plan->grid = grid;
+    plan->workspace_bytes = kWorkspaceHead + (size_t)3 * (size_t)plan->n_tiles * (size_t)v->tile_d * 8u;
+    return LINREC_OK;
+}
+
+// Device facts, queried once per device.  Caller holds g_mu.
+DeviceInfo *device_info(int dev) {
+    DeviceInfo &di = g_devices[dev];
+    if (!di.ready) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        di.supported = (major == 10 && minor == 3);
+        di.sm_count = sms;
+        di.ready = true;
+    }
+    return &di;
+}
+
+bool get_encoder() {
+    if (g_encode) return true;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) {
+        cudaGetLastError();
+        return false;
+    }
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    return true;
+}
+
+bool encode_map(CUtensorMap *map, const float *base, int64_t B, int64_t L, int64_t D, int tile_d, int tile_t) {
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)L, (cuuint64_t)B};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 4u, (cuuint64_t)L * (cuuint64_t)D * 4u};
+    const cuuint32_t box[3] = {(cuuint32_t)tile_d, (cuuint32_t)tile_t, 1u};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The look-back workspace of (dev, stream), grown in stream order.  Caller holds g_mu.
+Slot *workspace(int dev, cudaStream_t stream, size_t need) {
+    Slot &s = g_slots[{dev, reinterpret_cast<uintptr_t>(stream)}];
+    if (s.bytes >= need) return &s;
+    size_t bytes = (need + (1u << 20) - 1) & ~(size_t)((1u << 20) - 1);
+    void *p = nullptr;
+    if (cudaMallocAsync(&p, bytes, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (cudaMemsetAsync(p, 0, bytes, stream) != cudaSuccess) {
+        cudaGetLastError();
+        cudaFreeAsync(p, stream);
+        return nullptr;
+    }
+    if (s.base) cudaFreeAsync(s.base, stream);
+    s.base = static_cast<unsigned char *>(p);
+    s.bytes = bytes;
+    return &s;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *linrec_status_string(linrec_status_t s) {
+    switch (s) {
+        case LINREC_OK: return "LINREC_OK";
+        case LINREC_ERR_INVALID_VALUE: return "LINREC_ERR_INVALID_VALUE: bad size, NULL pointer or option";
+        case LINREC_ERR_ALIAS: return "LINREC_ERR_ALIAS: h overlaps a or b";
+        case LINREC_ERR_UNSUPPORTED_DEVICE: return "LINREC_ERR_UNSUPPORTED_DEVICE: needs compute capability 10.3";
+        case LINREC_ERR_LAUNCH: return "LINREC_ERR_LAUNCH: a CUDA call failed while enqueueing";
+        case LINREC_ERR_WORKSPACE: return "LINREC_ERR_WORKSPACE: look-back workspace allocation failed";
+        case LINREC_ERR_LOOKBACK_TIMEOUT: return "LINREC_ERR_LOOKBACK_TIMEOUT: a tile gave up on its predecessor";
+        case LINREC_ERR_TMA_TIMEOUT: return "LINREC_ERR_TMA_TIMEOUT: a bulk copy did not complete in time";
+    }
+    return "unknown linrec status";
+}
+
+int linrec_version(void) { return kVersion; }
+
+linrec_status_t linrec_plan_f32(int64_t B, int64_t L, int64_t D, int sm_count, int align_bytes, int ctas_per_sm,
+                                const linrec_options_t *opt, linrec_plan_t *plan) {
+    return plan_impl(B, L, D, sm_count, align_bytes, ctas_per_sm, opt, plan, nullptr);
+}
+
+linrec_status_t linrec_scan_f32_ex(const float *a, const float *b, float *h, int64_t B, int64_t L, int64_t D,
+                                   void *stream_ptr, const linrec_options_t *opt) {
+    linrec_options_t none = {};
+    if (!opt) opt = &none;
+    int64_t n = 0;
+    linrec_status_t st = check_sizes(B, L, D, &n);
+    if (st != LINREC_OK) return st;
+    if (n == 0) return LINREC_OK;
+    if (!a || !b || !h) return LINREC_ERR_INVALID_VALUE;
+    if (overlaps(h, a, n * 4) || overlaps(h, b, n * 4)) return LINREC_ERR_ALIAS;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return LINREC_ERR_LAUNCH;
+    }
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceInfo *di = device_info(dev);
+    if (!di) return LINREC_ERR_LAUNCH;
+    if (!di->supported) return LINREC_ERR_UNSUPPORTED_DEVICE;
+
+    const int align = align_of(a, b, h);
+    linrec_plan_t plan;
+    int vi = -1;
+    st = plan_impl(B, L, D, di->sm_count, align, 0, opt, &plan, &vi);
+    if (st != LINREC_OK) return st;
+
+    if (plan.path == LINREC_PATH_REGCARRY) {
+        cudaError_t err = launch_regcarry(plan.vec, plan.prefetch, plan.threads, a, b, h, B, L, D, stream);
+        return err == cudaSuccess ? LINREC_OK : LINREC_ERR_LAUNCH;
+    }
+
+    // chunked: resident CTAs per SM from the occupancy API, then the real plan
+    int nvar = 0;
+    const ChunkedVariant *variants = chunked_variants(&nvar);
+    if (vi < 0 || vi >= 64) return LINREC_ERR_INVALID_VALUE;
+    if (di->ctas_per_sm[vi] == 0) {
+        int c = 0;
+        if (chunked_ctas_per_sm(&variants[vi], &c) != cudaSuccess || c <= 0) {
+            cudaGetLastError();
+            return LINREC_ERR_LAUNCH;
+        }
+        di->ctas_per_sm[vi] = c;
+    }
+    st = plan_impl(B, L, D, di->sm_count, align, di->ctas_per_sm[vi], opt, &plan, &vi);
+    if (st != LINREC_OK) return st;
+    if (!get_encoder()) return LINREC_ERR_LAUNCH;
+
+    ChunkedLaunch p;
+    p.variant = &variants[vi];
+    if (!encode_map(&p.map_a, a, B, L, D, plan.tile_d, plan.tile_t) ||
+        !encode_map(&p.map_b, b, B, L, D, plan.tile_d, plan.tile_t))
+        return LINREC_ERR_LAUNCH;
+    Slot *ws = workspace(dev, stream, plan.workspace_bytes);
+    if (!ws) return LINREC_ERR_WORKSPACE;
+    p.h = h;
+    p.L = L;
+    p.D = D;
+    p.slices_per_batch = (D + plan.tile_d - 1) / plan.tile_d;
+    p.n_slices = B * p.slices_per_batch;
+    p.chunks = plan.chunks;
+    p.n_tiles = plan.n_tiles;
+    p.grid = plan.grid;
+    p.ctrl = reinterpret_cast<Control *>(ws->base);
+    p.words = reinterpret_cast<unsigned long long *>(ws->base + kWorkspaceHead);
+    p.status = opt->d_status ? opt->d_status : &p.ctrl->status;
+    p.spin_limit = opt->spin_limit > 0 ? opt->spin_limit : kDefaultSpinLimit;
+    p.silent_tile = opt->test_silent_tile > 0 ? opt->test_silent_tile - 1 : -1;
+    cudaError_t err = launch_chunked(p, stream);
+    if (err != cudaSuccess) {
+        cudaGetLastError();
+        return LINREC_ERR_LAUNCH;
+    }
+    return LINREC_OK;
+}
+
+linrec_status_t linrec_scan_f32(const float *a, const float *b, float *h, int64_t B, int64_t L, int64_t D,
+                                void *stream) {
+    return linrec_scan_f32_ex(a, b, h, B, L, D, stream, nullptr);
+}
+
+linrec_status_t linrec_stream_status(void *stream_ptr) {
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return LINREC_ERR_LAUNCH;
+    }
+    unsigned char *base = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        auto it = g_slots.find({dev, reinterpret_cast<uintptr_t>(stream)});
+        if (it == g_slots.end() || !it->second.base) return LINREC_OK;
+        base = it->second.base;
+    }
+    Control *ctrl = reinterpret_cast<Control *>(base);
+    unsigned int word = 0;
+    if (cudaMemcpyAsync(&word, &ctrl->status, sizeof(word), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess) {
+        cudaGetLastError();
+        return LINREC_ERR_LAUNCH;
+    }
+    if (word == 0) return LINREC_OK;
+    if (cudaMemsetAsync(&ctrl->status, 0, sizeof(word), stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess) {
+        cudaGetLastError();
+        return LINREC_ERR_LAUNCH;
+    }
+    if (word & kStatusLookbackTimeout) return LINREC_ERR_LOOKBACK_TIMEOUT;
+    if (word & kStatusTmaTimeout) return LINREC_ERR_TMA_TIMEOUT;
+    return LINREC_ERR_LAUNCH;
+}
+
+linrec_status_t linrec_copy_f32(const float *src, float *dst, int64_t n, void *stream) {
+    if (n < 0) return LINREC_ERR_INVALID_VALUE;
+    if (n == 0) return LINREC_OK;
+    if (!src || !dst) return LINREC_ERR_INVALID_VALUE;
+    if (n > INT64_MAX / 8) return LINREC_ERR_INVALID_VALUE;
+    if (overlaps(src, dst, n * 4)) return LINREC_ERR_ALIAS;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return LINREC_ERR_LAUNCH;
+    }
+    int sms = 0;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        DeviceInfo *di = device_info(dev);
+        if (!di) return LINREC_ERR_LAUNCH;
+        if (!di->supported) return LINREC_ERR_UNSUPPORTED_DEVICE;
+        sms = di->sm_count;
+    }
+    return launch_copy(src, dst, n, sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? LINREC_OK
+                                                                                            : LINREC_ERR_LAUNCH;
+}
+
+}  // extern "C"

@@ -1,0 +1,111 @@
+// regcarry.cu -- the register-carry path of the linear-recurrence scan.
+//
+// h_0 = b_0, h_t = a_t*h_{t-1} + b_t per channel (POPCORNBENCH "Kimi-K2.6 l1_p9",
+// problem statement).  One thread owns V adjacent channels of one batch index
+// (V = 4: one 16-byte load of a and of b per step; a warp covers 32*V
+// consecutive floats of a row, so every access is coalesced along D) and walks
+// t = 0 .. L-1 with h in registers.  Only the FMA chain is serial: the loads of
+// a_t, b_t do not depend on h, so the loads of the next P steps are kept in
+// flight in a register ring, which is what keeps HBM busy when the number of
+// channels alone does not.
+#include "kernels.cuh"
+
+namespace linrec {
+
+namespace {
+
+template <int V> struct VecT;
+template <> struct VecT<1> { using type = float; };
+template <> struct VecT<2> { using type = float2; };
+template <> struct VecT<4> { using type = float4; };
+
+__device__ __forceinline__ float ld_stream(const float *p) { return __ldcs(p); }
+__device__ __forceinline__ float2 ld_stream(const float2 *p) { return __ldcs(p); }
+__device__ __forceinline__ float4 ld_stream(const float4 *p) { return __ldcs(p); }
+__device__ __forceinline__ void st_stream(float *p, float v) { __stcs(p, v); }
+__device__ __forceinline__ void st_stream(float2 *p, float2 v) { __stcs(p, v); }
+__device__ __forceinline__ void st_stream(float4 *p, float4 v) { __stcs(p, v); }
+
+__device__ __forceinline__ float step(float a, float h, float b) { return fmaf(a, h, b); }
+__device__ __forceinline__ float2 step(float2 a, float2 h, float2 b) {
+    return make_float2(fmaf(a.x, h.x, b.x), fmaf(a.y, h.y, b.y));
+}
+__device__ __forceinline__ float4 step(float4 a, float4 h, float4 b) {
+    return make_float4(fmaf(a.x, h.x, b.x), fmaf(a.y, h.y, b.y), fmaf(a.z, h.z, b.z), fmaf(a.w, h.w, b.w));
+}
+__device__ __forceinline__ void zero(float &v) { v = 0.0f; }
+__device__ __forceinline__ void zero(float2 &v) { v = make_float2(0.0f, 0.0f); }
+__device__ __forceinline__ void zero(float4 &v) { v = make_float4(0.0f, 0.0f, 0.0f, 0.0f); }
+
+template <int V, int P>
+__global__ void __launch_bounds__(256)
+regcarry_kernel(const float *__restrict__ a, const float *__restrict__ b, float *__restrict__ h,
+                const long long L, const long long D, const long long groups_per_batch,
+                const long long n_groups)
+{
+    using vec = typename VecT<V>::type;
+    const long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (g >= n_groups) return;
+    const long long bi = g / groups_per_batch;
+    const long long off = bi * L * D + (g - bi * groups_per_batch) * V;
+    const vec *pa = reinterpret_cast<const vec *>(a + off);
+    const vec *pb = reinterpret_cast<const vec *>(b + off);
+    vec *ph = reinterpret_cast<vec *>(h + off);
+    const long long stride = D / V;           // one time step, in vectors
+
+    vec ra[P], rb[P];
+#pragma unroll
+    for (int j = 0; j < P; ++j) {
+        if (j < L) {
+            ra[j] = ld_stream(pa + j * stride);
+            rb[j] = ld_stream(pb + j * stride);
+        }
+    }
+    zero(ra[0]);                              // h_{-1} = 0 and a_0 is never used
+    vec hv;
+    zero(hv);
+    for (long long t0 = 0; t0 < L; t0 += P) {
+#pragma unroll
+        for (int j = 0; j < P; ++j) {
+            const long long t = t0 + j;
+            if (t < L) {
+                hv = step(ra[j], hv, rb[j]);
+                st_stream(ph + t * stride, hv);
+                const long long tn = t + P;
+                if (tn < L) {
+                    ra[j] = ld_stream(pa + tn * stride);
+                    rb[j] = ld_stream(pb + tn * stride);
+                }
+            }
+        }
+    }
+}
+
+template <int V, int P>
+cudaError_t launch_one(int threads, const float *a, const float *b, float *h, int64_t B, int64_t L,
+                       int64_t D, cudaStream_t stream) {
+    const long long gpb = D / V;
+    const long long n = B * gpb;
+    const long long blocks = (n + threads - 1) / threads;
+    regcarry_kernel<V, P><<<(unsigned)blocks, threads, 0, stream>>>(a, b, h, L, D, gpb, n);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool regcarry_supported(int vec, int prefetch) {
+    return (vec == 1 || vec == 2 || vec == 4) && (prefetch == 4 || prefetch == 8 || prefetch == 16);
+}
+
+cudaError_t launch_regcarry(int vec, int prefetch, int threads, const float *a, const float *b, float *h,
+                            int64_t B, int64_t L, int64_t D, cudaStream_t stream) {
+#define LINREC_RC(V, P) \
+    if (vec == V && prefetch == P) return launch_one<V, P>(threads, a, b, h, B, L, D, stream);
+    LINREC_RC(4, 4) LINREC_RC(4, 8) LINREC_RC(4, 16)
+    LINREC_RC(2, 4) LINREC_RC(2, 8) LINREC_RC(2, 16)
+    LINREC_RC(1, 4) LINREC_RC(1, 8) LINREC_RC(1, 16)
+#undef LINREC_RC
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace linrec

@@ -1,0 +1,136 @@
+"""The C ABI without a GPU: the library loads, exports what include/linrec.h
+declares, and its host logic (argument checks, dispatcher) behaves.  No call
+here reaches a CUDA API: every one returns before touching a device."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import linear_recurrence_scan_fp32_gb300 as lr
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    try:
+        return lr.lib()
+    except lr.LinrecError:
+        from linear_recurrence_scan_fp32_gb300 import _build
+        _build.build()
+        return lr.lib()
+
+
+def declared_functions():
+    names = set()
+    for path in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(path).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*[A-Za-z_][\w\s\*]*?\b(linrec_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ["linrec_scan_f32", "linrec_scan_f32_ex", "linrec_plan_f32", "linrec_stream_status",
+              "linrec_copy_f32", "linrec_status_string", "linrec_version"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    missing = [n for n in declared_functions() if not hasattr(L, n)]
+    assert not missing, f"declared but not exported: {missing}"
+
+
+def test_status_strings(L):
+    for code in range(8):
+        s = lr.linrec_status_string(code)
+        assert s.startswith("LINREC_")
+    assert "unknown" in lr.linrec_status_string(99)
+    assert lr.linrec_version() >= 100
+
+
+def _scan(L, a, b, h, B, Lx, D):
+    return L.linrec_scan_f32(a, b, h, B, Lx, D, None)
+
+
+def test_argument_checks_return_before_any_launch(L):
+    # negative sizes
+    assert _scan(L, 16, 4096, 8192, -1, 4, 4) == lr.LINREC_ERR_INVALID_VALUE
+    assert _scan(L, 16, 4096, 8192, 1, -4, 4) == lr.LINREC_ERR_INVALID_VALUE
+    # empty problems succeed with no launch, NULL pointers allowed
+    assert _scan(L, None, None, None, 0, 5, 5) == lr.LINREC_OK
+    assert _scan(L, None, None, None, 5, 0, 5) == lr.LINREC_OK
+    assert _scan(L, None, None, None, 5, 5, 0) == lr.LINREC_OK
+    # NULL with a non-zero size
+    assert _scan(L, None, 4096, 1 << 30, 1, 4, 4) == lr.LINREC_ERR_INVALID_VALUE
+    assert _scan(L, 4096, 4096, None, 1, 4, 4) == lr.LINREC_ERR_INVALID_VALUE
+    # B*L*D*4 overflowing int64
+    assert _scan(L, 16, 1 << 40, 1 << 41, 1 << 20, 1 << 20, 1 << 22) == lr.LINREC_ERR_INVALID_VALUE
+    # h overlapping a or b (fake addresses: rejected before any device access)
+    base = 1 << 32
+    assert _scan(L, base, base + (1 << 20), base + 8, 1, 4, 4) == lr.LINREC_ERR_ALIAS
+    assert _scan(L, base + (1 << 20), base, base + 60, 1, 4, 4) == lr.LINREC_ERR_ALIAS
+    # a and b may be the same buffer; h right after them does not overlap
+    n = 1 * 4 * 4
+    assert L.linrec_copy_f32(base, base + 8, n, None) == lr.LINREC_ERR_ALIAS
+    assert L.linrec_copy_f32(base, base + 8, -1, None) == lr.LINREC_ERR_INVALID_VALUE
+
+
+def test_plan_paths():
+    # many channels: the register path with 16-byte vectors
+    p = lr.linrec_plan_f32(256, 128, 4096)
+    assert p["path_name"] == "regcarry" and p["vec"] == 4
+    assert p["grid"] * p["threads"] >= 256 * 4096 // 4
+    # few channels, long sequence: the chunked look-back path
+    p = lr.linrec_plan_f32(1, 1 << 20, 64)
+    assert p["path_name"] == "chunked"
+    assert p["n_tiles"] == p["chunks"] * ((64 + p["tile_d"] - 1) // p["tile_d"])
+    assert p["chunks"] == -(-(1 << 20) // p["tile_t"])
+    assert p["workspace_bytes"] >= 3 * 8 * p["n_tiles"] * p["tile_d"]
+    # the pages' shape
+    p = lr.linrec_plan_f32(32, 4096, 256)
+    assert p["path_name"] in ("chunked", "regcarry")
+
+
+def test_plan_alignment_and_odd_d():
+    # D % 4 != 0 or pointers not 16-byte aligned: TMA is not allowed, scalar or pair loads instead
+    assert lr.linrec_plan_f32(1, 1 << 20, 63)["path_name"] == "regcarry"
+    assert lr.linrec_plan_f32(1, 1 << 20, 63)["vec"] == 1
+    assert lr.linrec_plan_f32(1, 1 << 20, 62, align_bytes=8)["vec"] == 2
+    assert lr.linrec_plan_f32(1, 1 << 20, 64, align_bytes=8)["path_name"] == "regcarry"
+    assert lr.linrec_plan_f32(1, 1 << 20, 64, align_bytes=4)["vec"] == 1
+    with pytest.raises(lr.LinrecError) as e:
+        lr.linrec_plan_f32(1, 1000, 63, path="chunked")
+    assert e.value.code == lr.LINREC_ERR_INVALID_VALUE
+    with pytest.raises(lr.LinrecError):
+        lr.linrec_plan_f32(1, 1000, 64, align_bytes=4, path="chunked")
+    with pytest.raises(lr.LinrecError):
+        lr.linrec_plan_f32(1, 1000, 64, path="regcarry", vec=4, align_bytes=8)
+
+
+def test_plan_forced_options():
+    p = lr.linrec_plan_f32(32, 4096, 256, path="chunked", tile_d=64, tile_t=64, stages=3)
+    assert (p["tile_d"], p["tile_t"], p["stages"]) == (64, 64, 3)
+    assert p["threads"] == p["tile_d"] * p["segments"]
+    with pytest.raises(lr.LinrecError):
+        lr.linrec_plan_f32(32, 4096, 256, path="chunked", tile_d=48, tile_t=64)
+    p = lr.linrec_plan_f32(32, 4096, 256, path="regcarry", vec=2, prefetch=4)
+    assert (p["vec"], p["prefetch"]) == (2, 4)
+    with pytest.raises(lr.LinrecError):
+        lr.linrec_plan_f32(32, 4096, 256, path="regcarry", prefetch=5)
+
+
+def test_plan_grid_bounds():
+    # grid never exceeds the tile count nor SMs x resident CTAs
+    for (B, L, D) in [(1, 64, 32), (1, 1 << 20, 64), (32, 4096, 256), (3, 5, 8)]:
+        p = lr.linrec_plan_f32(B, L, D, path="chunked", sm_count=152, resident_ctas=2)
+        assert 1 <= p["grid"] <= min(p["n_tiles"], 152 * 2)
+    p = lr.linrec_plan_f32(32, 4096, 256, path="chunked", sm_count=152, resident_ctas=3)
+    assert p["grid"] == min(p["n_tiles"], 152 * 3)
+    # the options' cap lowers the resident count
+    p = lr.linrec_plan_f32(32, 4096, 256, path="chunked", sm_count=152, resident_ctas=3, ctas_per_sm=1)
+    assert p["grid"] == min(p["n_tiles"], 152)

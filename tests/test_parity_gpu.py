@@ -1,0 +1,301 @@
+"""Parity of the CUDA kernels with the fp64 CPU oracle, through the C ABI.
+
+Bound (per element): |h - h64| <= 1e-4 * (1 + |h64|).  The closed-form
+variants with integer b (a = 1: prefix sums below 2^24; a = 0: h = b) must
+match bit for bit on every path.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import linear_recurrence_scan_fp32_gb300 as lr
+import oracle
+from linear_recurrence_scan_fp32_gb300 import inputs
+from tests._util import assert_close, max_errors
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from linear_recurrence_scan_fp32_gb300 import _build
+    _build.build()
+    torch.cuda.set_device(DEV)
+
+
+def run(a_d, b_d, **opt):
+    h = lr.linrec_scan_f32_ex(a_d, b_d, **opt) if opt else lr.linrec_scan_f32(a_d, b_d)
+    torch.cuda.synchronize()
+    return h
+
+
+def legal_paths(B, L, D, aligned=True):
+    paths = [{"path": "regcarry"}]
+    if aligned and D % 4 == 0:
+        paths.append({"path": "chunked"})
+    return paths
+
+
+# ---------------------------------------------------------------------------
+# the five workloads at full size, every path, against the full fp64 oracle
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", inputs.CONFIG_ORDER)
+def test_workload_full_size(name):
+    w = inputs.WORKLOADS[name]
+    a, b = inputs.generate_workload(w)
+    h64, _ = oracle.f64(a, b)
+    a_d, b_d = a.to(DEV), b.to(DEV)
+    del a, b
+    for opt in [{}] + legal_paths(w.B, w.L, w.D):
+        h = run(a_d, b_d, **opt).cpu().numpy()
+        assert_close(h, h64, f"{name} {opt or 'auto'}")
+        del h
+    assert lr.linrec_stream_status() == lr.LINREC_OK
+
+
+@pytest.mark.parametrize("name", ["short_ones_int", "short_zeros_int"])
+def test_closed_forms_bit_exact(name):
+    w = inputs.WORKLOADS[name]
+    a, b = inputs.generate_workload(w)
+    bn = b.numpy()
+    if w.a_dist == "ones":
+        want = np.cumsum(bn.astype(np.float64), axis=1).astype(np.float32)   # |sum| <= 1024: exact
+    else:
+        want = bn
+    a_d, b_d = a.to(DEV), b.to(DEV)
+    for opt in [{}] + legal_paths(w.B, w.L, w.D):
+        h = run(a_d, b_d, **opt).cpu().numpy()
+        assert np.array_equal(h, want), f"{name} {opt}: not bit-exact"
+
+
+@pytest.mark.parametrize("name", ["short_ones", "short_zeros"])
+def test_closed_forms_real_b(name):
+    w = inputs.WORKLOADS[name]
+    a, b = inputs.generate_workload(w)
+    h64, _ = oracle.f64(a, b)
+    a_d, b_d = a.to(DEV), b.to(DEV)
+    for opt in [{}] + legal_paths(w.B, w.L, w.D):
+        assert_close(run(a_d, b_d, **opt).cpu().numpy(), h64, f"{name} {opt}")
+    if w.a_dist == "zeros":   # a = 0 copies b exactly even with real b
+        for opt in [{}] + legal_paths(w.B, w.L, w.D):
+            assert torch.equal(run(a_d, b_d, **opt), b_d)
+
+
+def test_geometric_long_carry():
+    """Long-sequence shape (1, 1048576, 64), a = 0.99, b = 1: h_t = (1 - 0.99^(t+1)) / 0.01."""
+    B, L, D = 1, 1 << 20, 64
+    a_d = torch.full((B, L, D), 0.99, device=DEV)
+    b_d = torch.ones((B, L, D), device=DEV)
+    t = np.arange(L, dtype=np.float64)
+    want = (1.0 - np.float64(np.float32(0.99)) ** (t + 1)) / (1.0 - np.float64(np.float32(0.99)))
+    for opt in [{}] + legal_paths(B, L, D):
+        h = run(a_d, b_d, **opt).cpu().numpy()
+        for d in (0, 17, 63):
+            assert_close(h[0, :, d], want, f"geometric {opt} d={d}")
+
+
+# ---------------------------------------------------------------------------
+# ragged shapes, every path and every chunked variant
+# ---------------------------------------------------------------------------
+
+RAGGED = [(1, 1, 4), (1, 2, 8), (3, 31, 4), (2, 33, 36), (1, 65, 100), (3, 127, 132), (2, 129, 64),
+          (1, 1000, 260), (2, 257, 68), (1, 5000, 32), (1, 4097, 8), (4, 300, 1),
+          (1, 70, 3), (2, 33, 5), (3, 100, 33), (1, 2, 2), (2, 9, 6)]
+
+
+@pytest.mark.parametrize("shape", RAGGED, ids=lambda s: "x".join(map(str, s)))
+def test_ragged_shapes(shape):
+    B, L, D = shape
+    a, b = inputs.generate(B, L, D, seed=100 + L + D, a_dist="u[0.5,1)", b_dist="n(0,1)")
+    h64, _ = oracle.f64(a, b)
+    a_d, b_d = a.to(DEV), b.to(DEV)
+    opts = [{}] + legal_paths(B, L, D)
+    if D % 2 == 0:
+        opts.append({"path": "regcarry", "vec": 2})
+    opts.append({"path": "regcarry", "vec": 1, "prefetch": 4})
+    for opt in opts:
+        assert_close(run(a_d, b_d, **opt).cpu().numpy(), h64, f"{shape} {opt}")
+
+
+def _variants():
+    out = []
+    for td, tt, st in [(128, 64, 2), (128, 64, 3), (128, 32, 3), (256, 32, 2), (64, 128, 2), (64, 64, 2),
+                       (64, 64, 3), (32, 128, 2), (32, 64, 3)]:
+        out.append({"path": "chunked", "tile_d": td, "tile_t": tt, "stages": st})
+    return out
+
+
+@pytest.mark.parametrize("opt", _variants(), ids=lambda o: f"d{o['tile_d']}t{o['tile_t']}s{o['stages']}")
+def test_every_chunked_variant(opt):
+    for (B, L, D) in [(3, 1000, 260), (1, 20000, 64), (2, 777, 36)]:
+        a, b = inputs.generate(B, L, D, seed=7 + L, a_dist="u[0.9,1)", b_dist="n(0,1)")
+        h64, _ = oracle.f64(a, b)
+        h = run(a.to(DEV), b.to(DEV), **opt).cpu().numpy()
+        assert_close(h, h64, f"{(B, L, D)} {opt}")
+
+
+@pytest.mark.parametrize("vec,prefetch", [(v, p) for v in (1, 2, 4) for p in (4, 8, 16)])
+def test_every_regcarry_variant(vec, prefetch):
+    B, L, D = 2, 515, 132
+    a, b = inputs.generate(B, L, D, seed=55, a_dist="u[0,1)", b_dist="n(0,1)")
+    h64, _ = oracle.f64(a, b)
+    h = run(a.to(DEV), b.to(DEV), path="regcarry", vec=vec, prefetch=prefetch).cpu().numpy()
+    assert_close(h, h64, f"regcarry vec={vec} prefetch={prefetch}")
+
+
+# ---------------------------------------------------------------------------
+# memory safety, determinism, inputs untouched, misalignment
+# ---------------------------------------------------------------------------
+
+CANARY = 0x7fc0dead   # a NaN payload no kernel writes
+
+
+def test_guard_bands_and_inputs_untouched():
+    for (B, L, D) in [(3, 1000, 260), (1, 4097, 64), (2, 33, 5)]:
+        a, b = inputs.generate(B, L, D, seed=3, a_dist="u[0.5,1)", b_dist="n(0,1)")
+        h64, _ = oracle.f64(a, b)
+        n = B * L * D
+        guard = 4096
+        for opt in [{}] + legal_paths(B, L, D):
+            buf = torch.full((n + 2 * guard,), 0, dtype=torch.int32, device=DEV)
+            buf.fill_(CANARY)
+            hv = buf.view(torch.float32)[guard:guard + n].view(B, L, D)
+            a_d, b_d = a.to(DEV), b.to(DEV)
+            lr.linrec_scan_f32_ex(a_d, b_d, hv, **opt)
+            torch.cuda.synchronize()
+            assert (buf[:guard] == CANARY).all() and (buf[guard + n:] == CANARY).all(), f"guard band {opt}"
+            assert torch.equal(a_d.cpu(), a) and torch.equal(b_d.cpu(), b), "inputs modified"
+            assert_close(hv.cpu().numpy(), h64, f"guarded {opt}")
+
+
+def test_deterministic_bits():
+    for name in ("pages", "long"):
+        w = inputs.WORKLOADS[name]
+        a, b = inputs.generate_workload(w)
+        a_d, b_d = a.to(DEV), b.to(DEV)
+        for opt in [{}] + legal_paths(w.B, w.L, w.D):
+            h1 = run(a_d, b_d, **opt).clone()
+            for _ in range(3):
+                assert torch.equal(run(a_d, b_d, **opt), h1), f"{name} {opt}: bits changed between calls"
+
+
+def test_misaligned_pointers_take_the_scalar_path():
+    B, L, D = 2, 300, 64
+    a, b = inputs.generate(B, L, D, seed=9, a_dist="u[0.5,1)", b_dist="n(0,1)")
+    h64, _ = oracle.f64(a, b)
+    n = B * L * D
+    ab = torch.empty(2 * n + 2, device=DEV)
+    a_d = ab[1:1 + n]
+    b_d = ab[n + 2:]
+    a_d.copy_(a.reshape(-1).to(DEV))
+    b_d.copy_(b.reshape(-1).to(DEV))
+    hbuf = torch.empty(n + 1, device=DEV)
+    h_d = hbuf[1:]
+    L_ = lr.lib()
+    code = L_.linrec_scan_f32(a_d.data_ptr(), b_d.data_ptr(), h_d.data_ptr(), B, L, D,
+                              ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert code == lr.LINREC_OK
+    torch.cuda.synchronize()
+    assert_close(h_d.view(B, L, D).cpu().numpy(), h64, "misaligned auto")
+    # forcing TMA on misaligned pointers is refused, not run
+    opt = lr.make_options(path="chunked")
+    code = L_.linrec_scan_f32_ex(a_d.data_ptr(), b_d.data_ptr(), h_d.data_ptr(), B, L, D,
+                                 ctypes.c_void_p(torch.cuda.current_stream().cuda_stream), ctypes.byref(opt))
+    assert code == lr.LINREC_ERR_INVALID_VALUE
+
+
+def test_a0_is_ignored():
+    a, b = inputs.generate(2, 500, 64, seed=11, a_dist="u[0.5,1)", b_dist="n(0,1)")
+    h64, _ = oracle.f64(a, b)
+    a[:, 0, :] = float("nan")
+    a_d, b_d = a.to(DEV), b.to(DEV)
+    for opt in [{}] + legal_paths(2, 500, 64):
+        h = run(a_d, b_d, **opt).cpu().numpy()
+        assert np.isfinite(h).all()
+        assert_close(h, h64, f"a_0 = NaN {opt}")
+
+
+def test_aliasing_rejected_on_device_pointers():
+    a = torch.rand(1, 10, 8, device=DEV)
+    b = torch.rand(1, 10, 8, device=DEV)
+    with pytest.raises(lr.LinrecError) as e:
+        lr.linrec_scan_f32(a, b, a)
+    assert e.value.code == lr.LINREC_ERR_ALIAS
+    h = lr.linrec_scan_f32(a, a)   # a and b may be the same buffer
+    torch.cuda.synchronize()
+    h64, _ = oracle.f64(a.cpu(), a.cpu())
+    assert_close(h.cpu().numpy(), h64, "a is b")
+
+
+def test_streams_run_independently():
+    B, L, D = 1, 1 << 16, 64
+    a, b = inputs.generate(B, L, D, seed=12, a_dist="u[0.9,1)", b_dist="n(0,1)")
+    h64, _ = oracle.f64(a, b)
+    a_d, b_d = a.to(DEV), b.to(DEV)
+    streams = [torch.cuda.Stream() for _ in range(3)]
+    outs = []
+    for s in streams:
+        with torch.cuda.stream(s):
+            outs.append(lr.linrec_scan_f32_ex(a_d, b_d, stream=s, path="chunked"))
+    torch.cuda.synchronize()
+    for h in outs:
+        assert_close(h.cpu().numpy(), h64, "multi-stream")
+    for s in streams:
+        assert lr.linrec_stream_status(s) == lr.LINREC_OK
+
+
+# ---------------------------------------------------------------------------
+# failure detection without a fault: a bounded look-back wait that runs out
+# ---------------------------------------------------------------------------
+
+def test_lookback_timeout_reports_and_recovers():
+    B, L, D = 1, 64 * 64, 64
+    a, b = inputs.generate(B, L, D, seed=13, a_dist="u[0.5,1)", b_dist="n(0,1)")
+    h64, _ = oracle.f64(a, b)
+    a_d, b_d = a.to(DEV), b.to(DEV)
+    s = torch.cuda.Stream()
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    with torch.cuda.stream(s):
+        # tile 5 publishes nothing: tile 6 waits a bounded number of polls, then gives up
+        h = lr.linrec_scan_f32_ex(a_d, b_d, stream=s, path="chunked", tile_d=64, tile_t=64, stages=2,
+                                  spin_limit=2000, test_silent_tile=5 + 1, d_status=status)
+    s.synchronize()
+    assert int(status.item()) & (1 << lr.LINREC_ERR_LOOKBACK_TIMEOUT)
+    hn = h.cpu().numpy()
+    # tiles before the silent one's successor are intact; the lost carry shows as NaN after it
+    assert_close(hn[:, :6 * 64], h64[:, :6 * 64], "before the timeout")
+    assert np.isnan(hn[:, 6 * 64:]).any()
+    # the stream's own word: same failure through the plain status query
+    with torch.cuda.stream(s):
+        lr.linrec_scan_f32_ex(a_d, b_d, stream=s, path="chunked", tile_d=64, tile_t=64, stages=2,
+                              spin_limit=2000, test_silent_tile=5 + 1)
+    assert lr.linrec_stream_status(s) == lr.LINREC_ERR_LOOKBACK_TIMEOUT
+    assert lr.linrec_stream_status(s) == lr.LINREC_OK          # cleared
+    # the context is healthy: the next call on the same stream is exact
+    with torch.cuda.stream(s):
+        h = lr.linrec_scan_f32_ex(a_d, b_d, stream=s, path="chunked", tile_d=64, tile_t=64, stages=2)
+    s.synchronize()
+    assert_close(h.cpu().numpy(), h64, "after recovery")
+    assert lr.linrec_stream_status(s) == lr.LINREC_OK
+
+
+def test_copy_kernel():
+    x = torch.randn(1 << 20, device=DEV)
+    y = torch.empty_like(x)
+    lr.linrec_copy_f32(x, y)
+    torch.cuda.synchronize()
+    assert torch.equal(x, y)
+    y2 = torch.empty(x.numel() + 1, device=DEV)[1:]
+    lr.linrec_copy_f32(x[:-1], y2[:-1])
+    torch.cuda.synchronize()
+    assert torch.equal(x[:-1], y2[:-1])
+
+
+def test_errors_reported():
+    h64_err = max_errors(np.zeros(3), np.zeros(3))
+    assert h64_err == (0.0, 0.0)
