@@ -15,11 +15,12 @@
 //     the associative operator).  Its a, b values stay in registers.
 //  3. A warp-shuffle scan over the S segment pairs of each channel gives every
 //     segment its exclusive prefix and the tile its aggregate.
-//  4. Decoupled look-back (one thread per channel): publish the tile aggregate,
-//     walk back over earlier tiles of the same slice, composing aggregates
-//     until an inclusive value is found, publish this tile's inclusive value.
-//     Only the running value h crosses tile boundaries ("Kimi-K2.6 l1_p9",
-//     the running_h carry): h_out = A_prefix * h_in + B_prefix.
+//  4. Decoupled look-back (S lanes per channel, one predecessor per lane):
+//     publish the tile aggregate, walk back over earlier tiles of the same
+//     slice until an inclusive value is found, replay the chain of aggregates
+//     forward from it, publish this tile's inclusive value.  Only the running
+//     value h crosses tile boundaries ("Kimi-K2.6 l1_p9", the running_h
+//     carry): h_out = A_prefix * h_in + B_prefix.
 //  5. Every thread replays its K steps from the carried value and stores h.
 //
 // Tile ids come from an atomic counter, so every predecessor of a tile was
@@ -34,18 +35,17 @@ namespace linrec {
 namespace {
 
 constexpr uint32_t kTmaPolls = 1u << 22;   // ~1 s of polls with back-off
+constexpr unsigned kFull = 0xffffffffu;
 
 template <int TD, int TT, int S, int ST>
 struct __align__(128) ChunkSmem {
     float a[ST][TT * TD];
     float b[ST][TT * TD];
-    float segA[S][TD], segB[S][TD];     // per-segment aggregates
-    float preA[S][TD], preB[S][TD];     // exclusive prefix of each segment
-    float tileA[TD], tileB[TD], carry[TD];
+    float segA[S][TD], segB[S][TD];     // per-segment pairs, then their exclusive prefixes
+    float carry[TD];                    // h entering the tile, per channel
     uint64_t full[ST];                  // one mbarrier per ring stage
     long long tile_id[ST];              // tile loaded into each stage (>= n_tiles: none)
     uint32_t tag;                       // look-back tag of this launch
-    uint32_t ended;                     // the tile counter ran out (thread 0 only)
 };
 
 __device__ __forceinline__ void decode_tile(long long id, long long n_slices, long long slices_per_batch,
@@ -56,8 +56,122 @@ __device__ __forceinline__ void decode_tile(long long id, long long n_slices, lo
     d0 = (p - bi * slices_per_batch) * td;
 }
 
+// The h value entering tile `id` for channel cc, computed by the CTA's threads in
+// groups of S lanes per channel (lane ss of the group watches one predecessor).
+//
+// The inclusive value of a tile is defined as the chain H_i = A_i * H_{i-1} + B_i
+// (one fma per tile, H before the first chunk = 0).  The group reads a window of
+// S predecessors per round trip, walks back over windows that hold only
+// aggregates until it meets an inclusive value, and then replays the chain
+// forward from it, re-reading the aggregates it passed.  The result is the same
+// bits whichever predecessors happened to have finished: the carry is
+// deterministic.
+template <int S>
+__device__ __forceinline__ float lookback_carry(
+    const long long id, const long long n_slices, const int TD, const int cc, const int ss, const int gbase,
+    const uint32_t tag, const bool publish_agg, const float tA, const float tB,
+    unsigned long long *__restrict__ wAggA, unsigned long long *__restrict__ wAggB,
+    const unsigned long long *__restrict__ wInc, Control *__restrict__ ctrl, unsigned int *__restrict__ status,
+    const long long spin_limit)
+{
+    constexpr unsigned GM = (S == 32) ? kFull : ((1u << S) - 1u);
+    const long long me = id * TD + cc;
+    long long base = id - n_slices;           // tile at window position 0: the predecessor
+    int skipped = 0;                          // windows holding aggregates only
+    int pstar = -1;                           // window position of the nearest inclusive value
+    bool failed = false;
+    float vA = 1.0f, vB = 0.0f, vH = 0.0f;    // what this lane read for its tile
+    long long idle = 0;
+    unsigned int nap = 32;
+    for (int round = 0;; ++round) {
+        const bool active = pstar < 0 && !failed;
+        int kind = 2;                         // 0: nothing yet, 1: aggregate, 2: inclusive
+        if (active) {
+            const long long j = base - (long long)ss * n_slices;
+            if (j < 0) {
+                vH = 0.0f;                    // before the first chunk: h = 0
+            } else {
+                const unsigned long long wi = ld_relaxed_u64(&wInc[j * TD + cc]);
+                if (word_tag(wi) == tag) {
+                    vH = word_val(wi);
+                } else {
+                    const unsigned long long wa = ld_relaxed_u64(&wAggA[j * TD + cc]);
+                    const unsigned long long wb = ld_relaxed_u64(&wAggB[j * TD + cc]);
+                    if (word_tag(wa) == tag && word_tag(wb) == tag) {
+                        kind = 1;
+                        vA = word_val(wa);
+                        vB = word_val(wb);
+                    } else {
+                        kind = 0;
+                    }
+                }
+            }
+        }
+        const unsigned inc_g = (__ballot_sync(kFull, active && kind == 2) >> gbase) & GM;
+        const unsigned none_g = (__ballot_sync(kFull, active && kind == 0) >> gbase) & GM;
+        bool progressed = false;
+        if (active) {
+            if (inc_g) {
+                const int p = __ffs(inc_g) - 1;
+                if ((none_g & ((1u << p) - 1u)) == 0) {
+                    pstar = p;
+                    progressed = true;
+                }
+            } else if (none_g == 0) {
+                ++skipped;
+                base -= (long long)S * n_slices;
+                progressed = true;
+            }
+            // Successors may need this tile's aggregate unless its carry is known at once.
+            if (round == 0 && publish_agg && ss == 0 && pstar != 0) {
+                st_relaxed_u64(&wAggA[me], pack_word(tag, tA));
+                st_relaxed_u64(&wAggB[me], pack_word(tag, tB));
+            }
+            if (progressed) {
+                idle = 0;
+            } else if (++idle > spin_limit || ((idle & 63) == 0 && ld_relaxed_u32(&ctrl->abort) != 0)) {
+                failed = true;
+                if (ss == 0) atomicOr(status, kStatusLookbackTimeout);
+            }
+        }
+        if (__all_sync(kFull, pstar >= 0 || failed)) break;
+        if (__any_sync(kFull, progressed)) {
+            nap = 32;
+        } else {
+            __nanosleep(nap);
+            if (nap < 1024) nap <<= 1;
+        }
+    }
+
+    // Replay the chain forward from the inclusive value: the rest of its window, then
+    // every skipped window, nearest to this tile last.
+    float H = __shfl_sync(kFull, vH, pstar < 0 ? 0 : pstar, S);
+#pragma unroll
+    for (int p = S - 1; p >= 0; --p) {
+        const float ap = __shfl_sync(kFull, vA, p, S);
+        const float bp = __shfl_sync(kFull, vB, p, S);
+        if (p < pstar) H = fmaf(ap, H, bp);
+    }
+    const int most = __reduce_max_sync(kFull, failed ? 0 : skipped);
+    for (int w = most - 1; w >= 0; --w) {
+        const bool mine = !failed && w < skipped;
+        if (mine) {
+            const long long j = id - n_slices - ((long long)w * S + ss) * n_slices;
+            vA = word_val(ld_relaxed_u64(&wAggA[j * TD + cc]));
+            vB = word_val(ld_relaxed_u64(&wAggB[j * TD + cc]));
+        }
+#pragma unroll
+        for (int p = S - 1; p >= 0; --p) {
+            const float ap = __shfl_sync(kFull, vA, p, S);
+            const float bp = __shfl_sync(kFull, vB, p, S);
+            if (mine) H = fmaf(ap, H, bp);
+        }
+    }
+    return failed ? __uint_as_float(0x7fc00000u) : H;   // NaN marks a lost carry
+}
+
 template <int TD, int TT, int S, int ST>
-__global__ void __launch_bounds__(TD * S, 1)
+__global__ void __launch_bounds__(TD * S, (TD * S >= 512) ? 1 : 2)
 chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
                     const __grid_constant__ CUtensorMap map_b,
                     float *__restrict__ h,
@@ -70,7 +184,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
 {
     constexpr int K = TT / S;                 // time steps per thread
     constexpr uint32_t kStageBytes = 2u * TT * TD * sizeof(float);
-    static_assert(TT % S == 0 && TD % 32 == 0 && (32 % S) == 0 && ST >= 2, "tile shape");
+    static_assert(TT % S == 0 && TD % 32 == 0 && (32 % S) == 0 && S >= 2 && ST >= 2, "tile shape");
     using Smem = ChunkSmem<TD, TT, S, ST>;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
@@ -78,6 +192,9 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
     const int tid = threadIdx.x;
     const int c = tid % TD;                   // channel within the tile
     const int s = tid / TD;                   // segment within the tile
+    const int cc = tid / S;                   // transposed role: channel ...
+    const int ss = tid % S;                   // ... and segment / look-back window lane
+    const int gbase = (tid & 31) & ~(S - 1);  // first lane of this channel's group in the warp
 
     unsigned long long *const wAggA = words;
     unsigned long long *const wAggB = words + n_tiles * TD;
@@ -97,38 +214,34 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
     // TMA writes whole boxes at 128-byte aligned shared addresses; the layout
     // guarantees it when the dynamic window is aligned, so check that once.
     const bool misaligned = (smem_u32(smem_raw) & 127u) != 0;
-    if (misaligned) {
-        if (tid == 0) {
+    if (tid == 0) {
+        long long first = n_tiles;
+        if (misaligned) {
             atomicOr(status, kStatusTmaTimeout);
             atomicExch(&ctrl->abort, 1u);
+        } else {
+            for (int st = 0; st < ST; ++st) mbar_init(&sm.full[st], 1);
+            mbar_fence_init();
+            tmap_prefetch(&map_a);
+            tmap_prefetch(&map_b);
+            const uint32_t tag = ld_relaxed_u32(&ctrl->epoch) + 1u;
+            sm.tag = tag == 0 ? 1u : tag;
+            // One tile at launch: tiles are taken in the order CTAs start on them, so a
+            // tile's predecessors are never parked in another CTA's ring behind later work.
+            first = grab();
+            if (first >= n_tiles) first = n_tiles;
+            else issue(0, first);
         }
-    }
-    if (tid == 0 && !misaligned) {
-        for (int st = 0; st < ST; ++st) mbar_init(&sm.full[st], 1);
-        mbar_fence_init();
-        tmap_prefetch(&map_a);
-        tmap_prefetch(&map_b);
-        uint32_t tag = ld_relaxed_u32(&ctrl->epoch) + 1u;
-        sm.tag = tag == 0 ? 1u : tag;
-        uint32_t ended = 0;
-        for (int st = 0; st < ST; ++st) {
-            long long id = n_tiles;
-            if (!ended) {
-                id = grab();
-                if (id >= n_tiles) { ended = 1; id = n_tiles; }
-            }
-            sm.tile_id[st] = id;
-            if (id < n_tiles) issue(st, id);
-        }
-        sm.ended = ended;
-    }
-    if (misaligned && tid == 0) {
-        for (int st = 0; st < ST; ++st) sm.tile_id[st] = n_tiles;
+        sm.tile_id[0] = first;
     }
     __syncthreads();
 
     const uint32_t tag = sm.tag;
     uint32_t phases = 0;                      // bit st: parity of the next completion of stage st
+    long long next_fill = 1;                  // (thread 0) next ring slot to fill
+    bool ended = sm.tile_id[0] >= n_tiles;    // (thread 0) no more tiles to take
+    long long ahead = -1;                     // (thread 0) tile id taken one iteration early
+    uint32_t abort_seen = 0;                  // (thread 0) abort word, read one iteration early
 
     for (long long k = 0;; ++k) {
         const int st = (int)(k % ST);
@@ -141,6 +254,32 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
         }
         phases ^= 1u << st;
 
+        // Keep ST-1 tiles in flight behind this one.  The slot filled last
+        // (k + ST - 1) reuses the stage freed at the end of iteration k - 1.
+        // The next tile id is taken one iteration ahead, so the atomic's round
+        // trip overlaps this tile's work instead of delaying it.
+        if (tid == 0) {
+            if (!ended && abort_seen != 0) {
+                ended = true;
+                sm.tile_id[next_fill % ST] = n_tiles;
+            }
+            while (!ended && next_fill < k + ST) {
+                const int s2 = (int)(next_fill % ST);
+                const long long nid = ahead >= 0 ? ahead : grab();
+                ahead = -1;
+                if (nid >= n_tiles) {
+                    ended = true;
+                    sm.tile_id[s2] = n_tiles;
+                } else {
+                    sm.tile_id[s2] = nid;
+                    issue(s2, nid);
+                }
+                ++next_fill;
+            }
+            if (!ended && ahead < 0) ahead = grab();
+            abort_seen = ld_relaxed_u32(&ctrl->abort);
+        }
+
         long long q, bi, d0;
         decode_tile(id, n_slices, slices_per_batch, q, bi, d0, TD);
         const long long t0 = q * TT;
@@ -149,7 +288,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
         const int nv = rem <= 0 ? 0 : (rem >= K ? K : (int)rem);   // valid steps of this thread
         const bool seq_start = (q == 0 && s == 0);                  // holds t = 0 of its channel
 
-        // ---- 2. compose this thread's K steps -----------------------------
+        // ---- 2. compose this thread's K steps -----------------------------------
         const float *ta = sm.a[st] + r0 * TD + c;
         const float *tb = sm.b[st] + r0 * TD + c;
         float ra[K], rb[K];
@@ -167,96 +306,43 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
                 A = ra[j] * A;
             }
         }
+        sm.segA[s][c] = A;
+        sm.segB[s][c] = Bv;
+        __syncthreads();
 
-        // ---- 3. shuffle scan over the S segments of each channel --------------
-        float tA, tB;                          // tile aggregate (valid in threads tid < TD)
-        if constexpr (S > 1) {
-            sm.segA[s][c] = A;
-            sm.segB[s][c] = Bv;
-            __syncthreads();
-            const int cc = tid / S, ss = tid % S;   // transposed role: lanes walk the segments
-            float xA = sm.segA[ss][cc], xB = sm.segB[ss][cc];
+        // ---- 3. shuffle scan over the S segment pairs of each channel -----------
+        float xA = sm.segA[ss][cc], xB = sm.segB[ss][cc];
 #pragma unroll
-            for (int off = 1; off < S; off <<= 1) {
-                const float uA = __shfl_up_sync(0xffffffffu, xA, off, S);
-                const float uB = __shfl_up_sync(0xffffffffu, xB, off, S);
-                if (ss >= off) {               // (later) o (earlier)
-                    xB = fmaf(xA, uB, xB);
-                    xA = xA * uA;
-                }
+        for (int off = 1; off < S; off <<= 1) {
+            const float uA = __shfl_up_sync(kFull, xA, off, S);
+            const float uB = __shfl_up_sync(kFull, xB, off, S);
+            if (ss >= off) {                  // (later) o (earlier)
+                xB = fmaf(xA, uB, xB);
+                xA = xA * uA;
             }
-            float eA = __shfl_up_sync(0xffffffffu, xA, 1, S);
-            float eB = __shfl_up_sync(0xffffffffu, xB, 1, S);
-            if (ss == 0) { eA = 1.0f; eB = 0.0f; }
-            sm.preA[ss][cc] = eA;
-            sm.preB[ss][cc] = eB;
-            if (ss == S - 1) { sm.tileA[cc] = xA; sm.tileB[cc] = xB; }
-            __syncthreads();
-            tA = sm.tileA[c];
-            tB = sm.tileB[c];
-        } else {
-            tA = A;
-            tB = Bv;
         }
+        float eA = __shfl_up_sync(kFull, xA, 1, S);
+        float eB = __shfl_up_sync(kFull, xB, 1, S);
+        if (ss == 0) { eA = 1.0f; eB = 0.0f; }
+        sm.segA[ss][cc] = eA;                 // same slot this thread read: no other reader
+        sm.segB[ss][cc] = eB;
+        const float tA = __shfl_sync(kFull, xA, S - 1, S);   // the tile's aggregate
+        const float tB = __shfl_sync(kFull, xB, S - 1, S);
 
-        // ---- 4. decoupled look-back, one thread per channel --------------------
-        if (tid < TD) {
-            const bool publish = (q + 1 < chunks) && (id != silent_tile);
-            const long long me = id * TD + c;
-            float carry;
-            if (q == 0) {
-                carry = 0.0f;
-            } else {
-                long long j = id - n_slices;
-                const unsigned long long w = ld_relaxed_u64(&wInc[j * TD + c]);
-                if (word_tag(w) == tag) {
-                    carry = word_val(w);
-                } else {
-                    if (publish) {
-                        st_relaxed_u64(&wAggA[me], pack_word(tag, tA));
-                        st_relaxed_u64(&wAggB[me], pack_word(tag, tB));
-                    }
-                    float accA = 1.0f, accB = 0.0f;   // composition of tiles j+1 .. id-1
-                    long long polls = 0;
-                    unsigned int nap = 32;
-                    for (;;) {
-                        const unsigned long long wi = ld_relaxed_u64(&wInc[j * TD + c]);
-                        if (word_tag(wi) == tag) {
-                            carry = fmaf(accA, word_val(wi), accB);
-                            break;
-                        }
-                        const unsigned long long wa = ld_relaxed_u64(&wAggA[j * TD + c]);
-                        const unsigned long long wb = ld_relaxed_u64(&wAggB[j * TD + c]);
-                        if (word_tag(wa) == tag && word_tag(wb) == tag) {
-                            accB = fmaf(accA, word_val(wb), accB);   // acc o aggregate(j)
-                            accA = accA * word_val(wa);
-                            j -= n_slices;
-                            if (j < 0) { carry = accB; break; }      // h before the first chunk is 0
-                            polls = 0;
-                            nap = 32;
-                            continue;
-                        }
-                        if (++polls > spin_limit ||
-                            ((polls & 63) == 0 && ld_relaxed_u32(&ctrl->abort) != 0)) {
-                            atomicOr(status, kStatusLookbackTimeout);
-                            carry = __uint_as_float(0x7fc00000u);  // NaN marks the lost carry
-                            break;
-                        }
-                        __nanosleep(nap);
-                        if (nap < 1024) nap <<= 1;
-                    }
-                }
-            }
-            if (publish) st_relaxed_u64(&wInc[me], pack_word(tag, fmaf(tA, carry, tB)));
-            sm.carry[c] = carry;
+        // ---- 4. carry from earlier tiles of the slice ----------------------------
+        const bool publish = (q + 1 < chunks) && (id != silent_tile);
+        float carry = 0.0f;
+        if (q > 0)
+            carry = lookback_carry<S>(id, n_slices, TD, cc, ss, gbase, tag, publish, tA, tB,
+                                      wAggA, wAggB, wInc, ctrl, status, spin_limit);
+        if (ss == 0) {
+            if (publish) st_relaxed_u64(&wInc[id * TD + cc], pack_word(tag, fmaf(tA, carry, tB)));
+            sm.carry[cc] = carry;
         }
         __syncthreads();
 
-        // ---- 5. replay the steps from the carried value, store h ----------------
-        const float carry = sm.carry[c];
-        float hc;
-        if constexpr (S > 1) hc = fmaf(sm.preA[s][c], carry, sm.preB[s][c]);
-        else hc = carry;
+        // ---- 5. replay the steps from the carried value, store h -----------------
+        float hc = fmaf(sm.segA[s][c], sm.carry[c], sm.segB[s][c]);
         const bool dvalid = (d0 + c) < D;
         float *hp = h + ((bi * L + t0 + r0) * D + d0 + c);
 #pragma unroll
@@ -267,17 +353,6 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
             }
         }
         __syncthreads();                      // stage st and the scratch arrays are free again
-
-        if (tid == 0) {
-            long long nid = n_tiles;
-            if (!sm.ended && ld_relaxed_u32(&ctrl->abort) != 0) sm.ended = 1;
-            if (!sm.ended) {
-                nid = grab();
-                if (nid >= n_tiles) { sm.ended = 1; nid = n_tiles; }
-            }
-            sm.tile_id[st] = nid;
-            if (nid < n_tiles) issue(st, nid);
-        }
     }
 
     // The last CTA to finish resets the counters and advances the epoch for the next launch.
