@@ -131,6 +131,45 @@ linrec_status_t linrec_stream_status(void *stream);
  */
 linrec_status_t linrec_copy_f32(const float *src, float *dst, int64_t n, void *stream);
 
+/*
+ * linrec_scan_f32_noalloc -- the chunked look-back scan for callers that must
+ * not allocate device memory.  The pages this library follows have no
+ * counterpart to it.  Callers it is for: code that enqueues work while a CUDA
+ * graph is being captured or from a real-time loop, where an allocation can
+ * stall on a device-wide synchronisation; plug-ins whose host application owns
+ * all device memory through its own allocator and forbids other allocations;
+ * services that must keep a fixed, known memory footprint.
+ *
+ * Same operation, pointer and size rules as linrec_scan_f32, and also:
+ *  - a, b and h must be 16-byte aligned and D % 4 == 0 (the chunked kernel's
+ *    tensor copies need it); otherwise LINREC_ERR_INVALID_VALUE.
+ *  - The look-back scratch is one fixed array of LINREC_NOALLOC_SCRATCH_BYTES
+ *    (16 MiB) compiled into the library; every GPU that loads the library
+ *    holds it until the process exits.  The scratch a problem needs is about
+ *    24 * B * D * L / tile_t bytes (tile_t = 64 when D >= 128, else 128):
+ *    (32, 4096, 256) and (1, 1048576, 64) fit.  A problem that needs more
+ *    returns LINREC_ERR_WORKSPACE without launching anything.
+ *  - It calls no allocation routine: no cudaMalloc, cudaMallocAsync or
+ *    cudaFree, and nothing that calls them.
+ *  - The first call on each device looks up the array's device address and
+ *    the kernel's occupancy (once per device); make that first call before
+ *    any stream capture.
+ *  - Every call uses the same array, which keeps what the last call left.
+ *    Each call clears the array's tile counters (a 12-byte and a 4-byte
+ *    cudaMemsetAsync on `stream`) and tags its look-back words with a
+ *    per-call epoch, so words left by earlier calls are never mistaken for
+ *    its own.  Calls that overlap on the GPU (on different streams, or
+ *    graph launches in flight together) race on the array and return wrong
+ *    results: run them one after another.
+ *  - d_status (may be NULL): a device word the kernel ORs
+ *    1 << LINREC_ERR_LOOKBACK_TIMEOUT or 1 << LINREC_ERR_TMA_TIMEOUT into if
+ *    a bounded wait runs out; the output then holds NaN where the carry was lost.
+ */
+#define LINREC_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+linrec_status_t linrec_scan_f32_noalloc(const float *a, const float *b, float *h,
+                                        int64_t B, int64_t L, int64_t D, void *stream,
+                                        unsigned int *d_status);
+
 /* Human-readable name of a status code (static storage). */
 const char *linrec_status_string(linrec_status_t status);
 

@@ -1,0 +1,181 @@
+// noalloc.cu -- linrec_scan_f32_noalloc: the chunked look-back scan with its
+// scratch in a fixed array compiled into the library, for callers that may
+// not allocate device memory (see include/linrec.h for who they are).
+//
+// Nothing here allocates: no cudaMalloc / cudaMallocAsync / cudaFree, and no
+// library routine that does.  The array below is a static __device__ object:
+// each device that loads the library holds it until the process exits.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "kernels.cuh"
+#include "linrec.h"
+
+using namespace linrec;
+
+namespace {
+
+// [Control block, padded to 256 bytes][look-back words].  Zero at load time.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[LINREC_NOALLOC_SCRATCH_BYTES];
+
+constexpr size_t kHead = 256;
+constexpr int kMaxDevices = 64;
+constexpr int64_t kSpinLimit = 1 << 20;
+
+struct DeviceSetup {
+    bool ready = false;
+    bool supported = false;
+    int sm_count = 0;
+    unsigned char *scratch = nullptr;   // device address of g_noalloc_scratch on this device
+    int ctas_per_sm[64] = {};
+};
+
+std::mutex g_mu;
+DeviceSetup g_setup[kMaxDevices];
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+// Once per device, with that device current: its facts and the array's device address.
+// In host code g_noalloc_scratch names a host-side stand-in, never the device memory.
+bool setup_device(int dev, DeviceSetup *&out) {
+    DeviceSetup &s = g_setup[dev];
+    if (!s.ready) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+        s.supported = (major == 10 && minor == 3);
+        s.sm_count = sms;
+        if (s.supported) {
+            void *ptr = nullptr;
+            if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
+                cudaGetLastError();
+                return false;
+            }
+            s.scratch = static_cast<unsigned char *>(ptr);
+        }
+        s.ready = true;
+    }
+    out = &s;
+    return true;
+}
+
+bool encode(CUtensorMap *map, const float *base, int64_t B, int64_t L, int64_t D, int tile_d, int tile_t) {
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)L, (cuuint64_t)B};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 4u, (cuuint64_t)L * (cuuint64_t)D * 4u};
+    const cuuint32_t box[3] = {(cuuint32_t)tile_d, (cuuint32_t)tile_t, 1u};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool overlap(const void *x, const void *y, int64_t bytes) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(x), b0 = reinterpret_cast<uintptr_t>(y);
+    return a0 < b0 + (uintptr_t)bytes && b0 < a0 + (uintptr_t)bytes;
+}
+
+}  // namespace
+
+extern "C" linrec_status_t linrec_scan_f32_noalloc(const float *a, const float *b, float *h, int64_t B, int64_t L,
+                                                   int64_t D, void *stream_ptr, unsigned int *d_status) {
+    if (B < 0 || L < 0 || D < 0) return LINREC_ERR_INVALID_VALUE;
+    if (B == 0 || L == 0 || D == 0) return LINREC_OK;
+    const int64_t lim = INT64_MAX / 16;
+    if (L > lim / D || B > lim / (L * D)) return LINREC_ERR_INVALID_VALUE;
+    const int64_t n = B * L * D;
+    if (!a || !b || !h) return LINREC_ERR_INVALID_VALUE;
+    if (overlap(h, a, n * 4) || overlap(h, b, n * 4)) return LINREC_ERR_ALIAS;
+    const uintptr_t al = reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(b) |
+                         reinterpret_cast<uintptr_t>(h);
+    if ((al & 15u) != 0 || D % 4 != 0) return LINREC_ERR_INVALID_VALUE;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return LINREC_ERR_LAUNCH;
+    }
+    if (dev < 0 || dev >= kMaxDevices) return LINREC_ERR_LAUNCH;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceSetup *ds = nullptr;
+    if (!setup_device(dev, ds)) return LINREC_ERR_LAUNCH;
+    if (!ds->supported) return LINREC_ERR_UNSUPPORTED_DEVICE;
+
+    // The dispatcher's chunked tile for this shape, then the resident CTAs of that variant.
+    linrec_options_t opt = {};
+    opt.path = LINREC_PATH_CHUNKED;
+    linrec_plan_t plan;
+    linrec_status_t st = linrec_plan_f32(B, L, D, ds->sm_count, 16, 0, &opt, &plan);
+    if (st != LINREC_OK) return st;
+    if (plan.workspace_bytes > LINREC_NOALLOC_SCRATCH_BYTES) return LINREC_ERR_WORKSPACE;
+    int nvar = 0;
+    const ChunkedVariant *vars = chunked_variants(&nvar);
+    int vi = -1;
+    for (int i = 0; i < nvar && i < 64; ++i)
+        if (vars[i].tile_d == plan.tile_d && vars[i].tile_t == plan.tile_t && vars[i].stages == plan.stages) vi = i;
+    if (vi < 0) return LINREC_ERR_INVALID_VALUE;
+    if (ds->ctas_per_sm[vi] == 0) {
+        int c = 0;
+        if (chunked_ctas_per_sm(&vars[vi], &c) != cudaSuccess || c <= 0) {
+            cudaGetLastError();
+            return LINREC_ERR_LAUNCH;
+        }
+        ds->ctas_per_sm[vi] = c;
+    }
+    st = linrec_plan_f32(B, L, D, ds->sm_count, 16, ds->ctas_per_sm[vi], &opt, &plan);
+    if (st != LINREC_OK) return st;
+
+    if (!g_encode) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) {
+            cudaGetLastError();
+            return LINREC_ERR_LAUNCH;
+        }
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    ChunkedLaunch p;
+    p.variant = &vars[vi];
+    if (!encode(&p.map_a, a, B, L, D, plan.tile_d, plan.tile_t) ||
+        !encode(&p.map_b, b, B, L, D, plan.tile_d, plan.tile_t))
+        return LINREC_ERR_LAUNCH;
+
+    Control *ctrl = reinterpret_cast<Control *>(ds->scratch);
+    // The tile counter and the done count must start at zero.  The kernel's last
+    // CTA leaves them so, but a call that never finished would not have: clear
+    // them here (no allocation).  The epoch word is kept: it tells this call's
+    // look-back words from those the previous calls left in the array.
+    if (cudaMemsetAsync(ctrl, 0, offsetof(Control, epoch), stream) != cudaSuccess ||
+        cudaMemsetAsync(&ctrl->abort, 0, sizeof(ctrl->abort), stream) != cudaSuccess) {
+        cudaGetLastError();
+        return LINREC_ERR_LAUNCH;
+    }
+    p.h = h;
+    p.L = L;
+    p.D = D;
+    p.slices_per_batch = (D + plan.tile_d - 1) / plan.tile_d;
+    p.n_slices = B * p.slices_per_batch;
+    p.chunks = plan.chunks;
+    p.n_tiles = plan.n_tiles;
+    p.grid = plan.grid;
+    p.ctrl = ctrl;
+    p.words = reinterpret_cast<unsigned long long *>(ds->scratch + kHead);
+    p.status = d_status ? d_status : &ctrl->status;
+    p.spin_limit = kSpinLimit;
+    p.silent_tile = -1;
+    if (launch_chunked(p, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return LINREC_ERR_LAUNCH;
+    }
+    return LINREC_OK;
+}
