@@ -79,6 +79,9 @@ typedef struct {
     int tile_d;          /* chunked: channels per tile */
     int stages;          /* chunked: tiles in flight per CTA (shared-memory ring depth) */
     int ctas_per_sm;     /* chunked: cap on resident CTAs per SM (0 = as many as fit) */
+    int chunk_mode;      /* chunked: 1 = each CTA owns whole channel slices and carries h from
+                            chunk to chunk itself; 2 = chunks of a slice spread over CTAs, joined
+                            by the decoupled look-back; 0 = the dispatcher's choice */
     unsigned int *d_status; /* device word (may be NULL): the kernel ORs 1 << linrec_status_t
                                into it on a device-side failure; otherwise the stream's own word
                                is used (read it with linrec_stream_status) */
@@ -97,12 +100,13 @@ typedef struct {
     int path;              /* LINREC_PATH_REGCARRY or LINREC_PATH_CHUNKED */
     int vec, prefetch;     /* regcarry parameters */
     int tile_t, tile_d, segments, stages; /* chunked parameters */
+    int lookback;          /* chunked: 1 = look-back mode, 0 = slice-owner mode */
     int threads;           /* threads per CTA */
     int64_t grid;          /* CTAs launched */
     int64_t n_tiles;       /* chunked: tiles of tile_t x tile_d */
     int64_t chunks;        /* chunked: time chunks per channel slice */
     size_t smem_bytes;     /* dynamic shared memory per CTA */
-    size_t workspace_bytes;/* chunked: look-back words for this call */
+    size_t workspace_bytes;/* chunked: control block + look-back words for this call */
 } linrec_plan_t;
 
 /*
@@ -143,12 +147,14 @@ linrec_status_t linrec_copy_f32(const float *src, float *dst, int64_t n, void *s
  * Same operation, pointer and size rules as linrec_scan_f32, and also:
  *  - a, b and h must be 16-byte aligned and D % 4 == 0 (the chunked kernel's
  *    tensor copies need it); otherwise LINREC_ERR_INVALID_VALUE.
- *  - The look-back scratch is one fixed array of LINREC_NOALLOC_SCRATCH_BYTES
- *    (16 MiB) compiled into the library; every GPU that loads the library
- *    holds it until the process exits.  The scratch a problem needs is about
- *    24 * B * D * L / tile_t bytes (tile_t = 64 when D >= 128, else 128):
- *    (32, 4096, 256) and (1, 1048576, 64) fit.  A problem that needs more
- *    returns LINREC_ERR_WORKSPACE without launching anything.
+ *  - The scratch is one fixed array of LINREC_NOALLOC_SCRATCH_BYTES (16 MiB)
+ *    compiled into the library; every GPU that loads the library holds it
+ *    until the process exits.  Shapes with at least as many 32-channel
+ *    slices (B * ceil(D/32)) as the GPU has SMs need only its 256-byte
+ *    control block.  Fewer, longer slices use the look-back words, about
+ *    24 * B * D * L / 128 bytes: (1, 1048576, 64) fits, (1, 2^24, 64) does
+ *    not.  A problem that needs more returns LINREC_ERR_WORKSPACE without
+ *    launching anything.
  *  - It calls no allocation routine: no cudaMalloc, cudaMallocAsync or
  *    cudaFree, and nothing that calls them.
  *  - The first call on each device looks up the array's device address and

@@ -54,6 +54,7 @@ class Options(ctypes.Structure):
         ("tile_d", ctypes.c_int),
         ("stages", ctypes.c_int),
         ("ctas_per_sm", ctypes.c_int),
+        ("chunk_mode", ctypes.c_int),
         ("d_status", ctypes.c_void_p),
         ("spin_limit", ctypes.c_int64),
         ("test_silent_tile", ctypes.c_int64),
@@ -69,6 +70,7 @@ class Plan(ctypes.Structure):
         ("tile_d", ctypes.c_int),
         ("segments", ctypes.c_int),
         ("stages", ctypes.c_int),
+        ("lookback", ctypes.c_int),
         ("threads", ctypes.c_int),
         ("grid", ctypes.c_int64),
         ("n_tiles", ctypes.c_int64),
@@ -120,12 +122,16 @@ def _check(code: int, what: str):
         raise LinrecError(code, f"{what}: {linrec_status_string(code)}")
 
 
+CHUNK_MODES = {"auto": 0, "own": 1, "lookback": 2}
+
+
 def make_options(path="auto", vec=0, prefetch=0, tile_t=0, tile_d=0, stages=0, ctas_per_sm=0,
-                 d_status=None, spin_limit=0, test_silent_tile=0) -> Options:
+                 chunk_mode="auto", d_status=None, spin_limit=0, test_silent_tile=0) -> Options:
     o = Options()
     o.path = PATHS[path] if isinstance(path, str) else int(path)
     o.vec, o.prefetch, o.tile_t, o.tile_d, o.stages = int(vec), int(prefetch), int(tile_t), int(tile_d), int(stages)
     o.ctas_per_sm = int(ctas_per_sm)
+    o.chunk_mode = CHUNK_MODES[chunk_mode] if isinstance(chunk_mode, str) else int(chunk_mode)
     o.d_status = None if d_status is None else int(d_status.data_ptr() if hasattr(d_status, "data_ptr") else d_status)
     o.spin_limit = int(spin_limit)
     o.test_silent_tile = int(test_silent_tile)

@@ -1,10 +1,10 @@
-// chunked.cu -- the TMA-staged, look-back path of the linear-recurrence scan.
+// chunked.cu -- the TMA-staged chunked path of the linear-recurrence scan.
 //
 // h_0 = b_0, h_t = a_t*h_{t-1} + b_t per channel (POPCORNBENCH "Kimi-K2.6 l1_p9",
 // problem statement).  The (B, L, D) problem is cut into tiles of TT time steps
-// x TD channels of one batch index.  Tile id = chunk * n_slices + slice, so
-// tile ids advance in time for all channel slices together, and the tile
-// before tile i in the same slice is tile i - n_slices.
+// x TD channels of one batch index.  A slice is the TD channels of one batch
+// index over all L; its tiles are its time chunks q = 0 .. chunks-1, and tile
+// id = q * n_slices + slice.
 //
 // Per tile, inside one CTA of TD * S threads:
 //  1. TMA copies the a and b boxes (TT x TD fp32 each) into a shared-memory
@@ -14,19 +14,26 @@
 //     (a2,b2) o (a1,b1) = (a2*a1, a2*b1 + b2) ("Kimi-K2.6 l1_p9", derivation of
 //     the associative operator).  Its a, b values stay in registers.
 //  3. A warp-shuffle scan over the S segment pairs of each channel gives every
-//     segment its exclusive prefix and the tile its aggregate.
-//  4. Decoupled look-back (S lanes per channel, one predecessor per lane):
-//     publish the tile aggregate, walk back over earlier tiles of the same
-//     slice until an inclusive value is found, replay the chain of aggregates
-//     forward from it, publish this tile's inclusive value.  Only the running
-//     value h crosses tile boundaries ("Kimi-K2.6 l1_p9", the running_h
-//     carry): h_out = A_prefix * h_in + B_prefix.
-//  5. Every thread replays its K steps from the carried value and stores h.
+//     segment its exclusive prefix and the tile its aggregate (A_q, B_q).
+//  4. The carry: the h value entering the tile.  Only this running value
+//     crosses tile boundaries ("Kimi-K2.6 l1_p9", the running_h carry).  It is
+//     defined as the chain H_q = A_q * H_{q-1} + B_q over the slice's tiles
+//     (H before the first chunk = 0), which both modes below evaluate with the
+//     same fma sequence, so they return the same bits.
+//       slice-owner mode: a CTA owns whole slices (static round-robin) and
+//         walks their chunks in order; the carry stays in a register.
+//       look-back mode (few slices, long L): tiles of a slice run on different
+//         CTAs; each publishes its aggregate, walks back over earlier tiles of
+//         its slice to the nearest inclusive value (S lanes per channel, a
+//         window of S*R tiles per round trip), replays the chain forward from
+//         it and publishes its own inclusive value.
+//  5. Every thread replays its K steps from h_in = A_prefix * carry + B_prefix
+//     and stores h.
 //
-// Tile ids come from an atomic counter, so every predecessor of a tile was
-// handed to a CTA that is running or done: the look-back cannot wait on a tile
-// that is not yet scheduled.  Every wait is bounded; on expiry the kernel
-// records an error bit in the status word and carries on with NaN.
+// In look-back mode tile ids come from an atomic counter, taken in the order
+// CTAs start on them, so every predecessor of a tile was handed to a CTA that
+// is running or done.  Every wait is bounded; on expiry the kernel records an
+// error bit in the status word and carries on with NaN.
 #include "kernels.cuh"
 #include "ptx.cuh"
 
@@ -37,6 +44,15 @@ namespace {
 constexpr uint32_t kTmaPolls = 1u << 22;   // ~1 s of polls with back-off
 constexpr unsigned kFull = 0xffffffffu;
 
+// Where a ring stage's tile sits: decoded once by the thread that loads it.
+struct TileCoord {
+    long long id;                       // tile id (>= n_tiles: no tile, the CTA is done)
+    int q;                              // time chunk
+    int bi;                             // batch index
+    int d0;                             // first channel
+    int pad;
+};
+
 template <int TD, int TT, int S, int ST>
 struct __align__(128) ChunkSmem {
     float a[ST][TT * TD];
@@ -44,29 +60,19 @@ struct __align__(128) ChunkSmem {
     float segA[S][TD], segB[S][TD];     // per-segment pairs, then their exclusive prefixes
     float carry[TD];                    // h entering the tile, per channel
     uint64_t full[ST];                  // one mbarrier per ring stage
-    long long tile_id[ST];              // tile loaded into each stage (>= n_tiles: none)
+    TileCoord tile[ST];                 // tile loaded into each stage
     uint32_t tag;                       // look-back tag of this launch
 };
 
-__device__ __forceinline__ void decode_tile(long long id, long long n_slices, long long slices_per_batch,
-                                            long long &q, long long &bi, long long &d0, int td) {
-    q = id / n_slices;
-    const long long p = id - q * n_slices;
-    bi = p / slices_per_batch;
-    d0 = (p - bi * slices_per_batch) * td;
-}
-
-// The h value entering tile `id` for channel cc, computed by the CTA's threads in
-// groups of S lanes per channel (lane ss of the group watches one predecessor).
-//
-// The inclusive value of a tile is defined as the chain H_i = A_i * H_{i-1} + B_i
-// (one fma per tile, H before the first chunk = 0).  The group reads a window of
-// S predecessors per round trip, walks back over windows that hold only
-// aggregates until it meets an inclusive value, and then replays the chain
-// forward from it, re-reading the aggregates it passed.  The result is the same
-// bits whichever predecessors happened to have finished: the carry is
-// deterministic.
-template <int S>
+// Look-back mode: the h value entering tile `id` for channel cc, computed by
+// groups of S lanes per channel.  Lane ss watches R predecessors: window
+// position p = r*S + ss is tile id - (1 + p) * n_slices, so one round trip
+// covers W = S*R earlier tiles of the slice.  Each round reads the inclusive
+// words of the window first and the aggregate words only of the positions
+// between this tile and the nearest inclusive value.  The group walks back
+// over windows that hold aggregates only, then replays the chain forward
+// from the inclusive value it found, re-reading the aggregates it passed.
+template <int S, int R>
 __device__ __forceinline__ float lookback_carry(
     const long long id, const long long n_slices, const int TD, const int cc, const int ss, const int gbase,
     const uint32_t tag, const bool publish_agg, const float tA, const float tB,
@@ -74,58 +80,78 @@ __device__ __forceinline__ float lookback_carry(
     const unsigned long long *__restrict__ wInc, Control *__restrict__ ctrl, unsigned int *__restrict__ status,
     const long long spin_limit)
 {
+    constexpr int W = S * R;
+    static_assert(W <= 32, "window fits a 32-bit mask");
     constexpr unsigned GM = (S == 32) ? kFull : ((1u << S) - 1u);
     const long long me = id * TD + cc;
+    // Successors may need this tile's aggregate before its carry is known.
+    if (publish_agg && ss == 0) {
+        st_relaxed_u64(&wAggA[me], pack_word(tag, tA));
+        st_relaxed_u64(&wAggB[me], pack_word(tag, tB));
+    }
     long long base = id - n_slices;           // tile at window position 0: the predecessor
     int skipped = 0;                          // windows holding aggregates only
     int pstar = -1;                           // window position of the nearest inclusive value
     bool failed = false;
-    float vA = 1.0f, vB = 0.0f, vH = 0.0f;    // what this lane read for its tile
+    float vA[R], vB[R], vH[R];                // what this lane read for its R tiles
+    bool have[R];                             // aggregate of that tile already read
+#pragma unroll
+    for (int r = 0; r < R; ++r) { vA[r] = 1.0f; vB[r] = 0.0f; vH[r] = 0.0f; have[r] = false; }
     long long idle = 0;
     unsigned int nap = 32;
-    for (int round = 0;; ++round) {
+    for (;;) {
         const bool active = pstar < 0 && !failed;
-        int kind = 2;                         // 0: nothing yet, 1: aggregate, 2: inclusive
-        if (active) {
-            const long long j = base - (long long)ss * n_slices;
-            if (j < 0) {
-                vH = 0.0f;                    // before the first chunk: h = 0
-            } else {
-                const unsigned long long wi = ld_relaxed_u64(&wInc[j * TD + cc]);
-                if (word_tag(wi) == tag) {
-                    vH = word_val(wi);
+        // inclusive words of the window
+        unsigned inc_g = 0;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            bool inc = false;
+            if (active) {
+                const long long j = base - (long long)(r * S + ss) * n_slices;
+                if (j < 0) {
+                    inc = true;
+                    vH[r] = 0.0f;             // before the first chunk: h = 0
                 } else {
-                    const unsigned long long wa = ld_relaxed_u64(&wAggA[j * TD + cc]);
-                    const unsigned long long wb = ld_relaxed_u64(&wAggB[j * TD + cc]);
-                    if (word_tag(wa) == tag && word_tag(wb) == tag) {
-                        kind = 1;
-                        vA = word_val(wa);
-                        vB = word_val(wb);
-                    } else {
-                        kind = 0;
-                    }
+                    const unsigned long long wi = ld_relaxed_u64(&wInc[j * TD + cc]);
+                    inc = word_tag(wi) == tag;
+                    vH[r] = word_val(wi);
                 }
             }
+            inc_g |= ((__ballot_sync(kFull, active && inc) >> gbase) & GM) << (r * S);
         }
-        const unsigned inc_g = (__ballot_sync(kFull, active && kind == 2) >> gbase) & GM;
-        const unsigned none_g = (__ballot_sync(kFull, active && kind == 0) >> gbase) & GM;
+        const int pc = inc_g ? __ffs(inc_g) - 1 : W;   // nearest inclusive position (W: none)
+        // aggregate words of the positions before it
+        unsigned none_g = 0;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int p = r * S + ss;
+            bool missing = false;
+            if (active && p < pc && !have[r]) {
+                const long long j = base - (long long)p * n_slices;
+                const unsigned long long wa = ld_relaxed_u64(&wAggA[j * TD + cc]);
+                const unsigned long long wb = ld_relaxed_u64(&wAggB[j * TD + cc]);
+                if (word_tag(wa) == tag && word_tag(wb) == tag) {
+                    vA[r] = word_val(wa);
+                    vB[r] = word_val(wb);
+                    have[r] = true;
+                } else {
+                    missing = true;
+                }
+            }
+            none_g |= ((__ballot_sync(kFull, missing) >> gbase) & GM) << (r * S);
+        }
         bool progressed = false;
         if (active) {
-            if (inc_g) {
-                const int p = __ffs(inc_g) - 1;
-                if ((none_g & ((1u << p) - 1u)) == 0) {
-                    pstar = p;
-                    progressed = true;
+            if (none_g == 0) {
+                if (pc < W) {
+                    pstar = pc;
+                } else {
+                    ++skipped;
+                    base -= (long long)W * n_slices;
+#pragma unroll
+                    for (int r = 0; r < R; ++r) have[r] = false;
                 }
-            } else if (none_g == 0) {
-                ++skipped;
-                base -= (long long)S * n_slices;
                 progressed = true;
-            }
-            // Successors may need this tile's aggregate unless its carry is known at once.
-            if (round == 0 && publish_agg && ss == 0 && pstar != 0) {
-                st_relaxed_u64(&wAggA[me], pack_word(tag, tA));
-                st_relaxed_u64(&wAggB[me], pack_word(tag, tB));
             }
             if (progressed) {
                 idle = 0;
@@ -143,27 +169,35 @@ __device__ __forceinline__ float lookback_carry(
         }
     }
 
-    // Replay the chain forward from the inclusive value: the rest of its window, then
-    // every skipped window, nearest to this tile last.
-    float H = __shfl_sync(kFull, vH, pstar < 0 ? 0 : pstar, S);
+    // Replay the chain forward from the inclusive value: the rest of its window,
+    // then every skipped window, the one nearest to this tile last.
+    const int pf = pstar < 0 ? 0 : pstar;
+    float mine_h = vH[0];
 #pragma unroll
-    for (int p = S - 1; p >= 0; --p) {
-        const float ap = __shfl_sync(kFull, vA, p, S);
-        const float bp = __shfl_sync(kFull, vB, p, S);
+    for (int r = 1; r < R; ++r)
+        if (pf / S == r) mine_h = vH[r];
+    float H = __shfl_sync(kFull, mine_h, pf % S, S);
+#pragma unroll
+    for (int p = W - 1; p >= 0; --p) {
+        const float ap = __shfl_sync(kFull, vA[p / S], p % S, S);
+        const float bp = __shfl_sync(kFull, vB[p / S], p % S, S);
         if (p < pstar) H = fmaf(ap, H, bp);
     }
     const int most = __reduce_max_sync(kFull, failed ? 0 : skipped);
     for (int w = most - 1; w >= 0; --w) {
         const bool mine = !failed && w < skipped;
         if (mine) {
-            const long long j = id - n_slices - ((long long)w * S + ss) * n_slices;
-            vA = word_val(ld_relaxed_u64(&wAggA[j * TD + cc]));
-            vB = word_val(ld_relaxed_u64(&wAggB[j * TD + cc]));
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const long long j = id - n_slices - ((long long)w * W + r * S + ss) * n_slices;
+                vA[r] = word_val(ld_relaxed_u64(&wAggA[j * TD + cc]));
+                vB[r] = word_val(ld_relaxed_u64(&wAggB[j * TD + cc]));
+            }
         }
 #pragma unroll
-        for (int p = S - 1; p >= 0; --p) {
-            const float ap = __shfl_sync(kFull, vA, p, S);
-            const float bp = __shfl_sync(kFull, vB, p, S);
+        for (int p = W - 1; p >= 0; --p) {
+            const float ap = __shfl_sync(kFull, vA[p / S], p % S, S);
+            const float bp = __shfl_sync(kFull, vB[p / S], p % S, S);
             if (mine) H = fmaf(ap, H, bp);
         }
     }
@@ -178,11 +212,13 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
                     const long long L, const long long D,
                     const long long slices_per_batch, const long long n_slices,
                     const long long chunks, const long long n_tiles,
+                    const int own,               // 1: slice-owner mode, 0: look-back mode
                     Control *__restrict__ ctrl, unsigned long long *__restrict__ words,
                     unsigned int *__restrict__ status,
                     const long long spin_limit, const long long silent_tile)
 {
     constexpr int K = TT / S;                 // time steps per thread
+    constexpr int R = (S >= 4) ? 16 / S : 4;  // look-back: predecessors per lane
     constexpr uint32_t kStageBytes = 2u * TT * TD * sizeof(float);
     static_assert(TT % S == 0 && TD % 32 == 0 && (32 % S) == 0 && S >= 2 && ST >= 2, "tile shape");
     using Smem = ChunkSmem<TD, TT, S, ST>;
@@ -200,15 +236,33 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
     unsigned long long *const wAggB = words + n_tiles * TD;
     unsigned long long *const wInc = words + 2 * n_tiles * TD;
 
-    auto issue = [&](int st, long long id) {
-        long long q, bi, d0;
-        decode_tile(id, n_slices, slices_per_batch, q, bi, d0, TD);
+    // (thread 0) record stage st's tile and start its two box copies.
+    auto issue = [&](int st, long long id, long long q, long long slice) {
+        const long long bi = slice / slices_per_batch;
+        const int d0 = (int)((slice - bi * slices_per_batch) * TD);
+        sm.tile[st] = TileCoord{id, (int)q, (int)bi, d0, 0};
         mbar_arrive_expect_tx(&sm.full[st], kStageBytes);
-        tma_load_3d(sm.a[st], &map_a, &sm.full[st], (int)d0, (int)(q * TT), (int)bi);
-        tma_load_3d(sm.b[st], &map_b, &sm.full[st], (int)d0, (int)(q * TT), (int)bi);
+        tma_load_3d(sm.a[st], &map_a, &sm.full[st], d0, (int)(q * TT), (int)bi);
+        tma_load_3d(sm.b[st], &map_b, &sm.full[st], d0, (int)(q * TT), (int)bi);
     };
-    auto grab = [&]() -> long long {
-        return (long long)atomicAdd(&ctrl->tile_counter, 1ull);
+    auto finish = [&](int st) { sm.tile[st] = TileCoord{n_tiles, 0, 0, 0, 0}; };
+    // (thread 0) the CTA's next tile.  Slice-owner mode: slices blockIdx.x,
+    // blockIdx.x + gridDim.x, ... each walked from chunk 0 to chunks-1, tracked
+    // in (own_slice, own_q).  Look-back mode: the next id from the tile counter.
+    long long own_slice = blockIdx.x, own_q = 0;
+    auto next_tile = [&](long long &q, long long &slice) -> long long {
+        if (own) {
+            if (own_slice >= n_slices) return n_tiles;
+            q = own_q;
+            slice = own_slice;
+            if (++own_q == chunks) { own_q = 0; own_slice += gridDim.x; }
+            return q * n_slices + slice;
+        }
+        const long long id = (long long)atomicAdd(&ctrl->tile_counter, 1ull);
+        if (id >= n_tiles) return n_tiles;
+        q = id / n_slices;
+        slice = id - q * n_slices;
+        return id;
     };
 
     // TMA writes whole boxes at 128-byte aligned shared addresses; the layout
@@ -218,70 +272,76 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
         long long first = n_tiles;
         if (misaligned) {
             atomicOr(status, kStatusTmaTimeout);
-            atomicExch(&ctrl->abort, 1u);
+            if (!own) atomicExch(&ctrl->abort, 1u);
         } else {
             for (int st = 0; st < ST; ++st) mbar_init(&sm.full[st], 1);
             mbar_fence_init();
             tmap_prefetch(&map_a);
             tmap_prefetch(&map_b);
-            const uint32_t tag = ld_relaxed_u32(&ctrl->epoch) + 1u;
-            sm.tag = tag == 0 ? 1u : tag;
-            // One tile at launch: tiles are taken in the order CTAs start on them, so a
-            // tile's predecessors are never parked in another CTA's ring behind later work.
-            first = grab();
-            if (first >= n_tiles) first = n_tiles;
-            else issue(0, first);
+            if (!own) {
+                const uint32_t tag = ld_relaxed_u32(&ctrl->epoch) + 1u;
+                sm.tag = tag == 0 ? 1u : tag;
+            }
+            // One tile at launch: in look-back mode tiles are then taken in the order
+            // CTAs start on them, so a tile's predecessors are never parked in another
+            // CTA's ring behind later work.
+            long long q = 0, slice = 0;
+            first = next_tile(q, slice);
+            if (first < n_tiles) issue(0, first, q, slice);
         }
-        sm.tile_id[0] = first;
+        if (first >= n_tiles) finish(0);
     }
     __syncthreads();
 
-    const uint32_t tag = sm.tag;
+    const uint32_t tag = own ? 0u : sm.tag;
     uint32_t phases = 0;                      // bit st: parity of the next completion of stage st
     long long next_fill = 1;                  // (thread 0) next ring slot to fill
-    bool ended = sm.tile_id[0] >= n_tiles;    // (thread 0) no more tiles to take
-    long long ahead = -1;                     // (thread 0) tile id taken one iteration early
-    uint32_t abort_seen = 0;                  // (thread 0) abort word, read one iteration early
+    bool ended = sm.tile[0].id >= n_tiles;    // (thread 0) no more tiles to take
+    long long ahead = -1, ahead_q = 0, ahead_slice = 0;   // (thread 0, look-back) tile taken early
+    uint32_t abort_seen = 0;                  // (thread 0, look-back) abort word, read one iteration early
+    float run = 0.0f;                         // (slice-owner, ss == 0) inclusive value of the last tile
 
     for (long long k = 0;; ++k) {
         const int st = (int)(k % ST);
-        const long long id = sm.tile_id[st];
+        const TileCoord tc = sm.tile[st];
+        const long long id = tc.id;
         if (id >= n_tiles) break;
 
         if (!mbar_wait_bounded(&sm.full[st], (phases >> st) & 1u, kTmaPolls)) {
             atomicOr(status, kStatusTmaTimeout);
-            atomicExch(&ctrl->abort, 1u);
+            if (!own) atomicExch(&ctrl->abort, 1u);
         }
         phases ^= 1u << st;
 
         // Keep ST-1 tiles in flight behind this one.  The slot filled last
         // (k + ST - 1) reuses the stage freed at the end of iteration k - 1.
-        // The next tile id is taken one iteration ahead, so the atomic's round
-        // trip overlaps this tile's work instead of delaying it.
+        // In look-back mode the next tile id is taken one iteration ahead, so the
+        // atomic's round trip overlaps this tile's work instead of delaying it.
         if (tid == 0) {
             if (!ended && abort_seen != 0) {
                 ended = true;
-                sm.tile_id[next_fill % ST] = n_tiles;
+                finish((int)(next_fill % ST));
             }
             while (!ended && next_fill < k + ST) {
                 const int s2 = (int)(next_fill % ST);
-                const long long nid = ahead >= 0 ? ahead : grab();
+                long long nq = ahead_q, nslice = ahead_slice;
+                const long long nid = ahead >= 0 ? ahead : next_tile(nq, nslice);
                 ahead = -1;
                 if (nid >= n_tiles) {
                     ended = true;
-                    sm.tile_id[s2] = n_tiles;
+                    finish(s2);
                 } else {
-                    sm.tile_id[s2] = nid;
-                    issue(s2, nid);
+                    issue(s2, nid, nq, nslice);
                 }
                 ++next_fill;
             }
-            if (!ended && ahead < 0) ahead = grab();
-            abort_seen = ld_relaxed_u32(&ctrl->abort);
+            if (!own) {
+                if (!ended && ahead < 0) ahead = next_tile(ahead_q, ahead_slice);
+                abort_seen = ld_relaxed_u32(&ctrl->abort);
+            }
         }
 
-        long long q, bi, d0;
-        decode_tile(id, n_slices, slices_per_batch, q, bi, d0, TD);
+        const long long q = tc.q, bi = tc.bi, d0 = tc.d0;
         const long long t0 = q * TT;
         const int r0 = s * K;
         const long long rem = L - (t0 + r0);
@@ -329,44 +389,64 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
         const float tA = __shfl_sync(kFull, xA, S - 1, S);   // the tile's aggregate
         const float tB = __shfl_sync(kFull, xB, S - 1, S);
 
-        // ---- 4. carry from earlier tiles of the slice ----------------------------
-        const bool publish = (q + 1 < chunks) && (id != silent_tile);
-        float carry = 0.0f;
-        if (q > 0)
-            carry = lookback_carry<S>(id, n_slices, TD, cc, ss, gbase, tag, publish, tA, tB,
-                                      wAggA, wAggB, wInc, ctrl, status, spin_limit);
-        if (ss == 0) {
-            if (publish) st_relaxed_u64(&wInc[id * TD + cc], pack_word(tag, fmaf(tA, carry, tB)));
-            sm.carry[cc] = carry;
+        // ---- 4. the carry entering the tile ---------------------------------------
+        if (own) {
+            if (ss == 0) {
+                const float carry = (q == 0) ? 0.0f : run;
+                run = fmaf(tA, carry, tB);
+                sm.carry[cc] = carry;
+            }
+        } else {
+            const bool publish = (q + 1 < chunks) && (id != silent_tile);
+            float carry = 0.0f;
+            if (q > 0)
+                carry = lookback_carry<S, R>(id, n_slices, TD, cc, ss, gbase, tag, publish, tA, tB,
+                                             wAggA, wAggB, wInc, ctrl, status, spin_limit);
+            if (ss == 0) {
+                if (publish) st_relaxed_u64(&wInc[id * TD + cc], pack_word(tag, fmaf(tA, carry, tB)));
+                sm.carry[cc] = carry;
+            }
         }
         __syncthreads();
 
         // ---- 5. replay the steps from the carried value, store h -----------------
         float hc = fmaf(sm.segA[s][c], sm.carry[c], sm.segB[s][c]);
-        const bool dvalid = (d0 + c) < D;
-        float *hp = h + ((bi * L + t0 + r0) * D + d0 + c);
+        if ((d0 + c) < D) {
+            float *hp = h + ((bi * L + t0 + r0) * D + d0 + c);
+            if (nv == K) {
 #pragma unroll
-        for (int j = 0; j < K; ++j) {
-            if (j < nv) {
-                hc = fmaf(ra[j], hc, rb[j]);
-                if (dvalid) hp[(long long)j * D] = hc;
+                for (int j = 0; j < K; ++j) {
+                    hc = fmaf(ra[j], hc, rb[j]);
+                    hp[(long long)j * D] = hc;
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < K; ++j) {
+                    if (j < nv) {
+                        hc = fmaf(ra[j], hc, rb[j]);
+                        hp[(long long)j * D] = hc;
+                    }
+                }
             }
         }
         __syncthreads();                      // stage st and the scratch arrays are free again
     }
 
-    // The last CTA to finish resets the counters and advances the epoch for the next launch.
-    __syncthreads();
-    if (tid == 0) {
-        __threadfence();
-        const unsigned int prev = atomicAdd(&ctrl->done, 1u);
-        if (prev == gridDim.x - 1) {
+    // Look-back mode: the last CTA to finish resets the counters and advances the
+    // epoch for the next launch on this workspace.
+    if (!own) {
+        __syncthreads();
+        if (tid == 0) {
             __threadfence();
-            atomicExch(&ctrl->tile_counter, 0ull);
-            atomicExch(&ctrl->done, 0u);
-            atomicExch(&ctrl->abort, 0u);
-            atomicAdd(&ctrl->epoch, 1u);
-            __threadfence();
+            const unsigned int prev = atomicAdd(&ctrl->done, 1u);
+            if (prev == gridDim.x - 1) {
+                __threadfence();
+                atomicExch(&ctrl->tile_counter, 0ull);
+                atomicExch(&ctrl->done, 0u);
+                atomicExch(&ctrl->abort, 0u);
+                atomicAdd(&ctrl->epoch, 1u);
+                __threadfence();
+            }
         }
     }
 }
@@ -385,7 +465,10 @@ constexpr ChunkedVariant make_variant() {
     X(64, 64, 4, 2)                \
     X(64, 64, 4, 3)                \
     X(32, 128, 8, 2)               \
-    X(32, 64, 4, 3)
+    X(32, 128, 8, 3)               \
+    X(32, 64, 4, 3)                \
+    X(32, 64, 4, 4)                \
+    X(32, 32, 2, 6)
 
 #define LINREC_V_ENTRY(TD, TT, S, ST) make_variant<TD, TT, S, ST>(),
 const ChunkedVariant kVariants[] = {LINREC_CHUNKED_VARIANTS(LINREC_V_ENTRY)};
@@ -423,11 +506,12 @@ cudaError_t launch_chunked(const ChunkedLaunch &p, cudaStream_t stream) {
     if (err != cudaSuccess) return err;
     long long L = p.L, D = p.D, spb = p.slices_per_batch, ns = p.n_slices, ch = p.chunks, nt = p.n_tiles;
     long long spin = p.spin_limit, silent = p.silent_tile;
+    int own = p.own ? 1 : 0;
     float *h = p.h;
     Control *ctrl = p.ctrl;
     unsigned long long *words = p.words;
     unsigned int *status = p.status;
-    void *args[] = {(void *)&p.map_a, (void *)&p.map_b, &h, &L, &D, &spb, &ns, &ch, &nt,
+    void *args[] = {(void *)&p.map_a, (void *)&p.map_b, &h, &L, &D, &spb, &ns, &ch, &nt, &own,
                     &ctrl, &words, &status, &spin, &silent};
     return cudaLaunchKernel(fn, dim3((unsigned)p.grid), dim3((unsigned)p.variant->threads), args,
                             p.variant->smem_bytes, stream);

@@ -54,8 +54,9 @@ struct ChunkedLaunch {
     int64_t chunks;              // ceil(L / tile_t)
     int64_t n_tiles;             // n_slices * chunks
     int64_t grid;
+    bool own;                    // slice-owner mode (no look-back); else look-back mode
     Control *ctrl;
-    unsigned long long *words;   // 3 * n_tiles * tile_d look-back words
+    unsigned long long *words;   // look-back mode: 3 * n_tiles * tile_d words
     unsigned int *status;        // where device-side failures are recorded
     int64_t spin_limit;
     int64_t silent_tile;         // tile id that publishes nothing (tests), or -1

@@ -82,10 +82,13 @@ const ChunkedVariant *find_variant(int tile_d, int tile_t, int stages, int *inde
     return nullptr;
 }
 
-// Default chunked tile for a channel count D: the widest slice that D fills.
-void default_tile(int64_t D, int *tile_d, int *tile_t) {
-    if (D >= 128) { *tile_d = 128; *tile_t = 64; }
-    else if (D >= 64) { *tile_d = 64; *tile_t = 128; }
+// Default chunked tile.  Slice-owner mode: narrow 32-channel slices (more
+// slices to spread over the SMs) with a 3-deep ring.  Look-back mode: the
+// widest slice D fills, so fewer tiles take part in each carry chain.
+void default_tile(int64_t D, bool own, int *tile_d, int *tile_t, int *stages) {
+    if (own) { *tile_d = 32; *tile_t = 128; *stages = 3; return; }
+    *stages = 2;
+    if (D >= 64) { *tile_d = 64; *tile_t = 128; }
     else { *tile_d = 32; *tile_t = 128; }
 }
 
@@ -116,22 +119,39 @@ linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int ali
         if (!regcarry_supported(vec, prefetch)) return LINREC_ERR_INVALID_VALUE;
         plan->vec = vec;
         plan->prefetch = prefetch;
-        plan->threads = kRegcarryThreads;
+        // Narrower blocks when there are few channel groups, so the grid still
+        // covers every SM (at least two blocks per SM where the groups allow).
         const int64_t groups = B * (D / vec);
-        plan->grid = (groups + kRegcarryThreads - 1) / kRegcarryThreads;
+        int threads = kRegcarryThreads;
+        while (threads > 32 && (groups + threads - 1) / threads < 2 * (int64_t)sm_count) threads /= 2;
+        plan->threads = threads;
+        plan->grid = (groups + threads - 1) / threads;
         return LINREC_OK;
     }
     if (path != LINREC_PATH_CHUNKED || !tma_ok) return LINREC_ERR_INVALID_VALUE;
 
-    int tile_d = opt->tile_d, tile_t = opt->tile_t;
+    // Slice-owner mode when the channel slices alone give every SM work;
+    // otherwise split each slice's chunks over CTAs and join them by look-back.
+    if (opt->chunk_mode < 0 || opt->chunk_mode > 2) return LINREC_ERR_INVALID_VALUE;
+    bool own;
+    if (opt->chunk_mode == 0) {
+        const int td = opt->tile_d ? opt->tile_d : 32;
+        own = B * ((D + td - 1) / td) >= (int64_t)sm_count;
+    } else {
+        own = opt->chunk_mode == 1;
+    }
+    int tile_d = opt->tile_d, tile_t = opt->tile_t, stages = opt->stages;
     if (tile_d == 0 || tile_t == 0) {
-        int dd, dt;
-        default_tile(D, &dd, &dt);
+        int dd, dt, ds;
+        default_tile(D, own, &dd, &dt, &ds);
         if (tile_d == 0) tile_d = dd;
         if (tile_t == 0) tile_t = dt;
+        if (stages == 0) stages = ds;
     }
-    const ChunkedVariant *v = find_variant(tile_d, tile_t, opt->stages, variant_index);
+    const ChunkedVariant *v = find_variant(tile_d, tile_t, stages, variant_index);
+    if (!v && opt->stages == 0) v = find_variant(tile_d, tile_t, 0, variant_index);
     if (!v) return LINREC_ERR_INVALID_VALUE;
+    plan->lookback = own ? 0 : 1;
     plan->tile_d = v->tile_d;
     plan->tile_t = v->tile_t;
     plan->segments = v->segments;
@@ -148,9 +168,11 @@ linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int ali
     }
     if (opt->ctas_per_sm > 0 && opt->ctas_per_sm < per_sm) per_sm = opt->ctas_per_sm;
     int64_t grid = (int64_t)sm_count * per_sm;
-    if (grid > plan->n_tiles) grid = plan->n_tiles;
+    const int64_t units = own ? B * spb : plan->n_tiles;   // slices, or tiles
+    if (grid > units) grid = units;
     plan->grid = grid;
-    plan->workspace_bytes = kWorkspaceHead + (size_t)3 * (size_t)plan->n_tiles * (size_t)v->tile_d * 8u;
+    plan->workspace_bytes = kWorkspaceHead;
+    if (!own) plan->workspace_bytes += (size_t)3 * (size_t)plan->n_tiles * (size_t)v->tile_d * 8u;
     return LINREC_OK;
 }
 
@@ -305,6 +327,7 @@ linrec_status_t linrec_scan_f32_ex(const float *a, const float *b, float *h, int
     p.chunks = plan.chunks;
     p.n_tiles = plan.n_tiles;
     p.grid = plan.grid;
+    p.own = plan.lookback == 0;
     p.ctrl = reinterpret_cast<Control *>(ws->base);
     p.words = reinterpret_cast<unsigned long long *>(ws->base + kWorkspaceHead);
     p.status = opt->d_status ? opt->d_status : &p.ctrl->status;

@@ -168,6 +168,7 @@ extern "C" linrec_status_t linrec_scan_f32_noalloc(const float *a, const float *
     p.chunks = plan.chunks;
     p.n_tiles = plan.n_tiles;
     p.grid = plan.grid;
+    p.own = plan.lookback == 0;
     p.ctrl = ctrl;
     p.words = reinterpret_cast<unsigned long long *>(ds->scratch + kHead);
     p.status = d_status ? d_status : &ctrl->status;

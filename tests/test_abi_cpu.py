@@ -124,13 +124,32 @@ def test_plan_forced_options():
         lr.linrec_plan_f32(32, 4096, 256, path="regcarry", prefetch=5)
 
 
+def _units(p, B, D):
+    # slice-owner mode: one unit per channel slice; look-back mode: one per tile
+    return p["n_tiles"] if p["lookback"] else B * -(-D // p["tile_d"])
+
+
 def test_plan_grid_bounds():
-    # grid never exceeds the tile count nor SMs x resident CTAs
-    for (B, L, D) in [(1, 64, 32), (1, 1 << 20, 64), (32, 4096, 256), (3, 5, 8)]:
+    # grid never exceeds the work units nor SMs x resident CTAs
+    for (B, L, D) in [(1, 64, 32), (1, 1 << 20, 64), (32, 4096, 256), (3, 5, 8), (256, 128, 4096)]:
         p = lr.linrec_plan_f32(B, L, D, path="chunked", sm_count=152, resident_ctas=2)
-        assert 1 <= p["grid"] <= min(p["n_tiles"], 152 * 2)
-    p = lr.linrec_plan_f32(32, 4096, 256, path="chunked", sm_count=152, resident_ctas=3)
-    assert p["grid"] == min(p["n_tiles"], 152 * 3)
-    # the options' cap lowers the resident count
-    p = lr.linrec_plan_f32(32, 4096, 256, path="chunked", sm_count=152, resident_ctas=3, ctas_per_sm=1)
-    assert p["grid"] == min(p["n_tiles"], 152)
+        assert 1 <= p["grid"] <= min(_units(p, B, D), 152 * 2)
+    for mode in ("own", "lookback"):
+        p = lr.linrec_plan_f32(32, 4096, 256, path="chunked", sm_count=152, resident_ctas=3, chunk_mode=mode)
+        assert p["lookback"] == (mode == "lookback")
+        assert p["grid"] == min(_units(p, 32, 256), 152 * 3)
+        # the options' cap lowers the resident count
+        p = lr.linrec_plan_f32(32, 4096, 256, path="chunked", sm_count=152, resident_ctas=3, ctas_per_sm=1,
+                               chunk_mode=mode)
+        assert p["grid"] == min(_units(p, 32, 256), 152)
+
+
+def test_plan_chunk_modes():
+    # many slices: each CTA owns whole slices, no look-back words needed
+    p = lr.linrec_plan_f32(32, 4096, 256, path="chunked", sm_count=152)
+    assert p["lookback"] == 0 and p["workspace_bytes"] == 256
+    # one long slice: look-back mode with words for every tile
+    p = lr.linrec_plan_f32(1, 1 << 20, 64, path="chunked", sm_count=152)
+    assert p["lookback"] == 1 and p["workspace_bytes"] == 256 + 24 * p["n_tiles"] * p["tile_d"]
+    with pytest.raises(lr.LinrecError):
+        lr.linrec_plan_f32(1, 1000, 64, path="chunked", chunk_mode=3)

@@ -36,7 +36,8 @@ def run(a_d, b_d, **opt):
 def legal_paths(B, L, D, aligned=True):
     paths = [{"path": "regcarry"}]
     if aligned and D % 4 == 0:
-        paths.append({"path": "chunked"})
+        paths.append({"path": "chunked", "chunk_mode": "own"})
+        paths.append({"path": "chunked", "chunk_mode": "lookback"})
     return paths
 
 
@@ -122,21 +123,39 @@ def test_ragged_shapes(shape):
         assert_close(run(a_d, b_d, **opt).cpu().numpy(), h64, f"{shape} {opt}")
 
 
+VARIANTS = [(128, 64, 2), (128, 64, 3), (128, 32, 3), (256, 32, 2), (64, 128, 2), (64, 64, 2), (64, 64, 3),
+            (32, 128, 2), (32, 128, 3), (32, 64, 3), (32, 64, 4), (32, 32, 6)]
+
+
 def _variants():
     out = []
-    for td, tt, st in [(128, 64, 2), (128, 64, 3), (128, 32, 3), (256, 32, 2), (64, 128, 2), (64, 64, 2),
-                       (64, 64, 3), (32, 128, 2), (32, 64, 3)]:
-        out.append({"path": "chunked", "tile_d": td, "tile_t": tt, "stages": st})
+    for td, tt, st in VARIANTS:
+        for mode in ("own", "lookback"):
+            out.append({"path": "chunked", "tile_d": td, "tile_t": tt, "stages": st, "chunk_mode": mode})
     return out
 
 
-@pytest.mark.parametrize("opt", _variants(), ids=lambda o: f"d{o['tile_d']}t{o['tile_t']}s{o['stages']}")
+@pytest.mark.parametrize("opt", _variants(),
+                         ids=lambda o: f"d{o['tile_d']}t{o['tile_t']}s{o['stages']}-{o['chunk_mode']}")
 def test_every_chunked_variant(opt):
     for (B, L, D) in [(3, 1000, 260), (1, 20000, 64), (2, 777, 36)]:
         a, b = inputs.generate(B, L, D, seed=7 + L, a_dist="u[0.9,1)", b_dist="n(0,1)")
         h64, _ = oracle.f64(a, b)
         h = run(a.to(DEV), b.to(DEV), **opt).cpu().numpy()
         assert_close(h, h64, f"{(B, L, D)} {opt}")
+
+
+@pytest.mark.parametrize("tile", VARIANTS, ids=lambda t: f"d{t[0]}t{t[1]}s{t[2]}")
+def test_chunk_modes_agree_bit_for_bit(tile):
+    """Both modes evaluate the carry as the same chain H_q = A_q*H_{q-1} + B_q: identical bits."""
+    td, tt, st = tile
+    for (B, L, D, seed) in [(2, 3000, 128, 1), (1, 50000, 64, 2)]:
+        a, b = inputs.generate(B, L, D, seed=seed, a_dist="u[0,1)", b_dist="n(0,1)")
+        a_d, b_d = a.to(DEV), b.to(DEV)
+        opt = {"path": "chunked", "tile_d": td, "tile_t": tt, "stages": st}
+        h_own = run(a_d, b_d, chunk_mode="own", **opt)
+        h_lb = run(a_d, b_d, chunk_mode="lookback", **opt)
+        assert torch.equal(h_own, h_lb), f"{tile} {(B, L, D)}"
 
 
 @pytest.mark.parametrize("vec,prefetch", [(v, p) for v in (1, 2, 4) for p in (4, 8, 16)])
@@ -241,7 +260,7 @@ def test_streams_run_independently():
     outs = []
     for s in streams:
         with torch.cuda.stream(s):
-            outs.append(lr.linrec_scan_f32_ex(a_d, b_d, stream=s, path="chunked"))
+            outs.append(lr.linrec_scan_f32_ex(a_d, b_d, stream=s, path="chunked", chunk_mode="lookback"))
     torch.cuda.synchronize()
     for h in outs:
         assert_close(h.cpu().numpy(), h64, "multi-stream")
@@ -263,7 +282,7 @@ def test_lookback_timeout_reports_and_recovers():
     with torch.cuda.stream(s):
         # tile 5 publishes nothing: tile 6 waits a bounded number of polls, then gives up
         h = lr.linrec_scan_f32_ex(a_d, b_d, stream=s, path="chunked", tile_d=64, tile_t=64, stages=2,
-                                  spin_limit=2000, test_silent_tile=5 + 1, d_status=status)
+                                  chunk_mode="lookback", spin_limit=2000, test_silent_tile=5 + 1, d_status=status)
     s.synchronize()
     assert int(status.item()) & (1 << lr.LINREC_ERR_LOOKBACK_TIMEOUT)
     hn = h.cpu().numpy()
@@ -273,12 +292,13 @@ def test_lookback_timeout_reports_and_recovers():
     # the stream's own word: same failure through the plain status query
     with torch.cuda.stream(s):
         lr.linrec_scan_f32_ex(a_d, b_d, stream=s, path="chunked", tile_d=64, tile_t=64, stages=2,
-                              spin_limit=2000, test_silent_tile=5 + 1)
+                              chunk_mode="lookback", spin_limit=2000, test_silent_tile=5 + 1)
     assert lr.linrec_stream_status(s) == lr.LINREC_ERR_LOOKBACK_TIMEOUT
     assert lr.linrec_stream_status(s) == lr.LINREC_OK          # cleared
     # the context is healthy: the next call on the same stream is exact
     with torch.cuda.stream(s):
-        h = lr.linrec_scan_f32_ex(a_d, b_d, stream=s, path="chunked", tile_d=64, tile_t=64, stages=2)
+        h = lr.linrec_scan_f32_ex(a_d, b_d, stream=s, path="chunked", tile_d=64, tile_t=64, stages=2,
+                                  chunk_mode="lookback")
     s.synchronize()
     assert_close(h.cpu().numpy(), h64, "after recovery")
     assert lr.linrec_stream_status(s) == lr.LINREC_OK
