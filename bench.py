@@ -31,7 +31,13 @@ if ROOT not in sys.path:
 
 METRIC = "scan GB/s (a,b,h bytes) & % of GB300 HBM peak at B=32,L=4096,D=256 fp32"
 UNIT = "GB/s"
-WORKLOAD = "pages"
+WORKLOAD = "pages"          # the headline workload; --workload picks another for reports
+
+
+def metric_for(w) -> str:
+    if w.name == WORKLOAD:
+        return METRIC
+    return f"scan GB/s (a,b,h bytes) & % of GB300 HBM peak at B={w.B},L={w.L},D={w.D} fp32 ({w.name})"
 FALLBACK_HBM_GBS = 6800.0
 CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -186,7 +192,7 @@ def run_reference(args):
     from linear_recurrence_scan_fp32_gb300 import inputs
     import oracle
     oracle.build()
-    w = inputs.WORKLOADS[WORKLOAD]
+    w = inputs.WORKLOADS[args.workload]
     a, b = inputs.generate_workload(w)
     a, b = a.numpy(), b.numpy()
     threads = oracle.hardware_threads()
@@ -211,7 +217,7 @@ def run_reference(args):
     total = sum(times)
     value = sample_bytes * args.steps / total / 1e9
     line = {
-        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+        "impl": "reference", "metric": metric_for(w), "value": round(value, 3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "gpu_launches": 0,
@@ -244,15 +250,24 @@ def run_ours(args):
     _build.build()
     lr.lib()
 
-    w = inputs.WORKLOADS[WORKLOAD]
+    w = inputs.WORKLOADS[args.workload]
     a_cpu, b_cpu = inputs.generate(w.B, w.L, w.D, rank_seed(w.seed, rank), w.a_dist, w.b_dist)
     a = a_cpu.to(dev)
     b = b_cpu.to(dev)
     h = torch.empty_like(a)
     stream = torch.cuda.current_stream(dev)
     opt = {} if args.path == "auto" else {"path": args.path}
+    if args.chunk_mode != "auto":
+        opt.update(path="chunked", chunk_mode=args.chunk_mode)
+    if args.tile:
+        td, tt, st = (int(x) for x in args.tile.split(","))
+        opt.update(path="chunked", tile_d=td, tile_t=tt, stages=st)
     plan = lr.linrec_plan_f32(w.B, w.L, w.D, sm_count=torch.cuda.get_device_properties(dev).multi_processor_count,
                               **opt)
+    if plan["path_name"] == "chunked" and not plan["lookback"]:
+        kernel_tag = "chunked"
+    else:
+        kernel_tag = "chunked_lookback" if plan["path_name"] == "chunked" else "regcarry"
 
     def step():
         if opt:
@@ -294,8 +309,8 @@ def run_ours(args):
     mean_launch_s = statistics.fmean(per_launch_ms) / 1e3
     achieved = w.algorithmic_bytes / mean_launch_s / 1e9
     peak, peak_kind = hbm_peak()
-    kernel = "chunked" if plan["path_name"] == "chunked" else "regcarry"
-    traffic = committed_traffic(kernel, WORKLOAD)
+    kernel = kernel_tag
+    traffic = committed_traffic(kernel, w.name)
 
     # in-run copy ceiling over the same byte count: 1.5*N floats read and written
     n_copy = w.numel * 3 // 2
@@ -352,15 +367,16 @@ def run_ours(args):
     if rank == 0:
         clk = clocks.summary()
         line = {
-            "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "metric": metric_for(w), "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(seconds * 1e3 / args.steps, 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": w.about, "B": w.B, "L": w.L, "D": w.D, "seed": w.seed,
                        "global_batch": w.B * world,
-                       "l2": "inputs larger than L2: 402 MB per step vs 129 MB L2, no flush",
+                       "l2": (f"inputs larger than L2: {w.algorithmic_bytes / 1e6:.0f} MB per step vs 129 MB L2, "
+                              "no flush") if w.algorithmic_bytes > 129e6 else "working set fits L2: small case",
                        "path": plan["path_name"],
                        "plan": {k: plan[k] for k in ("vec", "prefetch", "tile_t", "tile_d", "segments", "stages",
-                                                     "threads", "grid")}},
+                                                     "lookback", "threads", "grid")}},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic,
                          "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
@@ -387,6 +403,10 @@ def main(argv=None):
     p.add_argument("--warmup", type=int, default=100)
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--path", choices=("auto", "regcarry", "chunked"), default="auto")
+    p.add_argument("--workload", default=WORKLOAD,
+                   help="named workload (tiny, pages, long, gated, short, ...); pages is the headline")
+    p.add_argument("--chunk-mode", choices=("auto", "own", "lookback"), default="auto")
+    p.add_argument("--tile", default="", help="chunked tile as tile_d,tile_t,stages")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0)

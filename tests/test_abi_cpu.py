@@ -81,10 +81,16 @@ def test_argument_checks_return_before_any_launch(L):
 
 
 def test_plan_paths():
-    # many channels: the register path with 16-byte vectors
+    # many channels: the chunked kernel, each CTA owning whole slices
     p = lr.linrec_plan_f32(256, 128, 4096)
+    assert p["path_name"] == "chunked" and p["lookback"] == 0
+    # the register path when forced: 16-byte vectors, a grid covering every group
+    p = lr.linrec_plan_f32(256, 128, 4096, path="regcarry")
     assert p["path_name"] == "regcarry" and p["vec"] == 4
     assert p["grid"] * p["threads"] >= 256 * 4096 // 4
+    # few channel groups: narrower blocks so that every SM gets some
+    p = lr.linrec_plan_f32(64, 2048, 1024, path="regcarry", sm_count=152)
+    assert p["grid"] >= 2 * 152 or p["threads"] == 32
     # few channels, long sequence: the chunked look-back path
     p = lr.linrec_plan_f32(1, 1 << 20, 64)
     assert p["path_name"] == "chunked"
