@@ -85,12 +85,37 @@ typedef struct {
     unsigned int *d_status; /* device word (may be NULL): the kernel ORs 1 << linrec_status_t
                                into it on a device-side failure; otherwise the stream's own word
                                is used (read it with linrec_stream_status) */
+    const float *h_init; /* (B, D) state each sequence continues from, or NULL (see linrec_scan_f32_carry) */
+    float *h_last;       /* (B, D) receives h[:, L-1, :], or NULL */
     int64_t spin_limit;  /* chunked: polls of a predecessor before giving up (0 = default, ~1 s) */
     int64_t test_silent_tile; /* chunked, tests only: 0 = off; k > 0 makes tile id k-1
                                  publish nothing, so its successor's look-back times out */
 } linrec_options_t;
 
-/* linrec_scan_f32 with explicit options (forced path, tile shape, status word). */
+/*
+ * linrec_scan_f32_carry -- the scan continued from a state, for scanning a long
+ * sequence in segments or streaming it.  The running value h is the only
+ * thing that crosses a chunk boundary ("Kimi-K2.6 l1_p9", the running_h
+ * carry); this entry point takes it in and hands it out:
+ *
+ *     h[i,t,d] = a[i,t,d] * h[i,t-1,d] + b[i,t,d]   for every t >= 0,
+ *     h[i,-1,d] = h_init[i*D + d]                    (so a[i,0,d] is used)
+ *     h_last[i*D + d] = h[i,L-1,d].
+ *
+ * h_init == NULL gives linrec_scan_f32's definition (h_0 = b_0, a_0 unused);
+ * h_last == NULL skips the last state.  h_init and h_last are (B, D) fp32
+ * device arrays, row-major, any 4-byte alignment.  h_last may be the same
+ * buffer as h_init (the state is updated in place: every channel reads its
+ * h_init before any h_last is written); any other overlap between h_init,
+ * h_last, a, b and h returns LINREC_ERR_ALIAS.  Scanning [0, L1) and then
+ * [L1, L) continued from the first call's h_last gives the same values as
+ * one call over [0, L) up to rounding (the tiles differ).
+ */
+linrec_status_t linrec_scan_f32_carry(const float *a, const float *b, float *h,
+                                      int64_t B, int64_t L, int64_t D,
+                                      const float *h_init, float *h_last, void *stream);
+
+/* linrec_scan_f32 with explicit options (forced path, tile shape, status word, carry). */
 linrec_status_t linrec_scan_f32_ex(const float *a, const float *b, float *h,
                                    int64_t B, int64_t L, int64_t D, void *stream,
                                    const linrec_options_t *opt);

@@ -12,6 +12,7 @@ library raises ``LinrecError``.
 Functions keep the C names:
     linrec_scan_f32(a, b, h=None, stream=None) -> h
     linrec_scan_f32_ex(a, b, h=None, stream=None, **options) -> h
+    linrec_scan_f32_carry(a, b, h=None, h_init=None, h_last=None, stream=None) -> h
     linrec_plan_f32(B, L, D, sm_count=152, align_bytes=16, resident_ctas=0, **options) -> dict
     linrec_stream_status(stream=None) -> int
     linrec_copy_f32(src, dst, stream=None)
@@ -56,6 +57,8 @@ class Options(ctypes.Structure):
         ("ctas_per_sm", ctypes.c_int),
         ("chunk_mode", ctypes.c_int),
         ("d_status", ctypes.c_void_p),
+        ("h_init", ctypes.c_void_p),
+        ("h_last", ctypes.c_void_p),
         ("spin_limit", ctypes.c_int64),
         ("test_silent_tile", ctypes.c_int64),
     ]
@@ -101,6 +104,8 @@ def lib():
         L.linrec_scan_f32_ex.restype = i32
         L.linrec_plan_f32.argtypes = [i64, i64, i64, i32, i32, i32, ctypes.POINTER(Options), ctypes.POINTER(Plan)]
         L.linrec_plan_f32.restype = i32
+        L.linrec_scan_f32_carry.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, vp]
+        L.linrec_scan_f32_carry.restype = i32
         L.linrec_stream_status.argtypes = [vp]
         L.linrec_stream_status.restype = i32
         L.linrec_copy_f32.argtypes = [vp, vp, i64, vp]
@@ -125,14 +130,23 @@ def _check(code: int, what: str):
 CHUNK_MODES = {"auto": 0, "own": 1, "lookback": 2}
 
 
+def _addr(x):
+    if x is None:
+        return None
+    return int(x.data_ptr() if hasattr(x, "data_ptr") else x)
+
+
 def make_options(path="auto", vec=0, prefetch=0, tile_t=0, tile_d=0, stages=0, ctas_per_sm=0,
-                 chunk_mode="auto", d_status=None, spin_limit=0, test_silent_tile=0) -> Options:
+                 chunk_mode="auto", d_status=None, h_init=None, h_last=None, spin_limit=0,
+                 test_silent_tile=0) -> Options:
     o = Options()
     o.path = PATHS[path] if isinstance(path, str) else int(path)
     o.vec, o.prefetch, o.tile_t, o.tile_d, o.stages = int(vec), int(prefetch), int(tile_t), int(tile_d), int(stages)
     o.ctas_per_sm = int(ctas_per_sm)
     o.chunk_mode = CHUNK_MODES[chunk_mode] if isinstance(chunk_mode, str) else int(chunk_mode)
-    o.d_status = None if d_status is None else int(d_status.data_ptr() if hasattr(d_status, "data_ptr") else d_status)
+    o.d_status = _addr(d_status)
+    o.h_init = _addr(h_init)
+    o.h_last = _addr(h_last)
     o.spin_limit = int(spin_limit)
     o.test_silent_tile = int(test_silent_tile)
     return o
@@ -186,6 +200,31 @@ def linrec_scan_f32(a, b, h=None, stream=None):
         h = torch.empty_like(a)
     code = lib().linrec_scan_f32(a.data_ptr(), b.data_ptr(), h.data_ptr(), B, L, D, _stream_handle(stream))
     _check(code, "linrec_scan_f32")
+    return h
+
+
+def _check_state(x, name, B, D):
+    import torch
+    if x is None:
+        return
+    if not isinstance(x, torch.Tensor) or x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous():
+        raise TypeError(f"{name} must be a contiguous float32 CUDA tensor")
+    if x.numel() != B * D:
+        raise ValueError(f"{name} must hold B*D = {B * D} values (shape (B, D))")
+
+
+def linrec_scan_f32_carry(a, b, h=None, h_init=None, h_last=None, stream=None):
+    """The scan continued from h_init (B, D) (None: h_0 = b_0); the last state goes to h_last (B, D)
+    if given.  Returns h."""
+    import torch
+    B, L, D = _shape_of(a, b, h)
+    _check_state(h_init, "h_init", B, D)
+    _check_state(h_last, "h_last", B, D)
+    if h is None:
+        h = torch.empty_like(a)
+    code = lib().linrec_scan_f32_carry(a.data_ptr(), b.data_ptr(), h.data_ptr(), B, L, D, _addr(h_init),
+                                       _addr(h_last), _stream_handle(stream))
+    _check(code, "linrec_scan_f32_carry")
     return h
 
 

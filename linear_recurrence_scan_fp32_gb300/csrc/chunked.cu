@@ -75,7 +75,7 @@ struct __align__(128) ChunkSmem {
 template <int S, int R>
 __device__ __forceinline__ float lookback_carry(
     const long long id, const long long n_slices, const int TD, const int cc, const int ss, const int gbase,
-    const uint32_t tag, const bool publish_agg, const float tA, const float tB,
+    const uint32_t tag, const bool publish_agg, const float tA, const float tB, const float h_before,
     unsigned long long *__restrict__ wAggA, unsigned long long *__restrict__ wAggB,
     const unsigned long long *__restrict__ wInc, Control *__restrict__ ctrl, unsigned int *__restrict__ status,
     const long long spin_limit)
@@ -110,7 +110,7 @@ __device__ __forceinline__ float lookback_carry(
                 const long long j = base - (long long)(r * S + ss) * n_slices;
                 if (j < 0) {
                     inc = true;
-                    vH[r] = 0.0f;             // before the first chunk: h = 0
+                    vH[r] = h_before;         // before the first chunk: the carried-in state
                 } else {
                     const unsigned long long wi = ld_relaxed_u64(&wInc[j * TD + cc]);
                     inc = word_tag(wi) == tag;
@@ -215,7 +215,8 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
                     const int own,               // 1: slice-owner mode, 0: look-back mode
                     Control *__restrict__ ctrl, unsigned long long *__restrict__ words,
                     unsigned int *__restrict__ status,
-                    const long long spin_limit, const long long silent_tile)
+                    const long long spin_limit, const long long silent_tile,
+                    const float *h_init, float *h_last)
 {
     constexpr int K = TT / S;                 // time steps per thread
     constexpr int R = (S >= 4) ? 16 / S : 4;  // look-back: predecessors per lane
@@ -357,7 +358,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
             ra[j] = ta[j * TD];
             rb[j] = tb[j * TD];
         }
-        if (seq_start) ra[0] = 0.0f;          // h_{-1} = 0: the first slope never matters
+        if (seq_start && !h_init) ra[0] = 0.0f;   // h_{-1} = 0: the first slope never matters
         float A = 1.0f, Bv = 0.0f;
 #pragma unroll
         for (int j = 0; j < K; ++j) {
@@ -390,17 +391,19 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
         const float tB = __shfl_sync(kFull, xB, S - 1, S);
 
         // ---- 4. the carry entering the tile ---------------------------------------
+        // h before the first chunk: the carried-in state, or 0.
+        const float h_before = (h_init && d0 + cc < D) ? h_init[bi * D + d0 + cc] : 0.0f;
         if (own) {
             if (ss == 0) {
-                const float carry = (q == 0) ? 0.0f : run;
+                const float carry = (q == 0) ? h_before : run;
                 run = fmaf(tA, carry, tB);
                 sm.carry[cc] = carry;
             }
         } else {
             const bool publish = (q + 1 < chunks) && (id != silent_tile);
-            float carry = 0.0f;
+            float carry = h_before;
             if (q > 0)
-                carry = lookback_carry<S, R>(id, n_slices, TD, cc, ss, gbase, tag, publish, tA, tB,
+                carry = lookback_carry<S, R>(id, n_slices, TD, cc, ss, gbase, tag, publish, tA, tB, h_before,
                                              wAggA, wAggB, wInc, ctrl, status, spin_limit);
             if (ss == 0) {
                 if (publish) st_relaxed_u64(&wInc[id * TD + cc], pack_word(tag, fmaf(tA, carry, tB)));
@@ -428,6 +431,8 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
                     }
                 }
             }
+            // the thread holding t = L-1 hands the state out
+            if (h_last && nv > 0 && t0 + r0 + nv == L) h_last[bi * D + d0 + c] = hc;
         }
         __syncthreads();                      // stage st and the scratch arrays are free again
     }
@@ -511,8 +516,10 @@ cudaError_t launch_chunked(const ChunkedLaunch &p, cudaStream_t stream) {
     Control *ctrl = p.ctrl;
     unsigned long long *words = p.words;
     unsigned int *status = p.status;
+    const float *h_init = p.h_init;
+    float *h_last = p.h_last;
     void *args[] = {(void *)&p.map_a, (void *)&p.map_b, &h, &L, &D, &spb, &ns, &ch, &nt, &own,
-                    &ctrl, &words, &status, &spin, &silent};
+                    &ctrl, &words, &status, &spin, &silent, &h_init, &h_last};
     return cudaLaunchKernel(fn, dim3((unsigned)p.grid), dim3((unsigned)p.variant->threads), args,
                             p.variant->smem_bytes, stream);
 }

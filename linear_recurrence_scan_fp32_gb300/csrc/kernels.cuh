@@ -29,9 +29,12 @@ constexpr unsigned int kStatusTmaTimeout = 1u << 7;       // 1 << LINREC_ERR_TMA
 // ---- register-carry path ---------------------------------------------------
 // One thread walks `vec` adjacent channels through all L steps, with the loads
 // of the next `prefetch` steps in flight in registers.
+// h_init (B x D, may be NULL): state each sequence continues from (a_0 is then
+// used); h_last (B x D, may be NULL): receives h[:, L-1, :].
 bool regcarry_supported(int vec, int prefetch);
 cudaError_t launch_regcarry(int vec, int prefetch, int threads, const float *a, const float *b,
-                            float *h, int64_t B, int64_t L, int64_t D, cudaStream_t stream);
+                            float *h, int64_t B, int64_t L, int64_t D, const float *h_init, float *h_last,
+                            cudaStream_t stream);
 
 // ---- chunked path ----------------------------------------------------------
 // A tile is (tile_t time steps) x (tile_d channels) of one batch index, staged in
@@ -60,6 +63,8 @@ struct ChunkedLaunch {
     unsigned int *status;        // where device-side failures are recorded
     int64_t spin_limit;
     int64_t silent_tile;         // tile id that publishes nothing (tests), or -1
+    const float *h_init = nullptr;   // (B x D) state to continue from, or NULL
+    float *h_last = nullptr;         // (B x D) last state out, or NULL
 };
 // Number of CTAs of this variant that fit on one SM (occupancy API).
 cudaError_t chunked_ctas_per_sm(const ChunkedVariant *v, int *ctas);

@@ -41,10 +41,12 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn g_encode = nullptr;
 
-bool overlaps(const void *x, const void *y, int64_t bytes) {
+// [x, x + xbytes) and [y, y + ybytes) share a byte.
+bool overlaps(const void *x, int64_t xbytes, const void *y, int64_t ybytes) {
     const uintptr_t a0 = reinterpret_cast<uintptr_t>(x), b0 = reinterpret_cast<uintptr_t>(y);
-    return a0 < b0 + (uintptr_t)bytes && b0 < a0 + (uintptr_t)bytes;
+    return a0 < b0 + (uintptr_t)ybytes && b0 < a0 + (uintptr_t)xbytes;
 }
+bool overlaps(const void *x, const void *y, int64_t bytes) { return overlaps(x, bytes, y, bytes); }
 
 int align_of(const void *a, const void *b, const void *h) {
     const uintptr_t u = reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(b) |
@@ -270,6 +272,15 @@ linrec_status_t linrec_scan_f32_ex(const float *a, const float *b, float *h, int
     if (n == 0) return LINREC_OK;
     if (!a || !b || !h) return LINREC_ERR_INVALID_VALUE;
     if (overlaps(h, a, n * 4) || overlaps(h, b, n * 4)) return LINREC_ERR_ALIAS;
+    const float *h_init = opt->h_init;
+    float *h_last = opt->h_last;
+    const int64_t nstate = B * D * 4;
+    if (h_init && (overlaps(h_init, nstate, h, n * 4) ||
+                   (h_last && h_last != h_init && overlaps(h_init, h_last, nstate))))
+        return LINREC_ERR_ALIAS;
+    if (h_last && (overlaps(h_last, nstate, a, n * 4) || overlaps(h_last, nstate, b, n * 4) ||
+                   overlaps(h_last, nstate, h, n * 4)))
+        return LINREC_ERR_ALIAS;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
 
     int dev = 0;
@@ -289,7 +300,8 @@ linrec_status_t linrec_scan_f32_ex(const float *a, const float *b, float *h, int
     if (st != LINREC_OK) return st;
 
     if (plan.path == LINREC_PATH_REGCARRY) {
-        cudaError_t err = launch_regcarry(plan.vec, plan.prefetch, plan.threads, a, b, h, B, L, D, stream);
+        cudaError_t err = launch_regcarry(plan.vec, plan.prefetch, plan.threads, a, b, h, B, L, D, h_init, h_last,
+                                          stream);
         return err == cudaSuccess ? LINREC_OK : LINREC_ERR_LAUNCH;
     }
 
@@ -330,6 +342,8 @@ linrec_status_t linrec_scan_f32_ex(const float *a, const float *b, float *h, int
     p.status = opt->d_status ? opt->d_status : &p.ctrl->status;
     p.spin_limit = opt->spin_limit > 0 ? opt->spin_limit : kDefaultSpinLimit;
     p.silent_tile = opt->test_silent_tile > 0 ? opt->test_silent_tile - 1 : -1;
+    p.h_init = h_init;
+    p.h_last = h_last;
     cudaError_t err = launch_chunked(p, stream);
     if (err != cudaSuccess) {
         cudaGetLastError();
@@ -341,6 +355,14 @@ linrec_status_t linrec_scan_f32_ex(const float *a, const float *b, float *h, int
 linrec_status_t linrec_scan_f32(const float *a, const float *b, float *h, int64_t B, int64_t L, int64_t D,
                                 void *stream) {
     return linrec_scan_f32_ex(a, b, h, B, L, D, stream, nullptr);
+}
+
+linrec_status_t linrec_scan_f32_carry(const float *a, const float *b, float *h, int64_t B, int64_t L, int64_t D,
+                                      const float *h_init, float *h_last, void *stream) {
+    linrec_options_t opt = {};
+    opt.h_init = h_init;
+    opt.h_last = h_last;
+    return linrec_scan_f32_ex(a, b, h, B, L, D, stream, &opt);
 }
 
 linrec_status_t linrec_stream_status(void *stream_ptr) {

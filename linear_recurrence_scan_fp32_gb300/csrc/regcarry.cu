@@ -41,13 +41,14 @@ template <int V, int P>
 __global__ void __launch_bounds__(256)
 regcarry_kernel(const float *__restrict__ a, const float *__restrict__ b, float *__restrict__ h,
                 const long long L, const long long D, const long long groups_per_batch,
-                const long long n_groups)
+                const long long n_groups, const float *h_init, float *h_last)
 {
     using vec = typename VecT<V>::type;
     const long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (g >= n_groups) return;
     const long long bi = g / groups_per_batch;
-    const long long off = bi * L * D + (g - bi * groups_per_batch) * V;
+    const long long dch = (g - bi * groups_per_batch) * V;   // first channel of this thread
+    const long long off = bi * L * D + dch;
     const vec *pa = reinterpret_cast<const vec *>(a + off);
     const vec *pb = reinterpret_cast<const vec *>(b + off);
     vec *ph = reinterpret_cast<vec *>(h + off);
@@ -61,9 +62,15 @@ regcarry_kernel(const float *__restrict__ a, const float *__restrict__ b, float 
             rb[j] = ld_stream(pb + j * stride);
         }
     }
-    zero(ra[0]);                              // h_{-1} = 0 and a_0 is never used
     vec hv;
     zero(hv);
+    if (h_init) {                             // continue from the given state: a_0 is used
+        float *hvs = reinterpret_cast<float *>(&hv);
+#pragma unroll
+        for (int v = 0; v < V; ++v) hvs[v] = h_init[bi * D + dch + v];
+    } else {
+        zero(ra[0]);                          // h_{-1} = 0 and a_0 is never used
+    }
     for (long long t0 = 0; t0 < L; t0 += P) {
 #pragma unroll
         for (int j = 0; j < P; ++j) {
@@ -79,15 +86,20 @@ regcarry_kernel(const float *__restrict__ a, const float *__restrict__ b, float 
             }
         }
     }
+    if (h_last) {
+        const float *hvs = reinterpret_cast<const float *>(&hv);
+#pragma unroll
+        for (int v = 0; v < V; ++v) h_last[bi * D + dch + v] = hvs[v];
+    }
 }
 
 template <int V, int P>
 cudaError_t launch_one(int threads, const float *a, const float *b, float *h, int64_t B, int64_t L,
-                       int64_t D, cudaStream_t stream) {
+                       int64_t D, const float *h_init, float *h_last, cudaStream_t stream) {
     const long long gpb = D / V;
     const long long n = B * gpb;
     const long long blocks = (n + threads - 1) / threads;
-    regcarry_kernel<V, P><<<(unsigned)blocks, threads, 0, stream>>>(a, b, h, L, D, gpb, n);
+    regcarry_kernel<V, P><<<(unsigned)blocks, threads, 0, stream>>>(a, b, h, L, D, gpb, n, h_init, h_last);
     return cudaGetLastError();
 }
 
@@ -98,9 +110,10 @@ bool regcarry_supported(int vec, int prefetch) {
 }
 
 cudaError_t launch_regcarry(int vec, int prefetch, int threads, const float *a, const float *b, float *h,
-                            int64_t B, int64_t L, int64_t D, cudaStream_t stream) {
+                            int64_t B, int64_t L, int64_t D, const float *h_init, float *h_last,
+                            cudaStream_t stream) {
 #define LINREC_RC(V, P) \
-    if (vec == V && prefetch == P) return launch_one<V, P>(threads, a, b, h, B, L, D, stream);
+    if (vec == V && prefetch == P) return launch_one<V, P>(threads, a, b, h, B, L, D, h_init, h_last, stream);
     LINREC_RC(4, 4) LINREC_RC(4, 8) LINREC_RC(4, 16)
     LINREC_RC(2, 4) LINREC_RC(2, 8) LINREC_RC(2, 16)
     LINREC_RC(1, 4) LINREC_RC(1, 8) LINREC_RC(1, 16)

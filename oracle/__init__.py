@@ -60,6 +60,8 @@ def _bind(lib):
     lib.linrec_oracle_f32seq.restype = i32
     lib.linrec_oracle_f64_channel.argtypes = [pf, pf, pd, i64, i64, i64, i64, i64]
     lib.linrec_oracle_f64_channel.restype = i32
+    lib.linrec_oracle_f64_carry.argtypes = [pf, pf, pd, pd, pd, i64, i64, i64]
+    lib.linrec_oracle_f64_carry.restype = i32
     lib.linrec_oracle_hardware_threads.argtypes = []
     lib.linrec_oracle_hardware_threads.restype = i32
     return lib
@@ -125,6 +127,25 @@ def f64_channel(a, b, i: int, d: int, lib=None) -> np.ndarray:
     if rc != 0:
         raise ValueError("oracle rejected its arguments")
     return h
+
+
+def f64_carry(a, b, h0=None, lib=None):
+    """The recurrence continued from h0 (a (B, D) array, or None for the plain
+    definition); returns (h in float64, last state (B, D) in float64)."""
+    a, b = _as_f32(a), _as_f32(b)
+    lib = lib or load()
+    B, L, D = a.shape
+    h = np.empty(a.shape, dtype=np.float64)
+    hlast = np.empty((B, D), dtype=np.float64)
+    h0p = None
+    if h0 is not None:
+        h0 = np.ascontiguousarray(h0, dtype=np.float64).reshape(B, D)
+        h0p = _ptr(h0, ctypes.c_double)
+    rc = lib.linrec_oracle_f64_carry(_ptr(a, ctypes.c_float), _ptr(b, ctypes.c_float), h0p,
+                                     _ptr(h, ctypes.c_double), _ptr(hlast, ctypes.c_double), B, L, D)
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return h, hlast
 
 
 def hardware_threads() -> int:

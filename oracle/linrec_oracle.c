@@ -28,6 +28,15 @@
  *                            `h = a[:, t] * h + b[:, t]` computes this).
  *   linrec_oracle_f64_channel -- one channel's whole sequence, for sampled
  *                            checks on workloads too large to hold in fp64.
+ *   linrec_oracle_f64_carry -- the recurrence continued from a given state:
+ *                            h[i,t,d] = a[i,t,d] * h[i,t-1,d] + b[i,t,d] for
+ *                            every t >= 0, with h[i,-1,d] = h0[i,d] (so a_0
+ *                            is used), and optionally the last state
+ *                            h[i,L-1,d] written to hlast[i,d].  h0 = NULL
+ *                            means the plain definition above.  This is the
+ *                            running-h carry of "Kimi-K2.6 l1_p9" (the value
+ *                            passed from one chunk to the next) exposed as an
+ *                            argument, so a sequence can be scanned in segments.
  *
  * Threads only split the set of independent channels; every channel is still
  * one sequential loop, so results do not depend on the thread count.
@@ -165,6 +174,39 @@ int linrec_oracle_f64_channel(const float *a, const float *b, double *h_col,
         const int64_t k = base + t * D;
         h = (double)a[k] * h + (double)b[k];
         h_col[t] = h;
+    }
+    return 0;
+}
+
+/* The recurrence continued from h0 (B x D, may be NULL), last state to hlast
+   (B x D, may be NULL).  Sequential in t per channel, fp64 accumulator. */
+int linrec_oracle_f64_carry(const float *a, const float *b, const double *h0, double *h, double *hlast,
+                            int64_t B, int64_t L, int64_t D)
+{
+    if (B < 0 || L < 0 || D < 0) return -1;
+    if (B == 0 || D == 0) return 0;
+    if (!a || !b || (L > 0 && !h)) return -1;
+    for (int64_t i = 0; i < B; ++i) {
+        const int64_t base = i * L * D;
+        for (int64_t d = 0; d < D; ++d) {
+            double hv;
+            int64_t t0;
+            if (h0) {
+                hv = h0[i * D + d];
+                t0 = 0;
+            } else {
+                if (L == 0) { if (hlast) hlast[i * D + d] = 0.0; continue; }
+                hv = (double)b[base + d];                       /* h_0 = b_0 */
+                h[base + d] = hv;
+                t0 = 1;
+            }
+            for (int64_t t = t0; t < L; ++t) {
+                const int64_t k = base + t * D + d;
+                hv = (double)a[k] * hv + (double)b[k];
+                h[k] = hv;
+            }
+            if (hlast) hlast[i * D + d] = hv;
+        }
     }
     return 0;
 }

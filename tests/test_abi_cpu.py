@@ -159,3 +159,21 @@ def test_plan_chunk_modes():
     assert p["lookback"] == 1 and p["workspace_bytes"] == 256 + 24 * p["n_tiles"] * p["tile_d"]
     with pytest.raises(lr.LinrecError):
         lr.linrec_plan_f32(1, 1000, 64, path="chunked", chunk_mode=3)
+
+
+def test_carry_state_overlap_checks(L):
+    # fake, never-dereferenced addresses: every check runs before any device access
+    B, Lx, D = 2, 100, 8
+    n = B * Lx * D * 4
+    a, b, h = 1 << 36, (1 << 36) + 2 * n, (1 << 36) + 4 * n
+    s1 = h + n                                  # right after h: no overlap
+    s2 = s1 + 1024
+    vp = ctypes.c_void_p
+    f = L.linrec_scan_f32_carry
+    f.argtypes = [vp, vp, vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vp, vp, vp]
+    f.restype = ctypes.c_int
+    assert f(a, b, h, B, Lx, D, h + 4, None, None) == lr.LINREC_ERR_ALIAS        # h_init inside h
+    assert f(a, b, h, B, Lx, D, None, a + n - 4, None) == lr.LINREC_ERR_ALIAS    # h_last ends a
+    assert f(a, b, h, B, Lx, D, s1, s1 + 8, None) == lr.LINREC_ERR_ALIAS         # partial overlap
+    assert f(a, b, h, -1, Lx, D, s1, s1, None) == lr.LINREC_ERR_INVALID_VALUE
+    assert f(None, None, None, 0, Lx, D, s1, s2, None) == lr.LINREC_OK

@@ -132,7 +132,65 @@ def pin_bruteforce(lib):
             assert err <= Fraction(1, 10 ** 12) * (1 + abs(e)), f"L={L} at {idx}: {float(h[idx])} vs {float(e)}"
 
 
-PINS = [pin_walkthrough, pin_prefix_sum, pin_copy, pin_running_product, pin_geometric, pin_bruteforce]
+def pin_carry_closed_forms(lib):
+    """Continued from h0 = x: a = c, b = 0 gives h_t = c^(t+1) x; a = 1 gives x + prefix sums of b."""
+    B, L, D = 2, 60, 3
+    x = np.array([[1.5, -2.0, 0.25], [4.0, 0.5, -1.0]])
+    a = np.full((B, L, D), 0.5, np.float32)
+    h, hl = oracle.f64_carry(a, np.zeros_like(a), x, lib=lib)
+    want = x[:, None, :] * 0.5 ** (np.arange(L)[None, :, None] + 1.0)
+    assert np.array_equal(h, want), "decay from the carried state"
+    assert np.array_equal(hl, want[:, -1, :]), "last state"
+    b = _f32(_rng(14).integers(-8, 9, size=(B, L, D)))
+    h, hl = oracle.f64_carry(np.ones_like(b), b, x, lib=lib)
+    want = x[:, None, :] + np.cumsum(b.astype(np.float64), axis=1)
+    assert np.array_equal(h, want), "prefix sum continued from the carried state"
+    assert np.array_equal(hl, want[:, -1, :])
+
+
+def pin_carry_bruteforce(lib):
+    """h_t = (a_0 ... a_t) x + sum_s (a_{s+1} ... a_t) b_s, exactly, a_0 used."""
+    rng = _rng(15)
+    for L in (1, 2, 5, 8):
+        a = _f32(rng.uniform(-2, 2, size=(2, L, 2)))
+        b = _f32(rng.standard_normal((2, L, 2)))
+        x = rng.standard_normal((2, 2))
+        h, hl = oracle.f64_carry(a, b, x, lib=lib)
+        for i in range(2):
+            for d in range(2):
+                af = [Fraction(float(v)) for v in a[i, :, d]]
+                bf = [Fraction(float(v)) for v in b[i, :, d]]
+                for t in range(L):
+                    p = Fraction(1)
+                    for r in range(0, t + 1):
+                        p *= af[r]
+                    e = p * Fraction(float(x[i, d]))
+                    for s_ in range(t + 1):
+                        q = Fraction(1)
+                        for r in range(s_ + 1, t + 1):
+                            q *= af[r]
+                        e += q * bf[s_]
+                    assert abs(Fraction(float(h[i, t, d])) - e) <= Fraction(1, 10 ** 12) * (1 + abs(e)), (L, i, t, d)
+                assert hl[i, d] == h[i, L - 1, d]
+
+
+def pin_carry_segments(lib):
+    """Scanning in segments, each continued from the last state of the one before, is the
+    unsplit scan bit for bit; with no state the carry entry is the plain definition."""
+    a, b = inputs.generate(3, 200, 7, seed=16)
+    a, b = a.numpy(), b.numpy()
+    full, _ = oracle.f64(a, b, lib=lib)
+    h0, hl0 = oracle.f64_carry(a, b, None, lib=lib)
+    assert np.array_equal(h0, full) and np.array_equal(hl0, full[:, -1, :])
+    parts, state = [], None
+    for lo, hi in [(0, 1), (1, 64), (64, 65), (65, 200)]:
+        h, state = oracle.f64_carry(a[:, lo:hi], b[:, lo:hi], state, lib=lib)
+        parts.append(h)
+    assert np.array_equal(np.concatenate(parts, axis=1), full), "segments differ from the unsplit scan"
+
+
+PINS = [pin_walkthrough, pin_prefix_sum, pin_copy, pin_running_product, pin_geometric, pin_bruteforce,
+        pin_carry_closed_forms, pin_carry_bruteforce, pin_carry_segments]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -205,7 +263,13 @@ def test_f32_loop_meets_bound_on_every_workload(oracle_lib):
 _F64_STEP = "h[row + d] = (double)a[row + d] * h[prev + d] + (double)b[row + d];"
 _F64_INIT = "h[base + d] = (double)b[base + d];                 /* h_0 = b_0 */"
 
+_CARRY_START = "hv = h0[i * D + d];"
+_CARRY_LAST = "if (hlast) hlast[i * D + d] = hv;"
+
 MUTANTS = {
+    "carry_state_ignored": (_CARRY_START, "hv = 0.0;"),
+    "carry_state_negated": (_CARRY_START, "hv = -h0[i * D + d];"),
+    "carry_last_state_wrong": (_CARRY_LAST, "if (hlast) hlast[i * D + d] = hv * 0.5;"),
     "operands_transposed": (_F64_STEP, "h[row + d] = (double)b[row + d] * h[prev + d] + (double)a[row + d];"),
     "a_index_off_by_one": (_F64_STEP, "h[row + d] = (double)a[prev + d] * h[prev + d] + (double)b[row + d];"),
     "b_term_dropped": (_F64_STEP, "h[row + d] = (double)a[row + d] * h[prev + d];"),
