@@ -62,6 +62,8 @@ def _bind(lib):
     lib.linrec_oracle_f64_channel.restype = i32
     lib.linrec_oracle_f64_carry.argtypes = [pf, pf, pd, pd, pd, i64, i64, i64]
     lib.linrec_oracle_f64_carry.restype = i32
+    lib.linrec_oracle_f64_backward.argtypes = [pf, pf, pf, pd, pd, pd, pd, pd, i64, i64, i64]
+    lib.linrec_oracle_f64_backward.restype = i32
     lib.linrec_oracle_hardware_threads.argtypes = []
     lib.linrec_oracle_hardware_threads.restype = i32
     return lib
@@ -146,6 +148,31 @@ def f64_carry(a, b, h0=None, lib=None):
     if rc != 0:
         raise ValueError("oracle rejected its arguments")
     return h, hlast
+
+
+def f64_backward(a, h, g, h0=None, dhlast=None, want_da=True, lib=None):
+    """Gradient of the carried recurrence: returns (da or None, db, dh0), float64."""
+    a, h, g = _as_f32(a), _as_f32(h), _as_f32(g)
+    lib = lib or load()
+    B, L, D = a.shape
+    db = np.empty(a.shape, dtype=np.float64)
+    da = np.empty(a.shape, dtype=np.float64) if want_da else None
+    dh0 = np.empty((B, D), dtype=np.float64)
+
+    def state(x):
+        if x is None:
+            return None, None
+        x = np.ascontiguousarray(x, dtype=np.float64).reshape(B, D)
+        return x, _ptr(x, ctypes.c_double)
+
+    h0, h0p = state(h0)
+    dhlast, dhp = state(dhlast)
+    rc = lib.linrec_oracle_f64_backward(_ptr(a, ctypes.c_float), _ptr(h, ctypes.c_float), _ptr(g, ctypes.c_float),
+                                        h0p, dhp, _ptr(da, ctypes.c_double) if want_da else None,
+                                        _ptr(db, ctypes.c_double), _ptr(dh0, ctypes.c_double), B, L, D)
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return da, db, dh0
 
 
 def hardware_threads() -> int:

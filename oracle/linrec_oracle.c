@@ -37,6 +37,15 @@
  *                            running-h carry of "Kimi-K2.6 l1_p9" (the value
  *                            passed from one chunk to the next) exposed as an
  *                            argument, so a sequence can be scanned in segments.
+ *   linrec_oracle_f64_backward -- the gradient of that recurrence for a loss
+ *                            with dL/dh = g: with c_t = dL/dh_t in total,
+ *                              c_{L-1} = g_{L-1} + dh_last,
+ *                              c_t     = g_t + a_{t+1} * c_{t+1}      (t < L-1),
+ *                              db_t = c_t,  da_t = c_t * h_{t-1},  dh0 = a_0 * c_0,
+ *                            h_{-1} = h0 (or 0 without h0, when a_0 is unused
+ *                            and da_0 = 0).  h is the forward output as given.
+ *                            Not on the pages: it follows from the definition
+ *                            by the chain rule.
  *
  * Threads only split the set of independent channels; every channel is still
  * one sequential loop, so results do not depend on the thread count.
@@ -206,6 +215,38 @@ int linrec_oracle_f64_carry(const float *a, const float *b, const double *h0, do
                 h[k] = hv;
             }
             if (hlast) hlast[i * D + d] = hv;
+        }
+    }
+    return 0;
+}
+
+/* Gradient of the carried recurrence.  a, h, g: (B, L, D); h0, dhlast: (B, D) or NULL;
+   da (may be NULL), db: (B, L, D) out; dh0: (B, D) out or NULL.  One reverse loop per channel. */
+int linrec_oracle_f64_backward(const float *a, const float *h, const float *g, const double *h0,
+                               const double *dhlast, double *da, double *db, double *dh0,
+                               int64_t B, int64_t L, int64_t D)
+{
+    if (B < 0 || L < 0 || D < 0) return -1;
+    if (B == 0 || D == 0 || L == 0) return 0;
+    if (!a || !g || !db || (da && !h)) return -1;
+    for (int64_t i = 0; i < B; ++i) {
+        const int64_t base = i * L * D;
+        for (int64_t d = 0; d < D; ++d) {
+            double c = dhlast ? dhlast[i * D + d] : 0.0;    /* c_L: what flows in from after L-1 */
+            double coef = 1.0;                              /* its weight in c_{L-1} */
+            for (int64_t t = L - 1; t >= 0; --t) {
+                const int64_t k = base + t * D + d;
+                c = (double)g[k] + coef * c;                /* c_t = g_t + a_{t+1} c_{t+1} */
+                db[k] = c;
+                if (da) {
+                    double hprev;
+                    if (t > 0) hprev = (double)h[k - D];
+                    else hprev = h0 ? h0[i * D + d] : 0.0;
+                    da[k] = c * hprev;
+                }
+                coef = (double)a[k];                        /* a_t weighs c_t in c_{t-1} */
+            }
+            if (dh0) dh0[i * D + d] = coef * c;             /* a_0 * c_0 */
         }
     }
     return 0;

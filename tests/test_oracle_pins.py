@@ -189,8 +189,111 @@ def pin_carry_segments(lib):
     assert np.array_equal(np.concatenate(parts, axis=1), full), "segments differ from the unsplit scan"
 
 
+def _dyadic(rng, shape, lo, hi, bits=8):
+    """Values on a 2^-bits grid, so that small power-of-two steps stay exact in fp32."""
+    return _f32(np.round(rng.uniform(lo, hi, size=shape) * 2 ** bits) / 2 ** bits)
+
+
+def pin_backward_finite_differences(lib):
+    """Gradients of loss = sum(g*h) + sum(w*h_{L-1}) match central differences of the forward oracle."""
+    rng = _rng(20)
+    B, L, D = 2, 6, 3
+    a = _dyadic(rng, (B, L, D), -1.25, 1.25)
+    b = _dyadic(rng, (B, L, D), -1.0, 1.0)
+    g = _dyadic(rng, (B, L, D), -1.0, 1.0)
+    w = rng.standard_normal((B, D))
+    x = rng.standard_normal((B, D))
+
+    def loss(a_, b_, x_):
+        h, hl = oracle.f64_carry(a_, b_, x_, lib=lib)
+        return float((g.astype(np.float64) * h).sum() + (w * hl).sum())
+
+    h, _ = oracle.f64_carry(a, b, x, lib=lib)
+    da, db, dx = oracle.f64_backward(a, h.astype(np.float32), g, x, w, lib=lib)
+    eps = 2.0 ** -12
+    for idx in [(0, 0, 0), (0, 3, 1), (1, 5, 2), (1, 1, 0), (0, 5, 2)]:
+        for arr, grad in ((a, da), (b, db)):
+            p_, m_ = arr.copy(), arr.copy()
+            p_[idx] += eps
+            m_[idx] -= eps
+            fd = (loss(p_ if arr is a else a, p_ if arr is b else b, x) -
+                  loss(m_ if arr is a else a, m_ if arr is b else b, x)) / (2 * eps)
+            assert abs(fd - grad[idx]) <= 1e-5 * (1 + abs(fd)), (idx, fd, grad[idx])
+    for i, d in [(0, 0), (1, 2)]:
+        xp, xm = x.copy(), x.copy()
+        xp[i, d] += eps
+        xm[i, d] -= eps
+        fd = (loss(a, b, xp) - loss(a, b, xm)) / (2 * eps)
+        assert abs(fd - dx[i, d]) <= 1e-7 * (1 + abs(fd)), ((i, d), fd, dx[i, d])
+
+
+def pin_backward_adjoint(lib):
+    """h is linear in b and in the start state: db = M^T g and dh0 = N^T g (dot-product test)."""
+    rng = _rng(21)
+    B, L, D = 2, 50, 4
+    a = _f32(rng.uniform(-1.1, 1.1, (B, L, D)))
+    g = _f32(rng.standard_normal((B, L, D)))
+    v = _f32(rng.standard_normal((B, L, D)))
+    w = rng.standard_normal((B, D))
+    hv, _ = oracle.f64(a, v, lib=lib)
+    _, db, _ = oracle.f64_backward(a, hv.astype(np.float32), g, None, None, want_da=False, lib=lib)
+    lhs, rhs = (g.astype(np.float64) * hv).sum(), (db * v).sum()
+    assert abs(lhs - rhs) <= 1e-10 * (1 + abs(lhs)), (lhs, rhs)
+    hw, _ = oracle.f64_carry(a, np.zeros_like(a), w, lib=lib)
+    _, _, dh0 = oracle.f64_backward(a, hw.astype(np.float32), g, w, None, lib=lib)
+    lhs, rhs = (g.astype(np.float64) * hw).sum(), (dh0 * w).sum()
+    assert abs(lhs - rhs) <= 1e-10 * (1 + abs(lhs)), (lhs, rhs)
+
+
+def pin_backward_closed_forms(lib):
+    """a = 1: db is the suffix sum of g (plus dh_last); a = 0: db = g; da_t = db_t * h_{t-1}."""
+    rng = _rng(22)
+    B, L, D = 2, 40, 3
+    g = _f32(rng.integers(-8, 9, (B, L, D)))
+    h = _f32(rng.integers(-8, 9, (B, L, D)))
+    w = rng.integers(-8, 9, (B, D)).astype(np.float64)
+    x = rng.integers(-8, 9, (B, D)).astype(np.float64)
+    da, db, dx = oracle.f64_backward(np.ones_like(g), h, g, x, w, lib=lib)
+    want = np.cumsum(g[:, ::-1].astype(np.float64), axis=1)[:, ::-1] + w[:, None, :]
+    assert np.array_equal(db, want), "suffix sums"
+    hprev = np.concatenate([x[:, None, :], h[:, :-1].astype(np.float64)], axis=1)
+    assert np.array_equal(da, want * hprev), "da = c * h_{t-1}"
+    assert np.array_equal(dx, want[:, 0, :]), "dh0 = a_0 c_0 with a_0 = 1"
+    da, db, dx = oracle.f64_backward(np.zeros_like(g), h, g, None, w, lib=lib)
+    want = g.astype(np.float64).copy()
+    want[:, -1, :] += w
+    assert np.array_equal(db, want), "a = 0: db = g"
+    assert np.all(da[:, 0, :] == 0), "no start state: da_0 = 0"
+
+
+def pin_backward_bruteforce(lib):
+    """db_s = sum_{t>=s} g_t a_{s+1}..a_t + w a_{s+1}..a_{L-1}, exactly."""
+    rng = _rng(23)
+    for L in (1, 2, 4, 7):
+        a = _f32(rng.uniform(-2, 2, (1, L, 2)))
+        g = _f32(rng.standard_normal((1, L, 2)))
+        w = rng.standard_normal((1, 2))
+        _, db, _ = oracle.f64_backward(a, np.zeros_like(a), g, None, w, want_da=False, lib=lib)
+        for d in range(2):
+            af = [Fraction(float(v)) for v in a[0, :, d]]
+            for s_ in range(L):
+                e = Fraction(0)
+                for t in range(s_, L):
+                    p = Fraction(1)
+                    for r in range(s_ + 1, t + 1):
+                        p *= af[r]
+                    e += p * Fraction(float(g[0, t, d]))
+                p = Fraction(1)
+                for r in range(s_ + 1, L):
+                    p *= af[r]
+                e += p * Fraction(float(w[0, d]))
+                assert abs(Fraction(float(db[0, s_, d])) - e) <= Fraction(1, 10 ** 12) * (1 + abs(e)), (L, s_, d)
+
+
 PINS = [pin_walkthrough, pin_prefix_sum, pin_copy, pin_running_product, pin_geometric, pin_bruteforce,
-        pin_carry_closed_forms, pin_carry_bruteforce, pin_carry_segments]
+        pin_carry_closed_forms, pin_carry_bruteforce, pin_carry_segments,
+        pin_backward_finite_differences, pin_backward_adjoint, pin_backward_closed_forms,
+        pin_backward_bruteforce]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -267,6 +370,10 @@ _CARRY_START = "hv = h0[i * D + d];"
 _CARRY_LAST = "if (hlast) hlast[i * D + d] = hv;"
 
 MUTANTS = {
+    "backward_slope_not_shifted": ("c = (double)g[k] + coef * c;", "c = (double)g[k] + (double)a[k] * c;"),
+    "backward_h_not_shifted": ("if (t > 0) hprev = (double)h[k - D];", "if (t > 0) hprev = (double)h[k];"),
+    "backward_dhlast_ignored": ("double c = dhlast ? dhlast[i * D + d] : 0.0;", "double c = 0.0;"),
+    "backward_dh0_without_a0": ("if (dh0) dh0[i * D + d] = coef * c;", "if (dh0) dh0[i * D + d] = c;"),
     "carry_state_ignored": (_CARRY_START, "hv = 0.0;"),
     "carry_state_negated": (_CARRY_START, "hv = -h0[i * D + d];"),
     "carry_last_state_wrong": (_CARRY_LAST, "if (hlast) hlast[i * D + d] = hv * 0.5;"),
