@@ -34,10 +34,18 @@ UNIT = "GB/s"
 WORKLOAD = "pages"          # the headline workload; --workload picks another for reports
 
 
-def metric_for(w) -> str:
+def metric_for(w, op: str = "forward") -> str:
+    if op == "backward":
+        return (f"scan backward GB/s (a,h,g read, da,db written) & % of GB300 HBM peak at "
+                f"B={w.B},L={w.L},D={w.D} fp32 ({w.name})")
     if w.name == WORKLOAD:
         return METRIC
     return f"scan GB/s (a,b,h bytes) & % of GB300 HBM peak at B={w.B},L={w.L},D={w.D} fp32 ({w.name})"
+
+
+def bytes_per_step(w, op: str) -> int:
+    # forward: read a, b, write h; backward: read a, h, g, write da, db (4 bytes each, once)
+    return (20 if op == "backward" else 12) * w.numel
 FALLBACK_HBM_GBS = 6800.0
 CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -185,6 +193,20 @@ def cpu_baseline(a, b, w, budget_s: float = 10.0):
             "sample": f"full {w.name} workload {w.shape}, fp64 sequential oracle, {reps} repetitions, {t_total:.1f} s"}
 
 
+def cpu_baseline_backward(a, h, g, w, nbytes, budget_s: float = 10.0):
+    """The oracle's reverse loop (single thread: it has no threaded form), for ~budget_s."""
+    import oracle
+    oracle.build()
+    reps, t_total = 0, 0.0
+    while t_total < budget_s and reps < 1000:
+        t0 = time.perf_counter()
+        oracle.f64_backward(a, h, g)
+        t_total += time.perf_counter() - t0
+        reps += 1
+    return {"value": nbytes * reps / t_total / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"full {w.name} workload {w.shape}, fp64 reverse loop, {reps} repetitions, {t_total:.1f} s"}
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -269,8 +291,22 @@ def run_ours(args):
     else:
         kernel_tag = "chunked_lookback" if plan["path_name"] == "chunked" else "regcarry"
 
+    if args.op == "backward":
+        lr.linrec_scan_f32(a, b, h, stream=stream)          # the forward output the gradient needs
+        g_cpu = inputs.generate(w.B, w.L, w.D, rank_seed(w.seed, rank) + 7, "u[0,1)", "n(0,1)")[1]
+        gd = g_cpu.to(dev)
+        da = torch.empty_like(a)
+        db = torch.empty_like(a)
+        plan = lr.linrec_plan_f32_backward(w.B, w.L, w.D,
+                                           sm_count=torch.cuda.get_device_properties(dev).multi_processor_count,
+                                           **opt)
+        kernel_tag = ("backward" if not plan["lookback"] else "backward_lookback") \
+            if plan["path_name"] == "chunked" else "regcarry_backward"
+
     def step():
-        if opt:
+        if args.op == "backward":
+            lr.linrec_scan_f32_backward(a, h, gd, da=da, db=db, stream=stream, **opt)
+        elif opt:
             lr.linrec_scan_f32_ex(a, b, h, stream=stream, **opt)
         else:
             lr.linrec_scan_f32(a, b, h, stream=stream)
@@ -303,17 +339,18 @@ def run_ours(args):
     if status != lr.LINREC_OK:
         raise SystemExit(f"device-side failure: {lr.linrec_status_string(status)}")
     seconds = max_over_ranks(elapsed_ms / 1e3, dev)
-    value = aggregate_gbs(w.algorithmic_bytes, world, args.steps, seconds)
+    nbytes = bytes_per_step(w, args.op)
+    value = aggregate_gbs(nbytes, world, args.steps, seconds)
 
     # roofline of the scan kernel (one launch per step)
     mean_launch_s = statistics.fmean(per_launch_ms) / 1e3
-    achieved = w.algorithmic_bytes / mean_launch_s / 1e9
+    achieved = nbytes / mean_launch_s / 1e9
     peak, peak_kind = hbm_peak()
     kernel = kernel_tag
     traffic = committed_traffic(kernel, w.name)
 
     # in-run copy ceiling over the same byte count: 1.5*N floats read and written
-    n_copy = w.numel * 3 // 2
+    n_copy = nbytes // 8
     src = torch.empty(n_copy, device=dev).uniform_()
     dst = torch.empty_like(src)
     copy_gbs = {}
@@ -334,7 +371,7 @@ def run_ours(args):
 
     # end to end through the public API: pinned host inputs in, result out, every step
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and args.op == "forward":
         a_h = a_cpu.pin_memory()
         b_h = b_cpu.pin_memory()
         h_h = torch.empty_like(a_cpu).pin_memory()
@@ -362,18 +399,24 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(a_cpu.numpy(), b_cpu.numpy(), w, budget_s=args.cpu_seconds)
+        if args.op == "backward":
+            cpu = cpu_baseline_backward(a_cpu.numpy(), h.cpu().numpy(), g_cpu.numpy(), w, nbytes,
+                                        budget_s=args.cpu_seconds)
+        else:
+            cpu = cpu_baseline(a_cpu.numpy(), b_cpu.numpy(), w, budget_s=args.cpu_seconds)
 
     if rank == 0:
         clk = clocks.summary()
         line = {
-            "metric": metric_for(w), "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "metric": metric_for(w, args.op), "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(seconds * 1e3 / args.steps, 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": w.about, "B": w.B, "L": w.L, "D": w.D, "seed": w.seed,
                        "global_batch": w.B * world,
-                       "l2": (f"inputs larger than L2: {w.algorithmic_bytes / 1e6:.0f} MB per step vs 129 MB L2, "
-                              "no flush") if w.algorithmic_bytes > 129e6 else "working set fits L2: small case",
+                       "op": args.op,
+                       "l2": (f"inputs larger than L2: {nbytes / 1e6:.0f} MB per step vs 129 MB L2, "
+                              "no flush") if nbytes > 129e6 else "working set fits L2: small case",
                        "path": plan["path_name"],
                        "plan": {k: plan[k] for k in ("vec", "prefetch", "tile_t", "tile_d", "segments", "stages",
                                                      "lookback", "threads", "grid")}},
@@ -381,7 +424,7 @@ def run_ours(args):
                          "frac": round(achieved / peak, 4), "traffic": traffic,
                          "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                          else "fallback 6.8 TB/s", "kernel": kernel,
-                         "algorithmic_bytes_per_launch": w.algorithmic_bytes},
+                         "algorithmic_bytes_per_launch": nbytes},
             "copy_ceiling_gbs": copy_gbs,
             "frac_of_copy_ceiling": round(value / ceiling, 4),
             "cpu_baseline": cpu,
@@ -407,6 +450,8 @@ def main(argv=None):
                    help="named workload (tiny, pages, long, gated, short, ...); pages is the headline")
     p.add_argument("--chunk-mode", choices=("auto", "own", "lookback"), default="auto")
     p.add_argument("--tile", default="", help="chunked tile as tile_d,tile_t,stages")
+    p.add_argument("--op", choices=("forward", "backward"), default="forward",
+                   help="forward scan (the headline) or its gradient")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0)

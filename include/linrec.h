@@ -115,6 +115,43 @@ linrec_status_t linrec_scan_f32_carry(const float *a, const float *b, float *h,
                                       int64_t B, int64_t L, int64_t D,
                                       const float *h_init, float *h_last, void *stream);
 
+/*
+ * linrec_scan_f32_backward -- the gradient of linrec_scan_f32_carry, for
+ * training.  The pages do not write it down; it follows from the definition
+ * above ("Kimi-K2.6 l1_p9", problem statement) by the chain rule.  With
+ * g = dL/dh (B, L, D) and c_t = dL/dh_t in total:
+ *
+ *     c_{L-1} = g_{L-1} + dh_last,    c_t = g_t + a_{t+1} * c_{t+1},
+ *     db_t = c_t,    da_t = c_t * h_{t-1},    dh_init = a_0 * c_0,
+ *
+ * with h_{-1} = h_init (or 0 when h_init is NULL: a_0 was unused, da_0 = 0).
+ * It is the same recurrence run right to left with the slope one step later,
+ * on the same kernels.  Pointers are device memory of the current device:
+ *   a, g        (B, L, D) in;  h (B, L, D) in: the forward output (needed
+ *               only for da; may be NULL when da is NULL);
+ *   da          (B, L, D) out or NULL (then h is not read: 12 bytes moved
+ *               per element instead of 20);  db (B, L, D) out;
+ *   h_init      (B, D) in or NULL: the forward's starting state;
+ *   dh_last     (B, D) in or NULL: gradient arriving at h[:, L-1, :] from
+ *               outside the scan (e.g. from a later segment's dh_init);
+ *   dh_init     (B, D) out or NULL: gradient of the starting state, to pass
+ *               to the earlier segment's dh_last when a long sequence was
+ *               scanned in segments.
+ * db may be the same buffer as g (updated in place); no other output may
+ * overlap an input or another output (LINREC_ERR_ALIAS).  Other conventions
+ * as for linrec_scan_f32.
+ */
+linrec_status_t linrec_scan_f32_backward(const float *a, const float *h, const float *g,
+                                         float *da, float *db, int64_t B, int64_t L, int64_t D,
+                                         const float *h_init, const float *dh_last, float *dh_init,
+                                         void *stream);
+
+/* linrec_scan_f32_backward with explicit options (path, chunk mode, tile, status word). */
+linrec_status_t linrec_scan_f32_backward_ex(const float *a, const float *h, const float *g,
+                                            float *da, float *db, int64_t B, int64_t L, int64_t D,
+                                            const float *h_init, const float *dh_last, float *dh_init,
+                                            void *stream, const linrec_options_t *opt);
+
 /* linrec_scan_f32 with explicit options (forced path, tile shape, status word, carry). */
 linrec_status_t linrec_scan_f32_ex(const float *a, const float *b, float *h,
                                    int64_t B, int64_t L, int64_t D, void *stream,
@@ -144,6 +181,10 @@ typedef struct {
  */
 linrec_status_t linrec_plan_f32(int64_t B, int64_t L, int64_t D, int sm_count, int align_bytes,
                                 int ctas_per_sm, const linrec_options_t *opt, linrec_plan_t *plan);
+
+/* The same for linrec_scan_f32_backward (its own tile table). */
+linrec_status_t linrec_plan_f32_backward(int64_t B, int64_t L, int64_t D, int sm_count, int align_bytes,
+                                         int ctas_per_sm, const linrec_options_t *opt, linrec_plan_t *plan);
 
 /*
  * linrec_stream_status -- synchronise `stream`, then return and clear the

@@ -13,6 +13,7 @@ Functions keep the C names:
     linrec_scan_f32(a, b, h=None, stream=None) -> h
     linrec_scan_f32_ex(a, b, h=None, stream=None, **options) -> h
     linrec_scan_f32_carry(a, b, h=None, h_init=None, h_last=None, stream=None) -> h
+    linrec_scan_f32_backward(a, h, g, da=None, db=None, h_init=None, dh_last=None, dh_init=None) -> (da, db)
     linrec_plan_f32(B, L, D, sm_count=152, align_bytes=16, resident_ctas=0, **options) -> dict
     linrec_stream_status(stream=None) -> int
     linrec_copy_f32(src, dst, stream=None)
@@ -106,6 +107,14 @@ def lib():
         L.linrec_plan_f32.restype = i32
         L.linrec_scan_f32_carry.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, vp]
         L.linrec_scan_f32_carry.restype = i32
+        L.linrec_scan_f32_backward.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, vp, vp, vp, vp]
+        L.linrec_scan_f32_backward.restype = i32
+        L.linrec_scan_f32_backward_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, vp, vp, vp, vp,
+                                                  ctypes.POINTER(Options)]
+        L.linrec_scan_f32_backward_ex.restype = i32
+        L.linrec_plan_f32_backward.argtypes = [i64, i64, i64, i32, i32, i32, ctypes.POINTER(Options),
+                                               ctypes.POINTER(Plan)]
+        L.linrec_plan_f32_backward.restype = i32
         L.linrec_stream_status.argtypes = [vp]
         L.linrec_stream_status.restype = i32
         L.linrec_copy_f32.argtypes = [vp, vp, i64, vp]
@@ -226,6 +235,47 @@ def linrec_scan_f32_carry(a, b, h=None, h_init=None, h_last=None, stream=None):
                                        _addr(h_last), _stream_handle(stream))
     _check(code, "linrec_scan_f32_carry")
     return h
+
+
+def linrec_scan_f32_backward(a, h, g, da=None, db=None, h_init=None, dh_last=None, dh_init=None, want_da=True,
+                             stream=None, **options):
+    """Gradient of the scan: returns (da, db).  With want_da=False, da is None and h is not read
+    (h may then be None).  dh_init (B, D), if given, receives the gradient of the starting state."""
+    import torch
+    B, L, D = _shape_of(a, g, None)
+    if want_da or da is not None:
+        if h is None:
+            raise ValueError("h (the forward output) is needed for da")
+        _shape_of(a, h, None)
+        if da is None:
+            da = torch.empty_like(a)
+        _shape_of(a, da, None)
+    if db is None:
+        db = torch.empty_like(a)
+    _shape_of(a, db, None)
+    for name, x in (("h_init", h_init), ("dh_last", dh_last), ("dh_init", dh_init)):
+        _check_state(x, name, B, D)
+    args = (a.data_ptr(), _addr(h) if da is not None else None, g.data_ptr(), _addr(da), db.data_ptr(), B, L, D,
+            _addr(h_init), _addr(dh_last), _addr(dh_init), _stream_handle(stream))
+    if options:
+        opt = make_options(**options)
+        code = lib().linrec_scan_f32_backward_ex(*args, ctypes.byref(opt))
+    else:
+        code = lib().linrec_scan_f32_backward(*args)
+    _check(code, "linrec_scan_f32_backward")
+    return da, db
+
+
+def linrec_plan_f32_backward(B, L, D, sm_count=152, align_bytes=16, resident_ctas=0, **options) -> dict:
+    """The dispatcher's choice for the gradient of a (B, L, D) scan, without a GPU."""
+    opt = make_options(**options)
+    plan = Plan()
+    code = lib().linrec_plan_f32_backward(int(B), int(L), int(D), int(sm_count), int(align_bytes),
+                                          int(resident_ctas), ctypes.byref(opt), ctypes.byref(plan))
+    _check(code, "linrec_plan_f32_backward")
+    out = {name: getattr(plan, name) for name, _ in Plan._fields_}
+    out["path_name"] = PATH_NAMES.get(out["path"], "none")
+    return out
 
 
 def linrec_plan_f32(B, L, D, sm_count=152, align_bytes=16, resident_ctas=0, **options) -> dict:

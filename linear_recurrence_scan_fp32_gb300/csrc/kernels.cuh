@@ -70,6 +70,31 @@ struct ChunkedLaunch {
 cudaError_t chunked_ctas_per_sm(const ChunkedVariant *v, int *ctas);
 cudaError_t launch_chunked(const ChunkedLaunch &args, cudaStream_t stream);
 
+// ---- backward (gradient) kernels -----------------------------------------------
+// c_t = g_t + a_{t+1} c_{t+1} (c_{L-1} = g_{L-1} + dh_last), db = c,
+// da_t = c_t h_{t-1} (h_{-1} = h_init or 0), dh_init = a_0 c_0.
+struct BackwardLaunch {
+    const ChunkedVariant *variant;
+    CUtensorMap map_g, map_a, map_h;   // 3-D {D, L, B} maps of g, a and h (h unused without da)
+    const float *a;                    // for a_0 in dh_init
+    float *da = nullptr, *db = nullptr;
+    int64_t L, D, slices_per_batch, n_slices, chunks, n_tiles, grid;
+    bool own;
+    Control *ctrl;
+    unsigned long long *words;
+    unsigned int *status;
+    int64_t spin_limit;
+    int64_t silent_tile;
+    const float *h_init = nullptr, *dh_last = nullptr;
+    float *dh_init = nullptr;
+};
+const ChunkedVariant *backward_variants(int *count);
+cudaError_t backward_ctas_per_sm(const ChunkedVariant *v, int *ctas);
+cudaError_t launch_backward(const BackwardLaunch &args, cudaStream_t stream);
+cudaError_t launch_regcarry_backward(int vec, int threads, const float *a, const float *h, const float *g, float *da,
+                                     float *db, int64_t B, int64_t L, int64_t D, const float *h_init,
+                                     const float *dh_last, float *dh_init, cudaStream_t stream);
+
 // ---- copy-ceiling kernel ---------------------------------------------------
 cudaError_t launch_copy(const float *src, float *dst, int64_t n, int sm_count, cudaStream_t stream);
 

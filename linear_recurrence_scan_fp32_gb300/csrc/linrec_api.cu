@@ -25,6 +25,7 @@ struct DeviceInfo {
     bool supported = false;
     int sm_count = 0;
     int ctas_per_sm[64] = {};               // per chunked variant, 0 = not queried yet
+    int back_ctas_per_sm[64] = {};          // per backward variant
 };
 
 std::mutex g_mu;
@@ -69,9 +70,9 @@ linrec_status_t check_sizes(int64_t B, int64_t L, int64_t D, int64_t *n_out) {
     return LINREC_OK;
 }
 
-const ChunkedVariant *find_variant(int tile_d, int tile_t, int stages, int *index) {
+const ChunkedVariant *find_variant(int tile_d, int tile_t, int stages, int *index, bool backward) {
     int n = 0;
-    const ChunkedVariant *v = chunked_variants(&n);
+    const ChunkedVariant *v = backward ? backward_variants(&n) : chunked_variants(&n);
     for (int i = 0; i < n; ++i) {
         if (v[i].tile_d == tile_d && v[i].tile_t == tile_t && (stages == 0 || v[i].stages == stages)) {
             if (index) *index = i;
@@ -84,14 +85,21 @@ const ChunkedVariant *find_variant(int tile_d, int tile_t, int stages, int *inde
 // Default chunked tile.  Slice-owner mode: narrow 32-channel slices (more
 // slices to spread over the SMs) with a 3-deep ring.  Look-back mode: the
 // widest slice D fills, so fewer tiles take part in each carry chain.
-void default_tile(int64_t D, bool own, int *tile_d, int *tile_t, int *stages) {
+void default_tile(int64_t D, bool own, bool backward, int *tile_d, int *tile_t, int *stages) {
+    if (backward) {   // three boxes per stage
+        if (own) { *tile_d = 32; *tile_t = 128; *stages = 2; return; }
+        if (D >= 64) { *tile_d = 64; *tile_t = 128; *stages = 2; }
+        else { *tile_d = 32; *tile_t = 128; *stages = 2; }
+        return;
+    }
     if (own) { *tile_d = 32; *tile_t = 128; *stages = 3; return; }
     if (D >= 64) { *tile_d = 64; *tile_t = 128; *stages = 2; }
     else { *tile_d = 32; *tile_t = 128; *stages = 3; }
 }
 
 linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int align_bytes, int ctas_per_sm,
-                          const linrec_options_t *opt, linrec_plan_t *plan, int *variant_index) {
+                          const linrec_options_t *opt, linrec_plan_t *plan, int *variant_index,
+                          bool backward = false) {
     linrec_options_t none = {};
     if (!opt) opt = &none;
     if (!plan || sm_count <= 0) return LINREC_ERR_INVALID_VALUE;
@@ -142,13 +150,13 @@ linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int ali
     int tile_d = opt->tile_d, tile_t = opt->tile_t, stages = opt->stages;
     if (tile_d == 0 || tile_t == 0) {
         int dd, dt, ds;
-        default_tile(D, own, &dd, &dt, &ds);
+        default_tile(D, own, backward, &dd, &dt, &ds);
         if (tile_d == 0) tile_d = dd;
         if (tile_t == 0) tile_t = dt;
         if (stages == 0) stages = ds;
     }
-    const ChunkedVariant *v = find_variant(tile_d, tile_t, stages, variant_index);
-    if (!v && opt->stages == 0) v = find_variant(tile_d, tile_t, 0, variant_index);
+    const ChunkedVariant *v = find_variant(tile_d, tile_t, stages, variant_index, backward);
+    if (!v && opt->stages == 0) v = find_variant(tile_d, tile_t, 0, variant_index, backward);
     if (!v) return LINREC_ERR_INVALID_VALUE;
     plan->lookback = own ? 0 : 1;
     plan->tile_d = v->tile_d;
@@ -355,6 +363,116 @@ linrec_status_t linrec_scan_f32_ex(const float *a, const float *b, float *h, int
 linrec_status_t linrec_scan_f32(const float *a, const float *b, float *h, int64_t B, int64_t L, int64_t D,
                                 void *stream) {
     return linrec_scan_f32_ex(a, b, h, B, L, D, stream, nullptr);
+}
+
+linrec_status_t linrec_plan_f32_backward(int64_t B, int64_t L, int64_t D, int sm_count, int align_bytes,
+                                         int ctas_per_sm, const linrec_options_t *opt, linrec_plan_t *plan) {
+    return plan_impl(B, L, D, sm_count, align_bytes, ctas_per_sm, opt, plan, nullptr, true);
+}
+
+linrec_status_t linrec_scan_f32_backward_ex(const float *a, const float *h, const float *g, float *da, float *db,
+                                            int64_t B, int64_t L, int64_t D, const float *h_init,
+                                            const float *dh_last, float *dh_init, void *stream_ptr,
+                                            const linrec_options_t *opt) {
+    linrec_options_t none = {};
+    if (!opt) opt = &none;
+    int64_t n = 0;
+    linrec_status_t st = check_sizes(B, L, D, &n);
+    if (st != LINREC_OK) return st;
+    if (n == 0) return LINREC_OK;
+    if (!a || !g || !db || (da && !h)) return LINREC_ERR_INVALID_VALUE;
+    const int64_t nb = n * 4, sb = B * D * 4;
+    // outputs against inputs and each other; db may be g itself
+    struct R { const void *p; int64_t bytes; };
+    const R ins[] = {{a, nb}, {da ? h : nullptr, nb}, {g, nb}, {h_init, sb}, {dh_last, sb}};
+    const R outs[] = {{da, nb}, {db, nb}, {dh_init, sb}};
+    for (int i = 0; i < 3; ++i) {
+        if (!outs[i].p) continue;
+        for (int j = 0; j < 5; ++j) {
+            if (!ins[j].p) continue;
+            if (i == 1 && j == 2 && db == g) continue;
+            if (overlaps(outs[i].p, outs[i].bytes, ins[j].p, ins[j].bytes)) return LINREC_ERR_ALIAS;
+        }
+        for (int j = i + 1; j < 3; ++j)
+            if (outs[j].p && overlaps(outs[i].p, outs[i].bytes, outs[j].p, outs[j].bytes)) return LINREC_ERR_ALIAS;
+    }
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return LINREC_ERR_LAUNCH;
+    }
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceInfo *di = device_info(dev);
+    if (!di) return LINREC_ERR_LAUNCH;
+    if (!di->supported) return LINREC_ERR_UNSUPPORTED_DEVICE;
+
+    const uintptr_t u = reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(g) |
+                        reinterpret_cast<uintptr_t>(db) | (da ? reinterpret_cast<uintptr_t>(da) |
+                                                                reinterpret_cast<uintptr_t>(h) : 0u);
+    const int align = (u & 15u) == 0 ? 16 : (u & 7u) == 0 ? 8 : 4;
+    linrec_plan_t plan;
+    int vi = -1;
+    st = plan_impl(B, L, D, di->sm_count, align, 0, opt, &plan, &vi, true);
+    if (st != LINREC_OK) return st;
+    if (plan.path == LINREC_PATH_REGCARRY) {
+        cudaError_t err = launch_regcarry_backward(plan.vec, plan.threads, a, h, g, da, db, B, L, D, h_init, dh_last,
+                                                   dh_init, stream);
+        return err == cudaSuccess ? LINREC_OK : LINREC_ERR_LAUNCH;
+    }
+    int nvar = 0;
+    const ChunkedVariant *variants = backward_variants(&nvar);
+    if (vi < 0 || vi >= 64) return LINREC_ERR_INVALID_VALUE;
+    if (di->back_ctas_per_sm[vi] == 0) {
+        int c = 0;
+        if (backward_ctas_per_sm(&variants[vi], &c) != cudaSuccess || c <= 0) {
+            cudaGetLastError();
+            return LINREC_ERR_LAUNCH;
+        }
+        di->back_ctas_per_sm[vi] = c;
+    }
+    st = plan_impl(B, L, D, di->sm_count, align, di->back_ctas_per_sm[vi], opt, &plan, &vi, true);
+    if (st != LINREC_OK) return st;
+    if (!get_encoder()) return LINREC_ERR_LAUNCH;
+    BackwardLaunch p;
+    p.variant = &variants[vi];
+    if (!encode_map(&p.map_g, g, B, L, D, plan.tile_d, plan.tile_t) ||
+        !encode_map(&p.map_a, a, B, L, D, plan.tile_d, plan.tile_t) ||
+        !encode_map(&p.map_h, da ? h : a, B, L, D, plan.tile_d, plan.tile_t))
+        return LINREC_ERR_LAUNCH;
+    Slot *ws = workspace(dev, stream, plan.workspace_bytes);
+    if (!ws) return LINREC_ERR_WORKSPACE;
+    p.a = a;
+    p.da = da;
+    p.db = db;
+    p.L = L;
+    p.D = D;
+    p.slices_per_batch = (D + plan.tile_d - 1) / plan.tile_d;
+    p.n_slices = B * p.slices_per_batch;
+    p.chunks = plan.chunks;
+    p.n_tiles = plan.n_tiles;
+    p.grid = plan.grid;
+    p.own = plan.lookback == 0;
+    p.ctrl = reinterpret_cast<Control *>(ws->base);
+    p.words = reinterpret_cast<unsigned long long *>(ws->base + kWorkspaceHead);
+    p.status = opt->d_status ? opt->d_status : &p.ctrl->status;
+    p.spin_limit = opt->spin_limit > 0 ? opt->spin_limit : kDefaultSpinLimit;
+    p.silent_tile = opt->test_silent_tile > 0 ? opt->test_silent_tile - 1 : -1;
+    p.h_init = h_init;
+    p.dh_last = dh_last;
+    p.dh_init = dh_init;
+    cudaError_t err = launch_backward(p, stream);
+    if (err != cudaSuccess) {
+        cudaGetLastError();
+        return LINREC_ERR_LAUNCH;
+    }
+    return LINREC_OK;
+}
+
+linrec_status_t linrec_scan_f32_backward(const float *a, const float *h, const float *g, float *da, float *db,
+                                         int64_t B, int64_t L, int64_t D, const float *h_init,
+                                         const float *dh_last, float *dh_init, void *stream) {
+    return linrec_scan_f32_backward_ex(a, h, g, da, db, B, L, D, h_init, dh_last, dh_init, stream, nullptr);
 }
 
 linrec_status_t linrec_scan_f32_carry(const float *a, const float *b, float *h, int64_t B, int64_t L, int64_t D,

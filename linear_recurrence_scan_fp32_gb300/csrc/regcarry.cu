@@ -103,7 +103,105 @@ cudaError_t launch_one(int threads, const float *a, const float *b, float *h, in
     return cudaGetLastError();
 }
 
+template <typename T, int V> __device__ __forceinline__ float &lane_of(T &v, int i) {
+    return reinterpret_cast<float *>(&v)[i];
+}
+
+// Gradient, right to left: c_t = a_{t+1} c_{t+1} + g_t; db_t = c_t; da_t = c_t h_{t-1}.
+// The ring holds (g_t, a_{t+1}, h_{t-1}) for the next P steps down.
+template <int V, int P>
+__global__ void __launch_bounds__(256)
+regcarry_backward_kernel(const float *__restrict__ a, const float *__restrict__ h, const float *__restrict__ g,
+                         float *__restrict__ da, float *__restrict__ db, const long long L, const long long D,
+                         const long long groups_per_batch, const long long n_groups, const float *h_init,
+                         const float *dh_last, float *dh_init)
+{
+    using vec = typename VecT<V>::type;
+    const long long gi = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (gi >= n_groups) return;
+    const long long bi = gi / groups_per_batch;
+    const long long dch = (gi - bi * groups_per_batch) * V;
+    const long long off = bi * L * D + dch;
+    const vec *pa = reinterpret_cast<const vec *>(a + off);
+    const vec *ph = reinterpret_cast<const vec *>(h + off);
+    const vec *pg = reinterpret_cast<const vec *>(g + off);
+    vec *pda = reinterpret_cast<vec *>(da + off);
+    vec *pdb = reinterpret_cast<vec *>(db + off);
+    const long long stride = D / V;
+    const bool want_da = da != nullptr;
+    vec one, zv;
+    zero(zv);
+#pragma unroll
+    for (int v = 0; v < V; ++v) lane_of<vec, V>(one, v) = 1.0f;
+
+    auto load = [&](long long t, vec &rg, vec &ra, vec &rh) {
+        rg = ld_stream(pg + t * stride);
+        ra = (t + 1 < L) ? ld_stream(pa + (t + 1) * stride) : one;   // the carry enters row L-1 whole
+        rh = (want_da && t >= 1) ? ld_stream(ph + (t - 1) * stride) : zv;
+    };
+    vec rg[P], ra[P], rh[P];
+#pragma unroll
+    for (int j = 0; j < P; ++j)
+        if (L - 1 - j >= 0) load(L - 1 - j, rg[j], ra[j], rh[j]);
+    vec cv;
+    zero(cv);
+    if (dh_last) {
+#pragma unroll
+        for (int v = 0; v < V; ++v) lane_of<vec, V>(cv, v) = dh_last[bi * D + dch + v];
+    }
+    for (long long t0 = 0; t0 < L; t0 += P) {
+#pragma unroll
+        for (int j = 0; j < P; ++j) {
+            const long long t = L - 1 - (t0 + j);
+            if (t >= 0) {
+                cv = step(ra[j], cv, rg[j]);
+                st_stream(pdb + t * stride, cv);
+                if (want_da) {
+                    vec hp = rh[j];
+                    if (t == 0) {
+#pragma unroll
+                        for (int v = 0; v < V; ++v)
+                            lane_of<vec, V>(hp, v) = h_init ? h_init[bi * D + dch + v] : 0.0f;
+                    }
+                    vec out;
+#pragma unroll
+                    for (int v = 0; v < V; ++v) lane_of<vec, V>(out, v) = lane_of<vec, V>(cv, v) * lane_of<vec, V>(hp, v);
+                    st_stream(pda + t * stride, out);
+                }
+                if (t == 0 && dh_init) {
+#pragma unroll
+                    for (int v = 0; v < V; ++v)
+                        dh_init[bi * D + dch + v] = a[off + v] * lane_of<vec, V>(cv, v);
+                }
+                const long long tn = t - P;
+                if (tn >= 0) load(tn, rg[j], ra[j], rh[j]);
+            }
+        }
+    }
+}
+
+template <int V>
+cudaError_t launch_back_one(int threads, const float *a, const float *h, const float *g, float *da, float *db,
+                            int64_t B, int64_t L, int64_t D, const float *h_init, const float *dh_last,
+                            float *dh_init, cudaStream_t stream) {
+    const long long gpb = D / V;
+    const long long n = B * gpb;
+    const long long blocks = (n + threads - 1) / threads;
+    regcarry_backward_kernel<V, 8><<<(unsigned)blocks, threads, 0, stream>>>(a, h, g, da, db, L, D, gpb, n, h_init,
+                                                                             dh_last, dh_init);
+    return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_regcarry_backward(int vec, int threads, const float *a, const float *h, const float *g, float *da,
+                                     float *db, int64_t B, int64_t L, int64_t D, const float *h_init,
+                                     const float *dh_last, float *dh_init, cudaStream_t stream) {
+    if (vec == 4) return launch_back_one<4>(threads, a, h, g, da, db, B, L, D, h_init, dh_last, dh_init, stream);
+    if (vec == 2) return launch_back_one<2>(threads, a, h, g, da, db, B, L, D, h_init, dh_last, dh_init, stream);
+    if (vec == 1) return launch_back_one<1>(threads, a, h, g, da, db, B, L, D, h_init, dh_last, dh_init, stream);
+    return cudaErrorInvalidValue;
+}
 
 bool regcarry_supported(int vec, int prefetch) {
     return (vec == 1 || vec == 2 || vec == 4) && (prefetch == 4 || prefetch == 8 || prefetch == 16);
