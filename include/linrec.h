@@ -152,6 +152,27 @@ linrec_status_t linrec_scan_f32_backward_ex(const float *a, const float *h, cons
                                             const float *h_init, const float *dh_last, float *dh_init,
                                             void *stream, const linrec_options_t *opt);
 
+/*
+ * linrec_scan_f32_host -- the scan on HOST buffers a, b (read) and h (written),
+ * row-major (B, L, D) like the device entry points.
+ *  - When a, b and h are all page-locked host memory the device can address
+ *    (cudaHostAlloc, cudaHostRegister), the kernels read and write them in
+ *    place over the host link: no copies, no device memory.
+ *  - Otherwise the library moves the data itself: the problem is cut into
+ *    pieces of about 48 MB (whole sequences of a few batch indices, or, for
+ *    long sequences, runs of time steps chained through the carry of
+ *    linrec_scan_f32_carry), and the copy to the device, the scan and the
+ *    copy back of successive pieces overlap on three internal streams
+ *    through a ring of three device slots, allocated on first use and kept
+ *    per device.
+ * Either way the work starts after what is already queued on `stream` and
+ * `stream` waits for its end: synchronise `stream` before reading h, and keep
+ * a, b, h alive until then.  h must not overlap a or b (LINREC_ERR_ALIAS).
+ * Pipelined calls are serialised per device by the library.
+ */
+linrec_status_t linrec_scan_f32_host(const float *a, const float *b, float *h,
+                                     int64_t B, int64_t L, int64_t D, void *stream);
+
 /* linrec_scan_f32 with explicit options (forced path, tile shape, status word, carry). */
 linrec_status_t linrec_scan_f32_ex(const float *a, const float *b, float *h,
                                    int64_t B, int64_t L, int64_t D, void *stream,

@@ -14,6 +14,7 @@ Functions keep the C names:
     linrec_scan_f32_ex(a, b, h=None, stream=None, **options) -> h
     linrec_scan_f32_carry(a, b, h=None, h_init=None, h_last=None, stream=None) -> h
     linrec_scan_f32_backward(a, h, g, da=None, db=None, h_init=None, dh_last=None, dh_init=None) -> (da, db)
+    linrec_scan_f32_host(a, b, h=None, stream=None) -> h   (host tensors; pipelined copies)
     linrec_plan_f32(B, L, D, sm_count=152, align_bytes=16, resident_ctas=0, **options) -> dict
     linrec_stream_status(stream=None) -> int
     linrec_copy_f32(src, dst, stream=None)
@@ -115,6 +116,8 @@ def lib():
         L.linrec_plan_f32_backward.argtypes = [i64, i64, i64, i32, i32, i32, ctypes.POINTER(Options),
                                                ctypes.POINTER(Plan)]
         L.linrec_plan_f32_backward.restype = i32
+        L.linrec_scan_f32_host.argtypes = [vp, vp, vp, i64, i64, i64, vp]
+        L.linrec_scan_f32_host.restype = i32
         L.linrec_stream_status.argtypes = [vp]
         L.linrec_stream_status.restype = i32
         L.linrec_copy_f32.argtypes = [vp, vp, i64, vp]
@@ -276,6 +279,25 @@ def linrec_plan_f32_backward(B, L, D, sm_count=152, align_bytes=16, resident_cta
     out = {name: getattr(plan, name) for name, _ in Plan._fields_}
     out["path_name"] = PATH_NAMES.get(out["path"], "none")
     return out
+
+
+def linrec_scan_f32_host(a, b, h=None, stream=None):
+    """The scan on CPU tensors (pinned memory for full speed): the library pipelines the copies to the
+    device, the kernels and the copies back.  Returns h (a CPU tensor, pinned if a is); it is complete
+    once `stream` (default: the current CUDA stream) is synchronised."""
+    import torch
+    for name, t in (("a", a), ("b", b)) + ((("h", h),) if h is not None else ()):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or t.is_cuda or t.dim() != 3 \
+                or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous float32 CPU tensor of shape (B, L, D)")
+    if a.shape != b.shape or (h is not None and h.shape != a.shape):
+        raise ValueError("a, b and h must have the same shape")
+    if h is None:
+        h = torch.empty(a.shape, dtype=torch.float32, pin_memory=a.is_pinned())
+    B, L, D = a.shape
+    code = lib().linrec_scan_f32_host(a.data_ptr(), b.data_ptr(), h.data_ptr(), B, L, D, _stream_handle(stream))
+    _check(code, "linrec_scan_f32_host")
+    return h
 
 
 def linrec_plan_f32(B, L, D, sm_count=152, align_bytes=16, resident_ctas=0, **options) -> dict:

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "liblinrec.so")
-SOURCES = ["linrec_api.cu", "chunked.cu", "backward.cu", "regcarry.cu", "copy.cu", "noalloc.cu"]
+SOURCES = ["linrec_api.cu", "chunked.cu", "backward.cu", "regcarry.cu", "copy.cu", "noalloc.cu", "host_pipeline.cu"]
 HEADERS = ["kernels.cuh", "ptx.cuh", "lookback.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
