@@ -81,7 +81,9 @@ typedef struct {
     int ctas_per_sm;     /* chunked: cap on resident CTAs per SM (0 = as many as fit) */
     int chunk_mode;      /* chunked: 1 = each CTA owns whole channel slices and carries h from
                             chunk to chunk itself; 2 = chunks of a slice spread over CTAs, joined
-                            by the decoupled look-back; 0 = the dispatcher's choice */
+                            by the decoupled look-back; 3 = two passes (forward scan only): a
+                            launch writes every chunk's aggregate, the aggregates are scanned,
+                            a launch applies them; 0 = the dispatcher's choice */
     unsigned int *d_status; /* device word (may be NULL): the kernel ORs 1 << linrec_status_t
                                into it on a device-side failure; otherwise the stream's own word
                                is used (read it with linrec_stream_status) */
@@ -183,7 +185,9 @@ typedef struct {
     int path;              /* LINREC_PATH_REGCARRY or LINREC_PATH_CHUNKED */
     int vec, prefetch;     /* regcarry parameters */
     int tile_t, tile_d, segments, stages; /* chunked parameters */
-    int lookback;          /* chunked: 1 = look-back mode, 0 = slice-owner mode */
+    int lookback;          /* chunked: 1 = look-back mode */
+    int twopass;           /* chunked: 1 = two-pass mode (reduce, scan of aggregates, apply);
+                              lookback = twopass = 0: slice-owner mode */
     int threads;           /* threads per CTA */
     int64_t grid;          /* CTAs launched */
     int64_t n_tiles;       /* chunked: tiles of tile_t x tile_d */

@@ -76,6 +76,7 @@ class Plan(ctypes.Structure):
         ("segments", ctypes.c_int),
         ("stages", ctypes.c_int),
         ("lookback", ctypes.c_int),
+        ("twopass", ctypes.c_int),
         ("threads", ctypes.c_int),
         ("grid", ctypes.c_int64),
         ("n_tiles", ctypes.c_int64),
@@ -139,7 +140,7 @@ def _check(code: int, what: str):
         raise LinrecError(code, f"{what}: {linrec_status_string(code)}")
 
 
-CHUNK_MODES = {"auto": 0, "own": 1, "lookback": 2}
+CHUNK_MODES = {"auto": 0, "own": 1, "lookback": 2, "twopass": 3}
 
 
 def _addr(x):

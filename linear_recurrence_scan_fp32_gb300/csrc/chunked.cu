@@ -27,6 +27,13 @@
 //         its slice to the nearest inclusive value (S lanes per channel, a
 //         window of S*R tiles per round trip), replays the chain forward from
 //         it and publishes its own inclusive value.
+//       two-pass mode (few slices, long L; three launches): a reduce launch
+//         writes every tile's aggregate, the library scans those aggregates
+//         (a problem 1/TT the size, with these same kernels), and an apply
+//         launch gives each tile the inclusive value of the tile before it.
+//         Tiles are independent in both launches; the apply launch visits
+//         them in reverse order so the inputs the reduce launch read last
+//         are still in L2.
 //  5. Every thread replays its K steps from h_in = A_prefix * carry + B_prefix
 //     and stores h.
 //
@@ -72,7 +79,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
                     const long long L, const long long D,
                     const long long slices_per_batch, const long long n_slices,
                     const long long chunks, const long long n_tiles,
-                    const int own,               // 1: slice-owner mode, 0: look-back mode
+                    const int mode,              // kModeLookback, kModeOwn, kModeReduce or kModeApply
                     Control *__restrict__ ctrl, unsigned long long *__restrict__ words,
                     unsigned int *__restrict__ status,
                     const long long spin_limit, const long long silent_tile,
@@ -81,6 +88,16 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
     constexpr int K = TT / S;                 // time steps per thread
     constexpr int R = (S >= 4) ? 16 / S : 4;  // look-back: predecessors per lane
     constexpr uint32_t kStageBytes = 2u * TT * TD * sizeof(float);
+    const bool own = mode == kModeOwn;
+    const bool lookback = mode == kModeLookback;
+    const bool reduce = mode == kModeReduce;
+    const bool apply = mode == kModeApply;
+    // two-pass mode: per-tile aggregates and the scanned inclusive values, indexed [tile id][channel],
+    // and each channel's starting state, indexed [slice][channel]
+    float *const tileA = reinterpret_cast<float *>(words);
+    float *const tileB = tileA + n_tiles * TD;
+    const float *const tileH = tileB + n_tiles * TD;
+    float *const tileX = tileB + 2 * n_tiles * TD;
     static_assert(TT % S == 0 && TD % 32 == 0 && (32 % S) == 0 && S >= 2 && ST >= 2, "tile shape");
     using Smem = ChunkSmem<TD, TT, S, ST>;
     extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -110,8 +127,16 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
     // (thread 0) the CTA's next tile.  Slice-owner mode: slices blockIdx.x,
     // blockIdx.x + gridDim.x, ... each walked from chunk 0 to chunks-1, tracked
     // in (own_slice, own_q).  Look-back mode: the next id from the tile counter.
-    long long own_slice = blockIdx.x, own_q = 0;
+    long long own_slice = blockIdx.x, own_q = 0, own_m = 0;
     auto next_tile = [&](long long &q, long long &slice) -> long long {
+        if (reduce || apply) {                // independent tiles, static round-robin
+            const long long k = blockIdx.x + (own_m++) * (long long)gridDim.x;
+            if (k >= n_tiles) return n_tiles;
+            const long long id = apply ? n_tiles - 1 - k : k;
+            q = id / n_slices;
+            slice = id - q * n_slices;
+            return id;
+        }
         if (own) {
             if (own_slice >= n_slices) return n_tiles;
             q = own_q;
@@ -133,13 +158,13 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
         long long first = n_tiles;
         if (misaligned) {
             atomicOr(status, kStatusTmaTimeout);
-            if (!own) atomicExch(&ctrl->abort, 1u);
+            if (lookback) atomicExch(&ctrl->abort, 1u);
         } else {
             for (int st = 0; st < ST; ++st) mbar_init(&sm.full[st], 1);
             mbar_fence_init();
             tmap_prefetch(&map_a);
             tmap_prefetch(&map_b);
-            if (!own) {
+            if (lookback) {
                 const uint32_t tag = ld_relaxed_u32(&ctrl->epoch) + 1u;
                 sm.tag = tag == 0 ? 1u : tag;
             }
@@ -154,7 +179,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
     }
     __syncthreads();
 
-    const uint32_t tag = own ? 0u : sm.tag;
+    const uint32_t tag = lookback ? sm.tag : 0u;
     uint32_t phases = 0;                      // bit st: parity of the next completion of stage st
     long long next_fill = 1;                  // (thread 0) next ring slot to fill
     bool ended = sm.tile[0].id >= n_tiles;    // (thread 0) no more tiles to take
@@ -170,7 +195,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
 
         if (!mbar_wait_bounded(&sm.full[st], (phases >> st) & 1u, kTmaPolls)) {
             atomicOr(status, kStatusTmaTimeout);
-            if (!own) atomicExch(&ctrl->abort, 1u);
+            if (lookback) atomicExch(&ctrl->abort, 1u);
         }
         phases ^= 1u << st;
 
@@ -196,7 +221,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
                 }
                 ++next_fill;
             }
-            if (!own) {
+            if (lookback) {
                 if (!ended && ahead < 0) ahead = next_tile(ahead_q, ahead_slice);
                 abort_seen = ld_relaxed_u32(&ctrl->abort);
             }
@@ -259,6 +284,18 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
                 run = fmaf(tA, carry, tB);
                 sm.carry[cc] = carry;
             }
+        } else if (reduce) {
+            // the tile's map; the first chunk's absorbs the carried-in state, so the scan of
+            // these maps from 0 is the chain of inclusive values
+            if (ss == 0) {
+                tileA[id * TD + cc] = (q == 0) ? 0.0f : tA;
+                tileB[id * TD + cc] = (q == 0) ? fmaf(tA, h_before, tB) : tB;
+                // kept for the apply launch: h_last may be the same buffer as h_init, and the
+                // apply launch writes it while other tiles still need the starting state
+                if (q == 0) tileX[id * TD + cc] = h_before;
+            }
+        } else if (apply) {
+            if (ss == 0) sm.carry[cc] = (q == 0) ? tileX[id * TD + cc] : tileH[(id - n_slices) * TD + cc];
         } else {
             const bool publish = (q + 1 < chunks) && (id != silent_tile);
             float carry = h_before;
@@ -274,7 +311,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
 
         // ---- 5. replay the steps from the carried value, store h -----------------
         float hc = fmaf(sm.segA[s][c], sm.carry[c], sm.segB[s][c]);
-        if ((d0 + c) < D) {
+        if (!reduce && (d0 + c) < D) {
             float *hp = h + ((bi * L + t0 + r0) * D + d0 + c);
             if (nv == K) {
 #pragma unroll
@@ -299,7 +336,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
 
     // Look-back mode: the last CTA to finish resets the counters and advances the
     // epoch for the next launch on this workspace.
-    if (!own) {
+    if (lookback) {
         __syncthreads();
         if (tid == 0) {
             __threadfence();
@@ -371,14 +408,14 @@ cudaError_t launch_chunked(const ChunkedLaunch &p, cudaStream_t stream) {
     if (err != cudaSuccess) return err;
     long long L = p.L, D = p.D, spb = p.slices_per_batch, ns = p.n_slices, ch = p.chunks, nt = p.n_tiles;
     long long spin = p.spin_limit, silent = p.silent_tile;
-    int own = p.own ? 1 : 0;
+    int mode = p.mode;
     float *h = p.h;
     Control *ctrl = p.ctrl;
     unsigned long long *words = p.words;
     unsigned int *status = p.status;
     const float *h_init = p.h_init;
     float *h_last = p.h_last;
-    void *args[] = {(void *)&p.map_a, (void *)&p.map_b, &h, &L, &D, &spb, &ns, &ch, &nt, &own,
+    void *args[] = {(void *)&p.map_a, (void *)&p.map_b, &h, &L, &D, &spb, &ns, &ch, &nt, &mode,
                     &ctrl, &words, &status, &spin, &silent, &h_init, &h_last};
     return cudaLaunchKernel(fn, dim3((unsigned)p.grid), dim3((unsigned)p.variant->threads), args,
                             p.variant->smem_bytes, stream);

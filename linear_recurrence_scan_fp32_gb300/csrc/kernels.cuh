@@ -47,6 +47,12 @@ struct ChunkedVariant {
 // The compiled variants (tile_d, tile_t, segments, stages combinations).
 const ChunkedVariant *chunked_variants(int *count);
 
+// How the chunked forward kernel gets each tile's carry.
+constexpr int kModeLookback = 0;   // tiles of a slice on different CTAs, decoupled look-back
+constexpr int kModeOwn = 1;        // a CTA owns whole slices, carry in a register
+constexpr int kModeReduce = 2;     // two-pass, first launch: write every tile's aggregate
+constexpr int kModeApply = 3;      // two-pass, last launch: carry from the scanned aggregates
+
 struct ChunkedLaunch {
     const ChunkedVariant *variant;
     CUtensorMap map_a, map_b;    // 3-D {D, L, B} fp32 maps, box {tile_d, tile_t, 1}
@@ -57,9 +63,10 @@ struct ChunkedLaunch {
     int64_t chunks;              // ceil(L / tile_t)
     int64_t n_tiles;             // n_slices * chunks
     int64_t grid;
-    bool own;                    // slice-owner mode (no look-back); else look-back mode
+    int mode;                    // kModeLookback, kModeOwn, kModeReduce, kModeApply
     Control *ctrl;
-    unsigned long long *words;   // look-back mode: 3 * n_tiles * tile_d words
+    unsigned long long *words;   // look-back mode: 3 * n_tiles * tile_d words; two-pass modes: the
+                                 // per-tile A, B and scanned H arrays (3 * n_tiles * tile_d floats)
     unsigned int *status;        // where device-side failures are recorded
     int64_t spin_limit;
     int64_t silent_tile;         // tile id that publishes nothing (tests), or -1

@@ -6,6 +6,7 @@
 
 #include <map>
 #include <mutex>
+#include <tuple>
 #include <utility>
 
 #include "kernels.cuh"
@@ -18,6 +19,8 @@ namespace {
 constexpr int kVersion = 100;               // 0.1.0
 constexpr int64_t kDefaultSpinLimit = 1 << 20;
 constexpr int kRegcarryThreads = 256;
+// Few slices: the two-pass mode from this many time chunks of 128 steps on.
+constexpr int64_t kTwoPassMinChunks = 64;
 constexpr size_t kWorkspaceHead = 256;      // Control block, padded
 
 struct DeviceInfo {
@@ -35,7 +38,13 @@ struct Slot {
     unsigned char *base = nullptr;
     size_t bytes = 0;
 };
-std::map<std::pair<int, uintptr_t>, Slot> g_slots;
+// What a workspace slot holds.  A look-back slot holds the Control block and
+// tagged words only (zero when allocated), so a word whose tag matches the
+// current epoch was written by this launch; the two-pass mode's plain float
+// arrays live in slots of their own, where no tag is ever looked for.
+enum SlotKind { kSlotTagged = 0, kSlotArrays = 1 };
+// keyed by (device, stream, level, kind): level 1 is the two-pass mode's scan of its aggregates
+std::map<std::tuple<int, uintptr_t, int, int>, Slot> g_slots;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
@@ -99,7 +108,7 @@ void default_tile(int64_t D, bool own, bool backward, int *tile_d, int *tile_t, 
 
 linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int align_bytes, int ctas_per_sm,
                           const linrec_options_t *opt, linrec_plan_t *plan, int *variant_index,
-                          bool backward = false) {
+                          bool backward = false, bool allow_twopass = true) {
     linrec_options_t none = {};
     if (!opt) opt = &none;
     if (!plan || sm_count <= 0) return LINREC_ERR_INVALID_VALUE;
@@ -137,20 +146,27 @@ linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int ali
     }
     if (path != LINREC_PATH_CHUNKED || !tma_ok) return LINREC_ERR_INVALID_VALUE;
 
-    // Slice-owner mode when the channel slices alone give every SM work;
-    // otherwise split each slice's chunks over CTAs and join them by look-back.
-    if (opt->chunk_mode < 0 || opt->chunk_mode > 2) return LINREC_ERR_INVALID_VALUE;
-    bool own;
+    // Slice-owner mode when the channel slices alone give every SM work.
+    // Otherwise each slice's chunks are spread over CTAs: joined by look-back
+    // when the chains are short, or, for long chains (whose look-back would be
+    // bound by how fast inclusive values travel down the chain), by the
+    // two-pass mode: reduce, scan the aggregates, apply.
+    if (opt->chunk_mode < 0 || opt->chunk_mode > 3) return LINREC_ERR_INVALID_VALUE;
+    if (opt->chunk_mode == 3 && (backward || !allow_twopass)) return LINREC_ERR_INVALID_VALUE;
+    bool own = false, twopass = false;
     if (opt->chunk_mode == 0) {
         const int td = opt->tile_d ? opt->tile_d : 32;
         own = B * ((D + td - 1) / td) >= (int64_t)sm_count;
+        const int tt = opt->tile_t ? opt->tile_t : 128;
+        twopass = !own && !backward && allow_twopass && (L + tt - 1) / tt >= kTwoPassMinChunks;
     } else {
         own = opt->chunk_mode == 1;
+        twopass = opt->chunk_mode == 3;
     }
     int tile_d = opt->tile_d, tile_t = opt->tile_t, stages = opt->stages;
     if (tile_d == 0 || tile_t == 0) {
         int dd, dt, ds;
-        default_tile(D, own, backward, &dd, &dt, &ds);
+        default_tile(D, own || twopass, backward, &dd, &dt, &ds);
         if (tile_d == 0) tile_d = dd;
         if (tile_t == 0) tile_t = dt;
         if (stages == 0) stages = ds;
@@ -158,7 +174,8 @@ linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int ali
     const ChunkedVariant *v = find_variant(tile_d, tile_t, stages, variant_index, backward);
     if (!v && opt->stages == 0) v = find_variant(tile_d, tile_t, 0, variant_index, backward);
     if (!v) return LINREC_ERR_INVALID_VALUE;
-    plan->lookback = own ? 0 : 1;
+    plan->lookback = (own || twopass) ? 0 : 1;
+    plan->twopass = twopass ? 1 : 0;
     plan->tile_d = v->tile_d;
     plan->tile_t = v->tile_t;
     plan->segments = v->segments;
@@ -179,7 +196,9 @@ linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int ali
     if (grid > units) grid = units;
     plan->grid = grid;
     plan->workspace_bytes = kWorkspaceHead;
-    if (!own) plan->workspace_bytes += (size_t)3 * (size_t)plan->n_tiles * (size_t)v->tile_d * 8u;
+    if (twopass) plan->workspace_bytes += ((size_t)3 * (size_t)plan->n_tiles + (size_t)(B * spb)) *
+                                          (size_t)v->tile_d * 4u;
+    else if (!own) plan->workspace_bytes += (size_t)3 * (size_t)plan->n_tiles * (size_t)v->tile_d * 8u;
     return LINREC_OK;
 }
 
@@ -224,9 +243,10 @@ bool encode_map(CUtensorMap *map, const float *base, int64_t B, int64_t L, int64
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The look-back workspace of (dev, stream), grown in stream order.  Caller holds g_mu.
-Slot *workspace(int dev, cudaStream_t stream, size_t need) {
-    Slot &s = g_slots[{dev, reinterpret_cast<uintptr_t>(stream)}];
+// The workspace of (dev, stream, level, kind), grown in stream order and zeroed
+// when (re)allocated.  Caller holds g_mu.
+Slot *workspace(int dev, cudaStream_t stream, size_t need, int level = 0, SlotKind kind = kSlotTagged) {
+    Slot &s = g_slots[std::make_tuple(dev, reinterpret_cast<uintptr_t>(stream), level, (int)kind)];
     if (s.bytes >= need) return &s;
     size_t bytes = (need + (1u << 20) - 1) & ~(size_t)((1u << 20) - 1);
     void *p = nullptr;
@@ -243,6 +263,97 @@ Slot *workspace(int dev, cudaStream_t stream, size_t need) {
     s.base = static_cast<unsigned char *>(p);
     s.bytes = bytes;
     return &s;
+}
+
+// The forward scan, arguments checked, g_mu held.  `level` is 0 for a caller's
+// problem and 1 for the two-pass mode's scan of its tile aggregates.
+linrec_status_t scan_locked(DeviceInfo *di, int dev, const float *a, const float *b, float *h, int64_t B,
+                            int64_t L, int64_t D, cudaStream_t stream, const linrec_options_t *opt, int level) {
+    const float *h_init = opt->h_init;
+    float *h_last = opt->h_last;
+    const int align = align_of(a, b, h);
+    linrec_plan_t plan;
+    int vi = -1;
+    linrec_status_t st = plan_impl(B, L, D, di->sm_count, align, 0, opt, &plan, &vi, false, level == 0);
+    if (st != LINREC_OK) return st;
+
+    if (plan.path == LINREC_PATH_REGCARRY) {
+        cudaError_t err = launch_regcarry(plan.vec, plan.prefetch, plan.threads, a, b, h, B, L, D, h_init, h_last,
+                                          stream);
+        return err == cudaSuccess ? LINREC_OK : LINREC_ERR_LAUNCH;
+    }
+
+    // chunked: resident CTAs per SM from the occupancy API, then the real plan
+    int nvar = 0;
+    const ChunkedVariant *variants = chunked_variants(&nvar);
+    if (vi < 0 || vi >= 64) return LINREC_ERR_INVALID_VALUE;
+    if (di->ctas_per_sm[vi] == 0) {
+        int c = 0;
+        if (chunked_ctas_per_sm(&variants[vi], &c) != cudaSuccess || c <= 0) {
+            cudaGetLastError();
+            return LINREC_ERR_LAUNCH;
+        }
+        di->ctas_per_sm[vi] = c;
+    }
+    st = plan_impl(B, L, D, di->sm_count, align, di->ctas_per_sm[vi], opt, &plan, &vi, false, level == 0);
+    if (st != LINREC_OK) return st;
+    if (!get_encoder()) return LINREC_ERR_LAUNCH;
+
+    ChunkedLaunch p;
+    p.variant = &variants[vi];
+    if (!encode_map(&p.map_a, a, B, L, D, plan.tile_d, plan.tile_t) ||
+        !encode_map(&p.map_b, b, B, L, D, plan.tile_d, plan.tile_t))
+        return LINREC_ERR_LAUNCH;
+    // two-pass: the Control block in the tagged slot (for the status word), the
+    // per-tile arrays in an array slot
+    Slot *ws = workspace(dev, stream, plan.twopass ? kWorkspaceHead : plan.workspace_bytes, level);
+    if (!ws) return LINREC_ERR_WORKSPACE;
+    Slot *arrays = nullptr;
+    if (plan.twopass) {
+        arrays = workspace(dev, stream, plan.workspace_bytes - kWorkspaceHead, level, kSlotArrays);
+        if (!arrays) return LINREC_ERR_WORKSPACE;
+    }
+    p.h = h;
+    p.L = L;
+    p.D = D;
+    p.slices_per_batch = (D + plan.tile_d - 1) / plan.tile_d;
+    p.n_slices = B * p.slices_per_batch;
+    p.chunks = plan.chunks;
+    p.n_tiles = plan.n_tiles;
+    p.grid = plan.grid;
+    p.mode = plan.twopass ? kModeReduce : plan.lookback ? kModeLookback : kModeOwn;
+    p.ctrl = reinterpret_cast<Control *>(ws->base);
+    p.words = reinterpret_cast<unsigned long long *>(arrays ? arrays->base : ws->base + kWorkspaceHead);
+    p.status = opt->d_status ? opt->d_status : &p.ctrl->status;
+    p.spin_limit = opt->spin_limit > 0 ? opt->spin_limit : kDefaultSpinLimit;
+    p.silent_tile = opt->test_silent_tile > 0 ? opt->test_silent_tile - 1 : -1;
+    p.h_init = h_init;
+    p.h_last = h_last;
+    cudaError_t err = launch_chunked(p, stream);
+    if (err != cudaSuccess) {
+        cudaGetLastError();
+        return LINREC_ERR_LAUNCH;
+    }
+    if (!plan.twopass) return LINREC_OK;
+
+    // Two-pass mode: the per-tile maps form a (1, chunks, n_slices * tile_d) problem, row-major
+    // by tile id; its scan gives every tile's inclusive value.  Then the apply launch.
+    float *tileA = reinterpret_cast<float *>(p.words);
+    float *tileB = tileA + p.n_tiles * plan.tile_d;
+    float *tileH = tileB + p.n_tiles * plan.tile_d;
+    linrec_options_t inner = {};
+    inner.d_status = p.status;
+    inner.spin_limit = opt->spin_limit;
+    st = scan_locked(di, dev, tileA, tileB, tileH, 1, p.chunks, p.n_slices * plan.tile_d, stream, &inner, level + 1);
+    if (st != LINREC_OK) return st;
+    p.mode = kModeApply;
+    p.grid = plan.grid;
+    err = launch_chunked(p, stream);
+    if (err != cudaSuccess) {
+        cudaGetLastError();
+        return LINREC_ERR_LAUNCH;
+    }
+    return LINREC_OK;
 }
 
 }  // namespace
@@ -301,63 +412,7 @@ linrec_status_t linrec_scan_f32_ex(const float *a, const float *b, float *h, int
     if (!di) return LINREC_ERR_LAUNCH;
     if (!di->supported) return LINREC_ERR_UNSUPPORTED_DEVICE;
 
-    const int align = align_of(a, b, h);
-    linrec_plan_t plan;
-    int vi = -1;
-    st = plan_impl(B, L, D, di->sm_count, align, 0, opt, &plan, &vi);
-    if (st != LINREC_OK) return st;
-
-    if (plan.path == LINREC_PATH_REGCARRY) {
-        cudaError_t err = launch_regcarry(plan.vec, plan.prefetch, plan.threads, a, b, h, B, L, D, h_init, h_last,
-                                          stream);
-        return err == cudaSuccess ? LINREC_OK : LINREC_ERR_LAUNCH;
-    }
-
-    // chunked: resident CTAs per SM from the occupancy API, then the real plan
-    int nvar = 0;
-    const ChunkedVariant *variants = chunked_variants(&nvar);
-    if (vi < 0 || vi >= 64) return LINREC_ERR_INVALID_VALUE;
-    if (di->ctas_per_sm[vi] == 0) {
-        int c = 0;
-        if (chunked_ctas_per_sm(&variants[vi], &c) != cudaSuccess || c <= 0) {
-            cudaGetLastError();
-            return LINREC_ERR_LAUNCH;
-        }
-        di->ctas_per_sm[vi] = c;
-    }
-    st = plan_impl(B, L, D, di->sm_count, align, di->ctas_per_sm[vi], opt, &plan, &vi);
-    if (st != LINREC_OK) return st;
-    if (!get_encoder()) return LINREC_ERR_LAUNCH;
-
-    ChunkedLaunch p;
-    p.variant = &variants[vi];
-    if (!encode_map(&p.map_a, a, B, L, D, plan.tile_d, plan.tile_t) ||
-        !encode_map(&p.map_b, b, B, L, D, plan.tile_d, plan.tile_t))
-        return LINREC_ERR_LAUNCH;
-    Slot *ws = workspace(dev, stream, plan.workspace_bytes);
-    if (!ws) return LINREC_ERR_WORKSPACE;
-    p.h = h;
-    p.L = L;
-    p.D = D;
-    p.slices_per_batch = (D + plan.tile_d - 1) / plan.tile_d;
-    p.n_slices = B * p.slices_per_batch;
-    p.chunks = plan.chunks;
-    p.n_tiles = plan.n_tiles;
-    p.grid = plan.grid;
-    p.own = plan.lookback == 0;
-    p.ctrl = reinterpret_cast<Control *>(ws->base);
-    p.words = reinterpret_cast<unsigned long long *>(ws->base + kWorkspaceHead);
-    p.status = opt->d_status ? opt->d_status : &p.ctrl->status;
-    p.spin_limit = opt->spin_limit > 0 ? opt->spin_limit : kDefaultSpinLimit;
-    p.silent_tile = opt->test_silent_tile > 0 ? opt->test_silent_tile - 1 : -1;
-    p.h_init = h_init;
-    p.h_last = h_last;
-    cudaError_t err = launch_chunked(p, stream);
-    if (err != cudaSuccess) {
-        cudaGetLastError();
-        return LINREC_ERR_LAUNCH;
-    }
-    return LINREC_OK;
+    return scan_locked(di, dev, a, b, h, B, L, D, stream, opt, 0);
 }
 
 linrec_status_t linrec_scan_f32(const float *a, const float *b, float *h, int64_t B, int64_t L, int64_t D,
@@ -493,7 +548,7 @@ linrec_status_t linrec_stream_status(void *stream_ptr) {
     unsigned char *base = nullptr;
     {
         std::lock_guard<std::mutex> lock(g_mu);
-        auto it = g_slots.find({dev, reinterpret_cast<uintptr_t>(stream)});
+        auto it = g_slots.find(std::make_tuple(dev, reinterpret_cast<uintptr_t>(stream), 0, (int)kSlotTagged));
         if (it == g_slots.end() || !it->second.base) return LINREC_OK;
         base = it->second.base;
     }

@@ -113,6 +113,12 @@ extern "C" linrec_status_t linrec_scan_f32_noalloc(const float *a, const float *
     // The dispatcher's chunked tile for this shape, then the resident CTAs of that variant.
     linrec_options_t opt = {};
     opt.path = LINREC_PATH_CHUNKED;
+    // one launch on the fixed array: slice-owner or look-back mode, never the two-pass mode
+    {
+        linrec_plan_t probe;
+        if (linrec_plan_f32(B, L, D, ds->sm_count, 16, 0, &opt, &probe) == LINREC_OK && probe.twopass)
+            opt.chunk_mode = 2;
+    }
     linrec_plan_t plan;
     linrec_status_t st = linrec_plan_f32(B, L, D, ds->sm_count, 16, 0, &opt, &plan);
     if (st != LINREC_OK) return st;
@@ -168,7 +174,7 @@ extern "C" linrec_status_t linrec_scan_f32_noalloc(const float *a, const float *
     p.chunks = plan.chunks;
     p.n_tiles = plan.n_tiles;
     p.grid = plan.grid;
-    p.own = plan.lookback == 0;
+    p.mode = plan.lookback ? kModeLookback : kModeOwn;
     p.ctrl = ctrl;
     p.words = reinterpret_cast<unsigned long long *>(ds->scratch + kHead);
     p.status = d_status ? d_status : &ctrl->status;

@@ -91,11 +91,15 @@ def test_plan_paths():
     # few channel groups: narrower blocks so that every SM gets some
     p = lr.linrec_plan_f32(64, 2048, 1024, path="regcarry", sm_count=152)
     assert p["grid"] >= 2 * 152 or p["threads"] == 32
-    # few channels, long sequence: the chunked look-back path
+    # few channels, long sequence: the chunked two-pass path (per-tile A, B, H arrays)
     p = lr.linrec_plan_f32(1, 1 << 20, 64)
-    assert p["path_name"] == "chunked"
+    assert p["path_name"] == "chunked" and p["twopass"] == 1 and p["lookback"] == 0
     assert p["n_tiles"] == p["chunks"] * ((64 + p["tile_d"] - 1) // p["tile_d"])
     assert p["chunks"] == -(-(1 << 20) // p["tile_t"])
+    assert p["workspace_bytes"] == 256 + 4 * (3 * p["n_tiles"] + 64 // p["tile_d"]) * p["tile_d"]
+    # few channels, short sequence: look-back
+    p = lr.linrec_plan_f32(1, 4096, 64)
+    assert p["lookback"] == 1 and p["twopass"] == 0
     assert p["workspace_bytes"] >= 3 * 8 * p["n_tiles"] * p["tile_d"]
     # the pages' shape
     p = lr.linrec_plan_f32(32, 4096, 256)
@@ -131,8 +135,8 @@ def test_plan_forced_options():
 
 
 def _units(p, B, D):
-    # slice-owner mode: one unit per channel slice; look-back mode: one per tile
-    return p["n_tiles"] if p["lookback"] else B * -(-D // p["tile_d"])
+    # slice-owner mode: one unit per channel slice; look-back and two-pass modes: one per tile
+    return p["n_tiles"] if (p["lookback"] or p["twopass"]) else B * -(-D // p["tile_d"])
 
 
 def test_plan_grid_bounds():
@@ -154,11 +158,17 @@ def test_plan_chunk_modes():
     # many slices: each CTA owns whole slices, no look-back words needed
     p = lr.linrec_plan_f32(32, 4096, 256, path="chunked", sm_count=152)
     assert p["lookback"] == 0 and p["workspace_bytes"] == 256
-    # one long slice: look-back mode with words for every tile
-    p = lr.linrec_plan_f32(1, 1 << 20, 64, path="chunked", sm_count=152)
+    # one long slice: look-back mode with words for every tile when asked for it
+    p = lr.linrec_plan_f32(1, 1 << 20, 64, path="chunked", sm_count=152, chunk_mode="lookback")
     assert p["lookback"] == 1 and p["workspace_bytes"] == 256 + 24 * p["n_tiles"] * p["tile_d"]
+    # ... and the two-pass mode by default
+    p = lr.linrec_plan_f32(1, 1 << 20, 64, path="chunked", sm_count=152)
+    assert p["twopass"] == 1 and p["workspace_bytes"] == 256 + 4 * (3 * p["n_tiles"] + 64 // p["tile_d"]) * p["tile_d"]
+    # the two-pass mode is forward-only
     with pytest.raises(lr.LinrecError):
-        lr.linrec_plan_f32(1, 1000, 64, path="chunked", chunk_mode=3)
+        lr.linrec_plan_f32_backward(1, 1 << 20, 64, chunk_mode="twopass")
+    with pytest.raises(lr.LinrecError):
+        lr.linrec_plan_f32(1, 1000, 64, path="chunked", chunk_mode=4)
 
 
 def test_carry_state_overlap_checks(L):

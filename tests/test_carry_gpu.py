@@ -17,7 +17,9 @@ pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
 PATHS = [{}, {"path": "regcarry"}, {"path": "regcarry", "vec": 1, "prefetch": 4},
          {"path": "chunked", "chunk_mode": "own"}, {"path": "chunked", "chunk_mode": "lookback"},
-         {"path": "chunked", "chunk_mode": "lookback", "tile_d": 32, "tile_t": 64, "stages": 3}]
+         {"path": "chunked", "chunk_mode": "lookback", "tile_d": 32, "tile_t": 64, "stages": 3},
+         {"path": "chunked", "chunk_mode": "twopass"},
+         {"path": "chunked", "chunk_mode": "twopass", "tile_d": 64, "tile_t": 64, "stages": 2}]
 
 
 @pytest.fixture(scope="module", autouse=True)

@@ -38,6 +38,7 @@ def legal_paths(B, L, D, aligned=True):
     if aligned and D % 4 == 0:
         paths.append({"path": "chunked", "chunk_mode": "own"})
         paths.append({"path": "chunked", "chunk_mode": "lookback"})
+        paths.append({"path": "chunked", "chunk_mode": "twopass"})
     return paths
 
 
@@ -130,7 +131,7 @@ VARIANTS = [(128, 64, 2), (128, 64, 3), (128, 32, 3), (256, 32, 2), (64, 128, 2)
 def _variants():
     out = []
     for td, tt, st in VARIANTS:
-        for mode in ("own", "lookback"):
+        for mode in ("own", "lookback", "twopass"):
             out.append({"path": "chunked", "tile_d": td, "tile_t": tt, "stages": st, "chunk_mode": mode})
     return out
 
@@ -266,6 +267,25 @@ def test_streams_run_independently():
         assert_close(h.cpu().numpy(), h64, "multi-stream")
     for s in streams:
         assert lr.linrec_stream_status(s) == lr.LINREC_OK
+
+
+def test_modes_alternating_on_one_stream():
+    """Two-pass and look-back calls take turns on one stream.  With a ~ U[0,1) the
+    two-pass mode's tile products underflow to denormals whose bit patterns equal
+    small look-back tags: the look-back must never see them."""
+    a1, b1 = inputs.generate(1, 1 << 20, 64, seed=13, a_dist="u[0,1)", b_dist="n(0,1)")
+    a2, b2 = inputs.generate(3, 1000, 260, seed=14, a_dist="u[0,1)", b_dist="n(0,1)")
+    want1, _ = oracle.f64(a1, b1)
+    want2, _ = oracle.f64(a2, b2)
+    d1 = (a1.to(DEV), b1.to(DEV))
+    d2 = (a2.to(DEV), b2.to(DEV))
+    for k in range(3):
+        h1 = run(*d1, path="chunked", chunk_mode="twopass")
+        assert_close(h1.cpu().numpy(), want1, f"two-pass, call {k}")
+        for mode in ("lookback", "twopass", "lookback"):
+            h2 = run(*d2, path="chunked", chunk_mode=mode)
+            assert_close(h2.cpu().numpy(), want2, f"{mode} after two-pass, call {k}")
+    assert lr.linrec_stream_status() == lr.LINREC_OK
 
 
 # ---------------------------------------------------------------------------

@@ -60,7 +60,9 @@ def test_noalloc_rejects_what_does_not_fit(noalloc):
     # (1, 2^24, 64): one slice in look-back mode, about 24*B*D*L/128 = 201 MB of look-back words:
     # refused, nothing launched
     B, L, D = 1, 1 << 24, 64
-    plan = lr.linrec_plan_f32(B, L, D, path="chunked", sm_count=torch.cuda.get_device_properties(DEV).multi_processor_count)
+    # the entry point runs one launch on its fixed array: the look-back mode, never the two-pass mode
+    plan = lr.linrec_plan_f32(B, L, D, path="chunked", chunk_mode="lookback",
+                              sm_count=torch.cuda.get_device_properties(DEV).multi_processor_count)
     assert plan["lookback"] == 1
     assert plan["workspace_bytes"] > SCRATCH_BYTES
     base = 1 << 40                       # never dereferenced: the size check comes first
