@@ -32,7 +32,7 @@ def build(force: bool = False) -> str:
             and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
         return _LIB
     tmp = _LIB + f".tmp{os.getpid()}"
-    subprocess.run(["gcc", *CFLAGS, _SRC, "-o", tmp], check=True)
+    subprocess.run(["gcc", *CFLAGS, _SRC, "-o", tmp, "-lm"], check=True)
     os.replace(tmp, _LIB)
     return _LIB
 
@@ -42,7 +42,7 @@ def build_variant(src_text: str, out_path: str) -> str:
     src_path = out_path + ".c"
     with open(src_path, "w") as f:
         f.write(src_text)
-    subprocess.run(["gcc", *CFLAGS, src_path, "-o", out_path], check=True)
+    subprocess.run(["gcc", *CFLAGS, src_path, "-o", out_path, "-lm"], check=True)
     return out_path
 
 
@@ -64,6 +64,11 @@ def _bind(lib):
     lib.linrec_oracle_f64_carry.restype = i32
     lib.linrec_oracle_f64_backward.argtypes = [pf, pf, pf, pd, pd, pd, pd, pd, i64, i64, i64]
     lib.linrec_oracle_f64_backward.restype = i32
+    pu16 = ctypes.POINTER(ctypes.c_uint16)
+    lib.linrec_oracle_decode16.argtypes = [i32, pu16, pd, i64]
+    lib.linrec_oracle_decode16.restype = i32
+    lib.linrec_oracle_encode16.argtypes = [i32, pd, pu16, i64]
+    lib.linrec_oracle_encode16.restype = i32
     lib.linrec_oracle_hardware_threads.argtypes = []
     lib.linrec_oracle_hardware_threads.restype = i32
     return lib
@@ -173,6 +178,48 @@ def f64_backward(a, h, g, h0=None, dhlast=None, want_da=True, lib=None):
     if rc != 0:
         raise ValueError("oracle rejected its arguments")
     return da, db, dh0
+
+
+KINDS16 = {"bf16": 0, "f16": 1}
+
+
+def _bits16(w) -> np.ndarray:
+    if hasattr(w, "detach"):          # a CPU torch tensor of 16-bit words (any 16-bit dtype)
+        import torch
+        w = w.detach().cpu().contiguous().view(torch.int16).numpy()
+    return np.ascontiguousarray(w).view(np.uint16)
+
+
+def decode16(kind: str, w, lib=None) -> np.ndarray:
+    """The exact value of every 16-bit word of format `kind` ("bf16" or "f16"), as float64."""
+    w = _bits16(w)
+    lib = lib or load()
+    x = np.empty(w.shape, dtype=np.float64)
+    if lib.linrec_oracle_decode16(KINDS16[kind], _ptr(w, ctypes.c_uint16), _ptr(x, ctypes.c_double), w.size):
+        raise ValueError("oracle rejected its arguments")
+    return x
+
+
+def encode16(kind: str, x, lib=None) -> np.ndarray:
+    """x (float64) rounded to the nearest word of format `kind`, ties to even; uint16 words."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    lib = lib or load()
+    w = np.empty(x.shape, dtype=np.uint16)
+    if lib.linrec_oracle_encode16(KINDS16[kind], _ptr(x, ctypes.c_double), _ptr(w, ctypes.c_uint16), x.size):
+        raise ValueError("oracle rejected its arguments")
+    return w
+
+
+def f64_16(kind: str, a, b, h0=None, lib=None):
+    """The scan of 16-bit inputs: each word decoded to its exact value, then the
+    definition (continued from h0 if given) in float64.  Returns (h, last state)."""
+    lib = lib or load()
+    xa, xb = decode16(kind, a, lib), decode16(kind, b, lib)
+    # every bfloat16 and binary16 value is a float32 value: the narrowing is exact
+    fa, fb = xa.astype(np.float32), xb.astype(np.float32)
+    if not (np.array_equal(fa, xa, equal_nan=True) and np.array_equal(fb, xb, equal_nan=True)):
+        raise AssertionError("a decoded 16-bit value is not a float32 value")
+    return f64_carry(fa, fb, h0, lib=lib)
 
 
 def hardware_threads() -> int:

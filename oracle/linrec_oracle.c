@@ -46,6 +46,17 @@
  *                            and da_0 = 0).  h is the forward output as given.
  *                            Not on the pages: it follows from the definition
  *                            by the chain rule.
+ *   linrec_oracle_decode16 / linrec_oracle_encode16 -- the two 16-bit storage
+ *                            formats (kind 0: bfloat16, sign 1 / exponent 8 /
+ *                            fraction 7 bits, bias 127; kind 1: IEEE 754
+ *                            binary16, sign 1 / exponent 5 / fraction 10 bits,
+ *                            bias 15).  decode16 gives a word's exact value from
+ *                            its fields; encode16 rounds a double to the nearest
+ *                            word, ties to the even significand, overflow to
+ *                            infinity.  Not on the pages: they store the scan in
+ *                            fp32 only.  A scan stored in 16 bits is, here, the
+ *                            definition above applied to the decoded inputs, its
+ *                            exact result then rounded once by encode16.
  *
  * Threads only split the set of independent channels; every channel is still
  * one sequential loop, so results do not depend on the thread count.
@@ -57,6 +68,7 @@
  * inputs; the page's symbolic walk-through for t = 0, 1, 2; planted mistakes
  * that each pin must catch.
  */
+#include <math.h>
 #include <pthread.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -249,5 +261,66 @@ int linrec_oracle_f64_backward(const float *a, const float *h, const float *g, c
             if (dh0) dh0[i * D + d] = coef * c;             /* a_0 * c_0 */
         }
     }
+    return 0;
+}
+
+/* ---- 16-bit storage formats --------------------------------------------------
+   A word is sign | exponent (ebits) | fraction (fbits).  Exponent field 0 holds
+   zero and the subnormals 0.f x 2^(1-bias); the all-ones field holds infinity
+   (fraction 0) and NaN; any other field e holds 1.f x 2^(e-bias). */
+typedef struct { int ebits, fbits, bias; } fmt16_t;
+static const fmt16_t kFmt16[2] = {{8, 7, 127}, {5, 10, 15}};   /* bfloat16, binary16 */
+
+static double decode16(fmt16_t f, uint16_t w)
+{
+    const int emask = (1 << f.ebits) - 1;
+    const int e = (w >> f.fbits) & emask;
+    const int m = w & ((1 << f.fbits) - 1);
+    double v;
+    if (e == emask) v = m ? NAN : INFINITY;
+    else if (e == 0) v = ldexp((double)m, 1 - f.bias - f.fbits);                 /* 0.f x 2^(1-bias) */
+    else v = ldexp((double)((1 << f.fbits) | m), e - f.bias - f.fbits);         /* 1.f x 2^(e-bias) */
+    return (w & 0x8000u) ? -v : v;
+}
+
+static uint16_t encode16(fmt16_t f, double x)
+{
+    const int emask = (1 << f.ebits) - 1;
+    const uint16_t sign = signbit(x) ? 0x8000u : 0u;
+    if (isnan(x)) return (uint16_t)(sign | (emask << f.fbits) | (1 << (f.fbits - 1)));   /* a quiet NaN */
+    const double ax = fabs(x);
+    if (isinf(ax)) return (uint16_t)(sign | (emask << f.fbits));
+    if (ax == 0.0) return sign;
+    int k = 0;
+    frexp(ax, &k);                            /* 2^(k-1) <= ax < 2^k */
+    int e = k - 1;                            /* ax's binade */
+    const int emin = 1 - f.bias;              /* the smallest normal binade; below it the step stays */
+    if (e < emin) e = emin;
+    /* ax in steps of 2^(e - fbits), the spacing of the words in binade e: a power-of-two
+       scaling, exact in double; rint rounds to the nearest step, ties to even */
+    long long n = (long long)rint(ldexp(ax, f.fbits - e));
+    if (n == (1ll << (f.fbits + 1))) {        /* rounded up into the next binade */
+        n >>= 1;
+        ++e;
+    }
+    if (n < (1ll << f.fbits))                 /* subnormal (e == emin): exponent field 0 */
+        return (uint16_t)(sign | n);
+    const int field = e + f.bias;
+    if (field >= emask) return (uint16_t)(sign | (emask << f.fbits));   /* overflow: infinity */
+    return (uint16_t)(sign | (field << f.fbits) | (n & ((1 << f.fbits) - 1)));
+}
+
+/* kind 0 = bfloat16, 1 = binary16.  Returns 0, or -1 on bad arguments. */
+int linrec_oracle_decode16(int kind, const uint16_t *w, double *x, int64_t n)
+{
+    if (kind < 0 || kind > 1 || n < 0 || (n > 0 && (!w || !x))) return -1;
+    for (int64_t i = 0; i < n; ++i) x[i] = decode16(kFmt16[kind], w[i]);
+    return 0;
+}
+
+int linrec_oracle_encode16(int kind, const double *x, uint16_t *w, int64_t n)
+{
+    if (kind < 0 || kind > 1 || n < 0 || (n > 0 && (!w || !x))) return -1;
+    for (int64_t i = 0; i < n; ++i) w[i] = encode16(kFmt16[kind], x[i]);
     return 0;
 }

@@ -290,10 +290,87 @@ def pin_backward_bruteforce(lib):
                 assert abs(Fraction(float(db[0, s_, d])) - e) <= Fraction(1, 10 ** 12) * (1 + abs(e)), (L, s_, d)
 
 
+# ---- 16-bit storage: the formats' definitions and the libraries that implement them ----
+
+_ALL16 = np.arange(1 << 16, dtype=np.uint16)
+_TOP16 = {"bf16": 0x7F7F, "f16": 0x7BFF}     # largest finite word of each format
+_INF16 = {"bf16": 0x7F80, "f16": 0x7C00}
+
+
+def _same(x, y):
+    return np.array_equal(np.asarray(x, dtype=np.float64), np.asarray(y, dtype=np.float64), equal_nan=True)
+
+
+def pin_decode16_library(lib):
+    """Every word's value against numpy's binary16 and torch's bfloat16 (and the
+    bfloat16 definition as the top half of a binary32 word)."""
+    import torch
+    x = oracle.decode16("f16", _ALL16, lib)
+    assert _same(x, _ALL16.view(np.float16).astype(np.float64)), "binary16 decode"
+    x = oracle.decode16("bf16", _ALL16, lib)
+    with np.errstate(invalid="ignore"):           # signalling NaN words widen to quiet NaNs
+        ref = (_ALL16.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    assert _same(x, ref), "bf16 decode"
+    ref = torch.from_numpy(_ALL16.view(np.int16).copy()).view(torch.bfloat16).double().numpy()
+    assert _same(x, ref), "bf16 decode vs torch"
+
+
+def pin_encode16_neighbours(lib):
+    """Round to nearest, ties to even, from the definition: every word encodes to
+    itself; the midpoint of two adjacent words goes to the one with the even
+    significand; a hair below or above it goes to the nearer word; the midpoint
+    above the largest finite word overflows to infinity; the sign is separate."""
+    for kind in ("bf16", "f16"):
+        top = _TOP16[kind]
+        w = _ALL16[: top + 1]                        # +0 .. largest finite
+        v = oracle.decode16(kind, w, lib)
+        assert np.array_equal(oracle.encode16(kind, v, lib), w), f"{kind}: a word is not its own encoding"
+        ulp_top = v[top] - v[top - 1]
+        upper = np.append(v[1:], v[top] + ulp_top)   # the next word up (infinity after the top)
+        mid = (v + upper) / 2                        # exact: dyadic values of few bits
+        nxt = np.append(w[1:], np.uint16(_INF16[kind]))
+        want = np.where(w % 2 == 0, w, nxt)
+        assert np.array_equal(oracle.encode16(kind, mid, lib), want), f"{kind}: ties"
+        assert np.array_equal(oracle.encode16(kind, np.nextafter(mid, -np.inf), lib), w), f"{kind}: below a tie"
+        assert np.array_equal(oracle.encode16(kind, np.nextafter(mid, np.inf), lib), nxt), f"{kind}: above a tie"
+        assert np.array_equal(oracle.encode16(kind, -v, lib), w | np.uint16(0x8000)), f"{kind}: sign"
+        assert oracle.encode16(kind, np.array([np.inf, 1e300]), lib).tolist() == [_INF16[kind]] * 2
+
+
+def pin_encode16_library(lib):
+    """Random doubles over each format's whole range against numpy's binary16
+    conversion, and binary32 values against torch's bfloat16 conversion."""
+    import torch
+    rng = _rng(16)
+    x = np.exp(rng.uniform(np.log(1e-9), np.log(7e4), 200_000)) * rng.choice([-1.0, 1.0], 200_000)
+    with np.errstate(over="ignore"):              # above 65520 both give infinity
+        ref = x.astype(np.float16).view(np.uint16)
+    assert np.array_equal(oracle.encode16("f16", x, lib), ref), "binary16"
+    y = (np.exp(rng.uniform(np.log(1e-40), np.log(3e38), 200_000)) * rng.choice([-1.0, 1.0], 200_000)).astype(np.float32)
+    ref = torch.from_numpy(y).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(oracle.encode16("bf16", y.astype(np.float64), lib), ref), "bf16"
+
+
+def pin_scan16_closed_forms(lib):
+    """The 16-bit scan: a = 1 with integer b gives the prefix sums exactly; a = 0 gives b."""
+    rng = _rng(17)
+    B, L, D = 2, 300, 8
+    for kind, one in (("bf16", 0x3F80), ("f16", 0x3C00)):
+        bi = rng.integers(-8, 9, (B, L, D)).astype(np.float64)
+        bw = oracle.encode16(kind, bi, lib)
+        ones = np.full((B, L, D), one, dtype=np.uint16)
+        h, last = oracle.f64_16(kind, ones, bw, lib=lib)
+        assert np.array_equal(h, np.cumsum(bi, axis=1)), f"{kind}: a = 1"
+        assert np.array_equal(last, h[:, -1]), f"{kind}: last state"
+        h, _ = oracle.f64_16(kind, np.zeros((B, L, D), np.uint16), bw, lib=lib)
+        assert np.array_equal(h, bi), f"{kind}: a = 0"
+
+
 PINS = [pin_walkthrough, pin_prefix_sum, pin_copy, pin_running_product, pin_geometric, pin_bruteforce,
         pin_carry_closed_forms, pin_carry_bruteforce, pin_carry_segments,
         pin_backward_finite_differences, pin_backward_adjoint, pin_backward_closed_forms,
-        pin_backward_bruteforce]
+        pin_backward_bruteforce, pin_decode16_library, pin_encode16_neighbours, pin_encode16_library,
+        pin_scan16_closed_forms]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -384,6 +461,13 @@ MUTANTS = {
     "carry_dropped": (_F64_STEP, "h[row + d] = (double)a[row + d] + (double)b[row + d];"),
     "a0_applied": (_F64_INIT, "h[base + d] = (double)a[base + d] * (double)b[base + d];"),
     "b_from_previous_step": (_F64_STEP, "h[row + d] = (double)a[row + d] * h[prev + d] + (double)b[prev + d];"),
+    "f16_bias_off_by_one": ("{5, 10, 15}", "{5, 10, 16}"),
+    "bf16_fraction_width": ("{{8, 7, 127}", "{{7, 8, 127}"),
+    "subnormal_scale_wrong": ("ldexp((double)m, 1 - f.bias - f.fbits)", "ldexp((double)m, -f.bias - f.fbits)"),
+    "encode_truncates": ("(long long)rint(ldexp(ax, f.fbits - e))", "(long long)floor(ldexp(ax, f.fbits - e))"),
+    "encode_ties_away": ("(long long)rint(ldexp(ax, f.fbits - e))", "(long long)round(ldexp(ax, f.fbits - e))"),
+    "encode_no_binade_carry": ("if (n == (1ll << (f.fbits + 1))) {", "if (0) {"),
+    "encode_no_overflow": ("if (field >= emask) return (uint16_t)(sign | (emask << f.fbits));", ""),
 }
 
 
