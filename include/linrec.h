@@ -73,7 +73,7 @@ linrec_status_t linrec_scan_f32(const float *a, const float *b, float *h,
  */
 typedef struct {
     int path;            /* linrec_path_t */
-    int vec;             /* regcarry: channels per thread, 1, 2 or 4 */
+    int vec;             /* regcarry: channels per thread, 1, 2 or 4 (16-bit storage: 1, 2, 4 or 8) */
     int prefetch;        /* regcarry: time steps loaded ahead, 4, 8 or 16 */
     int tile_t;          /* chunked: time steps per tile */
     int tile_d;          /* chunked: channels per tile */
@@ -210,6 +210,41 @@ linrec_status_t linrec_plan_f32(int64_t B, int64_t L, int64_t D, int sm_count, i
 /* The same for linrec_scan_f32_backward (its own tile table). */
 linrec_status_t linrec_plan_f32_backward(int64_t B, int64_t L, int64_t D, int sm_count, int align_bytes,
                                          int ctas_per_sm, const linrec_options_t *opt, linrec_plan_t *plan);
+
+/*
+ * 16-bit storage.  linrec_scan_bf16 and linrec_scan_f16 run the same scan with
+ * a, b and h stored as bfloat16 words (sign 1, exponent 8, fraction 7 bits) or
+ * IEEE 754 binary16 words (sign 1, exponent 5, fraction 10 bits), passed as
+ * uint16_t arrays of B*L*D elements in the same (B, L, D) layout.  The pages
+ * store everything in fp32; the scan is bound by the bytes it moves, and
+ * 16-bit storage moves half of them.
+ *  - Every element is widened exactly to fp32; all arithmetic and every
+ *    carried value are fp32, on the same kernels and in the same order as
+ *    linrec_scan_f32; each h is that fp32 result rounded once to the nearest
+ *    16-bit value, ties to even (binary16 overflows to infinity from 65520 on).
+ *    So |h - exact| <= u*|exact| + (1 + u)*e32, with u = 2^-8 (bfloat16) or
+ *    2^-11 (binary16) and e32 the error of the fp32 scan.
+ *  - Options as for linrec_scan_f32_ex.  h_init and h_last, when given, are
+ *    fp32 (B, D) arrays: the state carried between calls keeps full precision.
+ *  - 16-byte aligned a, b, h with D % 8 == 0 take the chunked kernel; other
+ *    inputs (any 2-byte alignment) take the register path.
+ * Other conventions as for linrec_scan_f32.
+ */
+linrec_status_t linrec_scan_bf16(const uint16_t *a, const uint16_t *b, uint16_t *h,
+                                 int64_t B, int64_t L, int64_t D, void *stream);
+linrec_status_t linrec_scan_f16(const uint16_t *a, const uint16_t *b, uint16_t *h,
+                                int64_t B, int64_t L, int64_t D, void *stream);
+linrec_status_t linrec_scan_bf16_ex(const uint16_t *a, const uint16_t *b, uint16_t *h,
+                                    int64_t B, int64_t L, int64_t D, void *stream,
+                                    const linrec_options_t *opt);
+linrec_status_t linrec_scan_f16_ex(const uint16_t *a, const uint16_t *b, uint16_t *h,
+                                   int64_t B, int64_t L, int64_t D, void *stream,
+                                   const linrec_options_t *opt);
+
+/* The dispatcher's decision for 16-bit storage (bfloat16 and binary16 alike);
+   align_bytes may also be 2.  Otherwise as linrec_plan_f32. */
+linrec_status_t linrec_plan_16(int64_t B, int64_t L, int64_t D, int sm_count, int align_bytes,
+                               int ctas_per_sm, const linrec_options_t *opt, linrec_plan_t *plan);
 
 /*
  * linrec_stream_status -- synchronise `stream`, then return and clear the

@@ -15,7 +15,11 @@ Functions keep the C names:
     linrec_scan_f32_carry(a, b, h=None, h_init=None, h_last=None, stream=None) -> h
     linrec_scan_f32_backward(a, h, g, da=None, db=None, h_init=None, dh_last=None, dh_init=None) -> (da, db)
     linrec_scan_f32_host(a, b, h=None, stream=None) -> h   (host tensors; pipelined copies)
+    linrec_scan_bf16(a, b, h=None, stream=None) -> h       (bfloat16 storage, fp32 arithmetic)
+    linrec_scan_f16(a, b, h=None, stream=None) -> h        (binary16 storage, fp32 arithmetic)
+    linrec_scan_bf16_ex / linrec_scan_f16_ex(a, b, h=None, stream=None, **options) -> h
     linrec_plan_f32(B, L, D, sm_count=152, align_bytes=16, resident_ctas=0, **options) -> dict
+    linrec_plan_16(B, L, D, sm_count=152, align_bytes=16, resident_ctas=0, **options) -> dict
     linrec_stream_status(stream=None) -> int
     linrec_copy_f32(src, dst, stream=None)
     linrec_status_string(code) -> str
@@ -119,6 +123,13 @@ def lib():
         L.linrec_plan_f32_backward.restype = i32
         L.linrec_scan_f32_host.argtypes = [vp, vp, vp, i64, i64, i64, vp]
         L.linrec_scan_f32_host.restype = i32
+        for name in ("linrec_scan_bf16", "linrec_scan_f16"):
+            getattr(L, name).argtypes = [vp, vp, vp, i64, i64, i64, vp]
+            getattr(L, name).restype = i32
+            getattr(L, name + "_ex").argtypes = [vp, vp, vp, i64, i64, i64, vp, ctypes.POINTER(Options)]
+            getattr(L, name + "_ex").restype = i32
+        L.linrec_plan_16.argtypes = [i64, i64, i64, i32, i32, i32, ctypes.POINTER(Options), ctypes.POINTER(Plan)]
+        L.linrec_plan_16.restype = i32
         L.linrec_stream_status.argtypes = [vp]
         L.linrec_stream_status.restype = i32
         L.linrec_copy_f32.argtypes = [vp, vp, i64, vp]
@@ -174,13 +185,14 @@ def _stream_handle(stream):
     return ctypes.c_void_p(int(stream))
 
 
-def _shape_of(a, b, h):
+def _shape_of(a, b, h, dtype=None):
     import torch
+    dtype = dtype or torch.float32
     for name, t in (("a", a), ("b", b)) + ((("h", h),) if h is not None else ()):
         if not isinstance(t, torch.Tensor):
             raise TypeError(f"{name} must be a torch.Tensor")
-        if t.dtype != torch.float32:
-            raise TypeError(f"{name} must be float32, got {t.dtype}")
+        if t.dtype != dtype:
+            raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
         if not t.is_cuda:
             raise ValueError(f"{name} must be a CUDA tensor")
         if t.dim() != 3:
@@ -214,6 +226,47 @@ def linrec_scan_f32(a, b, h=None, stream=None):
     code = lib().linrec_scan_f32(a.data_ptr(), b.data_ptr(), h.data_ptr(), B, L, D, _stream_handle(stream))
     _check(code, "linrec_scan_f32")
     return h
+
+
+def _scan16(fn, dtype, a, b, h, stream, options):
+    import torch
+    B, L, D = _shape_of(a, b, h, dtype)
+    if h is None:
+        h = torch.empty_like(a)
+    if options is None:
+        code = getattr(lib(), fn)(a.data_ptr(), b.data_ptr(), h.data_ptr(), B, L, D, _stream_handle(stream))
+    else:
+        _check_state(options.get("h_init"), "h_init", B, D)
+        _check_state(options.get("h_last"), "h_last", B, D)
+        opt = make_options(**options)
+        code = getattr(lib(), fn)(a.data_ptr(), b.data_ptr(), h.data_ptr(), B, L, D, _stream_handle(stream),
+                                  ctypes.byref(opt))
+    _check(code, fn)
+    return h
+
+
+def linrec_scan_bf16(a, b, h=None, stream=None):
+    """h = scan(a, b) on torch.bfloat16 CUDA tensors (B, L, D): fp32 arithmetic, h rounded once."""
+    import torch
+    return _scan16("linrec_scan_bf16", torch.bfloat16, a, b, h, stream, None)
+
+
+def linrec_scan_f16(a, b, h=None, stream=None):
+    """h = scan(a, b) on torch.float16 CUDA tensors (B, L, D): fp32 arithmetic, h rounded once."""
+    import torch
+    return _scan16("linrec_scan_f16", torch.float16, a, b, h, stream, None)
+
+
+def linrec_scan_bf16_ex(a, b, h=None, stream=None, **options):
+    """linrec_scan_bf16 with explicit options; h_init / h_last are float32 (B, D) tensors."""
+    import torch
+    return _scan16("linrec_scan_bf16_ex", torch.bfloat16, a, b, h, stream, options)
+
+
+def linrec_scan_f16_ex(a, b, h=None, stream=None, **options):
+    """linrec_scan_f16 with explicit options; h_init / h_last are float32 (B, D) tensors."""
+    import torch
+    return _scan16("linrec_scan_f16_ex", torch.float16, a, b, h, stream, options)
 
 
 def _check_state(x, name, B, D):
@@ -311,6 +364,18 @@ def linrec_plan_f32(B, L, D, sm_count=152, align_bytes=16, resident_ctas=0, **op
     code = lib().linrec_plan_f32(int(B), int(L), int(D), int(sm_count), int(align_bytes), int(resident_ctas),
                                  ctypes.byref(opt), ctypes.byref(plan))
     _check(code, "linrec_plan_f32")
+    out = {name: getattr(plan, name) for name, _ in Plan._fields_}
+    out["path_name"] = PATH_NAMES.get(out["path"], "none")
+    return out
+
+
+def linrec_plan_16(B, L, D, sm_count=152, align_bytes=16, resident_ctas=0, **options) -> dict:
+    """The dispatcher's choice for 16-bit storage (bfloat16 and binary16 alike), without a GPU."""
+    opt = make_options(**options)
+    plan = Plan()
+    code = lib().linrec_plan_16(int(B), int(L), int(D), int(sm_count), int(align_bytes), int(resident_ctas),
+                                ctypes.byref(opt), ctypes.byref(plan))
+    _check(code, "linrec_plan_16")
     out = {name: getattr(plan, name) for name, _ in Plan._fields_}
     out["path_name"] = PATH_NAMES.get(out["path"], "none")
     return out

@@ -1,0 +1,372 @@
+// chunked_kernel.cuh -- the TMA-staged chunked path of the linear-recurrence scan:
+// the kernel template, instantiated for fp32 storage in chunked.cu and for
+// 16-bit storage in chunked16.cu.
+//
+// h_0 = b_0, h_t = a_t*h_{t-1} + b_t per channel (POPCORNBENCH "Kimi-K2.6 l1_p9",
+// problem statement).  The (B, L, D) problem is cut into tiles of TT time steps
+// x TD channels of one batch index.  A slice is the TD channels of one batch
+// index over all L; its tiles are its time chunks q = 0 .. chunks-1, and tile
+// id = q * n_slices + slice.
+//
+// Per tile, inside one CTA of TD * S threads:
+//  1. TMA copies the a and b boxes (TT x TD stored elements each) into a
+//     shared-memory ring of ST stages; one mbarrier per stage counts the bytes.
+//     Elements are widened to fp32 as threads read them (storage.cuh); all
+//     arithmetic and every carry is fp32, and h is rounded once when stored.
+//  2. Thread (channel c, segment s) composes its K = TT/S consecutive affine
+//     maps x -> a*x + b into one pair (A, B), later map on the left:
+//     (a2,b2) o (a1,b1) = (a2*a1, a2*b1 + b2) ("Kimi-K2.6 l1_p9", derivation of
+//     the associative operator).  Its a, b values stay in registers.
+//  3. A warp-shuffle scan over the S segment pairs of each channel gives every
+//     segment its exclusive prefix and the tile its aggregate (A_q, B_q).
+//  4. The carry: the h value entering the tile.  Only this running value
+//     crosses tile boundaries ("Kimi-K2.6 l1_p9", the running_h carry).  It is
+//     defined as the chain H_q = A_q * H_{q-1} + B_q over the slice's tiles
+//     (H before the first chunk = 0), which both modes below evaluate with the
+//     same fma sequence, so they return the same bits.
+//       slice-owner mode: a CTA owns whole slices (static round-robin) and
+//         walks their chunks in order; the carry stays in a register.
+//       look-back mode (few slices, long L): tiles of a slice run on different
+//         CTAs; each publishes its aggregate, walks back over earlier tiles of
+//         its slice to the nearest inclusive value (S lanes per channel, a
+//         window of S*R tiles per round trip), replays the chain forward from
+//         it and publishes its own inclusive value.
+//       two-pass mode (few slices, long L; three launches): a reduce launch
+//         writes every tile's aggregate, the library scans those aggregates
+//         (a problem 1/TT the size, with these same kernels), and an apply
+//         launch gives each tile the inclusive value of the tile before it.
+//         Tiles are independent in both launches; the apply launch visits
+//         them in reverse order so the inputs the reduce launch read last
+//         are still in L2.
+//  5. Every thread replays its K steps from h_in = A_prefix * carry + B_prefix
+//     and stores h.
+//
+// In look-back mode tile ids come from an atomic counter, taken in the order
+// CTAs start on them, so every predecessor of a tile was handed to a CTA that
+// is running or done.  Every wait is bounded; on expiry the kernel records an
+// error bit in the status word and carries on with NaN.
+#pragma once
+
+#include "kernels.cuh"
+#include "lookback.cuh"
+#include "ptx.cuh"
+#include "storage.cuh"
+
+namespace linrec {
+
+namespace {
+
+constexpr uint32_t kTmaPolls = 1u << 22;   // ~1 s of polls with back-off
+
+// Where a ring stage's tile sits: decoded once by the thread that loads it.
+struct TileCoord {
+    long long id;                       // tile id (>= n_tiles: no tile, the CTA is done)
+    int q;                              // time chunk
+    int bi;                             // batch index
+    int d0;                             // first channel
+    int pad;
+};
+
+template <typename E, int TD, int TT, int S, int ST>
+struct __align__(128) ChunkSmem {
+    E a[ST][TT * TD];                   // stored elements, as the boxes arrive
+    E b[ST][TT * TD];
+    float segA[S][TD], segB[S][TD];     // per-segment pairs, then their exclusive prefixes
+    float carry[TD];                    // h entering the tile, per channel
+    uint64_t full[ST];                  // one mbarrier per ring stage
+    TileCoord tile[ST];                 // tile loaded into each stage
+    uint32_t tag;                       // look-back tag of this launch
+};
+
+template <int DT, int TD, int TT, int S, int ST>
+__global__ void __launch_bounds__(TD * S, (TD * S >= 512) ? 1 : 2)
+chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
+                    const __grid_constant__ CUtensorMap map_b,
+                    typename Storage<DT>::raw *__restrict__ h,
+                    const long long L, const long long D,
+                    const long long slices_per_batch, const long long n_slices,
+                    const long long chunks, const long long n_tiles,
+                    const int mode,              // kModeLookback, kModeOwn, kModeReduce or kModeApply
+                    Control *__restrict__ ctrl, unsigned long long *__restrict__ words,
+                    unsigned int *__restrict__ status,
+                    const long long spin_limit, const long long silent_tile,
+                    const float *h_init, float *h_last)
+{
+    constexpr int K = TT / S;                 // time steps per thread
+    constexpr int R = (S >= 4) ? 16 / S : 4;  // look-back: predecessors per lane
+    using E = typename Storage<DT>::raw;      // stored element type
+    constexpr uint32_t kStageBytes = 2u * TT * TD * sizeof(E);
+    const bool own = mode == kModeOwn;
+    const bool lookback = mode == kModeLookback;
+    const bool reduce = mode == kModeReduce;
+    const bool apply = mode == kModeApply;
+    // two-pass mode: per-tile aggregates and the scanned inclusive values, indexed [tile id][channel],
+    // and each channel's starting state, indexed [slice][channel]
+    float *const tileA = reinterpret_cast<float *>(words);
+    float *const tileB = tileA + n_tiles * TD;
+    const float *const tileH = tileB + n_tiles * TD;
+    float *const tileX = tileB + 2 * n_tiles * TD;
+    static_assert(TT % S == 0 && TD % 32 == 0 && (32 % S) == 0 && S >= 2 && ST >= 2, "tile shape");
+    using Smem = ChunkSmem<E, TD, TT, S, ST>;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
+
+    const int tid = threadIdx.x;
+    const int c = tid % TD;                   // channel within the tile
+    const int s = tid / TD;                   // segment within the tile
+    const int cc = tid / S;                   // transposed role: channel ...
+    const int ss = tid % S;                   // ... and segment / look-back window lane
+    const int gbase = (tid & 31) & ~(S - 1);  // first lane of this channel's group in the warp
+
+    unsigned long long *const wAggA = words;
+    unsigned long long *const wAggB = words + n_tiles * TD;
+    unsigned long long *const wInc = words + 2 * n_tiles * TD;
+
+    // (thread 0) record stage st's tile and start its two box copies.
+    auto issue = [&](int st, long long id, long long q, long long slice) {
+        const long long bi = slice / slices_per_batch;
+        const int d0 = (int)((slice - bi * slices_per_batch) * TD);
+        sm.tile[st] = TileCoord{id, (int)q, (int)bi, d0, 0};
+        mbar_arrive_expect_tx(&sm.full[st], kStageBytes);
+        tma_load_3d(sm.a[st], &map_a, &sm.full[st], d0, (int)(q * TT), (int)bi);
+        tma_load_3d(sm.b[st], &map_b, &sm.full[st], d0, (int)(q * TT), (int)bi);
+    };
+    auto finish = [&](int st) { sm.tile[st] = TileCoord{n_tiles, 0, 0, 0, 0}; };
+    // (thread 0) the CTA's next tile.  Slice-owner mode: slices blockIdx.x,
+    // blockIdx.x + gridDim.x, ... each walked from chunk 0 to chunks-1, tracked
+    // in (own_slice, own_q).  Look-back mode: the next id from the tile counter.
+    long long own_slice = blockIdx.x, own_q = 0, own_m = 0;
+    auto next_tile = [&](long long &q, long long &slice) -> long long {
+        if (reduce || apply) {                // independent tiles, static round-robin
+            const long long k = blockIdx.x + (own_m++) * (long long)gridDim.x;
+            if (k >= n_tiles) return n_tiles;
+            const long long id = apply ? n_tiles - 1 - k : k;
+            q = id / n_slices;
+            slice = id - q * n_slices;
+            return id;
+        }
+        if (own) {
+            if (own_slice >= n_slices) return n_tiles;
+            q = own_q;
+            slice = own_slice;
+            if (++own_q == chunks) { own_q = 0; own_slice += gridDim.x; }
+            return q * n_slices + slice;
+        }
+        const long long id = (long long)atomicAdd(&ctrl->tile_counter, 1ull);
+        if (id >= n_tiles) return n_tiles;
+        q = id / n_slices;
+        slice = id - q * n_slices;
+        return id;
+    };
+
+    // TMA writes whole boxes at 128-byte aligned shared addresses; the layout
+    // guarantees it when the dynamic window is aligned, so check that once.
+    const bool misaligned = (smem_u32(smem_raw) & 127u) != 0;
+    if (tid == 0) {
+        long long first = n_tiles;
+        if (misaligned) {
+            atomicOr(status, kStatusTmaTimeout);
+            if (lookback) atomicExch(&ctrl->abort, 1u);
+        } else {
+            for (int st = 0; st < ST; ++st) mbar_init(&sm.full[st], 1);
+            mbar_fence_init();
+            tmap_prefetch(&map_a);
+            tmap_prefetch(&map_b);
+            if (lookback) {
+                const uint32_t tag = ld_relaxed_u32(&ctrl->epoch) + 1u;
+                sm.tag = tag == 0 ? 1u : tag;
+            }
+            // One tile at launch: in look-back mode tiles are then taken in the order
+            // CTAs start on them, so a tile's predecessors are never parked in another
+            // CTA's ring behind later work.
+            long long q = 0, slice = 0;
+            first = next_tile(q, slice);
+            if (first < n_tiles) issue(0, first, q, slice);
+        }
+        if (first >= n_tiles) finish(0);
+    }
+    __syncthreads();
+
+    const uint32_t tag = lookback ? sm.tag : 0u;
+    uint32_t phases = 0;                      // bit st: parity of the next completion of stage st
+    long long next_fill = 1;                  // (thread 0) next ring slot to fill
+    bool ended = sm.tile[0].id >= n_tiles;    // (thread 0) no more tiles to take
+    long long ahead = -1, ahead_q = 0, ahead_slice = 0;   // (thread 0, look-back) tile taken early
+    uint32_t abort_seen = 0;                  // (thread 0, look-back) abort word, read one iteration early
+    float run = 0.0f;                         // (slice-owner, ss == 0) inclusive value of the last tile
+
+    for (long long k = 0;; ++k) {
+        const int st = (int)(k % ST);
+        const TileCoord tc = sm.tile[st];
+        const long long id = tc.id;
+        if (id >= n_tiles) break;
+
+        if (!mbar_wait_bounded(&sm.full[st], (phases >> st) & 1u, kTmaPolls)) {
+            atomicOr(status, kStatusTmaTimeout);
+            if (lookback) atomicExch(&ctrl->abort, 1u);
+        }
+        phases ^= 1u << st;
+
+        // Keep ST-1 tiles in flight behind this one.  The slot filled last
+        // (k + ST - 1) reuses the stage freed at the end of iteration k - 1.
+        // In look-back mode the next tile id is taken one iteration ahead, so the
+        // atomic's round trip overlaps this tile's work instead of delaying it.
+        if (tid == 0) {
+            if (!ended && abort_seen != 0) {
+                ended = true;
+                finish((int)(next_fill % ST));
+            }
+            while (!ended && next_fill < k + ST) {
+                const int s2 = (int)(next_fill % ST);
+                long long nq = ahead_q, nslice = ahead_slice;
+                const long long nid = ahead >= 0 ? ahead : next_tile(nq, nslice);
+                ahead = -1;
+                if (nid >= n_tiles) {
+                    ended = true;
+                    finish(s2);
+                } else {
+                    issue(s2, nid, nq, nslice);
+                }
+                ++next_fill;
+            }
+            if (lookback) {
+                if (!ended && ahead < 0) ahead = next_tile(ahead_q, ahead_slice);
+                abort_seen = ld_relaxed_u32(&ctrl->abort);
+            }
+        }
+
+        const long long q = tc.q, bi = tc.bi, d0 = tc.d0;
+        const long long t0 = q * TT;
+        const int r0 = s * K;
+        const long long rem = L - (t0 + r0);
+        const int nv = rem <= 0 ? 0 : (rem >= K ? K : (int)rem);   // valid steps of this thread
+        const bool seq_start = (q == 0 && s == 0);                  // holds t = 0 of its channel
+
+        // ---- 2. compose this thread's K steps -----------------------------------
+        const E *ta = sm.a[st] + r0 * TD + c;
+        const E *tb = sm.b[st] + r0 * TD + c;
+        float ra[K], rb[K];
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+            ra[j] = Storage<DT>::get(ta[j * TD]);
+            rb[j] = Storage<DT>::get(tb[j * TD]);
+        }
+        if (seq_start && !h_init) ra[0] = 0.0f;   // h_{-1} = 0: the first slope never matters
+        float A = 1.0f, Bv = 0.0f;
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+            if (j < nv) {
+                Bv = fmaf(ra[j], Bv, rb[j]);
+                A = ra[j] * A;
+            }
+        }
+        sm.segA[s][c] = A;
+        sm.segB[s][c] = Bv;
+        __syncthreads();
+
+        // ---- 3. shuffle scan over the S segment pairs of each channel -----------
+        float xA = sm.segA[ss][cc], xB = sm.segB[ss][cc];
+#pragma unroll
+        for (int off = 1; off < S; off <<= 1) {
+            const float uA = __shfl_up_sync(kFull, xA, off, S);
+            const float uB = __shfl_up_sync(kFull, xB, off, S);
+            if (ss >= off) {                  // (later) o (earlier)
+                xB = fmaf(xA, uB, xB);
+                xA = xA * uA;
+            }
+        }
+        float eA = __shfl_up_sync(kFull, xA, 1, S);
+        float eB = __shfl_up_sync(kFull, xB, 1, S);
+        if (ss == 0) { eA = 1.0f; eB = 0.0f; }
+        sm.segA[ss][cc] = eA;                 // same slot this thread read: no other reader
+        sm.segB[ss][cc] = eB;
+        const float tA = __shfl_sync(kFull, xA, S - 1, S);   // the tile's aggregate
+        const float tB = __shfl_sync(kFull, xB, S - 1, S);
+
+        // ---- 4. the carry entering the tile ---------------------------------------
+        // h before the first chunk: the carried-in state, or 0.
+        const float h_before = (h_init && d0 + cc < D) ? h_init[bi * D + d0 + cc] : 0.0f;
+        if (own) {
+            if (ss == 0) {
+                const float carry = (q == 0) ? h_before : run;
+                run = fmaf(tA, carry, tB);
+                sm.carry[cc] = carry;
+            }
+        } else if (reduce) {
+            // the tile's map; the first chunk's absorbs the carried-in state, so the scan of
+            // these maps from 0 is the chain of inclusive values
+            if (ss == 0) {
+                tileA[id * TD + cc] = (q == 0) ? 0.0f : tA;
+                tileB[id * TD + cc] = (q == 0) ? fmaf(tA, h_before, tB) : tB;
+                // kept for the apply launch: h_last may be the same buffer as h_init, and the
+                // apply launch writes it while other tiles still need the starting state
+                if (q == 0) tileX[id * TD + cc] = h_before;
+            }
+        } else if (apply) {
+            if (ss == 0) sm.carry[cc] = (q == 0) ? tileX[id * TD + cc] : tileH[(id - n_slices) * TD + cc];
+        } else {
+            const bool publish = (q + 1 < chunks) && (id != silent_tile);
+            float carry = h_before;
+            if (q > 0)
+                carry = lookback_carry<S, R>(id, n_slices, TD, cc, ss, gbase, tag, publish, tA, tB, h_before,
+                                             wAggA, wAggB, wInc, ctrl, status, spin_limit);
+            if (ss == 0) {
+                if (publish) st_relaxed_u64(&wInc[id * TD + cc], pack_word(tag, fmaf(tA, carry, tB)));
+                sm.carry[cc] = carry;
+            }
+        }
+        __syncthreads();
+
+        // ---- 5. replay the steps from the carried value, store h -----------------
+        float hc = fmaf(sm.segA[s][c], sm.carry[c], sm.segB[s][c]);
+        if (!reduce && (d0 + c) < D) {
+            E *hp = h + ((bi * L + t0 + r0) * D + d0 + c);
+            if (nv == K) {
+#pragma unroll
+                for (int j = 0; j < K; ++j) {
+                    hc = fmaf(ra[j], hc, rb[j]);
+                    hp[(long long)j * D] = Storage<DT>::put(hc);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < K; ++j) {
+                    if (j < nv) {
+                        hc = fmaf(ra[j], hc, rb[j]);
+                        hp[(long long)j * D] = Storage<DT>::put(hc);
+                    }
+                }
+            }
+            // the thread holding t = L-1 hands the state out
+            if (h_last && nv > 0 && t0 + r0 + nv == L) h_last[bi * D + d0 + c] = hc;
+        }
+        __syncthreads();                      // stage st and the scratch arrays are free again
+    }
+
+    // Look-back mode: the last CTA to finish resets the counters and advances the
+    // epoch for the next launch on this workspace.
+    if (lookback) {
+        __syncthreads();
+        if (tid == 0) {
+            __threadfence();
+            const unsigned int prev = atomicAdd(&ctrl->done, 1u);
+            if (prev == gridDim.x - 1) {
+                __threadfence();
+                atomicExch(&ctrl->tile_counter, 0ull);
+                atomicExch(&ctrl->done, 0u);
+                atomicExch(&ctrl->abort, 0u);
+                atomicAdd(&ctrl->epoch, 1u);
+                __threadfence();
+            }
+        }
+    }
+}
+
+template <int DT, int TD, int TT, int S, int ST>
+constexpr ChunkedVariant make_variant() {
+    return ChunkedVariant{TD, TT, S, ST, TD * S, sizeof(ChunkSmem<typename Storage<DT>::raw, TD, TT, S, ST>),
+                          (int)sizeof(typename Storage<DT>::raw)};
+}
+
+}  // namespace
+
+}  // namespace linrec

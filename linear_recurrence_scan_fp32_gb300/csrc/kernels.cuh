@@ -26,6 +26,13 @@ static_assert(sizeof(Control) == 64, "control block layout");
 constexpr unsigned int kStatusLookbackTimeout = 1u << 6;  // 1 << LINREC_ERR_LOOKBACK_TIMEOUT
 constexpr unsigned int kStatusTmaTimeout = 1u << 7;       // 1 << LINREC_ERR_TMA_TIMEOUT
 
+// How a, b and h are stored (the linrec_dtype_t values).  Arithmetic and
+// carries are fp32 for all three.
+constexpr int kDtypeF32 = 0;
+constexpr int kDtypeBF16 = 1;
+constexpr int kDtypeF16 = 2;
+constexpr int elem_bytes_of(int dtype) { return dtype == kDtypeF32 ? 4 : 2; }
+
 // ---- register-carry path ---------------------------------------------------
 // One thread walks `vec` adjacent channels through all L steps, with the loads
 // of the next `prefetch` steps in flight in registers.
@@ -35,6 +42,12 @@ bool regcarry_supported(int vec, int prefetch);
 cudaError_t launch_regcarry(int vec, int prefetch, int threads, const float *a, const float *b,
                             float *h, int64_t B, int64_t L, int64_t D, const float *h_init, float *h_last,
                             cudaStream_t stream);
+// The same on 16-bit storage (dtype kDtypeBF16 or kDtypeF16): `vec` in {1, 2, 4, 8}
+// elements per thread; h_init and h_last stay fp32.
+bool regcarry16_supported(int vec, int prefetch);
+cudaError_t launch_regcarry16(int dtype, int vec, int prefetch, int threads, const void *a, const void *b,
+                              void *h, int64_t B, int64_t L, int64_t D, const float *h_init, float *h_last,
+                              cudaStream_t stream);
 
 // ---- chunked path ----------------------------------------------------------
 // A tile is (tile_t time steps) x (tile_d channels) of one batch index, staged in
@@ -43,9 +56,14 @@ struct ChunkedVariant {
     int tile_d, tile_t, segments, stages;
     int threads;         // tile_d * segments
     size_t smem_bytes;   // dynamic shared memory per CTA
+    int elem_bytes = 4;  // stored element size: 4 (fp32) or 2 (bfloat16 and binary16)
 };
-// The compiled variants (tile_d, tile_t, segments, stages combinations).
+// The compiled variants (tile_d, tile_t, segments, stages combinations): fp32
+// storage, and 16-bit storage (each shape compiled for bfloat16 and binary16).
 const ChunkedVariant *chunked_variants(int *count);
+const ChunkedVariant *chunked_variants_16(int *count);
+// The kernel of a 16-bit variant for dtype kDtypeBF16 or kDtypeF16 (NULL if none).
+const void *chunked16_kernel(const ChunkedVariant *v, int dtype);
 
 // How the chunked forward kernel gets each tile's carry.
 constexpr int kModeLookback = 0;   // tiles of a slice on different CTAs, decoupled look-back
@@ -55,8 +73,9 @@ constexpr int kModeApply = 3;      // two-pass, last launch: carry from the scan
 
 struct ChunkedLaunch {
     const ChunkedVariant *variant;
-    CUtensorMap map_a, map_b;    // 3-D {D, L, B} fp32 maps, box {tile_d, tile_t, 1}
-    float *h;
+    int dtype = kDtypeF32;       // storage of a, b and h
+    CUtensorMap map_a, map_b;    // 3-D {D, L, B} maps of the stored type, box {tile_d, tile_t, 1}
+    void *h;
     int64_t L, D;
     int64_t slices_per_batch;    // ceil(D / tile_d)
     int64_t n_slices;            // B * slices_per_batch
@@ -74,7 +93,7 @@ struct ChunkedLaunch {
     float *h_last = nullptr;         // (B x D) last state out, or NULL
 };
 // Number of CTAs of this variant that fit on one SM (occupancy API).
-cudaError_t chunked_ctas_per_sm(const ChunkedVariant *v, int *ctas);
+cudaError_t chunked_ctas_per_sm(const ChunkedVariant *v, int *ctas, int dtype = kDtypeF32);
 cudaError_t launch_chunked(const ChunkedLaunch &args, cudaStream_t stream);
 
 // ---- backward (gradient) kernels -----------------------------------------------

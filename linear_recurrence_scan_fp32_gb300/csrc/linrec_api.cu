@@ -27,7 +27,7 @@ struct DeviceInfo {
     bool ready = false;
     bool supported = false;
     int sm_count = 0;
-    int ctas_per_sm[64] = {};               // per chunked variant, 0 = not queried yet
+    int ctas_per_sm[3][64] = {};            // per storage type and chunked variant, 0 = not queried yet
     int back_ctas_per_sm[64] = {};          // per backward variant
 };
 
@@ -63,10 +63,11 @@ int align_of(const void *a, const void *b, const void *h) {
                         reinterpret_cast<uintptr_t>(h);
     if ((u & 15u) == 0) return 16;
     if ((u & 7u) == 0) return 8;
-    return 4;
+    if ((u & 3u) == 0) return 4;
+    return 2;
 }
 
-// Sizes: non-negative, and B*L*D*4 bytes representable.
+// Sizes: non-negative, and B*L*D*16 bytes representable.
 linrec_status_t check_sizes(int64_t B, int64_t L, int64_t D, int64_t *n_out) {
     if (B < 0 || L < 0 || D < 0) return LINREC_ERR_INVALID_VALUE;
     *n_out = 0;
@@ -79,9 +80,14 @@ linrec_status_t check_sizes(int64_t B, int64_t L, int64_t D, int64_t *n_out) {
     return LINREC_OK;
 }
 
-const ChunkedVariant *find_variant(int tile_d, int tile_t, int stages, int *index, bool backward) {
+const ChunkedVariant *variants_of(bool backward, int dtype, int *n) {
+    if (backward) return backward_variants(n);
+    return dtype == kDtypeF32 ? chunked_variants(n) : chunked_variants_16(n);
+}
+
+const ChunkedVariant *find_variant(int tile_d, int tile_t, int stages, int *index, bool backward, int dtype) {
     int n = 0;
-    const ChunkedVariant *v = backward ? backward_variants(&n) : chunked_variants(&n);
+    const ChunkedVariant *v = variants_of(backward, dtype, &n);
     for (int i = 0; i < n; ++i) {
         if (v[i].tile_d == tile_d && v[i].tile_t == tile_t && (stages == 0 || v[i].stages == stages)) {
             if (index) *index = i;
@@ -93,8 +99,19 @@ const ChunkedVariant *find_variant(int tile_d, int tile_t, int stages, int *inde
 
 // Default chunked tile.  Slice-owner mode: narrow 32-channel slices (more
 // slices to spread over the SMs) with a 3-deep ring.  Look-back mode: the
-// widest slice D fills, so fewer tiles take part in each carry chain.
-void default_tile(int64_t D, bool own, bool backward, int *tile_d, int *tile_t, int *stages) {
+// widest slice D fills, so fewer tiles take part in each carry chain.  16-bit
+// storage (measured on GB300): 128-step tiles while slices are scarce, 64-step
+// tiles with a 6-deep ring once every SM has several slices and in two-pass
+// mode, {32, 128, 4} for look-back.
+void default_tile(int64_t B, int64_t D, int sm_count, bool own, bool twopass, bool backward, int dtype,
+                  int *tile_d, int *tile_t, int *stages) {
+    if (dtype != kDtypeF32) {
+        const bool many = B * ((D + 31) / 32) >= 4 * (int64_t)sm_count;
+        if (twopass || (own && many)) { *tile_d = 32; *tile_t = 64; *stages = 6; }
+        else { *tile_d = 32; *tile_t = 128; *stages = 4; }
+        return;
+    }
+    own = own || twopass;
     if (backward) {   // three boxes per stage
         if (own) { *tile_d = 32; *tile_t = 128; *stages = 2; return; }
         if (D >= 64) { *tile_d = 64; *tile_t = 128; *stages = 2; }
@@ -108,7 +125,7 @@ void default_tile(int64_t D, bool own, bool backward, int *tile_d, int *tile_t, 
 
 linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int align_bytes, int ctas_per_sm,
                           const linrec_options_t *opt, linrec_plan_t *plan, int *variant_index,
-                          bool backward = false, bool allow_twopass = true) {
+                          bool backward = false, bool allow_twopass = true, int dtype = kDtypeF32) {
     linrec_options_t none = {};
     if (!opt) opt = &none;
     if (!plan || sm_count <= 0) return LINREC_ERR_INVALID_VALUE;
@@ -118,7 +135,9 @@ linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int ali
     *plan = linrec_plan_t{};
     if (n == 0) return LINREC_OK;
 
-    const bool tma_ok = align_bytes >= 16 && D % 4 == 0 && D <= INT32_MAX && B <= INT32_MAX &&
+    const int eb = elem_bytes_of(dtype);
+    if (backward && dtype != kDtypeF32) return LINREC_ERR_INVALID_VALUE;
+    const bool tma_ok = align_bytes >= 16 && (D * eb) % 16 == 0 && D <= INT32_MAX && B <= INT32_MAX &&
                         L <= (int64_t)INT32_MAX - 1024;
     // The TMA-staged chunked kernel whenever its copies are legal: measured on
     // GB300 it beats the register path at every shape of the five workloads.
@@ -128,11 +147,17 @@ linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int ali
     plan->path = path;
 
     if (path == LINREC_PATH_REGCARRY) {
+        // widest vector of channels (16 bytes at most) that the alignment and D allow
+        const int maxv = 16 / eb;
         int vec = opt->vec;
-        if (vec == 0) vec = (align_bytes >= 16 && D % 4 == 0) ? 4 : (align_bytes >= 8 && D % 2 == 0) ? 2 : 1;
-        if (D % vec != 0 || align_bytes < 4 * vec) return LINREC_ERR_INVALID_VALUE;
-        int prefetch = opt->prefetch ? opt->prefetch : (vec == 4 ? 8 : 16);
-        if (!regcarry_supported(vec, prefetch)) return LINREC_ERR_INVALID_VALUE;
+        if (vec == 0) {
+            vec = maxv;
+            while (vec > 1 && (D % vec != 0 || align_bytes < eb * vec)) vec /= 2;
+        }
+        if (vec <= 0 || D % vec != 0 || align_bytes < eb * vec) return LINREC_ERR_INVALID_VALUE;
+        int prefetch = opt->prefetch ? opt->prefetch : (vec == maxv ? 8 : 16);
+        const bool ok = dtype == kDtypeF32 ? regcarry_supported(vec, prefetch) : regcarry16_supported(vec, prefetch);
+        if (!ok) return LINREC_ERR_INVALID_VALUE;
         plan->vec = vec;
         plan->prefetch = prefetch;
         // Narrower blocks when there are few channel groups, so the grid still
@@ -157,7 +182,7 @@ linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int ali
     if (opt->chunk_mode == 0) {
         const int td = opt->tile_d ? opt->tile_d : 32;
         own = B * ((D + td - 1) / td) >= (int64_t)sm_count;
-        const int tt = opt->tile_t ? opt->tile_t : 128;
+        const int tt = opt->tile_t ? opt->tile_t : (dtype == kDtypeF32 ? 128 : 64);
         twopass = !own && !backward && allow_twopass && (L + tt - 1) / tt >= kTwoPassMinChunks;
     } else {
         own = opt->chunk_mode == 1;
@@ -166,13 +191,13 @@ linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int ali
     int tile_d = opt->tile_d, tile_t = opt->tile_t, stages = opt->stages;
     if (tile_d == 0 || tile_t == 0) {
         int dd, dt, ds;
-        default_tile(D, own || twopass, backward, &dd, &dt, &ds);
+        default_tile(B, D, sm_count, own, twopass, backward, dtype, &dd, &dt, &ds);
         if (tile_d == 0) tile_d = dd;
         if (tile_t == 0) tile_t = dt;
         if (stages == 0) stages = ds;
     }
-    const ChunkedVariant *v = find_variant(tile_d, tile_t, stages, variant_index, backward);
-    if (!v && opt->stages == 0) v = find_variant(tile_d, tile_t, 0, variant_index, backward);
+    const ChunkedVariant *v = find_variant(tile_d, tile_t, stages, variant_index, backward, dtype);
+    if (!v && opt->stages == 0) v = find_variant(tile_d, tile_t, 0, variant_index, backward, dtype);
     if (!v) return LINREC_ERR_INVALID_VALUE;
     plan->lookback = (own || twopass) ? 0 : 1;
     plan->twopass = twopass ? 1 : 0;
@@ -233,12 +258,17 @@ bool get_encoder() {
     return true;
 }
 
-bool encode_map(CUtensorMap *map, const float *base, int64_t B, int64_t L, int64_t D, int tile_d, int tile_t) {
+bool encode_map(CUtensorMap *map, const void *base, int64_t B, int64_t L, int64_t D, int tile_d, int tile_t,
+                int dtype = kDtypeF32) {
+    const cuuint64_t eb = (cuuint64_t)elem_bytes_of(dtype);
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)L, (cuuint64_t)B};
-    const cuuint64_t strides[2] = {(cuuint64_t)D * 4u, (cuuint64_t)L * (cuuint64_t)D * 4u};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * eb, (cuuint64_t)L * (cuuint64_t)D * eb};
     const cuuint32_t box[3] = {(cuuint32_t)tile_d, (cuuint32_t)tile_t, 1u};
     const cuuint32_t estr[3] = {1u, 1u, 1u};
-    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(base), dims, strides, box, estr,
+    const CUtensorMapDataType type = dtype == kDtypeBF16  ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                     : dtype == kDtypeF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                          : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    return g_encode(map, type, 3, const_cast<void *>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -266,43 +296,51 @@ Slot *workspace(int dev, cudaStream_t stream, size_t need, int level = 0, SlotKi
 }
 
 // The forward scan, arguments checked, g_mu held.  `level` is 0 for a caller's
-// problem and 1 for the two-pass mode's scan of its tile aggregates.
-linrec_status_t scan_locked(DeviceInfo *di, int dev, const float *a, const float *b, float *h, int64_t B,
-                            int64_t L, int64_t D, cudaStream_t stream, const linrec_options_t *opt, int level) {
+// problem and 1 for the two-pass mode's scan of its tile aggregates (always fp32).
+linrec_status_t scan_locked(DeviceInfo *di, int dev, const void *a, const void *b, void *h, int64_t B,
+                            int64_t L, int64_t D, int dtype, cudaStream_t stream, const linrec_options_t *opt,
+                            int level) {
     const float *h_init = opt->h_init;
     float *h_last = opt->h_last;
     const int align = align_of(a, b, h);
     linrec_plan_t plan;
     int vi = -1;
-    linrec_status_t st = plan_impl(B, L, D, di->sm_count, align, 0, opt, &plan, &vi, false, level == 0);
+    linrec_status_t st = plan_impl(B, L, D, di->sm_count, align, 0, opt, &plan, &vi, false, level == 0, dtype);
     if (st != LINREC_OK) return st;
 
     if (plan.path == LINREC_PATH_REGCARRY) {
-        cudaError_t err = launch_regcarry(plan.vec, plan.prefetch, plan.threads, a, b, h, B, L, D, h_init, h_last,
-                                          stream);
+        cudaError_t err =
+            dtype == kDtypeF32
+                ? launch_regcarry(plan.vec, plan.prefetch, plan.threads, static_cast<const float *>(a),
+                                  static_cast<const float *>(b), static_cast<float *>(h), B, L, D, h_init, h_last,
+                                  stream)
+                : launch_regcarry16(dtype, plan.vec, plan.prefetch, plan.threads, a, b, h, B, L, D, h_init, h_last,
+                                    stream);
         return err == cudaSuccess ? LINREC_OK : LINREC_ERR_LAUNCH;
     }
 
     // chunked: resident CTAs per SM from the occupancy API, then the real plan
     int nvar = 0;
-    const ChunkedVariant *variants = chunked_variants(&nvar);
-    if (vi < 0 || vi >= 64) return LINREC_ERR_INVALID_VALUE;
-    if (di->ctas_per_sm[vi] == 0) {
+    const ChunkedVariant *variants = variants_of(false, dtype, &nvar);
+    if (vi < 0 || vi >= 64 || dtype < 0 || dtype > 2) return LINREC_ERR_INVALID_VALUE;
+    if (di->ctas_per_sm[dtype][vi] == 0) {
         int c = 0;
-        if (chunked_ctas_per_sm(&variants[vi], &c) != cudaSuccess || c <= 0) {
+        if (chunked_ctas_per_sm(&variants[vi], &c, dtype) != cudaSuccess || c <= 0) {
             cudaGetLastError();
             return LINREC_ERR_LAUNCH;
         }
-        di->ctas_per_sm[vi] = c;
+        di->ctas_per_sm[dtype][vi] = c;
     }
-    st = plan_impl(B, L, D, di->sm_count, align, di->ctas_per_sm[vi], opt, &plan, &vi, false, level == 0);
+    st = plan_impl(B, L, D, di->sm_count, align, di->ctas_per_sm[dtype][vi], opt, &plan, &vi, false, level == 0,
+                   dtype);
     if (st != LINREC_OK) return st;
     if (!get_encoder()) return LINREC_ERR_LAUNCH;
 
     ChunkedLaunch p;
     p.variant = &variants[vi];
-    if (!encode_map(&p.map_a, a, B, L, D, plan.tile_d, plan.tile_t) ||
-        !encode_map(&p.map_b, b, B, L, D, plan.tile_d, plan.tile_t))
+    p.dtype = dtype;
+    if (!encode_map(&p.map_a, a, B, L, D, plan.tile_d, plan.tile_t, dtype) ||
+        !encode_map(&p.map_b, b, B, L, D, plan.tile_d, plan.tile_t, dtype))
         return LINREC_ERR_LAUNCH;
     // two-pass: the Control block in the tagged slot (for the status word), the
     // per-tile arrays in an array slot
@@ -344,7 +382,8 @@ linrec_status_t scan_locked(DeviceInfo *di, int dev, const float *a, const float
     linrec_options_t inner = {};
     inner.d_status = p.status;
     inner.spin_limit = opt->spin_limit;
-    st = scan_locked(di, dev, tileA, tileB, tileH, 1, p.chunks, p.n_slices * plan.tile_d, stream, &inner, level + 1);
+    st = scan_locked(di, dev, tileA, tileB, tileH, 1, p.chunks, p.n_slices * plan.tile_d, kDtypeF32, stream, &inner,
+                     level + 1);
     if (st != LINREC_OK) return st;
     p.mode = kModeApply;
     p.grid = plan.grid;
@@ -381,8 +420,13 @@ linrec_status_t linrec_plan_f32(int64_t B, int64_t L, int64_t D, int sm_count, i
     return plan_impl(B, L, D, sm_count, align_bytes, ctas_per_sm, opt, plan, nullptr);
 }
 
-linrec_status_t linrec_scan_f32_ex(const float *a, const float *b, float *h, int64_t B, int64_t L, int64_t D,
-                                   void *stream_ptr, const linrec_options_t *opt) {
+}  // extern "C"
+
+namespace {
+
+// The forward entry points: argument checks, then scan_locked.
+linrec_status_t scan_entry(int dtype, const void *a, const void *b, void *h, int64_t B, int64_t L, int64_t D,
+                           void *stream_ptr, const linrec_options_t *opt) {
     linrec_options_t none = {};
     if (!opt) opt = &none;
     int64_t n = 0;
@@ -390,15 +434,16 @@ linrec_status_t linrec_scan_f32_ex(const float *a, const float *b, float *h, int
     if (st != LINREC_OK) return st;
     if (n == 0) return LINREC_OK;
     if (!a || !b || !h) return LINREC_ERR_INVALID_VALUE;
-    if (overlaps(h, a, n * 4) || overlaps(h, b, n * 4)) return LINREC_ERR_ALIAS;
+    const int64_t nb = n * elem_bytes_of(dtype);
+    if (overlaps(h, a, nb) || overlaps(h, b, nb)) return LINREC_ERR_ALIAS;
     const float *h_init = opt->h_init;
     float *h_last = opt->h_last;
     const int64_t nstate = B * D * 4;
-    if (h_init && (overlaps(h_init, nstate, h, n * 4) ||
+    if (h_init && (overlaps(h_init, nstate, h, nb) ||
                    (h_last && h_last != h_init && overlaps(h_init, h_last, nstate))))
         return LINREC_ERR_ALIAS;
-    if (h_last && (overlaps(h_last, nstate, a, n * 4) || overlaps(h_last, nstate, b, n * 4) ||
-                   overlaps(h_last, nstate, h, n * 4)))
+    if (h_last && (overlaps(h_last, nstate, a, nb) || overlaps(h_last, nstate, b, nb) ||
+                   overlaps(h_last, nstate, h, nb)))
         return LINREC_ERR_ALIAS;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
 
@@ -412,7 +457,41 @@ linrec_status_t linrec_scan_f32_ex(const float *a, const float *b, float *h, int
     if (!di) return LINREC_ERR_LAUNCH;
     if (!di->supported) return LINREC_ERR_UNSUPPORTED_DEVICE;
 
-    return scan_locked(di, dev, a, b, h, B, L, D, stream, opt, 0);
+    return scan_locked(di, dev, a, b, h, B, L, D, dtype, stream, opt, 0);
+}
+
+}  // namespace
+
+extern "C" {
+
+linrec_status_t linrec_scan_f32_ex(const float *a, const float *b, float *h, int64_t B, int64_t L, int64_t D,
+                                   void *stream, const linrec_options_t *opt) {
+    return scan_entry(kDtypeF32, a, b, h, B, L, D, stream, opt);
+}
+
+linrec_status_t linrec_scan_bf16_ex(const uint16_t *a, const uint16_t *b, uint16_t *h, int64_t B, int64_t L,
+                                    int64_t D, void *stream, const linrec_options_t *opt) {
+    return scan_entry(kDtypeBF16, a, b, h, B, L, D, stream, opt);
+}
+
+linrec_status_t linrec_scan_f16_ex(const uint16_t *a, const uint16_t *b, uint16_t *h, int64_t B, int64_t L,
+                                   int64_t D, void *stream, const linrec_options_t *opt) {
+    return scan_entry(kDtypeF16, a, b, h, B, L, D, stream, opt);
+}
+
+linrec_status_t linrec_scan_bf16(const uint16_t *a, const uint16_t *b, uint16_t *h, int64_t B, int64_t L,
+                                 int64_t D, void *stream) {
+    return scan_entry(kDtypeBF16, a, b, h, B, L, D, stream, nullptr);
+}
+
+linrec_status_t linrec_scan_f16(const uint16_t *a, const uint16_t *b, uint16_t *h, int64_t B, int64_t L, int64_t D,
+                                void *stream) {
+    return scan_entry(kDtypeF16, a, b, h, B, L, D, stream, nullptr);
+}
+
+linrec_status_t linrec_plan_16(int64_t B, int64_t L, int64_t D, int sm_count, int align_bytes, int ctas_per_sm,
+                               const linrec_options_t *opt, linrec_plan_t *plan) {
+    return plan_impl(B, L, D, sm_count, align_bytes, ctas_per_sm, opt, plan, nullptr, false, true, kDtypeBF16);
 }
 
 linrec_status_t linrec_scan_f32(const float *a, const float *b, float *h, int64_t B, int64_t L, int64_t D,

@@ -134,3 +134,13 @@ def generate_workload(w: Workload | str) -> Tuple[torch.Tensor, torch.Tensor]:
     if isinstance(w, str):
         w = WORKLOADS[w]
     return generate(w.B, w.L, w.D, w.seed, w.a_dist, w.b_dist)
+
+
+STORAGE16 = {"bf16": torch.bfloat16, "f16": torch.float16}
+
+
+def to_storage16(x: torch.Tensor, kind: str) -> torch.Tensor:
+    """The draws stored in 16 bits ("bf16" or "f16"), by torch's conversion: the
+    stored words are the test input itself, given to both the CUDA path and the
+    oracle (which decodes them by its own definition of the format)."""
+    return x.to(STORAGE16[kind]).contiguous()

@@ -187,3 +187,51 @@ def test_carry_state_overlap_checks(L):
     assert f(a, b, h, B, Lx, D, s1, s1 + 8, None) == lr.LINREC_ERR_ALIAS         # partial overlap
     assert f(a, b, h, -1, Lx, D, s1, s1, None) == lr.LINREC_ERR_INVALID_VALUE
     assert f(None, None, None, 0, Lx, D, s1, s2, None) == lr.LINREC_OK
+
+
+def test_plan_16bit_storage():
+    # 16-byte aligned with D % 8 == 0: the chunked kernel; 128-step tiles while slices are scarce,
+    # 64-step tiles with a 6-deep ring once every SM has several slices
+    p = lr.linrec_plan_16(32, 4096, 256, sm_count=152)
+    assert p["path_name"] == "chunked" and p["lookback"] == 0
+    assert (p["tile_d"], p["tile_t"], p["stages"]) == (32, 128, 4)
+    p = lr.linrec_plan_16(256, 128, 4096, sm_count=152)
+    assert (p["tile_d"], p["tile_t"], p["stages"], p["lookback"]) == (32, 64, 6, 0)
+    # few long slices: two-pass, whose aggregates are fp32 whatever the storage
+    p = lr.linrec_plan_16(1, 1 << 20, 64)
+    assert p["twopass"] == 1
+    assert p["workspace_bytes"] == 256 + 4 * (3 * p["n_tiles"] + 64 // p["tile_d"]) * p["tile_d"]
+    # D % 8 != 0 or fewer than 16 bytes of alignment: the register path, widest vector allowed
+    assert lr.linrec_plan_16(2, 77, 36)["path_name"] == "regcarry"
+    assert lr.linrec_plan_16(2, 77, 36)["vec"] == 4
+    assert lr.linrec_plan_16(2, 77, 40, align_bytes=16)["path_name"] == "chunked"
+    assert lr.linrec_plan_16(2, 77, 40, align_bytes=8)["vec"] == 4
+    assert lr.linrec_plan_16(2, 77, 40, align_bytes=4)["vec"] == 2
+    assert lr.linrec_plan_16(2, 77, 40, align_bytes=2)["vec"] == 1
+    assert lr.linrec_plan_16(2, 77, 7, align_bytes=16)["vec"] == 1
+    assert lr.linrec_plan_16(256, 128, 4096, path="regcarry")["vec"] == 8
+    with pytest.raises(lr.LinrecError):
+        lr.linrec_plan_16(2, 77, 36, path="chunked")               # D * 2 bytes not a multiple of 16
+    with pytest.raises(lr.LinrecError):
+        lr.linrec_plan_16(2, 77, 40, path="regcarry", vec=8, align_bytes=8)
+    with pytest.raises(lr.LinrecError):
+        lr.linrec_plan_16(32, 4096, 256, path="chunked", tile_d=32, tile_t=32)   # no such 16-bit variant
+    # every variant the 16-bit table reports by default exists and is shaped like the fp32 ones
+    for mode in ("own", "lookback", "twopass"):
+        p = lr.linrec_plan_16(4, 5000, 128, path="chunked", chunk_mode=mode)
+        assert p["threads"] == p["tile_d"] * p["segments"] and p["tile_t"] % p["segments"] == 0
+
+
+def test_16bit_argument_checks_count_two_bytes(L):
+    # fake, never-dereferenced addresses: the checks run before any device access
+    B, Lx, D = 1, 4, 8
+    n2 = B * Lx * D * 2
+    base = 1 << 36
+    for f in (L.linrec_scan_bf16, L.linrec_scan_f16):
+        f.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int64] * 3 + [ctypes.c_void_p]
+        f.restype = ctypes.c_int
+        assert f(base, base + 4 * n2, base + n2 - 2, B, Lx, D, None) == lr.LINREC_ERR_ALIAS   # h's first element in a
+        assert f(base, base + 4 * n2, base + 5 * n2 - 2, B, Lx, D, None) == lr.LINREC_ERR_ALIAS
+        assert f(None, base, base + 4 * n2, B, Lx, D, None) == lr.LINREC_ERR_INVALID_VALUE
+        assert f(base, base, base, -1, Lx, D, None) == lr.LINREC_ERR_INVALID_VALUE
+        assert f(None, None, None, 0, Lx, D, None) == lr.LINREC_OK
