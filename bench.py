@@ -11,6 +11,9 @@ no collective on the data path); rank 0 prints max-over-ranks timing.
 
 --impl reference times the CPU oracle (plain sequential loop, all host cores)
 on the same workload: the reference arm of this comparison.
+
+--dtype bf16 | f16 stores a, b and h in 16 bits (fp32 arithmetic and carry):
+6 bytes per element instead of 12, the same GB/s metric over those bytes.
 """
 from __future__ import annotations
 
@@ -34,18 +37,33 @@ UNIT = "GB/s"
 WORKLOAD = "pages"          # the headline workload; --workload picks another for reports
 
 
-def metric_for(w, op: str = "forward") -> str:
+STORAGE_BYTES = {"f32": 4, "bf16": 2, "f16": 2}
+
+
+def metric_for(w, op: str = "forward", dtype: str = "f32") -> str:
     if op == "backward":
         return (f"scan backward GB/s (a,h,g read, da,db written) & % of GB300 HBM peak at "
                 f"B={w.B},L={w.L},D={w.D} fp32 ({w.name})")
-    if w.name == WORKLOAD:
+    if w.name == WORKLOAD and dtype == "f32":
         return METRIC
-    return f"scan GB/s (a,b,h bytes) & % of GB300 HBM peak at B={w.B},L={w.L},D={w.D} fp32 ({w.name})"
+    store = "fp32" if dtype == "f32" else f"{dtype} storage, fp32 arithmetic"
+    return f"scan GB/s (a,b,h bytes) & % of GB300 HBM peak at B={w.B},L={w.L},D={w.D} {store} ({w.name})"
 
 
-def bytes_per_step(w, op: str) -> int:
-    # forward: read a, b, write h; backward: read a, h, g, write da, db (4 bytes each, once)
-    return (20 if op == "backward" else 12) * w.numel
+def bytes_per_step(w, op: str, dtype: str = "f32") -> int:
+    # forward: read a, b, write h; backward: read a, h, g, write da, db (each once)
+    if op == "backward":
+        return 20 * w.numel
+    return 3 * STORAGE_BYTES[dtype] * w.numel
+
+
+def launches_per_step(plan: dict, op: str) -> int:
+    """Kernel launches of one call.  Two-pass mode: the reduce launch, the scan of the
+    tile aggregates (one launch: at that level the dispatcher takes the slice-owner or
+    look-back mode, never two-pass again) and the apply launch."""
+    if op == "forward" and plan["path_name"] == "chunked" and plan["twopass"]:
+        return 3
+    return 1
 FALLBACK_HBM_GBS = 6800.0
 CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -178,19 +196,27 @@ def committed_traffic(kernel: str, workload: str):
 # arms
 # ---------------------------------------------------------------------------
 
-def cpu_baseline(a, b, w, budget_s: float = 10.0):
-    """The oracle as it stands, all host cores, repeated over the full workload for ~budget_s."""
+def cpu_baseline(a, b, w, budget_s: float = 10.0, dtype: str = "f32"):
+    """The oracle as it stands, all host cores, repeated over the full workload for ~budget_s.
+    16-bit storage: the oracle's decode of the stored words, then its fp64 scan (one thread
+    decodes; the scan runs on all cores)."""
     import oracle
     oracle.build()
     threads = oracle.hardware_threads()
     reps, t_total = 0, 0.0
+    used = threads
+    nbytes = bytes_per_step(w, "forward", dtype)
     while t_total < budget_s and reps < 1000:
         t0 = time.perf_counter()
-        _, used = oracle.f64(a, b, nthreads=threads)
+        if dtype == "f32":
+            _, used = oracle.f64(a, b, nthreads=threads)
+        else:
+            oracle.f64_16(dtype, a, b)
         t_total += time.perf_counter() - t0
         reps += 1
-    return {"value": w.algorithmic_bytes * reps / t_total / 1e9, "unit": UNIT, "cores": used, "kind": "oracle",
-            "sample": f"full {w.name} workload {w.shape}, fp64 sequential oracle, {reps} repetitions, {t_total:.1f} s"}
+    what = "fp64 sequential oracle" if dtype == "f32" else f"oracle {dtype} decode + fp64 scan"
+    return {"value": nbytes * reps / t_total / 1e9, "unit": UNIT, "cores": used, "kind": "oracle",
+            "sample": f"full {w.name} workload {w.shape}, {what}, {reps} repetitions, {t_total:.1f} s"}
 
 
 def cpu_baseline_backward(a, h, g, w, nbytes, budget_s: float = 10.0):
@@ -216,34 +242,48 @@ def run_reference(args):
     oracle.build()
     w = inputs.WORKLOADS[args.workload]
     a, b = inputs.generate_workload(w)
-    a, b = a.numpy(), b.numpy()
+    if args.dtype != "f32":
+        a, b = inputs.to_storage16(a, args.dtype), inputs.to_storage16(b, args.dtype)
+        a = a.view(__import__("torch").int16).numpy().view(np.uint16)
+        b = b.view(__import__("torch").int16).numpy().view(np.uint16)
+    else:
+        a, b = a.numpy(), b.numpy()
     threads = oracle.hardware_threads()
+    used = threads
+
+    def run_oracle(x, y):
+        nonlocal used
+        if args.dtype == "f32":
+            _, used = oracle.f64(x, y, nthreads=threads)
+        else:
+            oracle.f64_16(args.dtype, x, y)
+
     # size each step's sample so that warm-up + timed steps take about --ref-seconds
     t0 = time.perf_counter()
-    oracle.f64(a, b, nthreads=threads)
+    run_oracle(a, b)
     t_full = time.perf_counter() - t0
     per_step = args.ref_seconds / (args.steps + args.warmup)
     nb = max(1, min(w.B, int(w.B * per_step / t_full)))
     nl = w.L if nb > 1 else max(64, min(w.L, int(w.L * w.B * per_step / t_full)))
     a_s = np.ascontiguousarray(a[:nb, :nl])
     b_s = np.ascontiguousarray(b[:nb, :nl])
-    sample_bytes = 12 * a_s.size
+    sample_bytes = 3 * STORAGE_BYTES[args.dtype] * a_s.size
     for _ in range(args.warmup):
-        oracle.f64(a_s, b_s, nthreads=threads)
+        run_oracle(a_s, b_s)
     times = []
-    used = threads
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        _, used = oracle.f64(a_s, b_s, nthreads=threads)
+        run_oracle(a_s, b_s)
         times.append(time.perf_counter() - t0)
     total = sum(times)
     value = sample_bytes * args.steps / total / 1e9
     line = {
-        "impl": "reference", "metric": metric_for(w), "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+        "impl": "reference", "metric": metric_for(w, "forward", args.dtype), "value": round(value, 3), "unit": UNIT,
+        "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "gpu_launches": 0,
-        "config": {"workload": w.about, "B": w.B, "L": w.L, "D": w.D, "seed": w.seed,
+        "config": {"workload": w.about, "B": w.B, "L": w.L, "D": w.D, "seed": w.seed, "storage": args.dtype,
                    "l2": "host run: no device cache involved"},
         "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": used, "kind": "oracle",
                          "sample": f"per step: batches 0..{nb - 1}, steps 0..{nl - 1}, all {w.D} channels "
@@ -274,6 +314,10 @@ def run_ours(args):
 
     w = inputs.WORKLOADS[args.workload]
     a_cpu, b_cpu = inputs.generate(w.B, w.L, w.D, rank_seed(w.seed, rank), w.a_dist, w.b_dist)
+    if args.dtype != "f32":
+        if args.op != "forward":
+            raise SystemExit("16-bit storage is forward only")
+        a_cpu, b_cpu = inputs.to_storage16(a_cpu, args.dtype), inputs.to_storage16(b_cpu, args.dtype)
     a = a_cpu.to(dev)
     b = b_cpu.to(dev)
     h = torch.empty_like(a)
@@ -284,12 +328,16 @@ def run_ours(args):
     if args.tile:
         td, tt, st = (int(x) for x in args.tile.split(","))
         opt.update(path="chunked", tile_d=td, tile_t=tt, stages=st)
-    plan = lr.linrec_plan_f32(w.B, w.L, w.D, sm_count=torch.cuda.get_device_properties(dev).multi_processor_count,
-                              **opt)
-    if plan["path_name"] == "chunked" and not plan["lookback"]:
-        kernel_tag = "chunked"
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    plan_fn = lr.linrec_plan_f32 if args.dtype == "f32" else lr.linrec_plan_16
+    plan = plan_fn(w.B, w.L, w.D, sm_count=sms, **opt)
+    store = "" if args.dtype == "f32" else "_" + args.dtype
+    if plan["path_name"] == "chunked":
+        mode = "_twopass" if plan["twopass"] else "_lookback" if plan["lookback"] else ""
+        kernel_tag = "chunked" + store + mode
     else:
-        kernel_tag = "chunked_lookback" if plan["path_name"] == "chunked" else "regcarry"
+        kernel_tag = "regcarry" + store
+    scan16 = {"bf16": lr.linrec_scan_bf16_ex, "f16": lr.linrec_scan_f16_ex}.get(args.dtype)
 
     if args.op == "backward":
         lr.linrec_scan_f32(a, b, h, stream=stream)          # the forward output the gradient needs
@@ -306,6 +354,8 @@ def run_ours(args):
     def step():
         if args.op == "backward":
             lr.linrec_scan_f32_backward(a, h, gd, da=da, db=db, stream=stream, **opt)
+        elif scan16 is not None:
+            scan16(a, b, h, stream=stream, **opt)
         elif opt:
             lr.linrec_scan_f32_ex(a, b, h, stream=stream, **opt)
         else:
@@ -339,10 +389,11 @@ def run_ours(args):
     if status != lr.LINREC_OK:
         raise SystemExit(f"device-side failure: {lr.linrec_status_string(status)}")
     seconds = max_over_ranks(elapsed_ms / 1e3, dev)
-    nbytes = bytes_per_step(w, args.op)
+    nbytes = bytes_per_step(w, args.op, args.dtype)
     value = aggregate_gbs(nbytes, world, args.steps, seconds)
+    launches = launches_per_step(plan, args.op)
 
-    # roofline of the scan kernel (one launch per step)
+    # roofline of the scan: one launch per step, or the two-pass mode's three (timed together)
     mean_launch_s = statistics.fmean(per_launch_ms) / 1e3
     achieved = nbytes / mean_launch_s / 1e9
     peak, peak_kind = hbm_peak()
@@ -377,8 +428,18 @@ def run_ours(args):
         h_h = torch.empty_like(a_cpu).pin_memory()
         e_steps = max(3, min(args.steps, 20))
 
-        def e2e_step():
-            lr.linrec_scan_f32_host(a_h, b_h, h_h, stream=stream)
+        if scan16 is None:
+            def e2e_step():
+                lr.linrec_scan_f32_host(a_h, b_h, h_h, stream=stream)
+            e2e_path = ("linrec_scan_f32_host on pinned host a, b, h: the kernel reads and writes host "
+                        "memory in place over the host link")
+        else:
+            def e2e_step():
+                a.copy_(a_h, non_blocking=True)
+                b.copy_(b_h, non_blocking=True)
+                scan16(a, b, h, stream=stream)
+                h_h.copy_(h, non_blocking=True)
+            e2e_path = f"pinned host a, b copied in, linrec_scan_{args.dtype}_ex, h copied out, one stream"
 
         for _ in range(2):
             e2e_step()
@@ -390,10 +451,10 @@ def run_ours(args):
         e1.record(stream)
         torch.cuda.synchronize()
         e_sec = max_over_ranks(e0.elapsed_time(e1) / 1e3, dev)
-        e2e = {"value": round(aggregate_gbs(w.algorithmic_bytes, world, e_steps, e_sec), 3), "unit": UNIT,
-               "h2d_bytes_per_step": 8 * w.numel, "d2h_bytes_per_step": 4 * w.numel, "steps": e_steps,
-               "path": "linrec_scan_f32_host on pinned host a, b, h: the kernel reads and writes host "
-                       "memory in place over the host link"}
+        eb = STORAGE_BYTES[args.dtype]
+        e2e = {"value": round(aggregate_gbs(nbytes, world, e_steps, e_sec), 3), "unit": UNIT,
+               "h2d_bytes_per_step": 2 * eb * w.numel, "d2h_bytes_per_step": eb * w.numel, "steps": e_steps,
+               "path": e2e_path}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -401,33 +462,37 @@ def run_ours(args):
             cpu = cpu_baseline_backward(a_cpu.numpy(), h.cpu().numpy(), g_cpu.numpy(), w, nbytes,
                                         budget_s=args.cpu_seconds)
         else:
-            cpu = cpu_baseline(a_cpu.numpy(), b_cpu.numpy(), w, budget_s=args.cpu_seconds)
+            if args.dtype == "f32":
+                cpu = cpu_baseline(a_cpu.numpy(), b_cpu.numpy(), w, budget_s=args.cpu_seconds)
+            else:
+                cpu = cpu_baseline(a_cpu, b_cpu, w, budget_s=args.cpu_seconds, dtype=args.dtype)
 
     if rank == 0:
         clk = clocks.summary()
         line = {
-            "metric": metric_for(w, args.op), "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+            "metric": metric_for(w, args.op, args.dtype), "value": round(value, 3), "unit": UNIT, "n_gpus": world,
             "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(seconds * 1e3 / args.steps, 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": w.about, "B": w.B, "L": w.L, "D": w.D, "seed": w.seed,
                        "global_batch": w.B * world,
-                       "op": args.op,
+                       "op": args.op, "storage": args.dtype,
                        "l2": (f"inputs larger than L2: {nbytes / 1e6:.0f} MB per step vs 129 MB L2, "
                               "no flush") if nbytes > 129e6 else "working set fits L2: small case",
                        "path": plan["path_name"],
                        "plan": {k: plan[k] for k in ("vec", "prefetch", "tile_t", "tile_d", "segments", "stages",
-                                                     "lookback", "threads", "grid")}},
+                                                     "lookback", "twopass", "threads", "grid")}},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic,
                          "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                          else "fallback 6.8 TB/s", "kernel": kernel,
-                         "algorithmic_bytes_per_launch": nbytes},
+                         "algorithmic_bytes_per_step": nbytes, "launches_per_step": launches,
+                         "timed": "each step: every launch of one call, between two events"},
             "copy_ceiling_gbs": copy_gbs,
             "frac_of_copy_ceiling": round(value / ceiling, 4),
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": args.steps,
+            "gpu_launches": args.steps * launches,
             "clocks": clk,
             "wall_s": round(wall, 3),
         }
@@ -446,7 +511,9 @@ def main(argv=None):
     p.add_argument("--path", choices=("auto", "regcarry", "chunked"), default="auto")
     p.add_argument("--workload", default=WORKLOAD,
                    help="named workload (tiny, pages, long, gated, short, ...); pages is the headline")
-    p.add_argument("--chunk-mode", choices=("auto", "own", "lookback"), default="auto")
+    p.add_argument("--chunk-mode", choices=("auto", "own", "lookback", "twopass"), default="auto")
+    p.add_argument("--dtype", choices=("f32", "bf16", "f16"), default="f32",
+                   help="storage of a, b and h (arithmetic is fp32 for all three)")
     p.add_argument("--tile", default="", help="chunked tile as tile_d,tile_t,stages")
     p.add_argument("--op", choices=("forward", "backward"), default="forward",
                    help="forward scan (the headline) or its gradient")

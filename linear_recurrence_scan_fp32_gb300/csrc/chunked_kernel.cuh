@@ -71,8 +71,10 @@ template <typename E, int TD, int TT, int S, int ST>
 struct __align__(128) ChunkSmem {
     E a[ST][TT * TD];                   // stored elements, as the boxes arrive
     E b[ST][TT * TD];
-    float segA[S][TD], segB[S][TD];     // per-segment pairs, then their exclusive prefixes
-    float carry[TD];                    // h entering the tile, per channel
+    // Per-segment pairs, then their exclusive prefixes, and the h entering the tile:
+    // two copies, used by alternate tiles (see the barriers in the tile loop).
+    float segA[2][S][TD], segB[2][S][TD];
+    float carry[2][TD];
     uint64_t full[ST];                  // one mbarrier per ring stage
     TileCoord tile[ST];                 // tile loaded into each stage
     uint32_t tag;                       // look-back tag of this launch
@@ -260,12 +262,15 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
                 A = ra[j] * A;
             }
         }
-        sm.segA[s][c] = A;
-        sm.segB[s][c] = Bv;
+        float (&segA)[S][TD] = sm.segA[k & 1];
+        float (&segB)[S][TD] = sm.segB[k & 1];
+        float (&carry_in)[TD] = sm.carry[k & 1];
+        segA[s][c] = A;
+        segB[s][c] = Bv;
         __syncthreads();
 
         // ---- 3. shuffle scan over the S segment pairs of each channel -----------
-        float xA = sm.segA[ss][cc], xB = sm.segB[ss][cc];
+        float xA = segA[ss][cc], xB = segB[ss][cc];
 #pragma unroll
         for (int off = 1; off < S; off <<= 1) {
             const float uA = __shfl_up_sync(kFull, xA, off, S);
@@ -278,8 +283,8 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
         float eA = __shfl_up_sync(kFull, xA, 1, S);
         float eB = __shfl_up_sync(kFull, xB, 1, S);
         if (ss == 0) { eA = 1.0f; eB = 0.0f; }
-        sm.segA[ss][cc] = eA;                 // same slot this thread read: no other reader
-        sm.segB[ss][cc] = eB;
+        segA[ss][cc] = eA;                    // same slot this thread read: no other reader
+        segB[ss][cc] = eB;
         const float tA = __shfl_sync(kFull, xA, S - 1, S);   // the tile's aggregate
         const float tB = __shfl_sync(kFull, xB, S - 1, S);
 
@@ -290,7 +295,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
             if (ss == 0) {
                 const float carry = (q == 0) ? h_before : run;
                 run = fmaf(tA, carry, tB);
-                sm.carry[cc] = carry;
+                carry_in[cc] = carry;
             }
         } else if (reduce) {
             // the tile's map; the first chunk's absorbs the carried-in state, so the scan of
@@ -303,7 +308,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
                 if (q == 0) tileX[id * TD + cc] = h_before;
             }
         } else if (apply) {
-            if (ss == 0) sm.carry[cc] = (q == 0) ? tileX[id * TD + cc] : tileH[(id - n_slices) * TD + cc];
+            if (ss == 0) carry_in[cc] = (q == 0) ? tileX[id * TD + cc] : tileH[(id - n_slices) * TD + cc];
         } else {
             const bool publish = (q + 1 < chunks) && (id != silent_tile);
             float carry = h_before;
@@ -312,13 +317,13 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
                                              wAggA, wAggB, wInc, ctrl, status, spin_limit);
             if (ss == 0) {
                 if (publish) st_relaxed_u64(&wInc[id * TD + cc], pack_word(tag, fmaf(tA, carry, tB)));
-                sm.carry[cc] = carry;
+                carry_in[cc] = carry;
             }
         }
         __syncthreads();
 
         // ---- 5. replay the steps from the carried value, store h -----------------
-        float hc = fmaf(sm.segA[s][c], sm.carry[c], sm.segB[s][c]);
+        float hc = fmaf(segA[s][c], carry_in[c], segB[s][c]);
         if (!reduce && (d0 + c) < D) {
             E *hp = h + ((bi * L + t0 + r0) * D + d0 + c);
             if (nv == K) {
@@ -339,7 +344,11 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
             // the thread holding t = L-1 hands the state out
             if (h_last && nv > 0 && t0 + r0 + nv == L) h_last[bi * D + d0 + c] = hc;
         }
-        __syncthreads();                      // stage st and the scratch arrays are free again
+        // No barrier here.  Stage st was last read before this tile's first
+        // barrier, and thread 0 refills it only in the next iteration.  The next
+        // tile writes the other copy of segA / segB / carry; the one after it
+        // writes this copy again only after two more barriers, which every
+        // thread reaches after finishing this tile.
     }
 
     // Look-back mode: the last CTA to finish resets the counters and advances the

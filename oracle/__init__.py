@@ -210,15 +210,20 @@ def encode16(kind: str, x, lib=None) -> np.ndarray:
     return w
 
 
-def f64_16(kind: str, a, b, h0=None, lib=None):
+def f64_16(kind: str, a, b, h0=None, nthreads: int = 0, lib=None):
     """The scan of 16-bit inputs: each word decoded to its exact value, then the
-    definition (continued from h0 if given) in float64.  Returns (h, last state)."""
+    definition (continued from h0 if given) in float64.  Returns (h, last state).
+    Without h0 the channel-threaded definition runs (same values as the carried
+    loop with no state)."""
     lib = lib or load()
     xa, xb = decode16(kind, a, lib), decode16(kind, b, lib)
     # every bfloat16 and binary16 value is a float32 value: the narrowing is exact
     fa, fb = xa.astype(np.float32), xb.astype(np.float32)
     if not (np.array_equal(fa, xa, equal_nan=True) and np.array_equal(fb, xb, equal_nan=True)):
         raise AssertionError("a decoded 16-bit value is not a float32 value")
+    if h0 is None:
+        h, _ = f64(fa.reshape(fa.shape), fb, nthreads=nthreads, lib=lib)
+        return h, np.ascontiguousarray(h[:, -1, :])
     return f64_carry(fa, fb, h0, lib=lib)
 
 
