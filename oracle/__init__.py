@@ -64,6 +64,8 @@ def _bind(lib):
     lib.linrec_oracle_f64_carry.restype = i32
     lib.linrec_oracle_f64_backward.argtypes = [pf, pf, pf, pd, pd, pd, pd, pd, i64, i64, i64]
     lib.linrec_oracle_f64_backward.restype = i32
+    lib.linrec_oracle_f64_bdl.argtypes = [pf, pf, pd, pd, pd, i64, i64, i64]
+    lib.linrec_oracle_f64_bdl.restype = i32
     pu16 = ctypes.POINTER(ctypes.c_uint16)
     lib.linrec_oracle_decode16.argtypes = [i32, pu16, pd, i64]
     lib.linrec_oracle_decode16.restype = i32
@@ -178,6 +180,27 @@ def f64_backward(a, h, g, h0=None, dhlast=None, want_da=True, lib=None):
     if rc != 0:
         raise ValueError("oracle rejected its arguments")
     return da, db, dh0
+
+
+def f64_bdl(a, b, h0=None, lib=None):
+    """The definition for (B, D, L) tensors (time innermost), continued from h0
+    ((B, D) or None); returns (h in float64, last state (B, D) in float64)."""
+    a, b = _as_f32(a), _as_f32(b)
+    if a.shape != b.shape:
+        raise ValueError("a and b differ in shape")
+    lib = lib or load()
+    B, D, L = a.shape
+    h = np.empty(a.shape, dtype=np.float64)
+    hlast = np.empty((B, D), dtype=np.float64)
+    h0p = None
+    if h0 is not None:
+        h0 = np.ascontiguousarray(h0, dtype=np.float64).reshape(B, D)
+        h0p = _ptr(h0, ctypes.c_double)
+    rc = lib.linrec_oracle_f64_bdl(_ptr(a, ctypes.c_float), _ptr(b, ctypes.c_float), h0p,
+                                   _ptr(h, ctypes.c_double), _ptr(hlast, ctypes.c_double), B, D, L)
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return h, hlast
 
 
 KINDS16 = {"bf16": 0, "f16": 1}

@@ -46,6 +46,13 @@
  *                            and da_0 = 0).  h is the forward output as given.
  *                            Not on the pages: it follows from the definition
  *                            by the chain rule.
+ *   linrec_oracle_f64_bdl -- the same definition, carried from h0 like
+ *                            linrec_oracle_f64_carry, for tensors laid out
+ *                            (B, D, L) with time innermost: element (i, d, t)
+ *                            at i*D*L + d*L + t, so each channel's sequence is
+ *                            one contiguous row.  "Kimi-K2.6 l1_p9" weighs this
+ *                            layout (its transpose discussion) as the one in
+ *                            which a warp reads a channel's steps contiguously.
  *   linrec_oracle_decode16 / linrec_oracle_encode16 -- the two 16-bit storage
  *                            formats (kind 0: bfloat16, sign 1 / exponent 8 /
  *                            fraction 7 bits, bias 127; kind 1: IEEE 754
@@ -322,5 +329,29 @@ int linrec_oracle_encode16(int kind, const double *x, uint16_t *w, int64_t n)
 {
     if (kind < 0 || kind > 1 || n < 0 || (n > 0 && (!w || !x))) return -1;
     for (int64_t i = 0; i < n; ++i) w[i] = encode16(kFmt16[kind], x[i]);
+    return 0;
+}
+
+/* (B, D, L) layout: row i*D + d holds channel (i, d) over t = 0 .. L-1.
+   h0, hlast: (B, D) or NULL, as in linrec_oracle_f64_carry. */
+int linrec_oracle_f64_bdl(const float *a, const float *b, const double *h0, double *h, double *hlast,
+                          int64_t B, int64_t D, int64_t L)
+{
+    if (B < 0 || L < 0 || D < 0) return -1;
+    if (B == 0 || D == 0 || L == 0) return 0;
+    if (!a || !b || !h) return -1;
+    for (int64_t row = 0; row < B * D; ++row) {
+        const float *ar = a + row * L;
+        const float *br = b + row * L;
+        double *hr = h + row * L;
+        double hv = (double)br[0];                          /* h_0 = b_0 */
+        if (h0) hv = (double)ar[0] * h0[row] + (double)br[0];   /* h_{-1} = h0: a_0 used */
+        hr[0] = hv;
+        for (int64_t t = 1; t < L; ++t) {
+            hv = (double)ar[t] * hv + (double)br[t];
+            hr[t] = hv;
+        }
+        if (hlast) hlast[row] = hv;
+    }
     return 0;
 }

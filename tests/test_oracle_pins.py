@@ -366,11 +366,48 @@ def pin_scan16_closed_forms(lib):
         assert np.array_equal(h, bi), f"{kind}: a = 0"
 
 
+# ---- (B, D, L) layout ---------------------------------------------------------
+
+def pin_bdl_layout_invariance(lib):
+    """Laying channels out as rows changes no value: the (B, D, L) oracle equals the
+    transpose of the (B, L, D) oracle bit for bit, with and without a state, on
+    shapes whose three sizes differ."""
+    rng = _rng(30)
+    for (B, D, L) in [(2, 3, 50), (1, 7, 5), (3, 2, 9), (2, 5, 1)]:
+        a = rng.uniform(-1.2, 1.2, (B, D, L)).astype(np.float32)
+        b = rng.normal(size=(B, D, L)).astype(np.float32)
+        h0 = rng.normal(size=(B, D))
+        at, bt = np.ascontiguousarray(a.transpose(0, 2, 1)), np.ascontiguousarray(b.transpose(0, 2, 1))
+        h, last = oracle.f64_bdl(a, b, lib=lib)
+        ht, _ = oracle.f64(at, bt, lib=lib)
+        assert np.array_equal(h, ht.transpose(0, 2, 1)), (B, D, L)
+        assert np.array_equal(last, h[:, :, -1]), (B, D, L)
+        h, last = oracle.f64_bdl(a, b, h0, lib=lib)
+        ht, lt = oracle.f64_carry(at, bt, h0, lib=lib)
+        assert np.array_equal(h, ht.transpose(0, 2, 1)) and np.array_equal(last, lt), (B, D, L)
+
+
+def pin_bdl_closed_forms(lib):
+    """a = 1: prefix sums along the last axis (plus the state); a = 0: h = b."""
+    rng = _rng(31)
+    B, D, L = 3, 4, 200
+    b = rng.integers(-8, 9, (B, D, L)).astype(np.float32)
+    h0 = rng.integers(-5, 6, (B, D)).astype(np.float64)
+    ones, zeros = np.ones_like(b), np.zeros_like(b)
+    h, _ = oracle.f64_bdl(ones, b, lib=lib)
+    assert np.array_equal(h, np.cumsum(b.astype(np.float64), axis=2))
+    h, last = oracle.f64_bdl(ones, b, h0, lib=lib)
+    assert np.array_equal(h, h0[:, :, None] + np.cumsum(b.astype(np.float64), axis=2))
+    assert np.array_equal(last, h[:, :, -1])
+    h, _ = oracle.f64_bdl(zeros, b, h0, lib=lib)
+    assert np.array_equal(h, b.astype(np.float64))
+
+
 PINS = [pin_walkthrough, pin_prefix_sum, pin_copy, pin_running_product, pin_geometric, pin_bruteforce,
         pin_carry_closed_forms, pin_carry_bruteforce, pin_carry_segments,
         pin_backward_finite_differences, pin_backward_adjoint, pin_backward_closed_forms,
         pin_backward_bruteforce, pin_decode16_library, pin_encode16_neighbours, pin_encode16_library,
-        pin_scan16_closed_forms]
+        pin_scan16_closed_forms, pin_bdl_layout_invariance, pin_bdl_closed_forms]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -468,6 +505,10 @@ MUTANTS = {
     "encode_ties_away": ("(long long)rint(ldexp(ax, f.fbits - e))", "(long long)round(ldexp(ax, f.fbits - e))"),
     "encode_no_binade_carry": ("if (n == (1ll << (f.fbits + 1))) {", "if (0) {"),
     "encode_no_overflow": ("if (field >= emask) return (uint16_t)(sign | (emask << f.fbits));", ""),
+    "bdl_wrong_row": ("const float *ar = a + row * L;", "const float *ar = a + (row % D) * L;"),
+    "bdl_state_ignored": ("if (h0) hv = (double)ar[0] * h0[row] + (double)br[0];", ""),
+    "bdl_b_from_previous_step": ("hv = (double)ar[t] * hv + (double)br[t];", "hv = (double)ar[t] * hv + (double)br[t - 1];"),
+    "bdl_last_state_first_step": ("if (hlast) hlast[row] = hv;", "if (hlast) hlast[row] = hr[0];"),
 }
 
 
