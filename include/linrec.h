@@ -57,7 +57,8 @@ typedef enum {
 typedef enum {
     LINREC_PATH_AUTO = 0,      /* the dispatcher chooses */
     LINREC_PATH_REGCARRY = 1,  /* one thread per 1/2/4 adjacent channels, loads prefetched in registers */
-    LINREC_PATH_CHUNKED = 2    /* TMA-staged (time x channel) tiles, shuffle scan, decoupled look-back */
+    LINREC_PATH_CHUNKED = 2,   /* TMA-staged (time x channel) tiles, shuffle scan, decoupled look-back */
+    LINREC_PATH_ROWS = 3       /* (B, D, L) layout: a warp per row segment, shuffle scan along the row */
 } linrec_path_t;
 
 /*
@@ -92,6 +93,8 @@ typedef struct {
     int64_t spin_limit;  /* chunked: polls of a predecessor before giving up (0 = default, ~1 s) */
     int64_t test_silent_tile; /* chunked, tests only: 0 = off; k > 0 makes tile id k-1
                                  publish nothing, so its successor's look-back times out */
+    int rows_per_warp;   /* (B, D, L) layout, one pass: consecutive rows each warp scans as one
+                            stream (0 = the dispatcher's choice) */
 } linrec_options_t;
 
 /*
@@ -245,6 +248,51 @@ linrec_status_t linrec_scan_f16_ex(const uint16_t *a, const uint16_t *b, uint16_
    align_bytes may also be 2.  Otherwise as linrec_plan_f32. */
 linrec_status_t linrec_plan_16(int64_t B, int64_t L, int64_t D, int sm_count, int align_bytes,
                                int ctas_per_sm, const linrec_options_t *opt, linrec_plan_t *plan);
+
+/*
+ * (B, D, L) layout.  linrec_scan_f32_bdl runs the same recurrence on tensors
+ * whose TIME axis is innermost: element (i, d, t) at i*D*L + d*L + t, so every
+ * channel (i, d) is one contiguous row of L values (row i*D + d):
+ *
+ *     h[i,d,0] = b[i,d,0],    h[i,d,t] = a[i,d,t] * h[i,d,t-1] + b[i,d,t].
+ *
+ * "Kimi-K2.6 l1_p9" weighs this layout (its transpose discussion) as the one
+ * in which a warp reads a channel's steps contiguously; callers that hold their
+ * data this way need no transpose.  Note the argument order B, D, L.
+ *  - Many rows: one pass, a warp per row, L read in 32*V-step chunks with a
+ *    shuffle scan and the carry in a register.  Few long rows: two passes over
+ *    row segments (each segment's map, the scan of those maps by the (B, L, D)
+ *    kernels, each segment rescanned from its carry): 20 bytes per fp32
+ *    element instead of 12.
+ *  - Vector width V (stored elements per lane per chunk, 16 bytes at most) is
+ *    the widest that divides L and the pointers' alignment allows; any
+ *    alignment of the element type works.
+ *  - The _ex forms take the options: h_init / h_last ((B, D) fp32, row i*D + d,
+ *    as for linrec_scan_f32_carry), d_status, vec (1, 2, 4 or, for 16-bit
+ *    storage, 8), prefetch (2 or 4 chunks), chunk_mode (0 auto, 1 one pass,
+ *    3 two passes); path must be 0 or LINREC_PATH_ROWS.
+ * Other conventions as for linrec_scan_f32 (and, for the 16-bit forms, as for
+ * linrec_scan_bf16 / linrec_scan_f16).
+ */
+linrec_status_t linrec_scan_f32_bdl(const float *a, const float *b, float *h,
+                                    int64_t B, int64_t D, int64_t L, void *stream);
+linrec_status_t linrec_scan_f32_bdl_ex(const float *a, const float *b, float *h,
+                                       int64_t B, int64_t D, int64_t L, void *stream,
+                                       const linrec_options_t *opt);
+linrec_status_t linrec_scan_bf16_bdl_ex(const uint16_t *a, const uint16_t *b, uint16_t *h,
+                                        int64_t B, int64_t D, int64_t L, void *stream,
+                                        const linrec_options_t *opt);
+linrec_status_t linrec_scan_f16_bdl_ex(const uint16_t *a, const uint16_t *b, uint16_t *h,
+                                       int64_t B, int64_t D, int64_t L, void *stream,
+                                       const linrec_options_t *opt);
+
+/* The dispatcher's decision for the (B, D, L) layout with elem_bytes-byte storage
+   (4: fp32, 2: bfloat16 or binary16).  path = LINREC_PATH_ROWS; vec, prefetch;
+   one pass: tile_d = consecutive rows per warp; two passes: tile_t = the
+   segment length, chunks = segments per row; n_tiles = warps (units of work);
+   twopass; workspace_bytes = the two-pass arrays. */
+linrec_status_t linrec_plan_bdl(int64_t B, int64_t D, int64_t L, int elem_bytes, int sm_count,
+                                int align_bytes, const linrec_options_t *opt, linrec_plan_t *plan);
 
 /*
  * linrec_stream_status -- synchronise `stream`, then return and clear the

@@ -20,6 +20,9 @@ Functions keep the C names:
     linrec_scan_bf16_ex / linrec_scan_f16_ex(a, b, h=None, stream=None, **options) -> h
     linrec_plan_f32(B, L, D, sm_count=152, align_bytes=16, resident_ctas=0, **options) -> dict
     linrec_plan_16(B, L, D, sm_count=152, align_bytes=16, resident_ctas=0, **options) -> dict
+    linrec_scan_f32_bdl(a, b, h=None, stream=None) -> h    ((B, D, L) tensors: time innermost)
+    linrec_scan_f32_bdl_ex / linrec_scan_bf16_bdl_ex / linrec_scan_f16_bdl_ex(a, b, h=None, stream=None, **options)
+    linrec_plan_bdl(B, D, L, elem_bytes=4, sm_count=152, align_bytes=16, **options) -> dict
     linrec_stream_status(stream=None) -> int
     linrec_copy_f32(src, dst, stream=None)
     linrec_status_string(code) -> str
@@ -42,7 +45,7 @@ LINREC_ERR_WORKSPACE = 5
 LINREC_ERR_LOOKBACK_TIMEOUT = 6
 LINREC_ERR_TMA_TIMEOUT = 7
 
-PATHS = {"auto": 0, "regcarry": 1, "chunked": 2}
+PATHS = {"auto": 0, "regcarry": 1, "chunked": 2, "rows": 3}
 PATH_NAMES = {v: k for k, v in PATHS.items()}
 
 
@@ -67,6 +70,7 @@ class Options(ctypes.Structure):
         ("h_last", ctypes.c_void_p),
         ("spin_limit", ctypes.c_int64),
         ("test_silent_tile", ctypes.c_int64),
+        ("rows_per_warp", ctypes.c_int),
     ]
 
 
@@ -130,6 +134,13 @@ def lib():
             getattr(L, name + "_ex").restype = i32
         L.linrec_plan_16.argtypes = [i64, i64, i64, i32, i32, i32, ctypes.POINTER(Options), ctypes.POINTER(Plan)]
         L.linrec_plan_16.restype = i32
+        L.linrec_scan_f32_bdl.argtypes = [vp, vp, vp, i64, i64, i64, vp]
+        L.linrec_scan_f32_bdl.restype = i32
+        for name in ("linrec_scan_f32_bdl_ex", "linrec_scan_bf16_bdl_ex", "linrec_scan_f16_bdl_ex"):
+            getattr(L, name).argtypes = [vp, vp, vp, i64, i64, i64, vp, ctypes.POINTER(Options)]
+            getattr(L, name).restype = i32
+        L.linrec_plan_bdl.argtypes = [i64, i64, i64, i32, i32, i32, ctypes.POINTER(Options), ctypes.POINTER(Plan)]
+        L.linrec_plan_bdl.restype = i32
         L.linrec_stream_status.argtypes = [vp]
         L.linrec_stream_status.restype = i32
         L.linrec_copy_f32.argtypes = [vp, vp, i64, vp]
@@ -162,7 +173,7 @@ def _addr(x):
 
 def make_options(path="auto", vec=0, prefetch=0, tile_t=0, tile_d=0, stages=0, ctas_per_sm=0,
                  chunk_mode="auto", d_status=None, h_init=None, h_last=None, spin_limit=0,
-                 test_silent_tile=0) -> Options:
+                 test_silent_tile=0, rows_per_warp=0) -> Options:
     o = Options()
     o.path = PATHS[path] if isinstance(path, str) else int(path)
     o.vec, o.prefetch, o.tile_t, o.tile_d, o.stages = int(vec), int(prefetch), int(tile_t), int(tile_d), int(stages)
@@ -173,6 +184,7 @@ def make_options(path="auto", vec=0, prefetch=0, tile_t=0, tile_d=0, stages=0, c
     o.h_last = _addr(h_last)
     o.spin_limit = int(spin_limit)
     o.test_silent_tile = int(test_silent_tile)
+    o.rows_per_warp = int(rows_per_warp)
     return o
 
 
@@ -267,6 +279,59 @@ def linrec_scan_f16_ex(a, b, h=None, stream=None, **options):
     """linrec_scan_f16 with explicit options; h_init / h_last are float32 (B, D) tensors."""
     import torch
     return _scan16("linrec_scan_f16_ex", torch.float16, a, b, h, stream, options)
+
+
+def _scan_bdl(fn, dtype, a, b, h, stream, options):
+    import torch
+    B, D, L = _shape_of(a, b, h, dtype)
+    if h is None:
+        h = torch.empty_like(a)
+    if options is None:
+        code = getattr(lib(), fn)(a.data_ptr(), b.data_ptr(), h.data_ptr(), B, D, L, _stream_handle(stream))
+    else:
+        _check_state(options.get("h_init"), "h_init", B, D)
+        _check_state(options.get("h_last"), "h_last", B, D)
+        opt = make_options(**options)
+        code = getattr(lib(), fn)(a.data_ptr(), b.data_ptr(), h.data_ptr(), B, D, L, _stream_handle(stream),
+                                  ctypes.byref(opt))
+    _check(code, fn)
+    return h
+
+
+def linrec_scan_f32_bdl(a, b, h=None, stream=None):
+    """h = scan(a, b) on float32 CUDA tensors laid out (B, D, L): time innermost, each channel a row."""
+    import torch
+    return _scan_bdl("linrec_scan_f32_bdl", torch.float32, a, b, h, stream, None)
+
+
+def linrec_scan_f32_bdl_ex(a, b, h=None, stream=None, **options):
+    """linrec_scan_f32_bdl with options (chunk_mode "own" = one pass, "twopass"; h_init / h_last (B, D))."""
+    import torch
+    return _scan_bdl("linrec_scan_f32_bdl_ex", torch.float32, a, b, h, stream, options)
+
+
+def linrec_scan_bf16_bdl_ex(a, b, h=None, stream=None, **options):
+    """The (B, D, L) scan on torch.bfloat16 tensors (fp32 arithmetic); h_init / h_last float32 (B, D)."""
+    import torch
+    return _scan_bdl("linrec_scan_bf16_bdl_ex", torch.bfloat16, a, b, h, stream, options)
+
+
+def linrec_scan_f16_bdl_ex(a, b, h=None, stream=None, **options):
+    """The (B, D, L) scan on torch.float16 tensors (fp32 arithmetic); h_init / h_last float32 (B, D)."""
+    import torch
+    return _scan_bdl("linrec_scan_f16_bdl_ex", torch.float16, a, b, h, stream, options)
+
+
+def linrec_plan_bdl(B, D, L, elem_bytes=4, sm_count=152, align_bytes=16, **options) -> dict:
+    """The (B, D, L) dispatcher's choice, without a GPU (elem_bytes 4: fp32, 2: 16-bit storage)."""
+    opt = make_options(**options)
+    plan = Plan()
+    code = lib().linrec_plan_bdl(int(B), int(D), int(L), int(elem_bytes), int(sm_count), int(align_bytes),
+                                 ctypes.byref(opt), ctypes.byref(plan))
+    _check(code, "linrec_plan_bdl")
+    out = {name: getattr(plan, name) for name, _ in Plan._fields_}
+    out["path_name"] = PATH_NAMES.get(out["path"], "none")
+    return out
 
 
 def _check_state(x, name, B, D):

@@ -121,6 +121,31 @@ cudaError_t launch_regcarry_backward(int vec, int threads, const float *a, const
                                      float *db, int64_t B, int64_t L, int64_t D, const float *h_init,
                                      const float *dh_last, float *dh_init, cudaStream_t stream);
 
+// ---- (B, D, L) layout: one warp per row segment ------------------------------
+constexpr int kRowsThreads = 256;
+constexpr int kRowsFull = 0;     // whole rows, carry from h_init (or 0), write h
+constexpr int kRowsReduce = 1;   // two-pass, first launch: each segment's composed map to aggA / aggB
+constexpr int kRowsApply = 2;    // two-pass, last launch: rescan each segment from the h before it
+
+struct RowsLaunch {
+    int dtype = kDtypeF32;
+    int vec = 4;                 // stored elements per lane per chunk (one vector load)
+    int prefetch = 4;            // chunks whose loads are in flight ahead (2 or 4)
+    const void *a = nullptr, *b = nullptr;
+    void *h = nullptr;
+    int64_t R = 0, L = 0;        // rows (B * D) and their length
+    int64_t seg_len = 0, nseg = 1;   // segment length (a multiple of 32 * vec) and segments per row
+    int64_t rows_per_unit = 1;       // one pass: consecutive whole rows per warp (1 when nseg > 1)
+    int mode = kRowsFull;
+    const float *h_init = nullptr;   // (R) state each row continues from, or NULL
+    float *h_last = nullptr;         // (R) last state out, or NULL
+    float *aggA = nullptr, *aggB = nullptr;   // two-pass: [segment][row] composed maps
+    const float *aggH = nullptr;              // two-pass: [segment][row] last h of each segment
+    float *aggX = nullptr;                    // two-pass with h_init: (R) copy of the state for the apply launch
+};
+bool rows_supported(int dtype, int vec, int prefetch);
+cudaError_t launch_rows(const RowsLaunch &args, cudaStream_t stream);
+
 // ---- copy-ceiling kernel ---------------------------------------------------
 cudaError_t launch_copy(const float *src, float *dst, int64_t n, int sm_count, cudaStream_t stream);
 

@@ -22,6 +22,18 @@ constexpr int kRegcarryThreads = 256;
 // Few slices: the two-pass mode from this many time chunks of 128 steps on.
 constexpr int64_t kTwoPassMinChunks = 64;
 constexpr size_t kWorkspaceHead = 256;      // Control block, padded
+// (B, D, L) layout: rows alone give each SM this many warps -> one pass, each warp
+// scanning consecutive rows until it holds about kRowsStreamElems[16-bit] elements,
+// while at least kRowsStreamWarps warps per SM remain (measured on GB300: the many
+// short rows of the (256, 4096, 128) shape want 16 rows per warp in fp32, 64 in
+// 16-bit storage); otherwise two passes over segments of at least
+// kRowsMinSegChunks chunks, about kRowsTargetWarps warps per SM in all.
+constexpr int64_t kRowsMinWarps = 16;
+constexpr int64_t kRowsStreamWarps = 32;
+constexpr int64_t kRowsStreamElems = 2048;
+constexpr int64_t kRowsStreamElems16 = 8192;
+constexpr int64_t kRowsTargetWarps = 32;
+constexpr int64_t kRowsMinSegChunks = 8;
 
 struct DeviceInfo {
     bool ready = false;
@@ -399,6 +411,139 @@ linrec_status_t scan_locked(DeviceInfo *di, int dev, const void *a, const void *
     return LINREC_OK;
 }
 
+// The (B, D, L) dispatcher: vector width, one pass or two, segment length.
+linrec_status_t plan_bdl_impl(int64_t B, int64_t D, int64_t L, int dtype, int sm_count, int align_bytes,
+                              const linrec_options_t *opt, linrec_plan_t *plan, int64_t *seg_len_out) {
+    linrec_options_t none = {};
+    if (!opt) opt = &none;
+    if (!plan || sm_count <= 0 || dtype < 0 || dtype > 2) return LINREC_ERR_INVALID_VALUE;
+    int64_t n = 0;
+    linrec_status_t st = check_sizes(B, L, D, &n);
+    if (st != LINREC_OK) return st;
+    *plan = linrec_plan_t{};
+    plan->path = LINREC_PATH_ROWS;
+    if (opt->path != LINREC_PATH_AUTO && opt->path != LINREC_PATH_ROWS) return LINREC_ERR_INVALID_VALUE;
+    if (opt->chunk_mode != 0 && opt->chunk_mode != 1 && opt->chunk_mode != 3) return LINREC_ERR_INVALID_VALUE;
+    if (n == 0) return LINREC_OK;
+    const int eb = elem_bytes_of(dtype);
+    int vec = opt->vec;
+    if (vec == 0) {
+        vec = 16 / eb;
+        while (vec > 1 && (L % vec != 0 || align_bytes < eb * vec)) vec /= 2;
+    }
+    if (vec <= 0 || (vec & (vec - 1)) != 0 || vec * eb > 16 || L % vec != 0 || align_bytes < eb * vec)
+        return LINREC_ERR_INVALID_VALUE;
+    const int64_t R = B * D;
+    const int64_t ch = 32 * (int64_t)vec;
+    if (opt->rows_per_warp < 0 || (opt->rows_per_warp > 0 && opt->chunk_mode == 3)) return LINREC_ERR_INVALID_VALUE;
+    bool twopass = opt->chunk_mode == 3;
+    if (opt->chunk_mode == 0)
+        twopass = opt->rows_per_warp == 0 && R < kRowsMinWarps * sm_count && L >= 2 * kRowsMinSegChunks * ch;
+    int64_t seg_len = L, nseg = 1;
+    if (twopass) {
+        const int64_t want = (kRowsTargetWarps * sm_count + R - 1) / R;   // segments per row
+        int64_t len = (L + want - 1) / want;
+        len = (len + ch - 1) / ch * ch;
+        if (len < kRowsMinSegChunks * ch) len = kRowsMinSegChunks * ch;
+        seg_len = len;
+        nseg = (L + seg_len - 1) / seg_len;
+        if (nseg < 2 && opt->chunk_mode == 0) {
+            twopass = false;
+            seg_len = L;
+            nseg = 1;
+        }
+    }
+    int64_t k = 1;                            // rows per warp (one pass)
+    if (!twopass) {
+        if (opt->rows_per_warp > 0) {
+            k = opt->rows_per_warp;
+        } else {
+            k = (eb == 4 ? kRowsStreamElems : kRowsStreamElems16) / L;
+            const int64_t cap = R / (kRowsStreamWarps * sm_count);
+            if (k > cap) k = cap;
+        }
+        if (k < 1) k = 1;
+        if (k > R) k = R;
+    }
+    // loads in flight: 2 chunks (measured best on every one-pass shape and on fp32 two
+    // passes), 4 for 16-bit two passes
+    const int prefetch = opt->prefetch ? opt->prefetch : (twopass && eb == 2 ? 4 : 2);
+    if (!rows_supported(dtype, vec, prefetch)) return LINREC_ERR_INVALID_VALUE;
+    const int64_t units = twopass ? R * nseg : (R + k - 1) / k;
+    plan->vec = vec;
+    plan->prefetch = prefetch;
+    plan->tile_t = seg_len > INT32_MAX ? INT32_MAX : (int)seg_len;
+    plan->tile_d = k > INT32_MAX ? INT32_MAX : (int)k;
+    plan->chunks = nseg;
+    plan->twopass = twopass ? 1 : 0;
+    plan->threads = kRowsThreads;
+    plan->n_tiles = units;
+    plan->grid = (units * 32 + kRowsThreads - 1) / kRowsThreads;
+    plan->workspace_bytes = twopass ? kWorkspaceHead + (size_t)(3 * nseg * R + R) * 4u : 0;
+    if (seg_len_out) *seg_len_out = seg_len;
+    return LINREC_OK;
+}
+
+// The (B, D, L) scan, arguments checked, g_mu held.
+linrec_status_t scan_bdl_locked(DeviceInfo *di, int dev, const void *a, const void *b, void *h, int64_t B,
+                                int64_t D, int64_t L, int dtype, cudaStream_t stream, const linrec_options_t *opt) {
+    linrec_plan_t plan;
+    int64_t seg_len = 0;
+    linrec_status_t st = plan_bdl_impl(B, D, L, dtype, di->sm_count, align_of(a, b, h), opt, &plan, &seg_len);
+    if (st != LINREC_OK) return st;
+    RowsLaunch p;
+    p.dtype = dtype;
+    p.vec = plan.vec;
+    p.prefetch = plan.prefetch;
+    p.a = a;
+    p.b = b;
+    p.h = h;
+    p.R = B * D;
+    p.L = L;
+    p.seg_len = seg_len;
+    p.nseg = plan.chunks;
+    p.rows_per_unit = plan.twopass ? 1 : plan.tile_d;
+    p.h_init = opt->h_init;
+    p.h_last = opt->h_last;
+    if (!plan.twopass) {
+        p.mode = kRowsFull;
+        if (launch_rows(p, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return LINREC_ERR_LAUNCH;
+        }
+        return LINREC_OK;
+    }
+    // Two passes: the segments' maps, laid out (1, segments, rows), scanned by the (B, L, D) path.
+    Slot *ws = workspace(dev, stream, kWorkspaceHead, 0);            // control block: status word
+    if (!ws) return LINREC_ERR_WORKSPACE;
+    const size_t cells = (size_t)(p.nseg * p.R);
+    Slot *arr = workspace(dev, stream, (3 * cells + (size_t)p.R) * 4u, 0, kSlotArrays);
+    if (!arr) return LINREC_ERR_WORKSPACE;
+    float *aggA = reinterpret_cast<float *>(arr->base);
+    float *aggB = aggA + cells;
+    float *aggH = aggB + cells;
+    p.aggA = aggA;
+    p.aggB = aggB;
+    p.aggH = aggH;
+    p.aggX = aggH + cells;
+    p.mode = kRowsReduce;
+    if (launch_rows(p, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return LINREC_ERR_LAUNCH;
+    }
+    linrec_options_t inner = {};
+    inner.d_status = opt->d_status ? opt->d_status : &reinterpret_cast<Control *>(ws->base)->status;
+    inner.spin_limit = opt->spin_limit;
+    st = scan_locked(di, dev, aggA, aggB, aggH, 1, p.nseg, p.R, kDtypeF32, stream, &inner, 1);
+    if (st != LINREC_OK) return st;
+    p.mode = kRowsApply;
+    if (launch_rows(p, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return LINREC_ERR_LAUNCH;
+    }
+    return LINREC_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -428,9 +573,11 @@ linrec_status_t linrec_plan_f32(int64_t B, int64_t L, int64_t D, int sm_count, i
 
 namespace {
 
-// The forward entry points: argument checks, then scan_locked.
-linrec_status_t scan_entry(int dtype, const void *a, const void *b, void *h, int64_t B, int64_t L, int64_t D,
-                           void *stream_ptr, const linrec_options_t *opt) {
+// The forward entry points: argument checks, then the scan.  B, L, D are the
+// batch, time and channel sizes in either layout; bdl selects the time-innermost
+// (B, D, L) layout, otherwise the tensors are (B, L, D).
+linrec_status_t scan_entry(int dtype, bool bdl, const void *a, const void *b, void *h, int64_t B, int64_t L,
+                           int64_t D, void *stream_ptr, const linrec_options_t *opt) {
     linrec_options_t none = {};
     if (!opt) opt = &none;
     int64_t n = 0;
@@ -461,6 +608,7 @@ linrec_status_t scan_entry(int dtype, const void *a, const void *b, void *h, int
     if (!di) return LINREC_ERR_LAUNCH;
     if (!di->supported) return LINREC_ERR_UNSUPPORTED_DEVICE;
 
+    if (bdl) return scan_bdl_locked(di, dev, a, b, h, B, D, L, dtype, stream, opt);
     return scan_locked(di, dev, a, b, h, B, L, D, dtype, stream, opt, 0);
 }
 
@@ -470,32 +618,59 @@ extern "C" {
 
 linrec_status_t linrec_scan_f32_ex(const float *a, const float *b, float *h, int64_t B, int64_t L, int64_t D,
                                    void *stream, const linrec_options_t *opt) {
-    return scan_entry(kDtypeF32, a, b, h, B, L, D, stream, opt);
+    return scan_entry(kDtypeF32, false, a, b, h, B, L, D, stream, opt);
 }
 
 linrec_status_t linrec_scan_bf16_ex(const uint16_t *a, const uint16_t *b, uint16_t *h, int64_t B, int64_t L,
                                     int64_t D, void *stream, const linrec_options_t *opt) {
-    return scan_entry(kDtypeBF16, a, b, h, B, L, D, stream, opt);
+    return scan_entry(kDtypeBF16, false, a, b, h, B, L, D, stream, opt);
 }
 
 linrec_status_t linrec_scan_f16_ex(const uint16_t *a, const uint16_t *b, uint16_t *h, int64_t B, int64_t L,
                                    int64_t D, void *stream, const linrec_options_t *opt) {
-    return scan_entry(kDtypeF16, a, b, h, B, L, D, stream, opt);
+    return scan_entry(kDtypeF16, false, a, b, h, B, L, D, stream, opt);
 }
 
 linrec_status_t linrec_scan_bf16(const uint16_t *a, const uint16_t *b, uint16_t *h, int64_t B, int64_t L,
                                  int64_t D, void *stream) {
-    return scan_entry(kDtypeBF16, a, b, h, B, L, D, stream, nullptr);
+    return scan_entry(kDtypeBF16, false, a, b, h, B, L, D, stream, nullptr);
 }
 
 linrec_status_t linrec_scan_f16(const uint16_t *a, const uint16_t *b, uint16_t *h, int64_t B, int64_t L, int64_t D,
                                 void *stream) {
-    return scan_entry(kDtypeF16, a, b, h, B, L, D, stream, nullptr);
+    return scan_entry(kDtypeF16, false, a, b, h, B, L, D, stream, nullptr);
 }
 
 linrec_status_t linrec_plan_16(int64_t B, int64_t L, int64_t D, int sm_count, int align_bytes, int ctas_per_sm,
                                const linrec_options_t *opt, linrec_plan_t *plan) {
     return plan_impl(B, L, D, sm_count, align_bytes, ctas_per_sm, opt, plan, nullptr, false, true, kDtypeBF16);
+}
+
+linrec_status_t linrec_scan_f32_bdl(const float *a, const float *b, float *h, int64_t B, int64_t D, int64_t L,
+                                    void *stream) {
+    return scan_entry(kDtypeF32, true, a, b, h, B, L, D, stream, nullptr);
+}
+
+linrec_status_t linrec_scan_f32_bdl_ex(const float *a, const float *b, float *h, int64_t B, int64_t D, int64_t L,
+                                       void *stream, const linrec_options_t *opt) {
+    return scan_entry(kDtypeF32, true, a, b, h, B, L, D, stream, opt);
+}
+
+linrec_status_t linrec_scan_bf16_bdl_ex(const uint16_t *a, const uint16_t *b, uint16_t *h, int64_t B, int64_t D,
+                                        int64_t L, void *stream, const linrec_options_t *opt) {
+    return scan_entry(kDtypeBF16, true, a, b, h, B, L, D, stream, opt);
+}
+
+linrec_status_t linrec_scan_f16_bdl_ex(const uint16_t *a, const uint16_t *b, uint16_t *h, int64_t B, int64_t D,
+                                       int64_t L, void *stream, const linrec_options_t *opt) {
+    return scan_entry(kDtypeF16, true, a, b, h, B, L, D, stream, opt);
+}
+
+linrec_status_t linrec_plan_bdl(int64_t B, int64_t D, int64_t L, int elem_bytes, int sm_count, int align_bytes,
+                                const linrec_options_t *opt, linrec_plan_t *plan) {
+    if (elem_bytes != 4 && elem_bytes != 2) return LINREC_ERR_INVALID_VALUE;
+    return plan_bdl_impl(B, D, L, elem_bytes == 4 ? kDtypeF32 : kDtypeBF16, sm_count, align_bytes, opt, plan,
+                         nullptr);
 }
 
 linrec_status_t linrec_scan_f32(const float *a, const float *b, float *h, int64_t B, int64_t L, int64_t D,

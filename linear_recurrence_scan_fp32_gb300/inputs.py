@@ -144,3 +144,8 @@ def to_storage16(x: torch.Tensor, kind: str) -> torch.Tensor:
     stored words are the test input itself, given to both the CUDA path and the
     oracle (which decodes them by its own definition of the format)."""
     return x.to(STORAGE16[kind]).contiguous()
+
+
+def to_bdl(x: torch.Tensor) -> torch.Tensor:
+    """A (B, L, D) draw laid out (B, D, L), time innermost: the same values, moved."""
+    return x.transpose(1, 2).contiguous()

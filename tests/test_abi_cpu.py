@@ -235,3 +235,43 @@ def test_16bit_argument_checks_count_two_bytes(L):
         assert f(None, base, base + 4 * n2, B, Lx, D, None) == lr.LINREC_ERR_INVALID_VALUE
         assert f(base, base, base, -1, Lx, D, None) == lr.LINREC_ERR_INVALID_VALUE
         assert f(None, None, None, 0, Lx, D, None) == lr.LINREC_OK
+
+
+def test_plan_bdl_layout():
+    # many rows: one pass, a warp per row, 16-byte vectors when L and the pointers allow
+    p = lr.linrec_plan_bdl(32, 256, 4096, sm_count=152)
+    assert (p["path_name"], p["vec"], p["twopass"], p["chunks"], p["n_tiles"]) == ("rows", 4, 0, 1, 32 * 256)
+    assert p["grid"] * p["threads"] >= 32 * p["n_tiles"] and p["workspace_bytes"] == 0
+    # few long rows: two passes over segments that are whole chunks, about 32 warps per SM
+    p = lr.linrec_plan_bdl(1, 64, 1 << 20, sm_count=152)
+    assert p["twopass"] == 1 and p["tile_t"] % (32 * p["vec"]) == 0
+    assert p["chunks"] == -(-(1 << 20) // p["tile_t"]) and p["n_tiles"] == 64 * p["chunks"]
+    assert 152 * 16 <= p["n_tiles"] <= 152 * 64
+    assert p["workspace_bytes"] == 256 + 4 * (3 * p["n_tiles"] + 64)
+    # short rows stay in one pass whatever their number
+    assert lr.linrec_plan_bdl(1, 4, 1000)["twopass"] == 0
+    # the vector width follows L and the alignment; 16-bit storage reaches 8 elements
+    assert lr.linrec_plan_bdl(2, 3, 1001)["vec"] == 1
+    assert lr.linrec_plan_bdl(2, 3, 1002)["vec"] == 2
+    assert lr.linrec_plan_bdl(2, 3, 1000, align_bytes=8)["vec"] == 2
+    assert lr.linrec_plan_bdl(2, 3, 1000, elem_bytes=2)["vec"] == 8
+    assert lr.linrec_plan_bdl(2, 3, 1000, elem_bytes=2, align_bytes=2)["vec"] == 1
+    # forced modes and invalid options
+    assert lr.linrec_plan_bdl(32, 256, 4096, chunk_mode="twopass")["twopass"] == 1
+    assert lr.linrec_plan_bdl(1, 64, 1 << 20, chunk_mode="own")["twopass"] == 0
+    for bad in ({"chunk_mode": "lookback"}, {"path": "chunked"}, {"vec": 3}, {"vec": 8}, {"prefetch": 3}):
+        with pytest.raises(lr.LinrecError):
+            lr.linrec_plan_bdl(2, 3, 1000, **bad)
+    with pytest.raises(lr.LinrecError):
+        lr.linrec_plan_bdl(2, 3, 1000, elem_bytes=8)
+
+
+def test_bdl_argument_checks(L):
+    base = 1 << 36
+    B, D, Lx = 2, 3, 16
+    n = B * D * Lx * 4
+    f = L.linrec_scan_f32_bdl
+    assert f(base, base + 2 * n, base + 2 * n - 4, B, D, Lx, None) == lr.LINREC_ERR_ALIAS
+    assert f(None, base, base + 2 * n, B, D, Lx, None) == lr.LINREC_ERR_INVALID_VALUE
+    assert f(base, base, base + n, B, -1, Lx, None) == lr.LINREC_ERR_INVALID_VALUE
+    assert f(None, None, None, B, D, 0, None) == lr.LINREC_OK
