@@ -14,6 +14,9 @@ on the same workload: the reference arm of this comparison.
 
 --dtype bf16 | f16 stores a, b and h in 16 bits (fp32 arithmetic and carry):
 6 bytes per element instead of 12, the same GB/s metric over those bytes.
+
+--layout bdl holds the same values time-innermost, (B, D, L), and times the
+(B, D, L) entry points on them.
 """
 from __future__ import annotations
 
@@ -40,14 +43,16 @@ WORKLOAD = "pages"          # the headline workload; --workload picks another fo
 STORAGE_BYTES = {"f32": 4, "bf16": 2, "f16": 2}
 
 
-def metric_for(w, op: str = "forward", dtype: str = "f32") -> str:
+def metric_for(w, op: str = "forward", dtype: str = "f32", layout: str = "bld") -> str:
     if op == "backward":
         return (f"scan backward GB/s (a,h,g read, da,db written) & % of GB300 HBM peak at "
                 f"B={w.B},L={w.L},D={w.D} fp32 ({w.name})")
-    if w.name == WORKLOAD and dtype == "f32":
+    if w.name == WORKLOAD and dtype == "f32" and layout == "bld":
         return METRIC
     store = "fp32" if dtype == "f32" else f"{dtype} storage, fp32 arithmetic"
-    return f"scan GB/s (a,b,h bytes) & % of GB300 HBM peak at B={w.B},L={w.L},D={w.D} {store} ({w.name})"
+    lay = "" if layout == "bld" else ", (B,D,L) layout"
+    return (f"scan GB/s (a,b,h bytes) & % of GB300 HBM peak at B={w.B},L={w.L},D={w.D} {store}{lay} "
+            f"({w.name})")
 
 
 def bytes_per_step(w, op: str, dtype: str = "f32") -> int:
@@ -61,7 +66,7 @@ def launches_per_step(plan: dict, op: str) -> int:
     """Kernel launches of one call.  Two-pass mode: the reduce launch, the scan of the
     tile aggregates (one launch: at that level the dispatcher takes the slice-owner or
     look-back mode, never two-pass again) and the apply launch."""
-    if op == "forward" and plan["path_name"] == "chunked" and plan["twopass"]:
+    if op == "forward" and plan["path_name"] in ("chunked", "rows") and plan["twopass"]:
         return 3
     return 1
 FALLBACK_HBM_GBS = 6800.0
@@ -278,7 +283,7 @@ def run_reference(args):
     total = sum(times)
     value = sample_bytes * args.steps / total / 1e9
     line = {
-        "impl": "reference", "metric": metric_for(w, "forward", args.dtype), "value": round(value, 3), "unit": UNIT,
+        "impl": "reference", "metric": metric_for(w, "forward", args.dtype, args.layout), "value": round(value, 3), "unit": UNIT,
         "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -318,6 +323,12 @@ def run_ours(args):
         if args.op != "forward":
             raise SystemExit("16-bit storage is forward only")
         a_cpu, b_cpu = inputs.to_storage16(a_cpu, args.dtype), inputs.to_storage16(b_cpu, args.dtype)
+    bdl = args.layout == "bdl"
+    if bdl:
+        if args.op != "forward":
+            raise SystemExit("the (B, D, L) layout is timed forward only")
+        a_cpu = a_cpu.transpose(1, 2).contiguous()
+        b_cpu = b_cpu.transpose(1, 2).contiguous()
     a = a_cpu.to(dev)
     b = b_cpu.to(dev)
     h = torch.empty_like(a)
@@ -329,15 +340,24 @@ def run_ours(args):
         td, tt, st = (int(x) for x in args.tile.split(","))
         opt.update(path="chunked", tile_d=td, tile_t=tt, stages=st)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    plan_fn = lr.linrec_plan_f32 if args.dtype == "f32" else lr.linrec_plan_16
-    plan = plan_fn(w.B, w.L, w.D, sm_count=sms, **opt)
     store = "" if args.dtype == "f32" else "_" + args.dtype
-    if plan["path_name"] == "chunked":
-        mode = "_twopass" if plan["twopass"] else "_lookback" if plan["lookback"] else ""
-        kernel_tag = "chunked" + store + mode
+    if bdl:
+        if args.tile or args.path not in ("auto", "rows"):
+            raise SystemExit("the (B, D, L) layout takes --chunk-mode own | twopass only")
+        opt = {} if args.chunk_mode == "auto" else {"chunk_mode": args.chunk_mode}
+        plan = lr.linrec_plan_bdl(w.B, w.D, w.L, elem_bytes=STORAGE_BYTES[args.dtype], sm_count=sms, **opt)
+        kernel_tag = "rows" + store + ("_twopass" if plan["twopass"] else "")
+        scan16 = {"f32": lr.linrec_scan_f32_bdl_ex, "bf16": lr.linrec_scan_bf16_bdl_ex,
+                  "f16": lr.linrec_scan_f16_bdl_ex}[args.dtype]
     else:
-        kernel_tag = "regcarry" + store
-    scan16 = {"bf16": lr.linrec_scan_bf16_ex, "f16": lr.linrec_scan_f16_ex}.get(args.dtype)
+        plan_fn = lr.linrec_plan_f32 if args.dtype == "f32" else lr.linrec_plan_16
+        plan = plan_fn(w.B, w.L, w.D, sm_count=sms, **opt)
+        if plan["path_name"] == "chunked":
+            mode = "_twopass" if plan["twopass"] else "_lookback" if plan["lookback"] else ""
+            kernel_tag = "chunked" + store + mode
+        else:
+            kernel_tag = "regcarry" + store
+        scan16 = {"bf16": lr.linrec_scan_bf16_ex, "f16": lr.linrec_scan_f16_ex}.get(args.dtype)
 
     if args.op == "backward":
         lr.linrec_scan_f32(a, b, h, stream=stream)          # the forward output the gradient needs
@@ -354,6 +374,8 @@ def run_ours(args):
     def step():
         if args.op == "backward":
             lr.linrec_scan_f32_backward(a, h, gd, da=da, db=db, stream=stream, **opt)
+        elif bdl and not opt and args.dtype == "f32":
+            lr.linrec_scan_f32_bdl(a, b, h, stream=stream)
         elif scan16 is not None:
             scan16(a, b, h, stream=stream, **opt)
         elif opt:
@@ -428,7 +450,7 @@ def run_ours(args):
         h_h = torch.empty_like(a_cpu).pin_memory()
         e_steps = max(3, min(args.steps, 20))
 
-        if scan16 is None:
+        if scan16 is None and not bdl:
             def e2e_step():
                 lr.linrec_scan_f32_host(a_h, b_h, h_h, stream=stream)
             e2e_path = ("linrec_scan_f32_host on pinned host a, b, h: the kernel reads and writes host "
@@ -439,7 +461,8 @@ def run_ours(args):
                 b.copy_(b_h, non_blocking=True)
                 scan16(a, b, h, stream=stream)
                 h_h.copy_(h, non_blocking=True)
-            e2e_path = f"pinned host a, b copied in, linrec_scan_{args.dtype}_ex, h copied out, one stream"
+            e2e_path = (f"pinned host a, b copied in, linrec_scan_{args.dtype}{'_bdl' if bdl else ''}_ex, "
+                        "h copied out, one stream")
 
         for _ in range(2):
             e2e_step()
@@ -462,21 +485,24 @@ def run_ours(args):
             cpu = cpu_baseline_backward(a_cpu.numpy(), h.cpu().numpy(), g_cpu.numpy(), w, nbytes,
                                         budget_s=args.cpu_seconds)
         else:
+            # the oracle scans (B, L, D); the (B, D, L) values are the same numbers transposed
+            ca, cb = (a_cpu.transpose(1, 2).contiguous(), b_cpu.transpose(1, 2).contiguous()) if bdl \
+                else (a_cpu, b_cpu)
             if args.dtype == "f32":
-                cpu = cpu_baseline(a_cpu.numpy(), b_cpu.numpy(), w, budget_s=args.cpu_seconds)
+                cpu = cpu_baseline(ca.numpy(), cb.numpy(), w, budget_s=args.cpu_seconds)
             else:
-                cpu = cpu_baseline(a_cpu, b_cpu, w, budget_s=args.cpu_seconds, dtype=args.dtype)
+                cpu = cpu_baseline(ca, cb, w, budget_s=args.cpu_seconds, dtype=args.dtype)
 
     if rank == 0:
         clk = clocks.summary()
         line = {
-            "metric": metric_for(w, args.op, args.dtype), "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+            "metric": metric_for(w, args.op, args.dtype, args.layout), "value": round(value, 3), "unit": UNIT, "n_gpus": world,
             "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(seconds * 1e3 / args.steps, 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": w.about, "B": w.B, "L": w.L, "D": w.D, "seed": w.seed,
                        "global_batch": w.B * world,
-                       "op": args.op, "storage": args.dtype,
+                       "op": args.op, "storage": args.dtype, "layout": "(B,D,L)" if bdl else "(B,L,D)",
                        "l2": (f"inputs larger than L2: {nbytes / 1e6:.0f} MB per step vs 129 MB L2, "
                               "no flush") if nbytes > 129e6 else "working set fits L2: small case",
                        "path": plan["path_name"],
@@ -514,6 +540,8 @@ def main(argv=None):
     p.add_argument("--chunk-mode", choices=("auto", "own", "lookback", "twopass"), default="auto")
     p.add_argument("--dtype", choices=("f32", "bf16", "f16"), default="f32",
                    help="storage of a, b and h (arithmetic is fp32 for all three)")
+    p.add_argument("--layout", choices=("bld", "bdl"), default="bld",
+                   help="bld: (B, L, D), channels innermost (the pages'); bdl: (B, D, L), time innermost")
     p.add_argument("--tile", default="", help="chunked tile as tile_d,tile_t,stages")
     p.add_argument("--op", choices=("forward", "backward"), default="forward",
                    help="forward scan (the headline) or its gradient")

@@ -11,6 +11,8 @@
 // Per tile, inside one CTA of TD * S threads:
 //  1. TMA copies the a and b boxes (TT x TD stored elements each) into a
 //     shared-memory ring of ST stages; one mbarrier per stage counts the bytes.
+//     A stage is refilled as soon as every thread has its tile in registers
+//     (after the tile's first barrier), so up to ST + 1 tiles are in flight.
 //     Elements are widened to fp32 as threads read them (storage.cuh); all
 //     arithmetic and every carry is fp32, and h is rounded once when stored.
 //  2. Thread (channel c, segment s) composes its K = TT/S consecutive affine
@@ -197,45 +199,50 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
     uint32_t abort_seen = 0;                  // (thread 0, look-back) abort word, read one iteration early
     float run = 0.0f;                         // (slice-owner, ss == 0) inclusive value of the last tile
 
+    // (thread 0) fill ring slots up to (not including) slot `limit`; slot n goes to stage n % ST.
+    // In look-back mode the next tile id is taken one fill ahead, so the atomic's
+    // round trip overlaps a tile's work instead of delaying the next copy.
+    auto refill = [&](long long limit) {
+        if (!ended && abort_seen != 0) {
+            ended = true;
+            finish((int)(next_fill % ST));
+        }
+        while (!ended && next_fill < limit) {
+            const int s2 = (int)(next_fill % ST);
+            long long nq = ahead_q, nslice = ahead_slice;
+            const long long nid = ahead >= 0 ? ahead : next_tile(nq, nslice);
+            ahead = -1;
+            if (nid >= n_tiles) {
+                ended = true;
+                finish(s2);
+            } else {
+                issue(s2, nid, nq, nslice);
+            }
+            ++next_fill;
+        }
+        if (lookback) {
+            if (!ended && ahead < 0) ahead = next_tile(ahead_q, ahead_slice);
+            abort_seen = ld_relaxed_u32(&ctrl->abort);
+        }
+    };
+
     for (long long k = 0;; ++k) {
         const int st = (int)(k % ST);
         const TileCoord tc = sm.tile[st];
         const long long id = tc.id;
         if (id >= n_tiles) break;
 
+        // The first iteration fills the rest of the ring before it waits (the abort
+        // word is still unread, so no slot is closed here while others read this
+        // stage's TileCoord).  After that every stage is refilled as soon as its
+        // tile has been read, below.
+        if (tid == 0 && k == 0) refill(ST);
+
         if (!mbar_wait_bounded(&sm.full[st], (phases >> st) & 1u, kTmaPolls)) {
             atomicOr(status, kStatusTmaTimeout);
             if (lookback) atomicExch(&ctrl->abort, 1u);
         }
         phases ^= 1u << st;
-
-        // Keep ST-1 tiles in flight behind this one.  The slot filled last
-        // (k + ST - 1) reuses the stage freed at the end of iteration k - 1.
-        // In look-back mode the next tile id is taken one iteration ahead, so the
-        // atomic's round trip overlaps this tile's work instead of delaying it.
-        if (tid == 0) {
-            if (!ended && abort_seen != 0) {
-                ended = true;
-                finish((int)(next_fill % ST));
-            }
-            while (!ended && next_fill < k + ST) {
-                const int s2 = (int)(next_fill % ST);
-                long long nq = ahead_q, nslice = ahead_slice;
-                const long long nid = ahead >= 0 ? ahead : next_tile(nq, nslice);
-                ahead = -1;
-                if (nid >= n_tiles) {
-                    ended = true;
-                    finish(s2);
-                } else {
-                    issue(s2, nid, nq, nslice);
-                }
-                ++next_fill;
-            }
-            if (lookback) {
-                if (!ended && ahead < 0) ahead = next_tile(ahead_q, ahead_slice);
-                abort_seen = ld_relaxed_u32(&ctrl->abort);
-            }
-        }
 
         const long long q = tc.q, bi = tc.bi, d0 = tc.d0;
         const long long t0 = q * TT;
@@ -268,6 +275,9 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
         segA[s][c] = A;
         segB[s][c] = Bv;
         __syncthreads();
+        // Every thread now holds this tile's a and b in registers: stage st is free,
+        // so its next tile (slot k + ST) starts copying while this one is finished.
+        if (tid == 0) refill(k + ST + 1);
 
         // ---- 3. shuffle scan over the S segment pairs of each channel -----------
         float xA = segA[ss][cc], xB = segB[ss][cc];
@@ -345,10 +355,11 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
             if (h_last && nv > 0 && t0 + r0 + nv == L) h_last[bi * D + d0 + c] = hc;
         }
         // No barrier here.  Stage st was last read before this tile's first
-        // barrier, and thread 0 refills it only in the next iteration.  The next
-        // tile writes the other copy of segA / segB / carry; the one after it
-        // writes this copy again only after two more barriers, which every
-        // thread reaches after finishing this tile.
+        // barrier, after which thread 0 refilled it; its TileCoord was read into
+        // registers at the top of the iteration.  The next tile writes the other
+        // copy of segA / segB / carry; the one after it writes this copy again
+        // only after two more barriers, which every thread reaches after
+        // finishing this tile.
     }
 
     // Look-back mode: the last CTA to finish resets the counters and advances the

@@ -130,11 +130,11 @@ void default_tile(int64_t B, int64_t D, int sm_count, bool own, bool twopass, bo
         else { *tile_d = 32; *tile_t = 128; *stages = 2; }
         return;
     }
-    // fp32 slice-owner mode: a 3-deep ring while slices are scarce; with several
-    // slices per SM a 2-deep one (measured 5-7 % faster on the gated and short shapes)
-    const bool many = B * ((D + 31) / 32) >= 4 * (int64_t)sm_count;
-    if (own && !twopass && many) { *tile_d = 32; *tile_t = 128; *stages = 2; return; }
-    if (own) { *tile_d = 32; *tile_t = 128; *stages = 3; return; }
+    // fp32 slice-owner and two-pass modes: a 2-deep ring.  Each stage is refilled
+    // as soon as its tile is in registers, so up to three tiles are in flight per
+    // CTA; on GB300 a 3-deep ring (four in flight) measured 9-11 % slower at every
+    // shape (lower DRAM efficiency, not too few bytes in flight).
+    if (own) { *tile_d = 32; *tile_t = 128; *stages = 2; return; }
     if (D >= 64) { *tile_d = 64; *tile_t = 128; *stages = 2; }
     else { *tile_d = 32; *tile_t = 128; *stages = 3; }
 }
