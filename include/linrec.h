@@ -264,12 +264,14 @@ linrec_status_t linrec_plan_16(int64_t B, int64_t L, int64_t D, int sm_count, in
  *    row segments (each segment's map, the scan of those maps by the (B, L, D)
  *    kernels, each segment rescanned from its carry): 20 bytes per fp32
  *    element instead of 12.
- *  - Vector width V (stored elements per lane per chunk, 16 bytes at most) is
- *    the widest that divides L and the pointers' alignment allows; any
- *    alignment of the element type works.
+ *  - Vector width V (stored elements per lane per chunk): by default the widest
+ *    that divides L and that the pointers' alignment allows, up to 16 bytes for
+ *    fp32 and 32 bytes (two 16-byte accesses) for 16-bit storage; any alignment
+ *    of the element type works.
  *  - The _ex forms take the options: h_init / h_last ((B, D) fp32, row i*D + d,
- *    as for linrec_scan_f32_carry), d_status, vec (1, 2, 4 or, for 16-bit
- *    storage, 8), prefetch (2 or 4 chunks), chunk_mode (0 auto, 1 one pass,
+ *    as for linrec_scan_f32_carry), d_status, vec (1, 2, 4, 8 for fp32; 1, 2,
+ *    4, 8, 16 for 16-bit storage; at most 32 bytes, needing min(16, bytes)-byte
+ *    alignment), prefetch (2 or 4 chunks), chunk_mode (0 auto, 1 one pass,
  *    3 two passes); path must be 0 or LINREC_PATH_ROWS.
  * Other conventions as for linrec_scan_f32 (and, for the 16-bit forms, as for
  * linrec_scan_bf16 / linrec_scan_f16).

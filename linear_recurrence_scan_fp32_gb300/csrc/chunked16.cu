@@ -16,7 +16,9 @@ namespace {
     X(64, 128, 8, 3)                 \
     X(64, 64, 4, 4)                  \
     X(32, 64, 4, 6)                  \
-    X(128, 64, 4, 3)
+    X(128, 64, 4, 3)                 \
+    X(32, 256, 8, 2)                 \
+    X(32, 256, 8, 3)
 
 #define LINREC_V_ENTRY(TD, TT, S, ST) make_variant<kDtypeBF16, TD, TT, S, ST>(),
 const ChunkedVariant kVariants16[] = {LINREC_CHUNKED16_VARIANTS(LINREC_V_ENTRY)};

@@ -69,6 +69,49 @@ struct TileCoord {
     int pad;
 };
 
+// A thread's K steps of a and b, held in registers from the compose to the replay.
+// fp32 storage keeps them as floats.  16-bit storage keeps the stored words, two
+// steps to a 32-bit register, and widens each one (exactly) where it is used: a
+// 16-bit tile of twice the steps then costs the registers of an fp32 tile.
+template <int DT, int K, bool PACK = (Storage<DT>::bytes == 2) && (K % 2 == 0)>
+struct TileRegs;
+
+template <int DT, int K>
+struct TileRegs<DT, K, false> {
+    float a_[K], b_[K];
+    template <typename E>
+    __device__ __forceinline__ void load(const E *ta, const E *tb, int stride) {
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+            a_[j] = Storage<DT>::get(ta[j * stride]);
+            b_[j] = Storage<DT>::get(tb[j * stride]);
+        }
+    }
+    __device__ __forceinline__ float a(int j) const { return a_[j]; }
+    __device__ __forceinline__ float b(int j) const { return b_[j]; }
+    __device__ __forceinline__ void zero_a0() { a_[0] = 0.0f; }
+};
+
+template <int DT, int K>
+struct TileRegs<DT, K, true> {
+    uint32_t a_[K / 2], b_[K / 2];            // step 2i in the low half, step 2i + 1 in the high half
+    template <typename E>
+    __device__ __forceinline__ void load(const E *ta, const E *tb, int stride) {
+#pragma unroll
+        for (int i = 0; i < K / 2; ++i) {
+            a_[i] = (uint32_t)ta[2 * i * stride] | ((uint32_t)ta[(2 * i + 1) * stride] << 16);
+            b_[i] = (uint32_t)tb[2 * i * stride] | ((uint32_t)tb[(2 * i + 1) * stride] << 16);
+        }
+    }
+    __device__ __forceinline__ float a(int j) const {
+        return Storage<DT>::get((unsigned short)((j & 1) ? (a_[j >> 1] >> 16) : (a_[j >> 1] & 0xffffu)));
+    }
+    __device__ __forceinline__ float b(int j) const {
+        return Storage<DT>::get((unsigned short)((j & 1) ? (b_[j >> 1] >> 16) : (b_[j >> 1] & 0xffffu)));
+    }
+    __device__ __forceinline__ void zero_a0() { a_[0] &= 0xffff0000u; }   // the word 0 is +0 in both formats
+};
+
 template <typename E, int TD, int TT, int S, int ST>
 struct __align__(128) ChunkSmem {
     E a[ST][TT * TD];                   // stored elements, as the boxes arrive
@@ -254,19 +297,15 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
         // ---- 2. compose this thread's K steps -----------------------------------
         const E *ta = sm.a[st] + r0 * TD + c;
         const E *tb = sm.b[st] + r0 * TD + c;
-        float ra[K], rb[K];
-#pragma unroll
-        for (int j = 0; j < K; ++j) {
-            ra[j] = Storage<DT>::get(ta[j * TD]);
-            rb[j] = Storage<DT>::get(tb[j * TD]);
-        }
-        if (seq_start && !h_init) ra[0] = 0.0f;   // h_{-1} = 0: the first slope never matters
+        TileRegs<DT, K> r;
+        r.load(ta, tb, TD);
+        if (seq_start && !h_init) r.zero_a0();   // h_{-1} = 0: the first slope never matters
         float A = 1.0f, Bv = 0.0f;
 #pragma unroll
         for (int j = 0; j < K; ++j) {
             if (j < nv) {
-                Bv = fmaf(ra[j], Bv, rb[j]);
-                A = ra[j] * A;
+                Bv = fmaf(r.a(j), Bv, r.b(j));
+                A = r.a(j) * A;
             }
         }
         float (&segA)[S][TD] = sm.segA[k & 1];
@@ -339,14 +378,14 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
             if (nv == K) {
 #pragma unroll
                 for (int j = 0; j < K; ++j) {
-                    hc = fmaf(ra[j], hc, rb[j]);
+                    hc = fmaf(r.a(j), hc, r.b(j));
                     hp[(long long)j * D] = Storage<DT>::put(hc);
                 }
             } else {
 #pragma unroll
                 for (int j = 0; j < K; ++j) {
                     if (j < nv) {
-                        hc = fmaf(ra[j], hc, rb[j]);
+                        hc = fmaf(r.a(j), hc, r.b(j));
                         hp[(long long)j * D] = Storage<DT>::put(hc);
                     }
                 }

@@ -115,12 +115,18 @@ const ChunkedVariant *find_variant(int tile_d, int tile_t, int stages, int *inde
 // storage (measured on GB300): 128-step tiles while slices are scarce, 64-step
 // tiles with a 6-deep ring once every SM has several slices and in two-pass
 // mode, {32, 128, 4} for look-back.
-void default_tile(int64_t B, int64_t D, int sm_count, bool own, bool twopass, bool backward, int dtype,
+// 16-bit storage: tiles of 256 steps, the bytes of an fp32 tile of 128 (each thread
+// holds its 32 steps packed two to a register); measured on GB300 against 128-step
+// tiles: 4885 vs 3621 GB/s on (32, 4096, 256), 6269 vs 4343 on (64, 2048, 1024).
+// Sequences shorter than 256 steps take 64-step tiles with a 6-deep ring.
+int tile_t_16(int64_t L) { return L >= 256 ? 256 : 64; }
+
+void default_tile(int64_t B, int64_t L, int64_t D, int sm_count, bool own, bool twopass, bool backward, int dtype,
                   int *tile_d, int *tile_t, int *stages) {
     if (dtype != kDtypeF32) {
-        const bool many = B * ((D + 31) / 32) >= 4 * (int64_t)sm_count;
-        if (twopass || (own && many)) { *tile_d = 32; *tile_t = 64; *stages = 6; }
-        else { *tile_d = 32; *tile_t = 128; *stages = 4; }
+        *tile_d = 32;
+        *tile_t = tile_t_16(L);
+        *stages = *tile_t == 256 ? 2 : 6;
         return;
     }
     own = own || twopass;
@@ -198,7 +204,7 @@ linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int ali
     if (opt->chunk_mode == 0) {
         const int td = opt->tile_d ? opt->tile_d : 32;
         own = B * ((D + td - 1) / td) >= (int64_t)sm_count;
-        const int tt = opt->tile_t ? opt->tile_t : (dtype == kDtypeF32 ? 128 : 64);
+        const int tt = opt->tile_t ? opt->tile_t : (dtype == kDtypeF32 ? 128 : tile_t_16(L));
         twopass = !own && !backward && allow_twopass && (L + tt - 1) / tt >= kTwoPassMinChunks;
     } else {
         own = opt->chunk_mode == 1;
@@ -207,7 +213,7 @@ linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int ali
     int tile_d = opt->tile_d, tile_t = opt->tile_t, stages = opt->stages;
     if (tile_d == 0 || tile_t == 0) {
         int dd, dt, ds;
-        default_tile(B, D, sm_count, own, twopass, backward, dtype, &dd, &dt, &ds);
+        default_tile(B, L, D, sm_count, own, twopass, backward, dtype, &dd, &dt, &ds);
         if (tile_d == 0) tile_d = dd;
         if (tile_t == 0) tile_t = dt;
         if (stages == 0) stages = ds;
@@ -426,12 +432,18 @@ linrec_status_t plan_bdl_impl(int64_t B, int64_t D, int64_t L, int dtype, int sm
     if (opt->chunk_mode != 0 && opt->chunk_mode != 1 && opt->chunk_mode != 3) return LINREC_ERR_INVALID_VALUE;
     if (n == 0) return LINREC_OK;
     const int eb = elem_bytes_of(dtype);
+    // Widest lane vector that L and the pointers allow: 16 bytes for fp32, 32 (two
+    // 16-byte accesses) for 16-bit storage, whose chunks would otherwise spend more
+    // issue slots on the shuffle scan than on the elements (measured on GB300:
+    // (32, 256, 4096) bfloat16 at 6071 GB/s against 5520 with 16-byte lanes).
     int vec = opt->vec;
     if (vec == 0) {
-        vec = 16 / eb;
-        while (vec > 1 && (L % vec != 0 || align_bytes < eb * vec)) vec /= 2;
+        vec = (eb == 2 ? 32 : 16) / eb;
+        while (vec > 1 && (L % vec != 0 || align_bytes < (eb * vec < 16 ? eb * vec : 16))) vec /= 2;
     }
-    if (vec <= 0 || (vec & (vec - 1)) != 0 || vec * eb > 16 || L % vec != 0 || align_bytes < eb * vec)
+    // 32-byte vectors are two 16-byte accesses: 16-byte alignment suffices
+    if (vec <= 0 || (vec & (vec - 1)) != 0 || vec * eb > 32 || L % vec != 0 ||
+        align_bytes < (eb * vec < 16 ? eb * vec : 16))
         return LINREC_ERR_INVALID_VALUE;
     const int64_t R = B * D;
     const int64_t ch = 32 * (int64_t)vec;
@@ -465,9 +477,8 @@ linrec_status_t plan_bdl_impl(int64_t B, int64_t D, int64_t L, int dtype, int sm
         if (k < 1) k = 1;
         if (k > R) k = R;
     }
-    // loads in flight: 2 chunks (measured best on every one-pass shape and on fp32 two
-    // passes), 4 for 16-bit two passes
-    const int prefetch = opt->prefetch ? opt->prefetch : (twopass && eb == 2 ? 4 : 2);
+    // loads in flight: 2 chunks (measured best on every shape with the default vectors)
+    const int prefetch = opt->prefetch ? opt->prefetch : 2;
     if (!rows_supported(dtype, vec, prefetch)) return LINREC_ERR_INVALID_VALUE;
     const int64_t units = twopass ? R * nseg : (R + k - 1) / k;
     plan->vec = vec;

@@ -33,11 +33,33 @@ namespace {
 
 constexpr unsigned kAll = 0xffffffffu;
 
+// 32 bytes per lane: two 16-byte accesses, so the shuffle scan of each chunk is
+// shared by twice the elements.
+struct alignas(16) Vec32 { uint4 lo, hi; };
+
 template <int BYTES> struct RawVec;
+template <> struct RawVec<32> { using type = Vec32; };
 template <> struct RawVec<16> { using type = uint4; };
 template <> struct RawVec<8> { using type = uint2; };
 template <> struct RawVec<4> { using type = unsigned int; };
 template <> struct RawVec<2> { using type = unsigned short; };
+
+// Streaming (evict-first) vector load and store of one lane's V elements.
+template <typename W>
+__device__ __forceinline__ W ldcs_vec(const W *p) { return __ldcs(p); }
+template <>
+__device__ __forceinline__ Vec32 ldcs_vec<Vec32>(const Vec32 *p) {
+    const uint4 *q = reinterpret_cast<const uint4 *>(p);
+    return Vec32{__ldcs(q), __ldcs(q + 1)};
+}
+template <typename W>
+__device__ __forceinline__ void stcs_vec(W *p, const W &w) { __stcs(p, w); }
+template <>
+__device__ __forceinline__ void stcs_vec<Vec32>(Vec32 *p, const Vec32 &w) {
+    uint4 *q = reinterpret_cast<uint4 *>(p);
+    __stcs(q, w.lo);
+    __stcs(q + 1, w.hi);
+}
 
 template <int DT, int V, typename W>
 __device__ __forceinline__ void unpack(const W &w, float (&x)[V]) {
@@ -104,8 +126,8 @@ rows_scan_kernel(const typename Storage<DT>::raw *__restrict__ a, const typename
     for (int j = 0; j < P; ++j) {
         const long long off = (long long)j * CH + lane * V;
         if (off < n) {
-            ra[j] = __ldcs(reinterpret_cast<const W *>(pa + off));
-            rb[j] = __ldcs(reinterpret_cast<const W *>(pb + off));
+            ra[j] = ldcs_vec<W>(reinterpret_cast<const W *>(pa + off));
+            rb[j] = ldcs_vec<W>(reinterpret_cast<const W *>(pb + off));
         }
     }
     for (long long c0 = 0; c0 < n; c0 += (long long)P * CH) {
@@ -125,8 +147,8 @@ rows_scan_kernel(const typename Storage<DT>::raw *__restrict__ a, const typename
             }
             const long long nxt = off + (long long)P * CH;
             if (nxt < n) {
-                ra[j] = __ldcs(reinterpret_cast<const W *>(pa + nxt));
-                rb[j] = __ldcs(reinterpret_cast<const W *>(pb + nxt));
+                ra[j] = ldcs_vec<W>(reinterpret_cast<const W *>(pa + nxt));
+                rb[j] = ldcs_vec<W>(reinterpret_cast<const W *>(pb + nxt));
             }
             if (valid && t == 0) {            // a row's first step: the constant map
                 if (h_init) {
@@ -170,7 +192,7 @@ rows_scan_kernel(const typename Storage<DT>::raw *__restrict__ a, const typename
                     out[v] = hv;
                 }
                 if (valid) {
-                    __stcs(reinterpret_cast<W *>(ph + off), pack<DT, V, W>(out));
+                    stcs_vec<W>(reinterpret_cast<W *>(ph + off), pack<DT, V, W>(out));
                     if (h_last && t + V == L) h_last[row] = hv;
                 }
                 carry = __shfl_sync(kAll, hv, 31);   // h at the chunk's end (a partial chunk ends the unit)
@@ -205,6 +227,7 @@ template <int DT, int P>
 cudaError_t launch_dt(const RowsLaunch &p, cudaStream_t stream) {
     constexpr int EB = (int)sizeof(typename Storage<DT>::raw);
     switch (p.vec * EB) {
+        case 32: return launch_one<DT, 32 / EB, P>(p, stream);
         case 16: return launch_one<DT, 16 / EB, P>(p, stream);
         case 8: return launch_one<DT, 8 / EB, P>(p, stream);
         case 4: return launch_one<DT, 4 / EB, P>(p, stream);
@@ -219,7 +242,7 @@ cudaError_t launch_dt(const RowsLaunch &p, cudaStream_t stream) {
 
 bool rows_supported(int dtype, int vec, int prefetch) {
     const int eb = elem_bytes_of(dtype);
-    return vec >= 1 && (vec & (vec - 1)) == 0 && vec * eb <= 16 && (prefetch == 2 || prefetch == 4);
+    return vec >= 1 && (vec & (vec - 1)) == 0 && vec * eb <= 32 && (prefetch == 2 || prefetch == 4);
 }
 
 cudaError_t launch_rows(const RowsLaunch &p, cudaStream_t stream) {

@@ -15,6 +15,7 @@ template <int DT> struct Storage;
 
 template <> struct Storage<kDtypeF32> {
     using raw = float;
+    static constexpr int bytes = 4;
     static __device__ __forceinline__ float get(float x) { return x; }
     static __device__ __forceinline__ float put(float x) { return x; }
 };
@@ -22,6 +23,7 @@ template <> struct Storage<kDtypeF32> {
 // bfloat16: the upper 16 bits of the binary32 word of the same value.
 template <> struct Storage<kDtypeBF16> {
     using raw = unsigned short;
+    static constexpr int bytes = 2;
     static __device__ __forceinline__ float get(unsigned short w) { return __uint_as_float((unsigned int)w << 16); }
     static __device__ __forceinline__ unsigned short put(float x) {
         return __bfloat16_as_ushort(__float2bfloat16_rn(x));
@@ -31,6 +33,7 @@ template <> struct Storage<kDtypeBF16> {
 // IEEE 754 binary16.
 template <> struct Storage<kDtypeF16> {
     using raw = unsigned short;
+    static constexpr int bytes = 2;
     static __device__ __forceinline__ float get(unsigned short w) { return __half2float(__ushort_as_half(w)); }
     static __device__ __forceinline__ unsigned short put(float x) { return __half_as_ushort(__float2half_rn(x)); }
 };

@@ -190,11 +190,11 @@ def test_carry_state_overlap_checks(L):
 
 
 def test_plan_16bit_storage():
-    # 16-byte aligned with D % 8 == 0: the chunked kernel; 128-step tiles while slices are scarce,
-    # 64-step tiles with a 6-deep ring once every SM has several slices
+    # 16-byte aligned with D % 8 == 0: the chunked kernel; 256-step tiles (the bytes of a
+    # 128-step fp32 tile) with a 2-deep ring, 64-step tiles with a 6-deep ring below 256 steps
     p = lr.linrec_plan_16(32, 4096, 256, sm_count=152)
     assert p["path_name"] == "chunked" and p["lookback"] == 0
-    assert (p["tile_d"], p["tile_t"], p["stages"]) == (32, 128, 4)
+    assert (p["tile_d"], p["tile_t"], p["stages"]) == (32, 256, 2)
     p = lr.linrec_plan_16(256, 128, 4096, sm_count=152)
     assert (p["tile_d"], p["tile_t"], p["stages"], p["lookback"]) == (32, 64, 6, 0)
     # few long slices: two-pass, whose aggregates are fp32 whatever the storage
@@ -250,16 +250,20 @@ def test_plan_bdl_layout():
     assert p["workspace_bytes"] == 256 + 4 * (3 * p["n_tiles"] + 64)
     # short rows stay in one pass whatever their number
     assert lr.linrec_plan_bdl(1, 4, 1000)["twopass"] == 0
-    # the vector width follows L and the alignment; 16-bit storage reaches 8 elements
+    # the vector width follows L and the alignment; 16-bit storage reaches 16 elements
+    # (32 bytes, two 16-byte accesses: 16-byte alignment is enough)
     assert lr.linrec_plan_bdl(2, 3, 1001)["vec"] == 1
     assert lr.linrec_plan_bdl(2, 3, 1002)["vec"] == 2
     assert lr.linrec_plan_bdl(2, 3, 1000, align_bytes=8)["vec"] == 2
     assert lr.linrec_plan_bdl(2, 3, 1000, elem_bytes=2)["vec"] == 8
+    assert lr.linrec_plan_bdl(2, 3, 1024, elem_bytes=2)["vec"] == 16
+    assert lr.linrec_plan_bdl(2, 3, 1024, elem_bytes=2, align_bytes=8)["vec"] == 4
     assert lr.linrec_plan_bdl(2, 3, 1000, elem_bytes=2, align_bytes=2)["vec"] == 1
+    assert lr.linrec_plan_bdl(2, 3, 1024, vec=8)["vec"] == 8          # fp32, 32-byte lanes on request
     # forced modes and invalid options
     assert lr.linrec_plan_bdl(32, 256, 4096, chunk_mode="twopass")["twopass"] == 1
     assert lr.linrec_plan_bdl(1, 64, 1 << 20, chunk_mode="own")["twopass"] == 0
-    for bad in ({"chunk_mode": "lookback"}, {"path": "chunked"}, {"vec": 3}, {"vec": 8}, {"prefetch": 3}):
+    for bad in ({"chunk_mode": "lookback"}, {"path": "chunked"}, {"vec": 3}, {"vec": 16}, {"prefetch": 3}):
         with pytest.raises(lr.LinrecError):
             lr.linrec_plan_bdl(2, 3, 1000, **bad)
     with pytest.raises(lr.LinrecError):

@@ -89,7 +89,8 @@ def test_ragged_rows(shape):
     a, b = draw_bdl(B, D, L, 91 + L, a_dist="u[0.5,1)")
     h64, _ = oracle.f64_bdl(a, b)
     a_d, b_d = a.to(DEV), b.to(DEV)
-    for opt in MODES + [{"vec": 1}, {"vec": 1, "chunk_mode": "twopass"}]:
+    extra = [{"vec": 8}, {"vec": 8, "chunk_mode": "twopass"}] if L % 8 == 0 else []   # 32-byte lanes
+    for opt in MODES + [{"vec": 1}, {"vec": 1, "chunk_mode": "twopass"}] + extra:
         assert_close(run(a_d, b_d, **opt).cpu().numpy(), h64, f"{shape} {opt}")
 
 
@@ -145,7 +146,7 @@ def test_several_rows_per_warp(shape):
     hs64, last64 = oracle.f64_bdl(a, b, h0.double().numpy())
     a_d, b_d = a.to(DEV), b.to(DEV)
     for k in (1, 2, 3, 7, 64, B * D):
-        for vec in (0, 1):
+        for vec in (0, 1) + ((8,) if L % 8 == 0 else ()):
             opt = {"rows_per_warp": k, "vec": vec}
             assert_close(run(a_d, b_d, **opt).cpu().numpy(), h64, f"{shape} {opt}")
             last = torch.full((B, D), float("nan"), device=DEV)
@@ -204,7 +205,9 @@ def test_16bit_storage(kind, shape):
     h64, _ = oracle.f64_bdl(oracle.decode16(kind, a16).astype(np.float32),
                             oracle.decode16(kind, b16).astype(np.float32))
     a_d, b_d = a16.to(DEV), b16.to(DEV)
-    for opt in ({}, {"chunk_mode": "own"}, {"chunk_mode": "twopass"}):
+    # by default 32-byte lanes (16 elements) where L allows; 16-byte lanes on request
+    extra = ({"vec": 8}, {"vec": 8, "chunk_mode": "twopass"}) if L % 8 == 0 else ()
+    for opt in ({}, {"chunk_mode": "own"}, {"chunk_mode": "twopass"}) + extra:
         h = SCAN16[kind](a_d, b_d, **opt)
         torch.cuda.synchronize()
         _close16(kind, h, h64, f"{kind} {shape} {opt}")
