@@ -71,6 +71,7 @@ chunked_backward_kernel(const __grid_constant__ CUtensorMap map_g,
 
     const bool want_da = da != nullptr;
     const uint32_t stage_bytes = (want_da ? 3u : 2u) * kBox;
+    pdl_wait();   // launched as a programmatic dependent: nothing before it is touched yet
     const int tid = threadIdx.x;
     const int c = tid % TD;
     const int s = tid / TD;
@@ -265,6 +266,8 @@ chunked_backward_kernel(const __grid_constant__ CUtensorMap map_g,
         __syncthreads();
     }
 
+    pdl_release();   // this CTA's tiles are done: the next launch may be scheduled
+
     if (!own) {
         __syncthreads();
         if (tid == 0) {
@@ -340,8 +343,8 @@ cudaError_t launch_backward(const BackwardLaunch &p, cudaStream_t stream) {
     float *dh_init = p.dh_init;
     void *args[] = {(void *)&p.map_g, (void *)&p.map_a, (void *)&p.map_h, &a, &da, &db, &L, &D, &spb, &ns, &ch,
                     &nt, &own, &ctrl, &words, &status, &spin, &silent, &h_init, &dh_last, &dh_init};
-    return cudaLaunchKernel(fn, dim3((unsigned)p.grid), dim3((unsigned)p.variant->threads), args,
-                            p.variant->smem_bytes, stream);
+    return launch_dependent(fn, dim3((unsigned)p.grid), dim3((unsigned)p.variant->threads), p.variant->smem_bytes,
+                            stream, args);
 }
 
 }  // namespace linrec

@@ -68,8 +68,8 @@ cudaError_t launch_chunked(const ChunkedLaunch &p, cudaStream_t stream) {
     float *h_last = p.h_last;
     void *args[] = {(void *)&p.map_a, (void *)&p.map_b, &h, &L, &D, &spb, &ns, &ch, &nt, &mode,
                     &ctrl, &words, &status, &spin, &silent, &h_init, &h_last};
-    return cudaLaunchKernel(fn, dim3((unsigned)p.grid), dim3((unsigned)p.variant->threads), args,
-                            p.variant->smem_bytes, stream);
+    return launch_dependent(fn, dim3((unsigned)p.grid), dim3((unsigned)p.variant->threads), p.variant->smem_bytes,
+                            stream, args);
 }
 
 }  // namespace linrec

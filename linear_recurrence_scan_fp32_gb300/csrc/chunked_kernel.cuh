@@ -158,6 +158,8 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
     extern __shared__ __align__(128) unsigned char smem_raw[];
     Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
 
+    pdl_wait();   // launched as a programmatic dependent: nothing before it is touched yet
+
     const int tid = threadIdx.x;
     const int c = tid % TD;                   // channel within the tile
     const int s = tid / TD;                   // segment within the tile
@@ -400,6 +402,11 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
         // only after two more barriers, which every thread reaches after
         // finishing this tile.
     }
+
+    // This CTA's tiles are done: the launch that follows may be scheduled (it waits
+    // for this whole grid before it touches memory).  Not earlier: its CTAs would take
+    // slots while this grid still runs (measured 3 % slower on (32, 4096, 256)).
+    pdl_release();
 
     // Look-back mode: the last CTA to finish resets the counters and advances the
     // epoch for the next launch on this workspace.

@@ -33,6 +33,24 @@ constexpr int kDtypeBF16 = 1;
 constexpr int kDtypeF16 = 2;
 constexpr int elem_bytes_of(int dtype) { return dtype == kDtypeF32 ? 4 : 2; }
 
+// Launch `fn` as a programmatic dependent of the work before it on `stream` (the
+// kernel calls pdl_wait() before touching global memory): back-to-back calls then
+// overlap one launch's start with the previous one's drain.
+inline cudaError_t launch_dependent(const void *fn, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                    void **args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
 // ---- register-carry path ---------------------------------------------------
 // One thread walks `vec` adjacent channels through all L steps, with the loads
 // of the next `prefetch` steps in flight in registers.

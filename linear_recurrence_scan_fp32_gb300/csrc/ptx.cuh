@@ -49,6 +49,16 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     return false;
 }
 
+// ---- programmatic dependent launch ------------------------------------------
+// A kernel launched with launch_dependent() may be scheduled while the work before
+// it on the stream is finishing.  pdl_wait() blocks until that work has completed
+// and its writes are visible: every thread calls it before its first access to
+// global memory.  pdl_release() lets the launch after this one be scheduled (a
+// CTA calls it when its own work is done; exiting counts as well).
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---- TMA ------------------------------------------------------------------
 
 __device__ __forceinline__ void tmap_prefetch(const CUtensorMap *map) {

@@ -25,6 +25,7 @@
 // every segment's last h, and an apply launch rescans every segment from the h
 // before it.
 #include "kernels.cuh"
+#include "ptx.cuh"
 #include "storage.cuh"
 
 namespace linrec {
@@ -90,6 +91,7 @@ rows_scan_kernel(const typename Storage<DT>::raw *__restrict__ a, const typename
     using E = typename Storage<DT>::raw;
     using W = typename RawVec<V * (int)sizeof(E)>::type;
     constexpr int CH = 32 * V;                // elements per chunk
+    pdl_wait();   // launched as a programmatic dependent: nothing before it is touched yet
     const long long u = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     const long long units = nseg > 1 ? R * nseg : (R + rows_per_unit - 1) / rows_per_unit;
@@ -210,6 +212,7 @@ rows_scan_kernel(const typename Storage<DT>::raw *__restrict__ a, const typename
         aggA[g * R + r0] = runA;
         aggB[g * R + r0] = runB;
     }
+    pdl_release();   // this warp's unit is done: the next launch may be scheduled
 }
 
 template <int DT, int V, int P>
@@ -217,10 +220,15 @@ cudaError_t launch_one(const RowsLaunch &p, cudaStream_t stream) {
     using E = typename Storage<DT>::raw;
     const long long units = p.nseg > 1 ? p.R * p.nseg : (p.R + p.rows_per_unit - 1) / p.rows_per_unit;
     const long long blocks = (units * 32 + kRowsThreads - 1) / kRowsThreads;
-    rows_scan_kernel<DT, V, P><<<(unsigned)blocks, kRowsThreads, 0, stream>>>(
-        static_cast<const E *>(p.a), static_cast<const E *>(p.b), static_cast<E *>(p.h), p.R, p.L, p.seg_len, p.nseg,
-        p.rows_per_unit, p.mode, p.h_init, p.h_last, p.aggA, p.aggB, p.aggH, p.aggX);
-    return cudaGetLastError();
+    const E *a = static_cast<const E *>(p.a), *b = static_cast<const E *>(p.b);
+    E *h = static_cast<E *>(p.h);
+    long long R = p.R, L = p.L, seg_len = p.seg_len, nseg = p.nseg, rpu = p.rows_per_unit;
+    int mode = p.mode;
+    const float *h_init = p.h_init, *aggH = p.aggH;
+    float *h_last = p.h_last, *aggA = p.aggA, *aggB = p.aggB, *aggX = p.aggX;
+    void *args[] = {&a, &b, &h, &R, &L, &seg_len, &nseg, &rpu, &mode, &h_init, &h_last, &aggA, &aggB, &aggH, &aggX};
+    return launch_dependent(reinterpret_cast<const void *>(&rows_scan_kernel<DT, V, P>), dim3((unsigned)blocks),
+                            dim3(kRowsThreads), 0, stream, args);
 }
 
 template <int DT, int P>
