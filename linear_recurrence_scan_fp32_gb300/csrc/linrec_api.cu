@@ -19,6 +19,8 @@ namespace {
 constexpr int kVersion = 100;               // 0.1.0
 constexpr int64_t kDefaultSpinLimit = 1 << 20;
 constexpr int kRegcarryThreads = 256;
+// fp32 forward: the register path from this many 4-channel threads per SM on
+constexpr int64_t kRegcarryMinThreadsPerSm = 96;
 // Few slices: the two-pass mode from this many time chunks of 128 steps on.
 constexpr int64_t kTwoPassMinChunks = 64;
 constexpr size_t kWorkspaceHead = 256;      // Control block, padded
@@ -161,11 +163,19 @@ linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int ali
     if (backward && dtype != kDtypeF32) return LINREC_ERR_INVALID_VALUE;
     const bool tma_ok = align_bytes >= 16 && (D * eb) % 16 == 0 && D <= INT32_MAX && B <= INT32_MAX &&
                         L <= (int64_t)INT32_MAX - 1024;
-    // The TMA-staged chunked kernel whenever its copies are legal: measured on
-    // GB300 it beats the register path at every shape of the five workloads.
-    // The register path takes misaligned pointers and D % 4 != 0.
+    // The register path when the channels alone keep enough loads in flight: fp32
+    // forward with at least kRegcarryMinThreadsPerSm 4-channel threads per SM.
+    // Measured on GB300: (256, 128, 4096) 6922 vs 6007 GB/s for the chunked kernel,
+    // (64, 2048, 1024) 6193 vs 5976; at 32768 channels it loses (4361 vs 5722 on
+    // (8, 4096, 4096)), and in 16-bit storage it loses at every shape measured.
+    // Otherwise the TMA-staged chunked kernel whenever its copies are legal; the
+    // register path also takes misaligned pointers and D % 4 != 0.
     int path = opt->path;
-    if (path == LINREC_PATH_AUTO) path = tma_ok ? LINREC_PATH_CHUNKED : LINREC_PATH_REGCARRY;
+    if (path == LINREC_PATH_AUTO) {
+        const bool many = dtype == kDtypeF32 && !backward && D % 4 == 0 && align_bytes >= 16 &&
+                          B * (D / 4) >= kRegcarryMinThreadsPerSm * (int64_t)sm_count;
+        path = (tma_ok && !many) ? LINREC_PATH_CHUNKED : LINREC_PATH_REGCARRY;
+    }
     plan->path = path;
 
     if (path == LINREC_PATH_REGCARRY) {
@@ -177,7 +187,11 @@ linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int ali
             while (vec > 1 && (D % vec != 0 || align_bytes < eb * vec)) vec /= 2;
         }
         if (vec <= 0 || D % vec != 0 || align_bytes < eb * vec) return LINREC_ERR_INVALID_VALUE;
-        int prefetch = opt->prefetch ? opt->prefetch : (vec == maxv ? 8 : 16);
+        // steps loaded ahead: 16 when threads are scarce (under 160 per SM) or L is short,
+        // otherwise 8 (measured: (64, 1024, 4096) 6747 GB/s with 8, 6511 with 16)
+        const int64_t per_sm = B * (D / vec) / sm_count;
+        int prefetch = opt->prefetch ? opt->prefetch
+                                     : (vec != maxv || per_sm < 160 || L <= 512) ? 16 : 8;
         const bool ok = dtype == kDtypeF32 ? regcarry_supported(vec, prefetch) : regcarry16_supported(vec, prefetch);
         if (!ok) return LINREC_ERR_INVALID_VALUE;
         plan->vec = vec;

@@ -81,8 +81,18 @@ def test_argument_checks_return_before_any_launch(L):
 
 
 def test_plan_paths():
-    # many channels: the chunked kernel, each CTA owning whole slices
-    p = lr.linrec_plan_f32(256, 128, 4096)
+    # very many channels (fp32 forward): the register path, 16 steps ahead for short L
+    p = lr.linrec_plan_f32(256, 128, 4096, sm_count=152)
+    assert p["path_name"] == "regcarry" and (p["vec"], p["prefetch"]) == (4, 16)
+    p = lr.linrec_plan_f32(64, 1024, 4096, sm_count=152)
+    assert p["path_name"] == "regcarry" and p["prefetch"] == 8
+    # ... but not below 96 four-channel threads per SM, nor for 16-bit storage or the gradient
+    p = lr.linrec_plan_f32(8, 4096, 4096, sm_count=152)
+    assert p["path_name"] == "chunked" and p["lookback"] == 0
+    assert lr.linrec_plan_16(256, 128, 4096, sm_count=152)["path_name"] == "chunked"
+    assert lr.linrec_plan_f32_backward(256, 128, 4096, sm_count=152)["path_name"] == "chunked"
+    # many channels, fewer of them: the chunked kernel, each CTA owning whole slices
+    p = lr.linrec_plan_f32(32, 4096, 256, sm_count=152)
     assert p["path_name"] == "chunked" and p["lookback"] == 0
     # the register path when forced: 16-byte vectors, a grid covering every group
     p = lr.linrec_plan_f32(256, 128, 4096, path="regcarry")
