@@ -66,7 +66,7 @@ def launches_per_step(plan: dict, op: str) -> int:
     """Kernel launches of one call.  Two-pass mode: the reduce launch, the scan of the
     tile aggregates (one launch: at that level the dispatcher takes the slice-owner or
     look-back mode, never two-pass again) and the apply launch."""
-    if op == "forward" and plan["path_name"] in ("chunked", "rows") and plan["twopass"]:
+    if plan["path_name"] in ("chunked", "rows") and plan["twopass"]:
         return 3
     return 1
 FALLBACK_HBM_GBS = 6800.0
@@ -368,8 +368,8 @@ def run_ours(args):
         plan = lr.linrec_plan_f32_backward(w.B, w.L, w.D,
                                            sm_count=torch.cuda.get_device_properties(dev).multi_processor_count,
                                            **opt)
-        kernel_tag = ("backward" if not plan["lookback"] else "backward_lookback") \
-            if plan["path_name"] == "chunked" else "regcarry_backward"
+        kernel_tag = ("backward_twopass" if plan["twopass"] else "backward_lookback" if plan["lookback"]
+                      else "backward") if plan["path_name"] == "chunked" else "regcarry_backward"
 
     def step():
         if args.op == "backward":

@@ -12,7 +12,10 @@
 // reversed sequence: chunk qr = 0 is the last time chunk, a thread walks its
 // rows from the bottom of the tile up, and the carry entering a chunk (the
 // running c) comes from the chunk after it in time, in register (slice-owner
-// mode) or by the shared decoupled look-back.  Per tile the ring holds three
+// mode), by the shared decoupled look-back, or (two-pass mode, for few long
+// slices) from a scan of the tiles' maps: a reduce launch writes every tile's
+// map, the library's forward scan composes them in reversed chunk order, and
+// an apply launch gives each tile the running c of the chunk after it.  Per tile the ring holds three
 // boxes: g (rows t0 .. t0+TT-1), a one row later (a_{t+1}) and h one row
 // earlier (h_{t-1}; only when da is wanted).  Out-of-range rows arrive as
 // zeros; rows past L-1 are given the identity map (slope 1, value 0) so the
@@ -55,7 +58,8 @@ chunked_backward_kernel(const __grid_constant__ CUtensorMap map_g,
                         const float *__restrict__ a_glob, float *__restrict__ da, float *__restrict__ db,
                         const long long L, const long long D,
                         const long long slices_per_batch, const long long n_slices,
-                        const long long chunks, const long long n_tiles, const int own,
+                        const long long chunks, const long long n_tiles,
+                        const int mode,              // kModeOwn, kModeLookback, kModeReduce or kModeApply
                         Control *__restrict__ ctrl, unsigned long long *__restrict__ words,
                         unsigned int *__restrict__ status, const long long spin_limit,
                         const long long silent_tile, const float *h_init, const float *dh_last,
@@ -69,8 +73,19 @@ chunked_backward_kernel(const __grid_constant__ CUtensorMap map_g,
     extern __shared__ __align__(128) unsigned char smem_raw[];
     Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
 
+    const bool own = mode == kModeOwn;
+    const bool lookback = mode == kModeLookback;
+    const bool reduce = mode == kModeReduce;
+    const bool apply = mode == kModeApply;
     const bool want_da = da != nullptr;
-    const uint32_t stage_bytes = (want_da ? 3u : 2u) * kBox;
+    const bool load_h = want_da && !reduce;   // the reduce launch needs the maps only: g and a
+    const uint32_t stage_bytes = (load_h ? 3u : 2u) * kBox;
+    // two-pass mode: per-tile maps and the scanned running c, indexed [tile id][channel], and
+    // each slice's c entering the last chunk, indexed [slice][channel]
+    float *const tileA = reinterpret_cast<float *>(words);
+    float *const tileB = tileA + n_tiles * TD;
+    const float *const tileH = tileB + n_tiles * TD;
+    float *const tileX = tileB + 2 * n_tiles * TD;
     pdl_wait();   // launched as a programmatic dependent: nothing before it is touched yet
     const int tid = threadIdx.x;
     const int c = tid % TD;
@@ -91,11 +106,19 @@ chunked_backward_kernel(const __grid_constant__ CUtensorMap map_g,
         mbar_arrive_expect_tx(&sm.full[st], stage_bytes);
         tma_load_3d(sm.g[st], &map_g, &sm.full[st], d0, t0, (int)bi);
         tma_load_3d(sm.a[st], &map_a, &sm.full[st], d0, t0 + 1, (int)bi);
-        if (want_da) tma_load_3d(sm.h[st], &map_h, &sm.full[st], d0, t0 - 1, (int)bi);
+        if (load_h) tma_load_3d(sm.h[st], &map_h, &sm.full[st], d0, t0 - 1, (int)bi);
     };
     auto finish = [&](int st) { sm.tile[st] = TileCoord{n_tiles, 0, 0, 0, 0}; };
-    long long own_slice = blockIdx.x, own_q = 0;
+    long long own_slice = blockIdx.x, own_q = 0, own_m = 0;
     auto next_tile = [&](long long &qr, long long &slice) -> long long {
+        if (reduce || apply) {                // independent tiles, static round-robin
+            const long long k = blockIdx.x + (own_m++) * (long long)gridDim.x;
+            if (k >= n_tiles) return n_tiles;
+            const long long id = apply ? n_tiles - 1 - k : k;
+            qr = id / n_slices;
+            slice = id - qr * n_slices;
+            return id;
+        }
         if (own) {
             if (own_slice >= n_slices) return n_tiles;
             qr = own_q;
@@ -115,14 +138,14 @@ chunked_backward_kernel(const __grid_constant__ CUtensorMap map_g,
         long long first = n_tiles;
         if (misaligned) {
             atomicOr(status, kStatusTmaTimeout);
-            if (!own) atomicExch(&ctrl->abort, 1u);
+            if (lookback) atomicExch(&ctrl->abort, 1u);
         } else {
             for (int st = 0; st < ST; ++st) mbar_init(&sm.full[st], 1);
             mbar_fence_init();
             tmap_prefetch(&map_g);
             tmap_prefetch(&map_a);
-            if (want_da) tmap_prefetch(&map_h);
-            if (!own) {
+            if (load_h) tmap_prefetch(&map_h);
+            if (lookback) {
                 const uint32_t tag = ld_relaxed_u32(&ctrl->epoch) + 1u;
                 sm.tag = tag == 0 ? 1u : tag;
             }
@@ -134,7 +157,7 @@ chunked_backward_kernel(const __grid_constant__ CUtensorMap map_g,
     }
     __syncthreads();
 
-    const uint32_t tag = own ? 0u : sm.tag;
+    const uint32_t tag = lookback ? sm.tag : 0u;
     uint32_t phases = 0;
     long long next_fill = 1;
     bool ended = sm.tile[0].id >= n_tiles;
@@ -150,7 +173,7 @@ chunked_backward_kernel(const __grid_constant__ CUtensorMap map_g,
 
         if (!mbar_wait_bounded(&sm.full[st], (phases >> st) & 1u, kTmaPolls)) {
             atomicOr(status, kStatusTmaTimeout);
-            if (!own) atomicExch(&ctrl->abort, 1u);
+            if (lookback) atomicExch(&ctrl->abort, 1u);
         }
         phases ^= 1u << st;
 
@@ -172,7 +195,7 @@ chunked_backward_kernel(const __grid_constant__ CUtensorMap map_g,
                 }
                 ++next_fill;
             }
-            if (!own) {
+            if (lookback) {
                 if (!ended && ahead < 0) ahead = next_tile(ahead_q, ahead_slice);
                 abort_seen = ld_relaxed_u32(&ctrl->abort);
             }
@@ -228,6 +251,18 @@ chunked_backward_kernel(const __grid_constant__ CUtensorMap map_g,
                 run = fmaf(tA, carry, tB);
                 sm.carry[cc] = carry;
             }
+        } else if (reduce) {
+            // the tile's map; the last chunk's absorbs dh_last, so the scan of these maps
+            // from 0 (in reversed chunk order) is the chain of running c values
+            if (ss == 0) {
+                tileA[id * TD + cc] = (qr == 0) ? 0.0f : tA;
+                tileB[id * TD + cc] = (qr == 0) ? fmaf(tA, c_after, tB) : tB;
+                // kept for the apply launch: dh_init may be the same buffer as dh_last, and the
+                // apply launch writes it while other tiles still need the incoming state
+                if (qr == 0) tileX[id * TD + cc] = c_after;
+            }
+        } else if (apply) {
+            if (ss == 0) sm.carry[cc] = (qr == 0) ? tileX[id * TD + cc] : tileH[(id - n_slices) * TD + cc];
         } else {
             const bool publish = (qr + 1 < chunks) && (id != silent_tile);
             float carry = c_after;
@@ -244,7 +279,7 @@ chunked_backward_kernel(const __grid_constant__ CUtensorMap map_g,
         // ---- replay from the carried value; db = c, da = c * h_{t-1} ------------------
         float cv = fmaf(sm.segA[s][c], sm.carry[c], sm.segB[s][c]);
         const long long d = d0 + c;
-        if (d < D) {
+        if (!reduce && d < D) {
             const long long trow = t0 + rtop;             // latest row of this thread
             float *pdb = db + (bi * L + trow) * D + d;
             float *pda = want_da ? da + (bi * L + trow) * D + d : nullptr;
@@ -268,7 +303,7 @@ chunked_backward_kernel(const __grid_constant__ CUtensorMap map_g,
 
     pdl_release();   // this CTA's tiles are done: the next launch may be scheduled
 
-    if (!own) {
+    if (lookback) {
         __syncthreads();
         if (tid == 0) {
             __threadfence();
@@ -333,7 +368,7 @@ cudaError_t launch_backward(const BackwardLaunch &p, cudaStream_t stream) {
     if (err != cudaSuccess) return err;
     long long L = p.L, D = p.D, spb = p.slices_per_batch, ns = p.n_slices, ch = p.chunks, nt = p.n_tiles;
     long long spin = p.spin_limit, silent = p.silent_tile;
-    int own = p.own ? 1 : 0;
+    int mode = p.mode;
     const float *a = p.a;
     float *da = p.da, *db = p.db;
     Control *ctrl = p.ctrl;
@@ -342,7 +377,7 @@ cudaError_t launch_backward(const BackwardLaunch &p, cudaStream_t stream) {
     const float *h_init = p.h_init, *dh_last = p.dh_last;
     float *dh_init = p.dh_init;
     void *args[] = {(void *)&p.map_g, (void *)&p.map_a, (void *)&p.map_h, &a, &da, &db, &L, &D, &spb, &ns, &ch,
-                    &nt, &own, &ctrl, &words, &status, &spin, &silent, &h_init, &dh_last, &dh_init};
+                    &nt, &mode, &ctrl, &words, &status, &spin, &silent, &h_init, &dh_last, &dh_init};
     return launch_dependent(fn, dim3((unsigned)p.grid), dim3((unsigned)p.variant->threads), p.variant->smem_bytes,
                             stream, args);
 }

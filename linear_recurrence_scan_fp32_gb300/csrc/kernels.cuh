@@ -123,7 +123,7 @@ struct BackwardLaunch {
     const float *a;                    // for a_0 in dh_init
     float *da = nullptr, *db = nullptr;
     int64_t L, D, slices_per_batch, n_slices, chunks, n_tiles, grid;
-    bool own;
+    int mode;                          // kModeOwn, kModeLookback, kModeReduce, kModeApply
     Control *ctrl;
     unsigned long long *words;
     unsigned int *status;

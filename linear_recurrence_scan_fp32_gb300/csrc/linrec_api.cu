@@ -213,13 +213,13 @@ linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int ali
     // bound by how fast inclusive values travel down the chain), by the
     // two-pass mode: reduce, scan the aggregates, apply.
     if (opt->chunk_mode < 0 || opt->chunk_mode > 3) return LINREC_ERR_INVALID_VALUE;
-    if (opt->chunk_mode == 3 && (backward || !allow_twopass)) return LINREC_ERR_INVALID_VALUE;
+    if (opt->chunk_mode == 3 && !allow_twopass) return LINREC_ERR_INVALID_VALUE;
     bool own = false, twopass = false;
     if (opt->chunk_mode == 0) {
         const int td = opt->tile_d ? opt->tile_d : 32;
         own = B * ((D + td - 1) / td) >= (int64_t)sm_count;
         const int tt = opt->tile_t ? opt->tile_t : (dtype == kDtypeF32 ? 128 : tile_t_16(L));
-        twopass = !own && !backward && allow_twopass && (L + tt - 1) / tt >= kTwoPassMinChunks;
+        twopass = !own && allow_twopass && (L + tt - 1) / tt >= kTwoPassMinChunks;
     } else {
         own = opt->chunk_mode == 1;
         twopass = opt->chunk_mode == 3;
@@ -778,8 +778,14 @@ linrec_status_t linrec_scan_f32_backward_ex(const float *a, const float *h, cons
         !encode_map(&p.map_a, a, B, L, D, plan.tile_d, plan.tile_t) ||
         !encode_map(&p.map_h, da ? h : a, B, L, D, plan.tile_d, plan.tile_t))
         return LINREC_ERR_LAUNCH;
-    Slot *ws = workspace(dev, stream, plan.workspace_bytes);
+    // two-pass: the Control block in the tagged slot, the per-tile arrays in an array slot
+    Slot *ws = workspace(dev, stream, plan.twopass ? kWorkspaceHead : plan.workspace_bytes);
     if (!ws) return LINREC_ERR_WORKSPACE;
+    Slot *arrays = nullptr;
+    if (plan.twopass) {
+        arrays = workspace(dev, stream, plan.workspace_bytes - kWorkspaceHead, 0, kSlotArrays);
+        if (!arrays) return LINREC_ERR_WORKSPACE;
+    }
     p.a = a;
     p.da = da;
     p.db = db;
@@ -790,9 +796,9 @@ linrec_status_t linrec_scan_f32_backward_ex(const float *a, const float *h, cons
     p.chunks = plan.chunks;
     p.n_tiles = plan.n_tiles;
     p.grid = plan.grid;
-    p.own = plan.lookback == 0;
+    p.mode = plan.twopass ? kModeReduce : plan.lookback ? kModeLookback : kModeOwn;
     p.ctrl = reinterpret_cast<Control *>(ws->base);
-    p.words = reinterpret_cast<unsigned long long *>(ws->base + kWorkspaceHead);
+    p.words = reinterpret_cast<unsigned long long *>(arrays ? arrays->base : ws->base + kWorkspaceHead);
     p.status = opt->d_status ? opt->d_status : &p.ctrl->status;
     p.spin_limit = opt->spin_limit > 0 ? opt->spin_limit : kDefaultSpinLimit;
     p.silent_tile = opt->test_silent_tile > 0 ? opt->test_silent_tile - 1 : -1;
@@ -800,6 +806,25 @@ linrec_status_t linrec_scan_f32_backward_ex(const float *a, const float *h, cons
     p.dh_last = dh_last;
     p.dh_init = dh_init;
     cudaError_t err = launch_backward(p, stream);
+    if (err != cudaSuccess) {
+        cudaGetLastError();
+        return LINREC_ERR_LAUNCH;
+    }
+    if (!plan.twopass) return LINREC_OK;
+
+    // Two-pass mode: the tiles' maps, in reversed chunk order, form a (1, chunks,
+    // n_slices * tile_d) problem whose forward scan gives every tile's running c.
+    float *tileA = reinterpret_cast<float *>(p.words);
+    float *tileB = tileA + p.n_tiles * plan.tile_d;
+    float *tileH = tileB + p.n_tiles * plan.tile_d;
+    linrec_options_t inner = {};
+    inner.d_status = p.status;
+    inner.spin_limit = opt->spin_limit;
+    st = scan_locked(di, dev, tileA, tileB, tileH, 1, p.chunks, p.n_slices * plan.tile_d, kDtypeF32, stream, &inner,
+                     1);
+    if (st != LINREC_OK) return st;
+    p.mode = kModeApply;
+    err = launch_backward(p, stream);
     if (err != cudaSuccess) {
         cudaGetLastError();
         return LINREC_ERR_LAUNCH;

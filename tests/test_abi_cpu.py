@@ -174,9 +174,11 @@ def test_plan_chunk_modes():
     # ... and the two-pass mode by default
     p = lr.linrec_plan_f32(1, 1 << 20, 64, path="chunked", sm_count=152)
     assert p["twopass"] == 1 and p["workspace_bytes"] == 256 + 4 * (3 * p["n_tiles"] + 64 // p["tile_d"]) * p["tile_d"]
-    # the two-pass mode is forward-only
-    with pytest.raises(lr.LinrecError):
-        lr.linrec_plan_f32_backward(1, 1 << 20, 64, chunk_mode="twopass")
+    # the gradient takes the two-pass mode too, by default for few long slices
+    p = lr.linrec_plan_f32_backward(1, 1 << 20, 64, sm_count=152)
+    assert p["twopass"] == 1 and p["lookback"] == 0
+    assert p["workspace_bytes"] == 256 + 4 * (3 * p["n_tiles"] + 64 // p["tile_d"]) * p["tile_d"]
+    assert lr.linrec_plan_f32_backward(1, 1 << 20, 64, chunk_mode="lookback")["lookback"] == 1
     with pytest.raises(lr.LinrecError):
         lr.linrec_plan_f32(1, 1000, 64, path="chunked", chunk_mode=4)
 

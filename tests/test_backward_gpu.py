@@ -16,7 +16,9 @@ DEV = torch.device("cuda:0")
 PATHS = [{}, {"path": "regcarry"}, {"path": "regcarry", "vec": 1},
          {"path": "chunked", "chunk_mode": "own"}, {"path": "chunked", "chunk_mode": "lookback"},
          {"path": "chunked", "chunk_mode": "own", "tile_d": 32, "tile_t": 64, "stages": 3},
-         {"path": "chunked", "chunk_mode": "lookback", "tile_d": 64, "tile_t": 128, "stages": 2}]
+         {"path": "chunked", "chunk_mode": "lookback", "tile_d": 64, "tile_t": 128, "stages": 2},
+         {"path": "chunked", "chunk_mode": "twopass"},
+         {"path": "chunked", "chunk_mode": "twopass", "tile_d": 64, "tile_t": 64, "stages": 2}]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -79,7 +81,8 @@ def test_backward_full_size(name):
     h = h_d.cpu()
     da64, db64, _ = oracle.f64_backward(a, h, g)
     del a, h, g
-    for opt in [{}, {"path": "chunked", "chunk_mode": "own"}, {"path": "chunked", "chunk_mode": "lookback"}]:
+    for opt in [{}, {"path": "chunked", "chunk_mode": "own"}, {"path": "chunked", "chunk_mode": "lookback"},
+                {"path": "chunked", "chunk_mode": "twopass"}]:
         da, db = lr.linrec_scan_f32_backward(a_d, h_d, g_d, **opt)
         torch.cuda.synchronize()
         assert_close(db.cpu().numpy(), db64, f"{name} {opt} db")
