@@ -32,6 +32,10 @@
  *  - Thread-safe: calls from several host threads may run concurrently.  Calls
  *    on one stream run in order; each stream gets its own look-back workspace,
  *    so calls on different streams may overlap on the GPU.
+ *  - The kernels are launched as programmatic dependents: a call's kernel may
+ *    be scheduled while the previous work on the stream drains, but it touches
+ *    no memory before that work has completed, so stream order holds as for a
+ *    plain launch.
  */
 #ifndef LINREC_H_
 #define LINREC_H_
@@ -82,9 +86,10 @@ typedef struct {
     int ctas_per_sm;     /* chunked: cap on resident CTAs per SM (0 = as many as fit) */
     int chunk_mode;      /* chunked: 1 = each CTA owns whole channel slices and carries h from
                             chunk to chunk itself; 2 = chunks of a slice spread over CTAs, joined
-                            by the decoupled look-back; 3 = two passes (forward scan only): a
-                            launch writes every chunk's aggregate, the aggregates are scanned,
-                            a launch applies them; 0 = the dispatcher's choice */
+                            by the decoupled look-back; 3 = two passes: a launch writes every
+                            chunk's aggregate, the aggregates are scanned, a launch applies them
+                            (the gradient runs them in reversed chunk order); 0 = the
+                            dispatcher's choice */
     unsigned int *d_status; /* device word (may be NULL): the kernel ORs 1 << linrec_status_t
                                into it on a device-side failure; otherwise the stream's own word
                                is used (read it with linrec_stream_status) */
@@ -131,7 +136,9 @@ linrec_status_t linrec_scan_f32_carry(const float *a, const float *b, float *h,
  *
  * with h_{-1} = h_init (or 0 when h_init is NULL: a_0 was unused, da_0 = 0).
  * It is the same recurrence run right to left with the slope one step later,
- * on the same kernels.  Pointers are device memory of the current device:
+ * on the same machinery: slice-owner, look-back or (few long slices) two-pass
+ * mode, the last moving 28 bytes per element with da instead of 20 but
+ * waiting on no chain.  Pointers are device memory of the current device:
  *   a, g        (B, L, D) in;  h (B, L, D) in: the forward output (needed
  *               only for da; may be NULL when da is NULL);
  *   da          (B, L, D) out or NULL (then h is not read: 12 bytes moved
