@@ -19,7 +19,7 @@ namespace {
 constexpr int kVersion = 100;               // 0.1.0
 constexpr int64_t kDefaultSpinLimit = 1 << 20;
 constexpr int kRegcarryThreads = 256;
-// fp32 forward: the register path from this many 4-channel threads per SM on
+// forward scans: the register path from this many 16-byte threads per SM on
 constexpr int64_t kRegcarryMinThreadsPerSm = 96;
 // Few slices: the two-pass mode from this many time chunks of 128 steps on.
 constexpr int64_t kTwoPassMinChunks = 64;
@@ -163,17 +163,21 @@ linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int ali
     if (backward && dtype != kDtypeF32) return LINREC_ERR_INVALID_VALUE;
     const bool tma_ok = align_bytes >= 16 && (D * eb) % 16 == 0 && D <= INT32_MAX && B <= INT32_MAX &&
                         L <= (int64_t)INT32_MAX - 1024;
-    // The register path when the channels alone keep enough loads in flight: fp32
-    // forward with at least kRegcarryMinThreadsPerSm 4-channel threads per SM.
-    // Measured on GB300: (256, 128, 4096) 6922 vs 6007 GB/s for the chunked kernel,
-    // (64, 2048, 1024) 6193 vs 5976; at 32768 channels it loses (4361 vs 5722 on
-    // (8, 4096, 4096)), and in 16-bit storage it loses at every shape measured.
+    // The register path when the channels alone keep enough loads in flight: a
+    // forward scan with at least kRegcarryMinThreadsPerSm threads of 16 bytes of
+    // channels per SM.  Measured on GB300, fp32: (256, 128, 4096) 6922 vs 6007 GB/s
+    // for the chunked kernel, (64, 2048, 1024) 6193 vs 5976; at 32768 channels it
+    // loses (4361 vs 5722 on (8, 4096, 4096)).  16-bit storage: only below 256 steps,
+    // where the chunked kernel cannot use its 256-step tiles ((256, 128, 4096)
+    // bfloat16 6391 vs 4638; (64, 512, 4096) 6309 vs 6574 for the chunked kernel).
     // Otherwise the TMA-staged chunked kernel whenever its copies are legal; the
     // register path also takes misaligned pointers and D % 4 != 0.
     int path = opt->path;
     if (path == LINREC_PATH_AUTO) {
-        const bool many = dtype == kDtypeF32 && !backward && D % 4 == 0 && align_bytes >= 16 &&
-                          B * (D / 4) >= kRegcarryMinThreadsPerSm * (int64_t)sm_count;
+        const int lanes = 16 / eb;            // channels in 16 bytes
+        const bool many = !backward && D % lanes == 0 && align_bytes >= 16 &&
+                          (dtype == kDtypeF32 || L < 256) &&
+                          B * (D / lanes) >= kRegcarryMinThreadsPerSm * (int64_t)sm_count;
         path = (tma_ok && !many) ? LINREC_PATH_CHUNKED : LINREC_PATH_REGCARRY;
     }
     plan->path = path;

@@ -86,11 +86,15 @@ def test_plan_paths():
     assert p["path_name"] == "regcarry" and (p["vec"], p["prefetch"]) == (4, 16)
     p = lr.linrec_plan_f32(64, 1024, 4096, sm_count=152)
     assert p["path_name"] == "regcarry" and p["prefetch"] == 8
-    # ... but not below 96 four-channel threads per SM, nor for 16-bit storage or the gradient
+    # ... but not below 96 four-channel threads per SM, nor for the gradient
     p = lr.linrec_plan_f32(8, 4096, 4096, sm_count=152)
     assert p["path_name"] == "chunked" and p["lookback"] == 0
-    assert lr.linrec_plan_16(256, 128, 4096, sm_count=152)["path_name"] == "chunked"
     assert lr.linrec_plan_f32_backward(256, 128, 4096, sm_count=152)["path_name"] == "chunked"
+    # 16-bit storage: the register path only below 256 steps (eight channels per thread)
+    p = lr.linrec_plan_16(256, 128, 4096, sm_count=152)
+    assert p["path_name"] == "regcarry" and (p["vec"], p["prefetch"]) == (8, 16)
+    assert lr.linrec_plan_16(64, 512, 4096, sm_count=152)["path_name"] == "chunked"
+    assert lr.linrec_plan_16(8, 128, 4096, sm_count=152)["path_name"] == "chunked"
     # many channels, fewer of them: the chunked kernel, each CTA owning whole slices
     p = lr.linrec_plan_f32(32, 4096, 256, sm_count=152)
     assert p["path_name"] == "chunked" and p["lookback"] == 0
@@ -207,7 +211,7 @@ def test_plan_16bit_storage():
     p = lr.linrec_plan_16(32, 4096, 256, sm_count=152)
     assert p["path_name"] == "chunked" and p["lookback"] == 0
     assert (p["tile_d"], p["tile_t"], p["stages"]) == (32, 256, 2)
-    p = lr.linrec_plan_16(256, 128, 4096, sm_count=152)
+    p = lr.linrec_plan_16(256, 128, 4096, sm_count=152, path="chunked")
     assert (p["tile_d"], p["tile_t"], p["stages"], p["lookback"]) == (32, 64, 6, 0)
     # few long slices: two-pass, whose aggregates are fp32 whatever the storage
     p = lr.linrec_plan_16(1, 1 << 20, 64)
