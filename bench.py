@@ -201,27 +201,41 @@ def committed_traffic(kernel: str, workload: str):
 # arms
 # ---------------------------------------------------------------------------
 
-def cpu_baseline(a, b, w, budget_s: float = 10.0, dtype: str = "f32"):
+def cpu_baseline(a, b, w, budget_s: float = 10.0, dtype: str = "f32", h_gpu=None):
     """The oracle as it stands, all host cores, repeated over the full workload for ~budget_s.
     16-bit storage: the oracle's decode of the stored words, then its fp64 scan (one thread
-    decodes; the scan runs on all cores)."""
+    decodes; the scan runs on all cores).  Returns (baseline, parity): parity compares h_gpu,
+    the output of the timed GPU run, with the oracle's result, element by element."""
     import oracle
     oracle.build()
     threads = oracle.hardware_threads()
     reps, t_total = 0, 0.0
     used = threads
     nbytes = bytes_per_step(w, "forward", dtype)
+    h64 = None
     while t_total < budget_s and reps < 1000:
         t0 = time.perf_counter()
         if dtype == "f32":
-            _, used = oracle.f64(a, b, nthreads=threads)
+            h64, used = oracle.f64(a, b, nthreads=threads)
         else:
-            oracle.f64_16(dtype, a, b)
+            h64, _ = oracle.f64_16(dtype, a, b)
         t_total += time.perf_counter() - t0
         reps += 1
     what = "fp64 sequential oracle" if dtype == "f32" else f"oracle {dtype} decode + fp64 scan"
-    return {"value": nbytes * reps / t_total / 1e9, "unit": UNIT, "cores": used, "kind": "oracle",
+    base = {"value": nbytes * reps / t_total / 1e9, "unit": UNIT, "cores": used, "kind": "oracle",
             "sample": f"full {w.name} workload {w.shape}, {what}, {reps} repetitions, {t_total:.1f} s"}
+    parity = None
+    if h_gpu is not None and h64 is not None:
+        # 16-bit storage: the output words, decoded by the oracle's own definition of the format
+        got = np.asarray(h_gpu, dtype=np.float64) if dtype == "f32" else oracle.decode16(dtype, h_gpu)
+        err = np.abs(got - h64)
+        u = {"f32": 0.0, "bf16": 2.0 ** -8, "f16": 2.0 ** -11}[dtype]
+        bound = u * np.abs(h64) + (1 + u) * 1e-4 * (1 + np.abs(h64))
+        parity = {"vs": "fp64 oracle, every element of the timed run's output",
+                  "max_abs_err": float(err.max()), "max_rel_err": float((err / (1 + np.abs(h64))).max()),
+                  "bound": "u*|h64| + (1+u)*1e-4*(1+|h64|), u = 0 (fp32), 2^-8 (bf16), 2^-11 (f16)",
+                  "within_bound": bool((err <= bound).all())}
+    return base, parity
 
 
 def cpu_baseline_backward(a, h, g, w, nbytes, budget_s: float = 10.0):
@@ -484,6 +498,7 @@ def run_ours(args):
                "path": e2e_path}
 
     cpu = None
+    parity = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         if args.op == "backward":
             cpu = cpu_baseline_backward(a_cpu.numpy(), h.cpu().numpy(), g_cpu.numpy(), w, nbytes,
@@ -492,10 +507,14 @@ def run_ours(args):
             # the oracle scans (B, L, D); the (B, D, L) values are the same numbers transposed
             ca, cb = (a_cpu.transpose(1, 2).contiguous(), b_cpu.transpose(1, 2).contiguous()) if bdl \
                 else (a_cpu, b_cpu)
+            hc = h.cpu()
+            if bdl:
+                hc = hc.transpose(1, 2).contiguous()
             if args.dtype == "f32":
-                cpu = cpu_baseline(ca.numpy(), cb.numpy(), w, budget_s=args.cpu_seconds)
+                cpu, parity = cpu_baseline(ca.numpy(), cb.numpy(), w, budget_s=args.cpu_seconds, h_gpu=hc.numpy())
             else:
-                cpu = cpu_baseline(ca, cb, w, budget_s=args.cpu_seconds, dtype=args.dtype)
+                words = hc.view(torch.int16).numpy().view(np.uint16)
+                cpu, parity = cpu_baseline(ca, cb, w, budget_s=args.cpu_seconds, dtype=args.dtype, h_gpu=words)
 
     if rank == 0:
         clk = clocks.summary()
@@ -522,6 +541,7 @@ def run_ours(args):
             "copy_ceiling_gbs": copy_gbs,
             "frac_of_copy_ceiling": round(value / ceiling, 4),
             "cpu_baseline": cpu,
+            "parity": parity,
             "e2e": e2e,
             "gpu_launches": args.steps * launches,
             "clocks": clk,

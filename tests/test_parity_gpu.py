@@ -204,6 +204,25 @@ def test_deterministic_bits():
                 assert torch.equal(run(a_d, b_d, **opt), h1), f"{name} {opt}: bits changed between calls"
 
 
+@pytest.mark.parametrize("mode", ["lookback", "twopass"])
+def test_carry_modes_repeat_bit_identical(mode):
+    """A race check on the cross-CTA carry: 50 calls of the look-back or two-pass mode, whose
+    tiles land on different CTAs in a different order every time, all return the same bits."""
+    for (B, L, D, tile) in [(1, 1 << 18, 64, {}), (2, 50000, 128, {"tile_d": 32, "tile_t": 64, "stages": 3})]:
+        a, b = inputs.generate(B, L, D, seed=19 + L, a_dist="u[0.9,1)", b_dist="n(0,1)")
+        a_d, b_d = a.to(DEV), b.to(DEV)
+        opt = dict(path="chunked", chunk_mode=mode, **tile)
+        first = run(a_d, b_d, **opt).clone()
+        h = torch.empty_like(first)
+        for k in range(50):
+            lr.linrec_scan_f32_ex(a_d, b_d, h, **opt)
+            torch.cuda.synchronize()
+            assert torch.equal(h, first), f"{mode} {(B, L, D)} call {k}: bits changed"
+        h64, _ = oracle.f64(a, b)
+        assert_close(first.cpu().numpy(), h64, f"{mode} {(B, L, D)}")
+    assert lr.linrec_stream_status() == lr.LINREC_OK
+
+
 def test_misaligned_pointers_take_the_scalar_path():
     B, L, D = 2, 300, 64
     a, b = inputs.generate(B, L, D, seed=9, a_dist="u[0.5,1)", b_dist="n(0,1)")
