@@ -78,7 +78,9 @@ linrec_status_t linrec_scan_f32(const float *a, const float *b, float *h,
  */
 typedef struct {
     int path;            /* linrec_path_t */
-    int vec;             /* regcarry: channels per thread, 1, 2 or 4 (16-bit storage: 1, 2, 4 or 8) */
+    int vec;             /* regcarry: channels per thread, 1, 2 or 4 (16-bit storage: 1, 2, 4 or 8);
+                            chunked: adjacent channels per thread, 1, or 2 for 16-bit storage (one
+                            32-bit shared-memory load and one packed store per step for both) */
     int prefetch;        /* regcarry: time steps loaded ahead, 4, 8 or 16 */
     int tile_t;          /* chunked: time steps per tile */
     int tile_d;          /* chunked: channels per tile */
@@ -100,6 +102,9 @@ typedef struct {
                                  publish nothing, so its successor's look-back times out */
     int rows_per_warp;   /* (B, D, L) layout, one pass: consecutive rows each warp scans as one
                             stream (0 = the dispatcher's choice) */
+    int segments;        /* chunked: segments a tile's time steps are split into, one thread
+                            each per channel group (0 = the dispatcher's choice for its default
+                            16-bit tile, else the first compiled variant of the tile) */
 } linrec_options_t;
 
 /*

@@ -71,6 +71,7 @@ class Options(ctypes.Structure):
         ("spin_limit", ctypes.c_int64),
         ("test_silent_tile", ctypes.c_int64),
         ("rows_per_warp", ctypes.c_int),
+        ("segments", ctypes.c_int),
     ]
 
 
@@ -173,7 +174,7 @@ def _addr(x):
 
 def make_options(path="auto", vec=0, prefetch=0, tile_t=0, tile_d=0, stages=0, ctas_per_sm=0,
                  chunk_mode="auto", d_status=None, h_init=None, h_last=None, spin_limit=0,
-                 test_silent_tile=0, rows_per_warp=0) -> Options:
+                 test_silent_tile=0, rows_per_warp=0, segments=0) -> Options:
     o = Options()
     o.path = PATHS[path] if isinstance(path, str) else int(path)
     o.vec, o.prefetch, o.tile_t, o.tile_d, o.stages = int(vec), int(prefetch), int(tile_t), int(tile_d), int(stages)
@@ -185,6 +186,7 @@ def make_options(path="auto", vec=0, prefetch=0, tile_t=0, tile_d=0, stages=0, c
     o.spin_limit = int(spin_limit)
     o.test_silent_tile = int(test_silent_tile)
     o.rows_per_warp = int(rows_per_warp)
+    o.segments = int(segments)
     return o
 
 

@@ -43,7 +43,7 @@ struct __align__(128) BackSmem {
     float g[ST][TT * TD];
     float a[ST][TT * TD];               // row r holds a_{t0 + r + 1}
     float h[ST][TT * TD];               // row r holds h_{t0 + r - 1}
-    float segA[S][TD], segB[S][TD];
+    float segA[S][TD + 32 / S], segB[S][TD + 32 / S];   // padded: the transposed reads hit 32 banks
     float carry[TD];
     uint64_t full[ST];
     TileCoord tile[ST];

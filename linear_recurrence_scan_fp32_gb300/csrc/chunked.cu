@@ -21,16 +21,16 @@ namespace {
     X(32, 64, 4, 4)                \
     X(32, 32, 2, 6)
 
-#define LINREC_V_ENTRY(TD, TT, S, ST) make_variant<kDtypeF32, TD, TT, S, ST>(),
+#define LINREC_V_ENTRY(TD, TT, S, ST) make_variant<kDtypeF32, TD, TT, S, ST, 1>(),
 const ChunkedVariant kVariants[] = {LINREC_CHUNKED_VARIANTS(LINREC_V_ENTRY)};
 #undef LINREC_V_ENTRY
 
 const void *kernel_of(const ChunkedVariant *v, int dtype) {
     if (dtype != kDtypeF32) return chunked16_kernel(v, dtype);
     if (v->elem_bytes != 4) return nullptr;
-#define LINREC_K_ENTRY(TD, TT, S, ST)                                                        \
-    if (v->tile_d == TD && v->tile_t == TT && v->segments == S && v->stages == ST)           \
-        return reinterpret_cast<const void *>(&chunked_scan_kernel<kDtypeF32, TD, TT, S, ST>);
+#define LINREC_K_ENTRY(TD, TT, S, ST)                                                                \
+    if (v->tile_d == TD && v->tile_t == TT && v->segments == S && v->stages == ST && v->cpt == 1)    \
+        return reinterpret_cast<const void *>(&chunked_scan_kernel<kDtypeF32, TD, TT, S, ST, 1>);
     LINREC_CHUNKED_VARIANTS(LINREC_K_ENTRY)
 #undef LINREC_K_ENTRY
     return nullptr;

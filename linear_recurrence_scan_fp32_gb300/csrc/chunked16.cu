@@ -9,23 +9,26 @@ namespace linrec {
 namespace {
 
 #define LINREC_CHUNKED16_VARIANTS(X) \
-    X(32, 128, 8, 3)                 \
-    X(32, 128, 8, 4)                 \
-    X(32, 128, 8, 6)                 \
-    X(64, 128, 8, 2)                 \
-    X(64, 128, 8, 3)                 \
-    X(64, 64, 4, 4)                  \
-    X(32, 64, 4, 6)                  \
-    X(128, 64, 4, 3)                 \
-    X(32, 256, 8, 2)                 \
-    X(32, 256, 8, 3)
+    X(32, 128, 8, 3, 1)              \
+    X(32, 128, 8, 4, 1)              \
+    X(32, 128, 8, 6, 1)              \
+    X(64, 128, 8, 2, 1)              \
+    X(64, 128, 8, 3, 1)              \
+    X(64, 64, 4, 4, 1)               \
+    X(32, 64, 4, 6, 1)               \
+    X(128, 64, 4, 3, 1)              \
+    X(32, 256, 8, 2, 1)              \
+    X(32, 256, 8, 3, 1)              \
+    X(32, 256, 16, 2, 2)             \
+    X(32, 256, 8, 2, 2)              \
+    X(32, 64, 8, 6, 2)
 
-#define LINREC_V_ENTRY(TD, TT, S, ST) make_variant<kDtypeBF16, TD, TT, S, ST>(),
+#define LINREC_V_ENTRY(TD, TT, S, ST, CPT) make_variant<kDtypeBF16, TD, TT, S, ST, CPT>(),
 const ChunkedVariant kVariants16[] = {LINREC_CHUNKED16_VARIANTS(LINREC_V_ENTRY)};
 #undef LINREC_V_ENTRY
 
 // both 16-bit kinds share each variant's shared-memory layout
-#define LINREC_SAME_SIZE(TD, TT, S, ST)                                                          \
+#define LINREC_SAME_SIZE(TD, TT, S, ST, CPT)                                                     \
     static_assert(sizeof(ChunkSmem<Storage<kDtypeBF16>::raw, TD, TT, S, ST>) ==                  \
                   sizeof(ChunkSmem<Storage<kDtypeF16>::raw, TD, TT, S, ST>), "16-bit layouts");
 LINREC_CHUNKED16_VARIANTS(LINREC_SAME_SIZE)
@@ -40,13 +43,13 @@ const ChunkedVariant *chunked_variants_16(int *count) {
 
 const void *chunked16_kernel(const ChunkedVariant *v, int dtype) {
     if (v->elem_bytes != 2) return nullptr;
-#define LINREC_K_ENTRY(TD, TT, S, ST)                                                            \
-    if (v->tile_d == TD && v->tile_t == TT && v->segments == S && v->stages == ST) {             \
-        if (dtype == kDtypeBF16)                                                                 \
-            return reinterpret_cast<const void *>(&chunked_scan_kernel<kDtypeBF16, TD, TT, S, ST>); \
-        if (dtype == kDtypeF16)                                                                  \
-            return reinterpret_cast<const void *>(&chunked_scan_kernel<kDtypeF16, TD, TT, S, ST>);  \
-        return nullptr;                                                                          \
+#define LINREC_K_ENTRY(TD, TT, S, ST, CPT)                                                           \
+    if (v->tile_d == TD && v->tile_t == TT && v->segments == S && v->stages == ST && v->cpt == CPT) {   \
+        if (dtype == kDtypeBF16)                                                                      \
+            return reinterpret_cast<const void *>(&chunked_scan_kernel<kDtypeBF16, TD, TT, S, ST, CPT>); \
+        if (dtype == kDtypeF16)                                                                       \
+            return reinterpret_cast<const void *>(&chunked_scan_kernel<kDtypeF16, TD, TT, S, ST, CPT>);  \
+        return nullptr;                                                                               \
     }
     LINREC_CHUNKED16_VARIANTS(LINREC_K_ENTRY)
 #undef LINREC_K_ENTRY

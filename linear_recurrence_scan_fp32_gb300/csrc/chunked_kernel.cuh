@@ -8,15 +8,17 @@
 // index over all L; its tiles are its time chunks q = 0 .. chunks-1, and tile
 // id = q * n_slices + slice.
 //
-// Per tile, inside one CTA of TD * S threads:
+// Per tile, inside one CTA of TD/CPT * S threads (CPT = channels per thread, 1, or
+// 2 for 16-bit storage; the results do not depend on it):
 //  1. TMA copies the a and b boxes (TT x TD stored elements each) into a
 //     shared-memory ring of ST stages; one mbarrier per stage counts the bytes.
 //     A stage is refilled as soon as every thread has its tile in registers
 //     (after the tile's first barrier), so up to ST + 1 tiles are in flight.
 //     Elements are widened to fp32 as threads read them (storage.cuh); all
 //     arithmetic and every carry is fp32, and h is rounded once when stored.
-//  2. Thread (channel c, segment s) composes its K = TT/S consecutive affine
-//     maps x -> a*x + b into one pair (A, B), later map on the left:
+//  2. Thread (channel group c, segment s) composes, for each of its channels, its
+//     K = TT/S consecutive affine maps x -> a*x + b into one pair (A, B), later
+//     map on the left:
 //     (a2,b2) o (a1,b1) = (a2*a1, a2*b1 + b2) ("Kimi-K2.6 l1_p9", derivation of
 //     the associative operator).  Its a, b values stay in registers.
 //  3. A warp-shuffle scan over the S segment pairs of each channel gives every
@@ -69,15 +71,19 @@ struct TileCoord {
     int pad;
 };
 
-// A thread's K steps of a and b, held in registers from the compose to the replay.
-// fp32 storage keeps them as floats.  16-bit storage keeps the stored words, two
-// steps to a 32-bit register, and widens each one (exactly) where it is used: a
-// 16-bit tile of twice the steps then costs the registers of an fp32 tile.
-template <int DT, int K, bool PACK = (Storage<DT>::bytes == 2) && (K % 2 == 0)>
+// A thread's K steps of a and b for its CPT adjacent channels, held in registers
+// from the compose to the replay; a(j, i) and b(j, i) are step j of channel i.
+// fp32 storage keeps floats.  16-bit storage keeps the stored words and widens each
+// one (exactly) where it is used: with one channel per thread two steps share a
+// 32-bit register; with two channels a register holds both channels of a step, as
+// shared memory does, so one 32-bit load fetches it.  Either way a 16-bit tile of
+// twice the elements costs the registers of an fp32 tile.
+template <int DT, int K, int CPT,
+          int KIND = (Storage<DT>::bytes == 4 || (CPT == 1 && K % 2 != 0)) ? 0 : (CPT == 1 ? 1 : 2)>
 struct TileRegs;
 
 template <int DT, int K>
-struct TileRegs<DT, K, false> {
+struct TileRegs<DT, K, 1, 0> {
     float a_[K], b_[K];
     template <typename E>
     __device__ __forceinline__ void load(const E *ta, const E *tb, int stride) {
@@ -87,13 +93,17 @@ struct TileRegs<DT, K, false> {
             b_[j] = Storage<DT>::get(tb[j * stride]);
         }
     }
-    __device__ __forceinline__ float a(int j) const { return a_[j]; }
-    __device__ __forceinline__ float b(int j) const { return b_[j]; }
+    __device__ __forceinline__ float a(int j, int) const { return a_[j]; }
+    __device__ __forceinline__ float b(int j, int) const { return b_[j]; }
     __device__ __forceinline__ void zero_a0() { a_[0] = 0.0f; }
 };
 
+__device__ __forceinline__ unsigned short half_of(uint32_t w, int hi) {
+    return (unsigned short)(hi ? (w >> 16) : (w & 0xffffu));
+}
+
 template <int DT, int K>
-struct TileRegs<DT, K, true> {
+struct TileRegs<DT, K, 1, 1> {
     uint32_t a_[K / 2], b_[K / 2];            // step 2i in the low half, step 2i + 1 in the high half
     template <typename E>
     __device__ __forceinline__ void load(const E *ta, const E *tb, int stride) {
@@ -103,30 +113,67 @@ struct TileRegs<DT, K, true> {
             b_[i] = (uint32_t)tb[2 * i * stride] | ((uint32_t)tb[(2 * i + 1) * stride] << 16);
         }
     }
-    __device__ __forceinline__ float a(int j) const {
-        return Storage<DT>::get((unsigned short)((j & 1) ? (a_[j >> 1] >> 16) : (a_[j >> 1] & 0xffffu)));
-    }
-    __device__ __forceinline__ float b(int j) const {
-        return Storage<DT>::get((unsigned short)((j & 1) ? (b_[j >> 1] >> 16) : (b_[j >> 1] & 0xffffu)));
-    }
+    __device__ __forceinline__ float a(int j, int) const { return Storage<DT>::get(half_of(a_[j >> 1], j & 1)); }
+    __device__ __forceinline__ float b(int j, int) const { return Storage<DT>::get(half_of(b_[j >> 1], j & 1)); }
     __device__ __forceinline__ void zero_a0() { a_[0] &= 0xffff0000u; }   // the word 0 is +0 in both formats
 };
+
+template <int DT, int K>
+struct TileRegs<DT, K, 2, 2> {
+    uint32_t a_[K], b_[K];                    // step j: the first channel in the low half
+    template <typename E>
+    __device__ __forceinline__ void load(const E *ta, const E *tb, int stride) {
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+            a_[j] = *reinterpret_cast<const uint32_t *>(ta + j * stride);
+            b_[j] = *reinterpret_cast<const uint32_t *>(tb + j * stride);
+        }
+    }
+    __device__ __forceinline__ float a(int j, int i) const { return Storage<DT>::get(half_of(a_[j], i)); }
+    __device__ __forceinline__ float b(int j, int i) const { return Storage<DT>::get(half_of(b_[j], i)); }
+    __device__ __forceinline__ void zero_a0() { a_[0] = 0u; }
+};
+
+// A thread's CPT adjacent floats of a shared row (8-byte aligned for CPT = 2).
+template <int CPT>
+__device__ __forceinline__ void st_group(float *p, const float (&v)[CPT]) {
+    if constexpr (CPT == 1) *p = v[0];
+    else *reinterpret_cast<float2 *>(p) = make_float2(v[0], v[1]);
+}
+template <int CPT>
+__device__ __forceinline__ void ld_group(const float *p, float (&v)[CPT]) {
+    if constexpr (CPT == 1) {
+        v[0] = *p;
+    } else {
+        const float2 x = *reinterpret_cast<const float2 *>(p);
+        v[0] = x.x;
+        v[1] = x.y;
+    }
+}
+// h of a thread's CPT adjacent channels at one step, rounded once each.
+template <int DT, int CPT>
+__device__ __forceinline__ void st_h(typename Storage<DT>::raw *p, const float (&v)[CPT]) {
+    if constexpr (CPT == 1) *p = Storage<DT>::put(v[0]);
+    else *reinterpret_cast<uint32_t *>(p) = Storage<DT>::put2(v[0], v[1]);
+}
 
 template <typename E, int TD, int TT, int S, int ST>
 struct __align__(128) ChunkSmem {
     E a[ST][TT * TD];                   // stored elements, as the boxes arrive
     E b[ST][TT * TD];
     // Per-segment pairs, then their exclusive prefixes, and the h entering the tile:
-    // two copies, used by alternate tiles (see the barriers in the tile loop).
-    float segA[2][S][TD], segB[2][S][TD];
+    // two copies, used by alternate tiles (see the barriers in the tile loop).  A row
+    // holds TD + 32/S floats: a warp of the transposed role reads 32/S channels x S
+    // segments, which the padding spreads over all 32 banks.
+    float segA[2][S][TD + 32 / S], segB[2][S][TD + 32 / S];
     float carry[2][TD];
     uint64_t full[ST];                  // one mbarrier per ring stage
     TileCoord tile[ST];                 // tile loaded into each stage
     uint32_t tag;                       // look-back tag of this launch
 };
 
-template <int DT, int TD, int TT, int S, int ST>
-__global__ void __launch_bounds__(TD * S, (TD * S >= 512) ? 1 : 2)
+template <int DT, int TD, int TT, int S, int ST, int CPT>
+__global__ void __launch_bounds__(TD / CPT * S, (TD / CPT * S >= 512) ? 1 : 2)
 chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
                     const __grid_constant__ CUtensorMap map_b,
                     typename Storage<DT>::raw *__restrict__ h,
@@ -153,7 +200,10 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
     float *const tileB = tileA + n_tiles * TD;
     const float *const tileH = tileB + n_tiles * TD;
     float *const tileX = tileB + 2 * n_tiles * TD;
+    constexpr int TC = TD / CPT;              // channel groups of a tile
     static_assert(TT % S == 0 && TD % 32 == 0 && (32 % S) == 0 && S >= 2 && ST >= 2, "tile shape");
+    // two channels per thread: 16-bit storage, shared rows of an even number of floats
+    static_assert(CPT == 1 || (CPT == 2 && Storage<DT>::bytes == 2 && (32 / S) % 2 == 0), "channels per thread");
     using Smem = ChunkSmem<E, TD, TT, S, ST>;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
@@ -161,10 +211,10 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
     pdl_wait();   // launched as a programmatic dependent: nothing before it is touched yet
 
     const int tid = threadIdx.x;
-    const int c = tid % TD;                   // channel within the tile
-    const int s = tid / TD;                   // segment within the tile
-    const int cc = tid / S;                   // transposed role: channel ...
-    const int ss = tid % S;                   // ... and segment / look-back window lane
+    const int c = tid % TC;                   // channel group: channels CPT*c .. CPT*c + CPT-1 of the tile
+    const int s = tid / TC;                   // segment within the tile
+    const int cc = tid / S;                   // transposed role: channels cc, cc + TC, ... (one per
+    const int ss = tid % S;                   // group), and the segment / look-back window lane
     const int gbase = (tid & 31) & ~(S - 1);  // first lane of this channel's group in the warp
 
     unsigned long long *const wAggA = words;
@@ -242,7 +292,9 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
     bool ended = sm.tile[0].id >= n_tiles;    // (thread 0) no more tiles to take
     long long ahead = -1, ahead_q = 0, ahead_slice = 0;   // (thread 0, look-back) tile taken early
     uint32_t abort_seen = 0;                  // (thread 0, look-back) abort word, read one iteration early
-    float run = 0.0f;                         // (slice-owner, ss == 0) inclusive value of the last tile
+    float run[CPT];                           // (slice-owner, ss == 0) inclusive values of the last tile
+#pragma unroll
+    for (int i = 0; i < CPT; ++i) run[i] = 0.0f;
 
     // (thread 0) fill ring slots up to (not including) slot `limit`; slot n goes to stage n % ST.
     // In look-back mode the next tile id is taken one fill ahead, so the atomic's
@@ -297,103 +349,128 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
         const bool seq_start = (q == 0 && s == 0);                  // holds t = 0 of its channel
 
         // ---- 2. compose this thread's K steps -----------------------------------
-        const E *ta = sm.a[st] + r0 * TD + c;
-        const E *tb = sm.b[st] + r0 * TD + c;
-        TileRegs<DT, K> r;
+        const E *ta = sm.a[st] + r0 * TD + CPT * c;
+        const E *tb = sm.b[st] + r0 * TD + CPT * c;
+        TileRegs<DT, K, CPT> r;
         r.load(ta, tb, TD);
         if (seq_start && !h_init) r.zero_a0();   // h_{-1} = 0: the first slope never matters
-        float A = 1.0f, Bv = 0.0f;
+        float A[CPT], Bv[CPT];
+#pragma unroll
+        for (int i = 0; i < CPT; ++i) { A[i] = 1.0f; Bv[i] = 0.0f; }
 #pragma unroll
         for (int j = 0; j < K; ++j) {
             if (j < nv) {
-                Bv = fmaf(r.a(j), Bv, r.b(j));
-                A = r.a(j) * A;
+#pragma unroll
+                for (int i = 0; i < CPT; ++i) {
+                    Bv[i] = fmaf(r.a(j, i), Bv[i], r.b(j, i));
+                    A[i] = r.a(j, i) * A[i];
+                }
             }
         }
-        float (&segA)[S][TD] = sm.segA[k & 1];
-        float (&segB)[S][TD] = sm.segB[k & 1];
+        float (&segA)[S][TD + 32 / S] = sm.segA[k & 1];
+        float (&segB)[S][TD + 32 / S] = sm.segB[k & 1];
         float (&carry_in)[TD] = sm.carry[k & 1];
-        segA[s][c] = A;
-        segB[s][c] = Bv;
+        st_group<CPT>(&segA[s][CPT * c], A);
+        st_group<CPT>(&segB[s][CPT * c], Bv);
         __syncthreads();
         // Every thread now holds this tile's a and b in registers: stage st is free,
         // so its next tile (slot k + ST) starts copying while this one is finished.
         if (tid == 0) refill(k + ST + 1);
 
         // ---- 3. shuffle scan over the S segment pairs of each channel -----------
-        float xA = segA[ss][cc], xB = segB[ss][cc];
+        float tA[CPT], tB[CPT];                 // the tile's aggregate of each channel
 #pragma unroll
-        for (int off = 1; off < S; off <<= 1) {
-            const float uA = __shfl_up_sync(kFull, xA, off, S);
-            const float uB = __shfl_up_sync(kFull, xB, off, S);
-            if (ss >= off) {                  // (later) o (earlier)
-                xB = fmaf(xA, uB, xB);
-                xA = xA * uA;
+        for (int i = 0; i < CPT; ++i) {
+            const int ch = cc + i * TC;
+            float xA = segA[ss][ch], xB = segB[ss][ch];
+#pragma unroll
+            for (int off = 1; off < S; off <<= 1) {
+                const float uA = __shfl_up_sync(kFull, xA, off, S);
+                const float uB = __shfl_up_sync(kFull, xB, off, S);
+                if (ss >= off) {              // (later) o (earlier)
+                    xB = fmaf(xA, uB, xB);
+                    xA = xA * uA;
+                }
             }
+            float eA = __shfl_up_sync(kFull, xA, 1, S);
+            float eB = __shfl_up_sync(kFull, xB, 1, S);
+            if (ss == 0) { eA = 1.0f; eB = 0.0f; }
+            segA[ss][ch] = eA;                // same slot this thread read: no other reader
+            segB[ss][ch] = eB;
+            tA[i] = __shfl_sync(kFull, xA, S - 1, S);
+            tB[i] = __shfl_sync(kFull, xB, S - 1, S);
         }
-        float eA = __shfl_up_sync(kFull, xA, 1, S);
-        float eB = __shfl_up_sync(kFull, xB, 1, S);
-        if (ss == 0) { eA = 1.0f; eB = 0.0f; }
-        segA[ss][cc] = eA;                    // same slot this thread read: no other reader
-        segB[ss][cc] = eB;
-        const float tA = __shfl_sync(kFull, xA, S - 1, S);   // the tile's aggregate
-        const float tB = __shfl_sync(kFull, xB, S - 1, S);
 
         // ---- 4. the carry entering the tile ---------------------------------------
-        // h before the first chunk: the carried-in state, or 0.
-        const float h_before = (h_init && d0 + cc < D) ? h_init[bi * D + d0 + cc] : 0.0f;
-        if (own) {
-            if (ss == 0) {
-                const float carry = (q == 0) ? h_before : run;
-                run = fmaf(tA, carry, tB);
-                carry_in[cc] = carry;
-            }
-        } else if (reduce) {
-            // the tile's map; the first chunk's absorbs the carried-in state, so the scan of
-            // these maps from 0 is the chain of inclusive values
-            if (ss == 0) {
-                tileA[id * TD + cc] = (q == 0) ? 0.0f : tA;
-                tileB[id * TD + cc] = (q == 0) ? fmaf(tA, h_before, tB) : tB;
-                // kept for the apply launch: h_last may be the same buffer as h_init, and the
-                // apply launch writes it while other tiles still need the starting state
-                if (q == 0) tileX[id * TD + cc] = h_before;
-            }
-        } else if (apply) {
-            if (ss == 0) carry_in[cc] = (q == 0) ? tileX[id * TD + cc] : tileH[(id - n_slices) * TD + cc];
-        } else {
-            const bool publish = (q + 1 < chunks) && (id != silent_tile);
-            float carry = h_before;
-            if (q > 0)
-                carry = lookback_carry<S, R>(id, n_slices, TD, cc, ss, gbase, tag, publish, tA, tB, h_before,
-                                             wAggA, wAggB, wInc, ctrl, status, spin_limit);
-            if (ss == 0) {
-                if (publish) st_relaxed_u64(&wInc[id * TD + cc], pack_word(tag, fmaf(tA, carry, tB)));
-                carry_in[cc] = carry;
+#pragma unroll
+        for (int i = 0; i < CPT; ++i) {
+            const int ch = cc + i * TC;
+            // h before the first chunk: the carried-in state, or 0.
+            const float h_before = (h_init && d0 + ch < D) ? h_init[bi * D + d0 + ch] : 0.0f;
+            if (own) {
+                if (ss == 0) {
+                    const float carry = (q == 0) ? h_before : run[i];
+                    run[i] = fmaf(tA[i], carry, tB[i]);
+                    carry_in[ch] = carry;
+                }
+            } else if (reduce) {
+                // the tile's map; the first chunk's absorbs the carried-in state, so the scan of
+                // these maps from 0 is the chain of inclusive values
+                if (ss == 0) {
+                    tileA[id * TD + ch] = (q == 0) ? 0.0f : tA[i];
+                    tileB[id * TD + ch] = (q == 0) ? fmaf(tA[i], h_before, tB[i]) : tB[i];
+                    // kept for the apply launch: h_last may be the same buffer as h_init, and the
+                    // apply launch writes it while other tiles still need the starting state
+                    if (q == 0) tileX[id * TD + ch] = h_before;
+                }
+            } else if (apply) {
+                if (ss == 0) carry_in[ch] = (q == 0) ? tileX[id * TD + ch] : tileH[(id - n_slices) * TD + ch];
+            } else {
+                const bool publish = (q + 1 < chunks) && (id != silent_tile);
+                float carry = h_before;
+                if (q > 0)
+                    carry = lookback_carry<S, R>(id, n_slices, TD, ch, ss, gbase, tag, publish, tA[i], tB[i],
+                                                 h_before, wAggA, wAggB, wInc, ctrl, status, spin_limit);
+                if (ss == 0) {
+                    if (publish) st_relaxed_u64(&wInc[id * TD + ch], pack_word(tag, fmaf(tA[i], carry, tB[i])));
+                    carry_in[ch] = carry;
+                }
             }
         }
         __syncthreads();
 
         // ---- 5. replay the steps from the carried value, store h -----------------
-        float hc = fmaf(segA[s][c], carry_in[c], segB[s][c]);
-        if (!reduce && (d0 + c) < D) {
-            E *hp = h + ((bi * L + t0 + r0) * D + d0 + c);
+        float hc[CPT], pA[CPT], pB[CPT];
+        ld_group<CPT>(&segA[s][CPT * c], pA);
+        ld_group<CPT>(&segB[s][CPT * c], pB);
+        ld_group<CPT>(&carry_in[CPT * c], hc);
+#pragma unroll
+        for (int i = 0; i < CPT; ++i) hc[i] = fmaf(pA[i], hc[i], pB[i]);
+        // (D is even when CPT = 2, so a group is inside D or wholly past it)
+        if (!reduce && (d0 + CPT * c) < D) {
+            E *hp = h + ((bi * L + t0 + r0) * D + d0 + CPT * c);
             if (nv == K) {
 #pragma unroll
                 for (int j = 0; j < K; ++j) {
-                    hc = fmaf(r.a(j), hc, r.b(j));
-                    hp[(long long)j * D] = Storage<DT>::put(hc);
+#pragma unroll
+                    for (int i = 0; i < CPT; ++i) hc[i] = fmaf(r.a(j, i), hc[i], r.b(j, i));
+                    st_h<DT, CPT>(hp + (long long)j * D, hc);
                 }
             } else {
 #pragma unroll
                 for (int j = 0; j < K; ++j) {
                     if (j < nv) {
-                        hc = fmaf(r.a(j), hc, r.b(j));
-                        hp[(long long)j * D] = Storage<DT>::put(hc);
+#pragma unroll
+                        for (int i = 0; i < CPT; ++i) hc[i] = fmaf(r.a(j, i), hc[i], r.b(j, i));
+                        st_h<DT, CPT>(hp + (long long)j * D, hc);
                     }
                 }
             }
             // the thread holding t = L-1 hands the state out
-            if (h_last && nv > 0 && t0 + r0 + nv == L) h_last[bi * D + d0 + c] = hc;
+            if (h_last && nv > 0 && t0 + r0 + nv == L) {
+#pragma unroll
+                for (int i = 0; i < CPT; ++i) h_last[bi * D + d0 + CPT * c + i] = hc[i];
+            }
         }
         // No barrier here.  Stage st was last read before this tile's first
         // barrier, after which thread 0 refilled it; its TileCoord was read into
@@ -427,10 +504,10 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
     }
 }
 
-template <int DT, int TD, int TT, int S, int ST>
+template <int DT, int TD, int TT, int S, int ST, int CPT>
 constexpr ChunkedVariant make_variant() {
-    return ChunkedVariant{TD, TT, S, ST, TD * S, sizeof(ChunkSmem<typename Storage<DT>::raw, TD, TT, S, ST>),
-                          (int)sizeof(typename Storage<DT>::raw)};
+    return ChunkedVariant{TD, TT, S, ST, TD / CPT * S, sizeof(ChunkSmem<typename Storage<DT>::raw, TD, TT, S, ST>),
+                          (int)sizeof(typename Storage<DT>::raw), CPT};
 }
 
 }  // namespace

@@ -72,9 +72,10 @@ cudaError_t launch_regcarry16(int dtype, int vec, int prefetch, int threads, con
 // shared memory by TMA.  `segments` threads share each channel's tile_t steps.
 struct ChunkedVariant {
     int tile_d, tile_t, segments, stages;
-    int threads;         // tile_d * segments
+    int threads;         // tile_d / cpt * segments
     size_t smem_bytes;   // dynamic shared memory per CTA
     int elem_bytes = 4;  // stored element size: 4 (fp32) or 2 (bfloat16 and binary16)
+    int cpt = 1;         // adjacent channels per thread: 1, or 2 (16-bit storage)
 };
 // The compiled variants (tile_d, tile_t, segments, stages combinations): fp32
 // storage, and 16-bit storage (each shape compiled for bfloat16 and binary16).

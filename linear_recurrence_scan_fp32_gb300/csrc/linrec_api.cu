@@ -99,11 +99,13 @@ const ChunkedVariant *variants_of(bool backward, int dtype, int *n) {
     return dtype == kDtypeF32 ? chunked_variants(n) : chunked_variants_16(n);
 }
 
-const ChunkedVariant *find_variant(int tile_d, int tile_t, int stages, int *index, bool backward, int dtype) {
+const ChunkedVariant *find_variant(int tile_d, int tile_t, int stages, int cpt, int segments, int *index,
+                                   bool backward, int dtype) {
     int n = 0;
     const ChunkedVariant *v = variants_of(backward, dtype, &n);
     for (int i = 0; i < n; ++i) {
-        if (v[i].tile_d == tile_d && v[i].tile_t == tile_t && (stages == 0 || v[i].stages == stages)) {
+        if (v[i].tile_d == tile_d && v[i].tile_t == tile_t && (stages == 0 || v[i].stages == stages) &&
+            (cpt == 0 || v[i].cpt == cpt) && (segments == 0 || v[i].segments == segments)) {
             if (index) *index = i;
             return &v[i];
         }
@@ -122,6 +124,32 @@ const ChunkedVariant *find_variant(int tile_d, int tile_t, int stages, int *inde
 // tiles: 4885 vs 3621 GB/s on (32, 4096, 256), 6269 vs 4343 on (64, 2048, 1024).
 // Sequences shorter than 256 steps take 64-step tiles with a 6-deep ring.
 int tile_t_16(int64_t L) { return L >= 256 ? 256 : 64; }
+
+// 16-bit storage, the {32, 256, 2} tile: how many adjacent channels a thread owns
+// and how many segments share a channel's 256 steps.  Two channels per thread take
+// one 32-bit shared-memory load and one packed store per step for both.  Measured
+// on GB300 (bfloat16, us per call, one / two channels per thread):
+//  - slice-owner, sm_count < slices <= 3 * sm_count: 128 threads (2 channels,
+//    8 segments), three CTAs per SM, one wave: (32, 4096, 256) 38.4 -> 36.6,
+//    (57, 4096, 256) 71.8 -> 60.0, (8, 8192, 1024) 72.2 -> 68.7;
+//  - slice-owner otherwise: 256 threads (2 channels, 16 segments), no slower at any
+//    shape and 1-3 % faster at most: (64, 2048, 1024) 124.7 -> 122.7; the 128-thread
+//    CTAs leave a slow tail there ((76, 4096, 256) 73.7 -> 83.7);
+//  - two-pass: 128 threads, (1, 1048576, 64) 126.2 -> 116.2;
+//  - look-back: one channel per thread (35.0 against 36.7 on (4, 16384, 256)).
+void default_groups_16(int64_t slices, int sm_count, bool own, bool twopass, int *cpt, int *segments) {
+    if (own) {
+        const bool one_wave = slices > sm_count && slices <= 3 * (int64_t)sm_count;
+        *cpt = 2;
+        *segments = one_wave ? 8 : 16;
+    } else if (twopass) {
+        *cpt = 2;
+        *segments = 8;
+    } else {
+        *cpt = 1;
+        *segments = 8;
+    }
+}
 
 void default_tile(int64_t B, int64_t L, int64_t D, int sm_count, bool own, bool twopass, bool backward, int dtype,
                   int *tile_d, int *tile_t, int *stages) {
@@ -236,11 +264,18 @@ linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int ali
         if (tile_t == 0) tile_t = dt;
         if (stages == 0) stages = ds;
     }
-    const ChunkedVariant *v = find_variant(tile_d, tile_t, stages, variant_index, backward, dtype);
-    if (!v && opt->stages == 0) v = find_variant(tile_d, tile_t, 0, variant_index, backward, dtype);
+    // vec on the chunked path: channels per thread (0 = the first variant of the tile)
+    int cpt = opt->vec;
+    int segs = opt->segments;
+    if (cpt == 0 && segs == 0 && dtype != kDtypeF32 && !backward && tile_d == 32 && tile_t == 256 &&
+        (stages == 0 || stages == 2))
+        default_groups_16(B * ((D + 31) / 32), sm_count, own, twopass, &cpt, &segs);
+    const ChunkedVariant *v = find_variant(tile_d, tile_t, stages, cpt, segs, variant_index, backward, dtype);
+    if (!v && opt->stages == 0) v = find_variant(tile_d, tile_t, 0, cpt, segs, variant_index, backward, dtype);
     if (!v) return LINREC_ERR_INVALID_VALUE;
     plan->lookback = (own || twopass) ? 0 : 1;
     plan->twopass = twopass ? 1 : 0;
+    plan->vec = v->cpt;
     plan->tile_d = v->tile_d;
     plan->tile_t = v->tile_t;
     plan->segments = v->segments;

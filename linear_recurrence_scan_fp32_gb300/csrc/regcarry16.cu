@@ -26,33 +26,6 @@ __device__ __forceinline__ typename Word<V>::type ld_word(const typename Word<V>
 template <int V>
 __device__ __forceinline__ void st_word(typename Word<V>::type *p, typename Word<V>::type w) { __stcs(p, w); }
 
-// Two 16-bit elements in one 32-bit word (the one at the lower address in the low
-// half) widened exactly to fp32, and two fp32 values rounded once, to nearest with
-// ties to even, into one word: one instruction per pair where the format allows.
-template <int DT> __device__ __forceinline__ float2 widen2(uint32_t w);
-template <> __device__ __forceinline__ float2 widen2<kDtypeBF16>(uint32_t w) {
-    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-}
-template <> __device__ __forceinline__ float2 widen2<kDtypeF16>(uint32_t w) {
-    __half2 h2;
-    static_assert(sizeof(h2) == sizeof(w), "half2 is one word");
-    memcpy(&h2, &w, sizeof(w));
-    return __half22float2(h2);
-}
-template <int DT> __device__ __forceinline__ uint32_t narrow2(float x, float y);
-template <> __device__ __forceinline__ uint32_t narrow2<kDtypeBF16>(float x, float y) {
-    const __nv_bfloat162 v = __floats2bfloat162_rn(x, y);   // x in the low half
-    uint32_t w;
-    memcpy(&w, &v, sizeof(w));
-    return w;
-}
-template <> __device__ __forceinline__ uint32_t narrow2<kDtypeF16>(float x, float y) {
-    const __half2 v = __floats2half2_rn(x, y);               // x in the low half
-    uint32_t w;
-    memcpy(&w, &v, sizeof(w));
-    return w;
-}
-
 // A thread's V elements of one step: widened, and h rounded back.
 template <int DT, int V>
 __device__ __forceinline__ void widen(const typename Word<V>::type &w, float (&x)[V]) {
@@ -63,7 +36,7 @@ __device__ __forceinline__ void widen(const typename Word<V>::type &w, float (&x
         memcpy(u, &w, sizeof(u));
 #pragma unroll
         for (int i = 0; i < V / 2; ++i) {
-            const float2 f = widen2<DT>(u[i]);
+            const float2 f = Storage<DT>::get2(u[i]);
             x[2 * i] = f.x;
             x[2 * i + 1] = f.y;
         }
@@ -77,7 +50,7 @@ __device__ __forceinline__ typename Word<V>::type narrow(const float (&x)[V]) {
     } else {
         uint32_t u[V / 2];
 #pragma unroll
-        for (int i = 0; i < V / 2; ++i) u[i] = narrow2<DT>(x[2 * i], x[2 * i + 1]);
+        for (int i = 0; i < V / 2; ++i) u[i] = Storage<DT>::put2(x[2 * i], x[2 * i + 1]);
         memcpy(&w, u, sizeof(u));
     }
     return w;

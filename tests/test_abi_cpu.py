@@ -211,6 +211,26 @@ def test_plan_16bit_storage():
     p = lr.linrec_plan_16(32, 4096, 256, sm_count=152)
     assert p["path_name"] == "chunked" and p["lookback"] == 0
     assert (p["tile_d"], p["tile_t"], p["stages"]) == (32, 256, 2)
+    # channels per thread and segments of the 256-step tile: two channels per thread; 8 segments
+    # (128 threads) when the slices fill one wave of three CTAs per SM, and in two-pass mode
+    assert (p["vec"], p["segments"], p["threads"]) == (2, 8, 128)                       # 256 slices
+    p = lr.linrec_plan_16(19, 4096, 256, sm_count=152)                                   # 152 slices
+    assert (p["lookback"], p["vec"], p["segments"], p["threads"]) == (0, 2, 16, 256)
+    p = lr.linrec_plan_16(57, 4096, 256, sm_count=152)                                   # 456 slices
+    assert (p["vec"], p["segments"]) == (2, 8)
+    p = lr.linrec_plan_16(64, 2048, 1024, sm_count=152)                                  # 2048 slices
+    assert (p["vec"], p["segments"], p["threads"]) == (2, 16, 256)
+    p = lr.linrec_plan_16(1, 1 << 20, 64, sm_count=152)
+    assert (p["twopass"], p["vec"], p["segments"]) == (1, 2, 8)
+    p = lr.linrec_plan_16(4, 8192, 256, sm_count=152)                                    # look-back
+    assert (p["lookback"], p["vec"], p["segments"]) == (1, 1, 8)
+    # an explicit choice is kept, and other tiles keep their first variant
+    p = lr.linrec_plan_16(32, 4096, 256, sm_count=152, vec=1)
+    assert (p["vec"], p["segments"]) == (1, 8)
+    p = lr.linrec_plan_16(32, 4096, 256, sm_count=152, segments=16)
+    assert (p["vec"], p["segments"]) == (2, 16)
+    p = lr.linrec_plan_16(32, 4096, 256, sm_count=152, tile_d=32, tile_t=256, stages=3)
+    assert (p["vec"], p["segments"]) == (1, 8)
     p = lr.linrec_plan_16(256, 128, 4096, sm_count=152, path="chunked")
     assert (p["tile_d"], p["tile_t"], p["stages"], p["lookback"]) == (32, 64, 6, 0)
     # few long slices: two-pass, whose aggregates are fp32 whatever the storage
@@ -235,7 +255,24 @@ def test_plan_16bit_storage():
     # every variant the 16-bit table reports by default exists and is shaped like the fp32 ones
     for mode in ("own", "lookback", "twopass"):
         p = lr.linrec_plan_16(4, 5000, 128, path="chunked", chunk_mode=mode)
-        assert p["threads"] == p["tile_d"] * p["segments"] and p["tile_t"] % p["segments"] == 0
+        assert p["threads"] == p["tile_d"] // p["vec"] * p["segments"] and p["tile_t"] % p["segments"] == 0
+
+
+def test_plan_chunked_channels_per_thread():
+    # vec on the chunked path: adjacent channels per thread; segments picks among variants of a tile
+    p = lr.linrec_plan_16(32, 4096, 256, path="chunked", tile_d=32, tile_t=256, stages=2, vec=2, segments=8)
+    assert (p["vec"], p["segments"], p["threads"]) == (2, 8, 128)
+    p = lr.linrec_plan_16(32, 4096, 256, path="chunked", tile_d=32, tile_t=256, stages=2, vec=2, segments=16)
+    assert (p["vec"], p["segments"], p["threads"]) == (2, 16, 256)
+    p = lr.linrec_plan_16(32, 4096, 256, path="chunked", tile_d=32, tile_t=256, stages=2, vec=1)
+    assert (p["vec"], p["segments"], p["threads"]) == (1, 8, 256)
+    assert lr.linrec_plan_f32(32, 4096, 256, path="chunked")["vec"] == 1
+    with pytest.raises(lr.LinrecError):
+        lr.linrec_plan_f32(32, 4096, 256, path="chunked", vec=2)          # fp32 keeps one channel per thread
+    with pytest.raises(lr.LinrecError):
+        lr.linrec_plan_16(32, 4096, 256, path="chunked", tile_d=32, tile_t=256, vec=2, segments=4)
+    with pytest.raises(lr.LinrecError):
+        lr.linrec_plan_f32_backward(32, 4096, 256, path="chunked", vec=2)
 
 
 def test_16bit_argument_checks_count_two_bytes(L):

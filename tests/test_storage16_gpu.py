@@ -161,26 +161,51 @@ def test_misaligned_pointers_take_the_register_path(kind):
             SCAN[kind](a_v, b_v, path="chunked")
 
 
-CHUNKED16 = [(32, 128, 3), (32, 128, 4), (32, 128, 6), (64, 128, 2), (64, 128, 3), (64, 64, 4), (32, 64, 6),
-             (128, 64, 3), (32, 256, 2), (32, 256, 3)]
+# (tile_d, tile_t, stages, channels per thread, segments)
+CHUNKED16 = [(32, 128, 3, 1, 8), (32, 128, 4, 1, 8), (32, 128, 6, 1, 8), (64, 128, 2, 1, 8), (64, 128, 3, 1, 8),
+             (64, 64, 4, 1, 4), (32, 64, 6, 1, 4), (128, 64, 3, 1, 4), (32, 256, 2, 1, 8), (32, 256, 3, 1, 8),
+             (32, 256, 2, 2, 16), (32, 256, 2, 2, 8), (32, 64, 6, 2, 8)]
 
 
 @pytest.mark.parametrize("kind", KINDS)
-@pytest.mark.parametrize("tile", CHUNKED16, ids=lambda t: f"d{t[0]}t{t[1]}s{t[2]}")
+@pytest.mark.parametrize("tile", CHUNKED16, ids=lambda t: f"d{t[0]}t{t[1]}s{t[2]}c{t[3]}g{t[4]}")
 def test_every_chunked_variant_and_mode(kind, tile):
-    td, tt, st = tile
+    td, tt, st, cpt, segs = tile
     B, L, D = 2, 3001, 200
     a16, b16 = draw16(kind, B, L, D, 84)
     h64, _ = oracle.f64_16(kind, a16, b16)
     a_d, b_d = a16.to(DEV), b16.to(DEV)
+    var = dict(path="chunked", tile_d=td, tile_t=tt, stages=st, vec=cpt, segments=segs)
+    assert lr.linrec_plan_16(B, L, D, **var)["threads"] == td // cpt * segs
     got = {}
     for mode in ("own", "lookback", "twopass"):
-        h = run(kind, a_d, b_d, path="chunked", tile_d=td, tile_t=tt, stages=st, chunk_mode=mode)
+        h = run(kind, a_d, b_d, chunk_mode=mode, **var)
         assert_close16(kind, h, h64, f"{kind} {tile} {mode}")
         got[mode] = h
     assert torch.equal(got["own"], got["lookback"]), "slice-owner and look-back modes differ"
-    again = run(kind, a_d, b_d, path="chunked", tile_d=td, tile_t=tt, stages=st, chunk_mode="lookback")
+    again = run(kind, a_d, b_d, chunk_mode="lookback", **var)
     assert torch.equal(again, got["lookback"]), "not deterministic"
+    assert lr.linrec_stream_status() == lr.LINREC_OK
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("shape", [(2, 3001, 200), (3, 1000, 264), (1, 257, 8)], ids=lambda s: "x".join(map(str, s)))
+def test_two_channels_per_thread_same_bits(kind, shape):
+    """One or two channels per thread, same tile and segments: the same fma sequence, the same words."""
+    B, L, D = shape
+    a16, b16 = draw16(kind, B, L, D, 87 + L, a_dist="u[0.5,1)")
+    a_d, b_d = a16.to(DEV), b16.to(DEV)
+    g = torch.Generator().manual_seed(88)
+    h0 = torch.randn((B, D), generator=g).to(DEV)
+    for mode in ("own", "lookback", "twopass"):
+        outs = []
+        for cpt in (1, 2):
+            last = torch.full((B, D), float("nan"), device=DEV)
+            h = run(kind, a_d, b_d, path="chunked", tile_d=32, tile_t=256, stages=2, segments=8, vec=cpt,
+                    chunk_mode=mode, h_init=h0, h_last=last)
+            outs.append((h, last))
+        assert torch.equal(outs[0][0], outs[1][0]), f"{kind} {shape} {mode}: h differs"
+        assert torch.equal(outs[0][1], outs[1][1]), f"{kind} {shape} {mode}: h_last differs"
     assert lr.linrec_stream_status() == lr.LINREC_OK
 
 
