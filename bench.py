@@ -367,7 +367,8 @@ def run_ours(args):
         plan_fn = lr.linrec_plan_f32 if args.dtype == "f32" else lr.linrec_plan_16
         plan = plan_fn(w.B, w.L, w.D, sm_count=sms, **opt)
         if plan["path_name"] == "chunked":
-            mode = "_twopass" if plan["twopass"] else "_lookback" if plan["lookback"] else ""
+            mode = ("_twopass" if plan["twopass"] else "_blocks" if plan.get("blocks") else
+                    "_lookback" if plan["lookback"] else "")
             kernel_tag = "chunked" + store + mode
         else:
             kernel_tag = "regcarry" + store
@@ -530,7 +531,7 @@ def run_ours(args):
                               "no flush") if nbytes > 129e6 else "working set fits L2: small case",
                        "path": plan["path_name"],
                        "plan": {k: plan[k] for k in ("vec", "prefetch", "tile_t", "tile_d", "segments", "stages",
-                                                     "lookback", "twopass", "threads", "grid")}},
+                                                     "lookback", "twopass", "blocks", "threads", "grid")}},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic,
                          "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
@@ -562,7 +563,7 @@ def main(argv=None):
     p.add_argument("--path", choices=("auto", "regcarry", "chunked"), default="auto")
     p.add_argument("--workload", default=WORKLOAD,
                    help="named workload (tiny, pages, long, gated, short, ...); pages is the headline")
-    p.add_argument("--chunk-mode", choices=("auto", "own", "lookback", "twopass"), default="auto")
+    p.add_argument("--chunk-mode", choices=("auto", "own", "lookback", "twopass", "blocks"), default="auto")
     p.add_argument("--dtype", choices=("f32", "bf16", "f16"), default="f32",
                    help="storage of a, b and h (arithmetic is fp32 for all three)")
     p.add_argument("--layout", choices=("bld", "bdl"), default="bld",

@@ -90,7 +90,10 @@ typedef struct {
                             chunk to chunk itself; 2 = chunks of a slice spread over CTAs, joined
                             by the decoupled look-back; 3 = two passes: a launch writes every
                             chunk's aggregate, the aggregates are scanned, a launch applies them
-                            (the gradient runs them in reversed chunk order); 0 = the
+                            (the gradient runs them in reversed chunk order); 4 = blocks (forward
+                            only): one launch; a CTA composes a block of `group` consecutive
+                            chunks of a slice, joins the blocks of the slice by the decoupled
+                            look-back, then re-reads the block (from L2) and writes h; 0 = the
                             dispatcher's choice */
     unsigned int *d_status; /* device word (may be NULL): the kernel ORs 1 << linrec_status_t
                                into it on a device-side failure; otherwise the stream's own word
@@ -105,6 +108,8 @@ typedef struct {
     int segments;        /* chunked: segments a tile's time steps are split into, one thread
                             each per channel group (0 = the dispatcher's choice for its default
                             16-bit tile, else the first compiled variant of the tile) */
+    int group;           /* chunk_mode 4: chunks per block (0 = 1024 time steps' worth); any
+                            other chunk_mode takes 0 only */
 } linrec_options_t;
 
 /*
@@ -209,6 +214,7 @@ typedef struct {
     int64_t chunks;        /* chunked: time chunks per channel slice */
     size_t smem_bytes;     /* dynamic shared memory per CTA */
     size_t workspace_bytes;/* chunked: control block + look-back words for this call */
+    int blocks;            /* chunked: blocks mode, chunks per block (0 = another mode) */
 } linrec_plan_t;
 
 /*

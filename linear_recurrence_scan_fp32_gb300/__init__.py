@@ -72,6 +72,7 @@ class Options(ctypes.Structure):
         ("test_silent_tile", ctypes.c_int64),
         ("rows_per_warp", ctypes.c_int),
         ("segments", ctypes.c_int),
+        ("group", ctypes.c_int),
     ]
 
 
@@ -92,6 +93,7 @@ class Plan(ctypes.Structure):
         ("chunks", ctypes.c_int64),
         ("smem_bytes", ctypes.c_size_t),
         ("workspace_bytes", ctypes.c_size_t),
+        ("blocks", ctypes.c_int),
     ]
 
 
@@ -163,7 +165,7 @@ def _check(code: int, what: str):
         raise LinrecError(code, f"{what}: {linrec_status_string(code)}")
 
 
-CHUNK_MODES = {"auto": 0, "own": 1, "lookback": 2, "twopass": 3}
+CHUNK_MODES = {"auto": 0, "own": 1, "lookback": 2, "twopass": 3, "blocks": 4}
 
 
 def _addr(x):
@@ -174,7 +176,7 @@ def _addr(x):
 
 def make_options(path="auto", vec=0, prefetch=0, tile_t=0, tile_d=0, stages=0, ctas_per_sm=0,
                  chunk_mode="auto", d_status=None, h_init=None, h_last=None, spin_limit=0,
-                 test_silent_tile=0, rows_per_warp=0, segments=0) -> Options:
+                 test_silent_tile=0, rows_per_warp=0, segments=0, group=0) -> Options:
     o = Options()
     o.path = PATHS[path] if isinstance(path, str) else int(path)
     o.vec, o.prefetch, o.tile_t, o.tile_d, o.stages = int(vec), int(prefetch), int(tile_t), int(tile_d), int(stages)
@@ -187,6 +189,7 @@ def make_options(path="auto", vec=0, prefetch=0, tile_t=0, tile_d=0, stages=0, c
     o.test_silent_tile = int(test_silent_tile)
     o.rows_per_warp = int(rows_per_warp)
     o.segments = int(segments)
+    o.group = int(group)
     return o
 
 

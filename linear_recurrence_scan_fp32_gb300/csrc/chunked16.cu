@@ -22,10 +22,16 @@ namespace {
     X(32, 256, 16, 2, 2)             \
     X(32, 256, 8, 2, 2)              \
     X(32, 64, 8, 6, 2)
+// compiled again for blocks mode
+#define LINREC_CHUNKED16_BLOCK_VARIANTS(X) \
+    X(32, 256, 8, 2, 2)
 
 #define LINREC_V_ENTRY(TD, TT, S, ST, CPT) make_variant<kDtypeBF16, TD, TT, S, ST, CPT>(),
-const ChunkedVariant kVariants16[] = {LINREC_CHUNKED16_VARIANTS(LINREC_V_ENTRY)};
+#define LINREC_VB_ENTRY(TD, TT, S, ST, CPT) make_variant<kDtypeBF16, TD, TT, S, ST, CPT, true>(),
+const ChunkedVariant kVariants16[] = {LINREC_CHUNKED16_VARIANTS(LINREC_V_ENTRY)
+                                          LINREC_CHUNKED16_BLOCK_VARIANTS(LINREC_VB_ENTRY)};
 #undef LINREC_V_ENTRY
+#undef LINREC_VB_ENTRY
 
 // both 16-bit kinds share each variant's shared-memory layout
 #define LINREC_SAME_SIZE(TD, TT, S, ST, CPT)                                                     \
@@ -43,15 +49,21 @@ const ChunkedVariant *chunked_variants_16(int *count) {
 
 const void *chunked16_kernel(const ChunkedVariant *v, int dtype) {
     if (v->elem_bytes != 2) return nullptr;
-#define LINREC_K_ENTRY(TD, TT, S, ST, CPT)                                                           \
-    if (v->tile_d == TD && v->tile_t == TT && v->segments == S && v->stages == ST && v->cpt == CPT) {   \
-        if (dtype == kDtypeBF16)                                                                      \
-            return reinterpret_cast<const void *>(&chunked_scan_kernel<kDtypeBF16, TD, TT, S, ST, CPT>); \
-        if (dtype == kDtypeF16)                                                                       \
-            return reinterpret_cast<const void *>(&chunked_scan_kernel<kDtypeF16, TD, TT, S, ST, CPT>);  \
-        return nullptr;                                                                               \
+#define LINREC_K_ENTRY(TD, TT, S, ST, CPT, BM)                                                          \
+    if (v->tile_d == TD && v->tile_t == TT && v->segments == S && v->stages == ST && v->cpt == CPT &&     \
+        (v->blocks != 0) == BM) {                                                                        \
+        if (dtype == kDtypeBF16)                                                                         \
+            return reinterpret_cast<const void *>(&chunked_scan_kernel<kDtypeBF16, TD, TT, S, ST, CPT, BM>); \
+        if (dtype == kDtypeF16)                                                                          \
+            return reinterpret_cast<const void *>(&chunked_scan_kernel<kDtypeF16, TD, TT, S, ST, CPT, BM>);  \
+        return nullptr;                                                                                  \
     }
-    LINREC_CHUNKED16_VARIANTS(LINREC_K_ENTRY)
+#define LINREC_K_PLAIN(TD, TT, S, ST, CPT) LINREC_K_ENTRY(TD, TT, S, ST, CPT, false)
+#define LINREC_K_BLOCKS(TD, TT, S, ST, CPT) LINREC_K_ENTRY(TD, TT, S, ST, CPT, true)
+    LINREC_CHUNKED16_VARIANTS(LINREC_K_PLAIN)
+    LINREC_CHUNKED16_BLOCK_VARIANTS(LINREC_K_BLOCKS)
+#undef LINREC_K_PLAIN
+#undef LINREC_K_BLOCKS
 #undef LINREC_K_ENTRY
     return nullptr;
 }

@@ -42,6 +42,15 @@
 //         Tiles are independent in both launches; the apply launch visits
 //         them in reverse order so the inputs the reduce launch read last
 //         are still in L2.
+//       blocks mode (few slices, long L; one launch, a separate instantiation,
+//         BM = true): a block is G consecutive tiles of a slice, taken in order
+//         from a counter.  The CTA composes the block's tiles into one map
+//         (reduce pass, nothing stored), gets the h entering the block by the
+//         same decoupled look-back over block maps, then takes the same G
+//         tiles again (apply pass: re-read, mostly from L2) and finishes them
+//         as slice-owner mode does.  HBM traffic lies between the 12 bytes
+//         (fp32) per element of one pass and the 20 of two-pass, by how much
+//         of the re-read L2 still holds.
 //  5. Every thread replays its K steps from h_in = A_prefix * carry + B_prefix
 //     and stores h.
 //
@@ -68,8 +77,9 @@ struct TileCoord {
     int q;                              // time chunk
     int bi;                             // batch index
     int d0;                             // first channel
-    int pad;
+    int flags;                          // blocks mode: kApplyPass | kFirstOfPass | kLastOfPass
 };
+constexpr int kApplyPass = 1, kFirstOfPass = 2, kLastOfPass = 4;
 
 // A thread's K steps of a and b for its CPT adjacent channels, held in registers
 // from the compose to the replay; a(j, i) and b(j, i) are step j of channel i.
@@ -172,7 +182,7 @@ struct __align__(128) ChunkSmem {
     uint32_t tag;                       // look-back tag of this launch
 };
 
-template <int DT, int TD, int TT, int S, int ST, int CPT>
+template <int DT, int TD, int TT, int S, int ST, int CPT, bool BM = false>
 __global__ void __launch_bounds__(TD / CPT * S, (TD / CPT * S >= 512) ? 1 : 2)
 chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
                     const __grid_constant__ CUtensorMap map_b,
@@ -180,7 +190,9 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
                     const long long L, const long long D,
                     const long long slices_per_batch, const long long n_slices,
                     const long long chunks, const long long n_tiles,
-                    const int mode,              // kModeLookback, kModeOwn, kModeReduce or kModeApply
+                    const int mode,              // kModeLookback, kModeOwn, kModeReduce, kModeApply;
+                                                 // kModeBlocks (BM instantiations only)
+                    const int group,             // blocks mode: tiles per block (G)
                     Control *__restrict__ ctrl, unsigned long long *__restrict__ words,
                     unsigned int *__restrict__ status,
                     const long long spin_limit, const long long silent_tile,
@@ -194,6 +206,11 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
     const bool lookback = mode == kModeLookback;
     const bool reduce = mode == kModeReduce;
     const bool apply = mode == kModeApply;
+    const bool blocks = BM && mode == kModeBlocks;
+    const bool chained = lookback || blocks;  // tiles or blocks joined by the look-back words
+    // blocks mode: blocks per slice, and all blocks (block id = block index * n_slices + slice)
+    const long long bps = BM ? (chunks + group - 1) / group : 0;
+    const long long n_blocks = bps * n_slices;
     // two-pass mode: per-tile aggregates and the scanned inclusive values, indexed [tile id][channel],
     // and each channel's starting state, indexed [slice][channel]
     float *const tileA = reinterpret_cast<float *>(words);
@@ -217,15 +234,17 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
     const int ss = tid % S;                   // group), and the segment / look-back window lane
     const int gbase = (tid & 31) & ~(S - 1);  // first lane of this channel's group in the warp
 
+    // look-back words, [unit][channel]: units are tiles, or blocks in blocks mode
+    const long long n_units = blocks ? n_blocks : n_tiles;
     unsigned long long *const wAggA = words;
-    unsigned long long *const wAggB = words + n_tiles * TD;
-    unsigned long long *const wInc = words + 2 * n_tiles * TD;
+    unsigned long long *const wAggB = words + n_units * TD;
+    unsigned long long *const wInc = words + 2 * n_units * TD;
 
     // (thread 0) record stage st's tile and start its two box copies.
-    auto issue = [&](int st, long long id, long long q, long long slice) {
+    auto issue = [&](int st, long long id, long long q, long long slice, int flags) {
         const long long bi = slice / slices_per_batch;
         const int d0 = (int)((slice - bi * slices_per_batch) * TD);
-        sm.tile[st] = TileCoord{id, (int)q, (int)bi, d0, 0};
+        sm.tile[st] = TileCoord{id, (int)q, (int)bi, d0, flags};
         mbar_arrive_expect_tx(&sm.full[st], kStageBytes);
         tma_load_3d(sm.a[st], &map_a, &sm.full[st], d0, (int)(q * TT), (int)bi);
         tma_load_3d(sm.b[st], &map_b, &sm.full[st], d0, (int)(q * TT), (int)bi);
@@ -235,7 +254,35 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
     // blockIdx.x + gridDim.x, ... each walked from chunk 0 to chunks-1, tracked
     // in (own_slice, own_q).  Look-back mode: the next id from the tile counter.
     long long own_slice = blockIdx.x, own_q = 0, own_m = 0;
-    auto next_tile = [&](long long &q, long long &slice) -> long long {
+    // (thread 0, blocks mode) the block being walked, its pass, the next tile of the pass, its tiles
+    long long bm_blk = -1;
+    int bm_pass = 0, bm_g = 0, bm_cnt = 0;
+    auto next_tile = [&](long long &q, long long &slice, int &flags) -> long long {
+        flags = 0;
+        if constexpr (BM) {
+            if (blocks) {
+                // a block's G tiles twice (reduce pass, then apply pass), then the next block
+                if (bm_blk < 0 || (bm_pass == 1 && bm_g == bm_cnt)) {
+                    const long long b = (long long)atomicAdd(&ctrl->tile_counter, 1ull);
+                    if (b >= n_blocks) return n_tiles;
+                    bm_blk = b;
+                    bm_pass = 0;
+                    bm_g = 0;
+                    const long long left = chunks - (b / n_slices) * group;
+                    bm_cnt = left < group ? (int)left : group;
+                } else if (bm_g == bm_cnt) {
+                    bm_pass = 1;
+                    bm_g = 0;
+                }
+                const long long bq = bm_blk / n_slices;
+                slice = bm_blk - bq * n_slices;
+                q = bq * group + bm_g;
+                flags = (bm_pass ? kApplyPass : 0) | (bm_g == 0 ? kFirstOfPass : 0) |
+                        (bm_g == bm_cnt - 1 ? kLastOfPass : 0);
+                ++bm_g;
+                return q * n_slices + slice;
+            }
+        }
         if (reduce || apply) {                // independent tiles, static round-robin
             const long long k = blockIdx.x + (own_m++) * (long long)gridDim.x;
             if (k >= n_tiles) return n_tiles;
@@ -265,13 +312,13 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
         long long first = n_tiles;
         if (misaligned) {
             atomicOr(status, kStatusTmaTimeout);
-            if (lookback) atomicExch(&ctrl->abort, 1u);
+            if (chained) atomicExch(&ctrl->abort, 1u);
         } else {
             for (int st = 0; st < ST; ++st) mbar_init(&sm.full[st], 1);
             mbar_fence_init();
             tmap_prefetch(&map_a);
             tmap_prefetch(&map_b);
-            if (lookback) {
+            if (chained) {
                 const uint32_t tag = ld_relaxed_u32(&ctrl->epoch) + 1u;
                 sm.tag = tag == 0 ? 1u : tag;
             }
@@ -279,22 +326,24 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
             // CTAs start on them, so a tile's predecessors are never parked in another
             // CTA's ring behind later work.
             long long q = 0, slice = 0;
-            first = next_tile(q, slice);
-            if (first < n_tiles) issue(0, first, q, slice);
+            int flags = 0;
+            first = next_tile(q, slice, flags);
+            if (first < n_tiles) issue(0, first, q, slice, flags);
         }
         if (first >= n_tiles) finish(0);
     }
     __syncthreads();
 
-    const uint32_t tag = lookback ? sm.tag : 0u;
+    const uint32_t tag = chained ? sm.tag : 0u;
     uint32_t phases = 0;                      // bit st: parity of the next completion of stage st
     long long next_fill = 1;                  // (thread 0) next ring slot to fill
     bool ended = sm.tile[0].id >= n_tiles;    // (thread 0) no more tiles to take
     long long ahead = -1, ahead_q = 0, ahead_slice = 0;   // (thread 0, look-back) tile taken early
     uint32_t abort_seen = 0;                  // (thread 0, look-back) abort word, read one iteration early
     float run[CPT];                           // (slice-owner, ss == 0) inclusive values of the last tile
+    float bA[CPT], bB[CPT];                   // (blocks mode, reduce pass) the block's map so far
 #pragma unroll
-    for (int i = 0; i < CPT; ++i) run[i] = 0.0f;
+    for (int i = 0; i < CPT; ++i) { run[i] = 0.0f; bA[i] = 1.0f; bB[i] = 0.0f; }
 
     // (thread 0) fill ring slots up to (not including) slot `limit`; slot n goes to stage n % ST.
     // In look-back mode the next tile id is taken one fill ahead, so the atomic's
@@ -307,20 +356,22 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
         while (!ended && next_fill < limit) {
             const int s2 = (int)(next_fill % ST);
             long long nq = ahead_q, nslice = ahead_slice;
-            const long long nid = ahead >= 0 ? ahead : next_tile(nq, nslice);
+            int nflags = 0;
+            const long long nid = ahead >= 0 ? ahead : next_tile(nq, nslice, nflags);
             ahead = -1;
             if (nid >= n_tiles) {
                 ended = true;
                 finish(s2);
             } else {
-                issue(s2, nid, nq, nslice);
+                issue(s2, nid, nq, nslice, nflags);
             }
             ++next_fill;
         }
         if (lookback) {
-            if (!ended && ahead < 0) ahead = next_tile(ahead_q, ahead_slice);
-            abort_seen = ld_relaxed_u32(&ctrl->abort);
+            int unused = 0;
+            if (!ended && ahead < 0) ahead = next_tile(ahead_q, ahead_slice, unused);
         }
+        if (chained) abort_seen = ld_relaxed_u32(&ctrl->abort);
     };
 
     for (long long k = 0;; ++k) {
@@ -337,7 +388,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
 
         if (!mbar_wait_bounded(&sm.full[st], (phases >> st) & 1u, kTmaPolls)) {
             atomicOr(status, kStatusTmaTimeout);
-            if (lookback) atomicExch(&ctrl->abort, 1u);
+            if (chained) atomicExch(&ctrl->abort, 1u);
         }
         phases ^= 1u << st;
 
@@ -425,6 +476,39 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
                 }
             } else if (apply) {
                 if (ss == 0) carry_in[ch] = (q == 0) ? tileX[id * TD + ch] : tileH[(id - n_slices) * TD + ch];
+            } else if (blocks) {
+                if (tc.flags & kApplyPass) {
+                    // as slice-owner mode, from the h entering the block (left in run by the reduce pass)
+                    if (ss == 0) {
+                        const float carry = run[i];
+                        run[i] = fmaf(tA[i], carry, tB[i]);
+                        carry_in[ch] = carry;
+                    }
+                } else {
+                    // the block's map, later tile on the left; every lane of the group holds it
+                    if (tc.flags & kFirstOfPass) {
+                        bA[i] = tA[i];
+                        bB[i] = tB[i];
+                    } else {
+                        bB[i] = fmaf(tA[i], bB[i], tB[i]);
+                        bA[i] = tA[i] * bA[i];
+                    }
+                    if (tc.flags & kLastOfPass) {   // uniform over the CTA: the look-back's ballots
+                        const long long bq = q / group;
+                        const long long bid = bq * n_slices + bi * slices_per_batch + d0 / TD;
+                        const bool publish = (bq + 1 < bps) && (bid != silent_tile);
+                        float carry = h_before;
+                        if (bq > 0)
+                            carry = lookback_carry<S, R>(bid, n_slices, TD, ch, ss, gbase, tag, publish, bA[i],
+                                                         bB[i], h_before, wAggA, wAggB, wInc, ctrl, status,
+                                                         spin_limit);
+                        if (ss == 0) {
+                            if (publish)
+                                st_relaxed_u64(&wInc[bid * TD + ch], pack_word(tag, fmaf(bA[i], carry, bB[i])));
+                            run[i] = carry;
+                        }
+                    }
+                }
             } else {
                 const bool publish = (q + 1 < chunks) && (id != silent_tile);
                 float carry = h_before;
@@ -447,7 +531,8 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
 #pragma unroll
         for (int i = 0; i < CPT; ++i) hc[i] = fmaf(pA[i], hc[i], pB[i]);
         // (D is even when CPT = 2, so a group is inside D or wholly past it)
-        if (!reduce && (d0 + CPT * c) < D) {
+        const bool stores = !reduce && !(blocks && !(tc.flags & kApplyPass));
+        if (stores && (d0 + CPT * c) < D) {
             E *hp = h + ((bi * L + t0 + r0) * D + d0 + CPT * c);
             if (nv == K) {
 #pragma unroll
@@ -485,9 +570,9 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
     // slots while this grid still runs (measured 3 % slower on (32, 4096, 256)).
     pdl_release();
 
-    // Look-back mode: the last CTA to finish resets the counters and advances the
-    // epoch for the next launch on this workspace.
-    if (lookback) {
+    // Look-back and blocks modes: the last CTA to finish resets the counters and
+    // advances the epoch for the next launch on this workspace.
+    if (chained) {
         __syncthreads();
         if (tid == 0) {
             __threadfence();
@@ -504,10 +589,10 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
     }
 }
 
-template <int DT, int TD, int TT, int S, int ST, int CPT>
+template <int DT, int TD, int TT, int S, int ST, int CPT, bool BM = false>
 constexpr ChunkedVariant make_variant() {
     return ChunkedVariant{TD, TT, S, ST, TD / CPT * S, sizeof(ChunkSmem<typename Storage<DT>::raw, TD, TT, S, ST>),
-                          (int)sizeof(typename Storage<DT>::raw), CPT};
+                          (int)sizeof(typename Storage<DT>::raw), CPT, BM ? 1 : 0};
 }
 
 }  // namespace

@@ -76,6 +76,7 @@ struct ChunkedVariant {
     size_t smem_bytes;   // dynamic shared memory per CTA
     int elem_bytes = 4;  // stored element size: 4 (fp32) or 2 (bfloat16 and binary16)
     int cpt = 1;         // adjacent channels per thread: 1, or 2 (16-bit storage)
+    int blocks = 0;      // 1: compiled for blocks mode (and only used there)
 };
 // The compiled variants (tile_d, tile_t, segments, stages combinations): fp32
 // storage, and 16-bit storage (each shape compiled for bfloat16 and binary16).
@@ -89,6 +90,8 @@ constexpr int kModeLookback = 0;   // tiles of a slice on different CTAs, decoup
 constexpr int kModeOwn = 1;        // a CTA owns whole slices, carry in a register
 constexpr int kModeReduce = 2;     // two-pass, first launch: write every tile's aggregate
 constexpr int kModeApply = 3;      // two-pass, last launch: carry from the scanned aggregates
+constexpr int kModeBlocks = 4;     // one launch: blocks of G tiles, reduce, look-back over blocks,
+                                   // apply from L2 (variants with blocks = 1 only)
 
 struct ChunkedLaunch {
     const ChunkedVariant *variant;
@@ -101,10 +104,12 @@ struct ChunkedLaunch {
     int64_t chunks;              // ceil(L / tile_t)
     int64_t n_tiles;             // n_slices * chunks
     int64_t grid;
-    int mode;                    // kModeLookback, kModeOwn, kModeReduce, kModeApply
+    int mode;                    // kModeLookback, kModeOwn, kModeReduce, kModeApply, kModeBlocks
+    int group = 0;               // blocks mode: tiles per block
     Control *ctrl;
-    unsigned long long *words;   // look-back mode: 3 * n_tiles * tile_d words; two-pass modes: the
-                                 // per-tile A, B and scanned H arrays (3 * n_tiles * tile_d floats)
+    unsigned long long *words;   // look-back mode: 3 * n_tiles * tile_d words; blocks mode: 3 * blocks *
+                                 // tile_d words; two-pass modes: the per-tile A, B and scanned H arrays
+                                 // (3 * n_tiles * tile_d floats)
     unsigned int *status;        // where device-side failures are recorded
     int64_t spin_limit;
     int64_t silent_tile;         // tile id that publishes nothing (tests), or -1

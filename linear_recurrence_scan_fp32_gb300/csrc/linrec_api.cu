@@ -23,6 +23,8 @@ constexpr int kRegcarryThreads = 256;
 constexpr int64_t kRegcarryMinThreadsPerSm = 96;
 // Few slices: the two-pass mode from this many time chunks of 128 steps on.
 constexpr int64_t kTwoPassMinChunks = 64;
+// Blocks mode: default time steps per block (tiles per block = this / tile_t).
+constexpr int64_t kBlockSteps = 1024;
 constexpr size_t kWorkspaceHead = 256;      // Control block, padded
 // (B, D, L) layout: rows alone give each SM this many warps -> one pass, each warp
 // scanning consecutive rows until it holds about kRowsStreamElems[16-bit] elements,
@@ -100,12 +102,13 @@ const ChunkedVariant *variants_of(bool backward, int dtype, int *n) {
 }
 
 const ChunkedVariant *find_variant(int tile_d, int tile_t, int stages, int cpt, int segments, int *index,
-                                   bool backward, int dtype) {
+                                   bool backward, int dtype, bool blocks = false) {
     int n = 0;
     const ChunkedVariant *v = variants_of(backward, dtype, &n);
     for (int i = 0; i < n; ++i) {
         if (v[i].tile_d == tile_d && v[i].tile_t == tile_t && (stages == 0 || v[i].stages == stages) &&
-            (cpt == 0 || v[i].cpt == cpt) && (segments == 0 || v[i].segments == segments)) {
+            (cpt == 0 || v[i].cpt == cpt) && (segments == 0 || v[i].segments == segments) &&
+            (v[i].blocks != 0) == blocks) {
             if (index) *index = i;
             return &v[i];
         }
@@ -244,9 +247,11 @@ linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int ali
     // when the chains are short, or, for long chains (whose look-back would be
     // bound by how fast inclusive values travel down the chain), by the
     // two-pass mode: reduce, scan the aggregates, apply.
-    if (opt->chunk_mode < 0 || opt->chunk_mode > 3) return LINREC_ERR_INVALID_VALUE;
+    if (opt->chunk_mode < 0 || opt->chunk_mode > 4) return LINREC_ERR_INVALID_VALUE;
     if (opt->chunk_mode == 3 && !allow_twopass) return LINREC_ERR_INVALID_VALUE;
-    bool own = false, twopass = false;
+    if (opt->chunk_mode == 4 && backward) return LINREC_ERR_INVALID_VALUE;
+    if (opt->group < 0 || (opt->group > 0 && opt->chunk_mode != 4)) return LINREC_ERR_INVALID_VALUE;
+    bool own = false, twopass = false, blk = false;
     if (opt->chunk_mode == 0) {
         const int td = opt->tile_d ? opt->tile_d : 32;
         own = B * ((D + td - 1) / td) >= (int64_t)sm_count;
@@ -255,11 +260,14 @@ linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int ali
     } else {
         own = opt->chunk_mode == 1;
         twopass = opt->chunk_mode == 3;
+        blk = opt->chunk_mode == 4;
     }
     int tile_d = opt->tile_d, tile_t = opt->tile_t, stages = opt->stages;
     if (tile_d == 0 || tile_t == 0) {
         int dd, dt, ds;
-        default_tile(B, L, D, sm_count, own, twopass, backward, dtype, &dd, &dt, &ds);
+        default_tile(B, L, D, sm_count, own, twopass || blk, backward, dtype, &dd, &dt, &ds);
+        // blocks mode in 16-bit storage: the 256-step tile (the one compiled for it) at any L
+        if (blk && dtype != kDtypeF32) { dt = 256; ds = 2; }
         if (tile_d == 0) tile_d = dd;
         if (tile_t == 0) tile_t = dt;
         if (stages == 0) stages = ds;
@@ -269,12 +277,15 @@ linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int ali
     int segs = opt->segments;
     if (cpt == 0 && segs == 0 && dtype != kDtypeF32 && !backward && tile_d == 32 && tile_t == 256 &&
         (stages == 0 || stages == 2))
-        default_groups_16(B * ((D + 31) / 32), sm_count, own, twopass, &cpt, &segs);
-    const ChunkedVariant *v = find_variant(tile_d, tile_t, stages, cpt, segs, variant_index, backward, dtype);
-    if (!v && opt->stages == 0) v = find_variant(tile_d, tile_t, 0, cpt, segs, variant_index, backward, dtype);
+        default_groups_16(B * ((D + 31) / 32), sm_count, own, twopass || blk, &cpt, &segs);
+    const ChunkedVariant *v = find_variant(tile_d, tile_t, stages, cpt, segs, variant_index, backward, dtype, blk);
+    if (!v && opt->stages == 0)
+        v = find_variant(tile_d, tile_t, 0, cpt, segs, variant_index, backward, dtype, blk);
     if (!v) return LINREC_ERR_INVALID_VALUE;
-    plan->lookback = (own || twopass) ? 0 : 1;
+    plan->lookback = (own || twopass || blk) ? 0 : 1;
     plan->twopass = twopass ? 1 : 0;
+    // blocks mode: tiles per block, kBlockSteps time steps by default
+    plan->blocks = blk ? (opt->group > 0 ? opt->group : (int)((kBlockSteps + v->tile_t - 1) / v->tile_t)) : 0;
     plan->vec = v->cpt;
     plan->tile_d = v->tile_d;
     plan->tile_t = v->tile_t;
@@ -292,12 +303,14 @@ linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int ali
     }
     if (opt->ctas_per_sm > 0 && opt->ctas_per_sm < per_sm) per_sm = opt->ctas_per_sm;
     int64_t grid = (int64_t)sm_count * per_sm;
-    const int64_t units = own ? B * spb : plan->n_tiles;   // slices, or tiles
+    const int64_t n_blocks = blk ? B * spb * ((plan->chunks + plan->blocks - 1) / plan->blocks) : 0;
+    const int64_t units = own ? B * spb : blk ? n_blocks : plan->n_tiles;   // slices, blocks or tiles
     if (grid > units) grid = units;
     plan->grid = grid;
     plan->workspace_bytes = kWorkspaceHead;
     if (twopass) plan->workspace_bytes += ((size_t)3 * (size_t)plan->n_tiles + (size_t)(B * spb)) *
                                           (size_t)v->tile_d * 4u;
+    else if (blk) plan->workspace_bytes += (size_t)3 * (size_t)n_blocks * (size_t)v->tile_d * 8u;
     else if (!own) plan->workspace_bytes += (size_t)3 * (size_t)plan->n_tiles * (size_t)v->tile_d * 8u;
     return LINREC_OK;
 }
@@ -434,7 +447,8 @@ linrec_status_t scan_locked(DeviceInfo *di, int dev, const void *a, const void *
     p.chunks = plan.chunks;
     p.n_tiles = plan.n_tiles;
     p.grid = plan.grid;
-    p.mode = plan.twopass ? kModeReduce : plan.lookback ? kModeLookback : kModeOwn;
+    p.mode = plan.twopass ? kModeReduce : plan.blocks ? kModeBlocks : plan.lookback ? kModeLookback : kModeOwn;
+    p.group = plan.blocks;
     p.ctrl = reinterpret_cast<Control *>(ws->base);
     p.words = reinterpret_cast<unsigned long long *>(arrays ? arrays->base : ws->base + kWorkspaceHead);
     p.status = opt->d_status ? opt->d_status : &p.ctrl->status;

@@ -116,7 +116,8 @@ extern "C" linrec_status_t linrec_scan_f32_noalloc(const float *a, const float *
     // one launch on the fixed array: slice-owner or look-back mode, never the two-pass mode
     {
         linrec_plan_t probe;
-        if (linrec_plan_f32(B, L, D, ds->sm_count, 16, 0, &opt, &probe) == LINREC_OK && probe.twopass)
+        if (linrec_plan_f32(B, L, D, ds->sm_count, 16, 0, &opt, &probe) == LINREC_OK &&
+            (probe.twopass || probe.blocks))
             opt.chunk_mode = 2;
     }
     linrec_plan_t plan;
@@ -127,7 +128,9 @@ extern "C" linrec_status_t linrec_scan_f32_noalloc(const float *a, const float *
     const ChunkedVariant *vars = chunked_variants(&nvar);
     int vi = -1;
     for (int i = 0; i < nvar && i < 64; ++i)
-        if (vars[i].tile_d == plan.tile_d && vars[i].tile_t == plan.tile_t && vars[i].stages == plan.stages) vi = i;
+        if (vars[i].tile_d == plan.tile_d && vars[i].tile_t == plan.tile_t && vars[i].stages == plan.stages &&
+            !vars[i].blocks)
+            vi = i;
     if (vi < 0) return LINREC_ERR_INVALID_VALUE;
     if (ds->ctas_per_sm[vi] == 0) {
         int c = 0;

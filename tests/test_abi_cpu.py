@@ -184,7 +184,26 @@ def test_plan_chunk_modes():
     assert p["workspace_bytes"] == 256 + 4 * (3 * p["n_tiles"] + 64 // p["tile_d"]) * p["tile_d"]
     assert lr.linrec_plan_f32_backward(1, 1 << 20, 64, chunk_mode="lookback")["lookback"] == 1
     with pytest.raises(lr.LinrecError):
-        lr.linrec_plan_f32(1, 1000, 64, path="chunked", chunk_mode=4)
+        lr.linrec_plan_f32(1, 1000, 64, path="chunked", chunk_mode=5)
+    # blocks mode: one launch, `group` tiles per block (1024 steps by default), three look-back
+    # words per block and channel; forward only; group is taken by blocks mode alone
+    p = lr.linrec_plan_f32(1, 1 << 20, 64, path="chunked", chunk_mode="blocks", sm_count=152, resident_ctas=2)
+    assert (p["blocks"], p["lookback"], p["twopass"], p["tile_t"], p["grid"]) == (8, 0, 0, 128, 304)
+    n_blocks = 2 * (8192 // 8)
+    assert p["workspace_bytes"] == 256 + 3 * n_blocks * 32 * 8
+    p = lr.linrec_plan_f32(1, 1000, 64, chunk_mode="blocks", group=3, tile_d=64)
+    assert (p["blocks"], p["tile_d"], p["chunks"], p["grid"]) == (3, 64, 8, 3)
+    with pytest.raises(lr.LinrecError):
+        lr.linrec_plan_f32_backward(1, 1 << 20, 64, chunk_mode="blocks")
+    with pytest.raises(lr.LinrecError):
+        lr.linrec_plan_f32(1, 1 << 20, 64, chunk_mode="lookback", group=2)
+    with pytest.raises(lr.LinrecError):
+        lr.linrec_plan_f32(1, 1 << 20, 64, chunk_mode="blocks", group=-1)
+    with pytest.raises(lr.LinrecError):
+        lr.linrec_plan_f32(1, 1 << 20, 64, chunk_mode="blocks", tile_t=64)   # not compiled for blocks
+    assert lr.linrec_plan_16(1, 1 << 20, 64, chunk_mode="blocks")["blocks"] == 4
+    p = lr.linrec_plan_16(1, 64, 32, chunk_mode="blocks")            # short: still the 256-step tile
+    assert (p["tile_t"], p["blocks"], p["grid"]) == (256, 4, 1)
 
 
 def test_carry_state_overlap_checks(L):

@@ -56,7 +56,8 @@ def test_forward_every_path_past_2_31():
     a, b = _draw(71)
     h = torch.empty_like(a)
     for opt in ({}, {"path": "chunked", "chunk_mode": "own"}, {"path": "chunked", "chunk_mode": "lookback"},
-                {"path": "chunked", "chunk_mode": "twopass"}, {"path": "regcarry"}):
+                {"path": "chunked", "chunk_mode": "twopass"}, {"path": "chunked", "chunk_mode": "blocks"},
+                {"path": "regcarry"}):
         h.fill_(float("nan"))
         lr.linrec_scan_f32_ex(a, b, h, **opt) if opt else lr.linrec_scan_f32(a, b, h)
         _check(h, a, b, f"fp32 {opt or 'auto'}")

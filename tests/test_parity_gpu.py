@@ -39,6 +39,7 @@ def legal_paths(B, L, D, aligned=True):
         paths.append({"path": "chunked", "chunk_mode": "own"})
         paths.append({"path": "chunked", "chunk_mode": "lookback"})
         paths.append({"path": "chunked", "chunk_mode": "twopass"})
+        paths.append({"path": "chunked", "chunk_mode": "blocks"})
     return paths
 
 
@@ -204,11 +205,12 @@ def test_deterministic_bits():
                 assert torch.equal(run(a_d, b_d, **opt), h1), f"{name} {opt}: bits changed between calls"
 
 
-@pytest.mark.parametrize("mode", ["lookback", "twopass"])
+@pytest.mark.parametrize("mode", ["lookback", "twopass", "blocks"])
 def test_carry_modes_repeat_bit_identical(mode):
-    """A race check on the cross-CTA carry: 50 calls of the look-back or two-pass mode, whose
-    tiles land on different CTAs in a different order every time, all return the same bits."""
-    for (B, L, D, tile) in [(1, 1 << 18, 64, {}), (2, 50000, 128, {"tile_d": 32, "tile_t": 64, "stages": 3})]:
+    """A race check on the cross-CTA carry: 50 calls of the look-back, two-pass or blocks mode,
+    whose tiles land on different CTAs in a different order every time, all return the same bits."""
+    second = {"tile_d": 32, "tile_t": 64, "stages": 3} if mode != "blocks" else {"tile_d": 64, "group": 3}
+    for (B, L, D, tile) in [(1, 1 << 18, 64, {}), (2, 50000, 128, second)]:
         a, b = inputs.generate(B, L, D, seed=19 + L, a_dist="u[0.9,1)", b_dist="n(0,1)")
         a_d, b_d = a.to(DEV), b.to(DEV)
         opt = dict(path="chunked", chunk_mode=mode, **tile)
@@ -301,10 +303,58 @@ def test_modes_alternating_on_one_stream():
     for k in range(3):
         h1 = run(*d1, path="chunked", chunk_mode="twopass")
         assert_close(h1.cpu().numpy(), want1, f"two-pass, call {k}")
-        for mode in ("lookback", "twopass", "lookback"):
+        for mode in ("lookback", "twopass", "blocks", "lookback", "blocks"):
             h2 = run(*d2, path="chunked", chunk_mode=mode)
             assert_close(h2.cpu().numpy(), want2, f"{mode} after two-pass, call {k}")
     assert lr.linrec_stream_status() == lr.LINREC_OK
+
+
+# ---------------------------------------------------------------------------
+# blocks mode: G consecutive tiles per block, one look-back per block
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("tile_d", [32, 64])
+@pytest.mark.parametrize("group", [1, 2, 3, 8, 13])
+def test_blocks_mode_every_group(tile_d, group):
+    """Blocks of 1 to 13 tiles, with a last block of fewer tiles and a ragged last tile;
+    repeated calls return the same bits (the block chain is evaluated in one fixed order)."""
+    for (B, L, D) in [(2, 5000, 96), (1, 40001, 64), (3, 129, 260)]:
+        a, b = inputs.generate(B, L, D, seed=23 + L + group, a_dist="u[0.9,1)", b_dist="n(0,1)")
+        h64, _ = oracle.f64(a, b)
+        a_d, b_d = a.to(DEV), b.to(DEV)
+        opt = dict(path="chunked", chunk_mode="blocks", tile_d=tile_d, tile_t=128, group=group)
+        plan = lr.linrec_plan_f32(B, L, D, **opt)
+        assert plan["blocks"] == group and plan["lookback"] == 0 and plan["twopass"] == 0
+        h = run(a_d, b_d, **opt)
+        assert_close(h.cpu().numpy(), h64, f"blocks {(B, L, D)} {opt}")
+        assert torch.equal(run(a_d, b_d, **opt), h), f"blocks {(B, L, D)} {opt}: bits changed"
+    assert lr.linrec_stream_status() == lr.LINREC_OK
+
+
+def test_blocks_timeout_reports_and_recovers():
+    """Block 5 publishes nothing: block 6's look-back gives up after a bounded number of polls,
+    the status word says so, and the next call on the stream is exact."""
+    B, L, D = 1, 64 * 256, 64
+    a, b = inputs.generate(B, L, D, seed=29, a_dist="u[0.5,1)", b_dist="n(0,1)")
+    h64, _ = oracle.f64(a, b)
+    a_d, b_d = a.to(DEV), b.to(DEV)
+    opt = dict(path="chunked", chunk_mode="blocks", tile_d=64, tile_t=128, group=2)
+    s = torch.cuda.Stream()
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    with torch.cuda.stream(s):
+        h = lr.linrec_scan_f32_ex(a_d, b_d, stream=s, spin_limit=2000, test_silent_tile=5 + 1, d_status=status,
+                                  **opt)
+    s.synchronize()
+    assert int(status.item()) & (1 << lr.LINREC_ERR_LOOKBACK_TIMEOUT)
+    hn = h.cpu().numpy()
+    assert_close(hn[:, :6 * 256], h64[:, :6 * 256], "blocks before the timeout")
+    assert np.isnan(hn[:, 6 * 256:]).any()
+    assert lr.linrec_stream_status(s) == lr.LINREC_OK          # the failure went to d_status
+    with torch.cuda.stream(s):
+        h = lr.linrec_scan_f32_ex(a_d, b_d, stream=s, **opt)
+    s.synchronize()
+    assert_close(h.cpu().numpy(), h64, "blocks after recovery")
+    assert lr.linrec_stream_status(s) == lr.LINREC_OK
 
 
 # ---------------------------------------------------------------------------

@@ -56,7 +56,7 @@ def assert_close16(kind, h, h64, what):
 def paths(D, aligned=True):
     out = [{"path": "regcarry"}]
     if aligned and D % 8 == 0:
-        out += [{"path": "chunked", "chunk_mode": m} for m in ("own", "lookback", "twopass")]
+        out += [{"path": "chunked", "chunk_mode": m} for m in ("own", "lookback", "twopass", "blocks")]
     return out
 
 
@@ -112,8 +112,9 @@ def test_same_arithmetic_as_the_fp32_path(kind):
     a_d, b_d = a16.to(DEV), b16.to(DEV)
     # the same tile on both sides (the 16-bit default's 256 steps has no fp32 twin; the
     # ring depth does not change the arithmetic)
+    # (blocks mode is compiled for the 256-step 16-bit tile only)
     same = {"tile_d": 32, "tile_t": 128, "stages": 3}
-    opts = [dict(o, **same) if o.get("path") == "chunked" else o for o in paths(D)]
+    opts = [dict(o, **same) if o.get("path") == "chunked" else o for o in paths(D) if o.get("chunk_mode") != "blocks"]
     for opt in opts + [{"path": "chunked", "tile_d": 64, "tile_t": 128, "stages": 2, "chunk_mode": "lookback"}]:
         h16 = run(kind, a_d, b_d, **opt)
         f32opt = dict(opt)
@@ -226,3 +227,25 @@ def test_carry_state_is_fp32(kind, shape):
         assert_close16(kind, h, h64, f"{kind} {shape} {opt}")
         err = np.abs(last.cpu().double().numpy() - last64) - 1e-4 * (1 + np.abs(last64))
         assert (err <= 0).all(), f"{kind} {shape} {opt}: h_last off by {err.max()}"
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("group", [1, 3, 4, 7])
+def test_blocks_mode_groups(kind, group):
+    """Blocks of 1 to 7 tiles of 256 steps, a short last block, h_init / h_last in fp32;
+    a second call gives the same words."""
+    for (B, L, D) in [(1, 70001, 64), (2, 3001, 200)]:
+        a16, b16 = draw16(kind, B, L, D, 89 + L + group, a_dist="u[0.9,1)")
+        g = torch.Generator().manual_seed(90)
+        h0 = torch.randn((B, D), generator=g)
+        h64, last64 = oracle.f64_16(kind, a16, b16, h0.double().numpy())
+        a_d, b_d, h0_d = a16.to(DEV), b16.to(DEV), h0.to(DEV)
+        opt = dict(path="chunked", chunk_mode="blocks", group=group)
+        assert lr.linrec_plan_16(B, L, D, **opt)["blocks"] == group
+        last = torch.full((B, D), float("nan"), device=DEV)
+        h = run(kind, a_d, b_d, h_init=h0_d, h_last=last, **opt)
+        assert_close16(kind, h, h64, f"{kind} {(B, L, D)} {opt}")
+        err = np.abs(last.cpu().double().numpy() - last64) - 1e-4 * (1 + np.abs(last64))
+        assert (err <= 0).all(), f"{kind} {(B, L, D)} {opt}: h_last off by {err.max()}"
+        assert torch.equal(run(kind, a_d, b_d, h_init=h0_d, **opt), h), f"{kind} {opt}: words changed"
+    assert lr.linrec_stream_status() == lr.LINREC_OK
