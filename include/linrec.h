@@ -36,6 +36,17 @@
  *    be scheduled while the previous work on the stream drains, but it touches
  *    no memory before that work has completed, so stream order holds as for a
  *    plain launch.
+ *  - CUDA graphs: every device-pointer entry point (not linrec_scan_f32_host,
+ *    not linrec_stream_status, which synchronises) may be called on a stream
+ *    that is being captured.  The library allocates nothing during capture:
+ *    the call uses the workspace the library already holds for that stream,
+ *    so first make the same call (or one of the same shape and mode) once on
+ *    that stream outside capture; otherwise the call returns
+ *    LINREC_ERR_WORKSPACE and enqueues nothing.  A captured workspace is never
+ *    freed (later, larger calls on the stream get a new one).  Replays of the
+ *    graph use the capturing stream's workspace wherever they are launched, so
+ *    a replay must not overlap other work that uses it: an uncaptured call on
+ *    the capturing stream, or a replay of another graph captured on it.
  */
 #ifndef LINREC_H_
 #define LINREC_H_
@@ -53,7 +64,8 @@ typedef enum {
     LINREC_ERR_ALIAS = 2,              /* h overlaps a or b */
     LINREC_ERR_UNSUPPORTED_DEVICE = 3, /* the current device is not compute capability 10.3 */
     LINREC_ERR_LAUNCH = 4,             /* a CUDA call failed while enqueueing the work */
-    LINREC_ERR_WORKSPACE = 5,          /* the look-back workspace could not be allocated */
+    LINREC_ERR_WORKSPACE = 5,          /* the look-back workspace could not be allocated (or the
+                                          stream is capturing and holds too little: see below) */
     LINREC_ERR_LOOKBACK_TIMEOUT = 6,   /* a kernel gave up waiting on a predecessor tile */
     LINREC_ERR_TMA_TIMEOUT = 7         /* a kernel gave up waiting on a bulk copy */
 } linrec_status_t;

@@ -53,6 +53,7 @@ std::map<int, DeviceInfo> g_devices;
 struct Slot {
     unsigned char *base = nullptr;
     size_t bytes = 0;
+    bool captured = false;   // used by a call captured into a CUDA graph: never freed
 };
 // What a workspace slot holds.  A look-back slot holds the Control block and
 // tagged words only (zero when allocated), so a word whose tag matches the
@@ -365,6 +366,19 @@ bool encode_map(CUtensorMap *map, const void *base, int64_t B, int64_t L, int64_
 // when (re)allocated.  Caller holds g_mu.
 Slot *workspace(int dev, cudaStream_t stream, size_t need, int level = 0, SlotKind kind = kSlotTagged) {
     Slot &s = g_slots[std::make_tuple(dev, reinterpret_cast<uintptr_t>(stream), level, (int)kind)];
+    // While the stream is being captured into a CUDA graph nothing is allocated (the
+    // graph would own the memory); a slot a captured call uses stays allocated for good,
+    // since the graph keeps its address.
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (cap != cudaStreamCaptureStatusNone) {
+        if (s.bytes < need) return nullptr;
+        s.captured = true;
+        return &s;
+    }
     if (s.bytes >= need) return &s;
     size_t bytes = (need + (1u << 20) - 1) & ~(size_t)((1u << 20) - 1);
     void *p = nullptr;
@@ -377,9 +391,10 @@ Slot *workspace(int dev, cudaStream_t stream, size_t need, int level = 0, SlotKi
         cudaFreeAsync(p, stream);
         return nullptr;
     }
-    if (s.base) cudaFreeAsync(s.base, stream);
+    if (s.base && !s.captured) cudaFreeAsync(s.base, stream);
     s.base = static_cast<unsigned char *>(p);
     s.bytes = bytes;
+    s.captured = false;
     return &s;
 }
 
