@@ -385,6 +385,18 @@ linrec_status_t linrec_scan_f32_noalloc(const float *a, const float *b, float *h
 /* Human-readable name of a status code (static storage). */
 const char *linrec_status_string(linrec_status_t status);
 
+/*
+ * linrec_workspace_bytes -- device memory that a linrec_scan_f32 call on
+ * (B, L, D) with 16-byte-aligned pointers holds on the current device: the
+ * control block and look-back words, plus, in two-pass mode, the tile maps
+ * and the workspace of their scan.  The library allocates it on the call's
+ * stream at the first call that needs it, rounding each allocation up to a
+ * MiB, and keeps it for later calls on that stream (see CUDA graphs above).
+ * Returns 0 for the register path, an empty or invalid shape, or when no CUDA
+ * device is usable.
+ */
+size_t linrec_workspace_bytes(int64_t B, int64_t L, int64_t D);
+
 /* Library version as major*10000 + minor*100 + patch. */
 int linrec_version(void);
 

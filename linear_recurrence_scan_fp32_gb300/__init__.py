@@ -152,6 +152,8 @@ def lib():
         L.linrec_status_string.restype = ctypes.c_char_p
         L.linrec_version.argtypes = []
         L.linrec_version.restype = i32
+        L.linrec_workspace_bytes.argtypes = [i64, i64, i64]
+        L.linrec_workspace_bytes.restype = ctypes.c_size_t
         _lib = L
         return _lib
 
@@ -467,3 +469,8 @@ def linrec_copy_f32(src, dst, stream=None):
 
 def linrec_version() -> int:
     return int(lib().linrec_version())
+
+
+def linrec_workspace_bytes(B, L, D) -> int:
+    """Device memory a default linrec_scan_f32 call on (B, L, D) holds on the current device (0 if none)."""
+    return int(lib().linrec_workspace_bytes(int(B), int(L), int(D)))

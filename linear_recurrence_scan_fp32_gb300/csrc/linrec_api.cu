@@ -662,6 +662,30 @@ linrec_status_t linrec_plan_f32(int64_t B, int64_t L, int64_t D, int sm_count, i
     return plan_impl(B, L, D, sm_count, align_bytes, ctas_per_sm, opt, plan, nullptr);
 }
 
+size_t linrec_workspace_bytes(int64_t B, int64_t L, int64_t D) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess || sms <= 0) {
+        cudaGetLastError();
+        return 0;
+    }
+    // the plan of a default call (the grid does not change the workspace)
+    linrec_plan_t plan;
+    if (plan_impl(B, L, D, sms, 16, 0, nullptr, &plan, nullptr) != LINREC_OK || plan.path != LINREC_PATH_CHUNKED)
+        return 0;
+    size_t total = plan.workspace_bytes;
+    if (plan.twopass) {
+        // the scan of the tile maps, a (1, chunks, slices * tile_d) problem with a workspace of its own
+        const int64_t slices = B * ((D + plan.tile_d - 1) / plan.tile_d);
+        linrec_plan_t inner;
+        if (plan_impl(1, plan.chunks, slices * plan.tile_d, sms, 16, 0, nullptr, &inner, nullptr, false, false) ==
+                LINREC_OK &&
+            inner.path == LINREC_PATH_CHUNKED)
+            total += inner.workspace_bytes;
+    }
+    return total;
+}
+
 }  // extern "C"
 
 namespace {

@@ -36,7 +36,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ["linrec_scan_f32", "linrec_scan_f32_ex", "linrec_plan_f32", "linrec_stream_status",
-              "linrec_copy_f32", "linrec_status_string", "linrec_version"]:
+              "linrec_copy_f32", "linrec_status_string", "linrec_version", "linrec_workspace_bytes"]:
         assert n in names
 
 

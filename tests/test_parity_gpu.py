@@ -393,6 +393,22 @@ def test_lookback_timeout_reports_and_recovers():
     assert lr.linrec_stream_status(s) == lr.LINREC_OK
 
 
+def test_workspace_bytes():
+    """What a default call holds: the control block alone in slice-owner mode, plus three look-back
+    words per tile and channel in look-back mode, plus the tile maps and their scan's workspace in
+    two-pass mode; nothing on the register path or for an empty shape."""
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    assert lr.linrec_workspace_bytes(32, 4096, 256) == 256
+    assert lr.linrec_workspace_bytes(1, 64, 32) == 256 + 3 * 1 * 32 * 8
+    assert lr.linrec_workspace_bytes(256, 128, 4096) == 0
+    assert lr.linrec_workspace_bytes(0, 64, 32) == 0
+    assert lr.linrec_workspace_bytes(-1, 64, 32) == 0
+    p = lr.linrec_plan_f32(1, 1 << 20, 64, sm_count=sms)
+    inner = lr.linrec_plan_f32(1, p["chunks"], 64, sm_count=sms, chunk_mode="lookback")
+    assert p["twopass"] == 1
+    assert lr.linrec_workspace_bytes(1, 1 << 20, 64) == p["workspace_bytes"] + inner["workspace_bytes"]
+
+
 def test_copy_kernel():
     x = torch.randn(1 << 20, device=DEV)
     y = torch.empty_like(x)
