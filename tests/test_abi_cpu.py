@@ -168,6 +168,21 @@ def test_plan_grid_bounds():
         assert p["grid"] == min(_units(p, 32, 256), 152)
 
 
+def test_plan_slices_spread_evenly():
+    # fp32 slice-owner mode: the busiest CTA owns ceil(slices / resident) slices.  When fewer than
+    # half the resident CTAs would own a slice in that last round, the grid is the fewest CTAs that
+    # keep the same maximum (counts then differ by one at most); otherwise every resident CTA runs
+    for (B, D, want) in [(8, 4096, 256), (64, 1024, 304), (32, 256, 256), (48, 256, 192), (40, 512, 214),
+                         (19, 256, 152), (1000, 32, 250), (12, 1024, 192), (32, 2048, 304)]:
+        p = lr.linrec_plan_f32(B, 2048, D, path="chunked", chunk_mode="own", sm_count=152, resident_ctas=2)
+        slices = B * D // 32
+        waves = -(-slices // 304)
+        assert p["grid"] == want and -(-slices // p["grid"]) == waves, (B, D, p["grid"])
+    # 16-bit storage and the gradient keep every resident CTA
+    assert lr.linrec_plan_16(8, 4096, 4096, sm_count=152, resident_ctas=2)["grid"] == 304
+    assert lr.linrec_plan_f32_backward(8, 4096, 4096, sm_count=152, resident_ctas=2)["grid"] == 304
+
+
 def test_plan_chunk_modes():
     # many slices: each CTA owns whole slices, no look-back words needed
     p = lr.linrec_plan_f32(32, 4096, 256, path="chunked", sm_count=152)

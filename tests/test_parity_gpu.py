@@ -290,6 +290,47 @@ def test_streams_run_independently():
         assert lr.linrec_stream_status(s) == lr.LINREC_OK
 
 
+def test_concurrent_host_threads():
+    """Calls from several host threads at once, each thread on its own stream and chunk mode: the
+    library serialises its bookkeeping, each stream gets its own workspace, and every call returns
+    the bits of the same call made alone."""
+    import threading
+    modes = ["own", "lookback", "twopass", "blocks", "regcarry", "lookback"]
+    jobs = []
+    for k, mode in enumerate(modes):
+        a, b = inputs.generate(2, 20000, 96, seed=70 + k, a_dist="u[0.9,1)", b_dist="n(0,1)")
+        opt = {"path": "regcarry"} if mode == "regcarry" else {"path": "chunked", "chunk_mode": mode}
+        a_d, b_d = a.to(DEV), b.to(DEV)
+        jobs.append((a_d, b_d, opt, run(a_d, b_d, **opt).clone()))
+    errors = []
+
+    def worker(k):
+        try:
+            a_d, b_d, opt, want = jobs[k]
+            s = torch.cuda.Stream()
+            h = torch.empty_like(a_d)
+            for i in range(20):
+                with torch.cuda.stream(s):
+                    h.fill_(float("nan"))
+                    lr.linrec_scan_f32_ex(a_d, b_d, h, stream=s, **opt)
+                s.synchronize()
+                if not torch.equal(h, want):
+                    errors.append(f"thread {k} {opt} call {i}: bits differ")
+                    return
+            st = lr.linrec_stream_status(s)
+            if st != lr.LINREC_OK:
+                errors.append(f"thread {k}: status {lr.linrec_status_string(st)}")
+        except Exception as e:          # reported below: a thread's exception would be lost
+            errors.append(f"thread {k}: {e!r}")
+
+    threads = [threading.Thread(target=worker, args=(k,)) for k in range(len(jobs))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+
+
 def test_modes_alternating_on_one_stream():
     """Two-pass and look-back calls take turns on one stream.  With a ~ U[0,1) the
     two-pass mode's tile products underflow to denormals whose bit patterns equal
