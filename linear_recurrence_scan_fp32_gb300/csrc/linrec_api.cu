@@ -307,14 +307,15 @@ linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int ali
     const int64_t n_blocks = blk ? B * spb * ((plan->chunks + plan->blocks - 1) / plan->blocks) : 0;
     const int64_t units = own ? B * spb : blk ? n_blocks : plan->n_tiles;   // slices, blocks or tiles
     if (grid > units) grid = units;
-    if (own && dtype == kDtypeF32 && !backward) {
+    if (own && dtype == kDtypeF32) {
         // Slices go round-robin, so every CTA works on the same time rows of adjacent slices
         // at once (whole contiguous rows for the DRAM).  The busiest CTA owns ceil(slices /
         // grid) of them.  When fewer than half the CTAs have a slice in that last round, the
         // few still running cannot keep the DRAM busy: then take the fewest CTAs that keep
         // the same maximum, so every CTA owns (nearly) as many slices and all finish together.
         // Measured on GB300 (us per call): (8, 4096, 4096) 284 -> 262, (16, 2048, 2048) 140 ->
-        // 127, (48, 4096, 256) 119 -> 103, (40, 4096, 512) 173 -> 156; with a fuller last round
+        // 127, (48, 4096, 256) 119 -> 103, (40, 4096, 512) 173 -> 156; the gradient (8, 4096,
+        // 4096) 436 -> 395, (48, 4096, 256) 192 -> 171; with a fuller last round
         // it loses ((64, 2048, 1024) 272 -> 280), and so it does in 16-bit storage, where the
         // CTAs' issue rate rather than the DRAM bounds the kernel ((8, 4096, 4096) 126 -> 140).
         const int64_t waves = (units + grid - 1) / grid;

@@ -178,9 +178,9 @@ def test_plan_slices_spread_evenly():
         slices = B * D // 32
         waves = -(-slices // 304)
         assert p["grid"] == want and -(-slices // p["grid"]) == waves, (B, D, p["grid"])
-    # 16-bit storage and the gradient keep every resident CTA
+    # the gradient spreads the same way; 16-bit storage keeps every resident CTA
+    assert lr.linrec_plan_f32_backward(8, 4096, 4096, sm_count=152, resident_ctas=2)["grid"] == 256
     assert lr.linrec_plan_16(8, 4096, 4096, sm_count=152, resident_ctas=2)["grid"] == 304
-    assert lr.linrec_plan_f32_backward(8, 4096, 4096, sm_count=152, resident_ctas=2)["grid"] == 304
 
 
 def test_plan_chunk_modes():
