@@ -397,6 +397,26 @@ const char *linrec_status_string(linrec_status_t status);
  */
 size_t linrec_workspace_bytes(int64_t B, int64_t L, int64_t D);
 
+/*
+ * The index-checked build (compiled with -DLINREC_DEBUG, e.g. by the package's
+ * _build.build(checked=True) into liblinrec_checked.so).  Every plain global
+ * load and store of the scan kernels first tests that it lies inside its array;
+ * one outside is skipped (a load yields zeros) and counted.  TMA copies are
+ * clipped to the tensor by the hardware and need no test.  It serves as the
+ * memory checker of this library where no external one can run.
+ *
+ * linrec_debug_checks: 1 in the index-checked build, 0 otherwise.
+ * linrec_debug_bad_accesses: synchronises the current device, then returns
+ *   and clears the number of accesses skipped since the last call and the byte
+ *   offset of the first one from the start of its array (-1 if none); and sets
+ *   output_cap_bytes: > 0 makes every output array (h, da, db, the states
+ *   handed out) end at that many bytes, so that a test can watch the checks skip
+ *   stores without any real out-of-bounds access; 0 removes the cap.  The
+ *   normal build reports 0 and -1 and ignores the cap.
+ */
+int linrec_debug_checks(void);
+linrec_status_t linrec_debug_bad_accesses(uint64_t *count, int64_t *first_offset, int64_t output_cap_bytes);
+
 /* Library version as major*10000 + minor*100 + patch. */
 int linrec_version(void);
 

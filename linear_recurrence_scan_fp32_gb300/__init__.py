@@ -34,7 +34,8 @@ import os
 import threading
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "liblinrec.so")
+# LINREC_LIBRARY names another build of the same library (the index-checked one, for instance)
+LIB_PATH = os.environ.get("LINREC_LIBRARY") or os.path.join(_HERE, "liblinrec.so")
 
 LINREC_OK = 0
 LINREC_ERR_INVALID_VALUE = 1
@@ -154,6 +155,10 @@ def lib():
         L.linrec_version.restype = i32
         L.linrec_workspace_bytes.argtypes = [i64, i64, i64]
         L.linrec_workspace_bytes.restype = ctypes.c_size_t
+        L.linrec_debug_checks.argtypes = []
+        L.linrec_debug_checks.restype = i32
+        L.linrec_debug_bad_accesses.argtypes = [ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_int64), i64]
+        L.linrec_debug_bad_accesses.restype = i32
         _lib = L
         return _lib
 
@@ -469,6 +474,20 @@ def linrec_copy_f32(src, dst, stream=None):
 
 def linrec_version() -> int:
     return int(lib().linrec_version())
+
+
+def linrec_debug_checks() -> bool:
+    """Whether the loaded library is the index-checked build."""
+    return bool(lib().linrec_debug_checks())
+
+
+def linrec_debug_bad_accesses(output_cap_bytes: int = 0):
+    """(accesses skipped by the index checks since the last call, byte offset of the first or -1);
+    sets the output cap for the calls that follow (0: none).  Synchronises the device."""
+    count, first = ctypes.c_uint64(0), ctypes.c_int64(-1)
+    _check(lib().linrec_debug_bad_accesses(ctypes.byref(count), ctypes.byref(first), int(output_cap_bytes)),
+           "linrec_debug_bad_accesses")
+    return int(count.value), int(first.value)
 
 
 def linrec_workspace_bytes(B, L, D) -> int:

@@ -97,6 +97,9 @@ chunked_backward_kernel(const __grid_constant__ CUtensorMap map_g,
     unsigned long long *const wAggA = words;
     unsigned long long *const wAggB = words + n_tiles * TD;
     unsigned long long *const wInc = words + 2 * n_tiles * TD;
+    // extents for the index-checked build: elements of a, h, g, da, db, and of the (B, D) states
+    const long long n_all = (n_slices / slices_per_batch) * L * D;
+    const long long n_state = (n_slices / slices_per_batch) * D;
 
     auto issue = [&](int st, long long id, long long qr, long long slice) {
         const long long bi = slice / slices_per_batch;
@@ -244,7 +247,9 @@ chunked_backward_kernel(const __grid_constant__ CUtensorMap map_g,
         const float tB = __shfl_sync(kFull, xB, S - 1, S);
 
         // ---- the running c entering the tile from later in time ----------------------
-        const float c_after = (dh_last && d0 + cc < D) ? dh_last[bi * D + d0 + cc] : 0.0f;
+        const float c_after = (dh_last && d0 + cc < D && inside(dh_last + bi * D + d0 + cc, dh_last, n_state))
+                                  ? dh_last[bi * D + d0 + cc]
+                                  : 0.0f;
         if (own) {
             if (ss == 0) {
                 const float carry = (qr == 0) ? c_after : run;
@@ -255,22 +260,28 @@ chunked_backward_kernel(const __grid_constant__ CUtensorMap map_g,
             // the tile's map; the last chunk's absorbs dh_last, so the scan of these maps
             // from 0 (in reversed chunk order) is the chain of running c values
             if (ss == 0) {
-                tileA[id * TD + cc] = (qr == 0) ? 0.0f : tA;
-                tileB[id * TD + cc] = (qr == 0) ? fmaf(tA, c_after, tB) : tB;
+                if (inside(tileA + id * TD + cc, tileA, n_tiles * TD)) tileA[id * TD + cc] = (qr == 0) ? 0.0f : tA;
+                if (inside(tileB + id * TD + cc, tileB, n_tiles * TD))
+                    tileB[id * TD + cc] = (qr == 0) ? fmaf(tA, c_after, tB) : tB;
                 // kept for the apply launch: dh_init may be the same buffer as dh_last, and the
                 // apply launch writes it while other tiles still need the incoming state
-                if (qr == 0) tileX[id * TD + cc] = c_after;
+                if (qr == 0 && inside(tileX + id * TD + cc, tileX, n_slices * TD)) tileX[id * TD + cc] = c_after;
             }
         } else if (apply) {
-            if (ss == 0) sm.carry[cc] = (qr == 0) ? tileX[id * TD + cc] : tileH[(id - n_slices) * TD + cc];
+            if (ss == 0)
+                sm.carry[cc] = (qr == 0) ? (inside(tileX + id * TD + cc, tileX, n_slices * TD) ? tileX[id * TD + cc] : 0.0f)
+                                         : (inside(tileH + (id - n_slices) * TD + cc, tileH, n_tiles * TD)
+                                                ? tileH[(id - n_slices) * TD + cc]
+                                                : 0.0f);
         } else {
             const bool publish = (qr + 1 < chunks) && (id != silent_tile);
             float carry = c_after;
             if (qr > 0)
                 carry = lookback_carry<S, R>(id, n_slices, TD, cc, ss, gbase, tag, publish, tA, tB, c_after,
-                                             wAggA, wAggB, wInc, ctrl, status, spin_limit);
+                                             wAggA, wAggB, wInc, n_tiles * TD, ctrl, status, spin_limit);
             if (ss == 0) {
-                if (publish) st_relaxed_u64(&wInc[id * TD + cc], pack_word(tag, fmaf(tA, carry, tB)));
+                if (publish && inside(wInc + id * TD + cc, wInc, n_tiles * TD))
+                    st_relaxed_u64(&wInc[id * TD + cc], pack_word(tag, fmaf(tA, carry, tB)));
                 sm.carry[cc] = carry;
             }
         }
@@ -288,13 +299,17 @@ chunked_backward_kernel(const __grid_constant__ CUtensorMap map_g,
                 cv = fmaf(al[j], cv, gg[j]);
                 const long long t = trow - j;
                 if (t < L) {
-                    pdb[-(long long)j * D] = cv;
+                    if (inside(pdb - (long long)j * D, db, n_all, true)) pdb[-(long long)j * D] = cv;
                     if (want_da) {
-                        const float hp = (t == 0) ? (h_init ? h_init[bi * D + d] : 0.0f)
+                        const float hp = (t == 0) ? ((h_init && inside(h_init + bi * D + d, h_init, n_state))
+                                                         ? h_init[bi * D + d]
+                                                         : 0.0f)
                                                   : sm.h[st][(rtop - j) * TD + c];
-                        pda[-(long long)j * D] = cv * hp;
+                        if (inside(pda - (long long)j * D, da, n_all, true)) pda[-(long long)j * D] = cv * hp;
                     }
-                    if (t == 0 && dh_init) dh_init[bi * D + d] = a_glob[bi * L * D + d] * cv;
+                    if (t == 0 && dh_init && inside(dh_init + bi * D + d, dh_init, n_state, true) &&
+                        inside(a_glob + bi * L * D + d, a_glob, n_all))
+                        dh_init[bi * D + d] = a_glob[bi * L * D + d] * cv;
                 }
             }
         }
@@ -381,5 +396,7 @@ cudaError_t launch_backward(const BackwardLaunch &p, cudaStream_t stream) {
     return launch_dependent(fn, dim3((unsigned)p.grid), dim3((unsigned)p.variant->threads), p.variant->smem_bytes,
                             stream, args);
 }
+
+LINREC_CHECKED_REPORT(checked_report_backward)
 
 }  // namespace linrec

@@ -88,4 +88,6 @@ cudaError_t launch_chunked(const ChunkedLaunch &p, cudaStream_t stream) {
                             stream, args);
 }
 
+LINREC_CHECKED_REPORT(checked_report_chunked)
+
 }  // namespace linrec

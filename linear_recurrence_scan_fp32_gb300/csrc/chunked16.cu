@@ -68,4 +68,6 @@ const void *chunked16_kernel(const ChunkedVariant *v, int dtype) {
     return nullptr;
 }
 
+LINREC_CHECKED_REPORT(checked_report_chunked16)
+
 }  // namespace linrec

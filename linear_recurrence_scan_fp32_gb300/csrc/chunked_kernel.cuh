@@ -60,6 +60,7 @@
 // error bit in the status word and carries on with NaN.
 #pragma once
 
+#include "checked.cuh"
 #include "kernels.cuh"
 #include "lookback.cuh"
 #include "ptx.cuh"
@@ -236,6 +237,9 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
 
     // look-back words, [unit][channel]: units are tiles, or blocks in blocks mode
     const long long n_units = blocks ? n_blocks : n_tiles;
+    // extents for the index-checked build: elements of h, and of h_init / h_last
+    const long long n_h = (n_slices / slices_per_batch) * L * D;
+    const long long n_state = (n_slices / slices_per_batch) * D;
     unsigned long long *const wAggA = words;
     unsigned long long *const wAggB = words + n_units * TD;
     unsigned long long *const wInc = words + 2 * n_units * TD;
@@ -457,7 +461,9 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
         for (int i = 0; i < CPT; ++i) {
             const int ch = cc + i * TC;
             // h before the first chunk: the carried-in state, or 0.
-            const float h_before = (h_init && d0 + ch < D) ? h_init[bi * D + d0 + ch] : 0.0f;
+            const float h_before = (h_init && d0 + ch < D && inside(h_init + bi * D + d0 + ch, h_init, n_state))
+                                       ? h_init[bi * D + d0 + ch]
+                                       : 0.0f;
             if (own) {
                 if (ss == 0) {
                     const float carry = (q == 0) ? h_before : run[i];
@@ -468,14 +474,19 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
                 // the tile's map; the first chunk's absorbs the carried-in state, so the scan of
                 // these maps from 0 is the chain of inclusive values
                 if (ss == 0) {
-                    tileA[id * TD + ch] = (q == 0) ? 0.0f : tA[i];
-                    tileB[id * TD + ch] = (q == 0) ? fmaf(tA[i], h_before, tB[i]) : tB[i];
+                    if (inside(tileA + id * TD + ch, tileA, n_tiles * TD)) tileA[id * TD + ch] = (q == 0) ? 0.0f : tA[i];
+                    if (inside(tileB + id * TD + ch, tileB, n_tiles * TD))
+                        tileB[id * TD + ch] = (q == 0) ? fmaf(tA[i], h_before, tB[i]) : tB[i];
                     // kept for the apply launch: h_last may be the same buffer as h_init, and the
                     // apply launch writes it while other tiles still need the starting state
-                    if (q == 0) tileX[id * TD + ch] = h_before;
+                    if (q == 0 && inside(tileX + id * TD + ch, tileX, n_slices * TD)) tileX[id * TD + ch] = h_before;
                 }
             } else if (apply) {
-                if (ss == 0) carry_in[ch] = (q == 0) ? tileX[id * TD + ch] : tileH[(id - n_slices) * TD + ch];
+                if (ss == 0)
+                    carry_in[ch] = (q == 0) ? (inside(tileX + id * TD + ch, tileX, n_slices * TD) ? tileX[id * TD + ch] : 0.0f)
+                                            : (inside(tileH + (id - n_slices) * TD + ch, tileH, n_tiles * TD)
+                                                   ? tileH[(id - n_slices) * TD + ch]
+                                                   : 0.0f);
             } else if (blocks) {
                 if (tc.flags & kApplyPass) {
                     // as slice-owner mode, from the h entering the block (left in run by the reduce pass)
@@ -500,10 +511,10 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
                         float carry = h_before;
                         if (bq > 0)
                             carry = lookback_carry<S, R>(bid, n_slices, TD, ch, ss, gbase, tag, publish, bA[i],
-                                                         bB[i], h_before, wAggA, wAggB, wInc, ctrl, status,
-                                                         spin_limit);
+                                                         bB[i], h_before, wAggA, wAggB, wInc, n_units * TD, ctrl,
+                                                         status, spin_limit);
                         if (ss == 0) {
-                            if (publish)
+                            if (publish && inside(wInc + bid * TD + ch, wInc, n_units * TD))
                                 st_relaxed_u64(&wInc[bid * TD + ch], pack_word(tag, fmaf(bA[i], carry, bB[i])));
                             run[i] = carry;
                         }
@@ -514,9 +525,11 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
                 float carry = h_before;
                 if (q > 0)
                     carry = lookback_carry<S, R>(id, n_slices, TD, ch, ss, gbase, tag, publish, tA[i], tB[i],
-                                                 h_before, wAggA, wAggB, wInc, ctrl, status, spin_limit);
+                                                 h_before, wAggA, wAggB, wInc, n_units * TD, ctrl, status,
+                                                 spin_limit);
                 if (ss == 0) {
-                    if (publish) st_relaxed_u64(&wInc[id * TD + ch], pack_word(tag, fmaf(tA[i], carry, tB[i])));
+                    if (publish && inside(wInc + id * TD + ch, wInc, n_units * TD))
+                        st_relaxed_u64(&wInc[id * TD + ch], pack_word(tag, fmaf(tA[i], carry, tB[i])));
                     carry_in[ch] = carry;
                 }
             }
@@ -539,7 +552,8 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
                 for (int j = 0; j < K; ++j) {
 #pragma unroll
                     for (int i = 0; i < CPT; ++i) hc[i] = fmaf(r.a(j, i), hc[i], r.b(j, i));
-                    st_h<DT, CPT>(hp + (long long)j * D, hc);
+                    if (inside(hp + (long long)j * D, h, n_h, true, CPT * (long long)sizeof(E)))
+                        st_h<DT, CPT>(hp + (long long)j * D, hc);
                 }
             } else {
 #pragma unroll
@@ -547,14 +561,17 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
                     if (j < nv) {
 #pragma unroll
                         for (int i = 0; i < CPT; ++i) hc[i] = fmaf(r.a(j, i), hc[i], r.b(j, i));
-                        st_h<DT, CPT>(hp + (long long)j * D, hc);
+                        if (inside(hp + (long long)j * D, h, n_h, true, CPT * (long long)sizeof(E)))
+                            st_h<DT, CPT>(hp + (long long)j * D, hc);
                     }
                 }
             }
             // the thread holding t = L-1 hands the state out
             if (h_last && nv > 0 && t0 + r0 + nv == L) {
 #pragma unroll
-                for (int i = 0; i < CPT; ++i) h_last[bi * D + d0 + CPT * c + i] = hc[i];
+                for (int i = 0; i < CPT; ++i)
+                    if (inside(h_last + bi * D + d0 + CPT * c + i, h_last, n_state, true))
+                        h_last[bi * D + d0 + CPT * c + i] = hc[i];
             }
         }
         // No barrier here.  Stage st was last read before this tile's first

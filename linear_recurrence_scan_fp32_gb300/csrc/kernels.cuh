@@ -170,6 +170,17 @@ struct RowsLaunch {
 bool rows_supported(int dtype, int vec, int prefetch);
 cudaError_t launch_rows(const RowsLaunch &args, cudaStream_t stream);
 
+// ---- index-checked build -------------------------------------------------------
+// Per translation unit with kernels: read and clear the count of accesses skipped by
+// the checks of checked.cuh and the byte offset of the first; set the output cap
+// (tests).  In the normal build they report nothing.
+cudaError_t checked_report_chunked(unsigned long long *count, long long *first, long long out_cap);
+cudaError_t checked_report_chunked16(unsigned long long *count, long long *first, long long out_cap);
+cudaError_t checked_report_backward(unsigned long long *count, long long *first, long long out_cap);
+cudaError_t checked_report_regcarry(unsigned long long *count, long long *first, long long out_cap);
+cudaError_t checked_report_regcarry16(unsigned long long *count, long long *first, long long out_cap);
+cudaError_t checked_report_rows(unsigned long long *count, long long *first, long long out_cap);
+
 // ---- copy-ceiling kernel ---------------------------------------------------
 cudaError_t launch_copy(const float *src, float *dst, int64_t n, int sm_count, cudaStream_t stream);
 

@@ -672,6 +672,36 @@ const char *linrec_status_string(linrec_status_t s) {
 
 int linrec_version(void) { return kVersion; }
 
+int linrec_debug_checks(void) {
+#ifdef LINREC_DEBUG
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+linrec_status_t linrec_debug_bad_accesses(uint64_t *count, int64_t *first_offset, int64_t output_cap_bytes) {
+    if (!count || !first_offset || output_cap_bytes < 0) return LINREC_ERR_INVALID_VALUE;
+    using Report = cudaError_t (*)(unsigned long long *, long long *, long long);
+    const Report reports[] = {checked_report_chunked,  checked_report_chunked16, checked_report_backward,
+                              checked_report_regcarry, checked_report_regcarry16, checked_report_rows};
+    unsigned long long total = 0;
+    long long first = -1;
+    for (Report r : reports) {
+        unsigned long long c = 0;
+        long long f = -1;
+        if (r(&c, &f, (long long)output_cap_bytes) != cudaSuccess) {
+            cudaGetLastError();
+            return LINREC_ERR_LAUNCH;
+        }
+        total += c;
+        if (first < 0 && c > 0) first = f;
+    }
+    *count = total;
+    *first_offset = first;
+    return LINREC_OK;
+}
+
 linrec_status_t linrec_plan_f32(int64_t B, int64_t L, int64_t D, int sm_count, int align_bytes, int ctas_per_sm,
                                 const linrec_options_t *opt, linrec_plan_t *plan) {
     return plan_impl(B, L, D, sm_count, align_bytes, ctas_per_sm, opt, plan, nullptr);

@@ -3,6 +3,7 @@
 // the earlier tiles of its slice.
 #pragma once
 
+#include "checked.cuh"
 #include "kernels.cuh"
 #include "ptx.cuh"
 
@@ -23,15 +24,19 @@ __device__ __forceinline__ float lookback_carry(
     const long long id, const long long n_slices, const int TD, const int cc, const int ss, const int gbase,
     const uint32_t tag, const bool publish_agg, const float tA, const float tB, const float h_before,
     unsigned long long *__restrict__ wAggA, unsigned long long *__restrict__ wAggB,
-    const unsigned long long *__restrict__ wInc, Control *__restrict__ ctrl, unsigned int *__restrict__ status,
-    const long long spin_limit)
+    const unsigned long long *__restrict__ wInc, const long long n_words, Control *__restrict__ ctrl,
+    unsigned int *__restrict__ status, const long long spin_limit)
 {
+    // (n_words: the words of each of the three arrays; a word outside reads as untagged)
+    auto word = [&](const unsigned long long *arr, long long i) -> unsigned long long {
+        return inside(arr + i, arr, n_words) ? ld_relaxed_u64(arr + i) : 0ull;
+    };
     constexpr int W = S * R;
     static_assert(W <= 32, "window fits a 32-bit mask");
     constexpr unsigned GM = (S == 32) ? kFull : ((1u << S) - 1u);
     const long long me = id * TD + cc;
     // Successors may need this tile's aggregate before its carry is known.
-    if (publish_agg && ss == 0) {
+    if (publish_agg && ss == 0 && inside(wAggA + me, wAggA, n_words) && inside(wAggB + me, wAggB, n_words)) {
         st_relaxed_u64(&wAggA[me], pack_word(tag, tA));
         st_relaxed_u64(&wAggB[me], pack_word(tag, tB));
     }
@@ -58,7 +63,7 @@ __device__ __forceinline__ float lookback_carry(
                     inc = true;
                     vH[r] = h_before;         // before the first chunk: the carried-in state
                 } else {
-                    const unsigned long long wi = ld_relaxed_u64(&wInc[j * TD + cc]);
+                    const unsigned long long wi = word(wInc, j * TD + cc);
                     inc = word_tag(wi) == tag;
                     vH[r] = word_val(wi);
                 }
@@ -74,8 +79,8 @@ __device__ __forceinline__ float lookback_carry(
             bool missing = false;
             if (active && p < pc && !have[r]) {
                 const long long j = base - (long long)p * n_slices;
-                const unsigned long long wa = ld_relaxed_u64(&wAggA[j * TD + cc]);
-                const unsigned long long wb = ld_relaxed_u64(&wAggB[j * TD + cc]);
+                const unsigned long long wa = word(wAggA, j * TD + cc);
+                const unsigned long long wb = word(wAggB, j * TD + cc);
                 if (word_tag(wa) == tag && word_tag(wb) == tag) {
                     vA[r] = word_val(wa);
                     vB[r] = word_val(wb);
@@ -136,8 +141,8 @@ __device__ __forceinline__ float lookback_carry(
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 const long long j = id - n_slices - ((long long)w * W + r * S + ss) * n_slices;
-                vA[r] = word_val(ld_relaxed_u64(&wAggA[j * TD + cc]));
-                vB[r] = word_val(ld_relaxed_u64(&wAggB[j * TD + cc]));
+                vA[r] = word_val(word(wAggA, j * TD + cc));
+                vB[r] = word_val(word(wAggB, j * TD + cc));
             }
         }
 #pragma unroll

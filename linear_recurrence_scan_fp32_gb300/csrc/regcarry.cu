@@ -8,6 +8,7 @@
 // a_t, b_t do not depend on h, so the loads of the next P steps are kept in
 // flight in a register ring, which is what keeps HBM busy when the number of
 // channels alone does not.
+#include "checked.cuh"
 #include "kernels.cuh"
 
 namespace linrec {
@@ -53,13 +54,26 @@ regcarry_kernel(const float *__restrict__ a, const float *__restrict__ b, float 
     const vec *pb = reinterpret_cast<const vec *>(b + off);
     vec *ph = reinterpret_cast<vec *>(h + off);
     const long long stride = D / V;           // one time step, in vectors
+    // extents for the index-checked build: elements of a, b, h, and of h_init / h_last
+    const long long n_all = (n_groups / groups_per_batch) * L * D;
+    const long long n_state = (n_groups / groups_per_batch) * D;
+    auto ld = [&](const vec *p, const float *base) -> vec {
+#ifdef LINREC_DEBUG
+        if (!inside(p, base, n_all)) {
+            vec v;
+            zero(v);
+            return v;
+        }
+#endif
+        return ld_stream(p);
+    };
 
     vec ra[P], rb[P];
 #pragma unroll
     for (int j = 0; j < P; ++j) {
         if (j < L) {
-            ra[j] = ld_stream(pa + j * stride);
-            rb[j] = ld_stream(pb + j * stride);
+            ra[j] = ld(pa + j * stride, a);
+            rb[j] = ld(pb + j * stride, b);
         }
     }
     vec hv;
@@ -67,7 +81,10 @@ regcarry_kernel(const float *__restrict__ a, const float *__restrict__ b, float 
     if (h_init) {                             // continue from the given state: a_0 is used
         float *hvs = reinterpret_cast<float *>(&hv);
 #pragma unroll
-        for (int v = 0; v < V; ++v) hvs[v] = h_init[bi * D + dch + v];
+        for (int v = 0; v < V; ++v) {
+            const float *src = h_init + bi * D + dch + v;
+            hvs[v] = inside(src, h_init, n_state) ? *src : 0.0f;
+        }
     } else {
         zero(ra[0]);                          // h_{-1} = 0 and a_0 is never used
     }
@@ -77,11 +94,11 @@ regcarry_kernel(const float *__restrict__ a, const float *__restrict__ b, float 
             const long long t = t0 + j;
             if (t < L) {
                 hv = step(ra[j], hv, rb[j]);
-                st_stream(ph + t * stride, hv);
+                if (inside(ph + t * stride, h, n_all, true)) st_stream(ph + t * stride, hv);
                 const long long tn = t + P;
                 if (tn < L) {
-                    ra[j] = ld_stream(pa + tn * stride);
-                    rb[j] = ld_stream(pb + tn * stride);
+                    ra[j] = ld(pa + tn * stride, a);
+                    rb[j] = ld(pb + tn * stride, b);
                 }
             }
         }
@@ -89,7 +106,10 @@ regcarry_kernel(const float *__restrict__ a, const float *__restrict__ b, float 
     if (h_last) {
         const float *hvs = reinterpret_cast<const float *>(&hv);
 #pragma unroll
-        for (int v = 0; v < V; ++v) h_last[bi * D + dch + v] = hvs[v];
+        for (int v = 0; v < V; ++v) {
+            float *dst = h_last + bi * D + dch + v;
+            if (inside(dst, h_last, n_state, true)) *dst = hvs[v];
+        }
     }
 }
 
@@ -134,10 +154,14 @@ regcarry_backward_kernel(const float *__restrict__ a, const float *__restrict__ 
 #pragma unroll
     for (int v = 0; v < V; ++v) lane_of<vec, V>(one, v) = 1.0f;
 
+    // extents for the index-checked build: elements of a, h, g, da, db, and of the (B, D) states
+    const long long n_all = (n_groups / groups_per_batch) * L * D;
+    const long long n_state = (n_groups / groups_per_batch) * D;
+    auto ld = [&](const vec *p, const float *base) { return inside(p, base, n_all) ? ld_stream(p) : zv; };
     auto load = [&](long long t, vec &rg, vec &ra, vec &rh) {
-        rg = ld_stream(pg + t * stride);
-        ra = (t + 1 < L) ? ld_stream(pa + (t + 1) * stride) : one;   // the carry enters row L-1 whole
-        rh = (want_da && t >= 1) ? ld_stream(ph + (t - 1) * stride) : zv;
+        rg = ld(pg + t * stride, g);
+        ra = (t + 1 < L) ? ld(pa + (t + 1) * stride, a) : one;   // the carry enters row L-1 whole
+        rh = (want_da && t >= 1) ? ld(ph + (t - 1) * stride, h) : zv;
     };
     vec rg[P], ra[P], rh[P];
 #pragma unroll
@@ -147,7 +171,10 @@ regcarry_backward_kernel(const float *__restrict__ a, const float *__restrict__ 
     zero(cv);
     if (dh_last) {
 #pragma unroll
-        for (int v = 0; v < V; ++v) lane_of<vec, V>(cv, v) = dh_last[bi * D + dch + v];
+        for (int v = 0; v < V; ++v) {
+            const float *src = dh_last + bi * D + dch + v;
+            lane_of<vec, V>(cv, v) = inside(src, dh_last, n_state) ? *src : 0.0f;
+        }
     }
     for (long long t0 = 0; t0 < L; t0 += P) {
 #pragma unroll
@@ -155,23 +182,28 @@ regcarry_backward_kernel(const float *__restrict__ a, const float *__restrict__ 
             const long long t = L - 1 - (t0 + j);
             if (t >= 0) {
                 cv = step(ra[j], cv, rg[j]);
-                st_stream(pdb + t * stride, cv);
+                if (inside(pdb + t * stride, db, n_all, true)) st_stream(pdb + t * stride, cv);
                 if (want_da) {
                     vec hp = rh[j];
                     if (t == 0) {
 #pragma unroll
-                        for (int v = 0; v < V; ++v)
-                            lane_of<vec, V>(hp, v) = h_init ? h_init[bi * D + dch + v] : 0.0f;
+                        for (int v = 0; v < V; ++v) {
+                            const float *src = h_init + bi * D + dch + v;
+                            lane_of<vec, V>(hp, v) = (h_init && inside(src, h_init, n_state)) ? *src : 0.0f;
+                        }
                     }
                     vec out;
 #pragma unroll
                     for (int v = 0; v < V; ++v) lane_of<vec, V>(out, v) = lane_of<vec, V>(cv, v) * lane_of<vec, V>(hp, v);
-                    st_stream(pda + t * stride, out);
+                    if (inside(pda + t * stride, da, n_all, true)) st_stream(pda + t * stride, out);
                 }
                 if (t == 0 && dh_init) {
 #pragma unroll
-                    for (int v = 0; v < V; ++v)
-                        dh_init[bi * D + dch + v] = a[off + v] * lane_of<vec, V>(cv, v);
+                    for (int v = 0; v < V; ++v) {
+                        float *dst = dh_init + bi * D + dch + v;
+                        if (inside(dst, dh_init, n_state, true) && inside(a + off + v, a, n_all))
+                            *dst = a[off + v] * lane_of<vec, V>(cv, v);
+                    }
                 }
                 const long long tn = t - P;
                 if (tn >= 0) load(tn, rg[j], ra[j], rh[j]);
@@ -218,5 +250,7 @@ cudaError_t launch_regcarry(int vec, int prefetch, int threads, const float *a, 
 #undef LINREC_RC
     return cudaErrorInvalidValue;
 }
+
+LINREC_CHECKED_REPORT(checked_report_regcarry)
 
 }  // namespace linrec

@@ -8,6 +8,7 @@
 // step).  Each element is widened on load and each h rounded once on store
 // (storage.cuh).  It is the path for pointers not 16-byte aligned and for
 // D % 8 != 0, which the chunked path's copies cannot take.
+#include "checked.cuh"
 #include "kernels.cuh"
 #include "storage.cuh"
 
@@ -72,18 +73,32 @@ regcarry16_kernel(const unsigned short *__restrict__ a, const unsigned short *__
     const W *pb = reinterpret_cast<const W *>(b + off);
     W *ph = reinterpret_cast<W *>(h + off);
     const long long stride = D / V;           // one time step, in words
+    // extents for the index-checked build: elements of a, b, h, and of h_init / h_last
+    const long long n_all = (n_groups / groups_per_batch) * L * D;
+    const long long n_state = (n_groups / groups_per_batch) * D;
+    auto ld = [&](const W *p, const unsigned short *base) -> W {
+#ifdef LINREC_DEBUG
+        if (!inside(p, base, n_all)) {
+            W w;
+            memset(&w, 0, sizeof(W));
+            return w;
+        }
+#endif
+        return ld_word<V>(p);
+    };
 
     W ra[P], rb[P];
 #pragma unroll
     for (int j = 0; j < P; ++j) {
         if (j < L) {
-            ra[j] = ld_word<V>(pa + j * stride);
-            rb[j] = ld_word<V>(pb + j * stride);
+            ra[j] = ld(pa + j * stride, a);
+            rb[j] = ld(pb + j * stride, b);
         }
     }
     float hv[V];
 #pragma unroll
-    for (int v = 0; v < V; ++v) hv[v] = h_init ? h_init[bi * D + dch + v] : 0.0f;
+    for (int v = 0; v < V; ++v)
+        hv[v] = (h_init && inside(h_init + bi * D + dch + v, h_init, n_state)) ? h_init[bi * D + dch + v] : 0.0f;
     if (!h_init) memset(&ra[0], 0, sizeof(W));   // h_{-1} = 0 and a_0 is never used: its word := +0
     for (long long t0 = 0; t0 < L; t0 += P) {
 #pragma unroll
@@ -95,18 +110,19 @@ regcarry16_kernel(const unsigned short *__restrict__ a, const unsigned short *__
                 widen<DT, V>(rb[j], xb);
 #pragma unroll
                 for (int v = 0; v < V; ++v) hv[v] = fmaf(xa[v], hv[v], xb[v]);
-                st_word<V>(ph + t * stride, narrow<DT, V>(hv));
+                if (inside(ph + t * stride, h, n_all, true)) st_word<V>(ph + t * stride, narrow<DT, V>(hv));
                 const long long tn = t + P;
                 if (tn < L) {
-                    ra[j] = ld_word<V>(pa + tn * stride);
-                    rb[j] = ld_word<V>(pb + tn * stride);
+                    ra[j] = ld(pa + tn * stride, a);
+                    rb[j] = ld(pb + tn * stride, b);
                 }
             }
         }
     }
     if (h_last) {
 #pragma unroll
-        for (int v = 0; v < V; ++v) h_last[bi * D + dch + v] = hv[v];
+        for (int v = 0; v < V; ++v)
+            if (inside(h_last + bi * D + dch + v, h_last, n_state, true)) h_last[bi * D + dch + v] = hv[v];
     }
 }
 
@@ -150,5 +166,7 @@ cudaError_t launch_regcarry16(int dtype, int vec, int prefetch, int threads, con
         return launch_dt<kDtypeF16>(vec, prefetch, threads, a, b, h, B, L, D, h_init, h_last, stream);
     return cudaErrorInvalidValue;
 }
+
+LINREC_CHECKED_REPORT(checked_report_regcarry16)
 
 }  // namespace linrec

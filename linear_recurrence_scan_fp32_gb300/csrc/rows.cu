@@ -24,6 +24,7 @@
 // library's (B, L, D) scan turns the maps, laid out (1, segments, rows), into
 // every segment's last h, and an apply launch rescans every segment from the h
 // before it.
+#include "checked.cuh"
 #include "kernels.cuh"
 #include "ptx.cuh"
 #include "storage.cuh"
@@ -115,21 +116,34 @@ rows_scan_kernel(const typename Storage<DT>::raw *__restrict__ a, const typename
     // where this lane's first element of the current chunk is: row `row`, step `t`
     long long row = r0, t = t0 + lane * V;
     if (t >= L) { row += t / L; t %= L; }
+    // extents for the index-checked build: elements of a, b, h; of the per-row states; of the
+    // per-segment arrays
+    const long long n_all = R * L, n_seg = nseg * R;
     // the h entering the unit: irrelevant when it starts a row (the first map is constant)
-    float carry = (apply && g > 0) ? aggH[(g - 1) * R + r0] : 0.0f;
+    float carry = (apply && g > 0 && inside(aggH + (g - 1) * R + r0, aggH, n_seg)) ? aggH[(g - 1) * R + r0] : 0.0f;
     float runA = 1.0f, runB = 0.0f;           // reduce: the segment's composed map so far
 
     const E *pa = a + e0;
     const E *pb = b + e0;
     E *ph = h + e0;
     const long long n = e1 - e0;              // a multiple of V (L % V == 0)
+    auto ld = [&](const E *p, const E *base) -> W {
+#ifdef LINREC_DEBUG
+        if (!inside(reinterpret_cast<const W *>(p), base, n_all)) {
+            W w;
+            memset(&w, 0, sizeof(W));
+            return w;
+        }
+#endif
+        return ldcs_vec<W>(reinterpret_cast<const W *>(p));
+    };
     W ra[P], rb[P];
 #pragma unroll
     for (int j = 0; j < P; ++j) {
         const long long off = (long long)j * CH + lane * V;
         if (off < n) {
-            ra[j] = ldcs_vec<W>(reinterpret_cast<const W *>(pa + off));
-            rb[j] = ldcs_vec<W>(reinterpret_cast<const W *>(pb + off));
+            ra[j] = ld(pa + off, a);
+            rb[j] = ld(pb + off, b);
         }
     }
     for (long long c0 = 0; c0 < n; c0 += (long long)P * CH) {
@@ -149,15 +163,16 @@ rows_scan_kernel(const typename Storage<DT>::raw *__restrict__ a, const typename
             }
             const long long nxt = off + (long long)P * CH;
             if (nxt < n) {
-                ra[j] = ldcs_vec<W>(reinterpret_cast<const W *>(pa + nxt));
-                rb[j] = ldcs_vec<W>(reinterpret_cast<const W *>(pb + nxt));
+                ra[j] = ld(pa + nxt, a);
+                rb[j] = ld(pb + nxt, b);
             }
             if (valid && t == 0) {            // a row's first step: the constant map
                 if (h_init) {
                     // two passes: the apply launch reads the state the reduce launch kept,
                     // since h_last may be the same buffer as h_init
-                    const float s0 = apply ? aggX[row] : h_init[row];
-                    if (reduce) aggX[row] = s0;
+                    const float s0 = apply ? (inside(aggX + row, aggX, R) ? aggX[row] : 0.0f)
+                                           : (inside(h_init + row, h_init, R) ? h_init[row] : 0.0f);
+                    if (reduce && inside(aggX + row, aggX, R)) aggX[row] = s0;
                     xb[0] = fmaf(xa[0], s0, xb[0]);
                 }
                 xa[0] = 0.0f;
@@ -194,8 +209,9 @@ rows_scan_kernel(const typename Storage<DT>::raw *__restrict__ a, const typename
                     out[v] = hv;
                 }
                 if (valid) {
-                    stcs_vec<W>(reinterpret_cast<W *>(ph + off), pack<DT, V, W>(out));
-                    if (h_last && t + V == L) h_last[row] = hv;
+                    if (inside(reinterpret_cast<W *>(ph + off), h, n_all, true))
+                        stcs_vec<W>(reinterpret_cast<W *>(ph + off), pack<DT, V, W>(out));
+                    if (h_last && t + V == L && inside(h_last + row, h_last, R, true)) h_last[row] = hv;
                 }
                 carry = __shfl_sync(kAll, hv, 31);   // h at the chunk's end (a partial chunk ends the unit)
             }
@@ -209,8 +225,8 @@ rows_scan_kernel(const typename Storage<DT>::raw *__restrict__ a, const typename
     if (reduce && lane == 0) {
         // the first segment starts its row, so its map is constant: the scan of these
         // maps from 0 gives every segment's last h
-        aggA[g * R + r0] = runA;
-        aggB[g * R + r0] = runB;
+        if (inside(aggA + g * R + r0, aggA, n_seg)) aggA[g * R + r0] = runA;
+        if (inside(aggB + g * R + r0, aggB, n_seg)) aggB[g * R + r0] = runB;
     }
     pdl_release();   // this warp's unit is done: the next launch may be scheduled
 }
@@ -265,5 +281,7 @@ cudaError_t launch_rows(const RowsLaunch &p, cudaStream_t stream) {
                                                      : launch_dt<kDtypeF16, 2>(p, stream);
     return cudaErrorInvalidValue;
 }
+
+LINREC_CHECKED_REPORT(checked_report_rows)
 
 }  // namespace linrec

@@ -40,6 +40,14 @@ def test_header_declares_the_entry_points():
         assert n in names
 
 
+def test_normal_build_has_no_index_checks(L):
+    # the index checks exist only in the -DLINREC_DEBUG build; here nothing is counted (no CUDA call)
+    assert lr.linrec_debug_checks() is False
+    assert lr.linrec_debug_bad_accesses() == (0, -1)
+    with pytest.raises(lr.LinrecError):
+        lr.linrec_debug_bad_accesses(output_cap_bytes=-1)
+
+
 def test_library_exports_every_declared_symbol(L):
     missing = [n for n in declared_functions() if not hasattr(L, n)]
     assert not missing, f"declared but not exported: {missing}"

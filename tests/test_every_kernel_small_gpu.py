@@ -5,8 +5,8 @@ fp32 forward scan in each chunk mode and on the register path (each vector
 width), 16-bit storage, the (B, D, L) layout in one and two passes, the
 gradient, carried state, the host-buffer pipeline, the no-allocation entry
 and the copy kernel.  The shapes are small, so the file also serves as the
-workload of a memory checker run over the whole library (compute-sanitizer
-memcheck), which slows every kernel by orders of magnitude.
+workload of the index-checked build (test_checked_build_gpu.py runs it with
+liblinrec_checked.so), whose last test requires that no access was skipped.
 """
 import ctypes
 
@@ -164,3 +164,10 @@ def test_host_buffers_noalloc_and_copy():
     lr.linrec_copy_f32(src, dst)
     torch.cuda.synchronize()
     assert torch.equal(src, dst)
+
+
+def test_no_access_skipped():
+    """Run after the sweep above: in the index-checked build no access fell outside its array (in the
+    normal build the count is always 0)."""
+    count, first = lr.linrec_debug_bad_accesses()
+    assert count == 0, f"{count} accesses outside their arrays, the first at byte offset {first}"
