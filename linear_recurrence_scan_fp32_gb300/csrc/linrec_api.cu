@@ -23,6 +23,10 @@ constexpr int kRegcarryThreads = 256;
 constexpr int64_t kRegcarryMinThreadsPerSm = 96;
 // Few slices: the two-pass mode from this many time chunks of 128 steps on.
 constexpr int64_t kTwoPassMinChunks = 64;
+// Wide slices (see plan_impl): from this many time steps, on a grid of at least this
+// share of the SMs.
+constexpr int64_t kWideMinSteps = 1024;
+constexpr int kWideMinGridPct = 84;
 // Blocks mode: default time steps per block (tiles per block = this / tile_t).
 constexpr int64_t kBlockSteps = 1024;
 constexpr size_t kWorkspaceHead = 256;      // Control block, padded
@@ -204,13 +208,36 @@ linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int ali
     // bfloat16 6391 vs 4638; (64, 512, 4096) 6309 vs 6574 for the chunked kernel).
     // Otherwise the TMA-staged chunked kernel whenever its copies are legal; the
     // register path also takes misaligned pointers and D % 4 != 0.
+    // Wide slices first (fp32 forward, L >= kWideMinSteps, the dispatcher's tile): the
+    // widest of 256 or 128 channels whose slice count splits evenly into at least
+    // kWideMinGridPct % of the SMs, one CTA of 512 threads per SM.  Every CTA then owns
+    // the same number of slices, and each box row is 1 or 0.5 KB of contiguous memory.
+    // Measured on GB300 (us per call, the previous choice -> this one): (64, 2048, 1024)
+    // 260 (register path) -> 229 ({128, 64}, 128 CTAs x 4 slices), (128, 1024, 1024)
+    // 249 -> 232 ({256, 32}, 128 x 4), (8, 4096, 4096) 261 -> 234 ({256, 32}, 128 x 1),
+    // (32, 1024, 4096) 247 -> 229, (256, 1024, 256) 133 -> 118; at L <= 512 the register
+    // path stays ahead ((64, 512, 4096) 246 against 261).
+    int wide_td = 0;
+    int64_t wide_grid = 0;
+    if (dtype == kDtypeF32 && !backward && opt->chunk_mode == 0 && opt->tile_d == 0 && opt->tile_t == 0 &&
+        (opt->path == LINREC_PATH_AUTO || opt->path == LINREC_PATH_CHUNKED) && tma_ok && L >= kWideMinSteps) {
+        for (int td : {256, 128}) {
+            const int64_t slices = B * ((D + td - 1) / td);
+            const int64_t k = (slices + sm_count - 1) / sm_count;        // slices per CTA
+            if (slices % k == 0 && (slices / k) * 100 >= (int64_t)kWideMinGridPct * sm_count) {
+                wide_td = td;
+                wide_grid = slices / k;
+                break;
+            }
+        }
+    }
     int path = opt->path;
     if (path == LINREC_PATH_AUTO) {
         const int lanes = 16 / eb;            // channels in 16 bytes
         const bool many = !backward && D % lanes == 0 && align_bytes >= 16 &&
                           (dtype == kDtypeF32 || L < 256) &&
                           B * (D / lanes) >= kRegcarryMinThreadsPerSm * (int64_t)sm_count;
-        path = (tma_ok && !many) ? LINREC_PATH_CHUNKED : LINREC_PATH_REGCARRY;
+        path = (tma_ok && (!many || wide_td)) ? LINREC_PATH_CHUNKED : LINREC_PATH_REGCARRY;
     }
     plan->path = path;
 
@@ -253,7 +280,9 @@ linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int ali
     if (opt->chunk_mode == 4 && backward) return LINREC_ERR_INVALID_VALUE;
     if (opt->group < 0 || (opt->group > 0 && opt->chunk_mode != 4)) return LINREC_ERR_INVALID_VALUE;
     bool own = false, twopass = false, blk = false;
-    if (opt->chunk_mode == 0) {
+    if (wide_td) {
+        own = true;
+    } else if (opt->chunk_mode == 0) {
         const int td = opt->tile_d ? opt->tile_d : 32;
         own = B * ((D + td - 1) / td) >= (int64_t)sm_count;
         const int tt = opt->tile_t ? opt->tile_t : (dtype == kDtypeF32 ? 128 : tile_t_16(L));
@@ -264,7 +293,11 @@ linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int ali
         blk = opt->chunk_mode == 4;
     }
     int tile_d = opt->tile_d, tile_t = opt->tile_t, stages = opt->stages;
-    if (tile_d == 0 || tile_t == 0) {
+    if (wide_td) {
+        tile_d = wide_td;
+        tile_t = 8192 / wide_td;              // 32 KB per box: {256, 32} or {128, 64}
+        if (stages == 0) stages = 2;
+    } else if (tile_d == 0 || tile_t == 0) {
         int dd, dt, ds;
         default_tile(B, L, D, sm_count, own, twopass || blk, backward, dtype, &dd, &dt, &ds);
         // blocks mode in 16-bit storage: the 256-step tile (the one compiled for it) at any L
@@ -307,7 +340,9 @@ linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int ali
     const int64_t n_blocks = blk ? B * spb * ((plan->chunks + plan->blocks - 1) / plan->blocks) : 0;
     const int64_t units = own ? B * spb : blk ? n_blocks : plan->n_tiles;   // slices, blocks or tiles
     if (grid > units) grid = units;
-    if (own && dtype == kDtypeF32) {
+    if (wide_td && grid > wide_grid) {
+        grid = wide_grid;                     // the even split chosen above
+    } else if (own && dtype == kDtypeF32) {
         // Slices go round-robin, so every CTA works on the same time rows of adjacent slices
         // at once (whole contiguous rows for the DRAM).  The busiest CTA owns ceil(slices /
         // grid) of them.  When fewer than half the CTAs have a slice in that last round, the

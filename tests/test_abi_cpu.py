@@ -176,6 +176,29 @@ def test_plan_grid_bounds():
         assert p["grid"] == min(_units(p, 32, 256), 152)
 
 
+def test_plan_wide_slices():
+    # fp32 forward, L >= 1024: the widest of 256 or 128 channels whose slices split evenly over at
+    # least 84 % of the SMs takes slice-owner mode ahead of the register path
+    cases = [((64, 2048, 1024), (256, 32, 128)), ((128, 1024, 1024), (256, 32, 128)),
+             ((8, 4096, 4096), (256, 32, 128)), ((64, 4096, 256), (128, 64, 128)),
+             ((256, 1024, 256), (256, 32, 128)), ((19, 4096, 1024), (256, 32, 76))]
+    for shape, (td, tt, grid) in cases:
+        p = lr.linrec_plan_f32(*shape, sm_count=152, resident_ctas=1)
+        slices = shape[0] * -(-shape[2] // td)
+        if grid * 100 < 84 * 152:                      # no even split: not the wide tile
+            assert p["tile_d"] != td or p["path_name"] != "chunked", shape
+            continue
+        assert (p["path_name"], p["tile_d"], p["tile_t"], p["lookback"], p["twopass"]) == ("chunked", td, tt, 0, 0)
+        assert p["grid"] == grid and slices % grid == 0, shape
+    # not for short sequences, the pages shape, 16-bit storage, the gradient or a chosen tile or mode
+    assert lr.linrec_plan_f32(64, 512, 4096, sm_count=152)["path_name"] == "regcarry"
+    assert lr.linrec_plan_f32(32, 4096, 256, sm_count=152, resident_ctas=2)["tile_d"] == 32
+    assert lr.linrec_plan_16(64, 2048, 1024, sm_count=152)["tile_d"] == 32
+    assert lr.linrec_plan_f32_backward(64, 2048, 1024, sm_count=152)["tile_d"] != 256
+    assert lr.linrec_plan_f32(64, 2048, 1024, sm_count=152, path="chunked", chunk_mode="own")["tile_d"] == 32
+    assert lr.linrec_plan_f32(64, 2048, 1024, sm_count=152, path="regcarry")["path_name"] == "regcarry"
+
+
 def test_plan_slices_spread_evenly():
     # fp32 slice-owner mode: the busiest CTA owns ceil(slices / resident) slices.  When fewer than
     # half the resident CTAs would own a slice in that last round, the grid is the fewest CTAs that
