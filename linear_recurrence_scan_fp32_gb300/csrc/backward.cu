@@ -345,7 +345,9 @@ constexpr ChunkedVariant make_variant() {
     X(32, 64, 4, 3)                 \
     X(32, 64, 4, 4)                 \
     X(64, 64, 4, 2)                 \
-    X(64, 128, 8, 2)
+    X(64, 128, 8, 2)                \
+    X(128, 64, 4, 2)                \
+    X(256, 32, 2, 2)
 
 #define LINREC_V_ENTRY(TD, TT, S, ST) make_variant<TD, TT, S, ST>(),
 const ChunkedVariant kVariants[] = {LINREC_BACKWARD_VARIANTS(LINREC_V_ENTRY)};

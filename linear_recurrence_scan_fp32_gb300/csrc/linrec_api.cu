@@ -216,10 +216,11 @@ linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int ali
     // 260 (register path) -> 229 ({128, 64}, 128 CTAs x 4 slices), (128, 1024, 1024)
     // 249 -> 232 ({256, 32}, 128 x 4), (8, 4096, 4096) 261 -> 234 ({256, 32}, 128 x 1),
     // (32, 1024, 4096) 247 -> 229, (256, 1024, 256) 133 -> 118; at L <= 512 the register
-    // path stays ahead ((64, 512, 4096) 246 against 261).
+    // path stays ahead ((64, 512, 4096) 246 against 261).  The gradient kernel likewise:
+    // (64, 2048, 1024) 419 -> 395 ({128, 64} x 4), (128, 1024, 1024) 448 -> 391.
     int wide_td = 0;
     int64_t wide_grid = 0;
-    if (dtype == kDtypeF32 && !backward && opt->chunk_mode == 0 && opt->tile_d == 0 && opt->tile_t == 0 &&
+    if (dtype == kDtypeF32 && opt->chunk_mode == 0 && opt->tile_d == 0 && opt->tile_t == 0 &&
         (opt->path == LINREC_PATH_AUTO || opt->path == LINREC_PATH_CHUNKED) && tma_ok && L >= kWideMinSteps) {
         for (int td : {256, 128}) {
             const int64_t slices = B * ((D + td - 1) / td);

@@ -190,11 +190,12 @@ def test_plan_wide_slices():
             continue
         assert (p["path_name"], p["tile_d"], p["tile_t"], p["lookback"], p["twopass"]) == ("chunked", td, tt, 0, 0)
         assert p["grid"] == grid and slices % grid == 0, shape
-    # not for short sequences, the pages shape, 16-bit storage, the gradient or a chosen tile or mode
+    # not for short sequences, the pages shape, 16-bit storage or a chosen tile or mode
     assert lr.linrec_plan_f32(64, 512, 4096, sm_count=152)["path_name"] == "regcarry"
     assert lr.linrec_plan_f32(32, 4096, 256, sm_count=152, resident_ctas=2)["tile_d"] == 32
     assert lr.linrec_plan_16(64, 2048, 1024, sm_count=152)["tile_d"] == 32
-    assert lr.linrec_plan_f32_backward(64, 2048, 1024, sm_count=152)["tile_d"] != 256
+    p = lr.linrec_plan_f32_backward(128, 1024, 1024, sm_count=152, resident_ctas=1)    # the gradient too
+    assert (p["tile_d"], p["tile_t"], p["grid"]) == (256, 32, 128)
     assert lr.linrec_plan_f32(64, 2048, 1024, sm_count=152, path="chunked", chunk_mode="own")["tile_d"] == 32
     assert lr.linrec_plan_f32(64, 2048, 1024, sm_count=152, path="regcarry")["path_name"] == "regcarry"
 
@@ -210,7 +211,7 @@ def test_plan_slices_spread_evenly():
         waves = -(-slices // 304)
         assert p["grid"] == want and -(-slices // p["grid"]) == waves, (B, D, p["grid"])
     # the gradient spreads the same way; 16-bit storage keeps every resident CTA
-    assert lr.linrec_plan_f32_backward(8, 4096, 4096, sm_count=152, resident_ctas=2)["grid"] == 256
+    assert lr.linrec_plan_f32_backward(48, 4096, 256, sm_count=152, resident_ctas=2)["grid"] == 192
     assert lr.linrec_plan_16(8, 4096, 4096, sm_count=152, resident_ctas=2)["grid"] == 304
 
 

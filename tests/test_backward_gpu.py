@@ -107,7 +107,8 @@ def test_backward_closed_forms_bit_exact():
         assert torch.equal(db, g_d), f"a=0 {opt}"
 
 
-@pytest.mark.parametrize("tile", [(32, 128, 2), (32, 64, 3), (32, 64, 4), (64, 64, 2), (64, 128, 2)],
+@pytest.mark.parametrize("tile", [(32, 128, 2), (32, 64, 3), (32, 64, 4), (64, 64, 2), (64, 128, 2), (128, 64, 2),
+                                  (256, 32, 2)],
                          ids=lambda t: f"d{t[0]}t{t[1]}s{t[2]}")
 def test_backward_modes_agree_and_repeat(tile):
     td, tt, st = tile
@@ -123,6 +124,9 @@ def test_backward_modes_agree_and_repeat(tile):
     torch.cuda.synchronize()
     assert torch.equal(db1, db2) and torch.equal(da1, da2), "modes differ"
     assert torch.equal(db2, db3) and torch.equal(da2, da3), "not deterministic"
+    da64, db64, _ = oracle.f64_backward(a, h_d.cpu(), g)
+    assert_close(db1.cpu().numpy(), db64, f"db {tile}")
+    assert_close(da1.cpu().numpy(), da64, f"da {tile}")
 
 
 def test_backward_in_segments_chains_through_dh_init():
