@@ -25,7 +25,7 @@ constexpr int64_t kRegcarryMinThreadsPerSm = 96;
 constexpr int64_t kTwoPassMinChunks = 64;
 // Wide slices (see plan_impl): from this many time steps, on a grid of at least this
 // share of the SMs.
-constexpr int64_t kWideMinSteps = 1024;
+constexpr int64_t kWideMinSteps = 256;
 constexpr int kWideMinGridPct = 84;
 // Blocks mode: default time steps per block (tiles per block = this / tile_t).
 constexpr int64_t kBlockSteps = 1024;
@@ -208,15 +208,16 @@ linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int ali
     // bfloat16 6391 vs 4638; (64, 512, 4096) 6309 vs 6574 for the chunked kernel).
     // Otherwise the TMA-staged chunked kernel whenever its copies are legal; the
     // register path also takes misaligned pointers and D % 4 != 0.
-    // Wide slices first (fp32 forward, L >= kWideMinSteps, the dispatcher's tile): the
+    // Wide slices first (fp32, L >= kWideMinSteps, the dispatcher's tile): the
     // widest of 256 or 128 channels whose slice count splits evenly into at least
     // kWideMinGridPct % of the SMs, one CTA of 512 threads per SM.  Every CTA then owns
     // the same number of slices, and each box row is 1 or 0.5 KB of contiguous memory.
     // Measured on GB300 (us per call, the previous choice -> this one): (64, 2048, 1024)
     // 260 (register path) -> 229 ({128, 64}, 128 CTAs x 4 slices), (128, 1024, 1024)
     // 249 -> 232 ({256, 32}, 128 x 4), (8, 4096, 4096) 261 -> 234 ({256, 32}, 128 x 1),
-    // (32, 1024, 4096) 247 -> 229, (256, 1024, 256) 133 -> 118; at L <= 512 the register
-    // path stays ahead ((64, 512, 4096) 246 against 261).  The gradient kernel likewise:
+    // (32, 1024, 4096) 247 -> 229, (256, 1024, 256) 133 -> 118, (32, 512, 4096) 125 -> 117,
+    // (64, 256, 2048) 65 -> 61.  Without an even split the wide tiles lose ((64, 512, 4096):
+    // 1024 slices on 152 CTAs, 265 against 246 on the register path).  The gradient kernel likewise:
     // (64, 2048, 1024) 419 -> 395 ({128, 64} x 4), (128, 1024, 1024) 448 -> 391.
     int wide_td = 0;
     int64_t wide_grid = 0;

@@ -177,7 +177,7 @@ def test_plan_grid_bounds():
 
 
 def test_plan_wide_slices():
-    # fp32 forward, L >= 1024: the widest of 256 or 128 channels whose slices split evenly over at
+    # fp32, L >= 256: the widest of 256 or 128 channels whose slices split evenly over at
     # least 84 % of the SMs takes slice-owner mode ahead of the register path
     cases = [((64, 2048, 1024), (256, 32, 128)), ((128, 1024, 1024), (256, 32, 128)),
              ((8, 4096, 4096), (256, 32, 128)), ((64, 4096, 256), (128, 64, 128)),
@@ -190,8 +190,11 @@ def test_plan_wide_slices():
             continue
         assert (p["path_name"], p["tile_d"], p["tile_t"], p["lookback"], p["twopass"]) == ("chunked", td, tt, 0, 0)
         assert p["grid"] == grid and slices % grid == 0, shape
-    # not for short sequences, the pages shape, 16-bit storage or a chosen tile or mode
+    p = lr.linrec_plan_f32(32, 512, 4096, sm_count=152, resident_ctas=1)              # 512 slices, 4 each
+    assert (p["path_name"], p["tile_d"], p["grid"]) == ("chunked", 256, 128)
+    # not without an even split, for 128 steps, the pages shape, 16-bit storage or a chosen tile or mode
     assert lr.linrec_plan_f32(64, 512, 4096, sm_count=152)["path_name"] == "regcarry"
+    assert lr.linrec_plan_f32(32, 128, 4096, sm_count=152)["path_name"] == "regcarry"
     assert lr.linrec_plan_f32(32, 4096, 256, sm_count=152, resident_ctas=2)["tile_d"] == 32
     assert lr.linrec_plan_16(64, 2048, 1024, sm_count=152)["tile_d"] == 32
     p = lr.linrec_plan_f32_backward(128, 1024, 1024, sm_count=152, resident_ctas=1)    # the gradient too
