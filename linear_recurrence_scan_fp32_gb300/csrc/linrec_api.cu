@@ -26,6 +26,8 @@ constexpr int64_t kTwoPassMinChunks = 64;
 // Wide slices (see plan_impl): from this many time steps, on a grid of at least this
 // share of the SMs.
 constexpr int64_t kWideMinSteps = 256;
+// fp32 forward slice-owner mode from this share of the SM count in slices.
+constexpr int kOwnMinSlicesPct = 84;
 constexpr int kWideMinGridPct = 84;
 // Blocks mode: default time steps per block (tiles per block = this / tile_t).
 constexpr int64_t kBlockSteps = 1024;
@@ -178,6 +180,22 @@ void default_tile(int64_t B, int64_t L, int64_t D, int sm_count, bool own, bool 
     // as soon as its tile is in registers, so up to three tiles are in flight per
     // CTA; on GB300 a 3-deep ring (four in flight) measured 9-11 % slower at every
     // shape (lower DRAM efficiency, not too few bytes in flight).
+    if (own && !twopass && !backward) {
+        // Slices just past one round of the {32, 128} CTAs (two per SM): smaller CTAs (128
+        // threads, 64-step tiles) that take them all in one round.  Measured on GB300 (us per
+        // call, {32, 128, 2} -> this): 320 slices (40, 4096, 256) 102 -> 87 and (10, 4096, 1024)
+        // 102 -> 86 with a 4-deep ring; 352 slices (44, 8192, 256) 201 -> 174 (4-deep); 384
+        // slices (48, 4096, 256) 103 -> 94, (12, 4096, 1024) 103 -> 92, (24, 4096, 512)
+        // 103 -> 93 with a 3-deep ring (the 4-deep one there: 107, 103, 105).  From 448
+        // slices on the spread {32, 128} grid stays ahead.
+        const int64_t slices = B * ((D + 31) / 32), c1 = 2 * (int64_t)sm_count;
+        *tile_d = 32;
+        if (slices > c1 && slices * 100 <= c1 * 120) { *tile_t = 64; *stages = 4; return; }
+        if (slices * 100 > c1 * 120 && slices * 100 <= c1 * 133) { *tile_t = 64; *stages = 3; return; }
+        *tile_t = 128;
+        *stages = 2;
+        return;
+    }
     if (own) { *tile_d = 32; *tile_t = 128; *stages = 2; return; }
     if (D >= 64) { *tile_d = 64; *tile_t = 128; *stages = 2; }
     else { *tile_d = 32; *tile_t = 128; *stages = 3; }
@@ -286,7 +304,12 @@ linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int ali
         own = true;
     } else if (opt->chunk_mode == 0) {
         const int td = opt->tile_d ? opt->tile_d : 32;
-        own = B * ((D + td - 1) / td) >= (int64_t)sm_count;
+        // fp32 forward: slice-owner from kOwnMinSlicesPct % of the SM count on (128 slices of
+        // 32 channels on 152 SMs: (16, 4096, 256) 57 -> 44 us, (1, 32768, 4096) 406 -> 333
+        // against the look-back and two-pass modes); otherwise from one slice per SM
+        const int64_t need = (dtype == kDtypeF32 && !backward) ? ((int64_t)sm_count * kOwnMinSlicesPct + 99) / 100
+                                                               : (int64_t)sm_count;
+        own = B * ((D + td - 1) / td) >= need;
         const int tt = opt->tile_t ? opt->tile_t : (dtype == kDtypeF32 ? 128 : tile_t_16(L));
         twopass = !own && allow_twopass && (L + tt - 1) / tt >= kTwoPassMinChunks;
     } else {

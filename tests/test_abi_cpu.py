@@ -203,6 +203,25 @@ def test_plan_wide_slices():
     assert lr.linrec_plan_f32(64, 2048, 1024, sm_count=152, path="regcarry")["path_name"] == "regcarry"
 
 
+def test_plan_slice_owner_thresholds():
+    # fp32 forward: slice-owner mode from 84 % of the SM count in slices (128 on 152 SMs)
+    p = lr.linrec_plan_f32(16, 4096, 256, sm_count=152, resident_ctas=2)
+    assert (p["lookback"], p["twopass"], p["tile_d"], p["grid"]) == (0, 0, 32, 128)
+    p = lr.linrec_plan_f32(15, 4096, 256, sm_count=152, resident_ctas=2)                 # 120 slices
+    assert p["lookback"] or p["twopass"]
+    # the 16-bit forms and the gradient keep one slice per SM as the threshold
+    assert lr.linrec_plan_16(16, 4096, 256, sm_count=152)["lookback"] == 1
+    assert lr.linrec_plan_f32_backward(16, 4096, 256, sm_count=152)["lookback"] == 1
+    # slices just past one round of {32, 128} CTAs (304): 64-step tiles, 4-deep up to 1.2 rounds,
+    # 3-deep up to 1.33; beyond that the {32, 128} tile again
+    for (B, D, want) in [(40, 256, (64, 4)), (44, 256, (64, 4)), (48, 256, (64, 3)), (12, 1024, (64, 3)),
+                         (56, 256, (128, 2)), (32, 256, (128, 2)), (36, 256, (128, 2))]:
+        p = lr.linrec_plan_f32(B, 4096, D, sm_count=152)
+        assert (p["tile_d"], p["tile_t"], p["stages"]) == (32,) + want, (B, D)
+    p = lr.linrec_plan_f32(48, 4096, 256, sm_count=152, tile_d=32, tile_t=128)             # a chosen tile stays
+    assert (p["tile_t"], p["stages"]) == (128, 2)
+
+
 def test_plan_slices_spread_evenly():
     # fp32 slice-owner mode: the busiest CTA owns ceil(slices / resident) slices.  When fewer than
     # half the resident CTAs would own a slice in that last round, the grid is the fewest CTAs that
