@@ -68,6 +68,8 @@ def launches_per_step(plan: dict, op: str) -> int:
     look-back mode, never two-pass again) and the apply launch."""
     if plan["path_name"] in ("chunked", "rows") and plan["twopass"]:
         return 3
+    if plan["path_name"] == "regcarry" and plan["twopass"]:
+        return 2                              # segmented register path: reduce and apply
     return 1
 FALLBACK_HBM_GBS = 6800.0
 CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -371,7 +373,7 @@ def run_ours(args):
                     "_lookback" if plan["lookback"] else "")
             kernel_tag = "chunked" + store + mode
         else:
-            kernel_tag = "regcarry" + store
+            kernel_tag = "regcarry" + store + ("_segmented" if plan["twopass"] else "")
         scan16 = {"bf16": lr.linrec_scan_bf16_ex, "f16": lr.linrec_scan_f16_ex}.get(args.dtype)
 
     if args.op == "backward":

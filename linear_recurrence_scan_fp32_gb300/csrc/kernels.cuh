@@ -60,6 +60,12 @@ bool regcarry_supported(int vec, int prefetch);
 cudaError_t launch_regcarry(int vec, int prefetch, int threads, const float *a, const float *b,
                             float *h, int64_t B, int64_t L, int64_t D, const float *h_init, float *h_last,
                             cudaStream_t stream);
+// The segmented form for few channels: the time axis cut into nseg segments, a reduce
+// launch writing each segment's map to aggA / aggB ([segment][B * D] floats each) and an
+// apply launch that folds the earlier segments' maps into each segment's carry.
+cudaError_t launch_regcarry_segmented(int vec, int threads, const float *a, const float *b, float *h, int64_t B,
+                                      int64_t L, int64_t D, int64_t nseg, const float *h_init, float *h_last,
+                                      float *aggA, float *aggB, cudaStream_t stream);
 // The same on 16-bit storage (dtype kDtypeBF16 or kDtypeF16): `vec` in {1, 2, 4, 8}
 // elements per thread; h_init and h_last stay fp32.
 bool regcarry16_supported(int vec, int prefetch);

@@ -26,6 +26,11 @@ constexpr int64_t kTwoPassMinChunks = 64;
 // Wide slices (see plan_impl): from this many time steps, on a grid of at least this
 // share of the SMs.
 constexpr int64_t kWideMinSteps = 256;
+// Segmented register path: bytes of loads in flight to aim for per SM, the shortest
+// segment, the most segments.
+constexpr int64_t kSegBytesPerSm = 48 * 1024;
+constexpr int64_t kSegMinSteps = 64;
+constexpr int64_t kSegMax = 256;
 // fp32 forward slice-owner mode from this share of the SM count in slices.
 constexpr int kOwnMinSlicesPct = 84;
 constexpr int kWideMinGridPct = 84;
@@ -279,9 +284,32 @@ linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int ali
         if (!ok) return LINREC_ERR_INVALID_VALUE;
         plan->vec = vec;
         plan->prefetch = prefetch;
+        const int64_t groups = B * (D / vec);
+        // Few channel groups (fp32 forward; odd D and misaligned pointers land here): cut the
+        // time axis into segments, a reduce launch and an apply launch with 8 steps in flight,
+        // enough segments for about kSegBytesPerSm bytes of loads in flight per SM, each at
+        // least kSegMinSteps long, at most kSegMax (the apply launch folds the earlier maps one
+        // by one).  20 bytes per element instead of 12, but the channels alone would leave the
+        // GPU idle: (7, 3000, 777) 1593 us in one pass.
+        int64_t nseg = 1;
+        if (dtype == kDtypeF32 && !backward && allow_twopass && opt->chunk_mode != 1 &&
+            groups < kRegcarryMinThreadsPerSm * (int64_t)sm_count) {
+            const int64_t want = kSegBytesPerSm * (int64_t)sm_count / (8 * 8 * vec);   // threads
+            nseg = (want + groups - 1) / groups;
+            if (nseg > L / kSegMinSteps) nseg = L / kSegMinSteps;
+            if (nseg > kSegMax) nseg = kSegMax;
+            if (nseg < 2) nseg = 1;
+        }
+        if (nseg > 1) {
+            plan->twopass = 1;
+            plan->segments = (int)nseg;
+            plan->threads = kRegcarryThreads;
+            plan->grid = (groups * nseg + kRegcarryThreads - 1) / kRegcarryThreads;
+            plan->workspace_bytes = (size_t)2 * (size_t)nseg * (size_t)(B * D) * 4u;
+            return LINREC_OK;
+        }
         // Narrower blocks when there are few channel groups, so the grid still
         // covers every SM (at least two blocks per SM where the groups allow).
-        const int64_t groups = B * (D / vec);
         int threads = kRegcarryThreads;
         while (threads > 32 && (groups + threads - 1) / threads < 2 * (int64_t)sm_count) threads /= 2;
         plan->threads = threads;
@@ -486,6 +514,17 @@ linrec_status_t scan_locked(DeviceInfo *di, int dev, const void *a, const void *
     linrec_status_t st = plan_impl(B, L, D, di->sm_count, align, 0, opt, &plan, &vi, false, level == 0, dtype);
     if (st != LINREC_OK) return st;
 
+    if (plan.path == LINREC_PATH_REGCARRY && plan.twopass) {
+        // segmented: the per-segment maps in an array slot of this stream
+        Slot *arrays = workspace(dev, stream, plan.workspace_bytes, level, kSlotArrays);
+        if (!arrays) return LINREC_ERR_WORKSPACE;
+        float *aggA = reinterpret_cast<float *>(arrays->base);
+        float *aggB = aggA + (int64_t)plan.segments * B * D;
+        cudaError_t err = launch_regcarry_segmented(plan.vec, plan.threads, static_cast<const float *>(a),
+                                                    static_cast<const float *>(b), static_cast<float *>(h), B, L, D,
+                                                    plan.segments, h_init, h_last, aggA, aggB, stream);
+        return err == cudaSuccess ? LINREC_OK : LINREC_ERR_LAUNCH;
+    }
     if (plan.path == LINREC_PATH_REGCARRY) {
         cudaError_t err =
             dtype == kDtypeF32

@@ -127,6 +127,126 @@ template <typename T, int V> __device__ __forceinline__ float &lane_of(T &v, int
     return reinterpret_cast<float *>(&v)[i];
 }
 
+// Segmented form, for few channels and long sequences: thread (seg, g) owns channel
+// group g over the steps [seg * seg_len, (seg + 1) * seg_len).  Two launches.
+//  reduce: compose the segment's maps into (A, B) per channel -> aggA / aggB [seg][channel];
+//  apply:  fold the maps of segments 0 .. seg-1 over the state before the sequence (h_init
+//          or 0), in order, into the h entering the segment; replay the segment from it.
+// The first step's slope is dropped without a carried-in state, as in the one-pass kernel.
+template <int V, int P, bool APPLY>
+__global__ void __launch_bounds__(256)
+regcarry_seg_kernel(const float *__restrict__ a, const float *__restrict__ b, float *__restrict__ h,
+                    const long long L, const long long D, const long long groups_per_batch,
+                    const long long n_groups, const long long seg_len, const long long nseg,
+                    const float *h_init, float *h_last, float *__restrict__ aggA, float *__restrict__ aggB)
+{
+    using vec = typename VecT<V>::type;
+    const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (tid >= n_groups * nseg) return;
+    const long long seg = tid / n_groups;     // consecutive threads: consecutive channel groups
+    const long long g = tid - seg * n_groups;
+    const long long bi = g / groups_per_batch;
+    const long long dch = (g - bi * groups_per_batch) * V;
+    const long long n_ch = n_groups * V;      // channels, B * D
+    const long long ch0 = bi * D + dch;       // this thread's first channel, as an index of (B, D)
+    const long long t_begin = seg * seg_len;
+    const long long t_end = (t_begin + seg_len < L) ? t_begin + seg_len : L;
+    const long long off = bi * L * D + dch;
+    const vec *pa = reinterpret_cast<const vec *>(a + off);
+    const vec *pb = reinterpret_cast<const vec *>(b + off);
+    vec *ph = reinterpret_cast<vec *>(h + off);
+    const long long stride = D / V;
+    // extents for the index-checked build
+    const long long n_all = (n_groups / groups_per_batch) * L * D;
+    const long long n_state = n_ch, n_agg = nseg * n_ch;
+    auto ld = [&](const vec *p, const float *base) -> vec {
+#ifdef LINREC_DEBUG
+        if (!inside(p, base, n_all)) {
+            vec v;
+            zero(v);
+            return v;
+        }
+#endif
+        return ld_stream(p);
+    };
+
+    vec ra[P], rb[P];
+#pragma unroll
+    for (int j = 0; j < P; ++j) {
+        if (t_begin + j < t_end) {
+            ra[j] = ld(pa + (t_begin + j) * stride, a);
+            rb[j] = ld(pb + (t_begin + j) * stride, b);
+        }
+    }
+    if (seg == 0 && !h_init) zero(ra[0]);     // h_{-1} = 0 and a_0 is never used
+
+    vec hv, Av;                                // apply: running h; reduce: (Av, hv) is the composed map
+    zero(hv);
+#pragma unroll
+    for (int v = 0; v < V; ++v) lane_of<vec, V>(Av, v) = 1.0f;
+    if (APPLY) {
+        // the h entering the segment: the state before the sequence, then every earlier segment's map
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            float c = (h_init && inside(h_init + ch0 + v, h_init, n_state)) ? h_init[ch0 + v] : 0.0f;
+            for (long long j = 0; j < seg; ++j) {
+                const long long w = j * n_ch + ch0 + v;
+                if (inside(aggA + w, aggA, n_agg) && inside(aggB + w, aggB, n_agg)) c = fmaf(aggA[w], c, aggB[w]);
+            }
+            lane_of<vec, V>(hv, v) = c;
+        }
+    }
+    for (long long t0 = t_begin; t0 < t_end; t0 += P) {
+#pragma unroll
+        for (int j = 0; j < P; ++j) {
+            const long long t = t0 + j;
+            if (t < t_end) {
+                hv = step(ra[j], hv, rb[j]);
+                if (APPLY) {
+                    if (inside(ph + t * stride, h, n_all, true)) st_stream(ph + t * stride, hv);
+                } else {
+#pragma unroll
+                    for (int v = 0; v < V; ++v) lane_of<vec, V>(Av, v) *= lane_of<vec, V>(ra[j], v);
+                }
+                const long long tn = t + P;
+                if (tn < t_end) {
+                    ra[j] = ld(pa + tn * stride, a);
+                    rb[j] = ld(pb + tn * stride, b);
+                }
+            }
+        }
+    }
+    if (!APPLY) {
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            const long long w = seg * n_ch + ch0 + v;
+            if (inside(aggA + w, aggA, n_agg)) aggA[w] = lane_of<vec, V>(Av, v);
+            if (inside(aggB + w, aggB, n_agg)) aggB[w] = lane_of<vec, V>(hv, v);
+        }
+    } else if (h_last && t_end == L) {
+#pragma unroll
+        for (int v = 0; v < V; ++v)
+            if (inside(h_last + ch0 + v, h_last, n_state, true)) h_last[ch0 + v] = lane_of<vec, V>(hv, v);
+    }
+}
+
+template <int V>
+cudaError_t launch_seg_one(int threads, const float *a, const float *b, float *h, int64_t B, int64_t L, int64_t D,
+                           int64_t nseg, const float *h_init, float *h_last, float *aggA, float *aggB,
+                           cudaStream_t stream) {
+    const long long gpb = D / V;
+    const long long n = B * gpb;
+    const long long seg_len = (L + nseg - 1) / nseg;
+    const long long blocks = (n * nseg + threads - 1) / threads;
+    regcarry_seg_kernel<V, 8, false><<<(unsigned)blocks, threads, 0, stream>>>(a, b, h, L, D, gpb, n, seg_len, nseg,
+                                                                                h_init, h_last, aggA, aggB);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    regcarry_seg_kernel<V, 8, true><<<(unsigned)blocks, threads, 0, stream>>>(a, b, h, L, D, gpb, n, seg_len, nseg,
+                                                                               h_init, h_last, aggA, aggB);
+    return cudaGetLastError();
+}
+
 // Gradient, right to left: c_t = a_{t+1} c_{t+1} + g_t; db_t = c_t; da_t = c_t h_{t-1}.
 // The ring holds (g_t, a_{t+1}, h_{t-1}) for the next P steps down.
 template <int V, int P>
@@ -232,6 +352,16 @@ cudaError_t launch_regcarry_backward(int vec, int threads, const float *a, const
     if (vec == 4) return launch_back_one<4>(threads, a, h, g, da, db, B, L, D, h_init, dh_last, dh_init, stream);
     if (vec == 2) return launch_back_one<2>(threads, a, h, g, da, db, B, L, D, h_init, dh_last, dh_init, stream);
     if (vec == 1) return launch_back_one<1>(threads, a, h, g, da, db, B, L, D, h_init, dh_last, dh_init, stream);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_regcarry_segmented(int vec, int threads, const float *a, const float *b, float *h, int64_t B,
+                                      int64_t L, int64_t D, int64_t nseg, const float *h_init, float *h_last,
+                                      float *aggA, float *aggB, cudaStream_t stream) {
+    if (nseg < 1) return cudaErrorInvalidValue;
+    if (vec == 4) return launch_seg_one<4>(threads, a, b, h, B, L, D, nseg, h_init, h_last, aggA, aggB, stream);
+    if (vec == 2) return launch_seg_one<2>(threads, a, b, h, B, L, D, nseg, h_init, h_last, aggA, aggB, stream);
+    if (vec == 1) return launch_seg_one<1>(threads, a, b, h, B, L, D, nseg, h_init, h_last, aggA, aggB, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -203,6 +203,19 @@ def test_plan_wide_slices():
     assert lr.linrec_plan_f32(64, 2048, 1024, sm_count=152, path="regcarry")["path_name"] == "regcarry"
 
 
+def test_plan_segmented_register_path():
+    # few channel groups on the register path (odd D, misaligned pointers): the time axis in
+    # segments of at least 64 steps, at most 256 of them; 2 floats per segment and channel
+    p = lr.linrec_plan_f32(7, 3000, 777, sm_count=152)
+    assert (p["path_name"], p["vec"], p["twopass"], p["segments"]) == ("regcarry", 1, 1, 22)
+    assert p["workspace_bytes"] == 2 * 22 * 7 * 777 * 4
+    assert p["grid"] == -(-7 * 777 * 22 // 256)
+    assert lr.linrec_plan_f32(1, 1000000, 3, sm_count=152)["segments"] == 256
+    assert lr.linrec_plan_f32(1, 100, 3, sm_count=152)["twopass"] == 0          # under 128 steps: one pass
+    assert lr.linrec_plan_f32(256, 128, 4096, sm_count=152)["twopass"] == 0     # many channels: one pass
+    assert lr.linrec_plan_f32_backward(7, 3000, 777, sm_count=152)["twopass"] == 0
+
+
 def test_plan_slice_owner_thresholds():
     # fp32 forward: slice-owner mode from 84 % of the SM count in slices (128 on 152 SMs)
     p = lr.linrec_plan_f32(16, 4096, 256, sm_count=152, resident_ctas=2)

@@ -225,6 +225,34 @@ def test_carry_modes_repeat_bit_identical(mode):
     assert lr.linrec_stream_status() == lr.LINREC_OK
 
 
+@pytest.mark.parametrize("shape", [(7, 3000, 777), (1, 20000, 33), (3, 3001, 130), (4, 300, 1), (2, 5000, 6)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_segmented_register_path(shape):
+    """Few channels the TMA path cannot take (D * 4 not a multiple of 16): the register path cuts the
+    time axis into segments (a reduce launch, then an apply launch folding the earlier segments' maps),
+    with and without a carried state; repeated calls give the same bits."""
+    B, L, D = shape
+    plan = lr.linrec_plan_f32(B, L, D, sm_count=torch.cuda.get_device_properties(DEV).multi_processor_count)
+    assert plan["path_name"] == "regcarry" and plan["twopass"] == 1 and plan["segments"] > 1
+    a, b = inputs.generate(B, L, D, seed=50 + L + D, a_dist="u[0.9,1)", b_dist="n(0,1)")
+    a[:, 0, :] = float("nan")                 # a_0 is never used without a state
+    h64, _ = oracle.f64(a, b)
+    a_d, b_d = a.to(DEV), b.to(DEV)
+    h = run(a_d, b_d)
+    assert_close(h.cpu().numpy(), h64, f"segmented {shape}")
+    assert torch.equal(run(a_d, b_d), h), f"segmented {shape}: bits changed"
+    a[:, 0, :] = 0.5
+    a_d = a.to(DEV)
+    h0 = torch.randn((B, D), generator=torch.Generator().manual_seed(51))
+    hc64, last64 = oracle.f64_carry(a, b, h0.numpy().astype(np.float64))
+    last = torch.full((B, D), float("nan"), device=DEV)
+    h = lr.linrec_scan_f32_carry(a_d, b_d, h_init=h0.to(DEV), h_last=last)
+    torch.cuda.synchronize()
+    assert_close(h.cpu().numpy(), hc64, f"segmented carry {shape}")
+    assert_close(last.cpu().numpy(), last64, f"segmented h_last {shape}")
+    assert lr.linrec_stream_status() == lr.LINREC_OK
+
+
 def test_misaligned_pointers_take_the_scalar_path():
     B, L, D = 2, 300, 64
     a, b = inputs.generate(B, L, D, seed=9, a_dist="u[0.5,1)", b_dist="n(0,1)")
