@@ -166,6 +166,30 @@ void default_groups_16(int64_t slices, int sm_count, bool own, bool twopass, int
     }
 }
 
+// Wide slices (fp32, L >= kWideMinSteps, the dispatcher's own tile): the widest of 256
+// or 128 channels whose slice count splits evenly over at least kWideMinGridPct % of the
+// SMs, one CTA of 512 threads per SM; returns that width (0: none) and the grid.  Every
+// CTA then owns the same number of slices, and each box row is 1 or 0.5 KB of
+// contiguous memory.  Measured on GB300 (us per call, the previous choice -> this one):
+// (64, 2048, 1024) 260 (register path) -> 229 ({128, 64}, 128 CTAs x 4 slices), (128,
+// 1024, 1024) 249 -> 232 ({256, 32}, 128 x 4), (8, 4096, 4096) 261 -> 234 ({256, 32}, 128
+// x 1), (32, 1024, 4096) 247 -> 229, (256, 1024, 256) 133 -> 118, (32, 512, 4096) 125 ->
+// 117, (64, 256, 2048) 65 -> 61.  Without an even split the wide tiles lose ((64, 512,
+// 4096): 1024 slices on 152 CTAs, 265 against 246 on the register path).  The gradient
+// kernel likewise: (64, 2048, 1024) 419 -> 395 ({128, 64} x 4), (128, 1024, 1024) 448 -> 391.
+int wide_slices(int64_t B, int64_t L, int64_t D, int sm_count, int64_t *grid) {
+    if (L < kWideMinSteps) return 0;
+    for (int td : {256, 128}) {
+        const int64_t slices = B * ((D + td - 1) / td);
+        const int64_t k = (slices + sm_count - 1) / sm_count;        // slices per CTA
+        if (slices % k == 0 && (slices / k) * 100 >= (int64_t)kWideMinGridPct * sm_count) {
+            *grid = slices / k;
+            return td;
+        }
+    }
+    return 0;
+}
+
 void default_tile(int64_t B, int64_t L, int64_t D, int sm_count, bool own, bool twopass, bool backward, int dtype,
                   int *tile_d, int *tile_t, int *stages) {
     if (dtype != kDtypeF32) {
@@ -222,40 +246,22 @@ linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int ali
     if (backward && dtype != kDtypeF32) return LINREC_ERR_INVALID_VALUE;
     const bool tma_ok = align_bytes >= 16 && (D * eb) % 16 == 0 && D <= INT32_MAX && B <= INT32_MAX &&
                         L <= (int64_t)INT32_MAX - 1024;
-    // The register path when the channels alone keep enough loads in flight: a
+    // 1. Wide slices, ahead of everything else (see wide_slices).
+    int64_t wide_grid = 0;
+    const int wide_td = (dtype == kDtypeF32 && opt->chunk_mode == 0 && opt->tile_d == 0 && opt->tile_t == 0 &&
+                         (opt->path == LINREC_PATH_AUTO || opt->path == LINREC_PATH_CHUNKED) && tma_ok)
+                            ? wide_slices(B, L, D, sm_count, &wide_grid)
+                            : 0;
+    // 2. The register path when the channels alone keep enough loads in flight: a
     // forward scan with at least kRegcarryMinThreadsPerSm threads of 16 bytes of
     // channels per SM.  Measured on GB300, fp32: (256, 128, 4096) 6922 vs 6007 GB/s
-    // for the chunked kernel, (64, 2048, 1024) 6193 vs 5976; at 32768 channels it
-    // loses (4361 vs 5722 on (8, 4096, 4096)).  16-bit storage: only below 256 steps,
-    // where the chunked kernel cannot use its 256-step tiles ((256, 128, 4096)
-    // bfloat16 6391 vs 4638; (64, 512, 4096) 6309 vs 6574 for the chunked kernel).
-    // Otherwise the TMA-staged chunked kernel whenever its copies are legal; the
-    // register path also takes misaligned pointers and D % 4 != 0.
-    // Wide slices first (fp32, L >= kWideMinSteps, the dispatcher's tile): the
-    // widest of 256 or 128 channels whose slice count splits evenly into at least
-    // kWideMinGridPct % of the SMs, one CTA of 512 threads per SM.  Every CTA then owns
-    // the same number of slices, and each box row is 1 or 0.5 KB of contiguous memory.
-    // Measured on GB300 (us per call, the previous choice -> this one): (64, 2048, 1024)
-    // 260 (register path) -> 229 ({128, 64}, 128 CTAs x 4 slices), (128, 1024, 1024)
-    // 249 -> 232 ({256, 32}, 128 x 4), (8, 4096, 4096) 261 -> 234 ({256, 32}, 128 x 1),
-    // (32, 1024, 4096) 247 -> 229, (256, 1024, 256) 133 -> 118, (32, 512, 4096) 125 -> 117,
-    // (64, 256, 2048) 65 -> 61.  Without an even split the wide tiles lose ((64, 512, 4096):
-    // 1024 slices on 152 CTAs, 265 against 246 on the register path).  The gradient kernel likewise:
-    // (64, 2048, 1024) 419 -> 395 ({128, 64} x 4), (128, 1024, 1024) 448 -> 391.
-    int wide_td = 0;
-    int64_t wide_grid = 0;
-    if (dtype == kDtypeF32 && opt->chunk_mode == 0 && opt->tile_d == 0 && opt->tile_t == 0 &&
-        (opt->path == LINREC_PATH_AUTO || opt->path == LINREC_PATH_CHUNKED) && tma_ok && L >= kWideMinSteps) {
-        for (int td : {256, 128}) {
-            const int64_t slices = B * ((D + td - 1) / td);
-            const int64_t k = (slices + sm_count - 1) / sm_count;        // slices per CTA
-            if (slices % k == 0 && (slices / k) * 100 >= (int64_t)kWideMinGridPct * sm_count) {
-                wide_td = td;
-                wide_grid = slices / k;
-                break;
-            }
-        }
-    }
+    // for the chunked kernel; at 32768 channels it loses (4361 vs 5722 on (8, 4096,
+    // 4096)).  16-bit storage: only below 256 steps, where the chunked kernel cannot use
+    // its 256-step tiles ((256, 128, 4096) bfloat16 6391 vs 4638; (64, 512, 4096) 6309
+    // vs 6574 for the chunked kernel).
+    // 3. Otherwise the TMA-staged chunked kernel whenever its copies are legal; the
+    // register path also takes misaligned pointers and rows that are not a multiple of
+    // 16 bytes.
     int path = opt->path;
     if (path == LINREC_PATH_AUTO) {
         const int lanes = 16 / eb;            // channels in 16 bytes
