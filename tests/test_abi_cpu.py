@@ -433,3 +433,43 @@ def test_bdl_argument_checks(L):
     assert f(None, base, base + 2 * n, B, D, Lx, None) == lr.LINREC_ERR_INVALID_VALUE
     assert f(base, base, base + n, B, -1, Lx, None) == lr.LINREC_ERR_INVALID_VALUE
     assert f(None, None, None, B, D, 0, None) == lr.LINREC_OK
+
+
+def test_plan_invariants_over_a_grid():
+    """Every plan the dispatcher returns over a grid of shapes, storages and options is consistent:
+    the tile is a compiled one with threads = tile_d / vec * segments, the grid covers the work units
+    without exceeding them, the tile count is slices x chunks, and the workspace matches the mode."""
+    import itertools
+    Bs, Ls, Ds = [1, 3, 16, 40, 128], [1, 100, 300, 2048, 1 << 16], [1, 6, 8, 33, 64, 256, 777, 1024, 4096]
+    planners = [(lr.linrec_plan_f32, 4), (lr.linrec_plan_16, 2), (lr.linrec_plan_f32_backward, 4)]
+    n_plans = 0
+    for (B, L, D), (planner, eb), kw in itertools.product(
+            itertools.product(Bs, Ls, Ds), planners,
+            ({}, {"resident_ctas": 2}, {"align_bytes": 4}, {"path": "chunked"})):
+        try:
+            p = planner(B, L, D, sm_count=152, **kw)
+        except lr.LinrecError:
+            assert kw.get("path") == "chunked" or kw.get("align_bytes") == 4, (B, L, D, kw)
+            continue
+        n_plans += 1
+        if p["path_name"] == "regcarry":
+            assert D % p["vec"] == 0 and p["grid"] >= 1
+            groups = B * (D // p["vec"])
+            if p["twopass"]:                   # segmented: every (segment, group) a thread
+                assert eb == 4 and 2 <= p["segments"] <= 256 and L // p["segments"] >= 64
+                assert p["grid"] * p["threads"] >= groups * p["segments"]
+                assert p["workspace_bytes"] == 2 * p["segments"] * B * D * 4
+            else:
+                assert p["grid"] * p["threads"] >= groups
+            continue
+        assert p["path_name"] == "chunked" and (D * eb) % 16 == 0
+        assert p["threads"] == p["tile_d"] // p["vec"] * p["segments"] and p["tile_t"] % p["segments"] == 0
+        slices = B * -(-D // p["tile_d"])
+        assert p["chunks"] == -(-L // p["tile_t"]) and p["n_tiles"] == slices * p["chunks"]
+        units = slices if not (p["lookback"] or p["twopass"] or p["blocks"]) else p["n_tiles"]
+        assert 1 <= p["grid"] <= units
+        if p["lookback"]:
+            assert p["workspace_bytes"] == 256 + 24 * p["n_tiles"] * p["tile_d"]
+        elif not p["twopass"] and not p["blocks"]:
+            assert p["workspace_bytes"] == 256
+    assert n_plans > 1000
