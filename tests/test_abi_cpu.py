@@ -473,3 +473,52 @@ def test_plan_invariants_over_a_grid():
         elif not p["twopass"] and not p["blocks"]:
             assert p["workspace_bytes"] == 256
     assert n_plans > 1000
+
+
+def test_gradient_host_and_noalloc_argument_checks(L):
+    """The gradient, host-buffer and no-allocation entries reject bad sizes, null pointers, overlaps
+    and (no-allocation entry) unaligned pointers before any CUDA call; fake addresses, never read."""
+    vp = ctypes.c_void_p
+    B, Lx, D = 2, 100, 8
+    n = B * Lx * D * 4
+    base = 1 << 36
+    a, h, g, da, db = (base + k * n for k in range(5))
+    st1, st2, st3 = base + 5 * n, base + 5 * n + 1024, base + 5 * n + 2048
+    bw = L.linrec_scan_f32_backward_ex
+
+    def grad(*args, **over):
+        kw = dict(a=a, h=h, g=g, da=da, db=db, B=B, L=Lx, D=D, h_init=None, dh_last=None, dh_init=None)
+        kw.update(over)
+        return bw(kw["a"], kw["h"], kw["g"], kw["da"], kw["db"], kw["B"], kw["L"], kw["D"],
+                  kw["h_init"], kw["dh_last"], kw["dh_init"], None, None)
+
+    assert grad(B=-1) == lr.LINREC_ERR_INVALID_VALUE
+    assert grad(a=None, h=None, g=None, da=None, db=None, L=0) == lr.LINREC_OK
+    for missing in ("a", "g", "db"):
+        assert grad(**{missing: None}) == lr.LINREC_ERR_INVALID_VALUE, missing
+    assert grad(h=None) == lr.LINREC_ERR_INVALID_VALUE                      # da wanted without h
+    assert grad(da=a + 4) == lr.LINREC_ERR_ALIAS                            # da inside a
+    assert grad(db=h + n - 4) == lr.LINREC_ERR_ALIAS                        # db overlaps the end of h
+    assert grad(db=da + 8) == lr.LINREC_ERR_ALIAS                           # the two outputs overlap
+    assert grad(h_init=st1, dh_last=st2, dh_init=st2 + 4) == lr.LINREC_ERR_ALIAS
+    assert grad(h_init=st1, dh_init=db + 16) == lr.LINREC_ERR_ALIAS         # dh_init inside db
+
+    host = L.linrec_scan_f32_host
+    b = h
+    assert host(a, b, da, -1, Lx, D, None) == lr.LINREC_ERR_INVALID_VALUE
+    assert host(None, None, None, B, Lx, 0, None) == lr.LINREC_OK
+    assert host(a, None, da, B, Lx, D, None) == lr.LINREC_ERR_INVALID_VALUE
+    assert host(a, b, a + 12, B, Lx, D, None) == lr.LINREC_ERR_ALIAS
+    assert host(a, b, b - n + 4, B, Lx, D, None) == lr.LINREC_ERR_ALIAS
+    assert host(16, 32, 64, 1 << 20, 1 << 20, 1 << 22, None) == lr.LINREC_ERR_INVALID_VALUE
+
+    na = L.linrec_scan_f32_noalloc
+    na.argtypes = [vp, vp, vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vp, vp]
+    na.restype = ctypes.c_int
+    assert na(a, b, da, B, -Lx, D, None, None) == lr.LINREC_ERR_INVALID_VALUE
+    assert na(None, None, None, 0, Lx, D, None, None) == lr.LINREC_OK
+    assert na(a, b, None, B, Lx, D, None, None) == lr.LINREC_ERR_INVALID_VALUE
+    assert na(a, b, b + 16, B, Lx, D, None, None) == lr.LINREC_ERR_ALIAS
+    assert na(a + 4, b, da, B, Lx, D, None, None) == lr.LINREC_ERR_INVALID_VALUE   # not 16-byte aligned
+    assert na(a, b, da, B, Lx, 6, None, None) == lr.LINREC_ERR_INVALID_VALUE      # D not a multiple of 4
+    assert na(16, 32, 64, 1 << 20, 1 << 20, 1 << 22, None, None) == lr.LINREC_ERR_INVALID_VALUE
