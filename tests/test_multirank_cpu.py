@@ -55,3 +55,45 @@ def test_single_process_defaults(monkeypatch):
     assert bench.dist_env() == (0, 1, 0)
     assert bench.max_over_ranks(3.25) == 3.25
     assert bench.aggregate_gbs(12, 1, 1, 1e-9) == pytest.approx(12.0)
+
+
+def _reference_arm(extra, env_over=None):
+    import json
+    import subprocess
+    import sys
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    env.update(env_over or {})
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "3", "--warmup", "3",
+                        "--ref-seconds", "3"] + extra, cwd=root, env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [json.loads(x) for x in r.stdout.splitlines() if x.startswith("{")]
+    return lines
+
+
+@pytest.mark.parametrize("extra", [["--workload", "pages"], ["--workload", "tiny", "--dtype", "bf16"]],
+                         ids=("pages-f32", "tiny-bf16"))
+def test_reference_arm_line(extra):
+    """The reference arm (the oracle on host cores) prints one JSON line with the contract's keys, on a
+    bounded sample of the named workload."""
+    lines = _reference_arm(extra)
+    assert len(lines) == 1
+    line = lines[0]
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["steps"] == 3 and line["warmup"] == 3 and line["n_gpus"] == 1
+    assert line["value"] > 0 and line["higher_is_better"] is True
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"] == {"value": line["value"], "unit": line["unit"], "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    assert line["config"]["workload"]
+
+
+def test_reference_arm_other_ranks_do_no_work():
+    """Under torchrun only rank 0 runs the reference arm; the others exit 0 and print nothing."""
+    lines = _reference_arm(["--workload", "pages"],
+                           {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
+    assert lines == []
