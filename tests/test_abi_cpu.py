@@ -522,3 +522,25 @@ def test_gradient_host_and_noalloc_argument_checks(L):
     assert na(a + 4, b, da, B, Lx, D, None, None) == lr.LINREC_ERR_INVALID_VALUE   # not 16-byte aligned
     assert na(a, b, da, B, Lx, 6, None, None) == lr.LINREC_ERR_INVALID_VALUE      # D not a multiple of 4
     assert na(16, 32, 64, 1 << 20, 1 << 20, 1 << 22, None, None) == lr.LINREC_ERR_INVALID_VALUE
+
+
+def test_no_cpu_fallback():
+    """CPU tensors are refused rather than scanned on the host, and a missing library is an error that
+    names the build step, never a silent fallback (checked in a fresh interpreter)."""
+    import subprocess
+    import sys
+    import torch
+    a, b = torch.rand(1, 8, 4), torch.randn(1, 8, 4)
+    for call in (lambda: lr.linrec_scan_f32(a, b), lambda: lr.linrec_scan_f32_ex(a, b, path="regcarry"),
+                 lambda: lr.linrec_scan_f32_backward(a, a, b),
+                 lambda: lr.linrec_scan_bf16_ex(a.bfloat16(), b.bfloat16()),
+                 lambda: lr.linrec_scan_f32_bdl_ex(a, b)):
+        with pytest.raises(ValueError, match="CUDA tensor"):
+            call()
+    code = ("import linear_recurrence_scan_fp32_gb300 as lr\n"
+            "try:\n    lr.linrec_plan_f32(1, 64, 32)\nexcept lr.LinrecError as e:\n    print('refused:', e)\n")
+    env = dict(os.environ, LINREC_LIBRARY=os.path.join(ROOT, "no_such_dir", "liblinrec.so"))
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert "refused:" in r.stdout and "missing" in r.stdout and "no fallback" in r.stdout, r.stdout
