@@ -544,3 +544,23 @@ def test_no_cpu_fallback():
                        timeout=300)
     assert r.returncode == 0, r.stderr[-2000:]
     assert "refused:" in r.stdout and "missing" in r.stdout and "no fallback" in r.stdout, r.stdout
+
+
+@pytest.mark.parametrize("compiler", [["gcc", "-std=c99", "-pedantic"], ["g++", "-std=c++17", "-x", "c++"]],
+                         ids=("c99", "c++17"))
+def test_header_compiles_and_links_from_c(L, compiler, tmp_path):
+    """A plain C (and C++) consumer of include/linrec.h, linked against liblinrec.so: the header is valid
+    on its own and its declarations match what the library exports (tests/c/abi_check.c)."""
+    import shutil
+    import subprocess
+    if shutil.which(compiler[0]) is None:
+        pytest.skip(f"{compiler[0]} not installed")
+    libdir = os.path.dirname(lr.LIB_PATH)
+    exe = str(tmp_path / "abi_check")
+    cmd = compiler + ["-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+                      os.path.join(ROOT, "tests", "c", "abi_check.c"), "-L", libdir, "-llinrec",
+                      f"-Wl,-rpath,{libdir}", "-o", exe]
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-3000:]
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and "abi_check: ok" in r.stdout, r.stdout + r.stderr
