@@ -579,3 +579,28 @@ def test_composition_order(oracle_lib):
     assert excess(_blocked_scan(a, b, 16, _combine_right), h64, 1e-12, 1e-12) <= 0
     assert excess(_blocked_scan(a, b, 16, _combine_reversed), h64) > 0
     assert excess(_blocked_scan(a, b, 16, _combine_stale_a), h64) > 0
+
+
+# ---------------------------------------------------------------------------
+# the comparison every parity test uses
+# ---------------------------------------------------------------------------
+
+def test_tolerance_helper_accepts_the_bound_and_nothing_past_it():
+    want = np.array([0.0, 1.0, -3.0, 1e4, -2.5e-7])
+    at_bound = want + (1e-4 + 1e-4 * np.abs(want)) * np.array([1, -1, 1, -1, 1]) * (1 - 1e-12)
+    assert_close(at_bound, want, "on the bound")
+    assert excess(want, want) < 0
+    for k in range(want.size):                       # any single element just past the bound fails
+        bad = at_bound.copy()
+        bad[k] = want[k] + 1.01 * (1e-4 + 1e-4 * abs(want[k]))
+        with pytest.raises(AssertionError):
+            assert_close(bad, want, f"element {k} past the bound")
+    for poison in (np.nan, np.inf, -np.inf):         # non-finite output never passes
+        bad = want.copy()
+        bad[2] = poison
+        assert excess(bad, want) == np.inf
+        with pytest.raises(AssertionError):
+            assert_close(bad, want, "non-finite")
+    with pytest.raises(ValueError):                  # a shape mismatch is an error, not a broadcast
+        excess(want[:4], want)
+    assert excess(np.empty((0, 3)), np.empty((0, 3))) == -np.inf
