@@ -114,12 +114,17 @@ def aggregate_gbs(bytes_per_rank_step: int, world: int, steps: int, seconds: flo
 # ---------------------------------------------------------------------------
 
 class ClockSampler:
-    def __init__(self, index: int, period_ms: int = 100):
+    """nvidia-smi sampling of one GPU's clocks, power and throttle reasons every period_ms.
+    start() before the warm-up and wait_first() until the first sample is written, so that
+    the warm-up runs straight into the timed region with no idle gap; stop() after it."""
+
+    def __init__(self, index: int, period_ms: int = 20):
         self.index, self.period_ms = index, period_ms
         self.proc = None
         self.path = None
+        self.fh = None
 
-    def __enter__(self):
+    def start(self):
         try:
             fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
             self.fh = os.fdopen(fd, "w")
@@ -130,7 +135,17 @@ class ClockSampler:
             self.proc = None
         return self
 
-    def __exit__(self, *exc):
+    def wait_first(self, timeout_s: float = 2.0):
+        """Block until nvidia-smi has written its first sample (or timeout_s has passed)."""
+        if self.proc is None:
+            return
+        t_end = time.perf_counter() + timeout_s
+        while time.perf_counter() < t_end and self.proc.poll() is None:
+            if os.path.getsize(self.path) > 0:
+                return
+            time.sleep(0.01)
+
+    def stop(self):
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -140,6 +155,8 @@ class ClockSampler:
             self.fh.close()
 
     def summary(self):
+        window = (f"nvidia-smi every {self.period_ms} ms from before the warm-up to the end of the timed "
+                  "region (the warm-up runs straight into the timed region)")
         if self.proc is None or not self.path:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
         rows = []
@@ -150,13 +167,14 @@ class ClockSampler:
                     rows.append(parts)
         os.unlink(self.path)
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "window": window}
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
         return {"sm_mhz": statistics.median(float(r[1]) for r in rows),
                 "sm_max_mhz": max(float(r[2]) for r in rows),
-                "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit()) if rows else None,
-                "reasons": reasons, "samples": len(rows)}
+                "power_w_max": max(power) if power else None,
+                "reasons": reasons, "samples": len(rows), "window": window}
 
 
 # ---------------------------------------------------------------------------
@@ -203,29 +221,74 @@ def committed_traffic(kernel: str, workload: str):
 # arms
 # ---------------------------------------------------------------------------
 
+class OracleTimer:
+    """Repeated calls of one form of the oracle over fixed inputs, writing into one output array
+    allocated up front, so that repetitions time the scan rather than the page faults of a fresh
+    output.  The bench line's cpu_baseline leg and the reference arm both time the oracle
+    through this class.  form: "f64" (the definition in double precision) or "f32seq" (the
+    fp32 twin); 16-bit storage: the oracle's decode of the words, then its fp64 scan."""
+
+    def __init__(self, a, b, dtype: str = "f32", form: str = "f64", nthreads: int = 0):
+        import oracle
+        oracle.build()
+        self.oracle, self.dtype, self.form, self.nthreads = oracle, dtype, form, nthreads
+        self.a, self.b = a, b
+        self.used = nthreads
+        self.out = None
+        if dtype == "f32":
+            self.out = np.empty(np.shape(a), dtype=np.float64 if form == "f64" else np.float32)
+
+    def __call__(self):
+        o = self.oracle
+        if self.dtype != "f32":
+            h, _ = o.f64_16(self.dtype, self.a, self.b, nthreads=self.nthreads)
+            return h
+        fn = o.f64 if self.form == "f64" else o.f32seq
+        h, self.used = fn(self.a, self.b, nthreads=self.nthreads, out=self.out)
+        return h
+
+    def repeat(self, budget_s: float, min_reps: int = 1):
+        """Call until budget_s seconds of calls (at least min_reps); returns (reps, seconds, last h)."""
+        reps, t_total, h = 0, 0.0, None
+        while (t_total < budget_s or reps < min_reps) and reps < 100000:
+            t0 = time.perf_counter()
+            h = self()
+            t_total += time.perf_counter() - t0
+            reps += 1
+        return reps, t_total, h
+
+
+def _rate(nbytes: int, numel: int, reps: int, seconds: float, cores: int) -> dict:
+    return {"value": round(nbytes * reps / seconds / 1e9, 3), "unit": UNIT, "cores": cores,
+            "elements_per_s": round(numel * reps / seconds, 1), "ms_per_workload": round(1e3 * seconds / reps, 3),
+            "repetitions": reps}
+
+
 def cpu_baseline(a, b, w, budget_s: float = 10.0, dtype: str = "f32", h_gpu=None):
-    """The oracle as it stands, all host cores, repeated over the full workload for ~budget_s.
-    16-bit storage: the oracle's decode of the stored words, then its fp64 scan (one thread
-    decodes; the scan runs on all cores).  Returns (baseline, parity): parity compares h_gpu,
-    the output of the timed GPU run, with the oracle's result, element by element."""
+    """The oracle as it stands on the host cores, each form over the full workload with its
+    output allocated once: the fp64 definition on all cores (the line's value) and on one core,
+    and the fp32 twin on all cores (16-bit storage: decode + fp64 scan on all cores only).
+    Returns (baseline, parity): parity compares h_gpu, the output of the timed GPU run, with
+    the fp64 oracle's result, element by element."""
     import oracle
     oracle.build()
     threads = oracle.hardware_threads()
-    reps, t_total = 0, 0.0
-    used = threads
     nbytes = bytes_per_step(w, "forward", dtype)
-    h64 = None
-    while t_total < budget_s and reps < 100000:
-        t0 = time.perf_counter()
-        if dtype == "f32":
-            h64, used = oracle.f64(a, b, nthreads=threads)
-        else:
-            h64, _ = oracle.f64_16(dtype, a, b)
-        t_total += time.perf_counter() - t0
-        reps += 1
+    t64 = OracleTimer(a, b, dtype, "f64", threads)
+    reps, secs, h64 = t64.repeat(budget_s)
     what = "fp64 sequential oracle" if dtype == "f32" else f"oracle {dtype} decode + fp64 scan"
-    base = {"value": nbytes * reps / t_total / 1e9, "unit": UNIT, "cores": used, "kind": "oracle",
-            "sample": f"full {w.name} workload {w.shape}, {what}, {reps} repetitions, {t_total:.1f} s"}
+    base = {**_rate(nbytes, w.numel, reps, secs, t64.used), "kind": "oracle",
+            "sample": f"full {w.name} workload {w.shape}, {what}, all host cores, {reps} repetitions, "
+                      f"{secs:.1f} s, output allocated once",
+            "method": "the same timer as the reference arm (OracleTimer): one output array per form, "
+                      "run before the pinned host buffers of the e2e leg exist"}
+    if dtype == "f32":
+        one = OracleTimer(a, b, dtype, "f64", 1)
+        r1, s1, _ = one.repeat(budget_s / 2)
+        base["fp64_1core"] = _rate(nbytes, w.numel, r1, s1, one.used)
+        f32 = OracleTimer(a, b, dtype, "f32seq", threads)
+        r2, s2, _ = f32.repeat(budget_s / 2)
+        base["f32seq_all_cores"] = _rate(nbytes, w.numel, r2, s2, f32.used)
     parity = None
     if h_gpu is not None and h64 is not None:
         # 16-bit storage: the output words, decoded by the oracle's own definition of the format
@@ -270,18 +333,9 @@ def run_reference(args):
     else:
         a, b = a.numpy(), b.numpy()
     threads = oracle.hardware_threads()
-    used = threads
-
-    def run_oracle(x, y):
-        nonlocal used
-        if args.dtype == "f32":
-            _, used = oracle.f64(x, y, nthreads=threads)
-        else:
-            oracle.f64_16(args.dtype, x, y)
-
     # size each step's sample so that warm-up + timed steps take about --ref-seconds
     t0 = time.perf_counter()
-    run_oracle(a, b)
+    OracleTimer(a, b, args.dtype, "f64", threads)()
     t_full = time.perf_counter() - t0
     per_step = args.ref_seconds / (args.steps + args.warmup)
     nb = max(1, min(w.B, int(w.B * per_step / t_full)))
@@ -289,14 +343,16 @@ def run_reference(args):
     a_s = np.ascontiguousarray(a[:nb, :nl])
     b_s = np.ascontiguousarray(b[:nb, :nl])
     sample_bytes = 3 * STORAGE_BYTES[args.dtype] * a_s.size
+    timer = OracleTimer(a_s, b_s, args.dtype, "f64", threads)   # the cpu_baseline leg's timer
     for _ in range(args.warmup):
-        run_oracle(a_s, b_s)
+        timer()
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        run_oracle(a_s, b_s)
+        timer()
         times.append(time.perf_counter() - t0)
     total = sum(times)
+    used = timer.used
     value = sample_bytes * args.steps / total / 1e9
     line = {
         "impl": "reference", "metric": metric_for(w, "forward", args.dtype, args.layout), "value": round(value, 3), "unit": UNIT,
@@ -400,34 +456,35 @@ def run_ours(args):
         else:
             lr.linrec_scan_f32(a, b, h, stream=stream)
 
+    # The clock sampler starts first; once it has written a sample the W warm-up calls run
+    # straight into the timed region (a pause between them measured 2-3 us per call slower
+    # at K = 20 on the pages shape), with only the synchronisation and barrier between.
+    clocks = ClockSampler(local).start()
+    clocks.wait_first()
     for _ in range(args.warmup):
         step()
-    torch.cuda.synchronize()
-    if lr.linrec_stream_status(stream) != lr.LINREC_OK:
-        raise SystemExit("device-side failure during warm-up")
-
     # Two events around the K steps, nothing between them: the chunked kernels are
     # launched as programmatic dependents, so a call may be scheduled while the one
     # before it drains (it waits for it before touching memory); an event recorded
     # between two launches would cut that overlap.
     e_start = torch.cuda.Event(enable_timing=True)
     e_end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clocks:
-        time.sleep(0.3)   # let the sampler start before the timed region
-        t0 = time.perf_counter()
-        e_start.record(stream)
-        for i in range(args.steps):
-            step()
-        e_end.record(stream)
         torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
-        wall = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    e_start.record(stream)
+    for i in range(args.steps):
+        step()
+    e_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    wall = time.perf_counter() - t0
+    clocks.stop()
     elapsed_ms = e_start.elapsed_time(e_end)
-    status = lr.linrec_stream_status(stream)
+    status = lr.linrec_stream_status(stream)          # covers the warm-up and the timed calls
     if status != lr.LINREC_OK:
         raise SystemExit(f"device-side failure: {lr.linrec_status_string(status)}")
     seconds = max_over_ranks(elapsed_ms / 1e3, dev)
@@ -462,6 +519,26 @@ def run_ours(args):
         copy_gbs[name] = round(8 * n_copy * reps / (e0.elapsed_time(e1) / 1e3) / 1e9, 1)
     del src, dst
     ceiling = max(copy_gbs.values())
+
+    # the CPU oracle first, before the e2e leg pins host memory
+    cpu = None
+    parity = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        if args.op == "backward":
+            cpu = cpu_baseline_backward(a_cpu.numpy(), h.cpu().numpy(), g_cpu.numpy(), w, nbytes,
+                                        budget_s=args.cpu_seconds)
+        else:
+            # the oracle scans (B, L, D); the (B, D, L) values are the same numbers transposed
+            ca, cb = (a_cpu.transpose(1, 2).contiguous(), b_cpu.transpose(1, 2).contiguous()) if bdl \
+                else (a_cpu, b_cpu)
+            hc = h.cpu()
+            if bdl:
+                hc = hc.transpose(1, 2).contiguous()
+            if args.dtype == "f32":
+                cpu, parity = cpu_baseline(ca.numpy(), cb.numpy(), w, budget_s=args.cpu_seconds, h_gpu=hc.numpy())
+            else:
+                words = hc.view(torch.int16).numpy().view(np.uint16)
+                cpu, parity = cpu_baseline(ca, cb, w, budget_s=args.cpu_seconds, dtype=args.dtype, h_gpu=words)
 
     # end to end through the public API: pinned host inputs in, result out, every step
     e2e = None
@@ -499,25 +576,6 @@ def run_ours(args):
         e2e = {"value": round(aggregate_gbs(nbytes, world, e_steps, e_sec), 3), "unit": UNIT,
                "h2d_bytes_per_step": 2 * eb * w.numel, "d2h_bytes_per_step": eb * w.numel, "steps": e_steps,
                "path": e2e_path}
-
-    cpu = None
-    parity = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        if args.op == "backward":
-            cpu = cpu_baseline_backward(a_cpu.numpy(), h.cpu().numpy(), g_cpu.numpy(), w, nbytes,
-                                        budget_s=args.cpu_seconds)
-        else:
-            # the oracle scans (B, L, D); the (B, D, L) values are the same numbers transposed
-            ca, cb = (a_cpu.transpose(1, 2).contiguous(), b_cpu.transpose(1, 2).contiguous()) if bdl \
-                else (a_cpu, b_cpu)
-            hc = h.cpu()
-            if bdl:
-                hc = hc.transpose(1, 2).contiguous()
-            if args.dtype == "f32":
-                cpu, parity = cpu_baseline(ca.numpy(), cb.numpy(), w, budget_s=args.cpu_seconds, h_gpu=hc.numpy())
-            else:
-                words = hc.view(torch.int16).numpy().view(np.uint16)
-                cpu, parity = cpu_baseline(ca, cb, w, budget_s=args.cpu_seconds, dtype=args.dtype, h_gpu=words)
 
     if rank == 0:
         clk = clocks.summary()

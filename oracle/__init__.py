@@ -100,13 +100,22 @@ def _ptr(x, ctype):
     return x.ctypes.data_as(ctypes.POINTER(ctype))
 
 
-def f64(a, b, nthreads: int = 0, lib=None):
-    """h in float64 by the definition; returns (h, threads_used)."""
+def _out(out, shape, dtype):
+    """A caller's output array (reused across timed repetitions), or a new one."""
+    if out is None:
+        return np.empty(shape, dtype=dtype)
+    if out.shape != shape or out.dtype != dtype or not out.flags.c_contiguous:
+        raise ValueError(f"out must be a contiguous {np.dtype(dtype).name} array of shape {shape}")
+    return out
+
+
+def f64(a, b, nthreads: int = 0, lib=None, out=None):
+    """h in float64 by the definition; returns (h, threads_used).  out: an array to write h into."""
     a, b = _as_f32(a), _as_f32(b)
     if a.shape != b.shape:
         raise ValueError("a and b differ in shape")
     lib = lib or load()
-    h = np.empty(a.shape, dtype=np.float64)
+    h = _out(out, a.shape, np.float64)
     n = lib.linrec_oracle_f64(_ptr(a, ctypes.c_float), _ptr(b, ctypes.c_float),
                               _ptr(h, ctypes.c_double), *a.shape, nthreads)
     if n < 0:
@@ -114,11 +123,11 @@ def f64(a, b, nthreads: int = 0, lib=None):
     return h, n
 
 
-def f32seq(a, b, nthreads: int = 0, lib=None):
-    """h in fp32 with one rounded multiply and one rounded add per step."""
+def f32seq(a, b, nthreads: int = 0, lib=None, out=None):
+    """h in fp32 with one rounded multiply and one rounded add per step; returns (h, threads_used)."""
     a, b = _as_f32(a), _as_f32(b)
     lib = lib or load()
-    h = np.empty(a.shape, dtype=np.float32)
+    h = _out(out, a.shape, np.float32)
     n = lib.linrec_oracle_f32seq(_ptr(a, ctypes.c_float), _ptr(b, ctypes.c_float),
                                  _ptr(h, ctypes.c_float), *a.shape, nthreads)
     if n < 0:
