@@ -105,8 +105,14 @@ typedef struct {
                             (the gradient runs them in reversed chunk order); 4 = blocks (forward
                             only): one launch; a CTA composes a block of `group` consecutive
                             chunks of a slice, joins the blocks of the slice by the decoupled
-                            look-back, then re-reads the block (from L2) and writes h; 0 = the
-                            dispatcher's choice */
+                            look-back, then re-reads the block (from L2) and writes h; 5 = chain
+                            (forward only): one launch that reads and writes every element once;
+                            worker CTAs compose each chunk as it lands and publish its aggregate
+                            before they finish the chunk before it, while resolver CTAs fold each
+                            slice's aggregates in chunk order into the running h entering every
+                            chunk (the same values, bit for bit, as mode 1); it takes at most 128
+                            slices of 32 channels (B * ceil(D/32); 64 in 16-bit storage), more
+                            return LINREC_ERR_INVALID_VALUE; 0 = the dispatcher's choice */
     unsigned int *d_status; /* device word (may be NULL): the kernel ORs 1 << linrec_status_t
                                into it on a device-side failure; otherwise the stream's own word
                                is used (read it with linrec_stream_status) */
@@ -190,8 +196,10 @@ linrec_status_t linrec_scan_f32_backward_ex(const float *a, const float *h, cons
  * linrec_scan_f32_host -- the scan on HOST buffers a, b (read) and h (written),
  * row-major (B, L, D) like the device entry points.
  *  - When a, b and h are all page-locked host memory the device can address
- *    (cudaHostAlloc, cudaHostRegister), the kernels read and write them in
- *    place over the host link: no copies, no device memory.
+ *    (cudaHostAlloc, cudaHostRegister), every byte of each, the kernels read
+ *    and write them in place over the host link: no copies, no device memory.
+ *    A buffer only partly page-locked (say a registered prefix of a larger
+ *    block) is moved by the copy pipeline below instead.
  *  - Otherwise the library moves the data itself: the problem is cut into
  *    pieces of about 48 MB (whole sequences of a few batch indices, or, for
  *    long sequences, runs of time steps chained through the carry of
@@ -227,6 +235,9 @@ typedef struct {
     size_t smem_bytes;     /* dynamic shared memory per CTA */
     size_t workspace_bytes;/* chunked: control block + look-back words for this call */
     int blocks;            /* chunked: blocks mode, chunks per block (0 = another mode) */
+    int chain;             /* chunked: 1 = chain mode (one cooperative launch: worker CTAs publish
+                              each chunk's aggregate a chunk ahead, resolver CTAs walk each slice's
+                              chain of aggregates; grid = resolvers + workers) */
 } linrec_plan_t;
 
 /*
@@ -330,7 +341,10 @@ linrec_status_t linrec_plan_bdl(int64_t B, int64_t D, int64_t L, int elem_bytes,
  * linrec_stream_status -- synchronise `stream`, then return and clear the
  * device-side status of the library's work on it: LINREC_OK, or the first of
  * LINREC_ERR_LOOKBACK_TIMEOUT / LINREC_ERR_TMA_TIMEOUT that a kernel recorded.
- * A stream the library has not used reports LINREC_OK.
+ * It also reports and clears the failures of linrec_scan_f32_noalloc calls on
+ * the current device that were made with d_status == NULL (their fixed array
+ * keeps one status word for all streams).  A stream the library has not used
+ * reports LINREC_OK.
  */
 linrec_status_t linrec_stream_status(void *stream);
 
@@ -367,15 +381,20 @@ linrec_status_t linrec_copy_f32(const float *src, float *dst, int64_t n, void *s
  *    the kernel's occupancy (once per device); make that first call before
  *    any stream capture.
  *  - Every call uses the same array, which keeps what the last call left.
- *    Each call clears the array's tile counters (a 12-byte and a 4-byte
- *    cudaMemsetAsync on `stream`) and tags its look-back words with a
- *    per-call epoch, so words left by earlier calls are never mistaken for
- *    its own.  Calls that overlap on the GPU (on different streams, or
- *    graph launches in flight together) race on the array and return wrong
- *    results: run them one after another.
+ *    The array's tile counters are zero when the library loads and the last
+ *    block of every launch resets them (a launch whose waits ran out
+ *    included), so a call enqueues nothing but its kernel; each call tags its
+ *    look-back words with a per-call epoch that the launch advances, so words
+ *    left by earlier calls are never mistaken for its own.  Calls that
+ *    overlap on the GPU (on different streams, or graph launches in flight
+ *    together) race on the array and return wrong results: run them one
+ *    after another.
  *  - d_status (may be NULL): a device word the kernel ORs
  *    1 << LINREC_ERR_LOOKBACK_TIMEOUT or 1 << LINREC_ERR_TMA_TIMEOUT into if
- *    a bounded wait runs out; the output then holds NaN where the carry was lost.
+ *    a bounded wait runs out; the output then holds NaN where the carry was
+ *    lost.  With d_status == NULL the failure goes to a status word in the
+ *    array instead, which linrec_stream_status reports and clears (on any
+ *    stream of the device; synchronise the streams those calls ran on first).
  */
 #define LINREC_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
 linrec_status_t linrec_scan_f32_noalloc(const float *a, const float *b, float *h,
@@ -416,6 +435,26 @@ size_t linrec_workspace_bytes(int64_t B, int64_t L, int64_t D);
  */
 int linrec_debug_checks(void);
 linrec_status_t linrec_debug_bad_accesses(uint64_t *count, int64_t *first_offset, int64_t output_cap_bytes);
+
+/*
+ * linrec_debug_range_covers -- 1 if the bytes [p, p + bytes) lie inside the address
+ * range [range_start, range_start + range_size), else 0 (also for bytes == 0).  Pure
+ * host logic, exported so that tests can check it: linrec_scan_f32_host reads and
+ * writes host buffers in place only when the driver's range of each buffer's first
+ * byte covers the whole buffer (and its last byte is mapped at the matching device
+ * address); any buffer only partly page-locked goes through the copy pipeline.
+ */
+int linrec_debug_range_covers(uintptr_t range_start, size_t range_size, uintptr_t p, size_t bytes);
+
+/*
+ * linrec_debug_set_epoch -- tests only: write `epoch` into the epoch word of the
+ * look-back workspace the library holds for `stream` on the current device
+ * (fixed_array == 0; LINREC_ERR_WORKSPACE if it holds none yet), or of the fixed
+ * array of linrec_scan_f32_noalloc (fixed_array != 0).  Synchronous.  A launch
+ * tags its words with a tag derived from the epoch and moves the epoch on; this
+ * lets a test start just below the point where the epoch word wraps around.
+ */
+linrec_status_t linrec_debug_set_epoch(void *stream, int fixed_array, uint32_t epoch);
 
 /* Library version as major*10000 + minor*100 + patch. */
 int linrec_version(void);

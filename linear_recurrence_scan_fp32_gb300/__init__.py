@@ -95,6 +95,7 @@ class Plan(ctypes.Structure):
         ("smem_bytes", ctypes.c_size_t),
         ("workspace_bytes", ctypes.c_size_t),
         ("blocks", ctypes.c_int),
+        ("chain", ctypes.c_int),
     ]
 
 
@@ -105,6 +106,8 @@ _lib = None
 def lib():
     """The loaded liblinrec.so (ctypes handle).  Raises LinrecError if it was not built."""
     global _lib
+    if _lib is not None:                 # loaded: no lock on the per-call path
+        return _lib
     with _lock:
         if _lib is not None:
             return _lib
@@ -159,6 +162,10 @@ def lib():
         L.linrec_debug_checks.restype = i32
         L.linrec_debug_bad_accesses.argtypes = [ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_int64), i64]
         L.linrec_debug_bad_accesses.restype = i32
+        L.linrec_debug_range_covers.argtypes = [ctypes.c_size_t, ctypes.c_size_t, ctypes.c_size_t, ctypes.c_size_t]
+        L.linrec_debug_range_covers.restype = i32
+        L.linrec_debug_set_epoch.argtypes = [vp, i32, ctypes.c_uint32]
+        L.linrec_debug_set_epoch.restype = i32
         _lib = L
         return _lib
 
@@ -172,7 +179,7 @@ def _check(code: int, what: str):
         raise LinrecError(code, f"{what}: {linrec_status_string(code)}")
 
 
-CHUNK_MODES = {"auto": 0, "own": 1, "lookback": 2, "twopass": 3, "blocks": 4}
+CHUNK_MODES = {"auto": 0, "own": 1, "lookback": 2, "twopass": 3, "blocks": 4, "chain": 5}
 
 
 def _addr(x):
@@ -200,19 +207,40 @@ def make_options(path="auto", vec=0, prefetch=0, tile_t=0, tile_d=0, stages=0, c
     return o
 
 
-def _stream_handle(stream):
-    if stream is None:
+_torch = None
+_raw_stream = None
+
+
+def _torch_mod():
+    global _torch, _raw_stream
+    if _torch is None:
         import torch
-        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        # the current stream's handle without building a Stream object (several us per call),
+        # where this torch has the accessor; the public API otherwise
+        _raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        _torch = torch
+    return _torch
+
+
+def _stream_handle(stream):
+    """cudaStream_t of `stream`: a torch.cuda.Stream, a raw handle, or None for the current
+    device's current stream."""
+    if stream is None:
+        torch = _torch_mod()
+        if _raw_stream is not None:
+            return _raw_stream(torch.cuda.current_device())
+        return torch.cuda.current_stream().cuda_stream
     if hasattr(stream, "cuda_stream"):
-        return ctypes.c_void_p(stream.cuda_stream)
-    return ctypes.c_void_p(int(stream))
+        return stream.cuda_stream
+    return int(stream)
 
 
 def _shape_of(a, b, h, dtype=None):
-    import torch
+    torch = _torch_mod()
     dtype = dtype or torch.float32
-    for name, t in (("a", a), ("b", b)) + ((("h", h),) if h is not None else ()):
+    for name, t in (("a", a), ("b", b), ("h", h)):
+        if t is None:
+            continue
         if not isinstance(t, torch.Tensor):
             raise TypeError(f"{name} must be a torch.Tensor")
         if t.dtype != dtype:
@@ -488,6 +516,19 @@ def linrec_debug_bad_accesses(output_cap_bytes: int = 0):
     _check(lib().linrec_debug_bad_accesses(ctypes.byref(count), ctypes.byref(first), int(output_cap_bytes)),
            "linrec_debug_bad_accesses")
     return int(count.value), int(first.value)
+
+
+def linrec_debug_range_covers(range_start: int, range_size: int, p: int, nbytes: int) -> bool:
+    """Whether [p, p + nbytes) lies inside [range_start, range_start + range_size) (the test the
+    host entry point makes before it reads a page-locked buffer in place)."""
+    return bool(lib().linrec_debug_range_covers(int(range_start), int(range_size), int(p), int(nbytes)))
+
+
+def linrec_debug_set_epoch(epoch: int, stream=None, fixed_array: bool = False):
+    """Tests only: write the epoch word of the stream's look-back workspace (or of the fixed array of
+    linrec_scan_f32_noalloc) on the current device."""
+    _check(lib().linrec_debug_set_epoch(_stream_handle(stream), 1 if fixed_array else 0, int(epoch) & 0xffffffff),
+           "linrec_debug_set_epoch")
 
 
 def linrec_workspace_bytes(B, L, D) -> int:

@@ -149,8 +149,7 @@ chunked_backward_kernel(const __grid_constant__ CUtensorMap map_g,
             tmap_prefetch(&map_a);
             if (load_h) tmap_prefetch(&map_h);
             if (lookback) {
-                const uint32_t tag = ld_relaxed_u32(&ctrl->epoch) + 1u;
-                sm.tag = tag == 0 ? 1u : tag;
+                sm.tag = tag_of(ld_relaxed_u32(&ctrl->epoch));
             }
             long long qr = 0, slice = 0;
             first = next_tile(qr, slice);
@@ -328,7 +327,7 @@ chunked_backward_kernel(const __grid_constant__ CUtensorMap map_g,
                 atomicExch(&ctrl->tile_counter, 0ull);
                 atomicExch(&ctrl->done, 0u);
                 atomicExch(&ctrl->abort, 0u);
-                atomicAdd(&ctrl->epoch, 1u);
+                atomicExch(&ctrl->epoch, next_epoch(ld_relaxed_u32(&ctrl->epoch)));
                 __threadfence();
             }
         }

@@ -33,6 +33,7 @@ const ChunkedVariant kVariants[] = {LINREC_CHUNKED_VARIANTS(LINREC_V_ENTRY)
 #undef LINREC_VB_ENTRY
 
 const void *kernel_of(const ChunkedVariant *v, int dtype) {
+    if (v->chain) return chain_kernel(v, dtype);
     if (dtype != kDtypeF32) return chunked16_kernel(v, dtype);
     if (v->elem_bytes != 4) return nullptr;
 #define LINREC_K_ENTRY(TD, TT, S, ST)                                                                \
@@ -66,6 +67,7 @@ cudaError_t chunked_ctas_per_sm(const ChunkedVariant *v, int *ctas, int dtype) {
 }
 
 cudaError_t launch_chunked(const ChunkedLaunch &p, cudaStream_t stream) {
+    if (p.mode == kModeChain || p.variant->chain) return launch_chain(p, stream);
     const void *fn = kernel_of(p.variant, p.dtype);
     if (!fn) return cudaErrorInvalidValue;
     cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -323,8 +323,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
             tmap_prefetch(&map_a);
             tmap_prefetch(&map_b);
             if (chained) {
-                const uint32_t tag = ld_relaxed_u32(&ctrl->epoch) + 1u;
-                sm.tag = tag == 0 ? 1u : tag;
+                sm.tag = tag_of(ld_relaxed_u32(&ctrl->epoch));
             }
             // One tile at launch: in look-back mode tiles are then taken in the order
             // CTAs start on them, so a tile's predecessors are never parked in another
@@ -599,7 +598,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
                 atomicExch(&ctrl->tile_counter, 0ull);
                 atomicExch(&ctrl->done, 0u);
                 atomicExch(&ctrl->abort, 0u);
-                atomicAdd(&ctrl->epoch, 1u);
+                atomicExch(&ctrl->epoch, next_epoch(ld_relaxed_u32(&ctrl->epoch)));
                 __threadfence();
             }
         }

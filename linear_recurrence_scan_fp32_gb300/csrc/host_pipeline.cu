@@ -23,6 +23,7 @@
 // host memory directly over the host link (measured on GB300: ~300 GB/s of
 // scan traffic against ~250 GB/s for the copy pipeline, both close to the
 // link's ~210 GB/s host-to-device read rate, and no device memory is used).
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -30,6 +31,60 @@
 #include "linrec.h"
 
 namespace {
+
+typedef CUresult (*PointerAttrFn)(void *, CUpointer_attribute, CUdeviceptr);
+
+// The driver's record of the address range p belongs to (its start and size), where the
+// driver keeps one for this kind of memory; false when it does not say.
+bool range_of(const void *p, uintptr_t *start, size_t *size) {
+    static PointerAttrFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuPointerGetAttribute", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PointerAttrFn>(f);
+        cudaGetLastError();
+    });
+    if (!fn) return false;
+    CUdeviceptr s0 = 0;
+    size_t n = 0;
+    const CUdeviceptr at = static_cast<CUdeviceptr>(reinterpret_cast<uintptr_t>(p));
+    if (fn(&s0, CU_POINTER_ATTRIBUTE_RANGE_START_ADDR, at) != CUDA_SUCCESS ||
+        fn(&n, CU_POINTER_ATTRIBUTE_RANGE_SIZE, at) != CUDA_SUCCESS)
+        return false;
+    *start = static_cast<uintptr_t>(s0);
+    *size = n;
+    return true;
+}
+
+// Whether the device can address every byte of [p, p + bytes) through page-locked host
+// memory, and the device address of p.  A buffer only partly page-locked (a registration
+// of a prefix of a larger block, a pointer into a pinned block shorter than the buffer)
+// must take the copy pipeline: a kernel reading the rest would touch unmapped addresses.
+// So the first and the last byte must both be page-locked host memory, mapped at device
+// addresses the same distance apart, and, where the driver reports the range the first
+// byte belongs to, that range must hold the last byte too.
+bool mapped_whole(const void *p, size_t bytes, const void **dev) {
+    const char *q = static_cast<const char *>(p);
+    cudaPointerAttributes first, last;
+    if (cudaPointerGetAttributes(&first, q) != cudaSuccess || cudaPointerGetAttributes(&last, q + bytes - 1) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (first.type != cudaMemoryTypeHost || last.type != cudaMemoryTypeHost || !first.devicePointer ||
+        !last.devicePointer)
+        return false;
+    if (static_cast<const char *>(last.devicePointer) != static_cast<const char *>(first.devicePointer) + (bytes - 1))
+        return false;
+    uintptr_t start = 0;
+    size_t size = 0;
+    if (range_of(p, &start, &size) && !linrec_debug_range_covers(start, size, reinterpret_cast<uintptr_t>(p), bytes))
+        return false;
+    *dev = first.devicePointer;
+    return true;
+}
 
 constexpr int kSlots = 3;
 constexpr int64_t kPieceBytes = 48ll << 20;   // a + b + h per piece
@@ -121,20 +176,11 @@ extern "C" linrec_status_t linrec_scan_f32_host(const float *a, const float *b, 
         return LINREC_ERR_LAUNCH;
     }
 
-    // Page-locked host memory the device can address: scan it in place.
+    // Page-locked host memory the device can address, every byte of it: scan it in place.
     const void *dptr[3] = {nullptr, nullptr, nullptr};
     bool direct = true;
     const void *hptr[3] = {a, b, h};
-    for (int i = 0; i < 3 && direct; ++i) {
-        cudaPointerAttributes attr;
-        if (cudaPointerGetAttributes(&attr, hptr[i]) != cudaSuccess) {
-            cudaGetLastError();
-            direct = false;
-        } else {
-            direct = attr.type == cudaMemoryTypeHost && attr.devicePointer != nullptr;
-            dptr[i] = attr.devicePointer;
-        }
-    }
+    for (int i = 0; i < 3 && direct; ++i) direct = mapped_whole(hptr[i], (size_t)n * sizeof(float), &dptr[i]);
     if (direct)
         return linrec_scan_f32(static_cast<const float *>(dptr[0]), static_cast<const float *>(dptr[1]),
                                static_cast<float *>(const_cast<void *>(dptr[2])), B, L, D, stream_ptr);
@@ -218,4 +264,11 @@ extern "C" linrec_status_t linrec_scan_f32_host(const float *a, const float *b, 
         if (st == LINREC_OK) st = LINREC_ERR_LAUNCH;
     }
     return st;
+}
+
+extern "C" int linrec_debug_range_covers(uintptr_t range_start, size_t range_size, uintptr_t p, size_t bytes) {
+    // [p, p + bytes) inside [range_start, range_start + range_size), without overflow
+    if (bytes == 0 || p < range_start) return 0;
+    const uintptr_t off = p - range_start;
+    return off <= range_size && bytes <= range_size - off ? 1 : 0;
 }

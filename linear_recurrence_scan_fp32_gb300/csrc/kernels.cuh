@@ -83,6 +83,7 @@ struct ChunkedVariant {
     int elem_bytes = 4;  // stored element size: 4 (fp32) or 2 (bfloat16 and binary16)
     int cpt = 1;         // adjacent channels per thread: 1, or 2 (16-bit storage)
     int blocks = 0;      // 1: compiled for blocks mode (and only used there)
+    int chain = 0;       // 1: the chain-mode kernel (chain.cu), used only there
 };
 // The compiled variants (tile_d, tile_t, segments, stages combinations): fp32
 // storage, and 16-bit storage (each shape compiled for bfloat16 and binary16).
@@ -98,6 +99,8 @@ constexpr int kModeReduce = 2;     // two-pass, first launch: write every tile's
 constexpr int kModeApply = 3;      // two-pass, last launch: carry from the scanned aggregates
 constexpr int kModeBlocks = 4;     // one launch: blocks of G tiles, reduce, look-back over blocks,
                                    // apply from L2 (variants with blocks = 1 only)
+constexpr int kModeChain = 5;      // one cooperative launch: workers compose a tile ahead and publish its
+                                   // map, resolver CTAs walk each slice's chain of maps (chain.cu)
 
 struct ChunkedLaunch {
     const ChunkedVariant *variant;
@@ -125,6 +128,16 @@ struct ChunkedLaunch {
 // Number of CTAs of this variant that fit on one SM (occupancy API).
 cudaError_t chunked_ctas_per_sm(const ChunkedVariant *v, int *ctas, int dtype = kDtypeF32);
 cudaError_t launch_chunked(const ChunkedLaunch &args, cudaStream_t stream);
+
+// Chain mode (chain.cu): its compiled variants per storage type (the 16-bit ones serve
+// bfloat16 and binary16 alike), the kernel of one, the layout of the resolver CTAs
+// (returns their number; channels per group and groups per CTA out), and the launch
+// (mode kModeChain; grid = resolver CTAs + workers, all resident at once).
+const ChunkedVariant *chain_variants(int dtype, int *count);
+const void *chain_kernel(const ChunkedVariant *v, int dtype);
+int chain_layout(int64_t n_slices, int warps, int *cpg, int *gpc);
+constexpr int kChainMaxResolvers = 16;   // resolver CTAs at most (slices beyond them: no chain mode)
+cudaError_t launch_chain(const ChunkedLaunch &args, cudaStream_t stream);
 
 // ---- backward (gradient) kernels -----------------------------------------------
 // c_t = g_t + a_{t+1} c_{t+1} (c_{L-1} = g_{L-1} + dh_last), db = c,
@@ -186,6 +199,12 @@ cudaError_t checked_report_backward(unsigned long long *count, long long *first,
 cudaError_t checked_report_regcarry(unsigned long long *count, long long *first, long long out_cap);
 cudaError_t checked_report_regcarry16(unsigned long long *count, long long *first, long long out_cap);
 cudaError_t checked_report_rows(unsigned long long *count, long long *first, long long out_cap);
+
+// ---- the fixed array of linrec_scan_f32_noalloc (noalloc.cu) ---------------------
+// Its status word on device dev, read on `stream` and cleared (0 if unused); and, for
+// tests, its epoch word.
+cudaError_t noalloc_take_status(int dev, cudaStream_t stream, unsigned int *word);
+cudaError_t noalloc_set_epoch(int dev, unsigned int epoch);
 
 // ---- copy-ceiling kernel ---------------------------------------------------
 cudaError_t launch_copy(const float *src, float *dst, int64_t n, int sm_count, cudaStream_t stream);

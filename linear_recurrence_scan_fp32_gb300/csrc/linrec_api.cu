@@ -4,7 +4,9 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <map>
+#include <memory>
 #include <mutex>
 #include <tuple>
 #include <utility>
@@ -16,7 +18,7 @@ using namespace linrec;
 
 namespace {
 
-constexpr int kVersion = 100;               // 0.1.0
+constexpr int kVersion = 200;               // 0.2.0
 constexpr int64_t kDefaultSpinLimit = 1 << 20;
 constexpr int kRegcarryThreads = 256;
 // forward scans: the register path from this many 16-byte threads per SM on
@@ -50,14 +52,29 @@ constexpr int64_t kRowsStreamElems16 = 8192;
 constexpr int64_t kRowsTargetWarps = 32;
 constexpr int64_t kRowsMinSegChunks = 8;
 
+// Device facts: written once under g_mu before the pointer is handed out; the resident-CTA
+// counts are filled in as variants are first used, by any thread (atomics, 0 = not queried).
 struct DeviceInfo {
     bool ready = false;
     bool supported = false;
     int sm_count = 0;
-    int ctas_per_sm[3][64] = {};            // per storage type and chunked variant, 0 = not queried yet
-    int back_ctas_per_sm[64] = {};          // per backward variant
+    std::atomic<int> ctas_per_sm[3][64];       // per storage type and chunked variant
+    std::atomic<int> back_ctas_per_sm[64];     // per backward variant
+    std::atomic<int> chain_ctas_per_sm[3][8];  // per storage type and chain variant
+    DeviceInfo() {
+        for (auto &row : ctas_per_sm)
+            for (auto &x : row) x.store(0, std::memory_order_relaxed);
+        for (auto &x : back_ctas_per_sm) x.store(0, std::memory_order_relaxed);
+        for (auto &row : chain_ctas_per_sm)
+            for (auto &x : row) x.store(0, std::memory_order_relaxed);
+    }
 };
 
+// Locking: g_mu guards the two maps below and is held only to look an entry up.  A call
+// then holds its stream's own mutex for the rest of its work (plan, workspace, tensor maps,
+// launches): calls on different streams run concurrently; calls on one stream, which run in
+// order on the GPU anyway, take turns, so one never frees a workspace another is about to
+// launch with.
 std::mutex g_mu;
 std::map<int, DeviceInfo> g_devices;
 
@@ -71,8 +88,28 @@ struct Slot {
 // current epoch was written by this launch; the two-pass mode's plain float
 // arrays live in slots of their own, where no tag is ever looked for.
 enum SlotKind { kSlotTagged = 0, kSlotArrays = 1 };
-// keyed by (device, stream, level, kind): level 1 is the two-pass mode's scan of its aggregates
-std::map<std::tuple<int, uintptr_t, int, int>, Slot> g_slots;
+// The library's state for one (device, stream): its workspace slots keyed by (level, kind);
+// level 1 is the two-pass mode's scan of its aggregates.
+struct StreamState {
+    std::mutex mu;                           // held by a call on this stream for its whole work
+    std::map<std::pair<int, int>, Slot> slots;
+};
+std::map<std::pair<int, uintptr_t>, std::unique_ptr<StreamState>> g_streams;
+
+// The state of (dev, stream), created on first use (takes g_mu briefly).
+StreamState *stream_state(int dev, cudaStream_t stream) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    std::unique_ptr<StreamState> &p = g_streams[std::make_pair(dev, reinterpret_cast<uintptr_t>(stream))];
+    if (!p) p.reset(new StreamState);
+    return p.get();
+}
+
+// The state of (dev, stream) if the library has used that stream, else NULL.
+StreamState *find_stream_state(int dev, cudaStream_t stream) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    auto it = g_streams.find(std::make_pair(dev, reinterpret_cast<uintptr_t>(stream)));
+    return it == g_streams.end() ? nullptr : it->second.get();
+}
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
@@ -230,6 +267,54 @@ void default_tile(int64_t B, int64_t L, int64_t D, int sm_count, bool own, bool 
     else { *tile_d = 32; *tile_t = 128; *stages = 3; }
 }
 
+// Chain mode (chain.cu): its own tile (the first compiled chain variant of the storage type,
+// or the one opt names), every resident CTA launched: resolver CTAs first, one group of warps
+// per slice, then workers; the look-back words of every tile (three per channel).
+linrec_status_t plan_chain(int64_t B, int64_t L, int64_t D, int sm_count, int ctas_per_sm,
+                           const linrec_options_t *opt, linrec_plan_t *plan, int *variant_index, int dtype) {
+    int n = 0;
+    const ChunkedVariant *vars = chain_variants(dtype, &n);
+    const ChunkedVariant *v = nullptr;
+    for (int i = 0; i < n && !v; ++i) {
+        const ChunkedVariant &c = vars[i];
+        if ((opt->tile_d == 0 || opt->tile_d == c.tile_d) && (opt->tile_t == 0 || opt->tile_t == c.tile_t) &&
+            (opt->stages == 0 || opt->stages == c.stages) && (opt->segments == 0 || opt->segments == c.segments) &&
+            (opt->vec == 0 || opt->vec == c.cpt)) {
+            v = &c;
+            if (variant_index) *variant_index = i;
+        }
+    }
+    if (!v) return LINREC_ERR_INVALID_VALUE;
+    plan->chain = 1;
+    plan->vec = v->cpt;
+    plan->tile_d = v->tile_d;
+    plan->tile_t = v->tile_t;
+    plan->segments = v->segments;
+    plan->stages = v->stages;
+    plan->threads = v->threads;
+    plan->smem_bytes = v->smem_bytes;
+    const int64_t slices = B * ((D + v->tile_d - 1) / v->tile_d);
+    plan->chunks = (L + v->tile_t - 1) / v->tile_t;
+    plan->n_tiles = slices * plan->chunks;
+    int per_sm = ctas_per_sm;
+    if (per_sm <= 0) {
+        per_sm = (int)((227 * 1024) / (v->smem_bytes + 1024));
+        if (per_sm < 1) per_sm = 1;
+    }
+    if (opt->ctas_per_sm > 0 && opt->ctas_per_sm < per_sm) per_sm = opt->ctas_per_sm;
+    int cpg = 0, gpc = 0;
+    const int64_t n_res = chain_layout(slices, v->threads / 32, &cpg, &gpc);
+    // chain mode is for few slices: each resolver group serves one slice's channels, at most one
+    // group per warp of at most kChainMaxResolvers CTAs
+    if (n_res > kChainMaxResolvers) return LINREC_ERR_INVALID_VALUE;
+    int64_t grid = (int64_t)sm_count * per_sm;
+    if (grid > n_res + plan->n_tiles) grid = n_res + plan->n_tiles;
+    if (grid <= n_res) return LINREC_ERR_INVALID_VALUE;   // no room for a worker beside the resolvers
+    plan->grid = grid;
+    plan->workspace_bytes = kWorkspaceHead + (size_t)3 * (size_t)plan->n_tiles * (size_t)v->tile_d * 8u;
+    return LINREC_OK;
+}
+
 linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int align_bytes, int ctas_per_sm,
                           const linrec_options_t *opt, linrec_plan_t *plan, int *variant_index,
                           bool backward = false, bool allow_twopass = true, int dtype = kDtypeF32) {
@@ -329,10 +414,12 @@ linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int ali
     // when the chains are short, or, for long chains (whose look-back would be
     // bound by how fast inclusive values travel down the chain), by the
     // two-pass mode: reduce, scan the aggregates, apply.
-    if (opt->chunk_mode < 0 || opt->chunk_mode > 4) return LINREC_ERR_INVALID_VALUE;
+    if (opt->chunk_mode < 0 || opt->chunk_mode > 5) return LINREC_ERR_INVALID_VALUE;
     if (opt->chunk_mode == 3 && !allow_twopass) return LINREC_ERR_INVALID_VALUE;
-    if (opt->chunk_mode == 4 && backward) return LINREC_ERR_INVALID_VALUE;
+    if ((opt->chunk_mode == 4 || opt->chunk_mode == 5) && backward) return LINREC_ERR_INVALID_VALUE;
     if (opt->group < 0 || (opt->group > 0 && opt->chunk_mode != 4)) return LINREC_ERR_INVALID_VALUE;
+    if (opt->chunk_mode == 5 && !wide_td)
+        return plan_chain(B, L, D, sm_count, ctas_per_sm, opt, plan, variant_index, dtype);
     bool own = false, twopass = false, blk = false;
     if (wide_td) {
         own = true;
@@ -425,8 +512,9 @@ linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int ali
     return LINREC_OK;
 }
 
-// Device facts, queried once per device.  Caller holds g_mu.
+// Device facts, queried once per device (takes g_mu briefly).
 DeviceInfo *device_info(int dev) {
+    std::lock_guard<std::mutex> lock(g_mu);
     DeviceInfo &di = g_devices[dev];
     if (!di.ready) {
         int major = 0, minor = 0, sms = 0;
@@ -444,16 +532,29 @@ DeviceInfo *device_info(int dev) {
 }
 
 bool get_encoder() {
-    if (g_encode) return true;
-    void *fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-            cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) {
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess && fn)
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
         cudaGetLastError();
-        return false;
+    });
+    return g_encode != nullptr;
+}
+
+// The resident CTAs per SM cached in `slot`, queried with `query` the first time.
+template <typename Q>
+int cached_ctas(std::atomic<int> &slot, Q query) {
+    int c = slot.load(std::memory_order_relaxed);
+    if (c > 0) return c;
+    if (query(&c) != cudaSuccess || c <= 0) {
+        cudaGetLastError();
+        return 0;
     }
-    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
-    return true;
+    slot.store(c, std::memory_order_relaxed);
+    return c;
 }
 
 bool encode_map(CUtensorMap *map, const void *base, int64_t B, int64_t L, int64_t D, int tile_d, int tile_t,
@@ -472,9 +573,9 @@ bool encode_map(CUtensorMap *map, const void *base, int64_t B, int64_t L, int64_
 }
 
 // The workspace of (dev, stream, level, kind), grown in stream order and zeroed
-// when (re)allocated.  Caller holds g_mu.
+// when (re)allocated.  Caller holds the stream's mutex.
 Slot *workspace(int dev, cudaStream_t stream, size_t need, int level = 0, SlotKind kind = kSlotTagged) {
-    Slot &s = g_slots[std::make_tuple(dev, reinterpret_cast<uintptr_t>(stream), level, (int)kind)];
+    Slot &s = stream_state(dev, stream)->slots[std::make_pair(level, (int)kind)];
     // While the stream is being captured into a CUDA graph nothing is allocated (the
     // graph would own the memory); a slot a captured call uses stays allocated for good,
     // since the graph keeps its address.
@@ -507,7 +608,51 @@ Slot *workspace(int dev, cudaStream_t stream, size_t need, int level = 0, SlotKi
     return &s;
 }
 
-// The forward scan, arguments checked, g_mu held.  `level` is 0 for a caller's
+// Chain mode: every resident CTA of its variant (from the occupancy API), one cooperative launch.
+linrec_status_t scan_chain_locked(DeviceInfo *di, int dev, const void *a, const void *b, void *h, int64_t B,
+                                  int64_t L, int64_t D, int dtype, cudaStream_t stream, const linrec_options_t *opt,
+                                  int level, linrec_plan_t plan, int vi) {
+    int nvar = 0;
+    const ChunkedVariant *vars = chain_variants(dtype, &nvar);
+    if (vi < 0 || vi >= nvar || vi >= 8 || dtype < 0 || dtype > 2) return LINREC_ERR_INVALID_VALUE;
+    const int per_sm = cached_ctas(di->chain_ctas_per_sm[dtype][vi],
+                                   [&](int *c) { return chunked_ctas_per_sm(&vars[vi], c, dtype); });
+    if (per_sm <= 0) return LINREC_ERR_LAUNCH;
+    linrec_status_t st = plan_chain(B, L, D, di->sm_count, per_sm, opt, &plan, &vi, dtype);
+    if (st != LINREC_OK) return st;
+    if (!get_encoder()) return LINREC_ERR_LAUNCH;
+    ChunkedLaunch p;
+    p.variant = &vars[vi];
+    p.dtype = dtype;
+    if (!encode_map(&p.map_a, a, B, L, D, plan.tile_d, plan.tile_t, dtype) ||
+        !encode_map(&p.map_b, b, B, L, D, plan.tile_d, plan.tile_t, dtype))
+        return LINREC_ERR_LAUNCH;
+    Slot *ws = workspace(dev, stream, plan.workspace_bytes, level);
+    if (!ws) return LINREC_ERR_WORKSPACE;
+    p.h = h;
+    p.L = L;
+    p.D = D;
+    p.slices_per_batch = (D + plan.tile_d - 1) / plan.tile_d;
+    p.n_slices = B * p.slices_per_batch;
+    p.chunks = plan.chunks;
+    p.n_tiles = plan.n_tiles;
+    p.grid = plan.grid;
+    p.mode = kModeChain;
+    p.ctrl = reinterpret_cast<Control *>(ws->base);
+    p.words = reinterpret_cast<unsigned long long *>(ws->base + kWorkspaceHead);
+    p.status = opt->d_status ? opt->d_status : &p.ctrl->status;
+    p.spin_limit = opt->spin_limit > 0 ? opt->spin_limit : kDefaultSpinLimit;
+    p.silent_tile = opt->test_silent_tile > 0 ? opt->test_silent_tile - 1 : -1;
+    p.h_init = opt->h_init;
+    p.h_last = opt->h_last;
+    if (launch_chunked(p, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return LINREC_ERR_LAUNCH;
+    }
+    return LINREC_OK;
+}
+
+// The forward scan, arguments checked, the stream's mutex held.  `level` is 0 for a caller's
 // problem and 1 for the two-pass mode's scan of its tile aggregates (always fp32).
 linrec_status_t scan_locked(DeviceInfo *di, int dev, const void *a, const void *b, void *h, int64_t B,
                             int64_t L, int64_t D, int dtype, cudaStream_t stream, const linrec_options_t *opt,
@@ -542,19 +687,16 @@ linrec_status_t scan_locked(DeviceInfo *di, int dev, const void *a, const void *
         return err == cudaSuccess ? LINREC_OK : LINREC_ERR_LAUNCH;
     }
 
+    if (plan.chain) return scan_chain_locked(di, dev, a, b, h, B, L, D, dtype, stream, opt, level, plan, vi);
+
     // chunked: resident CTAs per SM from the occupancy API, then the real plan
     int nvar = 0;
     const ChunkedVariant *variants = variants_of(false, dtype, &nvar);
     if (vi < 0 || vi >= 64 || dtype < 0 || dtype > 2) return LINREC_ERR_INVALID_VALUE;
-    if (di->ctas_per_sm[dtype][vi] == 0) {
-        int c = 0;
-        if (chunked_ctas_per_sm(&variants[vi], &c, dtype) != cudaSuccess || c <= 0) {
-            cudaGetLastError();
-            return LINREC_ERR_LAUNCH;
-        }
-        di->ctas_per_sm[dtype][vi] = c;
-    }
-    st = plan_impl(B, L, D, di->sm_count, align, di->ctas_per_sm[dtype][vi], opt, &plan, &vi, false, level == 0,
+    const int per_sm = cached_ctas(di->ctas_per_sm[dtype][vi],
+                                   [&](int *c) { return chunked_ctas_per_sm(&variants[vi], c, dtype); });
+    if (per_sm <= 0) return LINREC_ERR_LAUNCH;
+    st = plan_impl(B, L, D, di->sm_count, align, per_sm, opt, &plan, &vi, false, level == 0,
                    dtype);
     if (st != LINREC_OK) return st;
     if (!get_encoder()) return LINREC_ERR_LAUNCH;
@@ -697,7 +839,7 @@ linrec_status_t plan_bdl_impl(int64_t B, int64_t D, int64_t L, int dtype, int sm
     return LINREC_OK;
 }
 
-// The (B, D, L) scan, arguments checked, g_mu held.
+// The (B, D, L) scan, arguments checked, the stream's mutex held.
 linrec_status_t scan_bdl_locked(DeviceInfo *di, int dev, const void *a, const void *b, void *h, int64_t B,
                                 int64_t D, int64_t L, int dtype, cudaStream_t stream, const linrec_options_t *opt) {
     linrec_plan_t plan;
@@ -870,10 +1012,10 @@ linrec_status_t scan_entry(int dtype, bool bdl, const void *a, const void *b, vo
         cudaGetLastError();
         return LINREC_ERR_LAUNCH;
     }
-    std::lock_guard<std::mutex> lock(g_mu);
     DeviceInfo *di = device_info(dev);
     if (!di) return LINREC_ERR_LAUNCH;
     if (!di->supported) return LINREC_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lock(stream_state(dev, stream)->mu);
 
     if (bdl) return scan_bdl_locked(di, dev, a, b, h, B, D, L, dtype, stream, opt);
     return scan_locked(di, dev, a, b, h, B, L, D, dtype, stream, opt, 0);
@@ -982,10 +1124,10 @@ linrec_status_t linrec_scan_f32_backward_ex(const float *a, const float *h, cons
         cudaGetLastError();
         return LINREC_ERR_LAUNCH;
     }
-    std::lock_guard<std::mutex> lock(g_mu);
     DeviceInfo *di = device_info(dev);
     if (!di) return LINREC_ERR_LAUNCH;
     if (!di->supported) return LINREC_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lock(stream_state(dev, stream)->mu);
 
     const uintptr_t u = reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(g) |
                         reinterpret_cast<uintptr_t>(db) | (da ? reinterpret_cast<uintptr_t>(da) |
@@ -1003,15 +1145,10 @@ linrec_status_t linrec_scan_f32_backward_ex(const float *a, const float *h, cons
     int nvar = 0;
     const ChunkedVariant *variants = backward_variants(&nvar);
     if (vi < 0 || vi >= 64) return LINREC_ERR_INVALID_VALUE;
-    if (di->back_ctas_per_sm[vi] == 0) {
-        int c = 0;
-        if (backward_ctas_per_sm(&variants[vi], &c) != cudaSuccess || c <= 0) {
-            cudaGetLastError();
-            return LINREC_ERR_LAUNCH;
-        }
-        di->back_ctas_per_sm[vi] = c;
-    }
-    st = plan_impl(B, L, D, di->sm_count, align, di->back_ctas_per_sm[vi], opt, &plan, &vi, true);
+    const int per_sm = cached_ctas(di->back_ctas_per_sm[vi],
+                                   [&](int *c) { return backward_ctas_per_sm(&variants[vi], c); });
+    if (per_sm <= 0) return LINREC_ERR_LAUNCH;
+    st = plan_impl(B, L, D, di->sm_count, align, per_sm, opt, &plan, &vi, true);
     if (st != LINREC_OK) return st;
     if (!get_encoder()) return LINREC_ERR_LAUNCH;
     BackwardLaunch p;
@@ -1096,28 +1233,66 @@ linrec_status_t linrec_stream_status(void *stream_ptr) {
         return LINREC_ERR_LAUNCH;
     }
     unsigned char *base = nullptr;
-    {
-        std::lock_guard<std::mutex> lock(g_mu);
-        auto it = g_slots.find(std::make_tuple(dev, reinterpret_cast<uintptr_t>(stream), 0, (int)kSlotTagged));
-        if (it == g_slots.end() || !it->second.base) return LINREC_OK;
-        base = it->second.base;
+    if (StreamState *ss = find_stream_state(dev, stream)) {
+        std::lock_guard<std::mutex> lock(ss->mu);
+        auto it = ss->slots.find(std::make_pair(0, (int)kSlotTagged));
+        if (it != ss->slots.end()) base = it->second.base;
     }
-    Control *ctrl = reinterpret_cast<Control *>(base);
     unsigned int word = 0;
-    if (cudaMemcpyAsync(&word, &ctrl->status, sizeof(word), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
-        cudaStreamSynchronize(stream) != cudaSuccess) {
+    if (base) {
+        Control *ctrl = reinterpret_cast<Control *>(base);
+        if (cudaMemcpyAsync(&word, &ctrl->status, sizeof(word), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+            cudaStreamSynchronize(stream) != cudaSuccess) {
+            cudaGetLastError();
+            return LINREC_ERR_LAUNCH;
+        }
+        if (word != 0 && (cudaMemsetAsync(&ctrl->status, 0, sizeof(word), stream) != cudaSuccess ||
+                          cudaStreamSynchronize(stream) != cudaSuccess)) {
+            cudaGetLastError();
+            return LINREC_ERR_LAUNCH;
+        }
+    }
+    // failures of linrec_scan_f32_noalloc calls made without a status word of their own
+    unsigned int fixed = 0;
+    if (noalloc_take_status(dev, stream, &fixed) != cudaSuccess) {
         cudaGetLastError();
         return LINREC_ERR_LAUNCH;
     }
+    word |= fixed;
     if (word == 0) return LINREC_OK;
-    if (cudaMemsetAsync(&ctrl->status, 0, sizeof(word), stream) != cudaSuccess ||
-        cudaStreamSynchronize(stream) != cudaSuccess) {
-        cudaGetLastError();
-        return LINREC_ERR_LAUNCH;
-    }
     if (word & kStatusLookbackTimeout) return LINREC_ERR_LOOKBACK_TIMEOUT;
     if (word & kStatusTmaTimeout) return LINREC_ERR_TMA_TIMEOUT;
     return LINREC_ERR_LAUNCH;
+}
+
+linrec_status_t linrec_debug_set_epoch(void *stream_ptr, int fixed_array, uint32_t epoch) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return LINREC_ERR_LAUNCH;
+    }
+    if (fixed_array) {
+        if (noalloc_set_epoch(dev, epoch) != cudaSuccess) {
+            cudaGetLastError();
+            return LINREC_ERR_WORKSPACE;
+        }
+        return LINREC_OK;
+    }
+    unsigned char *base = nullptr;
+    if (StreamState *ss = find_stream_state(dev, static_cast<cudaStream_t>(stream_ptr))) {
+        std::lock_guard<std::mutex> lock(ss->mu);
+        auto it = ss->slots.find(std::make_pair(0, (int)kSlotTagged));
+        if (it != ss->slots.end()) base = it->second.base;
+    }
+    if (!base) return LINREC_ERR_WORKSPACE;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+    Control *ctrl = reinterpret_cast<Control *>(base);
+    if (cudaMemcpyAsync(&ctrl->epoch, &epoch, sizeof(epoch), cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess) {
+        cudaGetLastError();
+        return LINREC_ERR_LAUNCH;
+    }
+    return LINREC_OK;
 }
 
 linrec_status_t linrec_copy_f32(const float *src, float *dst, int64_t n, void *stream) {
@@ -1133,7 +1308,6 @@ linrec_status_t linrec_copy_f32(const float *src, float *dst, int64_t n, void *s
     }
     int sms = 0;
     {
-        std::lock_guard<std::mutex> lock(g_mu);
         DeviceInfo *di = device_info(dev);
         if (!di) return LINREC_ERR_LAUNCH;
         if (!di->supported) return LINREC_ERR_UNSUPPORTED_DEVICE;

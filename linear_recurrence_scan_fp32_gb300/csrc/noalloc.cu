@@ -85,6 +85,42 @@ bool overlap(const void *x, const void *y, int64_t bytes) {
 
 }  // namespace
 
+namespace linrec {
+
+// The array's status word on device `dev` (set by noalloc calls made without a status
+// word of their own), read on `stream` and cleared when set; 0 if the device has not run
+// such a call.  Called by linrec_stream_status.
+cudaError_t noalloc_take_status(int dev, cudaStream_t stream, unsigned int *word) {
+    *word = 0;
+    if (dev < 0 || dev >= kMaxDevices) return cudaSuccess;
+    unsigned int *status = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (!g_setup[dev].ready || !g_setup[dev].scratch) return cudaSuccess;
+        status = &reinterpret_cast<Control *>(g_setup[dev].scratch)->status;
+    }
+    cudaError_t e = cudaMemcpyAsync(word, status, sizeof(*word), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e == cudaSuccess && *word != 0) {
+        e = cudaMemsetAsync(status, 0, sizeof(*word), stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    }
+    return e;
+}
+
+// Tests: the array's epoch word on device `dev` (set up first), written synchronously.
+cudaError_t noalloc_set_epoch(int dev, unsigned int epoch) {
+    DeviceSetup *ds = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (dev < 0 || dev >= kMaxDevices || !setup_device(dev, ds) || !ds->scratch) return cudaErrorInvalidValue;
+    }
+    Control *ctrl = reinterpret_cast<Control *>(ds->scratch);
+    return cudaMemcpy(&ctrl->epoch, &epoch, sizeof(epoch), cudaMemcpyHostToDevice);
+}
+
+}  // namespace linrec
+
 extern "C" linrec_status_t linrec_scan_f32_noalloc(const float *a, const float *b, float *h, int64_t B, int64_t L,
                                                    int64_t D, void *stream_ptr, unsigned int *d_status) {
     if (B < 0 || L < 0 || D < 0) return LINREC_ERR_INVALID_VALUE;
@@ -117,7 +153,7 @@ extern "C" linrec_status_t linrec_scan_f32_noalloc(const float *a, const float *
     {
         linrec_plan_t probe;
         if (linrec_plan_f32(B, L, D, ds->sm_count, 16, 0, &opt, &probe) == LINREC_OK &&
-            (probe.twopass || probe.blocks))
+            (probe.twopass || probe.blocks || probe.chain))
             opt.chunk_mode = 2;
     }
     linrec_plan_t plan;
@@ -159,16 +195,12 @@ extern "C" linrec_status_t linrec_scan_f32_noalloc(const float *a, const float *
         !encode(&p.map_b, b, B, L, D, plan.tile_d, plan.tile_t))
         return LINREC_ERR_LAUNCH;
 
+    // The tile counter, the done count and the abort word start at zero (the array is zero
+    // when the library loads) and the last CTA of every launch resets them, a launch whose
+    // waits ran out included; the epoch word it advances tells this call's look-back words
+    // from those earlier calls left in the array.  So nothing is cleared here, and nothing
+    // comes between this launch and the work before it on the stream.
     Control *ctrl = reinterpret_cast<Control *>(ds->scratch);
-    // The tile counter and the done count must start at zero.  The kernel's last
-    // CTA leaves them so, but a call that never finished would not have: clear
-    // them here (no allocation).  The epoch word is kept: it tells this call's
-    // look-back words from those the previous calls left in the array.
-    if (cudaMemsetAsync(ctrl, 0, offsetof(Control, epoch), stream) != cudaSuccess ||
-        cudaMemsetAsync(&ctrl->abort, 0, sizeof(ctrl->abort), stream) != cudaSuccess) {
-        cudaGetLastError();
-        return LINREC_ERR_LAUNCH;
-    }
     p.h = h;
     p.L = L;
     p.D = D;

@@ -59,6 +59,12 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// A barrier for `threads` threads (a multiple of 32) of the CTA on hardware barrier `id`
+// (1 .. 15; 0 is __syncthreads): lets groups of warps synchronise among themselves.
+__device__ __forceinline__ void bar_sync_group(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 // ---- TMA ------------------------------------------------------------------
 
 __device__ __forceinline__ void tmap_prefetch(const CUtensorMap *map) {
@@ -93,6 +99,16 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
     return v;
 }
 
+// Two adjacent words in one access; each 64-bit element is itself single-copy atomic.
+__device__ __forceinline__ void st_relaxed_v2_u64(unsigned long long *p, unsigned long long x, unsigned long long y) {
+    asm volatile("st.relaxed.gpu.global.v2.b64 [%0], {%1, %2};" ::"l"(p), "l"(x), "l"(y) : "memory");
+}
+
+__device__ __forceinline__ void ld_relaxed_v2_u64(const unsigned long long *p, unsigned long long &x,
+                                                  unsigned long long &y) {
+    asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(x), "=l"(y) : "l"(p) : "memory");
+}
+
 __device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t *p) {
     uint32_t v;
     asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -106,5 +122,12 @@ __device__ __forceinline__ uint32_t word_tag(unsigned long long w) { return stat
 __device__ __forceinline__ float word_val(unsigned long long w) {
     return __uint_as_float(static_cast<uint32_t>(w & 0xffffffffull));
 }
+
+// A launch tags its words with tag_of(epoch); the last CTA to finish stores
+// next_epoch(epoch).  Tags run through 1 .. 2^32 - 1 (0 is never a tag, so zeroed
+// memory never reads as published) and two consecutive launches never share one,
+// whatever value the epoch word holds, 0xffffffff included.
+__device__ __forceinline__ uint32_t tag_of(uint32_t epoch) { return epoch % 0xffffffffu + 1u; }
+__device__ __forceinline__ uint32_t next_epoch(uint32_t epoch) { return tag_of(epoch) % 0xffffffffu; }
 
 }  // namespace linrec

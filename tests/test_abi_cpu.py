@@ -266,7 +266,21 @@ def test_plan_chunk_modes():
     assert p["workspace_bytes"] == 256 + 4 * (3 * p["n_tiles"] + 64 // p["tile_d"]) * p["tile_d"]
     assert lr.linrec_plan_f32_backward(1, 1 << 20, 64, chunk_mode="lookback")["lookback"] == 1
     with pytest.raises(lr.LinrecError):
-        lr.linrec_plan_f32(1, 1000, 64, path="chunked", chunk_mode=5)
+        lr.linrec_plan_f32(1, 1000, 64, path="chunked", chunk_mode=6)
+    # chain mode: one cooperative launch of every resident CTA (resolvers first, then workers),
+    # its own tile, three look-back words per tile and channel; forward only
+    p = lr.linrec_plan_f32(1, 1 << 20, 64, path="chunked", chunk_mode="chain", sm_count=152, resident_ctas=2)
+    assert (p["chain"], p["lookback"], p["twopass"], p["blocks"]) == (1, 0, 0, 0)
+    assert (p["tile_d"], p["tile_t"], p["stages"], p["grid"]) == (32, 128, 3, 304)
+    assert p["workspace_bytes"] == 256 + 24 * p["n_tiles"] * p["tile_d"]
+    p = lr.linrec_plan_f32(1, 200, 32, path="chunked", chunk_mode="chain", sm_count=152, resident_ctas=2)
+    assert p["n_tiles"] == 2 and 2 < p["grid"] <= 2 + 8      # no more workers than tiles
+    q = lr.linrec_plan_16(1, 1 << 20, 64, path="chunked", chunk_mode="chain", sm_count=152, resident_ctas=2)
+    assert (q["chain"], q["tile_t"], q["vec"], q["segments"]) == (1, 256, 2, 8)
+    with pytest.raises(lr.LinrecError):
+        lr.linrec_plan_f32_backward(1, 1 << 20, 64, chunk_mode="chain")
+    with pytest.raises(lr.LinrecError):
+        lr.linrec_plan_f32(1, 1 << 20, 64, chunk_mode="chain", tile_t=64)     # not compiled for chain mode
     # blocks mode: one launch, `group` tiles per block (1024 steps by default), three look-back
     # words per block and channel; forward only; group is taken by blocks mode alone
     p = lr.linrec_plan_f32(1, 1 << 20, 64, path="chunked", chunk_mode="blocks", sm_count=152, resident_ctas=2)
@@ -522,6 +536,25 @@ def test_gradient_host_and_noalloc_argument_checks(L):
     assert na(a + 4, b, da, B, Lx, D, None, None) == lr.LINREC_ERR_INVALID_VALUE   # not 16-byte aligned
     assert na(a, b, da, B, Lx, 6, None, None) == lr.LINREC_ERR_INVALID_VALUE      # D not a multiple of 4
     assert na(16, 32, 64, 1 << 20, 1 << 20, 1 << 22, None, None) == lr.LINREC_ERR_INVALID_VALUE
+
+
+def test_host_range_check():
+    """linrec_scan_f32_host reads a page-locked buffer in place only when the registered range of
+    its first byte holds every byte; a range that ends early (a registered prefix), starts late,
+    or wraps around the address space sends the buffer through the copy pipeline."""
+    covers = lr.linrec_debug_range_covers
+    base, size = 1 << 40, 1 << 20
+    assert covers(base, size, base, size)
+    assert covers(base, size, base + 4096, size - 4096)
+    assert covers(base, size, base + size - 4, 4)
+    assert not covers(base, size, base, size + 1)                 # the last byte outside
+    assert not covers(base, size, base + 4096, size)              # ends past the range
+    assert not covers(base, size, base - 4, 8)                    # starts before it
+    assert not covers(base, size, base + size, 4)                 # just past the end
+    assert not covers(base, size, base, 0)                        # nothing to cover
+    top = (1 << 64) - 4096
+    assert covers(top, 4096, top, 4096)
+    assert not covers(top, 4096, top + 8, (1 << 64) - 1)          # would wrap
 
 
 def test_no_cpu_fallback():

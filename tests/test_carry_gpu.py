@@ -21,7 +21,8 @@ PATHS = [{}, {"path": "regcarry"}, {"path": "regcarry", "vec": 1, "prefetch": 4}
          {"path": "chunked", "chunk_mode": "twopass"},
          {"path": "chunked", "chunk_mode": "twopass", "tile_d": 64, "tile_t": 64, "stages": 2},
          {"path": "chunked", "chunk_mode": "blocks"},
-         {"path": "chunked", "chunk_mode": "blocks", "tile_d": 64, "group": 3}]
+         {"path": "chunked", "chunk_mode": "blocks", "tile_d": 64, "group": 3},
+         {"path": "chunked", "chunk_mode": "chain"}]
 
 
 @pytest.fixture(scope="module", autouse=True)

@@ -49,7 +49,7 @@ def _forward_options(D):
         opts.append({"path": "regcarry", "vec": 2, "prefetch": 8})
     if D % 4 == 0:
         opts.append({"path": "regcarry", "vec": 4, "prefetch": 16})
-        for mode in ("own", "lookback", "twopass", "blocks"):
+        for mode in ("own", "lookback", "twopass", "blocks", "chain"):
             opts.append({"path": "chunked", "chunk_mode": mode})
         opts.append({"path": "chunked", "chunk_mode": "blocks", "tile_d": 64, "group": 2})
     return opts
@@ -85,7 +85,7 @@ def test_16bit_storage(kind, shape):
     scan = {"bf16": lr.linrec_scan_bf16_ex, "f16": lr.linrec_scan_f16_ex}[kind]
     opts = [{}, {"path": "regcarry", "vec": 1, "prefetch": 4}]
     if D % 8 == 0:
-        opts += [{"path": "chunked", "chunk_mode": m} for m in ("own", "lookback", "twopass", "blocks")]
+        opts += [{"path": "chunked", "chunk_mode": m} for m in ("own", "lookback", "twopass", "blocks", "chain")]
         opts.append({"path": "chunked", "chunk_mode": "own", "vec": 1})
     u = UNIT[kind]
     for opt in opts:

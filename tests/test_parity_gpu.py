@@ -40,6 +40,8 @@ def legal_paths(B, L, D, aligned=True):
         paths.append({"path": "chunked", "chunk_mode": "lookback"})
         paths.append({"path": "chunked", "chunk_mode": "twopass"})
         paths.append({"path": "chunked", "chunk_mode": "blocks"})
+        if B * -(-D // 32) <= 128:         # chain mode serves few slices only
+            paths.append({"path": "chunked", "chunk_mode": "chain"})
     return paths
 
 
@@ -160,6 +162,26 @@ def test_chunk_modes_agree_bit_for_bit(tile):
         assert torch.equal(h_own, h_lb), f"{tile} {(B, L, D)}"
 
 
+@pytest.mark.parametrize("shape", [(2, 3000, 128), (1, 50000, 64), (3, 1000, 260), (1, 129, 32), (5, 4097, 36)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_chain_mode_same_bits_as_slice_owner(shape):
+    """Chain mode folds every slice's tile maps in chunk order, H_q = A_q*H_{q-1} + B_q, the
+    chain slice-owner mode carries in a register: the same tile gives identical bits, with
+    and without a carried-in state."""
+    B, L, D = shape
+    a, b = inputs.generate(B, L, D, seed=7 + L, a_dist="u[0,1)", b_dist="n(0,1)")
+    a_d, b_d = a.to(DEV), b.to(DEV)
+    tile = {"path": "chunked", "tile_d": 32, "tile_t": 128}
+    assert lr.linrec_plan_f32(B, L, D, chunk_mode="chain", **tile)["chain"] == 1
+    assert torch.equal(run(a_d, b_d, chunk_mode="chain", **tile), run(a_d, b_d, chunk_mode="own", **tile))
+    h0 = torch.randn(B, D, device=DEV)
+    outs = []
+    for mode in ("chain", "own"):
+        last = torch.empty(B, D, device=DEV)
+        outs.append((run(a_d, b_d, chunk_mode=mode, h_init=h0, h_last=last, **tile), last))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
 @pytest.mark.parametrize("vec,prefetch", [(v, p) for v in (1, 2, 4) for p in (4, 8, 16)])
 def test_every_regcarry_variant(vec, prefetch):
     B, L, D = 2, 515, 132
@@ -205,11 +227,12 @@ def test_deterministic_bits():
                 assert torch.equal(run(a_d, b_d, **opt), h1), f"{name} {opt}: bits changed between calls"
 
 
-@pytest.mark.parametrize("mode", ["lookback", "twopass", "blocks"])
+@pytest.mark.parametrize("mode", ["lookback", "twopass", "blocks", "chain"])
 def test_carry_modes_repeat_bit_identical(mode):
-    """A race check on the cross-CTA carry: 50 calls of the look-back, two-pass or blocks mode,
-    whose tiles land on different CTAs in a different order every time, all return the same bits."""
-    second = {"tile_d": 32, "tile_t": 64, "stages": 3} if mode != "blocks" else {"tile_d": 64, "group": 3}
+    """A race check on the cross-CTA carry: 50 calls of the look-back, two-pass, blocks or chain
+    mode, whose tiles land on different CTAs in a different order every time, all return the same
+    bits."""
+    second = {"blocks": {"tile_d": 64, "group": 3}, "chain": {}}.get(mode, {"tile_d": 32, "tile_t": 64, "stages": 3})
     for (B, L, D, tile) in [(1, 1 << 18, 64, {}), (2, 50000, 128, second)]:
         a, b = inputs.generate(B, L, D, seed=19 + L, a_dist="u[0.9,1)", b_dist="n(0,1)")
         a_d, b_d = a.to(DEV), b.to(DEV)
@@ -323,7 +346,7 @@ def test_concurrent_host_threads():
     library serialises its bookkeeping, each stream gets its own workspace, and every call returns
     the bits of the same call made alone."""
     import threading
-    modes = ["own", "lookback", "twopass", "blocks", "regcarry", "lookback"]
+    modes = ["own", "lookback", "twopass", "blocks", "regcarry", "chain"]
     jobs = []
     for k, mode in enumerate(modes):
         a, b = inputs.generate(2, 20000, 96, seed=70 + k, a_dist="u[0.9,1)", b_dist="n(0,1)")
@@ -372,7 +395,7 @@ def test_modes_alternating_on_one_stream():
     for k in range(3):
         h1 = run(*d1, path="chunked", chunk_mode="twopass")
         assert_close(h1.cpu().numpy(), want1, f"two-pass, call {k}")
-        for mode in ("lookback", "twopass", "blocks", "lookback", "blocks"):
+        for mode in ("lookback", "twopass", "blocks", "chain", "lookback", "blocks", "chain"):
             h2 = run(*d2, path="chunked", chunk_mode=mode)
             assert_close(h2.cpu().numpy(), want2, f"{mode} after two-pass, call {k}")
     assert lr.linrec_stream_status() == lr.LINREC_OK
@@ -459,6 +482,61 @@ def test_lookback_timeout_reports_and_recovers():
                                   chunk_mode="lookback")
     s.synchronize()
     assert_close(h.cpu().numpy(), h64, "after recovery")
+    assert lr.linrec_stream_status(s) == lr.LINREC_OK
+
+
+def test_chain_timeout_reports_and_recovers():
+    """Chain mode: tile 5 publishes no map, so the resolver stops before it and the workers
+    after it give up on their carries (bounded waits): the status word says so, the output
+    before it is intact, NaN marks the lost carries, and the next call on the stream is exact."""
+    B, L, D = 1, 64 * 128, 32
+    a, b = inputs.generate(B, L, D, seed=17, a_dist="u[0.5,1)", b_dist="n(0,1)")
+    h64, _ = oracle.f64(a, b)
+    a_d, b_d = a.to(DEV), b.to(DEV)
+    s = torch.cuda.Stream()
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    opt = dict(path="chunked", chunk_mode="chain")
+    with torch.cuda.stream(s):
+        h = lr.linrec_scan_f32_ex(a_d, b_d, stream=s, spin_limit=2000, test_silent_tile=5 + 1, d_status=status,
+                                  **opt)
+    s.synchronize()
+    assert int(status.item()) & (1 << lr.LINREC_ERR_LOOKBACK_TIMEOUT)
+    hn = h.cpu().numpy()
+    assert_close(hn[:, :6 * 128], h64[:, :6 * 128], "chain before the timeout")
+    assert np.isnan(hn[:, 6 * 128:]).any()
+    with torch.cuda.stream(s):
+        lr.linrec_scan_f32_ex(a_d, b_d, stream=s, spin_limit=2000, test_silent_tile=5 + 1, **opt)
+    assert lr.linrec_stream_status(s) == lr.LINREC_ERR_LOOKBACK_TIMEOUT
+    with torch.cuda.stream(s):
+        h = lr.linrec_scan_f32_ex(a_d, b_d, stream=s, **opt)
+    s.synchronize()
+    assert_close(h.cpu().numpy(), h64, "chain after recovery")
+    assert lr.linrec_stream_status(s) == lr.LINREC_OK
+
+
+@pytest.mark.parametrize("mode", ["lookback", "chain", "blocks"])
+def test_epoch_wraps_around(mode):
+    """The stream workspace's epoch word set just below the point where it wraps: consecutive
+    launches still tag their words differently, so four calls in a row return slice-owner mode's
+    bits (look-back, chain) or the same bits every time (blocks)."""
+    B, L, D = 1, 1 << 19, 64
+    a, b = inputs.generate(B, L, D, seed=65, a_dist="u[0.9,1)", b_dist="n(0,1)")
+    a_d, b_d = a.to(DEV), b.to(DEV)
+    s = torch.cuda.Stream()
+    tile = {"tile_d": 32, "tile_t": 128} if mode != "blocks" else {}
+    with torch.cuda.stream(s):
+        first = lr.linrec_scan_f32_ex(a_d, b_d, stream=s, path="chunked", chunk_mode=mode, **tile)
+        want = lr.linrec_scan_f32_ex(a_d, b_d, stream=s, path="chunked", chunk_mode="own", **tile) \
+            if mode != "blocks" else first.clone()
+    s.synchronize()
+    lr.linrec_debug_set_epoch(0xFFFFFFFD, stream=s)
+    h = torch.empty_like(a_d)
+    for call in range(4):
+        with torch.cuda.stream(s):
+            h.fill_(float("nan"))
+            lr.linrec_scan_f32_ex(a_d, b_d, h, stream=s, path="chunked", chunk_mode=mode, **tile)
+        s.synchronize()
+        assert torch.equal(h, want), f"{mode} call {call} across the epoch wrap"
     assert lr.linrec_stream_status(s) == lr.LINREC_OK
 
 

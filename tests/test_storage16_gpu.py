@@ -53,10 +53,12 @@ def assert_close16(kind, h, h64, what):
                              f"got {x[first]}, want {h64[first]}")
 
 
-def paths(D, aligned=True):
+def paths(D, aligned=True, B=1):
     out = [{"path": "regcarry"}]
     if aligned and D % 8 == 0:
         out += [{"path": "chunked", "chunk_mode": m} for m in ("own", "lookback", "twopass", "blocks")]
+        if B * -(-D // 32) <= 64:          # chain mode serves few slices only
+            out.append({"path": "chunked", "chunk_mode": "chain"})
     return out
 
 
@@ -80,7 +82,7 @@ def test_workload_full_size(kind, name):
     del a, b
     h64, _ = oracle.f64_16(kind, a16, b16)
     a_d, b_d = a16.to(DEV), b16.to(DEV)
-    for opt in [{}] + paths(w.D):
+    for opt in [{}] + paths(w.D, B=w.B):
         h = run(kind, a_d, b_d, **opt)
         assert_close16(kind, h, h64, f"{kind} {name} {opt}")
         del h
@@ -97,7 +99,7 @@ def test_integer_closed_forms_bit_exact(kind):
     ones = torch.full((B, L, D), ONE[kind], dtype=torch.int16).view(inputs.STORAGE16[kind])
     want = oracle.encode16(kind, np.cumsum(bi.double().numpy(), axis=1))
     b_d, ones_d, zeros_d = b16.to(DEV), ones.to(DEV), torch.zeros_like(b16).to(DEV)
-    for opt in [{}] + paths(D):
+    for opt in [{}] + paths(D, B=B):
         assert np.array_equal(words(run(kind, ones_d, b_d, **opt)), want), f"a = 1 {opt}"
         assert torch.equal(run(kind, zeros_d, b_d, **opt), b_d), f"a = 0 {opt}"
 
@@ -114,7 +116,9 @@ def test_same_arithmetic_as_the_fp32_path(kind):
     # ring depth does not change the arithmetic)
     # (blocks mode is compiled for the 256-step 16-bit tile only)
     same = {"tile_d": 32, "tile_t": 128, "stages": 3}
-    opts = [dict(o, **same) if o.get("path") == "chunked" else o for o in paths(D) if o.get("chunk_mode") != "blocks"]
+    # (chain mode's 16-bit variant has 256-step tiles only: no fp32 twin)
+    opts = [dict(o, **same) if o.get("path") == "chunked" else o for o in paths(D, B=B)
+            if o.get("chunk_mode") not in ("blocks", "chain")]
     for opt in opts + [{"path": "chunked", "tile_d": 64, "tile_t": 128, "stages": 2, "chunk_mode": "lookback"}]:
         h16 = run(kind, a_d, b_d, **opt)
         f32opt = dict(opt)
@@ -137,7 +141,7 @@ def test_ragged_shapes(kind, shape):
     a16, b16 = draw16(kind, B, L, D, 82 + L + D, a_dist="u[0.5,1)")
     h64, _ = oracle.f64_16(kind, a16, b16)
     a_d, b_d = a16.to(DEV), b16.to(DEV)
-    for opt in [{}] + paths(D):
+    for opt in [{}] + paths(D, B=B):
         assert_close16(kind, run(kind, a_d, b_d, **opt), h64, f"{kind} {shape} {opt}")
 
 
@@ -190,6 +194,22 @@ def test_every_chunked_variant_and_mode(kind, tile):
 
 
 @pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("shape", [(2, 3001, 200), (1, 40000, 64), (1, 257, 8)], ids=lambda s: "x".join(map(str, s)))
+def test_chain_mode_same_words_as_slice_owner(kind, shape):
+    """Chain mode on 16-bit storage folds the tile maps in chunk order, as slice-owner mode does
+    with the same tile (256 steps, two channels per thread, 8 segments): the same words."""
+    B, L, D = shape
+    a16, b16 = draw16(kind, B, L, D, 91 + L)
+    h64, _ = oracle.f64_16(kind, a16, b16)
+    a_d, b_d = a16.to(DEV), b16.to(DEV)
+    tile = dict(path="chunked", tile_d=32, tile_t=256, vec=2, segments=8)
+    h = run(kind, a_d, b_d, chunk_mode="chain", **tile)
+    assert_close16(kind, h, h64, f"{kind} {shape} chain")
+    assert torch.equal(h, run(kind, a_d, b_d, chunk_mode="own", stages=2, **tile))
+    assert lr.linrec_stream_status() == lr.LINREC_OK
+
+
+@pytest.mark.parametrize("kind", KINDS)
 @pytest.mark.parametrize("shape", [(2, 3001, 200), (3, 1000, 264), (1, 257, 8)], ids=lambda s: "x".join(map(str, s)))
 def test_two_channels_per_thread_same_bits(kind, shape):
     """One or two channels per thread, same tile and segments: the same fma sequence, the same words."""
@@ -221,7 +241,7 @@ def test_carry_state_is_fp32(kind, shape):
     h0 = torch.randn((B, D), generator=g)
     h64, last64 = oracle.f64_16(kind, a16, b16, h0.double().numpy())
     a_d, b_d, h0_d = a16.to(DEV), b16.to(DEV), h0.to(DEV)
-    for opt in [{}] + paths(D):
+    for opt in [{}] + paths(D, B=B):
         last = torch.full((B, D), float("nan"), device=DEV)
         h = run(kind, a_d, b_d, h_init=h0_d, h_last=last, **opt)
         assert_close16(kind, h, h64, f"{kind} {shape} {opt}")

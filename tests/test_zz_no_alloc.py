@@ -4,8 +4,9 @@ memory (graph capture, real-time loops, hosts that own every allocation).
 
 Its results are checked against the ordinary entry point, linrec_scan_f32,
 within the tolerance the other parity tests use, on two calls in a row (the
-second call runs on the array as the first one left it).  This file is
-collected last so that a stop at the first failure has run everything else.
+second call runs on the array as the first one left it), and every element
+against the fp64 oracle.  This file is collected last so that a stop at the
+first failure has run everything else.
 """
 import ctypes
 
@@ -14,6 +15,7 @@ import pytest
 import torch
 
 import linear_recurrence_scan_fp32_gb300 as lr
+import oracle
 from linear_recurrence_scan_fp32_gb300 import inputs
 from tests._util import assert_close
 
@@ -47,13 +49,59 @@ def test_noalloc_matches_the_allocating_entry_point(noalloc, shape):
     a_d, b_d = a.to(DEV), b.to(DEV)
     want = lr.linrec_scan_f32(a_d, b_d)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    h64, _ = oracle.f64(a, b)
     for call in range(2):
         h = torch.full_like(a_d, float("nan"))
         code = noalloc(a_d.data_ptr(), b_d.data_ptr(), h.data_ptr(), B, L, D, _stream(), status.data_ptr())
         assert code == lr.LINREC_OK, lr.linrec_status_string(code)
         torch.cuda.synchronize()
         assert int(status.item()) == 0, f"call {call}: device status {int(status.item())}"
-        assert_close(h.cpu().numpy(), want.cpu().numpy().astype(np.float64), f"{shape} call {call}")
+        got = h.cpu().numpy()
+        assert_close(got, want.cpu().numpy().astype(np.float64), f"{shape} call {call}")
+        assert_close(got, h64, f"{shape} call {call} against the oracle")
+
+
+def test_noalloc_modes_alternating(noalloc):
+    """Calls whose plans take slice-owner mode (many slices: only the control block is used) and
+    look-back mode (few long slices: the look-back words) alternate on the one array; each output
+    agrees with linrec_scan_f32 and with the oracle, and the array's own status word stays clear."""
+    cases = []
+    for (B, L, D, seed) in [(32, 4096, 256, 61), (1, 1 << 20, 64, 62), (3, 1000, 260, 63)]:
+        a, b = inputs.generate(B, L, D, seed=seed, a_dist="u[0.9,1)", b_dist="n(0,1)")
+        a_d, b_d = a.to(DEV), b.to(DEV)
+        cases.append((B, L, D, a_d, b_d, lr.linrec_scan_f32(a_d, b_d), oracle.f64(a, b)[0]))
+    for k in range(3):
+        for (B, L, D, a_d, b_d, want, h64) in cases:
+            h = torch.full_like(a_d, float("nan"))
+            code = noalloc(a_d.data_ptr(), b_d.data_ptr(), h.data_ptr(), B, L, D, _stream(), None)
+            assert code == lr.LINREC_OK, lr.linrec_status_string(code)
+            torch.cuda.synchronize()
+            assert_close(h.cpu().numpy(), want.cpu().numpy().astype(np.float64), f"{(B, L, D)} round {k}")
+            assert_close(h.cpu().numpy(), h64, f"{(B, L, D)} round {k} against the oracle")
+    # failures of calls made without a status word of their own would show here
+    assert lr.linrec_stream_status() == lr.LINREC_OK
+
+
+def test_noalloc_epoch_wraps_around(noalloc):
+    """The array's epoch word set just below the point where it wraps: four look-back calls in a row
+    each tag their words differently from the call before, so none takes the previous call's words
+    for its own; every output agrees with linrec_scan_f32."""
+    B, L, D = 1, 1 << 20, 64
+    a, b = inputs.generate(B, L, D, seed=64, a_dist="u[0.9,1)", b_dist="n(0,1)")
+    a_d, b_d = a.to(DEV), b.to(DEV)
+    want = lr.linrec_scan_f32(a_d, b_d).cpu().numpy().astype(np.float64)
+    h = torch.empty_like(a_d)
+    assert noalloc(a_d.data_ptr(), b_d.data_ptr(), h.data_ptr(), B, L, D, _stream(), None) == lr.LINREC_OK
+    lr.linrec_debug_set_epoch(0xFFFFFFFD, fixed_array=True)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    for call in range(4):
+        h.fill_(float("nan"))
+        code = noalloc(a_d.data_ptr(), b_d.data_ptr(), h.data_ptr(), B, L, D, _stream(), status.data_ptr())
+        assert code == lr.LINREC_OK, lr.linrec_status_string(code)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0, f"call {call}: device status {int(status.item())}"
+        assert_close(h.cpu().numpy(), want, f"call {call} across the epoch wrap")
+    assert lr.linrec_stream_status() == lr.LINREC_OK
 
 
 def test_noalloc_rejects_what_does_not_fit(noalloc):
