@@ -25,6 +25,13 @@ constexpr int kRegcarryThreads = 256;
 constexpr int64_t kRegcarryMinThreadsPerSm = 96;
 // Few slices: the two-pass mode from this many time chunks of 128 steps on.
 constexpr int64_t kTwoPassMinChunks = 64;
+// fp32 forward scans that would take the two-pass mode take chain mode instead from this
+// many 32-channel slices on.  Measured on GB300 (us per call, two-pass -> chain): (4, 131072,
+// 128) 206 -> 191, (4, 65536, 256) 209 -> 185, (8, 32768, 256) 208 -> 183, (3, 32768, 1024)
+// 306 -> 278, (4, 8192, 256) 31.9 -> 29.3, (2, 16384, 256) 32.1 -> 31.0; with fewer slices
+// chain mode loses ((2, 262144, 128) 208 -> 214, (1, 1048576, 64) 212 -> 528), and in
+// 16-bit storage it loses at every slice count measured.
+constexpr int64_t kChainMinSlices = 16;
 // Wide slices (see plan_impl): from this many time steps, on a grid of at least this
 // share of the SMs.
 constexpr int64_t kWideMinSteps = 256;
@@ -433,6 +440,9 @@ linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int ali
         own = B * ((D + td - 1) / td) >= need;
         const int tt = opt->tile_t ? opt->tile_t : (dtype == kDtypeF32 ? 128 : tile_t_16(L));
         twopass = !own && allow_twopass && (L + tt - 1) / tt >= kTwoPassMinChunks;
+        if (twopass && dtype == kDtypeF32 && !backward && opt->tile_d == 0 && opt->tile_t == 0 &&
+            opt->stages == 0 && B * ((D + 31) / 32) >= kChainMinSlices)
+            return plan_chain(B, L, D, sm_count, ctas_per_sm, opt, plan, variant_index, dtype);
     } else {
         own = opt->chunk_mode == 1;
         twopass = opt->chunk_mode == 3;

@@ -104,6 +104,9 @@ WORKLOADS: Dict[str, Workload] = {w.name: w for w in [
              "gated wide scan (64,2048,1024), a=sigmoid(z), b~N(0,0.5)"),
     Workload("short", 256, 128, 4096, 4, "u[0,1)", "n(0,1)",
              "many short scans (256,128,4096), a~U[0,1), b~N(0,1)"),
+    # long sequences over more channels: 32 slices of 32 channels, the chain mode's shape
+    Workload("long32", 4, 65536, 256, 5, "u[0.9,1)", "n(0,1)",
+             "long sequences, 32 channel slices (4,65536,256), a~U[0.9,1), b~N(0,1)"),
     # closed-form variants on the many-short-scans shape
     Workload("short_ones", 256, 128, 4096, 4, "ones", "n(0,1)", "a=1: inclusive prefix sum of b"),
     Workload("short_zeros", 256, 128, 4096, 4, "zeros", "n(0,1)", "a=0: h=b"),

@@ -456,7 +456,7 @@ def test_plan_invariants_over_a_grid():
     import itertools
     Bs, Ls, Ds = [1, 3, 16, 40, 128], [1, 100, 300, 2048, 1 << 16], [1, 6, 8, 33, 64, 256, 777, 1024, 4096]
     planners = [(lr.linrec_plan_f32, 4), (lr.linrec_plan_16, 2), (lr.linrec_plan_f32_backward, 4)]
-    n_plans = 0
+    n_plans = n_chain = 0
     for (B, L, D), (planner, eb), kw in itertools.product(
             itertools.product(Bs, Ls, Ds), planners,
             ({}, {"resident_ctas": 2}, {"align_bytes": 4}, {"path": "chunked"})):
@@ -480,13 +480,34 @@ def test_plan_invariants_over_a_grid():
         assert p["threads"] == p["tile_d"] // p["vec"] * p["segments"] and p["tile_t"] % p["segments"] == 0
         slices = B * -(-D // p["tile_d"])
         assert p["chunks"] == -(-L // p["tile_t"]) and p["n_tiles"] == slices * p["chunks"]
+        if p["chain"]:                         # every resident CTA: resolvers, then one worker per tile at most
+            assert eb == 4 and slices >= 16 and kw.get("path") != "regcarry"
+            assert 1 < p["grid"] <= min(p["n_tiles"] + 16, 152 * 2)
+            assert p["workspace_bytes"] == 256 + 24 * p["n_tiles"] * p["tile_d"]
+            n_chain += 1
+            continue
         units = slices if not (p["lookback"] or p["twopass"] or p["blocks"]) else p["n_tiles"]
         assert 1 <= p["grid"] <= units
         if p["lookback"]:
             assert p["workspace_bytes"] == 256 + 24 * p["n_tiles"] * p["tile_d"]
         elif not p["twopass"] and not p["blocks"]:
             assert p["workspace_bytes"] == 256
-    assert n_plans > 1000
+    assert n_plans > 1000 and n_chain > 0
+
+
+def test_plan_chain_mode_by_default():
+    """fp32 forward scans that would take the two-pass mode take chain mode from 16 slices of
+    32 channels on; fewer slices, 16-bit storage and the gradient keep the two-pass mode."""
+    for (B, L, D) in [(4, 65536, 256), (4, 131072, 128), (3, 32768, 1024), (2, 16384, 256)]:
+        p = lr.linrec_plan_f32(B, L, D, sm_count=152, resident_ctas=2)
+        assert p["chain"] == 1 and p["twopass"] == 0, (B, L, D)
+    for (B, L, D) in [(1, 1 << 20, 64), (2, 262144, 128), (1, 65536, 64)]:
+        p = lr.linrec_plan_f32(B, L, D, sm_count=152, resident_ctas=2)
+        assert p["chain"] == 0 and p["twopass"] == 1, (B, L, D)
+    assert lr.linrec_plan_16(4, 65536, 256, sm_count=152)["chain"] == 0
+    assert lr.linrec_plan_f32_backward(4, 65536, 256, sm_count=152)["chain"] == 0
+    # a forced tile keeps the mode it names or the two-pass mode
+    assert lr.linrec_plan_f32(4, 65536, 256, sm_count=152, tile_d=32, tile_t=128, stages=2)["chain"] == 0
 
 
 def test_gradient_host_and_noalloc_argument_checks(L):
