@@ -264,33 +264,34 @@ def _rate(nbytes: int, numel: int, reps: int, seconds: float, cores: int) -> dic
             "repetitions": reps}
 
 
-def cpu_baseline(a, b, w, budget_s: float = 10.0, dtype: str = "f32", h_gpu=None):
-    """The oracle as it stands on the host cores, each form over the full workload with its
-    output allocated once: the fp64 definition on all cores (the line's value) and on one core,
-    and the fp32 twin on all cores (16-bit storage: decode + fp64 scan on all cores only).
-    Returns (baseline, parity): parity compares h_gpu, the output of the timed GPU run, with
-    the fp64 oracle's result, element by element."""
+def cpu_baseline(a, b, w, budget_s: float = 10.0, dtype: str = "f32", h_gpu=None, layout: str = "bld"):
+    """The oracle as it stands on the host cores: the reference arm itself (--impl reference, the
+    fp64 definition on all cores, plus --extra-forms: one core, and the fp32 twin on all cores), run
+    as a child process that does not use the GPU, on a budget of about budget_s seconds.  So the
+    bench line and the reference arm report one measurement method.  Returns (baseline, parity):
+    parity compares h_gpu, the output of the timed GPU run, with the fp64 oracle's result (computed
+    here, untimed), element by element."""
     import oracle
     oracle.build()
-    threads = oracle.hardware_threads()
-    nbytes = bytes_per_step(w, "forward", dtype)
-    t64 = OracleTimer(a, b, dtype, "f64", threads)
-    reps, secs, h64 = t64.repeat(budget_s)
-    what = "fp64 sequential oracle" if dtype == "f32" else f"oracle {dtype} decode + fp64 scan"
-    base = {**_rate(nbytes, w.numel, reps, secs, t64.used), "kind": "oracle",
-            "sample": f"full {w.name} workload {w.shape}, {what}, all host cores, {reps} repetitions, "
-                      f"{secs:.1f} s, output allocated once",
-            "method": "the same timer as the reference arm (OracleTimer): one output array per form, "
-                      "run before the pinned host buffers of the e2e leg exist"}
-    if dtype == "f32":
-        one = OracleTimer(a, b, dtype, "f64", 1)
-        r1, s1, _ = one.repeat(budget_s / 2)
-        base["fp64_1core"] = _rate(nbytes, w.numel, r1, s1, one.used)
-        f32 = OracleTimer(a, b, dtype, "f32seq", threads)
-        r2, s2, _ = f32.repeat(budget_s / 2)
-        base["f32seq_all_cores"] = _rate(nbytes, w.numel, r2, s2, f32.used)
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "LOCAL_WORLD_SIZE", "MASTER_ADDR", "MASTER_PORT")}
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", w.name,
+           "--dtype", dtype, "--layout", layout, "--steps", "5", "--warmup", "3", "--ref-seconds", str(budget_s),
+           "--extra-forms"]
+    base = None
+    try:
+        out = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=30 + 10 * budget_s)
+        for line in out.stdout.splitlines():
+            if line.startswith("{"):
+                base = json.loads(line)["cpu_baseline"]
+                base["method"] = ("the reference arm (bench.py --impl reference --extra-forms --steps 5 --warmup 3 "
+                                  f"--ref-seconds {budget_s:g}) in a child process that does not use the GPU")
+    except (OSError, subprocess.TimeoutExpired, ValueError, KeyError):
+        base = None
     parity = None
-    if h_gpu is not None and h64 is not None:
+    if h_gpu is not None:
+        h64 = OracleTimer(a, b, dtype, "f64", oracle.hardware_threads())()
         # 16-bit storage: the output words, decoded by the oracle's own definition of the format
         got = np.asarray(h_gpu, dtype=np.float64) if dtype == "f32" else oracle.decode16(dtype, h_gpu)
         err = np.abs(got - h64)
@@ -362,6 +363,15 @@ def run_reference(args):
     total = sum(times)
     used = timer.used
     value = sample_bytes * args.steps / total / 1e9
+    elems = a_s.size * reps * args.steps
+    extra = {}
+    if args.extra_forms and args.dtype == "f32":
+        # the other forms of the oracle on the same sample: the fp64 definition on one core and the
+        # fp32 twin on all cores, each for a third of the budget
+        for key, form, nthreads in (("fp64_1core", "f64", 1), ("f32seq_all_cores", "f32seq", threads)):
+            t = OracleTimer(a_s, b_s, args.dtype, form, nthreads)
+            r, secs, _ = t.repeat(args.ref_seconds / 3)
+            extra[key] = _rate(3 * STORAGE_BYTES[args.dtype] * a_s.size, a_s.size, r, secs, t.used)
     line = {
         "impl": "reference", "metric": metric_for(w, "forward", args.dtype, args.layout), "value": round(value, 3), "unit": UNIT,
         "n_gpus": world,
@@ -371,9 +381,12 @@ def run_reference(args):
         "config": {"workload": w.about, "B": w.B, "L": w.L, "D": w.D, "seed": w.seed, "storage": args.dtype,
                    "l2": "host run: no device cache involved"},
         "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": used, "kind": "oracle",
+                         "elements_per_s": round(elems / total, 1),
+                         "ms_per_workload": round(1e3 * total / (reps * args.steps) * (w.numel / a_s.size), 3),
                          "sample": f"per step: {reps} scan(s) of batches 0..{nb - 1}, steps 0..{nl - 1}, all "
                                    f"{w.D} channels of the {w.name} workload {w.shape} ({a_s.size} elements), "
-                                   "output allocated once"},
+                                   "output allocated once, in a process that does not use the GPU",
+                         **extra},
         "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -544,10 +557,12 @@ def run_ours(args):
             if bdl:
                 hc = hc.transpose(1, 2).contiguous()
             if args.dtype == "f32":
-                cpu, parity = cpu_baseline(ca.numpy(), cb.numpy(), w, budget_s=args.cpu_seconds, h_gpu=hc.numpy())
+                cpu, parity = cpu_baseline(ca.numpy(), cb.numpy(), w, budget_s=args.cpu_seconds, h_gpu=hc.numpy(),
+                                           layout=args.layout)
             else:
                 words = hc.view(torch.int16).numpy().view(np.uint16)
-                cpu, parity = cpu_baseline(ca, cb, w, budget_s=args.cpu_seconds, dtype=args.dtype, h_gpu=words)
+                cpu, parity = cpu_baseline(ca, cb, w, budget_s=args.cpu_seconds, dtype=args.dtype, h_gpu=words,
+                                           layout=args.layout)
 
     # end to end through the public API: pinned host inputs in, result out, every step
     e2e = None
@@ -646,6 +661,8 @@ def main(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--ref-seconds", type=float, default=30.0,
                    help="reference arm: CPU time budget for warm-up + timed steps")
+    p.add_argument("--extra-forms", action="store_true",
+                   help="reference arm: also time the fp64 oracle on one core and the fp32 twin on all cores")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be at least 3")

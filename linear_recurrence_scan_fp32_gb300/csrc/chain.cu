@@ -515,7 +515,7 @@ chain_scan_kernel(const __grid_constant__ CUtensorMap map_a,
     }
 }
 
-#define LINREC_CHAIN_F32_VARIANTS(X) X(32, 128, 8, 3, 1)
+#define LINREC_CHAIN_F32_VARIANTS(X) X(32, 128, 8, 3, 1) X(32, 256, 16, 3, 1)
 #define LINREC_CHAIN_16_VARIANTS(X) X(32, 256, 8, 3, 2)
 
 template <int DT, int TD, int TT, int S, int ST, int CPT>

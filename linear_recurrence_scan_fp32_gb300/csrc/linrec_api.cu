@@ -26,12 +26,15 @@ constexpr int64_t kRegcarryMinThreadsPerSm = 96;
 // Few slices: the two-pass mode from this many time chunks of 128 steps on.
 constexpr int64_t kTwoPassMinChunks = 64;
 // fp32 forward scans that would take the two-pass mode take chain mode instead from this
-// many 32-channel slices on.  Measured on GB300 (us per call, two-pass -> chain): (4, 131072,
-// 128) 206 -> 191, (4, 65536, 256) 209 -> 185, (8, 32768, 256) 208 -> 183, (3, 32768, 1024)
-// 306 -> 278, (4, 8192, 256) 31.9 -> 29.3, (2, 16384, 256) 32.1 -> 31.0; with fewer slices
-// chain mode loses ((2, 262144, 128) 208 -> 214, (1, 1048576, 64) 212 -> 528), and in
+// many 32-channel slices on, with 256-step tiles from kChainLongSteps steps on (half the
+// tiles for the resolvers to fold), 128-step tiles below.  Measured on GB300 (us per call,
+// two-pass -> chain): (2, 131072, 128) 112 -> 106, (3, 131072, 128) 160 -> 145, (6, 65536,
+// 128) 158 -> 138, (4, 65536, 256) 209 -> 183, (3, 32768, 1024) 306 -> 262, (1, 32768, 512)
+// 61.7 -> 55.8, (16, 8192, 128) 59.8 -> 53.6 (128-step tiles; 55.1 with 256); with fewer
+// slices chain mode loses ((1, 524288, 128) 211 -> 228, (1, 1048576, 64) 212 -> 328), and in
 // 16-bit storage it loses at every slice count measured.
-constexpr int64_t kChainMinSlices = 16;
+constexpr int64_t kChainMinSlices = 8;
+constexpr int64_t kChainLongSteps = 32768;
 // Wide slices (see plan_impl): from this many time steps, on a grid of at least this
 // share of the SMs.
 constexpr int64_t kWideMinSteps = 256;
@@ -282,9 +285,11 @@ linrec_status_t plan_chain(int64_t B, int64_t L, int64_t D, int sm_count, int ct
     int n = 0;
     const ChunkedVariant *vars = chain_variants(dtype, &n);
     const ChunkedVariant *v = nullptr;
+    // fp32: 256-step tiles for long sequences, 128-step ones below (the 16-bit variant has 256)
+    const int want_t = opt->tile_t ? opt->tile_t : (dtype == kDtypeF32 ? (L >= kChainLongSteps ? 256 : 128) : 0);
     for (int i = 0; i < n && !v; ++i) {
         const ChunkedVariant &c = vars[i];
-        if ((opt->tile_d == 0 || opt->tile_d == c.tile_d) && (opt->tile_t == 0 || opt->tile_t == c.tile_t) &&
+        if ((opt->tile_d == 0 || opt->tile_d == c.tile_d) && (want_t == 0 || want_t == c.tile_t) &&
             (opt->stages == 0 || opt->stages == c.stages) && (opt->segments == 0 || opt->segments == c.segments) &&
             (opt->vec == 0 || opt->vec == c.cpt)) {
             v = &c;

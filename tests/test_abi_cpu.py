@@ -271,7 +271,9 @@ def test_plan_chunk_modes():
     # its own tile, three look-back words per tile and channel; forward only
     p = lr.linrec_plan_f32(1, 1 << 20, 64, path="chunked", chunk_mode="chain", sm_count=152, resident_ctas=2)
     assert (p["chain"], p["lookback"], p["twopass"], p["blocks"]) == (1, 0, 0, 0)
-    assert (p["tile_d"], p["tile_t"], p["stages"], p["grid"]) == (32, 128, 3, 304)
+    assert (p["tile_d"], p["tile_t"], p["stages"], p["grid"]) == (32, 256, 3, 304)     # 256 steps: long
+    p = lr.linrec_plan_f32(1, 8192, 64, path="chunked", chunk_mode="chain", sm_count=152, resident_ctas=2)
+    assert (p["tile_t"], p["threads"]) == (128, 256)                                      # 128 below 32768
     assert p["workspace_bytes"] == 256 + 24 * p["n_tiles"] * p["tile_d"]
     p = lr.linrec_plan_f32(1, 200, 32, path="chunked", chunk_mode="chain", sm_count=152, resident_ctas=2)
     assert p["n_tiles"] == 2 and 2 < p["grid"] <= 2 + 8      # no more workers than tiles
@@ -481,7 +483,7 @@ def test_plan_invariants_over_a_grid():
         slices = B * -(-D // p["tile_d"])
         assert p["chunks"] == -(-L // p["tile_t"]) and p["n_tiles"] == slices * p["chunks"]
         if p["chain"]:                         # every resident CTA: resolvers, then one worker per tile at most
-            assert eb == 4 and slices >= 16 and kw.get("path") != "regcarry"
+            assert eb == 4 and slices >= 8 and kw.get("path") != "regcarry"
             assert 1 < p["grid"] <= min(p["n_tiles"] + 16, 152 * 2)
             assert p["workspace_bytes"] == 256 + 24 * p["n_tiles"] * p["tile_d"]
             n_chain += 1
@@ -496,12 +498,14 @@ def test_plan_invariants_over_a_grid():
 
 
 def test_plan_chain_mode_by_default():
-    """fp32 forward scans that would take the two-pass mode take chain mode from 16 slices of
-    32 channels on; fewer slices, 16-bit storage and the gradient keep the two-pass mode."""
-    for (B, L, D) in [(4, 65536, 256), (4, 131072, 128), (3, 32768, 1024), (2, 16384, 256)]:
+    """fp32 forward scans that would take the two-pass mode take chain mode from 8 slices of
+    32 channels on (256-step tiles from 32768 steps on); fewer slices, 16-bit storage and the
+    gradient keep the two-pass mode."""
+    for (B, L, D, tt) in [(4, 65536, 256, 256), (4, 131072, 128, 256), (3, 32768, 1024, 256), (2, 16384, 256, 128),
+                          (2, 262144, 128, 256), (16, 8192, 128, 128)]:
         p = lr.linrec_plan_f32(B, L, D, sm_count=152, resident_ctas=2)
-        assert p["chain"] == 1 and p["twopass"] == 0, (B, L, D)
-    for (B, L, D) in [(1, 1 << 20, 64), (2, 262144, 128), (1, 65536, 64)]:
+        assert p["chain"] == 1 and p["twopass"] == 0 and p["tile_t"] == tt, (B, L, D)
+    for (B, L, D) in [(1, 1 << 20, 64), (1, 524288, 128), (1, 65536, 64)]:
         p = lr.linrec_plan_f32(B, L, D, sm_count=152, resident_ctas=2)
         assert p["chain"] == 0 and p["twopass"] == 1, (B, L, D)
     assert lr.linrec_plan_16(4, 65536, 256, sm_count=152)["chain"] == 0

@@ -182,6 +182,28 @@ def test_chain_mode_same_bits_as_slice_owner(shape):
     assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
 
 
+@pytest.mark.parametrize("shape", [(1, 40001, 36), (3, 33000, 64), (2, 65536, 100), (9, 32768, 32)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_chain_mode_long_tiles(shape):
+    """Chain mode's 256-step tile (512 threads, 16 segments), taken from 32768 steps on: every
+    element against the oracle, with and without a carried-in state, and the same bits on a
+    second call."""
+    B, L, D = shape
+    a, b = inputs.generate(B, L, D, seed=9 + L, a_dist="u[0.9,1)", b_dist="n(0,1)")
+    h0 = torch.randn(B, D)
+    a_d, b_d = a.to(DEV), b.to(DEV)
+    opt = {"path": "chunked", "chunk_mode": "chain"}
+    assert lr.linrec_plan_f32(B, L, D, **opt)["tile_t"] == 256
+    h = run(a_d, b_d, **opt)
+    assert_close(h.cpu().numpy(), oracle.f64(a, b)[0], f"chain {shape}")
+    assert torch.equal(run(a_d, b_d, **opt), h)
+    last = torch.empty(B, D, device=DEV)
+    h = run(a_d, b_d, h_init=h0.to(DEV), h_last=last, **opt)
+    h64, last64 = oracle.f64_carry(a, b, h0.numpy().astype(np.float64))
+    assert_close(h.cpu().numpy(), h64, f"chain {shape} with a state")
+    assert_close(last.cpu().numpy(), last64, f"chain {shape} last state")
+
+
 @pytest.mark.parametrize("vec,prefetch", [(v, p) for v in (1, 2, 4) for p in (4, 8, 16)])
 def test_every_regcarry_variant(vec, prefetch):
     B, L, D = 2, 515, 132
