@@ -215,7 +215,10 @@ linrec_status_t linrec_scan_f32_backward_ex(const float *a, const float *h, cons
 linrec_status_t linrec_scan_f32_host(const float *a, const float *b, float *h,
                                      int64_t B, int64_t L, int64_t D, void *stream);
 
-/* linrec_scan_f32 with explicit options (forced path, tile shape, status word, carry). */
+/* linrec_scan_f32 with explicit options (forced path, tile shape, status word, carry).  One
+   options struct stands where a minimal form would take (int path, unsigned int *d_status):
+   it carries both, plus the chunk mode, tile, carried state and test hooks, and NULL means
+   every default. */
 linrec_status_t linrec_scan_f32_ex(const float *a, const float *b, float *h,
                                    int64_t B, int64_t L, int64_t D, void *stream,
                                    const linrec_options_t *opt);
