@@ -46,6 +46,7 @@ constexpr int64_t kSegMax = 256;
 // fp32 forward slice-owner mode from this share of the SM count in slices.
 constexpr int kOwnMinSlicesPct = 84;
 constexpr int kWideMinGridPct = 84;
+constexpr int64_t kWide64MinSteps = 4096;
 // Blocks mode: default time steps per block (tiles per block = this / tile_t).
 constexpr int64_t kBlockSteps = 1024;
 constexpr size_t kWorkspaceHead = 256;      // Control block, padded
@@ -224,9 +225,18 @@ void default_groups_16(int64_t slices, int sm_count, bool own, bool twopass, int
 // 117, (64, 256, 2048) 65 -> 61.  Without an even split the wide tiles lose ((64, 512,
 // 4096): 1024 slices on 152 CTAs, 265 against 246 on the register path).  The gradient
 // kernel likewise: (64, 2048, 1024) 419 -> 395 ({128, 64} x 4), (128, 1024, 1024) 448 -> 391.
-int wide_slices(int64_t B, int64_t L, int64_t D, int sm_count, int64_t *grid) {
+// A tile wider than D is never taken: its boxes would be mostly padding ((128, 1024, 64)
+// took {256, 32} at 43 us).  Forward scans of at least kWide64MinSteps steps also take
+// 64-channel slices ({64, 128}, 512 threads, one CTA per SM) by the same rule, measured on
+// GB300 against the 32-channel default (us per call): (32, 4096, 256) 62.4 -> 61.3, (8, 8192,
+// 1024) 125.7 -> 117.4, (19, 4096, 512) 78.8 -> 75.2, (38, 4096, 256) 80.8 -> 75.9, (4, 8192,
+// 2048) 127.1 -> 117.7, (2, 32768, 4096) 522 -> 470; shorter sequences lose ((76, 2048, 256)
+// 73.8 -> 75.4, (32, 2048, 256) 31.7 -> 32.8) and so does the gradient ((32, 4096, 256) 101.9
+// -> 103.5).
+int wide_slices(int64_t B, int64_t L, int64_t D, int sm_count, bool backward, int64_t *grid) {
     if (L < kWideMinSteps) return 0;
-    for (int td : {256, 128}) {
+    for (int td : {256, 128, 64}) {
+        if (td > D || (td == 64 && (backward || L < kWide64MinSteps))) continue;
         const int64_t slices = B * ((D + td - 1) / td);
         const int64_t k = (slices + sm_count - 1) / sm_count;        // slices per CTA
         if (slices % k == 0 && (slices / k) * 100 >= (int64_t)kWideMinGridPct * sm_count) {
@@ -347,7 +357,7 @@ linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int ali
     int64_t wide_grid = 0;
     const int wide_td = (dtype == kDtypeF32 && opt->chunk_mode == 0 && opt->tile_d == 0 && opt->tile_t == 0 &&
                          (opt->path == LINREC_PATH_AUTO || opt->path == LINREC_PATH_CHUNKED) && tma_ok)
-                            ? wide_slices(B, L, D, sm_count, &wide_grid)
+                            ? wide_slices(B, L, D, sm_count, backward, &wide_grid)
                             : 0;
     // 2. The register path when the channels alone keep enough loads in flight: a
     // forward scan with at least kRegcarryMinThreadsPerSm threads of 16 bytes of

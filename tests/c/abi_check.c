@@ -28,14 +28,15 @@ int main(void) {
         EXPECT(name != NULL && strlen(name) > 0);
     }
 
-    /* the dispatcher, on the (32, 4096, 256) shape of the pages: slice-owner chunked tiles */
+    /* the dispatcher, on the (32, 4096, 256) shape of the pages: slice-owner chunked tiles of 64 channels */
     linrec_options_t opt;
     memset(&opt, 0, sizeof(opt));
     linrec_plan_t plan;
     memset(&plan, 0, sizeof(plan));
     EXPECT(linrec_plan_f32(32, 4096, 256, 152, 16, 0, &opt, &plan) == LINREC_OK);
     EXPECT(plan.path == LINREC_PATH_CHUNKED && plan.lookback == 0 && plan.twopass == 0 && plan.blocks == 0);
-    EXPECT(plan.tile_d == 32 && plan.chunks * plan.tile_t >= 4096 && plan.grid >= 1);
+    EXPECT(plan.tile_d == 64 && plan.chunks * plan.tile_t >= 4096 && plan.grid == 128);
+    EXPECT(plan.chain == 0);
     EXPECT(plan.n_tiles == (int64_t)32 * (256 / plan.tile_d) * plan.chunks);
     /* an option no input can take is refused */
     opt.chunk_mode = 9;

@@ -192,10 +192,18 @@ def test_plan_wide_slices():
         assert p["grid"] == grid and slices % grid == 0, shape
     p = lr.linrec_plan_f32(32, 512, 4096, sm_count=152, resident_ctas=1)              # 512 slices, 4 each
     assert (p["path_name"], p["tile_d"], p["grid"]) == ("chunked", 256, 128)
-    # not without an even split, for 128 steps, the pages shape, 16-bit storage or a chosen tile or mode
+    # not without an even split, for 128 steps, 16-bit storage or a chosen tile or mode
     assert lr.linrec_plan_f32(64, 512, 4096, sm_count=152)["path_name"] == "regcarry"
     assert lr.linrec_plan_f32(32, 128, 4096, sm_count=152)["path_name"] == "regcarry"
-    assert lr.linrec_plan_f32(32, 4096, 256, sm_count=152, resident_ctas=2)["tile_d"] == 32
+    # 64-channel slices, forward only, from 4096 steps: the pages shape splits into 128 of them
+    p = lr.linrec_plan_f32(32, 4096, 256, sm_count=152, resident_ctas=2)
+    assert (p["tile_d"], p["tile_t"], p["threads"], p["grid"]) == (64, 128, 512, 128)
+    assert lr.linrec_plan_f32(32, 2048, 256, sm_count=152, resident_ctas=2)["tile_d"] == 32
+    assert lr.linrec_plan_f32_backward(32, 4096, 256, sm_count=152, resident_ctas=2)["tile_d"] == 32
+    # never a tile wider than D (its boxes would be mostly padding)
+    for shape in [(128, 1024, 64), (256, 1024, 100), (512, 512, 128)]:
+        p = lr.linrec_plan_f32(*shape, sm_count=152, resident_ctas=2)
+        assert p["path_name"] != "chunked" or p["tile_d"] <= shape[2], shape
     assert lr.linrec_plan_16(64, 2048, 1024, sm_count=152)["tile_d"] == 32
     p = lr.linrec_plan_f32_backward(128, 1024, 1024, sm_count=152, resident_ctas=1)    # the gradient too
     assert (p["tile_d"], p["tile_t"], p["grid"]) == (256, 32, 128)
@@ -228,9 +236,14 @@ def test_plan_slice_owner_thresholds():
     # slices just past one round of {32, 128} CTAs (304): 64-step tiles, 4-deep up to 1.2 rounds,
     # 3-deep up to 1.33; beyond that the {32, 128} tile again
     for (B, D, want) in [(40, 256, (64, 4)), (44, 256, (64, 4)), (48, 256, (64, 3)), (12, 1024, (64, 3)),
-                         (56, 256, (128, 2)), (32, 256, (128, 2)), (36, 256, (128, 2))]:
+                         (56, 256, (128, 2))]:
         p = lr.linrec_plan_f32(B, 4096, D, sm_count=152)
         assert (p["tile_d"], p["tile_t"], p["stages"]) == (32,) + want, (B, D)
+    # 128 to 152 slices of 64 channels: one 64-channel slice per CTA instead
+    for (B, D) in [(32, 256), (36, 256), (38, 256)]:
+        p = lr.linrec_plan_f32(B, 4096, D, sm_count=152)
+        assert (p["tile_d"], p["tile_t"], p["grid"]) == (64, 128, B * D // 64), (B, D)
+    assert lr.linrec_plan_f32(32, 2048, 256, sm_count=152)["tile_d"] == 32       # shorter: 32 channels
     p = lr.linrec_plan_f32(48, 4096, 256, sm_count=152, tile_d=32, tile_t=128)             # a chosen tile stays
     assert (p["tile_t"], p["stages"]) == (128, 2)
 
