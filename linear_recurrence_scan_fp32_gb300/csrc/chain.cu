@@ -620,4 +620,6 @@ cudaError_t launch_chain(const ChunkedLaunch &p, cudaStream_t stream) {
     return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
+LINREC_CHECKED_REPORT(checked_report_chain)
+
 }  // namespace linrec

@@ -199,6 +199,7 @@ cudaError_t checked_report_backward(unsigned long long *count, long long *first,
 cudaError_t checked_report_regcarry(unsigned long long *count, long long *first, long long out_cap);
 cudaError_t checked_report_regcarry16(unsigned long long *count, long long *first, long long out_cap);
 cudaError_t checked_report_rows(unsigned long long *count, long long *first, long long out_cap);
+cudaError_t checked_report_chain(unsigned long long *count, long long *first, long long out_cap);
 
 // ---- the fixed array of linrec_scan_f32_noalloc (noalloc.cu) ---------------------
 // Its status word on device dev, read on `stream` and cleared (0 if unused); and, for

@@ -31,6 +31,7 @@ n = B * L * D
 a = 0.5 + 0.5 * torch.rand((B, L, D), generator=g, device="cuda")
 b = torch.randn((B, L, D), generator=g, device="cuda")
 for opt in ({"path": "chunked", "chunk_mode": "own"}, {"path": "chunked", "chunk_mode": "lookback"},
+            {"path": "chunked", "chunk_mode": "chain"},
             {"path": "regcarry", "vec": 1}, {"path": "regcarry", "vec": 4}):
     want = lr.linrec_scan_f32_ex(a, b, **opt)
     assert lr.linrec_debug_bad_accesses(output_cap_bytes=(n - 5) * 4) == (0, -1), "accesses skipped uncapped"
