@@ -393,6 +393,77 @@ def run_reference(args):
     return 0
 
 
+def side_measurements(args, lr, inputs, dev, stream, step, peak, a_pages, b_pages):
+    """Secondary figures from the same run, outside the timed region (rank 0 on one GPU, the
+    default workload only): the headline call with L2 flushed before every call; the other four
+    fp32 workloads through linrec_scan_f32 (the dispatcher's choice); the headline shape in
+    bfloat16 and binary16 storage.  Each: 3 warm-up calls, then K = min(steps, 20) calls between
+    two events (the flushed figure: one event pair around each call, the flush outside it)."""
+    import torch
+    k = max(3, min(args.steps, 20))
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+
+    def region(fn):
+        for _ in range(3):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(k):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if lr.linrec_stream_status(stream) != lr.LINREC_OK:
+            raise SystemExit("device-side failure in a side measurement")
+        return e0.elapsed_time(e1) / 1e3 / k
+
+    def entry(sec, nbytes, **extra):
+        gbs = nbytes / sec / 1e9
+        return {"value": round(gbs, 1), "unit": UNIT, "ms_per_step": round(sec * 1e3, 5),
+                "frac_of_peak": round(gbs / peak, 4), "steps": k, **extra}
+
+    out = {}
+    w = inputs.WORKLOADS[WORKLOAD]
+    # 1. the headline call with a cold L2: 256 MB (twice the L2) written before each call
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+    evs = []
+    with torch.cuda.stream(stream):
+        for i in range(3 + k):
+            flush.fill_(float(i))
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            step()
+            e1.record(stream)
+            evs.append((e0, e1))
+    torch.cuda.synchronize()
+    sec = sum(e0.elapsed_time(e1) for e0, e1 in evs[3:]) / 1e3 / k
+    out["pages_l2_flushed"] = entry(sec, bytes_per_step(w, "forward"),
+                                    flush="256 MB written before every call; one event pair around each call")
+    del flush, evs
+    # 2. the other fp32 workloads
+    for name in ("tiny", "long", "gated", "short"):
+        v = inputs.WORKLOADS[name]
+        a_c, b_c = inputs.generate(v.B, v.L, v.D, v.seed, v.a_dist, v.b_dist)
+        a, b = a_c.to(dev), b_c.to(dev)
+        h = torch.empty_like(a)
+        plan = lr.linrec_plan_f32(v.B, v.L, v.D, sm_count=sms)
+        how = plan["path_name"] + (" two-pass" if plan["twopass"] else " chain" if plan.get("chain") else "")
+        sec = region(lambda: lr.linrec_scan_f32(a, b, h, stream=stream))
+        out[name] = entry(sec, bytes_per_step(v, "forward"), shape=[v.B, v.L, v.D], path=how)
+        del a, b, h, a_c, b_c
+    # 3. the headline shape in 16-bit storage
+    for dt, fn in (("bf16", lr.linrec_scan_bf16), ("f16", lr.linrec_scan_f16)):
+        a16 = inputs.to_storage16(a_pages, dt).to(dev)
+        b16 = inputs.to_storage16(b_pages, dt).to(dev)
+        h16 = torch.empty_like(a16)
+        sec = region(lambda: fn(a16, b16, h16, stream=stream))
+        out["pages_" + dt] = entry(sec, bytes_per_step(w, "forward", dt), shape=[w.B, w.L, w.D], storage=dt)
+        del a16, b16, h16
+    out["note"] = ("outside the timed region; clocks not sampled; K = min(steps, 20) calls after 3 warm-up "
+                   "calls, L2 not flushed except in pages_l2_flushed")
+    return out
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -542,6 +613,11 @@ def run_ours(args):
     del src, dst
     ceiling = max(copy_gbs.values())
 
+    side = None
+    if (rank == 0 and world == 1 and not args.no_side and args.workload == WORKLOAD and args.dtype == "f32"
+            and args.op == "forward" and not bdl and not opt):
+        side = side_measurements(args, lr, inputs, dev, stream, step, peak, a_cpu, b_cpu)
+
     # the CPU oracle first, before the e2e leg pins host memory
     cpu = None
     parity = None
@@ -629,6 +705,7 @@ def run_ours(args):
             "cpu_baseline": cpu,
             "parity": parity,
             "e2e": e2e,
+            "side": side,
             "gpu_launches": args.steps * launches,
             "clocks": clk,
             "wall_s": round(wall, 3),
@@ -658,6 +735,8 @@ def main(argv=None):
                    help="forward scan (the headline) or its gradient")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-side", action="store_true",
+                   help="skip the side figures (cold L2, the other workloads, 16-bit storage)")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--ref-seconds", type=float, default=30.0,
                    help="reference arm: CPU time budget for warm-up + timed steps")
