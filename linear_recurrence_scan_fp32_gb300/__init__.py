@@ -188,22 +188,39 @@ def _addr(x):
     return int(x.data_ptr() if hasattr(x, "data_ptr") else x)
 
 
+_options_cache = {}
+
+
 def make_options(path="auto", vec=0, prefetch=0, tile_t=0, tile_d=0, stages=0, ctas_per_sm=0,
                  chunk_mode="auto", d_status=None, h_init=None, h_last=None, spin_limit=0,
                  test_silent_tile=0, rows_per_warp=0, segments=0, group=0) -> Options:
-    o = Options()
-    o.path = PATHS[path] if isinstance(path, str) else int(path)
-    o.vec, o.prefetch, o.tile_t, o.tile_d, o.stages = int(vec), int(prefetch), int(tile_t), int(tile_d), int(stages)
-    o.ctas_per_sm = int(ctas_per_sm)
-    o.chunk_mode = CHUNK_MODES[chunk_mode] if isinstance(chunk_mode, str) else int(chunk_mode)
-    o.d_status = _addr(d_status)
-    o.h_init = _addr(h_init)
-    o.h_last = _addr(h_last)
-    o.spin_limit = int(spin_limit)
-    o.test_silent_tile = int(test_silent_tile)
-    o.rows_per_warp = int(rows_per_warp)
-    o.segments = int(segments)
-    o.group = int(group)
+    # The fields other than the three pointers are filled once per distinct combination and
+    # copied from there (setting a ctypes field costs about 0.1 us; a repeated call with the
+    # same options should not pay for 16 of them).
+    key = (path, vec, prefetch, tile_t, tile_d, stages, ctas_per_sm, chunk_mode, spin_limit, test_silent_tile,
+           rows_per_warp, segments, group)
+    base = _options_cache.get(key)
+    if base is None:
+        base = Options()
+        base.path = PATHS[path] if isinstance(path, str) else int(path)
+        base.vec, base.prefetch, base.tile_t = int(vec), int(prefetch), int(tile_t)
+        base.tile_d, base.stages = int(tile_d), int(stages)
+        base.ctas_per_sm = int(ctas_per_sm)
+        base.chunk_mode = CHUNK_MODES[chunk_mode] if isinstance(chunk_mode, str) else int(chunk_mode)
+        base.spin_limit = int(spin_limit)
+        base.test_silent_tile = int(test_silent_tile)
+        base.rows_per_warp = int(rows_per_warp)
+        base.segments = int(segments)
+        base.group = int(group)
+        if len(_options_cache) < 1024:
+            _options_cache[key] = base
+    o = Options.from_buffer_copy(base)
+    if d_status is not None:
+        o.d_status = _addr(d_status)
+    if h_init is not None:
+        o.h_init = _addr(h_init)
+    if h_last is not None:
+        o.h_last = _addr(h_last)
     return o
 
 
@@ -236,8 +253,19 @@ def _stream_handle(stream):
 
 
 def _shape_of(a, b, h, dtype=None):
+    """(B, L, D) of a, b (and h), after checking that they are contiguous 3-D CUDA tensors of
+    `dtype` (float32 by default) of one shape.  One combined test on the per-call path; the
+    detailed checks below only run to say what is wrong."""
     torch = _torch_mod()
     dtype = dtype or torch.float32
+    try:
+        ok = (a.dtype is dtype and b.dtype is dtype and a.is_cuda and b.is_cuda and a.dim() == 3 and
+              a.is_contiguous() and b.is_contiguous() and a.shape == b.shape and
+              (h is None or (h.dtype is dtype and h.is_cuda and h.is_contiguous() and h.shape == a.shape)))
+    except AttributeError:
+        ok = False
+    if ok and isinstance(a, torch.Tensor) and isinstance(b, torch.Tensor) and (h is None or isinstance(h, torch.Tensor)):
+        return tuple(a.shape)
     for name, t in (("a", a), ("b", b), ("h", h)):
         if t is None:
             continue

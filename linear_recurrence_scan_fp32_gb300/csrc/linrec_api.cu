@@ -45,6 +45,13 @@ constexpr int64_t kSegMinSteps = 64;
 constexpr int64_t kSegMax = 256;
 // fp32 forward slice-owner mode from this share of the SM count in slices.
 constexpr int kOwnMinSlicesPct = 84;
+// ... and at any slice count when a slice has at most this many chunks of 128 steps: the
+// look-back mode's tile counter and end-of-launch atomics cost more than walking so few
+// chunks in order.  Measured on GB300 (us per call, CUDA graph of back-to-back calls,
+// look-back -> slice-owner): (1, 128, 32) 5.7 -> 2.2, (4, 256, 32) 6.2 -> 3.5, (32 slices,
+// 512 steps) 6.9 -> 6.2, (64 slices, 512) 7.4 -> 6.3, (127 slices, 512) 10.0 -> 6.3; at 6
+// chunks look-back wins below about 100 slices ((64 slices, 768) 8.4 against 8.9).
+constexpr int64_t kOwnShortChunks = 4;
 constexpr int kWideMinGridPct = 84;
 constexpr int64_t kWide64MinSteps = 4096;
 // Blocks mode: default time steps per block (tiles per block = this / tile_t).
@@ -454,6 +461,7 @@ linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int ali
                                                                : (int64_t)sm_count;
         own = B * ((D + td - 1) / td) >= need;
         const int tt = opt->tile_t ? opt->tile_t : (dtype == kDtypeF32 ? 128 : tile_t_16(L));
+        if (dtype == kDtypeF32 && !backward && (L + tt - 1) / tt <= kOwnShortChunks) own = true;
         twopass = !own && allow_twopass && (L + tt - 1) / tt >= kTwoPassMinChunks;
         if (twopass && dtype == kDtypeF32 && !backward && opt->tile_d == 0 && opt->tile_t == 0 &&
             opt->stages == 0 && B * ((D + 31) / 32) >= kChainMinSlices)

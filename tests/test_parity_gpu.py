@@ -568,7 +568,8 @@ def test_workspace_bytes():
     two-pass mode; nothing on the register path or for an empty shape."""
     sms = torch.cuda.get_device_properties(DEV).multi_processor_count
     assert lr.linrec_workspace_bytes(32, 4096, 256) == 256
-    assert lr.linrec_workspace_bytes(1, 64, 32) == 256 + 3 * 1 * 32 * 8
+    assert lr.linrec_workspace_bytes(1, 64, 32) == 256               # one short slice: slice-owner mode
+    assert lr.linrec_workspace_bytes(1, 4096, 32) == 256 + 3 * 32 * 32 * 8   # 32 chunks: look-back mode
     assert lr.linrec_workspace_bytes(256, 128, 4096) == 0
     assert lr.linrec_workspace_bytes(0, 64, 32) == 0
     assert lr.linrec_workspace_bytes(-1, 64, 32) == 0
