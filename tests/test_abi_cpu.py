@@ -230,6 +230,16 @@ def test_plan_slice_owner_thresholds():
     assert (p["lookback"], p["twopass"], p["tile_d"], p["grid"]) == (0, 0, 32, 128)
     p = lr.linrec_plan_f32(15, 4096, 256, sm_count=152, resident_ctas=2)                 # 120 slices
     assert p["lookback"] or p["twopass"]
+    # ... and at any slice count when every slice has at most 4 chunks of 128 steps
+    for (B, L, D) in [(1, 64, 32), (1, 512, 32), (4, 128, 64), (127, 512, 32), (15, 300, 256)]:
+        p = lr.linrec_plan_f32(B, L, D, sm_count=152)
+        assert (p["path_name"], p["lookback"], p["twopass"], p["tile_d"], p["tile_t"]) == ("chunked", 0, 0, 32, 128), \
+            (B, L, D)
+        assert p["grid"] == B * -(-D // 32) and p["workspace_bytes"] == 256
+    for (B, L, D) in [(1, 513, 32), (16, 1024, 32), (1, 4096, 64)]:              # 5 chunks and more
+        assert lr.linrec_plan_f32(B, L, D, sm_count=152)["lookback"] == 1, (B, L, D)
+    assert lr.linrec_plan_16(4, 512, 64, sm_count=152)["lookback"] == 1          # fp32 forward only
+    assert lr.linrec_plan_f32_backward(4, 512, 64, sm_count=152)["lookback"] == 1
     # the 16-bit forms and the gradient keep one slice per SM as the threshold
     assert lr.linrec_plan_16(16, 4096, 256, sm_count=152)["lookback"] == 1
     assert lr.linrec_plan_f32_backward(16, 4096, 256, sm_count=152)["lookback"] == 1
