@@ -68,7 +68,8 @@ cudaError_t chunked_ctas_per_sm(const ChunkedVariant *v, int *ctas, int dtype) {
 
 cudaError_t launch_chunked(const ChunkedLaunch &p, cudaStream_t stream) {
     if (p.mode == kModeChain || p.variant->chain) return launch_chain(p, stream);
-    const void *fn = kernel_of(p.variant, p.dtype);
+    const void *fn = p.mode == kModeOwn ? own_kernel(p.variant, p.dtype) : nullptr;
+    if (!fn) fn = kernel_of(p.variant, p.dtype);
     if (!fn) return cudaErrorInvalidValue;
     cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)p.variant->smem_bytes);
