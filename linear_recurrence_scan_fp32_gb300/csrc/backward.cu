@@ -50,7 +50,13 @@ struct __align__(128) BackSmem {
     uint32_t tag;
 };
 
-template <int TD, int TT, int S, int ST>
+// OWN = true compiles slice-owner mode alone (`mode` must be kModeOwn); launch_backward takes that
+// copy for slice-owner calls.  Without the other modes' code it needs 80-92 registers against
+// 103-130, and resident CTAs per SM stay the same (shared memory or the launch bounds hold them).
+// Measured on GB300, us per call, general -> slice-owner-only: (32, 4096, 256) 103.3 -> 101.7,
+// (56, 4096, 256) 182.7 -> 177.8, (64, 512, 1024) 102.6 -> 100.8, (64, 2048, 1024) 388.7 -> 385.6;
+// (16, 4096, 256), (1, 32768, 4096) and (8, 4096, 4096) unchanged.
+template <int TD, int TT, int S, int ST, bool OWN = false>
 __global__ void __launch_bounds__(TD * S, (TD * S >= 512) ? 1 : 2)
 chunked_backward_kernel(const __grid_constant__ CUtensorMap map_g,
                         const __grid_constant__ CUtensorMap map_a,
@@ -73,10 +79,10 @@ chunked_backward_kernel(const __grid_constant__ CUtensorMap map_g,
     extern __shared__ __align__(128) unsigned char smem_raw[];
     Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
 
-    const bool own = mode == kModeOwn;
-    const bool lookback = mode == kModeLookback;
-    const bool reduce = mode == kModeReduce;
-    const bool apply = mode == kModeApply;
+    const bool own = OWN || mode == kModeOwn;
+    const bool lookback = !OWN && mode == kModeLookback;
+    const bool reduce = !OWN && mode == kModeReduce;
+    const bool apply = !OWN && mode == kModeApply;
     const bool want_da = da != nullptr;
     const bool load_h = want_da && !reduce;   // the reduce launch needs the maps only: g and a
     const uint32_t stage_bytes = (load_h ? 3u : 2u) * kBox;
@@ -376,8 +382,19 @@ cudaError_t backward_ctas_per_sm(const ChunkedVariant *v, int *ctas) {
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, fn, v->threads, v->smem_bytes);
 }
 
+// The slice-owner-only copy of a variant's kernel.
+static const void *own_backward_kernel(const ChunkedVariant *v) {
+#define LINREC_OB_ENTRY(TD, TT, S, ST)                                                              \
+    if (v->tile_d == TD && v->tile_t == TT && v->segments == S && v->stages == ST)                  \
+        return reinterpret_cast<const void *>(&chunked_backward_kernel<TD, TT, S, ST, true>);
+    LINREC_BACKWARD_VARIANTS(LINREC_OB_ENTRY)
+#undef LINREC_OB_ENTRY
+    return nullptr;
+}
+
 cudaError_t launch_backward(const BackwardLaunch &p, cudaStream_t stream) {
-    const void *fn = kernel_of(p.variant);
+    const void *fn = p.mode == kModeOwn ? own_backward_kernel(p.variant) : nullptr;
+    if (!fn) fn = kernel_of(p.variant);
     if (!fn) return cudaErrorInvalidValue;
     cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)p.variant->smem_bytes);
