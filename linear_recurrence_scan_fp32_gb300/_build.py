@@ -20,7 +20,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "liblinrec.so")
 SOURCES = ["linrec_api.cu", "chunked.cu", "chunked16.cu", "backward.cu", "regcarry.cu", "regcarry16.cu", "copy.cu",
            "noalloc.cu", "host_pipeline.cu", "rows.cu", "chain.cu",
-           "chunked_own.cu"]
+           "chunked_fixed.cu", "chunked16_fixed.cu"]
 HEADERS = ["kernels.cuh", "ptx.cuh", "lookback.cuh", "chunked_kernel.cuh", "storage.cuh", "checked.cuh"]
 # the index-checked build (every plain global access tested against its array first)
 CHECKED_BUILD = os.path.join(PKG, "_build_checked")

@@ -183,9 +183,10 @@ struct __align__(128) ChunkSmem {
     uint32_t tag;                       // look-back tag of this launch
 };
 
-// OWN = true compiles slice-owner mode alone (`mode` must be kModeOwn): none of the other
-// modes' code is in the kernel, which then needs fewer registers and instructions.
-template <int DT, int TD, int TT, int S, int ST, int CPT, bool BM = false, bool OWN = false>
+// FM >= 0 compiles the one carry mode FM (kModeOwn, kModeLookback, kModeReduce or kModeApply;
+// `mode` must equal it): none of the other modes' code is in the kernel, which then needs fewer
+// registers and instructions.  FM = -1 takes the mode at run time.
+template <int DT, int TD, int TT, int S, int ST, int CPT, bool BM = false, int FM = -1>
 __global__ void __launch_bounds__(TD / CPT * S, (TD / CPT * S >= 512) ? 1 : 2)
 chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
                     const __grid_constant__ CUtensorMap map_b,
@@ -205,11 +206,11 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
     constexpr int R = (S >= 4) ? 16 / S : 4;  // look-back: predecessors per lane
     using E = typename Storage<DT>::raw;      // stored element type
     constexpr uint32_t kStageBytes = 2u * TT * TD * sizeof(E);
-    const bool own = OWN || mode == kModeOwn;
-    const bool lookback = !OWN && mode == kModeLookback;
-    const bool reduce = !OWN && mode == kModeReduce;
-    const bool apply = !OWN && mode == kModeApply;
-    const bool blocks = !OWN && BM && mode == kModeBlocks;
+    const bool own = FM >= 0 ? FM == kModeOwn : mode == kModeOwn;
+    const bool lookback = FM >= 0 ? FM == kModeLookback : mode == kModeLookback;
+    const bool reduce = FM >= 0 ? FM == kModeReduce : mode == kModeReduce;
+    const bool apply = FM >= 0 ? FM == kModeApply : mode == kModeApply;
+    const bool blocks = FM < 0 && BM && mode == kModeBlocks;
     const bool chained = lookback || blocks;  // tiles or blocks joined by the look-back words
     // blocks mode: blocks per slice, and all blocks (block id = block index * n_slices + slice)
     const long long bps = BM ? (chunks + group - 1) / group : 0;

@@ -127,9 +127,11 @@ struct ChunkedLaunch {
 };
 // Number of CTAs of this variant that fit on one SM (occupancy API).
 cudaError_t chunked_ctas_per_sm(const ChunkedVariant *v, int *ctas, int dtype = kDtypeF32);
-// The slice-owner-only kernel of a variant (chunked_own.cu), which launch_chunked takes in
-// place of the general kernel for mode kModeOwn; NULL where there is none.
-const void *own_kernel(const ChunkedVariant *v, int dtype);
+// The copy of a variant's kernel compiled for carry mode `mode` alone (chunked_fixed.cu for fp32,
+// chunked16_fixed.cu for 16-bit storage), which launch_chunked takes in place of the general
+// kernel; NULL where there is none.
+const void *fixed_kernel_f32(const ChunkedVariant *v, int mode);
+const void *fixed_kernel_16(const ChunkedVariant *v, int dtype, int mode);
 cudaError_t launch_chunked(const ChunkedLaunch &args, cudaStream_t stream);
 
 // Chain mode (chain.cu): its compiled variants per storage type (the 16-bit ones serve
@@ -203,7 +205,8 @@ cudaError_t checked_report_regcarry(unsigned long long *count, long long *first,
 cudaError_t checked_report_regcarry16(unsigned long long *count, long long *first, long long out_cap);
 cudaError_t checked_report_rows(unsigned long long *count, long long *first, long long out_cap);
 cudaError_t checked_report_chain(unsigned long long *count, long long *first, long long out_cap);
-cudaError_t checked_report_own(unsigned long long *count, long long *first, long long out_cap);
+cudaError_t checked_report_fixed(unsigned long long *count, long long *first, long long out_cap);
+cudaError_t checked_report_fixed16(unsigned long long *count, long long *first, long long out_cap);
 
 // ---- the fixed array of linrec_scan_f32_noalloc (noalloc.cu) ---------------------
 // Its status word on device dev, read on `stream` and cleared (0 if unused); and, for

@@ -965,7 +965,7 @@ linrec_status_t linrec_debug_bad_accesses(uint64_t *count, int64_t *first_offset
     using Report = cudaError_t (*)(unsigned long long *, long long *, long long);
     const Report reports[] = {checked_report_chunked,  checked_report_chunked16, checked_report_backward,
                               checked_report_regcarry, checked_report_regcarry16, checked_report_rows,
-                              checked_report_chain,    checked_report_own};
+                              checked_report_chain,    checked_report_fixed,     checked_report_fixed16};
     unsigned long long total = 0;
     long long first = -1;
     for (Report r : reports) {
