@@ -50,13 +50,14 @@ struct __align__(128) BackSmem {
     uint32_t tag;
 };
 
-// OWN = true compiles slice-owner mode alone (`mode` must be kModeOwn); launch_backward takes that
-// copy for slice-owner calls.  Without the other modes' code it needs 80-92 registers against
-// 103-130, and resident CTAs per SM stay the same (shared memory or the launch bounds hold them).
-// Measured on GB300, us per call, general -> slice-owner-only: (32, 4096, 256) 103.3 -> 101.7,
-// (56, 4096, 256) 182.7 -> 177.8, (64, 512, 1024) 102.6 -> 100.8, (64, 2048, 1024) 388.7 -> 385.6;
-// (16, 4096, 256), (1, 32768, 4096) and (8, 4096, 4096) unchanged.
-template <int TD, int TT, int S, int ST, bool OWN = false>
+// FM >= 0 compiles the one carry mode FM (`mode` must equal it; -1 takes it at run time), and
+// launch_backward takes such a copy where there is one.  Without the other modes' code the slice-
+// owner copies need 80-92 registers against 103-130, and resident CTAs per SM stay the same
+// (shared memory or the launch bounds hold them).  Measured on GB300, us per call, general ->
+// slice-owner copy: (32, 4096, 256) 103.3 -> 101.7, (56, 4096, 256) 182.7 -> 177.8, (64, 512,
+// 1024) 102.6 -> 100.8, (64, 2048, 1024) 388.7 -> 385.6; (16, 4096, 256), (1, 32768, 4096) and
+// (8, 4096, 4096) unchanged.
+template <int TD, int TT, int S, int ST, int FM = -1>
 __global__ void __launch_bounds__(TD * S, (TD * S >= 512) ? 1 : 2)
 chunked_backward_kernel(const __grid_constant__ CUtensorMap map_g,
                         const __grid_constant__ CUtensorMap map_a,
@@ -79,10 +80,10 @@ chunked_backward_kernel(const __grid_constant__ CUtensorMap map_g,
     extern __shared__ __align__(128) unsigned char smem_raw[];
     Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
 
-    const bool own = OWN || mode == kModeOwn;
-    const bool lookback = !OWN && mode == kModeLookback;
-    const bool reduce = !OWN && mode == kModeReduce;
-    const bool apply = !OWN && mode == kModeApply;
+    const bool own = FM >= 0 ? FM == kModeOwn : mode == kModeOwn;
+    const bool lookback = FM >= 0 ? FM == kModeLookback : mode == kModeLookback;
+    const bool reduce = FM >= 0 ? FM == kModeReduce : mode == kModeReduce;
+    const bool apply = FM >= 0 ? FM == kModeApply : mode == kModeApply;
     const bool want_da = da != nullptr;
     const bool load_h = want_da && !reduce;   // the reduce launch needs the maps only: g and a
     const uint32_t stage_bytes = (load_h ? 3u : 2u) * kBox;
@@ -382,18 +383,31 @@ cudaError_t backward_ctas_per_sm(const ChunkedVariant *v, int *ctas) {
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, fn, v->threads, v->smem_bytes);
 }
 
-// The slice-owner-only copy of a variant's kernel.
-static const void *own_backward_kernel(const ChunkedVariant *v) {
+// The copy of a variant's kernel compiled for carry mode `mode` alone: every tile in slice-owner
+// mode; the tiles of the two-pass and look-back modes ({32, 128} and {64, 128}) in those too.
+static const void *fixed_backward_kernel(const ChunkedVariant *v, int mode) {
 #define LINREC_OB_ENTRY(TD, TT, S, ST)                                                              \
-    if (v->tile_d == TD && v->tile_t == TT && v->segments == S && v->stages == ST)                  \
-        return reinterpret_cast<const void *>(&chunked_backward_kernel<TD, TT, S, ST, true>);
+    if (mode == kModeOwn && v->tile_d == TD && v->tile_t == TT && v->segments == S && v->stages == ST) \
+        return reinterpret_cast<const void *>(&chunked_backward_kernel<TD, TT, S, ST, kModeOwn>);
     LINREC_BACKWARD_VARIANTS(LINREC_OB_ENTRY)
 #undef LINREC_OB_ENTRY
+#define LINREC_OB_CHAINED(TD, TT, S, ST)                                                            \
+    if (v->tile_d == TD && v->tile_t == TT && v->segments == S && v->stages == ST) {                \
+        if (mode == kModeLookback)                                                                  \
+            return reinterpret_cast<const void *>(&chunked_backward_kernel<TD, TT, S, ST, kModeLookback>); \
+        if (mode == kModeReduce)                                                                    \
+            return reinterpret_cast<const void *>(&chunked_backward_kernel<TD, TT, S, ST, kModeReduce>);   \
+        if (mode == kModeApply)                                                                     \
+            return reinterpret_cast<const void *>(&chunked_backward_kernel<TD, TT, S, ST, kModeApply>);    \
+    }
+    LINREC_OB_CHAINED(32, 128, 8, 2)
+    LINREC_OB_CHAINED(64, 128, 8, 2)
+#undef LINREC_OB_CHAINED
     return nullptr;
 }
 
 cudaError_t launch_backward(const BackwardLaunch &p, cudaStream_t stream) {
-    const void *fn = p.mode == kModeOwn ? own_backward_kernel(p.variant) : nullptr;
+    const void *fn = fixed_backward_kernel(p.variant, p.mode);
     if (!fn) fn = kernel_of(p.variant);
     if (!fn) return cudaErrorInvalidValue;
     cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
