@@ -62,11 +62,14 @@ def bytes_per_step(w, op: str, dtype: str = "f32") -> int:
     return 3 * STORAGE_BYTES[dtype] * w.numel
 
 
-def launches_per_step(plan: dict, op: str) -> int:
+def launches_per_step(plan: dict, op: str, inner_plan=None) -> int:
     """Kernel launches of one call.  Two-pass mode: the reduce launch, the scan of the
-    tile aggregates (one launch: at that level the dispatcher takes the slice-owner or
-    look-back mode, never two-pass again) and the apply launch."""
-    if plan["path_name"] in ("chunked", "rows") and plan["twopass"]:
+    tile aggregates and the apply launch.  That scan is a call of its own on a (1, chunks,
+    slices * tile_d) problem (inner_plan: its plan, None for one launch), which may itself
+    take two-pass mode (three launches); the scan of its maps never does."""
+    if plan["path_name"] == "chunked" and plan["twopass"]:
+        return 2 + (launches_per_step(inner_plan, "forward") if inner_plan is not None else 1)
+    if plan["path_name"] == "rows" and plan["twopass"]:
         return 3
     if plan["path_name"] == "regcarry" and plan["twopass"]:
         return 2                              # segmented register path: reduce and apply
@@ -583,7 +586,11 @@ def run_ours(args):
     seconds = max_over_ranks(elapsed_ms / 1e3, dev)
     nbytes = bytes_per_step(w, args.op, args.dtype)
     value = aggregate_gbs(nbytes, world, args.steps, seconds)
-    launches = launches_per_step(plan, args.op)
+    inner_plan = None
+    if plan["path_name"] == "chunked" and plan["twopass"]:
+        width = w.B * -(-w.D // plan["tile_d"]) * plan["tile_d"]
+        inner_plan = lr.linrec_plan_f32(1, plan["chunks"], width, sm_count=sms)
+    launches = launches_per_step(plan, args.op, inner_plan)
 
     # roofline of the scan: the kernel is the only work in the timed region, so its mean
     # duration per call (one launch, or the two-pass mode's three) is the region over K

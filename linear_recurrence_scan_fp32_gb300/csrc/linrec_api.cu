@@ -25,6 +25,11 @@ constexpr int kRegcarryThreads = 256;
 constexpr int64_t kRegcarryMinThreadsPerSm = 96;
 // Few slices: the two-pass mode from this many time chunks of 128 steps on.
 constexpr int64_t kTwoPassMinChunks = 64;
+// Two-pass levels: a call's own problem (level 0) and the scan of its tile maps (level 1) may take
+// two-pass mode; the scan of those maps' maps (level 2) may not.  Measured on GB300 (us per call,
+// the level-1 scan in look-back -> two-pass mode): (1, 1048576, 64) 204.0 -> 200.1, whose level-1
+// problem (1, 8192, 64) has 64 chunks; the rest of the long shapes measured had fewer (unchanged).
+constexpr int kTwoPassLevels = 2;
 // fp32 forward scans that would take the two-pass mode take chain mode instead from this
 // many 32-channel slices on, with 256-step tiles from kChainLongSteps steps on (half the
 // tiles for the resolvers to fold), 128-step tiles below.  Measured on GB300 (us per call,
@@ -695,7 +700,8 @@ linrec_status_t scan_locked(DeviceInfo *di, int dev, const void *a, const void *
     const int align = align_of(a, b, h);
     linrec_plan_t plan;
     int vi = -1;
-    linrec_status_t st = plan_impl(B, L, D, di->sm_count, align, 0, opt, &plan, &vi, false, level == 0, dtype);
+    linrec_status_t st = plan_impl(B, L, D, di->sm_count, align, 0, opt, &plan, &vi, false, level < kTwoPassLevels,
+                                   dtype);
     if (st != LINREC_OK) return st;
 
     if (plan.path == LINREC_PATH_REGCARRY && plan.twopass) {
@@ -729,7 +735,7 @@ linrec_status_t scan_locked(DeviceInfo *di, int dev, const void *a, const void *
     const int per_sm = cached_ctas(di->ctas_per_sm[dtype][vi],
                                    [&](int *c) { return chunked_ctas_per_sm(&variants[vi], c, dtype); });
     if (per_sm <= 0) return LINREC_ERR_LAUNCH;
-    st = plan_impl(B, L, D, di->sm_count, align, per_sm, opt, &plan, &vi, false, level == 0,
+    st = plan_impl(B, L, D, di->sm_count, align, per_sm, opt, &plan, &vi, false, level < kTwoPassLevels,
                    dtype);
     if (st != LINREC_OK) return st;
     if (!get_encoder()) return LINREC_ERR_LAUNCH;
@@ -1000,14 +1006,19 @@ size_t linrec_workspace_bytes(int64_t B, int64_t L, int64_t D) {
     if (plan_impl(B, L, D, sms, 16, 0, nullptr, &plan, nullptr) != LINREC_OK || plan.path != LINREC_PATH_CHUNKED)
         return 0;
     size_t total = plan.workspace_bytes;
-    if (plan.twopass) {
-        // the scan of the tile maps, a (1, chunks, slices * tile_d) problem with a workspace of its own
-        const int64_t slices = B * ((D + plan.tile_d - 1) / plan.tile_d);
+    // each two-pass level scans its tile maps, a (1, chunks, slices * tile_d) problem with a
+    // workspace of its own, which may itself take two-pass mode while level < kTwoPassLevels
+    int64_t b = B, d = D;
+    for (int level = 1; plan.twopass && plan.path == LINREC_PATH_CHUNKED; ++level) {
+        const int64_t width = b * ((d + plan.tile_d - 1) / plan.tile_d) * plan.tile_d;
         linrec_plan_t inner;
-        if (plan_impl(1, plan.chunks, slices * plan.tile_d, sms, 16, 0, nullptr, &inner, nullptr, false, false) ==
-                LINREC_OK &&
-            inner.path == LINREC_PATH_CHUNKED)
-            total += inner.workspace_bytes;
+        if (plan_impl(1, plan.chunks, width, sms, 16, 0, nullptr, &inner, nullptr, false, level < kTwoPassLevels) !=
+            LINREC_OK)
+            break;
+        total += inner.workspace_bytes;
+        b = 1;
+        d = width;
+        plan = inner;
     }
     return total;
 }

@@ -573,10 +573,14 @@ def test_workspace_bytes():
     assert lr.linrec_workspace_bytes(256, 128, 4096) == 0
     assert lr.linrec_workspace_bytes(0, 64, 32) == 0
     assert lr.linrec_workspace_bytes(-1, 64, 32) == 0
+    # two-pass, whose scan of the tile maps (1, 8192, 64) is two-pass too, and that scan's maps
+    # (1, 64, 64) one short slice-owner call
     p = lr.linrec_plan_f32(1, 1 << 20, 64, sm_count=sms)
-    inner = lr.linrec_plan_f32(1, p["chunks"], 64, sm_count=sms, chunk_mode="lookback")
-    assert p["twopass"] == 1
-    assert lr.linrec_workspace_bytes(1, 1 << 20, 64) == p["workspace_bytes"] + inner["workspace_bytes"]
+    inner = lr.linrec_plan_f32(1, p["chunks"], 64, sm_count=sms)
+    inner2 = lr.linrec_plan_f32(1, inner["chunks"], 64, sm_count=sms)
+    assert (p["twopass"], inner["twopass"], inner2["twopass"], inner2["lookback"]) == (1, 1, 0, 0)
+    assert lr.linrec_workspace_bytes(1, 1 << 20, 64) == (p["workspace_bytes"] + inner["workspace_bytes"] +
+                                                         inner2["workspace_bytes"])
 
 
 def test_copy_kernel():
