@@ -1,12 +1,15 @@
-// chunked16_fixed.cu -- copies of a 16-bit chunked tile (bfloat16 and binary16) compiled for one carry mode each (chunked_kernel.cuh, FM >= 0),
-// which launch_chunked takes in place of the general kernel of the same tile when a call runs in
-// that mode.  Without the other modes' code they need fewer registers and instructions; resident
-// CTAs per SM do not drop (launch bounds, shared memory or the registers of the general kernel
-// still set them).  Measured on GB300, us per call, general -> fixed-mode copy:
-//   slice-owner, {32, 256} with two channels per thread: (32, 4096, 256) bfloat16 35.8 -> 32.5,
-//     binary16 34.3 -> 32.3; other shapes within 1 %.
-// The other 16-bit tiles keep the general kernel ({32, 256} with 16 segments measured slower:
-// (64, 2048, 1024) bfloat16 122.9 -> 139.8).
+// chunked16_fixed.cu -- copies of a 16-bit chunked tile (bfloat16 and binary16), each compiled
+// for one carry mode (chunked_kernel.cuh, FM >= 0), which launch_chunked takes in place of the
+// general kernel of the same tile when a call runs in that mode.  Without the other modes' code
+// they need fewer registers and instructions (slice-owner 124, look-back 142, reduce 54, apply
+// 126, against 159); resident CTAs per SM do not drop (shared memory holds them to three).
+// Measured on GB300, us per call, general -> fixed-mode copy, {32, 256} with two channels per
+// thread:
+//   slice-owner: (32, 4096, 256) bfloat16 35.8 -> 32.5, binary16 34.3 -> 32.3; other shapes
+//     within 1 %;
+//   two-pass: (1, 1048576, 64) bfloat16 116.5 -> 109.9, (1, 131072, 64) 20.6 -> 18.1.
+// The other 16-bit tiles keep the general kernel ({32, 256} with 16 segments measured slower in
+// slice-owner mode: (64, 2048, 1024) bfloat16 122.9 -> 139.8).
 #include "chunked_kernel.cuh"
 
 namespace linrec {

@@ -1,8 +1,9 @@
-// chunked_fixed.cu -- copies of fp32 chunked tiles compiled for one carry mode each (chunked_kernel.cuh, FM >= 0),
-// which launch_chunked takes in place of the general kernel of the same tile when a call runs in
-// that mode.  Without the other modes' code they need fewer registers and instructions; resident
-// CTAs per SM do not drop (launch bounds, shared memory or the registers of the general kernel
-// still set them).  Measured on GB300, us per call, general -> fixed-mode copy:
+// chunked_fixed.cu -- copies of fp32 chunked tiles, each compiled for one carry mode
+// (chunked_kernel.cuh, FM >= 0), which launch_chunked takes in place of the general kernel of
+// the same tile when a call runs in that mode.  Without the other modes' code they need fewer
+// registers and instructions ({32, 128}: slice-owner 90, look-back 96, reduce 56, apply 92,
+// against 108); resident CTAs per SM do not drop (launch bounds, shared memory or the registers
+// of the general kernel still set them).  Measured on GB300, us per call, general -> copy:
 //   slice-owner, {32, 128}: (16, 4096, 256) 44.3 -> 36.3, (1, 32768, 4096) 334 -> 276; other
 //     shapes within 1 % ((56, 4096, 256) 106.8 -> 107.7);
 //   two-pass (reduce and apply {32, 128}, the scan of the tile maps in look-back {64, 128} or
