@@ -63,12 +63,14 @@ def bytes_per_step(w, op: str, dtype: str = "f32") -> int:
 
 
 def launches_per_step(plan: dict, op: str, inner_plan=None) -> int:
-    """Kernel launches of one call.  Two-pass mode: the reduce launch, the scan of the
-    tile aggregates and the apply launch.  That scan is a call of its own on a (1, chunks,
+    """Kernel launches of one call.  Speculative mode: two.  Two-pass mode: the reduce launch,
+    the scan of the tile aggregates and the apply launch.  That scan is a call of its own on a (1, chunks,
     slices * tile_d) problem (inner_plan: its plan, None for one launch), which may itself
     take two-pass mode (three launches); the scan of its maps never does."""
     if plan["path_name"] == "chunked" and plan["twopass"]:
         return 2 + (launches_per_step(inner_plan, "forward") if inner_plan is not None else 1)
+    if plan["path_name"] == "chunked" and plan.get("speculative"):
+        return 2                              # speculative launch and repair launch
     if plan["path_name"] == "rows" and plan["twopass"]:
         return 3
     if plan["path_name"] == "regcarry" and plan["twopass"]:
@@ -450,7 +452,8 @@ def side_measurements(args, lr, inputs, dev, stream, step, peak, a_pages, b_page
         a, b = a_c.to(dev), b_c.to(dev)
         h = torch.empty_like(a)
         plan = lr.linrec_plan_f32(v.B, v.L, v.D, sm_count=sms)
-        how = plan["path_name"] + (" two-pass" if plan["twopass"] else " chain" if plan.get("chain") else "")
+        how = plan["path_name"] + (" two-pass" if plan["twopass"] else " chain" if plan.get("chain") else
+                                   " speculative" if plan.get("speculative") else "")
         sec = region(lambda: lr.linrec_scan_f32(a, b, h, stream=stream))
         out[name] = entry(sec, bytes_per_step(v, "forward"), shape=[v.B, v.L, v.D], path=how)
         del a, b, h, a_c, b_c
@@ -522,7 +525,8 @@ def run_ours(args):
         plan = plan_fn(w.B, w.L, w.D, sm_count=sms, **opt)
         if plan["path_name"] == "chunked":
             mode = ("_twopass" if plan["twopass"] else "_blocks" if plan.get("blocks") else
-                    "_chain" if plan.get("chain") else "_lookback" if plan["lookback"] else "")
+                    "_chain" if plan.get("chain") else "_speculative" if plan.get("speculative") else
+                    "_lookback" if plan["lookback"] else "")
             kernel_tag = "chunked" + store + mode
         else:
             kernel_tag = "regcarry" + store + ("_segmented" if plan["twopass"] else "")
@@ -593,7 +597,8 @@ def run_ours(args):
     launches = launches_per_step(plan, args.op, inner_plan)
 
     # roofline of the scan: the kernel is the only work in the timed region, so its mean
-    # duration per call (one launch, or the two-pass mode's three) is the region over K
+    # duration per call (one launch, or the two-pass and speculative modes' several) is the
+    # region over K
     mean_launch_s = elapsed_ms / 1e3 / args.steps
     achieved = nbytes / mean_launch_s / 1e9
     peak, peak_kind = hbm_peak()
@@ -699,6 +704,7 @@ def run_ours(args):
                        "path": plan["path_name"],
                        "plan": {k: plan.get(k, 0) for k in ("vec", "prefetch", "tile_t", "tile_d", "segments",
                                                             "stages", "lookback", "twopass", "blocks", "chain",
+                                                            "speculative",
                                                             "threads", "grid")}},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic,
@@ -732,7 +738,8 @@ def main(argv=None):
     p.add_argument("--path", choices=("auto", "regcarry", "chunked"), default="auto")
     p.add_argument("--workload", default=WORKLOAD,
                    help="named workload (tiny, pages, long, gated, short, ...); pages is the headline")
-    p.add_argument("--chunk-mode", choices=("auto", "own", "lookback", "twopass", "blocks", "chain"), default="auto")
+    p.add_argument("--chunk-mode", choices=("auto", "own", "lookback", "twopass", "blocks", "chain", "speculative"),
+                   default="auto")
     p.add_argument("--dtype", choices=("f32", "bf16", "f16"), default="f32",
                    help="storage of a, b and h (arithmetic is fp32 for all three)")
     p.add_argument("--layout", choices=("bld", "bdl"), default="bld",

@@ -112,7 +112,17 @@ typedef struct {
                             slice's aggregates in chunk order into the running h entering every
                             chunk (the same values, bit for bit, as mode 1); it takes at most 128
                             slices of 32 channels (B * ceil(D/32); 64 in 16-bit storage), more
-                            return LINREC_ERR_INVALID_VALUE; 0 = the dispatcher's choice */
+                            return LINREC_ERR_INVALID_VALUE; 6 = speculative (fp32 forward only):
+                            two launches; each sequence is cut into G equal segments (G divides
+                            L, L/G >= 1024; `group`, else the dispatcher's), every segment is
+                            scanned from 0 (the first from the carried-in state) and publishes
+                            its map, and a chunk is stored once the product of the slopes from
+                            the segment's start to it is exactly 0 in fp32 in all 32 channels of
+                            its slice (the true carry then no longer reaches h); the second
+                            launch takes each later segment's true carry from the maps before it
+                            and writes the chunks left unstored.  12 bytes moved per element
+                            plus 8 for each element before that point: 20, as for mode 3, where
+                            the slopes never decay; 0 = the dispatcher's choice */
     unsigned int *d_status; /* device word (may be NULL): the kernel ORs 1 << linrec_status_t
                                into it on a device-side failure; otherwise the stream's own word
                                is used (read it with linrec_stream_status) */
@@ -126,8 +136,9 @@ typedef struct {
     int segments;        /* chunked: segments a tile's time steps are split into, one thread
                             each per channel group (0 = the dispatcher's choice for its default
                             16-bit tile, else the first compiled variant of the tile) */
-    int group;           /* chunk_mode 4: chunks per block (0 = 1024 time steps' worth); any
-                            other chunk_mode takes 0 only */
+    int group;           /* chunk_mode 4: chunks per block (0 = 1024 time steps' worth);
+                            chunk_mode 6: segments per sequence (0 = the dispatcher's choice);
+                            any other chunk_mode takes 0 only */
 } linrec_options_t;
 
 /*
@@ -241,6 +252,8 @@ typedef struct {
     int chain;             /* chunked: 1 = chain mode (one cooperative launch: worker CTAs publish
                               each chunk's aggregate a chunk ahead, resolver CTAs walk each slice's
                               chain of aggregates; grid = resolvers + workers) */
+    int speculative;       /* chunked: speculative mode, segments per sequence (0 = another mode);
+                              chunks and n_tiles count the segments as sequences of L/segments */
 } linrec_plan_t;
 
 /*

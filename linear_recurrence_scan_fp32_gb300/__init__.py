@@ -96,6 +96,7 @@ class Plan(ctypes.Structure):
         ("workspace_bytes", ctypes.c_size_t),
         ("blocks", ctypes.c_int),
         ("chain", ctypes.c_int),
+        ("speculative", ctypes.c_int),
     ]
 
 
@@ -179,7 +180,7 @@ def _check(code: int, what: str):
         raise LinrecError(code, f"{what}: {linrec_status_string(code)}")
 
 
-CHUNK_MODES = {"auto": 0, "own": 1, "lookback": 2, "twopass": 3, "blocks": 4, "chain": 5}
+CHUNK_MODES = {"auto": 0, "own": 1, "lookback": 2, "twopass": 3, "blocks": 4, "chain": 5, "speculative": 6}
 
 
 def _addr(x):

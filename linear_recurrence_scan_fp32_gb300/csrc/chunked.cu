@@ -70,6 +70,8 @@ cudaError_t launch_chunked(const ChunkedLaunch &p, cudaStream_t stream) {
     if (p.mode == kModeChain || p.variant->chain) return launch_chain(p, stream);
     const void *fn = p.dtype == kDtypeF32 ? fixed_kernel_f32(p.variant, p.mode)
                                           : fixed_kernel_16(p.variant, p.dtype, p.mode);
+    // the speculative modes are compiled into their fixed copies only
+    if (!fn && (p.mode == kModeSpec || p.mode == kModeRepair)) return cudaErrorInvalidValue;
     if (!fn) fn = kernel_of(p.variant, p.dtype);
     if (!fn) return cudaErrorInvalidValue;
     cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -17,9 +17,11 @@
 namespace linrec {
 
 // {tile_d, tile_t, segments, stages}: the fp32 tiles with copies in slice-owner, look-back,
-// reduce and apply modes (the second list: look-back, reduce and apply only)
+// reduce and apply modes (the second list: look-back, reduce and apply only; the third: the two
+// speculative modes, which exist in these copies alone)
 #define LINREC_FIXED_F32_ALL(X) X(32, 128, 8, 2)
 #define LINREC_FIXED_F32_CHAINED(X) X(32, 128, 8, 3) X(64, 128, 8, 2)
+#define LINREC_FIXED_F32_SPEC(X) X(32, 128, 8, 2)
 
 const void *fixed_kernel_f32(const ChunkedVariant *v, int mode) {
     if (v->blocks || v->chain || v->elem_bytes != 4 || v->cpt != 1) return nullptr;
@@ -35,10 +37,16 @@ const void *fixed_kernel_f32(const ChunkedVariant *v, int mode) {
         LINREC_FX(TD, TT, S, ST, kModeLookback) LINREC_FX(TD, TT, S, ST, kModeReduce)                        \
         LINREC_FX(TD, TT, S, ST, kModeApply)                                                                 \
     }
+#define LINREC_FX_SPEC(TD, TT, S, ST)                                                                        \
+    if (v->tile_d == TD && v->tile_t == TT && v->segments == S && v->stages == ST) {                         \
+        LINREC_FX(TD, TT, S, ST, kModeSpec) LINREC_FX(TD, TT, S, ST, kModeRepair)                            \
+    }
     LINREC_FIXED_F32_ALL(LINREC_FX_ALL)
     LINREC_FIXED_F32_CHAINED(LINREC_FX_CHAINED)
+    LINREC_FIXED_F32_SPEC(LINREC_FX_SPEC)
 #undef LINREC_FX_ALL
 #undef LINREC_FX_CHAINED
+#undef LINREC_FX_SPEC
 #undef LINREC_FX
     return nullptr;
 }

@@ -211,6 +211,10 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
     const bool reduce = FM >= 0 ? FM == kModeReduce : mode == kModeReduce;
     const bool apply = FM >= 0 ? FM == kModeApply : mode == kModeApply;
     const bool blocks = FM < 0 && BM && mode == kModeBlocks;
+    // speculative mode (copies compiled for it alone): `group` segments of each sequence, seen as
+    // batch rows bi = b * group + segment of a (B * group, L / group, D) view of the same memory
+    const bool spec = FM == kModeSpec;        // segments scanned from 0, their maps published
+    const bool repair = FM == kModeRepair;    // the tiles left unstored, from the true carry
     const bool chained = lookback || blocks;  // tiles or blocks joined by the look-back words
     // blocks mode: blocks per slice, and all blocks (block id = block index * n_slices + slice)
     const long long bps = BM ? (chunks + group - 1) / group : 0;
@@ -242,7 +246,10 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
     const long long n_units = blocks ? n_blocks : n_tiles;
     // extents for the index-checked build: elements of h, and of h_init / h_last
     const long long n_h = (n_slices / slices_per_batch) * L * D;
-    const long long n_state = (n_slices / slices_per_batch) * D;
+    const long long n_state = (n_slices / slices_per_batch) * D / ((spec || repair) ? group : 1);
+    // speculative mode: each slice's map over its segment, [slice][channel] pairs (A, B)
+    float *const segmap = reinterpret_cast<float *>(words);
+    const long long n_segmap = 2 * n_slices * TD;
     unsigned long long *const wAggA = words;
     unsigned long long *const wAggB = words + n_units * TD;
     unsigned long long *const wInc = words + 2 * n_units * TD;
@@ -261,6 +268,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
     // blockIdx.x + gridDim.x, ... each walked from chunk 0 to chunks-1, tracked
     // in (own_slice, own_q).  Look-back mode: the next id from the tile counter.
     long long own_slice = blockIdx.x, own_q = 0, own_m = 0;
+    long long stop_slice = -1;                // (repair, every thread) the slice whose repair has ended
     // (thread 0, blocks mode) the block being walked, its pass, the next tile of the pass, its tiles
     long long bm_blk = -1;
     int bm_pass = 0, bm_g = 0, bm_cnt = 0;
@@ -298,12 +306,23 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
             slice = id - q * n_slices;
             return id;
         }
-        if (own) {
-            if (own_slice >= n_slices) return n_tiles;
-            q = own_q;
-            slice = own_slice;
-            if (++own_q == chunks) { own_q = 0; own_slice += gridDim.x; }
-            return q * n_slices + slice;
+        if (own || spec || repair) {
+            for (;;) {
+                if (own_slice >= n_slices) return n_tiles;
+                // repair: no first segment (the speculative launch stored it), and nothing of a
+                // slice after its slopes' product reached 0 (the speculative launch stored the rest)
+                if (repair && (((own_slice / slices_per_batch) % group) == 0 ||
+                               (own_q > 0 && own_slice == stop_slice))) {
+                    own_q = 0;
+                    own_slice += gridDim.x;
+                    continue;
+                }
+                q = own_q;
+                slice = own_slice;
+                if (repair && own_q == 0) flags |= kFirstOfPass;
+                if (++own_q == chunks) { own_q = 0; own_slice += gridDim.x; }
+                return q * n_slices + slice;
+            }
         }
         const long long id = (long long)atomicAdd(&ctrl->tile_counter, 1ull);
         if (id >= n_tiles) return n_tiles;
@@ -348,8 +367,10 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
     uint32_t abort_seen = 0;                  // (thread 0, look-back) abort word, read one iteration early
     float run[CPT];                           // (slice-owner, ss == 0) inclusive values of the last tile
     float bA[CPT], bB[CPT];                   // (blocks mode, reduce pass) the block's map so far
+    float runA[CPT];                          // (speculative, repair; ss == 0) slope product of the segment
+                                              // through the current tile
 #pragma unroll
-    for (int i = 0; i < CPT; ++i) { run[i] = 0.0f; bA[i] = 1.0f; bB[i] = 0.0f; }
+    for (int i = 0; i < CPT; ++i) { run[i] = 0.0f; bA[i] = 1.0f; bB[i] = 0.0f; runA[i] = 1.0f; }
 
     // (thread 0) fill ring slots up to (not including) slot `limit`; slot n goes to stage n % ST.
     // In look-back mode the next tile id is taken one fill ahead, so the atomic's
@@ -404,13 +425,20 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
         const long long rem = L - (t0 + r0);
         const int nv = rem <= 0 ? 0 : (rem >= K ? K : (int)rem);   // valid steps of this thread
         const bool seq_start = (q == 0 && s == 0);                  // holds t = 0 of its channel
+        // the batch row of h_init / h_last (speculative mode: the sequence, not its segment)
+        const long long sbi = (spec || repair) ? bi / group : bi;
+        // repair: a tile loaded ahead of its slice's stop stores nothing (the speculative launch did)
+        const bool skip = repair && (id - q * n_slices) == stop_slice;
+        bool live = false;                  // (speculative, repair; ss == 0) a slope product not yet 0
 
         // ---- 2. compose this thread's K steps -----------------------------------
         const E *ta = sm.a[st] + r0 * TD + CPT * c;
         const E *tb = sm.b[st] + r0 * TD + CPT * c;
         TileRegs<DT, K, CPT> r;
         r.load(ta, tb, TD);
-        if (seq_start && !h_init) r.zero_a0();   // h_{-1} = 0: the first slope never matters
+        // h_{-1} = 0: the first slope never matters (speculative mode: only at the real start; a
+        // later segment starts from 0 but its first slope belongs to the segment's map)
+        if (seq_start && !h_init && ((!spec && !repair) || (bi % group) == 0)) r.zero_a0();
         float A[CPT], Bv[CPT];
 #pragma unroll
         for (int i = 0; i < CPT; ++i) { A[i] = 1.0f; Bv[i] = 0.0f; }
@@ -463,10 +491,77 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
         for (int i = 0; i < CPT; ++i) {
             const int ch = cc + i * TC;
             // h before the first chunk: the carried-in state, or 0.
-            const float h_before = (h_init && d0 + ch < D && inside(h_init + bi * D + d0 + ch, h_init, n_state))
-                                       ? h_init[bi * D + d0 + ch]
+            const float h_before = (h_init && d0 + ch < D && inside(h_init + sbi * D + d0 + ch, h_init, n_state))
+                                       ? h_init[sbi * D + d0 + ch]
                                        : 0.0f;
-            if (own) {
+            if (spec) {
+                // a segment's chain from 0 (the first segment's from the carried-in state); at its
+                // end the segment's map (slope product, h) goes out, the first segment's with slope 0.
+                // A tile is exact, and stored, once the slope product before it is 0.
+                if (ss == 0) {
+                    const bool first_seg = (bi % group) == 0;
+                    const float carry = (q == 0) ? (first_seg ? h_before : 0.0f) : run[i];
+                    run[i] = fmaf(tA[i], carry, tB[i]);
+                    live = live || q == 0 || runA[i] != 0.0f;
+                    runA[i] = (q == 0) ? tA[i] : tA[i] * runA[i];
+                    carry_in[ch] = carry;
+                    if (q + 1 == chunks) {
+                        const long long at = ((id - q * n_slices) * TD + ch) * 2;
+                        if (inside(segmap + at, segmap, n_segmap, false, 8)) {
+                            segmap[at] = first_seg ? 0.0f : runA[i];
+                            segmap[at + 1] = run[i];
+                        }
+                    }
+                }
+            } else if (repair) {
+                // the tiles the speculative launch left unstored, from the true h entering the
+                // segment, up to the first tile after which the slope product is 0 in every channel
+                float hin = 0.0f;
+                if (tc.flags & kFirstOfPass) {   // the same for the whole CTA
+                    // the maps of segments 0 .. g-1 of this sequence and channel slice, in order
+                    // (later on the left); lane ss composes its part of them, kSpecParts loads
+                    // in flight a round, and the shuffle scan joins the parts.  The first map's
+                    // slope is 0, so the offset is that h.
+                    const long long slice = id - q * n_slices;
+                    const long long g = bi % group;
+                    const long long base = slice - g * slices_per_batch;   // the first segment's slice
+                    const int part = (int)((g + S - 1) / S);
+                    float xA = 1.0f, xB = 0.0f;
+                    for (int j0 = 0; j0 < part; j0 += kSpecParts) {
+                        float mA[kSpecParts], mB[kSpecParts];
+#pragma unroll
+                        for (int j = 0; j < kSpecParts; ++j) {
+                            const long long sj = (long long)ss * part + j0 + j;
+                            const long long at = ((base + sj * slices_per_batch) * TD + ch) * 2;
+                            const bool ok = j0 + j < part && sj < g && inside(segmap + at, segmap, n_segmap, false, 8);
+                            mA[j] = ok ? segmap[at] : 1.0f;
+                            mB[j] = ok ? segmap[at + 1] : 0.0f;
+                        }
+#pragma unroll
+                        for (int j = 0; j < kSpecParts; ++j) {
+                            xB = fmaf(mA[j], xB, mB[j]);
+                            xA = mA[j] * xA;
+                        }
+                    }
+#pragma unroll
+                    for (int off = 1; off < S; off <<= 1) {
+                        const float uA = __shfl_up_sync(kFull, xA, off, S);
+                        const float uB = __shfl_up_sync(kFull, xB, off, S);
+                        if (ss >= off) {
+                            xB = fmaf(xA, uB, xB);
+                            xA = xA * uA;
+                        }
+                    }
+                    hin = __shfl_sync(kFull, xB, S - 1, S);
+                }
+                if (ss == 0) {
+                    const float carry = (q == 0) ? hin : run[i];
+                    run[i] = fmaf(tA[i], carry, tB[i]);
+                    runA[i] = (q == 0) ? tA[i] : tA[i] * runA[i];
+                    live = live || runA[i] != 0.0f;
+                    carry_in[ch] = carry;
+                }
+            } else if (own) {
                 if (ss == 0) {
                     const float carry = (q == 0) ? h_before : run[i];
                     run[i] = fmaf(tA[i], carry, tB[i]);
@@ -536,7 +631,17 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
                 }
             }
         }
-        __syncthreads();
+        // Once the slope product is exactly 0 in every channel of the slice, the true carry no
+        // longer reaches h: the rest of the segment's speculative h is exact.  The two launches
+        // take the same products of the same tiles, so they draw the line at the same tile.
+        bool defer = false;                     // (speculative) the tile is left to the repair launch
+        if (spec) {
+            defer = __syncthreads_or(live) && (bi % group) != 0;
+        } else if (repair) {
+            if (!__syncthreads_or(live)) stop_slice = id - q * n_slices;
+        } else {
+            __syncthreads();
+        }
 
         // ---- 5. replay the steps from the carried value, store h -----------------
         float hc[CPT], pA[CPT], pB[CPT];
@@ -546,7 +651,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
 #pragma unroll
         for (int i = 0; i < CPT; ++i) hc[i] = fmaf(pA[i], hc[i], pB[i]);
         // (D is even when CPT = 2, so a group is inside D or wholly past it)
-        const bool stores = !reduce && !(blocks && !(tc.flags & kApplyPass));
+        const bool stores = !reduce && !(blocks && !(tc.flags & kApplyPass)) && !skip && !defer;
         if (stores && (d0 + CPT * c) < D) {
             E *hp = h + ((bi * L + t0 + r0) * D + d0 + CPT * c);
             if (nv == K) {
@@ -568,12 +673,12 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
                     }
                 }
             }
-            // the thread holding t = L-1 hands the state out
-            if (h_last && nv > 0 && t0 + r0 + nv == L) {
+            // the thread holding t = L-1 hands the state out (speculative mode: of the last segment)
+            if (h_last && nv > 0 && t0 + r0 + nv == L && (!(spec || repair) || (bi % group) == group - 1)) {
 #pragma unroll
                 for (int i = 0; i < CPT; ++i)
-                    if (inside(h_last + bi * D + d0 + CPT * c + i, h_last, n_state, true))
-                        h_last[bi * D + d0 + CPT * c + i] = hc[i];
+                    if (inside(h_last + sbi * D + d0 + CPT * c + i, h_last, n_state, true))
+                        h_last[sbi * D + d0 + CPT * c + i] = hc[i];
             }
         }
         // No barrier here.  Stage st was last read before this tile's first

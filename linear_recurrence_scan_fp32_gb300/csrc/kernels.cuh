@@ -101,6 +101,13 @@ constexpr int kModeBlocks = 4;     // one launch: blocks of G tiles, reduce, loo
                                    // apply from L2 (variants with blocks = 1 only)
 constexpr int kModeChain = 5;      // one cooperative launch: workers compose a tile ahead and publish its
                                    // map, resolver CTAs walk each slice's chain of maps (chain.cu)
+// Speculative mode, two launches over a (B * G, L / G, D) view of the problem (G segments per
+// sequence, `group` = G), compiled only into copies fixed to one of them (chunked_fixed.cu):
+constexpr int kModeSpec = 6;       // each segment scanned from 0 (the first from the carried-in state),
+                                   // its map (slope product, h) published: [slice][channel] pairs
+constexpr int kModeRepair = 7;     // each later segment's start corrected with its true carry until
+                                   // the slope product reaches exactly 0
+constexpr int kSpecParts = 16;     // repair: earlier segments' maps a lane loads at once
 
 struct ChunkedLaunch {
     const ChunkedVariant *variant;

@@ -30,6 +30,17 @@ constexpr int64_t kTwoPassMinChunks = 64;
 // the level-1 scan in look-back -> two-pass mode): (1, 1048576, 64) 204.0 -> 200.1, whose level-1
 // problem (1, 8192, 64) has 64 chunks; the rest of the long shapes measured had fewer (unchanged).
 constexpr int kTwoPassLevels = 2;
+// Speculative mode: the shortest segment, the most segments, and the shortest segment for the
+// dispatcher's choice.  The repair launch recomputes each segment's tiles up to the first after
+// which the slope product is exactly 0 in fp32; the rest the speculative launch stored.  Bytes
+// per element: 12 + 8 * (that share of the segment), 20 where the slopes never decay.  With
+// a ~ U[0.9, 1) the product reaches 0 after about 2000 steps: 16 tiles of a 64-tile segment.
+// Measured on GB300, us per call against two-pass: (1, 1048576, 64) 148.8 vs 200.5, a = 1
+// 215.7 vs 199.9; (1, 131072, 64), 1024-step segments, 29.2 vs 26.9.
+constexpr int64_t kSpecMinSteps = 1024;
+constexpr int64_t kSpecMaxSegments = 1024;
+constexpr int kSpecCtasPerSm = 2;
+constexpr int64_t kSpecDefaultSteps = 8192;
 // fp32 forward scans that would take the two-pass mode take chain mode instead from this
 // many 32-channel slices on, with 256-step tiles from kChainLongSteps steps on (half the
 // tiles for the resolvers to fold), 128-step tiles below.  Measured on GB300 (us per call,
@@ -349,6 +360,65 @@ linrec_status_t plan_chain(int64_t B, int64_t L, int64_t D, int sm_count, int ct
     return LINREC_OK;
 }
 
+// Speculative mode (chunk_mode 6): the {32, 128, 2-stage} tile, whose fixed copies hold the two
+// modes (a 3-stage ring measured 4-11 % slower: (1, 1048576, 64) 148.4 -> 154.8 us); G segments
+// per sequence (opt->group, else the largest divisor of L with at least kSpecMinSteps steps per
+// segment, at most kSpecMaxSegments, and slices within one round of kSpecCtasPerSm CTAs per SM:
+// the repair copy's registers hold it to two, and a fixed figure gives the same G with or without
+// the occupancy query); one CTA per slice of the (B * G, L / G, D) view in both launches; the
+// segments' maps as plain floats (two per channel and slice).
+linrec_status_t plan_speculative(int64_t B, int64_t L, int64_t D, int sm_count, int ctas_per_sm,
+                                 const linrec_options_t *opt, linrec_plan_t *plan, int *variant_index) {
+    int n = 0;
+    const ChunkedVariant *vars = chunked_variants(&n);
+    const ChunkedVariant *v = nullptr;
+    for (int i = 0; i < n && !v; ++i) {
+        const ChunkedVariant &c = vars[i];
+        if (c.tile_d == 32 && c.tile_t == 128 && c.segments == 8 && c.stages == 2 && !c.blocks && !c.chain &&
+            (opt->tile_d == 0 || opt->tile_d == 32) && (opt->tile_t == 0 || opt->tile_t == 128) &&
+            (opt->stages == 0 || opt->stages == 2) && (opt->segments == 0 || opt->segments == 8) &&
+            (opt->vec == 0 || opt->vec == 1)) {
+            v = &c;
+            if (variant_index) *variant_index = i;
+        }
+    }
+    if (!v) return LINREC_ERR_INVALID_VALUE;
+    int per_sm = ctas_per_sm;
+    if (per_sm <= 0) {
+        per_sm = (int)((227 * 1024) / (v->smem_bytes + 1024));
+        if (per_sm < 1) per_sm = 1;
+    }
+    if (opt->ctas_per_sm > 0 && opt->ctas_per_sm < per_sm) per_sm = opt->ctas_per_sm;
+    const int64_t spb = (D + v->tile_d - 1) / v->tile_d;
+    const int64_t round = (int64_t)sm_count * per_sm;
+    int64_t G = 0;
+    if (opt->group > 0) {
+        G = opt->group;
+        if (L % G != 0 || L / G < kSpecMinSteps || G > kSpecMaxSegments) return LINREC_ERR_INVALID_VALUE;
+    } else {
+        const int64_t per_sm_g = per_sm < kSpecCtasPerSm ? per_sm : kSpecCtasPerSm;
+        int64_t most = (int64_t)sm_count * per_sm_g / (B * spb);
+        if (most > kSpecMaxSegments) most = kSpecMaxSegments;
+        for (int64_t g = most; g >= 2 && G == 0; --g)
+            if (L % g == 0 && L / g >= kSpecMinSteps) G = g;
+    }
+    if (G < 2) return LINREC_ERR_INVALID_VALUE;
+    plan->speculative = (int)G;
+    plan->vec = 1;
+    plan->tile_d = v->tile_d;
+    plan->tile_t = v->tile_t;
+    plan->segments = v->segments;
+    plan->stages = v->stages;
+    plan->threads = v->threads;
+    plan->smem_bytes = v->smem_bytes;
+    const int64_t slices = B * G * spb;
+    plan->chunks = (L / G + v->tile_t - 1) / v->tile_t;
+    plan->n_tiles = slices * plan->chunks;
+    plan->grid = slices < round ? slices : round;
+    plan->workspace_bytes = kWorkspaceHead + (size_t)2 * (size_t)slices * (size_t)v->tile_d * 4u;
+    return LINREC_OK;
+}
+
 linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int align_bytes, int ctas_per_sm,
                           const linrec_options_t *opt, linrec_plan_t *plan, int *variant_index,
                           bool backward = false, bool allow_twopass = true, int dtype = kDtypeF32) {
@@ -448,12 +518,17 @@ linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int ali
     // when the chains are short, or, for long chains (whose look-back would be
     // bound by how fast inclusive values travel down the chain), by the
     // two-pass mode: reduce, scan the aggregates, apply.
-    if (opt->chunk_mode < 0 || opt->chunk_mode > 5) return LINREC_ERR_INVALID_VALUE;
+    if (opt->chunk_mode < 0 || opt->chunk_mode > 6) return LINREC_ERR_INVALID_VALUE;
     if (opt->chunk_mode == 3 && !allow_twopass) return LINREC_ERR_INVALID_VALUE;
     if ((opt->chunk_mode == 4 || opt->chunk_mode == 5) && backward) return LINREC_ERR_INVALID_VALUE;
-    if (opt->group < 0 || (opt->group > 0 && opt->chunk_mode != 4)) return LINREC_ERR_INVALID_VALUE;
+    if (opt->group < 0 || (opt->group > 0 && opt->chunk_mode != 4 && opt->chunk_mode != 6))
+        return LINREC_ERR_INVALID_VALUE;
     if (opt->chunk_mode == 5 && !wide_td)
         return plan_chain(B, L, D, sm_count, ctas_per_sm, opt, plan, variant_index, dtype);
+    if (opt->chunk_mode == 6) {
+        if (dtype != kDtypeF32 || backward) return LINREC_ERR_INVALID_VALUE;
+        return plan_speculative(B, L, D, sm_count, ctas_per_sm, opt, plan, variant_index);
+    }
     bool own = false, twopass = false, blk = false;
     if (wide_td) {
         own = true;
@@ -468,8 +543,20 @@ linrec_status_t plan_impl(int64_t B, int64_t L, int64_t D, int sm_count, int ali
         const int tt = opt->tile_t ? opt->tile_t : (dtype == kDtypeF32 ? 128 : tile_t_16(L));
         if (dtype == kDtypeF32 && !backward && (L + tt - 1) / tt <= kOwnShortChunks) own = true;
         twopass = !own && allow_twopass && (L + tt - 1) / tt >= kTwoPassMinChunks;
-        if (twopass && dtype == kDtypeF32 && !backward && opt->tile_d == 0 && opt->tile_t == 0 &&
-            opt->stages == 0 && B * ((D + 31) / 32) >= kChainMinSlices)
+        const bool plain = dtype == kDtypeF32 && !backward && opt->tile_d == 0 && opt->tile_t == 0 &&
+                           opt->stages == 0 && opt->segments == 0 && opt->vec == 0;
+        if (twopass && plain) {
+            // few long chains: speculative mode where its segments are long
+            linrec_plan_t sp = *plan;
+            int svi = -1;
+            if (plan_speculative(B, L, D, sm_count, ctas_per_sm, opt, &sp, &svi) == LINREC_OK &&
+                L / sp.speculative >= kSpecDefaultSteps) {
+                *plan = sp;
+                if (variant_index) *variant_index = svi;
+                return LINREC_OK;
+            }
+        }
+        if (twopass && plain && B * ((D + 31) / 32) >= kChainMinSlices)
             return plan_chain(B, L, D, sm_count, ctas_per_sm, opt, plan, variant_index, dtype);
     } else {
         own = opt->chunk_mode == 1;
@@ -690,6 +777,60 @@ linrec_status_t scan_chain_locked(DeviceInfo *di, int dev, const void *a, const 
     return LINREC_OK;
 }
 
+// Speculative mode: the (B * G, L / G, D) view of a, b and h, the speculative launch, then the
+// repair launch.
+linrec_status_t scan_spec_locked(DeviceInfo *di, int dev, const void *a, const void *b, void *h, int64_t B,
+                                 int64_t L, int64_t D, cudaStream_t stream, const linrec_options_t *opt, int level,
+                                 linrec_plan_t plan, int vi) {
+    int nvar = 0;
+    const ChunkedVariant *vars = chunked_variants(&nvar);
+    if (vi < 0 || vi >= nvar || vi >= 64) return LINREC_ERR_INVALID_VALUE;
+    const int per_sm = cached_ctas(di->ctas_per_sm[kDtypeF32][vi],
+                                   [&](int *c) { return chunked_ctas_per_sm(&vars[vi], c, kDtypeF32); });
+    if (per_sm <= 0) return LINREC_ERR_LAUNCH;
+    linrec_status_t st = plan_speculative(B, L, D, di->sm_count, per_sm, opt, &plan, &vi);
+    if (st != LINREC_OK) return st;
+    if (!get_encoder()) return LINREC_ERR_LAUNCH;
+    const int64_t G = plan.speculative, Bv = B * G, Lv = L / G;
+    ChunkedLaunch p;
+    p.variant = &vars[vi];
+    p.dtype = kDtypeF32;
+    if (!encode_map(&p.map_a, a, Bv, Lv, D, plan.tile_d, plan.tile_t) ||
+        !encode_map(&p.map_b, b, Bv, Lv, D, plan.tile_d, plan.tile_t))
+        return LINREC_ERR_LAUNCH;
+    Slot *ws = workspace(dev, stream, kWorkspaceHead, level);
+    if (!ws) return LINREC_ERR_WORKSPACE;
+    Slot *arrays = workspace(dev, stream, plan.workspace_bytes - kWorkspaceHead, level, kSlotArrays);
+    if (!arrays) return LINREC_ERR_WORKSPACE;
+    p.h = h;
+    p.L = Lv;
+    p.D = D;
+    p.slices_per_batch = (D + plan.tile_d - 1) / plan.tile_d;
+    p.n_slices = Bv * p.slices_per_batch;
+    p.chunks = plan.chunks;
+    p.n_tiles = plan.n_tiles;
+    p.grid = plan.grid;
+    p.mode = kModeSpec;
+    p.group = (int)G;
+    p.ctrl = reinterpret_cast<Control *>(ws->base);
+    p.words = reinterpret_cast<unsigned long long *>(arrays->base);
+    p.status = opt->d_status ? opt->d_status : &p.ctrl->status;
+    p.spin_limit = opt->spin_limit > 0 ? opt->spin_limit : kDefaultSpinLimit;
+    p.silent_tile = -1;
+    p.h_init = opt->h_init;
+    p.h_last = opt->h_last;
+    if (launch_chunked(p, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return LINREC_ERR_LAUNCH;
+    }
+    p.mode = kModeRepair;
+    if (launch_chunked(p, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return LINREC_ERR_LAUNCH;
+    }
+    return LINREC_OK;
+}
+
 // The forward scan, arguments checked, the stream's mutex held.  `level` is 0 for a caller's
 // problem and 1 for the two-pass mode's scan of its tile aggregates (always fp32).
 linrec_status_t scan_locked(DeviceInfo *di, int dev, const void *a, const void *b, void *h, int64_t B,
@@ -727,6 +868,7 @@ linrec_status_t scan_locked(DeviceInfo *di, int dev, const void *a, const void *
     }
 
     if (plan.chain) return scan_chain_locked(di, dev, a, b, h, B, L, D, dtype, stream, opt, level, plan, vi);
+    if (plan.speculative) return scan_spec_locked(di, dev, a, b, h, B, L, D, stream, opt, level, plan, vi);
 
     // chunked: resident CTAs per SM from the occupancy API, then the real plan
     int nvar = 0;

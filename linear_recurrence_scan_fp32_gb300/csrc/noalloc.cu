@@ -153,7 +153,7 @@ extern "C" linrec_status_t linrec_scan_f32_noalloc(const float *a, const float *
     {
         linrec_plan_t probe;
         if (linrec_plan_f32(B, L, D, ds->sm_count, 16, 0, &opt, &probe) == LINREC_OK &&
-            (probe.twopass || probe.blocks || probe.chain))
+            (probe.twopass || probe.blocks || probe.chain || probe.speculative))
             opt.chunk_mode = 2;
     }
     linrec_plan_t plan;

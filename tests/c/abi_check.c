@@ -36,8 +36,11 @@ int main(void) {
     EXPECT(linrec_plan_f32(32, 4096, 256, 152, 16, 0, &opt, &plan) == LINREC_OK);
     EXPECT(plan.path == LINREC_PATH_CHUNKED && plan.lookback == 0 && plan.twopass == 0 && plan.blocks == 0);
     EXPECT(plan.tile_d == 64 && plan.chunks * plan.tile_t >= 4096 && plan.grid == 128);
-    EXPECT(plan.chain == 0);
+    EXPECT(plan.chain == 0 && plan.speculative == 0);
     EXPECT(plan.n_tiles == (int64_t)32 * (256 / plan.tile_d) * plan.chunks);
+    /* one long sequence: the speculative mode, 128 segments of 8192 steps */
+    EXPECT(linrec_plan_f32(1, (int64_t)1 << 20, 64, 152, 16, 0, &opt, &plan) == LINREC_OK);
+    EXPECT(plan.speculative == 128 && plan.twopass == 0 && plan.chunks == 64 && plan.grid == 256);
     /* an option no input can take is refused */
     opt.chunk_mode = 9;
     EXPECT(linrec_plan_f32(32, 4096, 256, 152, 16, 0, &opt, &plan) == LINREC_ERR_INVALID_VALUE);

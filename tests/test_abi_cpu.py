@@ -113,12 +113,18 @@ def test_plan_paths():
     # few channel groups: narrower blocks so that every SM gets some
     p = lr.linrec_plan_f32(64, 2048, 1024, path="regcarry", sm_count=152)
     assert p["grid"] >= 2 * 152 or p["threads"] == 32
-    # few channels, long sequence: the chunked two-pass path (per-tile A, B, H arrays)
-    p = lr.linrec_plan_f32(1, 1 << 20, 64)
-    assert p["path_name"] == "chunked" and p["twopass"] == 1 and p["lookback"] == 0
-    assert p["n_tiles"] == p["chunks"] * ((64 + p["tile_d"] - 1) // p["tile_d"])
+    # few channels, long sequence: the chunked speculative path (segments of 8192 steps, a map
+    # per segment and channel) ...
+    p = lr.linrec_plan_f32(1, 1 << 20, 64, sm_count=152)
+    assert p["path_name"] == "chunked" and p["speculative"] == 128 and p["twopass"] == 0 and p["lookback"] == 0
+    assert (p["tile_d"], p["tile_t"], p["stages"], p["chunks"], p["grid"]) == (32, 128, 2, 64, 256)
+    assert p["n_tiles"] == 256 * 64 and p["workspace_bytes"] == 256 + 2 * 256 * 32 * 4
+    # ... or, where its segments would be shorter, the two-pass path (per-tile A, B, H arrays)
+    p = lr.linrec_plan_f32(1, 1 << 20, 32, sm_count=152)
+    assert p["path_name"] == "chunked" and p["twopass"] == 1 and p["lookback"] == 0 and p["speculative"] == 0
+    assert p["n_tiles"] == p["chunks"] * ((32 + p["tile_d"] - 1) // p["tile_d"])
     assert p["chunks"] == -(-(1 << 20) // p["tile_t"])
-    assert p["workspace_bytes"] == 256 + 4 * (3 * p["n_tiles"] + 64 // p["tile_d"]) * p["tile_d"]
+    assert p["workspace_bytes"] == 256 + 4 * (3 * p["n_tiles"] + 32 // p["tile_d"]) * p["tile_d"]
     # few channels, short sequence: look-back
     p = lr.linrec_plan_f32(1, 4096, 64)
     assert p["lookback"] == 1 and p["twopass"] == 0
@@ -157,7 +163,10 @@ def test_plan_forced_options():
 
 
 def _units(p, B, D):
-    # slice-owner mode: one unit per channel slice; look-back and two-pass modes: one per tile
+    # slice-owner mode: one unit per channel slice; look-back and two-pass modes: one per tile;
+    # speculative mode: one per channel slice of every segment
+    if p["speculative"]:
+        return B * p["speculative"] * -(-D // p["tile_d"])
     return p["n_tiles"] if (p["lookback"] or p["twopass"]) else B * -(-D // p["tile_d"])
 
 
@@ -280,8 +289,8 @@ def test_plan_chunk_modes():
     # one long slice: look-back mode with words for every tile when asked for it
     p = lr.linrec_plan_f32(1, 1 << 20, 64, path="chunked", sm_count=152, chunk_mode="lookback")
     assert p["lookback"] == 1 and p["workspace_bytes"] == 256 + 24 * p["n_tiles"] * p["tile_d"]
-    # ... and the two-pass mode by default
-    p = lr.linrec_plan_f32(1, 1 << 20, 64, path="chunked", sm_count=152)
+    # ... and the two-pass mode when asked for it
+    p = lr.linrec_plan_f32(1, 1 << 20, 64, path="chunked", sm_count=152, chunk_mode="twopass")
     assert p["twopass"] == 1 and p["workspace_bytes"] == 256 + 4 * (3 * p["n_tiles"] + 64 // p["tile_d"]) * p["tile_d"]
     # the gradient takes the two-pass mode too, by default for few long slices
     p = lr.linrec_plan_f32_backward(1, 1 << 20, 64, sm_count=152)
@@ -289,7 +298,7 @@ def test_plan_chunk_modes():
     assert p["workspace_bytes"] == 256 + 4 * (3 * p["n_tiles"] + 64 // p["tile_d"]) * p["tile_d"]
     assert lr.linrec_plan_f32_backward(1, 1 << 20, 64, chunk_mode="lookback")["lookback"] == 1
     with pytest.raises(lr.LinrecError):
-        lr.linrec_plan_f32(1, 1000, 64, path="chunked", chunk_mode=6)
+        lr.linrec_plan_f32(1, 1000, 64, path="chunked", chunk_mode=7)
     # chain mode: one cooperative launch of every resident CTA (resolvers first, then workers),
     # its own tile, three look-back words per tile and channel; forward only
     p = lr.linrec_plan_f32(1, 1 << 20, 64, path="chunked", chunk_mode="chain", sm_count=152, resident_ctas=2)
@@ -481,7 +490,7 @@ def test_plan_invariants_over_a_grid():
     import itertools
     Bs, Ls, Ds = [1, 3, 16, 40, 128], [1, 100, 300, 2048, 1 << 16], [1, 6, 8, 33, 64, 256, 777, 1024, 4096]
     planners = [(lr.linrec_plan_f32, 4), (lr.linrec_plan_16, 2), (lr.linrec_plan_f32_backward, 4)]
-    n_plans = n_chain = 0
+    n_plans = n_chain = n_spec = 0
     for (B, L, D), (planner, eb), kw in itertools.product(
             itertools.product(Bs, Ls, Ds), planners,
             ({}, {"resident_ctas": 2}, {"align_bytes": 4}, {"path": "chunked"})):
@@ -504,6 +513,15 @@ def test_plan_invariants_over_a_grid():
         assert p["path_name"] == "chunked" and (D * eb) % 16 == 0
         assert p["threads"] == p["tile_d"] // p["vec"] * p["segments"] and p["tile_t"] % p["segments"] == 0
         slices = B * -(-D // p["tile_d"])
+        if p["speculative"]:                   # fp32 forward, segments of 8192 steps at least
+            G = p["speculative"]
+            assert eb == 4 and planner is lr.linrec_plan_f32 and L % G == 0 and L // G >= 8192
+            assert (p["tile_d"], p["tile_t"], p["stages"], p["twopass"], p["lookback"]) == (32, 128, 2, 0, 0)
+            assert p["chunks"] == -(-(L // G) // 128) and p["n_tiles"] == slices * G * p["chunks"]
+            assert 1 <= p["grid"] <= min(slices * G, 152 * 3)
+            assert p["workspace_bytes"] == 256 + 2 * slices * G * 32 * 4
+            n_spec += 1
+            continue
         assert p["chunks"] == -(-L // p["tile_t"]) and p["n_tiles"] == slices * p["chunks"]
         if p["chain"]:                         # every resident CTA: resolvers, then one worker per tile at most
             assert eb == 4 and slices >= 8 and kw.get("path") != "regcarry"
@@ -517,24 +535,66 @@ def test_plan_invariants_over_a_grid():
             assert p["workspace_bytes"] == 256 + 24 * p["n_tiles"] * p["tile_d"]
         elif not p["twopass"] and not p["blocks"]:
             assert p["workspace_bytes"] == 256
-    assert n_plans > 1000 and n_chain > 0
+    assert n_plans > 1000 and n_chain > 0 and n_spec > 0
 
 
 def test_plan_chain_mode_by_default():
-    """fp32 forward scans that would take the two-pass mode take chain mode from 8 slices of
-    32 channels on (256-step tiles from 32768 steps on); fewer slices, 16-bit storage and the
-    gradient keep the two-pass mode."""
-    for (B, L, D, tt) in [(4, 65536, 256, 256), (4, 131072, 128, 256), (3, 32768, 1024, 256), (2, 16384, 256, 128),
-                          (2, 262144, 128, 256), (16, 8192, 128, 128)]:
+    """fp32 forward scans that would take the two-pass mode and whose speculative segments
+    would be short take chain mode from 8 slices of 32 channels on (256-step tiles from 32768
+    steps on); fewer slices, 16-bit storage and the gradient keep the two-pass mode."""
+    for (B, L, D, tt) in [(2, 16384, 256, 128), (16, 8192, 128, 128), (8, 65536, 64, 256), (3, 50000, 100, 256)]:
         p = lr.linrec_plan_f32(B, L, D, sm_count=152, resident_ctas=2)
-        assert p["chain"] == 1 and p["twopass"] == 0 and p["tile_t"] == tt, (B, L, D)
-    for (B, L, D) in [(1, 1 << 20, 64), (1, 524288, 128), (1, 65536, 64)]:
+        assert p["chain"] == 1 and p["twopass"] == 0 and p["speculative"] == 0 and p["tile_t"] == tt, (B, L, D)
+    for (B, L, D) in [(1, 65536, 64), (1, 1 << 20, 32), (1, 131072, 64)]:
         p = lr.linrec_plan_f32(B, L, D, sm_count=152, resident_ctas=2)
-        assert p["chain"] == 0 and p["twopass"] == 1, (B, L, D)
+        assert p["chain"] == 0 and p["twopass"] == 1 and p["speculative"] == 0, (B, L, D)
     assert lr.linrec_plan_16(4, 65536, 256, sm_count=152)["chain"] == 0
     assert lr.linrec_plan_f32_backward(4, 65536, 256, sm_count=152)["chain"] == 0
     # a forced tile keeps the mode it names or the two-pass mode
-    assert lr.linrec_plan_f32(4, 65536, 256, sm_count=152, tile_d=32, tile_t=128, stages=2)["chain"] == 0
+    p = lr.linrec_plan_f32(4, 65536, 256, sm_count=152, tile_d=32, tile_t=128, stages=2)
+    assert p["chain"] == 0 and p["speculative"] == 0
+
+
+def test_plan_speculative():
+    """Speculative mode: by default where the two-pass or chain mode would be taken and the
+    largest segment count G (a divisor of L, slices of the (B * G, L / G, D) view within one
+    round of resident CTAs) leaves segments of 8192 steps at least; forced, segments of 1024
+    steps at least; `group` names G; fp32 forward only."""
+    for (B, L, D, G) in [(1, 1 << 20, 64, 128), (4, 65536, 256, 8), (4, 131072, 128, 16), (3, 32768, 1024, 2),
+                         (2, 262144, 128, 32), (1, 524288, 128, 64), (1, 1 << 22, 32, 256)]:
+        p = lr.linrec_plan_f32(B, L, D, sm_count=152, resident_ctas=2)
+        assert (p["speculative"], p["chain"], p["twopass"], p["lookback"]) == (G, 0, 0, 0), (B, L, D)
+        slices = B * G * -(-D // 32)
+        assert p["grid"] == min(slices, 304) and p["n_tiles"] == slices * -(-(L // G) // 128)
+    # one resident CTA per SM: at most 152 slices
+    assert lr.linrec_plan_f32(1, 1 << 22, 32, sm_count=152, resident_ctas=1)["speculative"] == 128
+    # G is chosen for at most two CTAs per SM (the repair copy's registers), so the plan made without
+    # the occupancy query (three by shared memory) and the call's agree: 1638400 = 2^16 * 25 has the
+    # divisor 200 within 3 * 152 / 2 slices per G but not within 2 * 152 / 2
+    for res in (2, 3):
+        assert lr.linrec_plan_f32(1, 1638400, 64, sm_count=152, resident_ctas=res)["speculative"] == 128
+    sp = dict(path="chunked", chunk_mode="speculative", sm_count=152)
+    assert lr.linrec_plan_f32(1, 131072, 64, **sp)["speculative"] == 128             # 1024-step segments
+    assert lr.linrec_plan_f32(3, 50000, 100, **sp)["speculative"] == 25               # a divisor of L
+    p = lr.linrec_plan_f32(1, 1 << 20, 64, group=64, **sp)
+    assert (p["speculative"], p["chunks"], p["grid"]) == (64, 128, 128)
+    p = lr.linrec_plan_f32(1, 1 << 20, 64, group=1024, **sp)                         # the most segments
+    assert (p["speculative"], p["chunks"], p["grid"]) == (1024, 8, 456)              # more slices than CTAs
+    for bad in (dict(group=3), dict(group=2048)):                                    # no divisor; 512 steps
+        with pytest.raises(lr.LinrecError):
+            lr.linrec_plan_f32(1, 1 << 20, 64, **sp, **bad)
+    for bad in (dict(tile_d=64), dict(tile_t=64), dict(stages=3)):                   # its one compiled tile
+        with pytest.raises(lr.LinrecError):
+            lr.linrec_plan_f32(1, 1 << 20, 64, **sp, **bad)
+    for shape in [(1, 2047, 64), (1, 1500, 32), (456, 4096, 32)]:                    # no 2 segments of 1024
+        with pytest.raises(lr.LinrecError):
+            lr.linrec_plan_f32(*shape, **sp)
+    with pytest.raises(lr.LinrecError):
+        lr.linrec_plan_16(1, 1 << 20, 64, **sp)
+    with pytest.raises(lr.LinrecError):
+        lr.linrec_plan_f32_backward(1, 1 << 20, 64, chunk_mode="speculative")
+    with pytest.raises(lr.LinrecError):
+        lr.linrec_plan_f32(1, 1 << 20, 64, chunk_mode="own", group=8)
 
 
 def test_gradient_host_and_noalloc_argument_checks(L):

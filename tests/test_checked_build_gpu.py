@@ -45,6 +45,25 @@ for opt in ({"path": "chunked", "chunk_mode": "own"}, {"path": "chunked", "chunk
     assert torch.equal(flat[: n - 8], ref[: n - 8]), opt
     assert torch.isnan(flat[n - 5:]).all(), opt
     assert lr.linrec_stream_status() == lr.LINREC_OK
+# speculative mode: two segments of 2048 steps, two launches; the slopes' product reaches 0
+# within the second segment, so its last tile is stored by the speculative launch
+B, L, D = 1, 4096, 64
+n = B * L * D
+a = 0.5 + 0.5 * torch.rand((B, L, D), generator=g, device="cuda")
+b = torch.randn((B, L, D), generator=g, device="cuda")
+opt = {"path": "chunked", "chunk_mode": "speculative", "group": 2}
+assert lr.linrec_plan_f32(B, L, D, **opt)["speculative"] == 2
+want = lr.linrec_scan_f32_ex(a, b, **opt)
+assert lr.linrec_debug_bad_accesses(output_cap_bytes=(n - 5) * 4) == (0, -1), "accesses skipped uncapped"
+h = torch.full_like(a, float("nan"))
+lr.linrec_scan_f32_ex(a, b, h, **opt)
+count, first = lr.linrec_debug_bad_accesses(output_cap_bytes=0)
+flat, ref = h.flatten(), want.flatten()
+assert count == 5, count
+assert (n - 8) * 4 <= first < n * 4, first
+assert torch.equal(flat[: n - 8], ref[: n - 8])
+assert torch.isnan(flat[n - 5:]).all()
+assert lr.linrec_stream_status() == lr.LINREC_OK
 print("cap ok")
 """
 

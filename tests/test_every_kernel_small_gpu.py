@@ -43,7 +43,7 @@ def _sync_ok(what):
     assert st == lr.LINREC_OK, f"{what}: {lr.linrec_status_string(st)}"
 
 
-def _forward_options(D):
+def _forward_options(L, D):
     opts = [{}, {"path": "regcarry", "vec": 1, "prefetch": 4}]
     if D % 2 == 0:
         opts.append({"path": "regcarry", "vec": 2, "prefetch": 8})
@@ -52,6 +52,8 @@ def _forward_options(D):
         for mode in ("own", "lookback", "twopass", "blocks", "chain"):
             opts.append({"path": "chunked", "chunk_mode": mode})
         opts.append({"path": "chunked", "chunk_mode": "blocks", "tile_d": 64, "group": 2})
+        if L % 2 == 0 and L >= 2048:       # two segments at least 1024 steps long
+            opts.append({"path": "chunked", "chunk_mode": "speculative"})
     return opts
 
 
@@ -63,7 +65,7 @@ def test_forward_and_carry(shape):
     h64, _ = oracle.f64(a, b)
     hc64, last64 = oracle.f64_carry(a, b, h0.numpy().astype(np.float64))
     a_d, b_d, h0_d = a.to(DEV), b.to(DEV), h0.to(DEV)
-    for opt in _forward_options(D):
+    for opt in _forward_options(L, D):
         h = lr.linrec_scan_f32_ex(a_d, b_d, **opt) if opt else lr.linrec_scan_f32(a_d, b_d)
         _sync_ok(f"{shape} {opt}")
         assert_close(h.cpu().numpy(), h64, f"{shape} {opt}")

@@ -57,6 +57,22 @@ def test_single_process_defaults(monkeypatch):
     assert bench.aggregate_gbs(12, 1, 1, 1e-9) == pytest.approx(12.0)
 
 
+def test_launches_per_step():
+    """The bench's count of kernel launches per call (its gpu_launches claim) follows the plan:
+    one for a single-launch mode, two for the speculative mode and the segmented register path,
+    and for two-pass mode the reduce and apply launches plus those of the scan of the tile maps,
+    which is itself two-pass on the long workload."""
+    import linear_recurrence_scan_fp32_gb300 as lr
+    plan = lr.linrec_plan_f32(1, 1 << 20, 64, sm_count=152)
+    assert plan["speculative"] and bench.launches_per_step(plan, "forward") == 2
+    plan = lr.linrec_plan_f32(1, 1 << 20, 64, sm_count=152, path="chunked", chunk_mode="twopass")
+    inner = lr.linrec_plan_f32(1, plan["chunks"], 64, sm_count=152)
+    assert inner["twopass"] and bench.launches_per_step(plan, "forward", inner) == 5
+    assert bench.launches_per_step(lr.linrec_plan_f32(32, 4096, 256, sm_count=152), "forward") == 1
+    plan = lr.linrec_plan_f32(7, 3000, 777, sm_count=152)
+    assert plan["path_name"] == "regcarry" and plan["twopass"] and bench.launches_per_step(plan, "forward") == 2
+
+
 def _reference_arm(extra, env_over=None):
     import json
     import subprocess

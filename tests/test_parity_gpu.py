@@ -368,7 +368,7 @@ def test_concurrent_host_threads():
     library serialises its bookkeeping, each stream gets its own workspace, and every call returns
     the bits of the same call made alone."""
     import threading
-    modes = ["own", "lookback", "twopass", "blocks", "regcarry", "chain"]
+    modes = ["own", "lookback", "twopass", "blocks", "regcarry", "chain", "speculative"]
     jobs = []
     for k, mode in enumerate(modes):
         a, b = inputs.generate(2, 20000, 96, seed=70 + k, a_dist="u[0.9,1)", b_dist="n(0,1)")
@@ -405,9 +405,10 @@ def test_concurrent_host_threads():
 
 
 def test_modes_alternating_on_one_stream():
-    """Two-pass and look-back calls take turns on one stream.  With a ~ U[0,1) the
-    two-pass mode's tile products underflow to denormals whose bit patterns equal
-    small look-back tags: the look-back must never see them."""
+    """Two-pass, speculative and look-back calls take turns on one stream.  With a ~ U[0,1)
+    the two-pass mode's tile products underflow to denormals whose bit patterns equal
+    small look-back tags: the look-back must never see them.  The speculative and two-pass
+    modes share the stream's array workspace."""
     a1, b1 = inputs.generate(1, 1 << 20, 64, seed=13, a_dist="u[0,1)", b_dist="n(0,1)")
     a2, b2 = inputs.generate(3, 1000, 260, seed=14, a_dist="u[0,1)", b_dist="n(0,1)")
     want1, _ = oracle.f64(a1, b1)
@@ -417,10 +418,78 @@ def test_modes_alternating_on_one_stream():
     for k in range(3):
         h1 = run(*d1, path="chunked", chunk_mode="twopass")
         assert_close(h1.cpu().numpy(), want1, f"two-pass, call {k}")
+        h1 = run(*d1, path="chunked", chunk_mode="speculative")
+        assert_close(h1.cpu().numpy(), want1, f"speculative, call {k}")
         for mode in ("lookback", "twopass", "blocks", "chain", "lookback", "blocks", "chain"):
             h2 = run(*d2, path="chunked", chunk_mode=mode)
             assert_close(h2.cpu().numpy(), want2, f"{mode} after two-pass, call {k}")
     assert lr.linrec_stream_status() == lr.LINREC_OK
+
+
+# ---------------------------------------------------------------------------
+# speculative mode: G segments scanned from 0, then the unstored tiles from the true carry
+# ---------------------------------------------------------------------------
+
+SPEC = {"path": "chunked", "chunk_mode": "speculative"}
+
+
+@pytest.mark.parametrize("case", [
+    ((1, 131072, 64), "u[0.9,1)", 0),      # 1024-step segments: the product never reaches 0, all repaired
+    ((3, 50000, 100), "u[0.5,1)", 25),     # ragged channel slice, 2000-step segments (a ragged last tile)
+    ((2, 262144, 36), "u[0.9,1)", 256),    # 32 maps a lane in the repair's fold (two rounds); 1024 slices
+    ((1, 65536, 32), "u[0,1)", 64),        # the product reaches 0 in the first tile
+    ((1, 1 << 22, 32), "u[0.9,1)", 0),     # 256 segments of 16384 steps: a quarter of each repaired
+], ids=lambda c: "x".join(map(str, c[0])) + f"-{c[1]}-G{c[2]}")
+def test_speculative_mode(case):
+    """Every element against the oracle, with and without a carried-in state, h_last, and the
+    same bits on a second call (no atomics: the result is a fixed function of the input)."""
+    (B, L, D), ad, G = case
+    a, b = inputs.generate(B, L, D, seed=21 + L, a_dist=ad, b_dist="n(0,1)")
+    h0 = torch.randn(B, D, generator=torch.Generator().manual_seed(22))
+    opt = dict(SPEC, group=G) if G else SPEC
+    p = lr.linrec_plan_f32(B, L, D, **opt)
+    assert p["speculative"] == (G or p["speculative"]) and p["speculative"] >= 2 and L % p["speculative"] == 0
+    a_d, b_d = a.to(DEV), b.to(DEV)
+    h = run(a_d, b_d, **opt)
+    assert_close(h.cpu().numpy(), oracle.f64(a, b)[0], f"speculative {case}")
+    assert torch.equal(run(a_d, b_d, **opt), h)
+    hc64, last64 = oracle.f64_carry(a, b, h0.numpy().astype(np.float64))
+    last = torch.full((B, D), float("nan"), device=DEV)
+    hc = run(a_d, b_d, h_init=h0.to(DEV), h_last=last, **opt)
+    assert_close(hc.cpu().numpy(), hc64, f"speculative {case} carry")
+    assert_close(last.cpu().numpy(), last64, f"speculative {case} h_last")
+    assert lr.linrec_stream_status() == lr.LINREC_OK
+
+
+def test_speculative_mode_closed_forms():
+    """Closed forms the speculative mode must meet bit for bit.  a = 0: h = b, the product is
+    0 after one step, so every later tile comes from the speculative launch.  a = 1 with
+    integer b: h is the prefix sum, exact in fp32 below 2^24 in any order; the product never
+    reaches 0, so every segment after the first is recomputed from the composed maps of the
+    segments before it."""
+    B, L, D = 2, 65536, 64
+    b = torch.randint(-8, 9, (B, L, D), generator=torch.Generator().manual_seed(23)).float()
+    b_d = b.to(DEV)
+    for G in (0, 2, 64):
+        opt = dict(SPEC, group=G) if G else SPEC
+        h = run(torch.zeros_like(b_d), b_d, **opt)
+        assert torch.equal(h, b_d), G
+        h0 = torch.randint(-8, 9, (B, D), generator=torch.Generator().manual_seed(24)).float()
+        last = torch.empty(B, D, device=DEV)
+        h = run(torch.ones_like(b_d), b_d, h_init=h0.to(DEV), h_last=last, **opt)
+        want = torch.cumsum(b.double(), dim=1) + h0.double()[:, None, :]
+        assert torch.equal(h.cpu().double(), want), G
+        assert torch.equal(last.cpu().double(), want[:, -1]), G
+    assert lr.linrec_stream_status() == lr.LINREC_OK
+
+
+def test_speculative_mode_is_the_default_for_long_chains():
+    """The long workload (1, 1048576, 64) takes the speculative mode by default, and its result
+    is the forced call's, bit for bit."""
+    a, b = inputs.generate(1, 1 << 20, 64, seed=25, a_dist="u[0.9,1)", b_dist="n(0,1)")
+    a_d, b_d = a.to(DEV), b.to(DEV)
+    assert lr.linrec_plan_f32(1, 1 << 20, 64)["speculative"] == 128
+    assert torch.equal(run(a_d, b_d), run(a_d, b_d, **SPEC))
 
 
 # ---------------------------------------------------------------------------
@@ -564,8 +633,9 @@ def test_epoch_wraps_around(mode):
 
 def test_workspace_bytes():
     """What a default call holds: the control block alone in slice-owner mode, plus three look-back
-    words per tile and channel in look-back mode, plus the tile maps and their scan's workspace in
-    two-pass mode; nothing on the register path or for an empty shape."""
+    words per tile and channel in look-back mode, plus the segments' maps in speculative mode, plus
+    the tile maps and their scan's workspace in two-pass mode; nothing on the register path or for
+    an empty shape."""
     sms = torch.cuda.get_device_properties(DEV).multi_processor_count
     assert lr.linrec_workspace_bytes(32, 4096, 256) == 256
     assert lr.linrec_workspace_bytes(1, 64, 32) == 256               # one short slice: slice-owner mode
@@ -573,13 +643,17 @@ def test_workspace_bytes():
     assert lr.linrec_workspace_bytes(256, 128, 4096) == 0
     assert lr.linrec_workspace_bytes(0, 64, 32) == 0
     assert lr.linrec_workspace_bytes(-1, 64, 32) == 0
-    # two-pass, whose scan of the tile maps (1, 8192, 64) is two-pass too, and that scan's maps
-    # (1, 64, 64) one short slice-owner call
+    # speculative: the control block and the segments' maps
     p = lr.linrec_plan_f32(1, 1 << 20, 64, sm_count=sms)
-    inner = lr.linrec_plan_f32(1, p["chunks"], 64, sm_count=sms)
-    inner2 = lr.linrec_plan_f32(1, inner["chunks"], 64, sm_count=sms)
+    assert p["speculative"] == 128 and lr.linrec_workspace_bytes(1, 1 << 20, 64) == p["workspace_bytes"] == \
+        256 + 2 * 256 * 32 * 4
+    # two-pass, whose scan of the tile maps (1, 8192, 32) is two-pass too, and that scan's maps
+    # (1, 64, 32) one short slice-owner call
+    p = lr.linrec_plan_f32(1, 1 << 20, 32, sm_count=sms)
+    inner = lr.linrec_plan_f32(1, p["chunks"], 32, sm_count=sms)
+    inner2 = lr.linrec_plan_f32(1, inner["chunks"], 32, sm_count=sms)
     assert (p["twopass"], inner["twopass"], inner2["twopass"], inner2["lookback"]) == (1, 1, 0, 0)
-    assert lr.linrec_workspace_bytes(1, 1 << 20, 64) == (p["workspace_bytes"] + inner["workspace_bytes"] +
+    assert lr.linrec_workspace_bytes(1, 1 << 20, 32) == (p["workspace_bytes"] + inner["workspace_bytes"] +
                                                          inner2["workspace_bytes"])
 
 
