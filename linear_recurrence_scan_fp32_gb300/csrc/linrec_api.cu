@@ -35,14 +35,16 @@ constexpr int kTwoPassLevels = 2;
 // which the slope product is exactly 0 in fp32; the rest the speculative launch stored.  Bytes
 // per element: 12 + 8 * (that share of the segment), 20 where the slopes never decay.  With
 // a ~ U[0.9, 1) the product reaches 0 after about 2000 steps: 16 tiles of a 64-tile segment.
-// Measured on GB300, us per call against two-pass: (1, 1048576, 64) 148.8 vs 200.5, a = 1
-// 215.7 vs 199.9; (1, 131072, 64), 1024-step segments, 29.2 vs 26.9.
+// Measured on GB300, us per call against two-pass or chain mode, a ~ U[0.9, 1) / a = 1:
+// (1, 1048576, 64) 148.8 / 215.7 vs 200.5; (1, 4194304, 32) 270 / 428 vs 398; (4, 65536, 256)
+// 147 / 209 vs chain 183; with 4096-step segments 9-12 % faster / 6-12 % slower ((1, 1048576, 32),
+// (8, 65536, 64)); with 1024-step segments slower either way ((1, 131072, 64) 29.2 vs 26.9).
 constexpr int64_t kSpecMinSteps = 1024;
 constexpr int64_t kSpecMaxSegments = 1024;
 constexpr int kSpecCtasPerSm = 2;
 constexpr int64_t kSpecDefaultSteps = 8192;
-// fp32 forward scans that would take the two-pass mode take chain mode instead from this
-// many 32-channel slices on, with 256-step tiles from kChainLongSteps steps on (half the
+// fp32 forward scans that would take the two-pass mode, and that the speculative mode does not
+// take, take chain mode instead from this many 32-channel slices on, with 256-step tiles from kChainLongSteps steps on (half the
 // tiles for the resolvers to fold), 128-step tiles below.  Measured on GB300 (us per call,
 // two-pass -> chain): (2, 131072, 128) 112 -> 106, (3, 131072, 128) 160 -> 145, (6, 65536,
 // 128) 158 -> 138, (4, 65536, 256) 209 -> 183, (3, 32768, 1024) 306 -> 262, (1, 32768, 512)

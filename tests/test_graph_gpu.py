@@ -30,7 +30,8 @@ def _built():
 
 MODES = [{}, {"path": "regcarry"}, {"path": "chunked", "chunk_mode": "own"},
          {"path": "chunked", "chunk_mode": "lookback"}, {"path": "chunked", "chunk_mode": "twopass"},
-         {"path": "chunked", "chunk_mode": "blocks"}, {"path": "chunked", "chunk_mode": "chain"}]
+         {"path": "chunked", "chunk_mode": "blocks"}, {"path": "chunked", "chunk_mode": "chain"},
+         {"path": "chunked", "chunk_mode": "speculative"}]
 
 
 def _scan(a, b, h, opt, stream=None):
