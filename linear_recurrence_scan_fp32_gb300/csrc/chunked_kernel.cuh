@@ -268,7 +268,8 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
     // blockIdx.x + gridDim.x, ... each walked from chunk 0 to chunks-1, tracked
     // in (own_slice, own_q).  Look-back mode: the next id from the tile counter.
     long long own_slice = blockIdx.x, own_q = 0, own_m = 0;
-    long long stop_slice = -1;                // (repair, every thread) the slice whose repair has ended
+    long long stop_slice = -1;                // (speculative, repair; every thread) the slice whose slope
+                                              // product has reached 0: from there on it stays decided
     // (thread 0, blocks mode) the block being walked, its pass, the next tile of the pass, its tiles
     long long bm_blk = -1;
     int bm_pass = 0, bm_g = 0, bm_cnt = 0;
@@ -516,6 +517,8 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
             } else if (repair) {
                 // the tiles the speculative launch left unstored, from the true h entering the
                 // segment, up to the first tile after which the slope product is 0 in every channel
+                // and the carry finite (0 * NaN is NaN: a NaN carried in reaches every later h, so
+                // the tiles the speculative launch stored are then written again)
                 float hin = 0.0f;
                 if (tc.flags & kFirstOfPass) {   // the same for the whole CTA
                     // the maps of segments 0 .. g-1 of this sequence and channel slice, in order
@@ -558,7 +561,7 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
                     const float carry = (q == 0) ? hin : run[i];
                     run[i] = fmaf(tA[i], carry, tB[i]);
                     runA[i] = (q == 0) ? tA[i] : tA[i] * runA[i];
-                    live = live || runA[i] != 0.0f;
+                    live = live || runA[i] != 0.0f || !isfinite(run[i]);
                     carry_in[ch] = carry;
                 }
             } else if (own) {
@@ -633,10 +636,13 @@ chunked_scan_kernel(const __grid_constant__ CUtensorMap map_a,
         }
         // Once the slope product is exactly 0 in every channel of the slice, the true carry no
         // longer reaches h: the rest of the segment's speculative h is exact.  The two launches
-        // take the same products of the same tiles, so they draw the line at the same tile.
+        // take the same products of the same tiles, so they draw the line at the same tile, and
+        // neither goes back on it (a later non-finite slope would turn the product's 0 into NaN).
         bool defer = false;                     // (speculative) the tile is left to the repair launch
         if (spec) {
-            defer = __syncthreads_or(live) && (bi % group) != 0;
+            const long long sl = id - q * n_slices;
+            if (!__syncthreads_or(live)) stop_slice = sl;
+            defer = stop_slice != sl && (bi % group) != 0;
         } else if (repair) {
             if (!__syncthreads_or(live)) stop_slice = id - q * n_slices;
         } else {

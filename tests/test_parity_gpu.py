@@ -483,6 +483,34 @@ def test_speculative_mode_closed_forms():
     assert lr.linrec_stream_status() == lr.LINREC_OK
 
 
+def test_speculative_mode_propagates_nan():
+    """a = 1/2: the slope product of a segment is 2^-128 after one tile and 0 after two, so the
+    speculative launch stores the rest of each segment.  A NaN in a or b makes every later h of
+    its channel NaN, in later segments too (0 * NaN is NaN), and a NaN slope turns a product that
+    reached 0 into NaN.  Every element must be written: NaN exactly where the oracle has it, the
+    rest within the bound."""
+    B, L, D = 1, 4096, 32
+    a = torch.full((B, L, D), 0.5)
+    b = torch.randn(B, L, D, generator=torch.Generator().manual_seed(26))
+    a[0, 1000, 5] = float("nan")      # first segment: carried into every later one
+    b[0, 1500, 20] = float("nan")
+    a[0, 3000, 9] = float("nan")      # after the second segment's product reached 0
+    h64, _ = oracle.f64(a, b)
+    assert np.isnan(h64[0, 1000:, 5]).all() and np.isnan(h64[0, 1500:, 20]).all()
+    assert np.isnan(h64[0, 3000:, 9]).all() and np.isnan(h64).sum() == 3096 + 2596 + 1096
+    a_d, b_d = a.to(DEV), b.to(DEV)
+    for G in (2, 4):
+        h = torch.full_like(a_d, 12345.0)
+        lr.linrec_scan_f32_ex(a_d, b_d, h, group=G, **SPEC)
+        torch.cuda.synchronize()
+        got = h.cpu().numpy().astype(np.float64)
+        assert not (got == 12345.0).any(), f"G = {G}: elements left unwritten"
+        assert np.array_equal(np.isnan(got), np.isnan(h64)), f"G = {G}: NaN pattern differs"
+        fin = ~np.isnan(h64)
+        assert_close(got[fin], h64[fin], f"speculative, NaN inputs, G = {G}")
+    assert lr.linrec_stream_status() == lr.LINREC_OK
+
+
 def test_speculative_mode_is_the_default_for_long_chains():
     """The long workload (1, 1048576, 64) takes the speculative mode by default, and its result
     is the forced call's, bit for bit."""
