@@ -204,22 +204,28 @@ def kernel_source_digest(names) -> str:
     return h.hexdigest()[:16]
 
 
-def committed_traffic(kernel: str, workload: str):
-    """dram read+write bytes per launch from the committed ncu summary, if the kernel is unchanged."""
-    path = os.path.join(ROOT, "profiles", f"traffic_{kernel}_{workload}.txt")
+def committed_capture(kernel: str, workload: str):
+    """The committed ncu summary of the kernel on the workload: (dram read+write bytes per launch,
+    whether the digest of its kernel sources still matches the tree, the file), or None."""
+    rel = os.path.join("profiles", f"traffic_{kernel}_{workload}.txt")
     try:
         kv = {}
-        with open(path) as f:
+        with open(os.path.join(ROOT, rel)) as f:
             for line in f:
                 if ":" in line and not line.startswith("#"):
                     k, v = line.split(":", 1)
                     kv[k.strip()] = v.strip()
         src = kv["kernel_sources"].split(",")
-        if kernel_source_digest([s.strip() for s in src]) != kv["kernel_source_sha256_16"]:
-            return None
-        return int(kv["dram_bytes_per_launch"])
+        same = kernel_source_digest([s.strip() for s in src]) == kv["kernel_source_sha256_16"]
+        return int(kv["dram_bytes_per_launch"]), same, rel
     except (OSError, KeyError, ValueError):
         return None
+
+
+def committed_traffic(kernel: str, workload: str):
+    """dram read+write bytes per launch from the committed ncu summary, if the kernel is unchanged."""
+    cap = committed_capture(kernel, workload)
+    return cap[0] if cap and cap[1] else None
 
 
 # ---------------------------------------------------------------------------
@@ -604,6 +610,7 @@ def run_ours(args):
     peak, peak_kind = hbm_peak()
     kernel = kernel_tag
     traffic = committed_traffic(kernel, w.name)
+    capture = committed_capture(kernel, w.name)
 
     # in-run copy ceiling over the same byte count: 1.5*N floats read and written
     n_copy = nbytes // 8
@@ -708,6 +715,10 @@ def run_ours(args):
                                                             "threads", "grid")}},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "traffic_earlier_sources": ({"bytes": capture[0], "file": capture[2],
+                                                      "note": "captured on an earlier digest of the kernel "
+                                                              "sources; not the current kernel's"}
+                                                     if capture and not capture[1] else None),
                          "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                          else "fallback 6.8 TB/s", "kernel": kernel,
                          "algorithmic_bytes_per_step": nbytes, "launches_per_step": launches,

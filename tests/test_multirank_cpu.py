@@ -73,6 +73,26 @@ def test_launches_per_step():
     assert plan["path_name"] == "regcarry" and plan["twopass"] and bench.launches_per_step(plan, "forward") == 2
 
 
+def test_committed_traffic_follows_the_source_digest(tmp_path, monkeypatch):
+    """The bench line's roofline.traffic comes from a committed capture only while the digest of the
+    kernel sources it lists matches the tree; a capture on other sources is reported apart."""
+    csrc = tmp_path / "linear_recurrence_scan_fp32_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (csrc / "k.cu").write_text("kernel v1")
+    (tmp_path / "profiles").mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    digest = bench.kernel_source_digest(["k.cu"])
+    (tmp_path / "profiles" / "traffic_kern_work.txt").write_text(
+        "# a capture\nkernel_sources: k.cu\n"
+        f"kernel_source_sha256_16: {digest}\ndram_bytes_per_launch: 1234\n")
+    assert bench.committed_traffic("kern", "work") == 1234
+    assert bench.committed_capture("kern", "work") == (1234, True, "profiles/traffic_kern_work.txt")
+    (csrc / "k.cu").write_text("kernel v2")
+    assert bench.committed_traffic("kern", "work") is None
+    assert bench.committed_capture("kern", "work") == (1234, False, "profiles/traffic_kern_work.txt")
+    assert bench.committed_capture("kern", "other") is None
+
+
 def _reference_arm(extra, env_over=None):
     import json
     import subprocess
